@@ -1,0 +1,338 @@
+"""WKV7 forward + backward throughput on the RWKV-7 1.5B-shaped layer scan.
+
+One step = the forward scan (y, s_final and checkpoints) plus the backward
+(dr, dw, dk, dv, da, db, dS_init) over B=4, T=4096, H=32, N=64 with bf16
+inputs and fp32 state and gradients, inputs resident in HBM. Prints one JSON
+line. `--impl reference` times the CPU oracle on a bounded sample of the same
+workload instead.
+
+Multi-GPU (torchrun, one process per GPU): every rank scans its own batch of
+the same shape (independent (b, h) problems, no data-path collective); the
+slowest rank's time counts and `value` is the tokens of all ranks per second.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "WKV7 fwd+bwd tokens/s (B·T) at 1.5B shape; achieved % of roofline"
+FP32_LANES_PER_SM = 128  # Blackwell SM: 4 partitions x 32 FP32 lanes
+
+
+def _peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return {"hbm_gbs": float(p["hbm_gbs"]), "sm_max_mhz": float(p.get("sm_max_mhz", 2070.0)),
+                "source": "measured"}
+    except (OSError, KeyError, ValueError):
+        return {"hbm_gbs": 6800.0, "sm_max_mhz": 2070.0, "source": "fallback"}
+
+
+def _dist():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def _init_pg(world, backend):
+    import torch.distributed as dist
+
+    if world > 1 and not dist.is_initialized():
+        os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+        dist.init_process_group(backend)
+    return dist if world > 1 else None
+
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons during a region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int):
+        self.dev = device_index
+        self.proc = None
+        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_rank{device_index}.csv")
+
+    def __enter__(self):
+        try:
+            os.makedirs(os.path.dirname(self.path), exist_ok=True)
+            self.fh = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits", "-lms", "200",
+                 "-i", str(self.dev)], stdout=self.fh, stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            self.fh.close()
+
+    def summary(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) >= 9:
+                    rows.append(parts)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        reasons = sorted({n for r in rows for n, v in zip(names, r[5:9]) if v.lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(rows)}
+
+
+def _work_per_token_head(N, C, in_bytes):
+    """Algorithmic FLOP and bytes per token-head (fwd, bwd).
+
+    FLOP: 4 N^2 multiply-adds forward (sa, v k^T, sa b^T, y) and 12 N^2
+    backward, each counted as 2 FLOP. Bytes: forward reads r, w, k, v, a, b
+    and writes y and 1/C of a checkpoint; backward reads r, w, k, v, a, b,
+    dy and 1/C of a checkpoint and writes six fp32 gradients.
+    """
+    f_flop, b_flop = 8 * N * N, 24 * N * N
+    ck = 4 * N * N / C
+    f_bytes = 7 * N * in_bytes + ck
+    b_bytes = 7 * N * in_bytes + ck + 6 * N * 4
+    return f_flop, b_flop, f_bytes, b_bytes
+
+
+def cpu_baseline_sample(wl, d, heads_per_round, rounds=1, nthreads=0):
+    """Time the oracle (fwd + bwd, fp64) on whole heads of the workload."""
+    import numpy as np
+
+    import oracle
+    from linear_rnn_state_gb300 import inputs
+
+    cores = nthreads or len(os.sched_getaffinity(0))
+    P = min(wl.B * wl.H, heads_per_round * rounds)
+    heads = [(i // wl.H, i % wl.H) for i in range(P)]
+    o = {n: inputs.as_f64(d[n], wl.storage) for n in ("r", "w", "k", "v", "a", "b", "dy")}
+    sel = {n: np.stack([o[n][bi, :, hi, :] for bi, hi in heads])[:, :, None, :] for n in o}
+    t0 = time.perf_counter()
+    oracle.forward(*(sel[n] for n in ("r", "w", "k", "v", "a", "b")), nthreads=cores)
+    oracle.backward(*(sel[n] for n in ("r", "w", "k", "v", "a", "b", "dy")), nthreads=cores)
+    dt = time.perf_counter() - t0
+    tokens = wl.T * P / wl.H  # one head is 1/H of a batch row's tokens
+    return tokens / dt, cores, P, dt
+
+
+def run_reference(args):
+    world, rank, _ = _dist()
+    if rank != 0:
+        return 0
+    from linear_rnn_state_gb300 import configs, inputs
+
+    wl = configs.WORKLOADS[configs.BENCH_WORKLOAD]
+    d = inputs.generate(wl.B, wl.T, wl.H, wl.N, wl.storage, wl.s_init_std, seed=0)
+    cores = len(os.sched_getaffinity(0))
+    for _ in range(args.warmup):
+        cpu_baseline_sample(wl, d, cores)
+    times, toks = [], 0.0
+    for _ in range(args.steps):
+        v, used, P, dt = cpu_baseline_sample(wl, d, cores)
+        times.append(dt)
+        toks += wl.T * P / wl.H
+    value = toks / sum(times)
+    line = {
+        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": 1000 * sum(times) / len(times), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "impl": "reference",
+        "config": {"workload": wl.name, "B": wl.B, "T": wl.T, "H": wl.H, "N": wl.N, "storage": wl.storage},
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": used, "kind": "oracle",
+                         "sample": f"{P} of {wl.B * wl.H} (b,h) heads, full T={wl.T}, fwd+bwd in fp64 per step"},
+        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def run_gpu(args):
+    import numpy as np
+    import torch
+
+    from linear_rnn_state_gb300 import configs, inputs, wkv7
+
+    world, rank, local = _dist()
+    torch.cuda.set_device(local)
+    dist = _init_pg(world, "nccl")
+    wkv7.load()
+    dev = torch.device("cuda", local)
+    wl = configs.WORKLOADS[configs.BENCH_WORKLOAD]
+    B, T, H, N = wl.B, wl.T, wl.H, wl.N
+    bf16 = wl.storage == "bf16"
+    C = wkv7.wkv7_default_ckpt_every(N, bf16)
+    names = ("r", "w", "k", "v", "a", "b", "dy")
+    d = inputs.generate(B, T, H, N, wl.storage, wl.s_init_std, seed=rank)
+
+    def to_dev(x):
+        t = torch.from_numpy(x)
+        return (t.view(torch.bfloat16) if bf16 else t).to(dev)
+
+    t_in = {n: to_dev(d[n]) for n in names}
+    tdt = torch.bfloat16 if bf16 else torch.float32
+    y = torch.empty((B, T, H, N), dtype=tdt, device=dev)
+    s_final = torch.empty((B, H, N, N), dtype=torch.float32, device=dev)
+    nck = (T + C - 1) // C
+    ckpt = torch.empty((B, H, nck, N, N), dtype=torch.float32, device=dev)
+    grads = {n: torch.empty((B, T, H, N), dtype=torch.float32, device=dev) for n in ("dr", "dw", "dk", "dv", "da", "db")}
+    dS = torch.empty((B, H, N, N), dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream()
+    sp = stream.cuda_stream
+    fwd = wkv7.wkv7_forward_bf16 if bf16 else wkv7.wkv7_forward
+    bwd = wkv7.wkv7_backward_bf16 if bf16 else wkv7.wkv7_backward
+    fwd_args = [t_in[n].data_ptr() for n in names[:6]] + [None, y.data_ptr(), s_final.data_ptr(), ckpt.data_ptr(),
+                                                           C, B, T, H, N, sp]
+    bwd_args = [t_in[n].data_ptr() for n in names] + [None, ckpt.data_ptr(), C] + [
+        grads[n].data_ptr() for n in ("dr", "dw", "dk", "dv", "da", "db")] + [dS.data_ptr(), B, T, H, N, sp]
+
+    def step(ev=None):
+        if ev is not None:
+            ev[0].record(stream)
+        rc = fwd(*fwd_args)
+        if ev is not None:
+            ev[1].record(stream)
+        rc2 = bwd(*bwd_args)
+        if ev is not None:
+            ev[2].record(stream)
+        if rc or rc2:
+            raise RuntimeError(wkv7.last_error())
+
+    for _ in range(args.warmup):
+        step()
+    wkv7.status()
+    events = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clocks:
+        start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        start.record(stream)
+        for k in range(args.steps):
+            step(events[k])
+        end.record(stream)
+        torch.cuda.synchronize()
+    wkv7.status()
+    if dist:
+        dist.barrier()
+    total_ms = start.elapsed_time(end)
+    fwd_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in events)
+    bwd_ms = statistics.mean(e[1].elapsed_time(e[2]) for e in events)
+    ms = total_ms / args.steps
+    if dist:
+        tt = torch.tensor([ms], device=dev)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        ms = tt.item()
+
+    # ---- end to end through the C ABI with host buffers (pinned)
+    host_in = {n: torch.from_numpy(d[n]).pin_memory() for n in names}
+    host_out = {n: torch.empty(grads[n].shape, dtype=torch.float32).pin_memory() for n in grads}
+    host_y = torch.empty(y.shape, dtype=tdt).pin_memory()
+    host_dS = torch.empty(dS.shape, dtype=torch.float32).pin_memory()
+    h2d = sum(x.numel() * x.element_size() for x in host_in.values())
+    d2h = sum(x.numel() * x.element_size() for x in host_out.values()) + host_y.numel() * host_y.element_size() \
+        + host_dS.numel() * 4
+
+    def e2e_step():
+        for n in names:
+            dst = t_in[n].view(torch.int16) if bf16 else t_in[n]
+            src = host_in[n].view(torch.int16) if bf16 else host_in[n]
+            dst.copy_(src, non_blocking=True)
+        step()
+        for n in grads:
+            host_out[n].copy_(grads[n], non_blocking=True)
+        host_y.copy_(y, non_blocking=True)
+        host_dS.copy_(dS, non_blocking=True)
+
+    e2e_steps = max(1, min(args.steps, 5))
+    e2e_step()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1) / e2e_steps
+    if dist:
+        tt = torch.tensor([e2e_ms], device=dev)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        e2e_ms = tt.item()
+
+    if rank != 0:
+        return 0
+    peaks = _peaks()
+    BTH = B * T * H
+    f_flop, b_flop, f_bytes, b_bytes = _work_per_token_head(N, C, 2 if bf16 else 4)
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    peak_flops = sms * FP32_LANES_PER_SM * 2 * peaks["sm_max_mhz"] * 1e6
+    achieved = b_flop * BTH / (bwd_ms * 1e-3)
+    t_roof = max((f_flop + b_flop) * BTH / peak_flops, (f_bytes + b_bytes) * BTH / (peaks["hbm_gbs"] * 1e9))
+    value = world * B * T / (ms * 1e-3)
+    ncores = len(os.sched_getaffinity(0))
+    cpu_v, cpu_cores, cpu_P, cpu_dt = cpu_baseline_sample(wl, d, ncores) if not args.no_cpu_baseline else (
+        None, 0, 0, 0.0)
+    line = {
+        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": wl.name, "B": B, "T": T, "H": H, "N": N, "storage": wl.storage, "ckpt_every": C,
+                   "l2": "no flush: inputs, checkpoints and gradients (%.1f GB) exceed the 129 MB L2"
+                         % ((7 * BTH * N * (2 if bf16 else 4) + ckpt.numel() * 4 + 6 * BTH * N * 4) / 1e9)},
+        "fwd_ms": fwd_ms, "bwd_ms": bwd_ms, "step_roofline_frac": t_roof / (ms * 1e-3),
+        "roofline": {"bound": "alu", "achieved": achieved / 1e12, "peak": peak_flops / 1e12, "unit": "TFLOP/s",
+                     "frac": achieved / peak_flops, "traffic": None, "kernel": "wkv7_bwd_kernel",
+                     "peak_source": f"{sms} SMs x {FP32_LANES_PER_SM} FP32 lanes x 2 x {peaks['sm_max_mhz']:.0f} MHz",
+                     "hbm_gbs_achieved": b_bytes * BTH / (bwd_ms * 1e-3) / 1e9, "hbm_peak_gbs": peaks["hbm_gbs"]},
+        "e2e": {"value": world * B * T / (e2e_ms * 1e-3), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h},
+        "gpu_launches": 2 * args.steps,
+        "clocks": clocks.summary(),
+    }
+    if cpu_v is not None:
+        line["cpu_baseline"] = {"value": cpu_v, "unit": "tokens/s", "cores": cpu_cores, "kind": "oracle",
+                                "sample": f"{cpu_P} of {B * H} (b,h) heads, full T={T}, fwd+bwd fp64 ({cpu_dt:.1f} s)"}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["gb300", "reference"], default="gb300")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_gpu(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

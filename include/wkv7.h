@@ -1,0 +1,130 @@
+/*
+ * wkv7.h - C ABI of the GB300 WKV7 library: the RWKV-7 matrix-state
+ * recurrence and its backward-through-time on one GPU (sm_103a).
+ *
+ * The operation ("rx_pretrain.c", rx_wkv7_forward_seq and rx_wkv7_backward
+ * with the reverse-scan equations (1)-(3) in the comment above it). For every
+ * batch b and head h an N x N fp32 state S (row i = value index, column
+ * j = key index) runs over t = 0 .. T-1:
+ *     sa  = S a_t
+ *     S  <- S diag(w_t) + v_t k_t^T + sa b_t^T
+ *     y_t = S r_t                       (read after the update)
+ * The backward carries G = dL/dS from t = T-1 down to 0, starting at zero
+ * (no gradient enters through the final state):
+ *     dr_t = S_t^T dy_t ;  G += dy_t r_t^T
+ *     dk_t = G^T v_t ;  db_t = G^T sa_t ;  dw_t = colsum(G o S_prev)
+ *     dv_t = G k_t ;    dsa = G b_t ;      da_t = S_prev^T dsa
+ *     G <- G diag(w_t) + dsa a_t^T
+ * and returns G after t = 0 as the gradient of the initial state. dw is the
+ * gradient with respect to the effective decay w itself.
+ *
+ * Layout ("rx_pretrain.c", helpers vx and sx). Per-step vectors r, w, k, v,
+ * a, b, y, dy and the six input gradients are row-major [B][T][H][N];
+ * states s_init, s_final and dS_init are [B][H][N][N] with S_ij at
+ * ((b*H + h)*N + i)*N + j. Checkpoints are [B][H][nck][N][N] with
+ * nck = ceil(T / ckpt_every); checkpoint c is the state before step
+ * c*ckpt_every (checkpoint 0 is the initial state).
+ *
+ * Memory and streams. Every pointer is device memory owned by the caller;
+ * the library never frees or keeps it. Work is enqueued on `stream` (a
+ * cudaStream_t; NULL is the legacy default stream) and the calls return
+ * without waiting for it, except wkv7_status. Outputs are overwritten, not
+ * accumulated, and must not overlap any input. Every pointer must be 16-byte
+ * aligned. N must be 16, 32 or 64; B, T and H may be 0 (an empty problem:
+ * with T = 0 the forward copies s_init, or zeros, to s_final and the backward
+ * zeroes dS_init; buffers of zero size may be NULL).
+ *
+ * Status codes: WKV7_OK on success, otherwise a negative code; the message of
+ * the calling thread's last error is in wkv7_last_error(). An invalid
+ * argument is reported before anything is enqueued.
+ */
+#ifndef WKV7_H
+#define WKV7_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define WKV7_OK 0
+#define WKV7_ERR_ALLOC (-1)   /* a workspace could not be allocated */
+#define WKV7_ERR_INVALID (-2) /* bad pointer, size, alignment or overlap */
+#define WKV7_ERR_CUDA (-3)    /* a CUDA launch or runtime call failed */
+#define WKV7_ERR_TIMEOUT (-4) /* a kernel gave up a bounded wait (wkv7_status) */
+
+/* bfloat16 values are passed as their 16-bit patterns. */
+typedef uint16_t wkv7_bf16;
+
+/*
+ * Forward scan, fp32 inputs.
+ *   r, w, k, v, a, b  [B][T][H][N] inputs (required).
+ *   s_init            [B][H][N][N] initial state, or NULL for zeros.
+ *   y                 [B][T][H][N] output, or NULL to skip it.
+ *   s_final           [B][H][N][N] final state, or NULL to skip it.
+ *   ckpt              checkpoint buffer of wkv7_ckpt_bytes(B, T, H, N,
+ *                     ckpt_every) bytes for wkv7_backward, or NULL.
+ *   ckpt_every        checkpoint interval in steps (>= 1 when ckpt is set).
+ * Returns WKV7_OK, WKV7_ERR_INVALID or WKV7_ERR_CUDA.
+ */
+int wkv7_forward(const float* r, const float* w, const float* k, const float* v, const float* a,
+                 const float* b, const float* s_init, float* y, float* s_final, float* ckpt,
+                 int ckpt_every, int B, int T, int H, int N, void* stream);
+
+/* Forward scan with bfloat16 r, w, k, v, a, b and y; the state, s_init,
+ * s_final and the checkpoints stay fp32 and the arithmetic is fp32. */
+int wkv7_forward_bf16(const wkv7_bf16* r, const wkv7_bf16* w, const wkv7_bf16* k, const wkv7_bf16* v,
+                      const wkv7_bf16* a, const wkv7_bf16* b, const float* s_init, wkv7_bf16* y,
+                      float* s_final, float* ckpt, int ckpt_every, int B, int T, int H, int N,
+                      void* stream);
+
+/*
+ * Backward-through-time, fp32 inputs.
+ *   r, w, k, v, a, b, dy  [B][T][H][N] (required; dy = dL/dy).
+ *   s_init         [B][H][N][N] initial state or NULL for zeros; read only
+ *                  when ckpt is NULL.
+ *   ckpt           the checkpoints wkv7_forward wrote with the same
+ *                  ckpt_every, or NULL: the library then runs its own
+ *                  checkpointing forward into a workspace taken with
+ *                  cudaMallocAsync on `stream` and freed on it after the
+ *                  backward (WKV7_ERR_ALLOC if that fails). With ckpt NULL,
+ *                  ckpt_every <= 0 lets the library pick the interval.
+ *   dr, dw, dk, dv, da, db  [B][T][H][N] gradients (required).
+ *   dS_init        [B][H][N][N] gradient of the initial state, or NULL.
+ * Returns WKV7_OK, WKV7_ERR_INVALID, WKV7_ERR_ALLOC or WKV7_ERR_CUDA.
+ */
+int wkv7_backward(const float* r, const float* w, const float* k, const float* v, const float* a,
+                  const float* b, const float* dy, const float* s_init, const float* ckpt,
+                  int ckpt_every, float* dr, float* dw, float* dk, float* dv, float* da, float* db,
+                  float* dS_init, int B, int T, int H, int N, void* stream);
+
+/* Backward with bfloat16 r, w, k, v, a, b and dy; checkpoints, s_init, every
+ * gradient and the arithmetic are fp32. */
+int wkv7_backward_bf16(const wkv7_bf16* r, const wkv7_bf16* w, const wkv7_bf16* k, const wkv7_bf16* v,
+                       const wkv7_bf16* a, const wkv7_bf16* b, const wkv7_bf16* dy, const float* s_init,
+                       const float* ckpt, int ckpt_every, float* dr, float* dw, float* dk, float* dv,
+                       float* da, float* db, float* dS_init, int B, int T, int H, int N, void* stream);
+
+/* Bytes of the checkpoint buffer: B*H*ceil(T/ckpt_every)*N*N*4, or 0 for an
+ * invalid size. */
+size_t wkv7_ckpt_bytes(int B, int T, int H, int N, int ckpt_every);
+
+/* The checkpoint interval the library picks for N and the input type
+ * (bf16 != 0 for bfloat16 inputs): the backward replays whole chunks of this
+ * length from shared memory. 0 for an unsupported N. */
+int wkv7_default_ckpt_every(int N, int bf16);
+
+/* Waits for `stream`, then reports (and clears) what the kernels flagged on
+ * the current device: WKV7_OK, WKV7_ERR_TIMEOUT when a bounded wait inside a
+ * kernel gave up, or WKV7_ERR_CUDA for a CUDA error. */
+int wkv7_status(void* stream);
+
+/* Message of the calling thread's last failed call ("" if none). */
+const char* wkv7_last_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* WKV7_H */

@@ -1,0 +1,368 @@
+// C ABI of the WKV7 library: argument validation, TMA tensor-map encoding,
+// the backward's optional checkpoint workspace, and the device status word.
+#include <cudaTypedefs.h>
+
+#include <cstdarg>
+#include <cstdio>
+#include <cstdlib>
+#include <mutex>
+#include <string>
+
+#include "wkv7.h"
+#include "wkv7_common.cuh"
+#include "wkv7_launch.h"
+
+namespace wkv7 {
+namespace {
+
+__device__ unsigned g_status_word;
+
+thread_local std::string t_last_error;
+
+int fail(int code, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  std::vsnprintf(buf, sizeof buf, fmt, ap);
+  va_end(ap);
+  t_last_error = buf;
+  return code;
+}
+
+int fail_cuda(cudaError_t e, const char* what) {
+  return fail(WKV7_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+// ---------------------------------------------------------- validation ---
+
+constexpr int kMaxDevices = 64;
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int check_dims(int B, int T, int H, int N) {
+  if (B < 0 || T < 0 || H < 0) return fail(WKV7_ERR_INVALID, "B, T and H must be >= 0 (got %d, %d, %d)", B, T, H);
+  if (N != 16 && N != 32 && N != 64) return fail(WKV7_ERR_INVALID, "N must be 16, 32 or 64 (got %d)", N);
+  // Grid sizes stay below 2^31 and tensor-map strides below 2^40 bytes.
+  const unsigned long long heads = (unsigned long long)B * H;
+  if (heads * (N / 16) >= (1ull << 31)) return fail(WKV7_ERR_INVALID, "B*H too large");
+  const unsigned long long elems = heads * (unsigned long long)T * N;
+  if (elems * 4ull >= (1ull << 40)) return fail(WKV7_ERR_INVALID, "B*T*H*N too large");
+  return WKV7_OK;
+}
+
+struct Span {
+  const void* p;
+  size_t bytes;
+  const char* name;
+};
+
+bool overlaps(const Span& x, const Span& y) {
+  if (!x.p || !y.p) return false;
+  const uintptr_t a0 = reinterpret_cast<uintptr_t>(x.p), a1 = a0 + x.bytes;
+  const uintptr_t b0 = reinterpret_cast<uintptr_t>(y.p), b1 = b0 + y.bytes;
+  return a0 < b1 && b0 < a1;
+}
+
+// Required pointers non-null, every pointer 16-byte aligned, no output
+// overlapping an input or another output.
+int check_spans(const Span* ins, int nin, const Span* outs, int nout, int required_in, int required_out) {
+  for (int i = 0; i < nin; ++i) {
+    if (i < required_in && !ins[i].p) return fail(WKV7_ERR_INVALID, "%s must not be NULL", ins[i].name);
+    if (ins[i].p && !aligned16(ins[i].p)) return fail(WKV7_ERR_INVALID, "%s is not 16-byte aligned", ins[i].name);
+  }
+  for (int o = 0; o < nout; ++o) {
+    if (o < required_out && !outs[o].p) return fail(WKV7_ERR_INVALID, "%s must not be NULL", outs[o].name);
+    if (outs[o].p && !aligned16(outs[o].p)) return fail(WKV7_ERR_INVALID, "%s is not 16-byte aligned", outs[o].name);
+    for (int i = 0; i < nin; ++i)
+      if (overlaps(outs[o], ins[i])) return fail(WKV7_ERR_INVALID, "%s overlaps input %s", outs[o].name, ins[i].name);
+    for (int q = 0; q < o; ++q)
+      if (overlaps(outs[o], outs[q])) return fail(WKV7_ERR_INVALID, "%s overlaps output %s", outs[o].name, outs[q].name);
+  }
+  return WKV7_OK;
+}
+
+size_t ckpt_bytes(int B, int T, int H, int N, int C) {
+  const size_t nck = (size_t)(((long long)T + C - 1) / C);
+  return (size_t)B * H * nck * N * N * sizeof(float);
+}
+
+// ------------------------------------------------------ device helpers ---
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+// [B][T][H][N] tensor as a 4-D map (N, H, T, B) with a box of `steps` rows of
+// one head.
+int make_map(CUtensorMap* map, const void* base, bool bf16, int B, int T, int H, int N, int steps) {
+  auto enc = encode_fn();
+  if (!enc) return fail(WKV7_ERR_CUDA, "cuTensorMapEncodeTiled is unavailable");
+  const cuuint64_t es = bf16 ? 2 : 4;
+  cuuint64_t dims[4] = {(cuuint64_t)N, (cuuint64_t)H, (cuuint64_t)T, (cuuint64_t)B};
+  cuuint64_t strides[3] = {N * es, (cuuint64_t)H * N * es, (cuuint64_t)T * H * N * es};
+  cuuint32_t box[4] = {(cuuint32_t)N, 1, (cuuint32_t)steps, 1};
+  cuuint32_t estr[4] = {1, 1, 1, 1};
+  CUresult r = enc(map, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4,
+                   const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                   CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(WKV7_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", (int)r);
+  return WKV7_OK;
+}
+
+std::mutex g_status_mu;
+unsigned* g_status_ptr[kMaxDevices];
+
+// Device address of this library's status word on the current device.
+int status_word(unsigned** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return fail_cuda(e, "cudaGetDevice");
+  if (dev < 0 || dev >= kMaxDevices) return fail(WKV7_ERR_CUDA, "device ordinal %d out of range", dev);
+  std::lock_guard<std::mutex> lock(g_status_mu);
+  if (!g_status_ptr[dev]) {
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_status_word);
+    if (e != cudaSuccess) return fail_cuda(e, "cudaGetSymbolAddress(status)");
+    g_status_ptr[dev] = static_cast<unsigned*>(p);
+  }
+  *out = g_status_ptr[dev];
+  return WKV7_OK;
+}
+
+// ------------------------------------------------------------ forward ---
+
+int forward_impl(bool bf16, const void* const in[6], const float* s_init, void* y, float* s_final,
+                 float* ckpt, int C, int B, int T, int H, int N, cudaStream_t stream) {
+  int rc = check_dims(B, T, H, N);
+  if (rc) return rc;
+  if (ckpt && C < 1) return fail(WKV7_ERR_INVALID, "ckpt_every must be >= 1 (got %d)", C);
+  const size_t es = bf16 ? 2 : 4;
+  const size_t vec = (size_t)B * T * H * N * es;
+  const size_t st = (size_t)B * H * N * N * 4;
+  const Span ins[7] = {{in[0], vec, "r"}, {in[1], vec, "w"}, {in[2], vec, "k"}, {in[3], vec, "v"},
+                       {in[4], vec, "a"}, {in[5], vec, "b"}, {s_init, st, "s_init"}};
+  const Span outs[3] = {{y, vec, "y"}, {s_final, st, "s_final"},
+                        {ckpt, ckpt ? ckpt_bytes(B, T, H, N, C) : 0, "ckpt"}};
+  // Empty problems: nothing to scan. With T = 0 the final state is the
+  // initial one; zero-sized vector buffers may be NULL.
+  if ((size_t)B * H == 0) return WKV7_OK;
+  if (T == 0) {
+    rc = check_spans(ins + 6, 1, outs + 1, 1, 0, 0);
+    if (rc) return rc;
+    if (!s_final) return WKV7_OK;
+    cudaError_t e = s_init ? cudaMemcpyAsync(s_final, s_init, st, cudaMemcpyDeviceToDevice, stream)
+                           : cudaMemsetAsync(s_final, 0, st, stream);
+    return e == cudaSuccess ? WKV7_OK : fail_cuda(e, "empty forward");
+  }
+  rc = check_spans(ins, 7, outs, 3, 6, 0);
+  if (rc) return rc;
+
+  FwdArgs args;
+  const int K = fwd_steps_per_stage(N, bf16);
+  for (int v = 0; v < 6; ++v)
+    if ((rc = make_map(&args.map[v], in[v], bf16, B, T, H, N, K))) return rc;
+  if ((rc = status_word(&args.status))) return rc;
+  args.s_init = s_init;
+  args.y = y;
+  args.s_final = s_final;
+  args.ckpt = ckpt;
+  args.C = ckpt ? C : 1;
+  args.nck = ckpt ? (T + C - 1) / C : 0;
+  args.B = B;
+  args.T = T;
+  args.H = H;
+  cudaError_t e = launch_fwd(args, bf16, N, stream);
+  if (e != cudaSuccess) return fail_cuda(e, "forward launch");
+  return WKV7_OK;
+}
+
+// ----------------------------------------------------------- backward ---
+
+int backward_impl(bool bf16, const void* const in[7], const float* s_init, const float* ckpt, int C,
+                  float* const grads[6], float* dS_init, int B, int T, int H, int N, cudaStream_t stream) {
+  int rc = check_dims(B, T, H, N);
+  if (rc) return rc;
+  if (ckpt && C < 1) return fail(WKV7_ERR_INVALID, "ckpt_every must be >= 1 (got %d)", C);
+  const int C_eff = ckpt ? C : (C >= 1 ? C : bwd_steps_per_stage(N, bf16));
+  const size_t es = bf16 ? 2 : 4;
+  const size_t vec = (size_t)B * T * H * N * es;
+  const size_t gvec = (size_t)B * T * H * N * 4;
+  const size_t st = (size_t)B * H * N * N * 4;
+  const Span ins[9] = {{in[0], vec, "r"},  {in[1], vec, "w"},     {in[2], vec, "k"},
+                       {in[3], vec, "v"},  {in[4], vec, "a"},     {in[5], vec, "b"},
+                       {in[6], vec, "dy"}, {s_init, st, "s_init"}, {ckpt, ckpt ? ckpt_bytes(B, T, H, N, C) : 0, "ckpt"}};
+  const Span outs[7] = {{grads[0], gvec, "dr"}, {grads[1], gvec, "dw"}, {grads[2], gvec, "dk"},
+                        {grads[3], gvec, "dv"}, {grads[4], gvec, "da"}, {grads[5], gvec, "db"},
+                        {dS_init, st, "dS_init"}};
+  // Empty problems: no step runs, so the carried gradient stays zero.
+  if ((size_t)B * H == 0) return WKV7_OK;
+  if (T == 0) {
+    rc = check_spans(ins + 7, 1, outs + 6, 1, 0, 0);
+    if (rc) return rc;
+    if (!dS_init) return WKV7_OK;
+    cudaError_t e = cudaMemsetAsync(dS_init, 0, st, stream);
+    return e == cudaSuccess ? WKV7_OK : fail_cuda(e, "empty backward");
+  }
+  rc = check_spans(ins, 9, outs, 7, 7, 6);
+  if (rc) return rc;
+
+  if (!ckpt) {
+    // Fault injection for tests: make the workspace allocation fail.
+    const char* inject = std::getenv("WKV7_FAIL_ALLOC");
+    if (inject && inject[0] == '1')
+      return fail(WKV7_ERR_ALLOC, "checkpoint workspace allocation failed (injected by WKV7_FAIL_ALLOC)");
+  }
+
+  BwdArgs args;
+  const int KS = bwd_steps_per_stage(N, bf16);
+  for (int v = 0; v < 7; ++v)
+    if ((rc = make_map(&args.map[v], in[v], bf16, B, T, H, N, KS))) return rc;
+
+  float* ws = nullptr;
+  if (!ckpt) {
+    const size_t bytes = ckpt_bytes(B, T, H, N, C_eff);
+    cudaError_t e = cudaMallocAsync(reinterpret_cast<void**>(&ws), bytes, stream);
+    if (e != cudaSuccess) {
+      cudaGetLastError();
+      return fail(WKV7_ERR_ALLOC, "checkpoint workspace of %zu bytes: %s", bytes, cudaGetErrorString(e));
+    }
+    FwdArgs fa;
+    const int K = fwd_steps_per_stage(N, bf16);
+    for (int v = 0; v < 6; ++v)
+      if ((rc = make_map(&fa.map[v], in[v], bf16, B, T, H, N, K))) {
+        cudaFreeAsync(ws, stream);
+        return rc;
+      }
+    if ((rc = status_word(&fa.status))) {
+      cudaFreeAsync(ws, stream);
+      return rc;
+    }
+    fa.s_init = s_init;
+    fa.y = nullptr;
+    fa.s_final = nullptr;
+    fa.ckpt = ws;
+    fa.C = C_eff;
+    fa.nck = (T + C_eff - 1) / C_eff;
+    fa.B = B;
+    fa.T = T;
+    fa.H = H;
+    e = launch_fwd(fa, bf16, N, stream);
+    if (e != cudaSuccess) {
+      cudaFreeAsync(ws, stream);
+      return fail_cuda(e, "checkpointing forward launch");
+    }
+  }
+  if ((rc = status_word(&args.status))) {
+    if (ws) cudaFreeAsync(ws, stream);
+    return rc;
+  }
+  args.ckpt = ckpt ? ckpt : ws;
+  args.dr = grads[0];
+  args.dw = grads[1];
+  args.dk = grads[2];
+  args.dv = grads[3];
+  args.da = grads[4];
+  args.db = grads[5];
+  args.dS_init = dS_init;
+  args.C = C_eff;
+  args.nck = (T + C_eff - 1) / C_eff;
+  args.B = B;
+  args.T = T;
+  args.H = H;
+  cudaError_t e = launch_bwd(args, bf16, N, stream);
+  if (ws) {
+    cudaError_t e2 = cudaFreeAsync(ws, stream);
+    if (e == cudaSuccess && e2 != cudaSuccess) return fail_cuda(e2, "cudaFreeAsync(workspace)");
+  }
+  if (e != cudaSuccess) return fail_cuda(e, "backward launch");
+  return WKV7_OK;
+}
+
+}  // namespace
+}  // namespace wkv7
+
+// ============================================================== C ABI ===
+
+using namespace wkv7;
+
+extern "C" {
+
+int wkv7_forward(const float* r, const float* w, const float* k, const float* v, const float* a,
+                 const float* b, const float* s_init, float* y, float* s_final, float* ckpt,
+                 int ckpt_every, int B, int T, int H, int N, void* stream) {
+  const void* in[6] = {r, w, k, v, a, b};
+  return forward_impl(false, in, s_init, y, s_final, ckpt, ckpt_every, B, T, H, N,
+                      static_cast<cudaStream_t>(stream));
+}
+
+int wkv7_forward_bf16(const wkv7_bf16* r, const wkv7_bf16* w, const wkv7_bf16* k, const wkv7_bf16* v,
+                      const wkv7_bf16* a, const wkv7_bf16* b, const float* s_init, wkv7_bf16* y,
+                      float* s_final, float* ckpt, int ckpt_every, int B, int T, int H, int N,
+                      void* stream) {
+  const void* in[6] = {r, w, k, v, a, b};
+  return forward_impl(true, in, s_init, y, s_final, ckpt, ckpt_every, B, T, H, N,
+                      static_cast<cudaStream_t>(stream));
+}
+
+int wkv7_backward(const float* r, const float* w, const float* k, const float* v, const float* a,
+                  const float* b, const float* dy, const float* s_init, const float* ckpt,
+                  int ckpt_every, float* dr, float* dw, float* dk, float* dv, float* da, float* db,
+                  float* dS_init, int B, int T, int H, int N, void* stream) {
+  const void* in[7] = {r, w, k, v, a, b, dy};
+  float* const grads[6] = {dr, dw, dk, dv, da, db};
+  return backward_impl(false, in, s_init, ckpt, ckpt_every, grads, dS_init, B, T, H, N,
+                       static_cast<cudaStream_t>(stream));
+}
+
+int wkv7_backward_bf16(const wkv7_bf16* r, const wkv7_bf16* w, const wkv7_bf16* k, const wkv7_bf16* v,
+                       const wkv7_bf16* a, const wkv7_bf16* b, const wkv7_bf16* dy, const float* s_init,
+                       const float* ckpt, int ckpt_every, float* dr, float* dw, float* dk, float* dv,
+                       float* da, float* db, float* dS_init, int B, int T, int H, int N, void* stream) {
+  const void* in[7] = {r, w, k, v, a, b, dy};
+  float* const grads[6] = {dr, dw, dk, dv, da, db};
+  return backward_impl(true, in, s_init, ckpt, ckpt_every, grads, dS_init, B, T, H, N,
+                       static_cast<cudaStream_t>(stream));
+}
+
+size_t wkv7_ckpt_bytes(int B, int T, int H, int N, int ckpt_every) {
+  if (ckpt_every < 1 || check_dims(B, T, H, N) != WKV7_OK) return 0;
+  return ckpt_bytes(B, T, H, N, ckpt_every);
+}
+
+int wkv7_default_ckpt_every(int N, int bf16) {
+  if (N != 16 && N != 32 && N != 64) return 0;
+  return bwd_steps_per_stage(N, bf16 != 0);
+}
+
+int wkv7_status(void* stream) {
+  cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return fail_cuda(e, "stream synchronize");
+  unsigned* word = nullptr;
+  int rc = status_word(&word);
+  if (rc) return rc;
+  unsigned host = 0;
+  e = cudaMemcpy(&host, word, sizeof host, cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess) return fail_cuda(e, "reading the status word");
+  if (host) {
+    const unsigned zero = 0;
+    e = cudaMemcpy(word, &zero, sizeof zero, cudaMemcpyHostToDevice);
+    if (e != cudaSuccess) return fail_cuda(e, "clearing the status word");
+    if (host & STATUS_TIMEOUT) return fail(WKV7_ERR_TIMEOUT, "a kernel gave up a bounded wait");
+  }
+  return WKV7_OK;
+}
+
+const char* wkv7_last_error(void) { return t_last_error.c_str(); }
+
+}  // extern "C"

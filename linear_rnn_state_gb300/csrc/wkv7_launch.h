@@ -1,0 +1,49 @@
+// Internal launch interface between the C ABI (wkv7_api.cu) and the kernels.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stddef.h>
+
+namespace wkv7 {
+
+// Forward kernel arguments. The tensor maps describe r, w, k, v, a, b as
+// 4-D tensors (N, H, T, B) with a box of (N, 1, K, 1): K steps of one head.
+struct FwdArgs {
+  CUtensorMap map[6];
+  const float* s_init;  // [B][H][N][N] or null (zeros)
+  void* y;              // [B][T][H][N] of the input type, or null
+  float* s_final;       // [B][H][N][N] or null
+  float* ckpt;          // [B][H][nck][N][N] or null
+  unsigned* status;     // device status word (timeout flag)
+  int C;                // checkpoint interval (steps)
+  int nck;              // ceil(T / C)
+  int B, T, H;
+};
+
+// Backward kernel arguments. Tensor maps for r, w, k, v, a, b, dy with a box
+// of (N, 1, KS, 1).
+struct BwdArgs {
+  CUtensorMap map[7];
+  const float* ckpt;  // [B][H][nck][N][N], checkpoint c = state before step c*C
+  float* dr;
+  float* dw;
+  float* dk;
+  float* dv;
+  float* da;
+  float* db;
+  float* dS_init;  // [B][H][N][N] or null
+  unsigned* status;
+  int C, nck;
+  int B, T, H;
+};
+
+// Steps per TMA box for each kernel (the K / KS template parameter chosen
+// for this N and input type).
+int fwd_steps_per_stage(int N, bool bf16);
+int bwd_steps_per_stage(int N, bool bf16);
+
+cudaError_t launch_fwd(const FwdArgs& args, bool bf16, int N, cudaStream_t stream);
+cudaError_t launch_bwd(const BwdArgs& args, bool bf16, int N, cudaStream_t stream);
+
+}  // namespace wkv7
