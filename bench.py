@@ -121,15 +121,16 @@ def _work_per_token_head(N, C, in_bytes):
     return f_flop, b_flop, f_bytes, b_bytes
 
 
-def cpu_baseline_sample(wl, d, heads_per_round, rounds=1, nthreads=0):
-    """Time the oracle (fwd + bwd, fp64) on whole heads of the workload."""
+def cpu_baseline_sample(wl, d, heads, nthreads=0):
+    """Time the oracle (fwd + bwd, fp64) on the first `heads` (b, h) heads of
+    the workload, each over its whole sequence, on every host core."""
     import numpy as np
 
     import oracle
     from linear_rnn_state_gb300 import inputs
 
     cores = nthreads or len(os.sched_getaffinity(0))
-    P = min(wl.B * wl.H, heads_per_round * rounds)
+    P = min(wl.B * wl.H, heads)
     heads = [(i // wl.H, i % wl.H) for i in range(P)]
     o = {n: inputs.as_f64(d[n], wl.storage) for n in ("r", "w", "k", "v", "a", "b", "dy")}
     sel = {n: np.stack([o[n][bi, :, hi, :] for bi, hi in heads])[:, :, None, :] for n in o}
@@ -149,12 +150,12 @@ def run_reference(args):
 
     wl = configs.WORKLOADS[configs.BENCH_WORKLOAD]
     d = inputs.generate(wl.B, wl.T, wl.H, wl.N, wl.storage, wl.s_init_std, seed=0)
-    cores = len(os.sched_getaffinity(0))
+    # each step: the whole workload (every (b, h) head over its full sequence)
     for _ in range(args.warmup):
-        cpu_baseline_sample(wl, d, cores)
+        cpu_baseline_sample(wl, d, wl.B * wl.H)
     times, toks = [], 0.0
     for _ in range(args.steps):
-        v, used, P, dt = cpu_baseline_sample(wl, d, cores)
+        v, used, P, dt = cpu_baseline_sample(wl, d, wl.B * wl.H)
         times.append(dt)
         toks += wl.T * P / wl.H
     value = toks / sum(times)
@@ -185,6 +186,8 @@ def run_gpu(args):
     dev = torch.device("cuda", local)
     wl = configs.WORKLOADS[configs.BENCH_WORKLOAD]
     B, T, H, N = wl.B, wl.T, wl.H, wl.N
+    if args.T:  # shorter sequence of the same layer shape, for profiler captures
+        T = args.T
     bf16 = wl.storage == "bf16"
     C = wkv7.wkv7_default_ckpt_every(N, bf16)
     names = ("r", "w", "k", "v", "a", "b", "dy")
@@ -249,7 +252,20 @@ def run_gpu(args):
         dist.all_reduce(tt, op=dist.ReduceOp.MAX)
         ms = tt.item()
 
-    # ---- end to end through the C ABI with host buffers (pinned)
+    if args.no_e2e:
+        e2e_ms = None
+    else:
+        e2e_ms = _e2e(args, d, names, t_in, grads, y, dS, bf16, tdt, step, stream, dist, dev)
+    if rank != 0:
+        return 0
+    return _report(args, wl, world, B, T, H, N, C, bf16, ms, fwd_ms, bwd_ms, e2e_ms, ckpt, d, clocks, dev)
+
+
+def _e2e(args, d, names, t_in, grads, y, dS, bf16, tdt, step, stream, dist, dev):
+    """End-to-end step through the C ABI with pinned host buffers: copy the
+    step's inputs in, run forward + backward, copy every output back."""
+    import torch
+
     host_in = {n: torch.from_numpy(d[n]).pin_memory() for n in names}
     host_out = {n: torch.empty(grads[n].shape, dtype=torch.float32).pin_memory() for n in grads}
     host_y = torch.empty(y.shape, dtype=tdt).pin_memory()
@@ -283,9 +299,12 @@ def run_gpu(args):
         tt = torch.tensor([e2e_ms], device=dev)
         dist.all_reduce(tt, op=dist.ReduceOp.MAX)
         e2e_ms = tt.item()
+    return e2e_ms, h2d, d2h
 
-    if rank != 0:
-        return 0
+
+def _report(args, wl, world, B, T, H, N, C, bf16, ms, fwd_ms, bwd_ms, e2e, ckpt, d, clocks, dev):
+    import torch
+
     peaks = _peaks()
     BTH = B * T * H
     f_flop, b_flop, f_bytes, b_bytes = _work_per_token_head(N, C, 2 if bf16 else 4)
@@ -294,14 +313,13 @@ def run_gpu(args):
     achieved = b_flop * BTH / (bwd_ms * 1e-3)
     t_roof = max((f_flop + b_flop) * BTH / peak_flops, (f_bytes + b_bytes) * BTH / (peaks["hbm_gbs"] * 1e9))
     value = world * B * T / (ms * 1e-3)
-    ncores = len(os.sched_getaffinity(0))
-    cpu_v, cpu_cores, cpu_P, cpu_dt = cpu_baseline_sample(wl, d, ncores) if not args.no_cpu_baseline else (
-        None, 0, 0, 0.0)
+    cpu_v, cpu_cores, cpu_P, cpu_dt = cpu_baseline_sample(wl, d, B * H) if not args.no_cpu_baseline and T == wl.T \
+        else (None, 0, 0, 0.0)
     line = {
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f32", "data": "synthetic",
-        "config": {"workload": wl.name, "B": B, "T": T, "H": H, "N": N, "storage": wl.storage, "ckpt_every": C,
+        "config": {"workload": wl.name if T == wl.T else f"{wl.name} (T={T})", "B": B, "T": T, "H": H, "N": N, "storage": wl.storage, "ckpt_every": C,
                    "l2": "no flush: inputs, checkpoints and gradients (%.1f GB) exceed the 129 MB L2"
                          % ((7 * BTH * N * (2 if bf16 else 4) + ckpt.numel() * 4 + 6 * BTH * N * 4) / 1e9)},
         "fwd_ms": fwd_ms, "bwd_ms": bwd_ms, "step_roofline_frac": t_roof / (ms * 1e-3),
@@ -309,8 +327,9 @@ def run_gpu(args):
                      "frac": achieved / peak_flops, "traffic": None, "kernel": "wkv7_bwd_kernel",
                      "peak_source": f"{sms} SMs x {FP32_LANES_PER_SM} FP32 lanes x 2 x {peaks['sm_max_mhz']:.0f} MHz",
                      "hbm_gbs_achieved": b_bytes * BTH / (bwd_ms * 1e-3) / 1e9, "hbm_peak_gbs": peaks["hbm_gbs"]},
-        "e2e": {"value": world * B * T / (e2e_ms * 1e-3), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
-                "d2h_bytes_per_step": d2h},
+        "e2e": None if e2e is None else {
+            "value": world * B * T / (e2e[0] * 1e-3), "unit": "tokens/s", "h2d_bytes_per_step": e2e[1],
+            "d2h_bytes_per_step": e2e[2]},
         "gpu_launches": 2 * args.steps,
         "clocks": clocks.summary(),
     }
@@ -327,7 +346,9 @@ def main():
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["gb300", "reference"], default="gb300")
-    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true", help="skip the timed oracle sample")
+    ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end measurement")
+    ap.add_argument("--T", type=int, default=0, help="override T (profiler captures of a smaller case)")
     args = ap.parse_args()
     if args.impl == "reference":
         return run_reference(args)
