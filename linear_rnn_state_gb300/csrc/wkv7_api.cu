@@ -120,6 +120,21 @@ int make_map(CUtensorMap* map, const void* base, bool bf16, int B, int T, int H,
   return WKV7_OK;
 }
 
+// Checkpoints [B*H*nck][N][N] fp32 as a 3-D map (N, N, B*H*nck), one state per box.
+int make_ckpt_map(CUtensorMap* map, const float* ckpt, int B, int H, int N, int nck) {
+  auto enc = encode_fn();
+  if (!enc) return fail(WKV7_ERR_CUDA, "cuTensorMapEncodeTiled is unavailable");
+  cuuint64_t dims[3] = {(cuuint64_t)N, (cuuint64_t)N, (cuuint64_t)B * H * nck};
+  cuuint64_t strides[2] = {(cuuint64_t)N * 4, (cuuint64_t)N * N * 4};
+  cuuint32_t box[3] = {(cuuint32_t)N, (cuuint32_t)N, 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<float*>(ckpt), dims, strides, box, estr,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(WKV7_ERR_CUDA, "cuTensorMapEncodeTiled (checkpoints) failed (%d)", (int)r);
+  return WKV7_OK;
+}
+
 std::mutex g_status_mu;
 unsigned* g_status_ptr[kMaxDevices];
 
@@ -182,7 +197,7 @@ int forward_impl(bool bf16, const void* const in[6], const float* s_init, void* 
   args.B = B;
   args.T = T;
   args.H = H;
-  cudaError_t e = launch_fwd(args, bf16, N, stream);
+  cudaError_t e = launch_fwd2(args, bf16, N, stream);
   if (e != cudaSuccess) return fail_cuda(e, "forward launch");
   return WKV7_OK;
 }
@@ -194,7 +209,7 @@ int backward_impl(bool bf16, const void* const in[7], const float* s_init, const
   int rc = check_dims(B, T, H, N);
   if (rc) return rc;
   if (ckpt && C < 1) return fail(WKV7_ERR_INVALID, "ckpt_every must be >= 1 (got %d)", C);
-  const int C_eff = ckpt ? C : (C >= 1 ? C : bwd_steps_per_stage(N, bf16));
+  const int C_eff = ckpt ? C : (C >= 1 ? C : bwd2_steps_per_window(N, bf16));
   const size_t es = bf16 ? 2 : 4;
   const size_t vec = (size_t)B * T * H * N * es;
   const size_t gvec = (size_t)B * T * H * N * 4;
@@ -225,7 +240,7 @@ int backward_impl(bool bf16, const void* const in[7], const float* s_init, const
   }
 
   BwdArgs args;
-  const int KS = bwd_steps_per_stage(N, bf16);
+  const int KS = bwd2_steps_per_window(N, bf16);
   for (int v = 0; v < 7; ++v)
     if ((rc = make_map(&args.map[v], in[v], bf16, B, T, H, N, KS))) return rc;
 
@@ -257,7 +272,7 @@ int backward_impl(bool bf16, const void* const in[7], const float* s_init, const
     fa.B = B;
     fa.T = T;
     fa.H = H;
-    e = launch_fwd(fa, bf16, N, stream);
+    e = launch_fwd2(fa, bf16, N, stream);
     if (e != cudaSuccess) {
       cudaFreeAsync(ws, stream);
       return fail_cuda(e, "checkpointing forward launch");
@@ -268,6 +283,10 @@ int backward_impl(bool bf16, const void* const in[7], const float* s_init, const
     return rc;
   }
   args.ckpt = ckpt ? ckpt : ws;
+  if ((rc = make_ckpt_map(&args.ckmap, args.ckpt, B, H, N, (T + C_eff - 1) / C_eff))) {
+    if (ws) cudaFreeAsync(ws, stream);
+    return rc;
+  }
   args.dr = grads[0];
   args.dw = grads[1];
   args.dk = grads[2];
@@ -280,7 +299,7 @@ int backward_impl(bool bf16, const void* const in[7], const float* s_init, const
   args.B = B;
   args.T = T;
   args.H = H;
-  cudaError_t e = launch_bwd(args, bf16, N, stream);
+  cudaError_t e = launch_bwd2(args, bf16, N, stream);
   if (ws) {
     cudaError_t e2 = cudaFreeAsync(ws, stream);
     if (e == cudaSuccess && e2 != cudaSuccess) return fail_cuda(e2, "cudaFreeAsync(workspace)");
@@ -342,7 +361,7 @@ size_t wkv7_ckpt_bytes(int B, int T, int H, int N, int ckpt_every) {
 
 int wkv7_default_ckpt_every(int N, int bf16) {
   if (N != 16 && N != 32 && N != 64) return 0;
-  return bwd_steps_per_stage(N, bf16 != 0);
+  return bwd2_steps_per_window(N, bf16 != 0);
 }
 
 int wkv7_status(void* stream) {

@@ -25,6 +25,7 @@ struct FwdArgs {
 // of (N, 1, KS, 1).
 struct BwdArgs {
   CUtensorMap map[7];
+  CUtensorMap ckmap;  // checkpoints as (N, N, B*H*nck), box (N, N, 1)
   const float* ckpt;  // [B][H][nck][N][N], checkpoint c = state before step c*C
   float* dr;
   float* dw;
@@ -44,6 +45,9 @@ int fwd_steps_per_stage(int N, bool bf16);
 int bwd_steps_per_stage(int N, bool bf16);
 
 cudaError_t launch_fwd(const FwdArgs& args, bool bf16, int N, cudaStream_t stream);
+cudaError_t launch_fwd2(const FwdArgs& args, bool bf16, int N, cudaStream_t stream);
 cudaError_t launch_bwd(const BwdArgs& args, bool bf16, int N, cudaStream_t stream);
+cudaError_t launch_bwd2(const BwdArgs& args, bool bf16, int N, cudaStream_t stream);
+int bwd2_steps_per_window(int N, bool bf16);
 
 }  // namespace wkv7
