@@ -60,9 +60,9 @@ struct Bwd2Cfg {
   static constexpr int DV = KS * N;
   static constexpr int NDER = 10;  // k, b, a, r, c, ic, w, v, dy, sa
   static constexpr size_t OFF_DER = NSTAGE * STAGE_BYTES;
-  static constexpr size_t OFF_SC = OFF_DER + (size_t)NDER * DV * 4;  // beta[KS], rho[KS]
+  static constexpr size_t OFF_SC = OFF_DER + (size_t)NDER * DV * 4;  // beta, rho partials
   static constexpr int NSUM = 5;                                       // dr, dk, db, dw, da
-  static constexpr size_t OFF_COL = a128(OFF_SC + (size_t)2 * KS * 4);
+  static constexpr size_t OFF_COL = a128(OFF_SC + (size_t)4 * KS * 4);
   static constexpr size_t COL_BYTES = (size_t)KS * NWARPS * NSUM * N * 4;
   static constexpr size_t OFF_BAR = OFF_COL + COL_BYTES;
   static constexpr size_t SMEM_BYTES = OFF_BAR + 64;
@@ -133,7 +133,7 @@ __global__ void __launch_bounds__(Bwd2Cfg<TIn, N, R, E, KS>::THREADS, 1)
   float* d_dy = d_v + DV;
   float* d_sa = d_dy + DV;
   float* beta = reinterpret_cast<float*>(smem + Cfg::OFF_SC);
-  float* rho = beta + KS;
+  float* rho = beta + 2 * KS;
   float* colbuf = reinterpret_cast<float*>(smem + Cfg::OFF_COL);
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + Cfg::OFF_BAR);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + Cfg::OFF_BAR + 32);
@@ -207,6 +207,12 @@ __global__ void __launch_bounds__(Bwd2Cfg<TIn, N, R, E, KS>::THREADS, 1)
       pre_valid = w_next(pre);
     }
 
+  // Prologue split: SPLIT threads per column, each scanning KS / SPLIT steps.
+  constexpr int SPLIT = Cfg::THREADS / N >= 2 ? 2 : 1;
+  constexpr int LS = KS / SPLIT;
+  constexpr int BPN = N > 32 ? N / 32 : 1;  // partial dot products per step
+  const int pj = tid % N, ppart = tid / N;
+
   float2 Gt[R][NP];
 #pragma unroll
   for (int i = 0; i < R; ++i)
@@ -242,50 +248,45 @@ __global__ void __launch_bounds__(Bwd2Cfg<TIn, N, R, E, KS>::THREADS, 1)
         }
     }
 
+    // ---- prologue, scaled form (identity steps beyond len): c(l) = w(0)..w(l)
+    // of this window; k~ = k/c, b~ = b/c, a^ = c(l-1) a, r^ = c r, 1/c; beta
+    // and rho as per-warp partial dot products. Also checks the decays.
     bool unsafe = false;
-    for (int o = tid; o < len * N; o += Cfg::THREADS)
-      if (!decay_is_safe(raw1(rs + V_W * RV + o))) unsafe = true;
-    const bool direct = __syncthreads_or(unsafe) != 0;
-
-    // ---- prologue: per-step fp32 vectors (identity steps beyond len)
-    for (int j = tid; j < N; j += Cfg::THREADS) {
+    if (ppart < SPLIT) {
+      const int l0 = ppart * LS;
       float cv = 1.f;
-      for (int l = 0; l < KS; ++l) {
-        const int o = l * N + j;
+      for (int l = 0; l < l0; ++l)
+        if (l < len) cv *= raw1(rs + V_W * RV + l * N + pj);
+#pragma unroll 4
+      for (int l = l0; l < l0 + LS; ++l) {
+        const int o = l * N + pj;
         const bool valid = l < len;
         const float w = valid ? raw1(rs + V_W * RV + o) : 1.f;
-        const float k = valid ? raw1(rs + V_K * RV + o) : 0.f;
+        if (!decay_is_safe(w)) unsafe = true;
         const float b = valid ? raw1(rs + V_B * RV + o) : 0.f;
         const float r = valid ? raw1(rs + V_R * RV + o) : 0.f;
-        const float a = valid ? raw1(rs + V_A * RV + o) : 0.f;
+        const float cp = cv;
+        cv *= w;
+        const float ic = rcp_approx(cv);
+        d_k[o] = valid ? raw1(rs + V_K * RV + o) * ic : 0.f;
+        d_b[o] = b * ic;
+        d_a[o] = valid ? raw1(rs + V_A * RV + o) * cp : 0.f;
+        d_r[o] = r * cv;
+        d_c[o] = cv;
+        d_ic[o] = ic;
+        d_w[o] = w;
         d_v[o] = valid ? raw1(rs + V_V * RV + o) : 0.f;
         d_dy[o] = valid ? raw1(rs + V_DY * RV + o) : 0.f;
-        d_w[o] = w;
-        if (direct) {
-          d_k[o] = k; d_b[o] = b; d_a[o] = a; d_r[o] = r; d_c[o] = 1.f; d_ic[o] = 1.f;
-        } else {
-          const float cp = cv;
-          cv = cv * w;
-          const float ic = __frcp_rn(cv);
-          d_k[o] = k * ic; d_b[o] = b * ic; d_a[o] = a * cp; d_r[o] = r * cv; d_c[o] = cv; d_ic[o] = ic;
+        const float an = l + 1 < len ? raw1(rs + V_A * RV + o + N) : 0.f;
+        float pb = b * an, pr = r * b;
+#pragma unroll
+        for (int mask = 1; mask < (N < 32 ? N : 32); mask <<= 1) {
+          pb += __shfl_xor_sync(0xffffffffu, pb, mask);
+          pr += __shfl_xor_sync(0xffffffffu, pr, mask);
         }
-      }
-    }
-    if (!direct) {  // beta(l) = b(l) . a(l+1), rho(l) = r(l) . b(l)
-      for (int l = warp; l < KS; l += NWARPS) {
-        float sb = 0.f, sr = 0.f;
-        for (int j = lane; j < N; j += 32) {
-          const float b = l < len ? raw1(rs + V_B * RV + l * N + j) : 0.f;
-          const float an = l + 1 < len ? raw1(rs + V_A * RV + (l + 1) * N + j) : 0.f;
-          const float r = l < len ? raw1(rs + V_R * RV + l * N + j) : 0.f;
-          sb = fmaf(b, an, sb);
-          sr = fmaf(r, b, sr);
-        }
-        sb = group_allreduce<32>(sb);
-        sr = group_allreduce<32>(sr);
-        if (lane == 0) {
-          beta[l] = sb;
-          rho[l] = sr;
+        if ((lane & ((N < 32 ? N : 32) - 1)) == 0) {
+          beta[(pj / 32) * KS + l] = pb;
+          rho[(pj / 32) * KS + l] = pr;
         }
       }
     }
@@ -307,7 +308,20 @@ __global__ void __launch_bounds__(Bwd2Cfg<TIn, N, R, E, KS>::THREADS, 1)
     }
 #pragma unroll
     for (int i = 0; i < R; ++i) sa[i] = group_allreduce<G>(sa[i]);
-    __syncthreads();  // per-step vectors complete; the raw stage is free
+    const bool direct = __syncthreads_or(unsafe) != 0;  // per-step vectors complete
+    if (direct) {
+      // ---- rare: some decay outside the safe range; plain vectors instead
+      for (int o = tid; o < KS * N; o += Cfg::THREADS) {
+        const bool valid = o / N < len;
+        d_k[o] = valid ? raw1(rs + V_K * RV + o) : 0.f;
+        d_b[o] = valid ? raw1(rs + V_B * RV + o) : 0.f;
+        d_a[o] = valid ? raw1(rs + V_A * RV + o) : 0.f;
+        d_r[o] = valid ? raw1(rs + V_R * RV + o) : 0.f;
+        d_c[o] = 1.f;
+        d_ic[o] = 1.f;
+      }
+      __syncthreads();
+    }
     if (tid == 0 && pre_valid) {
       issue(pre, st);
       pre_valid = w_next(pre);
@@ -337,33 +351,50 @@ __global__ void __launch_bounds__(Bwd2Cfg<TIn, N, R, E, KS>::THREADS, 1)
         if (record && cg == 0)
 #pragma unroll
           for (int i = 0; i < R; ++i) d_sa[l * N + row0 + i] = sa[i];
-        float X[R];
-#pragma unroll
-        for (int i = 0; i < R; ++i) X[i] = 0.f;
         const bool ahead = l + 1 < KS;
+        float2 kv[NP], bv[NP], av[NP];
 #pragma unroll
         for (int m = 0; m < Q; ++m) {
           const float4 k4 = ld_f4(d_k + l * N + colq(m));
           const float4 b4 = ld_f4(d_b + l * N + colq(m));
           const float4 a4 = ahead ? ld_f4(d_a + (l + 1) * N + colq(m)) : make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-          for (int h = 0; h < 2; ++h) {
-            const int p = 2 * m + h;
-            const float2 k2 = h ? hi2(k4) : lo2(k4), b2 = h ? hi2(b4) : lo2(b4), a2 = h ? hi2(a4) : lo2(a4);
-            float2 dr2 = make_float2(0.f, 0.f);
-#pragma unroll
-            for (int i = 0; i < R; ++i) {
-              const float2 u = ffma2(f2(vr[i]), k2, S[i][p]);
-              const float2 xa = fmul2(u, a2);
-              X[i] += xa.x + xa.y;
-              S[i][p] = ffma2(f2(sa[i]), b2, u);
-              dr2 = ffma2(S[i][p], f2(dyr[i]), dr2);
-            }
-            pdr[2 * p] = dr2.x;
-            pdr[2 * p + 1] = dr2.y;
-          }
+          kv[2 * m] = lo2(k4); kv[2 * m + 1] = hi2(k4);
+          bv[2 * m] = lo2(b4); bv[2 * m + 1] = hi2(b4);
+          av[2 * m] = lo2(a4); av[2 * m + 1] = hi2(a4);
         }
-        const float bl = beta[l];
+        float bl = beta[l];
+#pragma unroll
+        for (int q = 1; q < BPN; ++q) bl += beta[q * KS + l];
+        // u~ = S~ + v k~
+#pragma unroll
+        for (int i = 0; i < R; ++i)
+#pragma unroll
+          for (int p = 0; p < NP; ++p) S[i][p] = ffma2(f2(vr[i]), kv[p], S[i][p]);
+        float X[R];
+#pragma unroll
+        for (int i = 0; i < R; ++i) {
+          float2 x0 = fmul2(S[i][0], av[0]);
+          float2 x1 = fmul2(S[i][1], av[1]);
+#pragma unroll
+          for (int p = 2; p < NP; p += 2) {
+            x0 = ffma2(S[i][p], av[p], x0);
+            x1 = ffma2(S[i][p + 1], av[p + 1], x1);
+          }
+          X[i] = hsum(fadd2(x0, x1));
+        }
+        // S~ = u~ + sa b~, and dr partials over this thread's rows
+#pragma unroll
+        for (int i = 0; i < R; ++i)
+#pragma unroll
+          for (int p = 0; p < NP; ++p) S[i][p] = ffma2(f2(sa[i]), bv[p], S[i][p]);
+#pragma unroll
+        for (int p = 0; p < NP; ++p) {
+          float2 d2 = fmul2(S[0][p], f2(dyr[0]));
+#pragma unroll
+          for (int i = 1; i < R; ++i) d2 = ffma2(S[i][p], f2(dyr[i]), d2);
+          pdr[2 * p] = d2.x;
+          pdr[2 * p + 1] = d2.y;
+        }
 #pragma unroll
         for (int i = 0; i < R; ++i) sa[i] = fmaf(sa[i], bl, group_allreduce<G>(X[i]));
       } else {
@@ -453,89 +484,123 @@ __global__ void __launch_bounds__(Bwd2Cfg<TIn, N, R, E, KS>::THREADS, 1)
         dsa_next[i] = 0.f;
         zc[i] = 0.f;
       }
+      float spv[TILE];  // S~_prev tile of the step, loaded one step ahead
+      tmem_ld<TILE>(tlane + (uint32_t)((KS - 1) * TILE), spv);
 #pragma unroll 1
       for (int l = KS - 1; l >= 0; --l) {
-        float spv[TILE];
-        tmem_ld<TILE>(tlane + (uint32_t)(l * TILE), spv);
         tmem_wait_ld();
         float dyr[R], vr[R], sar[R];
         ld_rows<R>(d_dy + l * N + row0, dyr);
         ld_rows<R>(d_v + l * N + row0, vr);
         ld_rows<R>(d_sa + l * N + row0, sar);
-        const bool first = l == KS - 1;  // dsa from the full row sum
-        constexpr int NV1 = (3 * E + RGN - 1) / RGN * RGN;
-        float p1[NV1];  // dk, db, dw partials
-        float pdv[R], pz[R], pds[R];
-#pragma unroll
-        for (int i = 0; i < R; ++i) { pdv[i] = 0.f; pz[i] = 0.f; pds[i] = 0.f; }
+        const bool first = l == KS - 1;           // dsa from the full row sum
+        const bool use_z = !direct && l > 0;      // row sum feeding dsa(t-1)
+        const bool use_d = direct || first;
+        float2 r2[NP], k2[NP], bz[NP], bd[NP];
 #pragma unroll
         for (int m = 0; m < Q; ++m) {
           const float4 r4 = ld_f4(d_r + l * N + colq(m));
           const float4 k4 = ld_f4(d_k + l * N + colq(m));
-          const float4 bz4 = (!direct && l > 0) ? ld_f4(d_b + (l - 1) * N + colq(m)) : make_float4(0.f, 0.f, 0.f, 0.f);
-          const float4 bd4 = (direct || first) ? ld_f4(d_b + l * N + colq(m)) : make_float4(0.f, 0.f, 0.f, 0.f);
+          const float4 z4 = use_z ? ld_f4(d_b + (l - 1) * N + colq(m)) : make_float4(0.f, 0.f, 0.f, 0.f);
+          const float4 d4 = use_d ? ld_f4(d_b + l * N + colq(m)) : make_float4(0.f, 0.f, 0.f, 0.f);
+          r2[2 * m] = lo2(r4); r2[2 * m + 1] = hi2(r4);
+          k2[2 * m] = lo2(k4); k2[2 * m + 1] = hi2(k4);
+          bz[2 * m] = lo2(z4); bz[2 * m + 1] = hi2(z4);
+          bd[2 * m] = lo2(d4); bd[2 * m + 1] = hi2(d4);
+        }
+        // G~ += dy r^
 #pragma unroll
-          for (int h = 0; h < 2; ++h) {
-            const int p = 2 * m + h;
-            const float2 r2 = h ? hi2(r4) : lo2(r4), k2 = h ? hi2(k4) : lo2(k4);
-            const float2 bz = h ? hi2(bz4) : lo2(bz4), bd = h ? hi2(bd4) : lo2(bd4);
-            float2 ak = make_float2(0.f, 0.f), ab = ak, aw = ak;
+        for (int i = 0; i < R; ++i)
 #pragma unroll
-            for (int i = 0; i < R; ++i) {
-              Gt[i][p] = ffma2(f2(dyr[i]), r2, Gt[i][p]);
-              ak = ffma2(Gt[i][p], f2(vr[i]), ak);
-              ab = ffma2(Gt[i][p], f2(sar[i]), ab);
-              aw = ffma2(Gt[i][p], make_float2(spv[i * E + 2 * p], spv[i * E + 2 * p + 1]), aw);
-              const float2 dv2 = fmul2(Gt[i][p], k2);
-              pdv[i] += dv2.x + dv2.y;
-              const float2 z2 = fmul2(Gt[i][p], bz);
-              pz[i] += z2.x + z2.y;
-              const float2 d2 = fmul2(Gt[i][p], bd);
-              pds[i] += d2.x + d2.y;
-            }
-            p1[2 * p] = ak.x; p1[2 * p + 1] = ak.y;
-            p1[E + 2 * p] = ab.x; p1[E + 2 * p + 1] = ab.y;
-            p1[2 * E + 2 * p] = aw.x; p1[2 * E + 2 * p + 1] = aw.y;
+          for (int p = 0; p < NP; ++p) Gt[i][p] = ffma2(f2(dyr[i]), r2[p], Gt[i][p]);
+        // column partials: dk (G~^T v), db (G~^T sa), dw (colsum G~ o S~_prev)
+        constexpr int NV1 = (3 * E + RGN - 1) / RGN * RGN;
+        float p1[NV1];
+#pragma unroll
+        for (int p = 0; p < NP; ++p) {
+          const float2 s0 = make_float2(spv[2 * p], spv[2 * p + 1]);
+          float2 ak = fmul2(Gt[0][p], f2(vr[0]));
+          float2 ab = fmul2(Gt[0][p], f2(sar[0]));
+          float2 aw = fmul2(Gt[0][p], s0);
+#pragma unroll
+          for (int i = 1; i < R; ++i) {
+            ak = ffma2(Gt[i][p], f2(vr[i]), ak);
+            ab = ffma2(Gt[i][p], f2(sar[i]), ab);
+            aw = ffma2(Gt[i][p], make_float2(spv[i * E + 2 * p], spv[i * E + 2 * p + 1]), aw);
           }
+          p1[2 * p] = ak.x; p1[2 * p + 1] = ak.y;
+          p1[E + 2 * p] = ab.x; p1[E + 2 * p + 1] = ab.y;
+          p1[2 * E + 2 * p] = aw.x; p1[2 * E + 2 * p + 1] = aw.y;
         }
 #pragma unroll
         for (int v = 3 * E; v < NV1; ++v) p1[v] = 0.f;
-        float dsa[R];
-        const float bl = beta[l], rl = rho[l];
+        // row partials: dv (G~ k~), z (G~ b~(t-1)) and, first / direct, dsa (G~ b~(t))
+        float pdv[R], pz[R], pds[R];
 #pragma unroll
         for (int i = 0; i < R; ++i) {
-          if (direct || first) dsa[i] = group_allreduce<G>(pds[i]);
-          else dsa[i] = zc[i] + dsa_next[i] * bl + dyr[i] * rl;
-          zc[i] = direct ? 0.f : group_allreduce<G>(pz[i]);
-          pdv[i] = group_allreduce<G>(pdv[i]);
-        }
-        if (cg == 0 && l < len) {
-          float* dvp = args.dv + vbase + (size_t)(start + l) * vstep + row0;
+          float2 d0 = fmul2(Gt[i][0], k2[0]), d1 = fmul2(Gt[i][1], k2[1]);
+          float2 z0 = fmul2(Gt[i][0], bz[0]), z1 = fmul2(Gt[i][1], bz[1]);
+          float2 e0 = fmul2(Gt[i][0], bd[0]), e1 = fmul2(Gt[i][1], bd[1]);
 #pragma unroll
-          for (int i = 0; i < R; ++i) dvp[i] = pdv[i];
+          for (int p = 2; p < NP; p += 2) {
+            d0 = ffma2(Gt[i][p], k2[p], d0); d1 = ffma2(Gt[i][p + 1], k2[p + 1], d1);
+            z0 = ffma2(Gt[i][p], bz[p], z0); z1 = ffma2(Gt[i][p + 1], bz[p + 1], z1);
+            e0 = ffma2(Gt[i][p], bd[p], e0); e1 = ffma2(Gt[i][p + 1], bd[p + 1], e1);
+          }
+          pdv[i] = hsum(fadd2(d0, d1));
+          pz[i] = hsum(fadd2(z0, z1));
+          pds[i] = hsum(fadd2(e0, e1));
         }
+        float bl = beta[l], rl = rho[l];
+#pragma unroll
+        for (int q = 1; q < BPN; ++q) {
+          bl += beta[q * KS + l];
+          rl += rho[q * KS + l];
+        }
+        float dsa[R];
+#pragma unroll
+        for (int i = 0; i < R; ++i) {
+          dsa[i] = use_d ? group_allreduce<G>(pds[i]) : zc[i] + dsa_next[i] * bl + dyr[i] * rl;
+          zc[i] = use_z ? group_allreduce<G>(pz[i]) : 0.f;
+        }
+        {
+          const float dvv = rowsum_scatter<G, R>(pdv, cg);
+          if (l < len && row_writer<G, R>(cg))
+            args.dv[vbase + (size_t)(start + l) * vstep + row0 + row_of_lane<G, R>(cg)] = dvv;
+        }
+        // da partials (S~_prev^T dsa) and the carry G~ += dsa a^ (direct: G = G w + dsa a)
         constexpr int NV2 = (E + RGN - 1) / RGN * RGN;
-        float p2[NV2];  // da partials
+        float p2[NV2];
+        float2 a2[NP], w2[NP];
 #pragma unroll
         for (int m = 0; m < Q; ++m) {
           const float4 a4 = ld_f4(d_a + l * N + colq(m));
           const float4 w4 = direct ? ld_f4(d_w + l * N + colq(m)) : make_float4(1.f, 1.f, 1.f, 1.f);
+          a2[2 * m] = lo2(a4); a2[2 * m + 1] = hi2(a4);
+          w2[2 * m] = lo2(w4); w2[2 * m + 1] = hi2(w4);
+        }
 #pragma unroll
-          for (int h = 0; h < 2; ++h) {
-            const int p = 2 * m + h;
-            const float2 a2 = h ? hi2(a4) : lo2(a4), w2 = h ? hi2(w4) : lo2(w4);
-            float2 aa = make_float2(0.f, 0.f);
+        for (int p = 0; p < NP; ++p) {
+          float2 aa = fmul2(f2(dsa[0]), make_float2(spv[2 * p], spv[2 * p + 1]));
 #pragma unroll
-            for (int i = 0; i < R; ++i) {
-              aa = ffma2(f2(dsa[i]), make_float2(spv[i * E + 2 * p], spv[i * E + 2 * p + 1]), aa);
-              Gt[i][p] = direct ? ffma2(Gt[i][p], w2, fmul2(f2(dsa[i]), a2)) : ffma2(f2(dsa[i]), a2, Gt[i][p]);
-            }
-            p2[2 * p] = aa.x;
-            p2[2 * p + 1] = aa.y;
-          }
+          for (int i = 1; i < R; ++i) aa = ffma2(f2(dsa[i]), make_float2(spv[i * E + 2 * p], spv[i * E + 2 * p + 1]), aa);
+          p2[2 * p] = aa.x;
+          p2[2 * p + 1] = aa.y;
         }
 #pragma unroll
         for (int v = E; v < NV2; ++v) p2[v] = 0.f;
+        if (!direct) {
+#pragma unroll
+          for (int i = 0; i < R; ++i)
+#pragma unroll
+            for (int p = 0; p < NP; ++p) Gt[i][p] = ffma2(f2(dsa[i]), a2[p], Gt[i][p]);
+        } else {
+#pragma unroll
+          for (int i = 0; i < R; ++i)
+#pragma unroll
+            for (int p = 0; p < NP; ++p) Gt[i][p] = ffma2(Gt[i][p], w2[p], fmul2(f2(dsa[i]), a2[p]));
+        }
+        if (l > 0) tmem_ld<TILE>(tlane + (uint32_t)((l - 1) * TILE), spv);  // next step's tile
 #pragma unroll
         for (int i = 0; i < R; ++i) dsa_next[i] = dsa[i];
 

@@ -37,10 +37,10 @@ struct Fwd2Cfg {
   static constexpr int NSTAGE = 2;
   static constexpr int DV = K * N;  // floats per derived vector
   static constexpr size_t OFF_DER = align128((size_t)NSTAGE * RAW_STAGE_BYTES);
-  static constexpr size_t DER_BYTES = (size_t)6 * DV * 4 + (size_t)K * 4;
+  static constexpr size_t DER_BYTES = (size_t)6 * DV * 4 + (size_t)K * 4;  // + beta
   static constexpr size_t OFF_BAR = align128(OFF_DER + DER_BYTES);
   static constexpr size_t SMEM_BYTES = OFF_BAR + 64;
-  static_assert(E % 4 == 0 && 32 % G == 0 && N % R == 0 && (R == 2 || R == 4), "bad tiling");
+  static_assert(E % 4 == 0 && 32 % G == 0 && N % R == 0 && (R == 2 || R % 4 == 0) && R <= G, "bad tiling");
   static_assert(THREADS % 32 == 0, "whole warps");
   static_assert(SMEM_BYTES <= 227 * 1024, "shared memory over budget");
 };
@@ -49,9 +49,12 @@ enum { V_R = 0, V_W = 1, V_K = 2, V_V = 3, V_A = 4, V_B = 5 };
 
 template <int R>
 __device__ __forceinline__ void ld_rows(const float* p, float (&out)[R]) {
-  if constexpr (R == 4) {
-    const float4 v = ld_f4(p);
-    out[0] = v.x; out[1] = v.y; out[2] = v.z; out[3] = v.w;
+  if constexpr (R % 4 == 0) {
+#pragma unroll
+    for (int q = 0; q < R / 4; ++q) {
+      const float4 v = ld_f4(p + 4 * q);
+      out[4 * q] = v.x; out[4 * q + 1] = v.y; out[4 * q + 2] = v.z; out[4 * q + 3] = v.w;
+    }
   } else {
     const float2 v = *reinterpret_cast<const float2*>(p);
     out[0] = v.x; out[1] = v.y;
@@ -117,6 +120,13 @@ __global__ void __launch_bounds__(Fwd2Cfg<TIn, N, R, E, K>::THREADS)
   float* ck_base = args.ckpt ? args.ckpt + ((size_t)head * args.nck * N + row0) * N : nullptr;
   int ck_left = 0;  // steps until the next checkpoint
 
+  // Prologue mapping: thread = (column quad pq, step group pg); each thread
+  // forms the scaled vectors of 4 columns for SG consecutive steps.
+  constexpr int NQ = N / 4;
+  constexpr int SG = K * NQ / Cfg::THREADS;
+  static_assert(SG >= 1 && K % SG == 0 && NQ <= 32 && Cfg::THREADS % NQ == 0, "prologue mapping");
+  const int pq = tid % NQ, pg = tid / NQ;
+
   for (int c = 0; c < nchunks; ++c) {
     const int st = c % Cfg::NSTAGE;
     const int t0 = c * K;
@@ -128,42 +138,47 @@ __global__ void __launch_bounds__(Fwd2Cfg<TIn, N, R, E, K>::THREADS)
     }
     const TIn* rs = raw + st * Cfg::RAW_STAGE;
 
-    // ---- is every decay of this chunk in the scaled form's safe range?
+    // ---- prologue, scaled form: c(l) = w(0)...w(l) of this chunk; k~ = k/c,
+    // b~ = b/c, a^(l+1) = c(l) a(l+1), r^ = c r; beta(l) = b(l) . a(l+1).
+    // Also checks the decays.
     bool unsafe = false;
-    for (int o = tid; o < K * N; o += Cfg::THREADS)
-      if (t0 + o / N < T && !decay_is_safe(raw1(rs + V_W * RV + o))) unsafe = true;
-    const bool direct = __syncthreads_or(unsafe) != 0;
-
-    // ---- prologue: per-step fp32 vectors for this chunk
-    for (int j = tid; j < N; j += Cfg::THREADS) {
-      float cv = 1.f;
-      for (int l = 0; l < K; ++l) {
-        const int o = l * N + j;
-        const bool valid = t0 + l < T;
-        const float w = valid ? raw1(rs + V_W * RV + o) : 1.f;
-        const float k = valid ? raw1(rs + V_K * RV + o) : 0.f;
-        const float b = valid ? raw1(rs + V_B * RV + o) : 0.f;
-        const float r = valid ? raw1(rs + V_R * RV + o) : 0.f;
-        d_v[o] = valid ? raw1(rs + V_V * RV + o) : 0.f;
-        if (direct) {
-          d_k[o] = k; d_b[o] = b; d_r[o] = r; d_c[o] = w;
-          d_a[o] = valid ? raw1(rs + V_A * RV + o) : 0.f;
-        } else {
-          cv = cv * w;
-          const float ic = __frcp_rn(cv);
-          d_k[o] = k * ic; d_b[o] = b * ic; d_r[o] = r * cv; d_c[o] = cv;
-          d_a[o] = (l + 1 < K && t0 + l + 1 < T) ? raw1(rs + V_A * RV + o + N) * cv : 0.f;
+    {
+      const int col = 4 * pq;
+      float4 cp = make_float4(1.f, 1.f, 1.f, 1.f);  // running product before step l
+      for (int l = 0; l < pg * SG; ++l) {
+        if (t0 + l < T) {
+          const float4 w4 = lds4(rs + V_W * RV + l * N + col);
+          cp = make_float4(cp.x * w4.x, cp.y * w4.y, cp.z * w4.z, cp.w * w4.w);
         }
       }
-    }
-    if (!direct) {  // beta(l) = b(l) . a(l+1) inside the chunk
-      for (int l = warp; l < K; l += Cfg::NWARPS) {
-        float s = 0.f;
-        if (l + 1 < K && t0 + l + 1 < T)
-          for (int j = lane; j < N; j += 32)
-            s = fmaf(raw1(rs + V_B * RV + l * N + j), raw1(rs + V_A * RV + (l + 1) * N + j), s);
-        s = group_allreduce<32>(s);
-        if (lane == 0) beta[l] = s;
+#pragma unroll
+      for (int g = 0; g < SG; ++g) {
+        const int l = pg * SG + g;
+        const int o = l * N + col;
+        const bool valid = t0 + l < T;
+        const bool next = l + 1 < K && t0 + l + 1 < T;
+        const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
+        const float4 w4 = valid ? lds4(rs + V_W * RV + o) : make_float4(1.f, 1.f, 1.f, 1.f);
+        const float4 k4 = valid ? lds4(rs + V_K * RV + o) : z;
+        const float4 b4 = valid ? lds4(rs + V_B * RV + o) : z;
+        const float4 r4 = valid ? lds4(rs + V_R * RV + o) : z;
+        const float4 v4 = valid ? lds4(rs + V_V * RV + o) : z;
+        const float4 a4 = next ? lds4(rs + V_A * RV + o + N) : z;
+        if (!decay_is_safe(w4.x) || !decay_is_safe(w4.y) || !decay_is_safe(w4.z) || !decay_is_safe(w4.w))
+          unsafe = true;
+        const float4 c4 = make_float4(cp.x * w4.x, cp.y * w4.y, cp.z * w4.z, cp.w * w4.w);
+        const float4 i4 = make_float4(rcp_approx(c4.x), rcp_approx(c4.y), rcp_approx(c4.z), rcp_approx(c4.w));
+        *reinterpret_cast<float4*>(d_k + o) = make_float4(k4.x * i4.x, k4.y * i4.y, k4.z * i4.z, k4.w * i4.w);
+        *reinterpret_cast<float4*>(d_b + o) = make_float4(b4.x * i4.x, b4.y * i4.y, b4.z * i4.z, b4.w * i4.w);
+        *reinterpret_cast<float4*>(d_r + o) = make_float4(r4.x * c4.x, r4.y * c4.y, r4.z * c4.z, r4.w * c4.w);
+        *reinterpret_cast<float4*>(d_a + o) = make_float4(a4.x * c4.x, a4.y * c4.y, a4.z * c4.z, a4.w * c4.w);
+        *reinterpret_cast<float4*>(d_c + o) = c4;
+        *reinterpret_cast<float4*>(d_v + o) = v4;
+        float pb = b4.x * a4.x + b4.y * a4.y + b4.z * a4.z + b4.w * a4.w;
+#pragma unroll
+        for (int mask = 1; mask < NQ; mask <<= 1) pb += __shfl_xor_sync(0xffffffffu, pb, mask);
+        if (pq == 0) beta[l] = pb;
+        cp = c4;
       }
     }
     // ---- sa at the chunk's first step, directly: S(t0-1) a(t0)
@@ -177,42 +192,47 @@ __global__ void __launch_bounds__(Fwd2Cfg<TIn, N, R, E, K>::THREADS)
       for (int e = 0; e < 4; ++e) a4[e] = raw1(rs + V_A * RV + colq(m) + e);
 #pragma unroll
       for (int i = 0; i < R; ++i) {
-        sa[i] = fmaf(S[i][2 * m].x, a4[0], sa[i]);
-        sa[i] = fmaf(S[i][2 * m].y, a4[1], sa[i]);
-        sa[i] = fmaf(S[i][2 * m + 1].x, a4[2], sa[i]);
-        sa[i] = fmaf(S[i][2 * m + 1].y, a4[3], sa[i]);
+        const float2 p = ffma2(S[i][2 * m + 1], make_float2(a4[2], a4[3]), fmul2(S[i][2 * m], make_float2(a4[0], a4[1])));
+        sa[i] += hsum(p);
       }
     }
 #pragma unroll
     for (int i = 0; i < R; ++i) sa[i] = group_allreduce<G>(sa[i]);
-    __syncthreads();  // the per-step vectors are complete; the raw stage is free
+    const bool direct = __syncthreads_or(unsafe) != 0;
+    if (direct) {
+      // ---- rare: some decay outside the safe range; plain vectors instead
+      for (int o = tid; o < K * N; o += Cfg::THREADS) {
+        const bool valid = t0 + o / N < T;
+        d_k[o] = valid ? raw1(rs + V_K * RV + o) : 0.f;
+        d_b[o] = valid ? raw1(rs + V_B * RV + o) : 0.f;
+        d_r[o] = valid ? raw1(rs + V_R * RV + o) : 0.f;
+        d_a[o] = valid ? raw1(rs + V_A * RV + o) : 0.f;
+        d_c[o] = valid ? raw1(rs + V_W * RV + o) : 1.f;
+      }
+      __syncthreads();
+    }
     if (tid == 0 && c + Cfg::NSTAGE < nchunks) issue(c + Cfg::NSTAGE, st);
 
-    if (!direct) {
-      // ---- K scaled steps
-#pragma unroll
-      for (int l = 0; l < K; ++l) {
-        const int t = t0 + l;
-        if (ck_base && t < T) {
-          if (ck_left == 0) {
-            float* dst = ck_base + (size_t)(t / args.C) * N * N;
-#pragma unroll
-            for (int m = 0; m < Q; ++m) {
-              float4 c4 = make_float4(1.f, 1.f, 1.f, 1.f);
-              if (l > 0) c4 = ld_f4(d_c + (l - 1) * N + colq(m));
-#pragma unroll
-              for (int i = 0; i < R; ++i)
-                *reinterpret_cast<float4*>(dst + (size_t)i * N + colq(m)) =
-                    make_float4(S[i][2 * m].x * c4.x, S[i][2 * m].y * c4.y, S[i][2 * m + 1].x * c4.z,
-                                S[i][2 * m + 1].y * c4.w);
-            }
-            ck_left = args.C;
-          }
-          --ck_left;
+    // steps of this chunk that start with a checkpoint
+    unsigned ckmask = 0;
+    if (ck_base) {
+      for (int l = 0; l < K && t0 + l < T; ++l) {
+        if (ck_left == 0) {
+          ckmask |= 1u << l;
+          ck_left = args.C;
         }
-        float vr[R];
+        --ck_left;
+      }
+    }
+
+    if (!direct) {
+      // ---- K scaled steps, software-pipelined: the cross-lane sum X(l) that
+      // feeds sa(l+1) is started before the rest of step l and the loads of
+      // step l+1, and consumed last.
+      float vr[R];
+      float2 kv[NP], av[NP], bv[NP], rv[NP];
+      auto load_step = [&](int l) {
         ld_rows<R>(d_v + l * N + row0, vr);
-        float2 kv[NP], av[NP], bv[NP], rv[NP];
 #pragma unroll
         for (int m = 0; m < Q; ++m) {
           const float4 k4 = ld_f4(d_k + l * N + colq(m));
@@ -224,32 +244,64 @@ __global__ void __launch_bounds__(Fwd2Cfg<TIn, N, R, E, K>::THREADS)
           bv[2 * m] = make_float2(b4.x, b4.y); bv[2 * m + 1] = make_float2(b4.z, b4.w);
           rv[2 * m] = make_float2(r4.x, r4.y); rv[2 * m + 1] = make_float2(r4.z, r4.w);
         }
-        float X[R], Y[R];
+      };
+      load_step(0);
+#pragma unroll 4
+      for (int l = 0; l < K; ++l) {
+        const int t = t0 + l;
+        if (ckmask & (1u << l)) {
+          float* dst = ck_base + (size_t)(t / args.C) * N * N;
 #pragma unroll
-        for (int i = 0; i < R; ++i) {
-          const float2 vi = f2(vr[i]), si = f2(sa[i]);
-          float2 xa = make_float2(0.f, 0.f), ya = make_float2(0.f, 0.f);
+          for (int m = 0; m < Q; ++m) {
+            const float4 c4 = l > 0 ? ld_f4(d_c + (l - 1) * N + colq(m)) : make_float4(1.f, 1.f, 1.f, 1.f);
 #pragma unroll
-          for (int p = 0; p < NP; ++p) {
-            const float2 u = ffma2(vi, kv[p], S[i][p]);
-            xa = ffma2(u, av[p], xa);
-            S[i][p] = ffma2(si, bv[p], u);
-            ya = ffma2(S[i][p], rv[p], ya);
+            for (int i = 0; i < R; ++i)
+              *reinterpret_cast<float4*>(dst + (size_t)i * N + colq(m)) =
+                  make_float4(S[i][2 * m].x * c4.x, S[i][2 * m].y * c4.y, S[i][2 * m + 1].x * c4.z,
+                              S[i][2 * m + 1].y * c4.w);
           }
-          X[i] = xa.x + xa.y;
-          Y[i] = ya.x + ya.y;
         }
         const float bl = beta[l];
+        // u~ = S~ + v k~ and the partial of X = u~ a^(l+1)
+        float X[R];
 #pragma unroll
         for (int i = 0; i < R; ++i) {
-          X[i] = group_allreduce<G>(X[i]);
-          Y[i] = group_allreduce<G>(Y[i]);
-          sa[i] = fmaf(sa[i], bl, X[i]);
-        }
-        if (y && cg == 0 && t < T) {
 #pragma unroll
-          for (int i = 0; i < R; ++i) st1(y + vbase + (size_t)t * vstep + row0 + i, Y[i]);
+          for (int p = 0; p < NP; ++p) S[i][p] = ffma2(f2(vr[i]), kv[p], S[i][p]);
+          float2 x0 = fmul2(S[i][0], av[0]);
+          float2 x1 = fmul2(S[i][1], av[1]);
+#pragma unroll
+          for (int p = 2; p < NP; p += 2) {
+            x0 = ffma2(S[i][p], av[p], x0);
+            x1 = ffma2(S[i][p + 1], av[p + 1], x1);
+          }
+          X[i] = hsum(fadd2(x0, x1));
         }
+        // start the cross-lane sums of X (needed only at the end of the step)
+#pragma unroll
+        for (int o = 1; o < G; o <<= 1)
+#pragma unroll
+          for (int i = 0; i < R; ++i) X[i] += __shfl_xor_sync(0xffffffffu, X[i], o);
+        // S~ = u~ + sa b~ and y partials
+        float Y[R];
+#pragma unroll
+        for (int i = 0; i < R; ++i) {
+#pragma unroll
+          for (int p = 0; p < NP; ++p) S[i][p] = ffma2(f2(sa[i]), bv[p], S[i][p]);
+          float2 y0 = fmul2(S[i][0], rv[0]);
+          float2 y1 = fmul2(S[i][1], rv[1]);
+#pragma unroll
+          for (int p = 2; p < NP; p += 2) {
+            y0 = ffma2(S[i][p], rv[p], y0);
+            y1 = ffma2(S[i][p + 1], rv[p + 1], y1);
+          }
+          Y[i] = hsum(fadd2(y0, y1));
+        }
+        if (l + 1 < K) load_step(l + 1);
+        const float yv = rowsum_scatter<G, R>(Y, cg);
+        if (y && t < T && row_writer<G, R>(cg)) st1(y + vbase + (size_t)t * vstep + row0 + row_of_lane<G, R>(cg), yv);
+#pragma unroll
+        for (int i = 0; i < R; ++i) sa[i] = fmaf(sa[i], bl, X[i]);
       }
       // ---- renormalise: S = S~ diag(c(last step))
 #pragma unroll
@@ -265,18 +317,14 @@ __global__ void __launch_bounds__(Fwd2Cfg<TIn, N, R, E, K>::THREADS)
       // ---- K direct-form steps (any decay): sa = S a; S = S w + v k + sa b; y = S r
       for (int l = 0; l < K; ++l) {
         const int t = t0 + l;
-        if (ck_base && t < T) {
-          if (ck_left == 0) {
-            float* dst = ck_base + (size_t)(t / args.C) * N * N;
+        if (ckmask & (1u << l)) {
+          float* dst = ck_base + (size_t)(t / args.C) * N * N;
 #pragma unroll
-            for (int m = 0; m < Q; ++m)
+          for (int m = 0; m < Q; ++m)
 #pragma unroll
-              for (int i = 0; i < R; ++i)
-                *reinterpret_cast<float4*>(dst + (size_t)i * N + colq(m)) =
-                    make_float4(S[i][2 * m].x, S[i][2 * m].y, S[i][2 * m + 1].x, S[i][2 * m + 1].y);
-            ck_left = args.C;
-          }
-          --ck_left;
+            for (int i = 0; i < R; ++i)
+              *reinterpret_cast<float4*>(dst + (size_t)i * N + colq(m)) =
+                  make_float4(S[i][2 * m].x, S[i][2 * m].y, S[i][2 * m + 1].x, S[i][2 * m + 1].y);
         }
         float vr[R];
         ld_rows<R>(d_v + l * N + row0, vr);
@@ -287,11 +335,8 @@ __global__ void __launch_bounds__(Fwd2Cfg<TIn, N, R, E, K>::THREADS)
           for (int m = 0; m < Q; ++m) {
             const float4 a4 = ld_f4(d_a + l * N + colq(m));
 #pragma unroll
-            for (int i = 0; i < R; ++i) {
-              float2 p = fmul2(S[i][2 * m], make_float2(a4.x, a4.y));
-              p = ffma2(S[i][2 * m + 1], make_float2(a4.z, a4.w), p);
-              sa[i] += p.x + p.y;
-            }
+            for (int i = 0; i < R; ++i)
+              sa[i] += hsum(ffma2(S[i][2 * m + 1], make_float2(a4.z, a4.w), fmul2(S[i][2 * m], make_float2(a4.x, a4.y))));
           }
 #pragma unroll
           for (int i = 0; i < R; ++i) sa[i] = group_allreduce<G>(sa[i]);
@@ -315,17 +360,12 @@ __global__ void __launch_bounds__(Fwd2Cfg<TIn, N, R, E, K>::THREADS)
               const float2 r2 = h ? make_float2(r4.z, r4.w) : make_float2(r4.x, r4.y);
               float2& s2 = S[i][2 * m + h];
               s2 = ffma2(f2(sa[i]), b2, ffma2(s2, w2, fmul2(k2, f2(vr[i]))));
-              const float2 yr = fmul2(s2, r2);
-              Y[i] += yr.x + yr.y;
+              Y[i] += hsum(fmul2(s2, r2));
             }
           }
         }
-#pragma unroll
-        for (int i = 0; i < R; ++i) Y[i] = group_allreduce<G>(Y[i]);
-        if (y && cg == 0 && t < T) {
-#pragma unroll
-          for (int i = 0; i < R; ++i) st1(y + vbase + (size_t)t * vstep + row0 + i, Y[i]);
-        }
+        const float yv = rowsum_scatter<G, R>(Y, cg);
+        if (y && t < T && row_writer<G, R>(cg)) st1(y + vbase + (size_t)t * vstep + row0 + row_of_lane<G, R>(cg), yv);
       }
     }
   }

@@ -35,8 +35,63 @@ __device__ __forceinline__ bool decay_is_safe(float w) { return w >= kWMin && w 
 
 __device__ __forceinline__ float2 f2(float s) { return make_float2(s, s); }
 
+// Element-pair arithmetic: packed fp32x2 FMA (fma.rn.f32x2), one
+// instruction for two multiply-adds; the kernels are issue-bound, so fewer
+// instructions beat the packed form's longer issue interval.
 __device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 c) { return __ffma2_rn(a, b, c); }
 __device__ __forceinline__ float2 fmul2(float2 a, float2 b) { return __fmul2_rn(a, b); }
+__device__ __forceinline__ float2 fadd2(float2 a, float2 b) { return __fadd2_rn(a, b); }
+__device__ __forceinline__ float hsum(float2 a) { return a.x + a.y; }
+
+// Hardware reciprocal approximation (PTX rcp.approx.f32, at most 1 ulp off).
+// Used for 1/c: a scale factor whose exact rounding does not matter, since
+// the state is multiplied back by c itself.
+__device__ __forceinline__ float rcp_approx(float x) {
+  float r;
+  asm("rcp.approx.f32 %0, %1;" : "=f"(r) : "f"(x));
+  return r;
+}
+
+// Sum each of R per-row values over the G lanes of a row group
+// (reduce-scatter: the set halves on each of the high lane bits, then the
+// last value is summed over the remaining bits). Returns the total of row
+// row_of_lane<G, R>(cg) of the caller's row group.
+template <int G, int R>
+__device__ __forceinline__ float rowsum_scatter(float (&v)[R], int cg) {
+  int n = R;
+#pragma unroll
+  for (int mask = G / 2; mask >= 1; mask >>= 1) {
+    if (n > 1) {
+      const int h = n / 2;
+      const bool upper = (cg & mask) != 0;
+#pragma unroll
+      for (int i = 0; i < R / 2; ++i) {
+        if (i < h) {
+          const float send = upper ? v[i] : v[h + i];
+          const float keep = upper ? v[h + i] : v[i];
+          v[i] = keep + __shfl_xor_sync(0xffffffffu, send, mask);
+        }
+      }
+      n = h;
+    } else {
+      v[0] += __shfl_xor_sync(0xffffffffu, v[0], mask);
+    }
+  }
+  return v[0];
+}
+
+// Row (within the row group) whose total rowsum_scatter leaves in lane cg,
+// and whether this lane is the first of the copies holding it.
+template <int G, int R>
+__device__ __forceinline__ int row_of_lane(int cg) {
+  constexpr int copies = G / R;
+  return cg / copies;
+}
+template <int G, int R>
+__device__ __forceinline__ bool row_writer(int cg) {
+  constexpr int copies = G / R;
+  return (cg % copies) == 0;
+}
 
 __device__ __forceinline__ float4 ld_f4(const float* p) { return *reinterpret_cast<const float4*>(p); }
 
