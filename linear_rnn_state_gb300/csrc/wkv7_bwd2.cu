@@ -62,7 +62,7 @@ struct Bwd2Cfg {
   static constexpr size_t OFF_DER = NSTAGE * STAGE_BYTES;
   static constexpr size_t OFF_SC = OFF_DER + (size_t)NDER * DV * 4;  // beta, rho partials
   static constexpr int NSUM = 5;                                       // dr, dk, db, dw, da
-  static constexpr size_t OFF_COL = a128(OFF_SC + (size_t)4 * KS * 4);
+  static constexpr size_t OFF_COL = a128(OFF_SC + (size_t)2 * KS * 4);
   static constexpr size_t COL_BYTES = (size_t)KS * NWARPS * NSUM * N * 4;
   static constexpr size_t OFF_BAR = OFF_COL + COL_BYTES;
   static constexpr size_t SMEM_BYTES = OFF_BAR + 64;
@@ -133,7 +133,7 @@ __global__ void __launch_bounds__(Bwd2Cfg<TIn, N, R, E, KS>::THREADS, 1)
   float* d_dy = d_v + DV;
   float* d_sa = d_dy + DV;
   float* beta = reinterpret_cast<float*>(smem + Cfg::OFF_SC);
-  float* rho = beta + 2 * KS;
+  float* rho = beta + KS;
   float* colbuf = reinterpret_cast<float*>(smem + Cfg::OFF_COL);
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + Cfg::OFF_BAR);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + Cfg::OFF_BAR + 32);
@@ -207,11 +207,12 @@ __global__ void __launch_bounds__(Bwd2Cfg<TIn, N, R, E, KS>::THREADS, 1)
       pre_valid = w_next(pre);
     }
 
-  // Prologue split: SPLIT threads per column, each scanning KS / SPLIT steps.
-  constexpr int SPLIT = Cfg::THREADS / N >= 2 ? 2 : 1;
-  constexpr int LS = KS / SPLIT;
-  constexpr int BPN = N > 32 ? N / 32 : 1;  // partial dot products per step
-  const int pj = tid % N, ppart = tid / N;
+  // Prologue mapping: thread = (column quad pq, step group pg); each thread
+  // forms the per-step vectors of 4 columns for SG consecutive steps.
+  constexpr int NQ = N / 4;
+  constexpr int SG = KS * NQ / Cfg::THREADS;
+  static_assert(SG >= 1 && KS % SG == 0 && NQ <= 32 && Cfg::THREADS % NQ == 0, "prologue mapping");
+  const int pq = tid % NQ, pg = tid / NQ;
 
   float2 Gt[R][NP];
 #pragma unroll
@@ -249,45 +250,59 @@ __global__ void __launch_bounds__(Bwd2Cfg<TIn, N, R, E, KS>::THREADS, 1)
     }
 
     // ---- prologue, scaled form (identity steps beyond len): c(l) = w(0)..w(l)
-    // of this window; k~ = k/c, b~ = b/c, a^ = c(l-1) a, r^ = c r, 1/c; beta
-    // and rho as per-warp partial dot products. Also checks the decays.
+    // of this window; k~ = k/c, b~ = b/c, a^ = c(l-1) a, r^ = c r, 1/c;
+    // beta(l) = b(l) . a(l+1) and rho(l) = r(l) . b(l). Also checks the decays.
     bool unsafe = false;
-    if (ppart < SPLIT) {
-      const int l0 = ppart * LS;
-      float cv = 1.f;
-      for (int l = 0; l < l0; ++l)
-        if (l < len) cv *= raw1(rs + V_W * RV + l * N + pj);
-#pragma unroll 4
-      for (int l = l0; l < l0 + LS; ++l) {
-        const int o = l * N + pj;
-        const bool valid = l < len;
-        const float w = valid ? raw1(rs + V_W * RV + o) : 1.f;
-        if (!decay_is_safe(w)) unsafe = true;
-        const float b = valid ? raw1(rs + V_B * RV + o) : 0.f;
-        const float r = valid ? raw1(rs + V_R * RV + o) : 0.f;
-        const float cp = cv;
-        cv *= w;
-        const float ic = rcp_approx(cv);
-        d_k[o] = valid ? raw1(rs + V_K * RV + o) * ic : 0.f;
-        d_b[o] = b * ic;
-        d_a[o] = valid ? raw1(rs + V_A * RV + o) * cp : 0.f;
-        d_r[o] = r * cv;
-        d_c[o] = cv;
-        d_ic[o] = ic;
-        d_w[o] = w;
-        d_v[o] = valid ? raw1(rs + V_V * RV + o) : 0.f;
-        d_dy[o] = valid ? raw1(rs + V_DY * RV + o) : 0.f;
-        const float an = l + 1 < len ? raw1(rs + V_A * RV + o + N) : 0.f;
-        float pb = b * an, pr = r * b;
+    {
+      const int col = 4 * pq;
+      const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
+      float4 cp = make_float4(1.f, 1.f, 1.f, 1.f);  // running product before step l
 #pragma unroll
-        for (int mask = 1; mask < (N < 32 ? N : 32); mask <<= 1) {
+      for (int l = 0; l < KS - SG; ++l) {
+        if (l < pg * SG && l < len) {
+          const float4 w4 = lds4(rs + V_W * RV + l * N + col);
+          cp = make_float4(cp.x * w4.x, cp.y * w4.y, cp.z * w4.z, cp.w * w4.w);
+        }
+      }
+#pragma unroll
+      for (int g = 0; g < SG; ++g) {
+        const int l = pg * SG + g;
+        const int o = l * N + col;
+        const bool valid = l < len;
+        const bool next = l + 1 < len;
+        const float4 w4 = valid ? lds4(rs + V_W * RV + o) : make_float4(1.f, 1.f, 1.f, 1.f);
+        const float4 k4 = valid ? lds4(rs + V_K * RV + o) : z;
+        const float4 b4 = valid ? lds4(rs + V_B * RV + o) : z;
+        const float4 r4 = valid ? lds4(rs + V_R * RV + o) : z;
+        const float4 a4 = valid ? lds4(rs + V_A * RV + o) : z;
+        const float4 v4 = valid ? lds4(rs + V_V * RV + o) : z;
+        const float4 y4 = valid ? lds4(rs + V_DY * RV + o) : z;
+        const float4 an = next ? lds4(rs + V_A * RV + o + N) : z;
+        if (!decay_is_safe(w4.x) || !decay_is_safe(w4.y) || !decay_is_safe(w4.z) || !decay_is_safe(w4.w))
+          unsafe = true;
+        const float4 c4 = make_float4(cp.x * w4.x, cp.y * w4.y, cp.z * w4.z, cp.w * w4.w);
+        const float4 i4 = make_float4(rcp_approx(c4.x), rcp_approx(c4.y), rcp_approx(c4.z), rcp_approx(c4.w));
+        *reinterpret_cast<float4*>(d_k + o) = make_float4(k4.x * i4.x, k4.y * i4.y, k4.z * i4.z, k4.w * i4.w);
+        *reinterpret_cast<float4*>(d_b + o) = make_float4(b4.x * i4.x, b4.y * i4.y, b4.z * i4.z, b4.w * i4.w);
+        *reinterpret_cast<float4*>(d_a + o) = make_float4(a4.x * cp.x, a4.y * cp.y, a4.z * cp.z, a4.w * cp.w);
+        *reinterpret_cast<float4*>(d_r + o) = make_float4(r4.x * c4.x, r4.y * c4.y, r4.z * c4.z, r4.w * c4.w);
+        *reinterpret_cast<float4*>(d_c + o) = c4;
+        *reinterpret_cast<float4*>(d_ic + o) = i4;
+        *reinterpret_cast<float4*>(d_w + o) = w4;
+        *reinterpret_cast<float4*>(d_v + o) = v4;
+        *reinterpret_cast<float4*>(d_dy + o) = y4;
+        float pb = b4.x * an.x + b4.y * an.y + b4.z * an.z + b4.w * an.w;
+        float pr = r4.x * b4.x + r4.y * b4.y + r4.z * b4.z + r4.w * b4.w;
+#pragma unroll
+        for (int mask = 1; mask < NQ; mask <<= 1) {
           pb += __shfl_xor_sync(0xffffffffu, pb, mask);
           pr += __shfl_xor_sync(0xffffffffu, pr, mask);
         }
-        if ((lane & ((N < 32 ? N : 32) - 1)) == 0) {
-          beta[(pj / 32) * KS + l] = pb;
-          rho[(pj / 32) * KS + l] = pr;
+        if (pq == 0) {
+          beta[l] = pb;
+          rho[l] = pr;
         }
+        cp = c4;
       }
     }
     // sa at the window's first step, directly
@@ -362,9 +377,7 @@ __global__ void __launch_bounds__(Bwd2Cfg<TIn, N, R, E, KS>::THREADS, 1)
           bv[2 * m] = lo2(b4); bv[2 * m + 1] = hi2(b4);
           av[2 * m] = lo2(a4); av[2 * m + 1] = hi2(a4);
         }
-        float bl = beta[l];
-#pragma unroll
-        for (int q = 1; q < BPN; ++q) bl += beta[q * KS + l];
+        const float bl = beta[l];
         // u~ = S~ + v k~
 #pragma unroll
         for (int i = 0; i < R; ++i)
@@ -540,23 +553,25 @@ __global__ void __launch_bounds__(Bwd2Cfg<TIn, N, R, E, KS>::THREADS, 1)
         for (int i = 0; i < R; ++i) {
           float2 d0 = fmul2(Gt[i][0], k2[0]), d1 = fmul2(Gt[i][1], k2[1]);
           float2 z0 = fmul2(Gt[i][0], bz[0]), z1 = fmul2(Gt[i][1], bz[1]);
-          float2 e0 = fmul2(Gt[i][0], bd[0]), e1 = fmul2(Gt[i][1], bd[1]);
 #pragma unroll
           for (int p = 2; p < NP; p += 2) {
             d0 = ffma2(Gt[i][p], k2[p], d0); d1 = ffma2(Gt[i][p + 1], k2[p + 1], d1);
             z0 = ffma2(Gt[i][p], bz[p], z0); z1 = ffma2(Gt[i][p + 1], bz[p + 1], z1);
-            e0 = ffma2(Gt[i][p], bd[p], e0); e1 = ffma2(Gt[i][p + 1], bd[p + 1], e1);
           }
           pdv[i] = hsum(fadd2(d0, d1));
           pz[i] = hsum(fadd2(z0, z1));
-          pds[i] = hsum(fadd2(e0, e1));
-        }
-        float bl = beta[l], rl = rho[l];
+          pds[i] = 0.f;
+          if (use_d) {
+            float2 e0 = fmul2(Gt[i][0], bd[0]), e1 = fmul2(Gt[i][1], bd[1]);
 #pragma unroll
-        for (int q = 1; q < BPN; ++q) {
-          bl += beta[q * KS + l];
-          rl += rho[q * KS + l];
+            for (int p = 2; p < NP; p += 2) {
+              e0 = ffma2(Gt[i][p], bd[p], e0);
+              e1 = ffma2(Gt[i][p + 1], bd[p + 1], e1);
+            }
+            pds[i] = hsum(fadd2(e0, e1));
+          }
         }
+        const float bl = beta[l], rl = rho[l];
         float dsa[R];
 #pragma unroll
         for (int i = 0; i < R; ++i) {
@@ -627,29 +642,33 @@ __global__ void __launch_bounds__(Bwd2Cfg<TIn, N, R, E, KS>::THREADS, 1)
       }
       __syncthreads();  // column partials of every warp are in shared memory
 
-      // ---- cross-warp sums, scaled to true values, written out
-      for (int idx = tid; idx < len * NSUM * (N / 4); idx += Cfg::THREADS) {
-        const int q4 = idx % (N / 4);
-        const int rest = idx / (N / 4);
-        const int s = rest % NSUM, l = rest / NSUM;
-        const int col = 4 * q4;
-        float4 acc = ld_f4(colbuf + ((size_t)(l * NWARPS + 0) * NSUM + s) * N + col);
-#pragma unroll
-        for (int wv = 1; wv < NWARPS; ++wv) {
-          const float4 x = ld_f4(colbuf + ((size_t)(l * NWARPS + wv) * NSUM + s) * N + col);
-          acc.x += x.x; acc.y += x.y; acc.z += x.z; acc.w += x.w;
-        }
+      // ---- cross-warp sums, scaled to true values, written out: one item is
+      // a (step, column quad) with all five sums
+      for (int idx = tid; idx < len * (N / 4); idx += Cfg::THREADS) {
+        const int l = idx / (N / 4), col = 4 * (idx % (N / 4));
         const float4 cl = ld_f4(d_c + l * N + col);
         const float4 il = ld_f4(d_ic + l * N + col);
         const float4 cp = l > 0 ? ld_f4(d_c + (l - 1) * N + col) : make_float4(1.f, 1.f, 1.f, 1.f);
-        float4 sc;
-        if (s == 0) sc = cl;
-        else if (s == 1 || s == 2) sc = il;
-        else if (s == 3) sc = make_float4(cp.x * il.x, cp.y * il.y, cp.z * il.z, cp.w * il.w);
-        else sc = cp;
-        float* out = s == 0 ? args.dr : s == 1 ? args.dk : s == 2 ? args.db : s == 3 ? args.dw : args.da;
-        *reinterpret_cast<float4*>(out + vbase + (size_t)(start + l) * vstep + col) =
-            make_float4(acc.x * sc.x, acc.y * sc.y, acc.z * sc.z, acc.w * sc.w);
+        float4 acc[NSUM];
+#pragma unroll
+        for (int s = 0; s < NSUM; ++s) acc[s] = ld_f4(colbuf + ((size_t)(l * NWARPS + 0) * NSUM + s) * N + col);
+#pragma unroll
+        for (int wv = 1; wv < NWARPS; ++wv)
+#pragma unroll
+          for (int s = 0; s < NSUM; ++s) {
+            const float4 x = ld_f4(colbuf + ((size_t)(l * NWARPS + wv) * NSUM + s) * N + col);
+            acc[s].x += x.x; acc[s].y += x.y; acc[s].z += x.z; acc[s].w += x.w;
+          }
+        const size_t go = vbase + (size_t)(start + l) * vstep + col;
+        const float4 cw = make_float4(cp.x * il.x, cp.y * il.y, cp.z * il.z, cp.w * il.w);
+        auto put = [&](float* out, const float4& a, const float4& sc) {
+          *reinterpret_cast<float4*>(out + go) = make_float4(a.x * sc.x, a.y * sc.y, a.z * sc.z, a.w * sc.w);
+        };
+        put(args.dr, acc[0], cl);
+        put(args.dk, acc[1], il);
+        put(args.db, acc[2], il);
+        put(args.dw, acc[3], cw);
+        put(args.da, acc[4], cp);
       }
     }
     if (!w_next(cur)) break;

@@ -145,8 +145,9 @@ __global__ void __launch_bounds__(Fwd2Cfg<TIn, N, R, E, K>::THREADS)
     {
       const int col = 4 * pq;
       float4 cp = make_float4(1.f, 1.f, 1.f, 1.f);  // running product before step l
-      for (int l = 0; l < pg * SG; ++l) {
-        if (t0 + l < T) {
+#pragma unroll
+      for (int l = 0; l < K - SG; ++l) {
+        if (l < pg * SG && t0 + l < T) {
           const float4 w4 = lds4(rs + V_W * RV + l * N + col);
           cp = make_float4(cp.x * w4.x, cp.y * w4.y, cp.z * w4.z, cp.w * w4.w);
         }
@@ -232,13 +233,14 @@ __global__ void __launch_bounds__(Fwd2Cfg<TIn, N, R, E, K>::THREADS)
       float vr[R];
       float2 kv[NP], av[NP], bv[NP], rv[NP];
       auto load_step = [&](int l) {
-        ld_rows<R>(d_v + l * N + row0, vr);
+#pragma unroll
+        for (int i = 0; i < R; ++i) vr[i] = lds32(d_v + l * N + row0 + i);
 #pragma unroll
         for (int m = 0; m < Q; ++m) {
-          const float4 k4 = ld_f4(d_k + l * N + colq(m));
-          const float4 a4 = ld_f4(d_a + l * N + colq(m));
-          const float4 b4 = ld_f4(d_b + l * N + colq(m));
-          const float4 r4 = ld_f4(d_r + l * N + colq(m));
+          const float4 k4 = lds32x4(d_k + l * N + colq(m));
+          const float4 a4 = lds32x4(d_a + l * N + colq(m));
+          const float4 b4 = lds32x4(d_b + l * N + colq(m));
+          const float4 r4 = lds32x4(d_r + l * N + colq(m));
           kv[2 * m] = make_float2(k4.x, k4.y); kv[2 * m + 1] = make_float2(k4.z, k4.w);
           av[2 * m] = make_float2(a4.x, a4.y); av[2 * m + 1] = make_float2(a4.z, a4.w);
           bv[2 * m] = make_float2(b4.x, b4.y); bv[2 * m + 1] = make_float2(b4.z, b4.w);
