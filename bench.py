@@ -45,6 +45,27 @@ def _dist():
     return world, rank, local
 
 
+def shard_seed(rank: int) -> int:
+    """Each rank scans its own batch: the generator is seeded with the rank."""
+    return rank
+
+
+def reduce_max(value: float, dist, device=None) -> float:
+    """Slowest rank's value (max over ranks); identity on one process."""
+    if dist is None:
+        return value
+    import torch
+
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return t.item()
+
+
+def aggregate_tokens_per_s(world: int, B: int, T: int, ms_per_step: float) -> float:
+    """Tokens of all ranks (each B*T per step) per second of the slowest rank."""
+    return world * B * T / (ms_per_step * 1e-3)
+
+
 def _init_pg(world, backend):
     import torch.distributed as dist
 
@@ -191,7 +212,7 @@ def run_gpu(args):
     bf16 = wl.storage == "bf16"
     C = wkv7.wkv7_default_ckpt_every(N, bf16)
     names = ("r", "w", "k", "v", "a", "b", "dy")
-    d = inputs.generate(B, T, H, N, wl.storage, wl.s_init_std, seed=rank)
+    d = inputs.generate(B, T, H, N, wl.storage, wl.s_init_std, seed=shard_seed(rank))
 
     def to_dev(x):
         t = torch.from_numpy(x)
@@ -246,11 +267,7 @@ def run_gpu(args):
     total_ms = start.elapsed_time(end)
     fwd_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in events)
     bwd_ms = statistics.mean(e[1].elapsed_time(e[2]) for e in events)
-    ms = total_ms / args.steps
-    if dist:
-        tt = torch.tensor([ms], device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        ms = tt.item()
+    ms = reduce_max(total_ms / args.steps, dist, dev)
 
     if args.no_e2e:
         e2e_ms = None
@@ -294,11 +311,7 @@ def _e2e(args, d, names, t_in, grads, y, dS, bf16, tdt, step, stream, dist, dev)
         e2e_step()
     e1.record(stream)
     torch.cuda.synchronize()
-    e2e_ms = e0.elapsed_time(e1) / e2e_steps
-    if dist:
-        tt = torch.tensor([e2e_ms], device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        e2e_ms = tt.item()
+    e2e_ms = reduce_max(e0.elapsed_time(e1) / e2e_steps, dist, dev)
     return e2e_ms, h2d, d2h
 
 
@@ -312,7 +325,7 @@ def _report(args, wl, world, B, T, H, N, C, bf16, ms, fwd_ms, bwd_ms, e2e, ckpt,
     peak_flops = sms * FP32_LANES_PER_SM * 2 * peaks["sm_max_mhz"] * 1e6
     achieved = b_flop * BTH / (bwd_ms * 1e-3)
     t_roof = max((f_flop + b_flop) * BTH / peak_flops, (f_bytes + b_bytes) * BTH / (peaks["hbm_gbs"] * 1e9))
-    value = world * B * T / (ms * 1e-3)
+    value = aggregate_tokens_per_s(world, B, T, ms)
     cpu_v, cpu_cores, cpu_P, cpu_dt = cpu_baseline_sample(wl, d, B * H) if not args.no_cpu_baseline and T == wl.T \
         else (None, 0, 0, 0.0)
     line = {
@@ -328,7 +341,7 @@ def _report(args, wl, world, B, T, H, N, C, bf16, ms, fwd_ms, bwd_ms, e2e, ckpt,
                      "peak_source": f"{sms} SMs x {FP32_LANES_PER_SM} FP32 lanes x 2 x {peaks['sm_max_mhz']:.0f} MHz",
                      "hbm_gbs_achieved": b_bytes * BTH / (bwd_ms * 1e-3) / 1e9, "hbm_peak_gbs": peaks["hbm_gbs"]},
         "e2e": None if e2e is None else {
-            "value": world * B * T / (e2e[0] * 1e-3), "unit": "tokens/s", "h2d_bytes_per_step": e2e[1],
+            "value": aggregate_tokens_per_s(world, B, T, e2e[0]), "unit": "tokens/s", "h2d_bytes_per_step": e2e[1],
             "d2h_bytes_per_step": e2e[2]},
         "gpu_launches": 2 * args.steps,
         "clocks": clocks.summary(),

@@ -1,0 +1,74 @@
+"""The multi-GPU benchmark path, run as two gloo ranks on the CPU.
+
+(b, h) heads are independent, so ranks shard by batch with no data-path
+collective: each rank draws its own inputs (seed = rank), the step time is
+the maximum over ranks and throughput counts the tokens of every rank. The
+reference arm runs on rank 0 only.
+"""
+import os
+import subprocess
+import sys
+
+import numpy as np
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _worker(rank, world, port, q):
+    import torch.distributed as dist
+
+    sys.path.insert(0, ROOT)
+    import bench
+    from linear_rnn_state_gb300 import inputs
+
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port), RANK=str(rank), WORLD_SIZE=str(world))
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    try:
+        local_ms = 10.0 + 5.0 * rank  # rank 1 is the slow one
+        ms = bench.reduce_max(local_ms, dist)
+        value = bench.aggregate_tokens_per_s(world, 4, 4096, ms)
+        d = inputs.generate(1, 8, 2, 16, "f32", seed=bench.shard_seed(rank))
+        q.put((rank, ms, value, float(d["r"].sum())))
+    finally:
+        dist.destroy_process_group()
+
+
+def test_two_gloo_ranks_agree_on_the_slowest_rank():
+    import multiprocessing as mp
+
+    import socket
+
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        port = s.getsockname()[1]
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    procs = [ctx.Process(target=_worker, args=(r, 2, port, q)) for r in range(2)]
+    for p in procs:
+        p.start()
+    for p in procs:
+        p.join(timeout=120)
+        assert p.exitcode == 0
+    res = sorted(q.get(timeout=10) for _ in range(2))
+    (_, ms0, v0, s0), (_, ms1, v1, s1) = res
+    assert ms0 == ms1 == 15.0
+    assert v0 == v1 == pytest.approx(2 * 4 * 4096 / 15e-3)
+    assert s0 != s1  # each rank scans its own batch
+
+
+def test_reference_arm_runs_on_rank_zero_only():
+    env = dict(os.environ, RANK="1", WORLD_SIZE="2", LOCAL_RANK="1")
+    out = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference", "--steps", "1",
+                          "--warmup", "0"], env=env, capture_output=True, text=True, timeout=120)
+    assert out.returncode == 0
+    assert out.stdout.strip() == ""
+
+
+def test_single_process_reduction_is_identity():
+    sys.path.insert(0, ROOT)
+    import bench
+
+    assert bench.reduce_max(3.5, None) == 3.5
+    assert bench.aggregate_tokens_per_s(1, 4, 4096, 2.0) == pytest.approx(4 * 4096 / 2e-3)
+    assert np.isfinite(bench.aggregate_tokens_per_s(8, 4, 4096, 1.0))
