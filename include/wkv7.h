@@ -123,6 +123,32 @@ int wkv7_status(void* stream);
 /* Message of the calling thread's last failed call ("" if none). */
 const char* wkv7_last_error(void);
 
+/*
+ * Backward-through-time, fp32 inputs, with no device allocation. This entry
+ * point has no counterpart on the pages; it serves callers that cannot
+ * allocate device memory (a stream being captured into a graph that must not
+ * contain allocation nodes, or a framework that owns every device byte through
+ * its own allocator). It behaves like wkv7_backward with ckpt = NULL and the
+ * default interval (16 steps), but its own forward writes the checkpoints into
+ * a fixed 64 MiB scratch array of the library, held on every GPU that loads the
+ * library until the process exits, instead of a cudaMallocAsync workspace.
+ *   Limit: B*H*ceil(T/16)*N*N*4 bytes of checkpoints must fit in 64 MiB
+ *   (e.g. B*H = 16 heads of T = 4096, N = 64); a larger problem returns
+ *   WKV7_ERR_INVALID before anything is enqueued.
+ *   The first call on a device looks the scratch array up
+ *   (cudaGetSymbolAddress); make that first call before any stream capture.
+ *   All calls share the one array and it keeps the last call's contents:
+ *   every checkpoint a call reads is written by that call first, so nothing
+ *   needs clearing, but calls whose work overlaps on the GPU (other streams,
+ *   other threads) race on it; serialize them.
+ * Arguments, layouts and status codes as wkv7_backward; no cudaMalloc,
+ * cudaFree or allocating library call is made.
+ */
+int wkv7_backward_noalloc(const float* r, const float* w, const float* k, const float* v, const float* a,
+                          const float* b, const float* dy, const float* s_init, float* dr, float* dw, float* dk,
+                          float* dv, float* da, float* db, float* dS_init, int B, int T, int H, int N,
+                          void* stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -309,6 +309,117 @@ int backward_impl(bool bf16, const void* const in[7], const float* s_init, const
 }
 
 }  // namespace
+
+// ======================================== backward without allocation ===
+//
+// For callers that cannot allocate device memory: code running inside a
+// CUDA graph being captured or replayed where allocation nodes are not
+// allowed, or a host framework that owns all device memory through its own
+// allocator and forbids library calls to cudaMalloc. The checkpoints of the
+// backward's own forward pass go to a fixed scratch array of this library
+// instead of a stream-ordered workspace.
+
+namespace {
+
+constexpr size_t kNoAllocScratchBytes = size_t(64) << 20;  // 64 MiB
+
+// Every GPU that loads the library holds this array until the process exits.
+// Host code must not pass the name itself to a kernel: in host code it is a
+// stand-in, not a device address. The device address comes from
+// cudaGetSymbolAddress, once per device (noalloc_scratch below).
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
+
+std::mutex g_noalloc_mu;
+float* g_noalloc_ptr[kMaxDevices];
+
+// Device address of the scratch array on the current device; looked up on
+// the first call on each device.
+int noalloc_scratch(float** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return fail_cuda(e, "cudaGetDevice");
+  if (dev < 0 || dev >= kMaxDevices) return fail(WKV7_ERR_CUDA, "device ordinal %d out of range", dev);
+  std::lock_guard<std::mutex> lock(g_noalloc_mu);
+  if (!g_noalloc_ptr[dev]) {
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+    if (e != cudaSuccess) return fail_cuda(e, "cudaGetSymbolAddress(no-allocation scratch)");
+    g_noalloc_ptr[dev] = static_cast<float*>(p);
+  }
+  *out = g_noalloc_ptr[dev];
+  return WKV7_OK;
+}
+
+int backward_noalloc_impl(const float* const in[7], const float* s_init, float* const grads[6], float* dS_init,
+                          int B, int T, int H, int N, cudaStream_t stream) {
+  int rc = check_dims(B, T, H, N);
+  if (rc) return rc;
+  const size_t vec = (size_t)B * T * H * N * 4;
+  const size_t st = (size_t)B * H * N * N * 4;
+  const Span ins[8] = {{in[0], vec, "r"}, {in[1], vec, "w"}, {in[2], vec, "k"}, {in[3], vec, "v"},
+                       {in[4], vec, "a"}, {in[5], vec, "b"}, {in[6], vec, "dy"}, {s_init, st, "s_init"}};
+  const Span outs[7] = {{grads[0], vec, "dr"}, {grads[1], vec, "dw"}, {grads[2], vec, "dk"},
+                        {grads[3], vec, "dv"}, {grads[4], vec, "da"}, {grads[5], vec, "db"},
+                        {dS_init, st, "dS_init"}};
+  if ((size_t)B * H == 0) return WKV7_OK;
+  if (T == 0) {
+    rc = check_spans(ins + 7, 1, outs + 6, 1, 0, 0);
+    if (rc) return rc;
+    if (!dS_init) return WKV7_OK;
+    cudaError_t e = cudaMemsetAsync(dS_init, 0, st, stream);
+    return e == cudaSuccess ? WKV7_OK : fail_cuda(e, "empty backward");
+  }
+  rc = check_spans(ins, 8, outs, 7, 7, 6);
+  if (rc) return rc;
+  const int C = bwd2_steps_per_window(N, false);
+  const size_t bytes = ckpt_bytes(B, T, H, N, C);
+  if (bytes > kNoAllocScratchBytes)
+    return fail(WKV7_ERR_INVALID,
+                "wkv7_backward_noalloc: this problem needs %zu bytes of checkpoints "
+                "(B*H*ceil(T/%d)*N*N*4), the fixed scratch holds %zu",
+                bytes, C, kNoAllocScratchBytes);
+
+  float* scratch = nullptr;
+  if ((rc = noalloc_scratch(&scratch))) return rc;
+  FwdArgs fa;
+  for (int v = 0; v < 6; ++v)
+    if ((rc = make_map(&fa.map[v], in[v], false, B, T, H, N, fwd_steps_per_stage(N, false)))) return rc;
+  if ((rc = status_word(&fa.status))) return rc;
+  fa.s_init = s_init;
+  fa.y = nullptr;
+  fa.s_final = nullptr;
+  fa.ckpt = scratch;  // every checkpoint the backward reads is written first
+  fa.C = C;
+  fa.nck = (T + C - 1) / C;
+  fa.B = B;
+  fa.T = T;
+  fa.H = H;
+  BwdArgs ba;
+  for (int v = 0; v < 7; ++v)
+    if ((rc = make_map(&ba.map[v], in[v], false, B, T, H, N, bwd2_steps_per_window(N, false)))) return rc;
+  if ((rc = make_ckpt_map(&ba.ckmap, scratch, B, H, N, fa.nck))) return rc;
+  if ((rc = status_word(&ba.status))) return rc;
+  ba.ckpt = scratch;
+  ba.dr = grads[0];
+  ba.dw = grads[1];
+  ba.dk = grads[2];
+  ba.dv = grads[3];
+  ba.da = grads[4];
+  ba.db = grads[5];
+  ba.dS_init = dS_init;
+  ba.C = C;
+  ba.nck = fa.nck;
+  ba.B = B;
+  ba.T = T;
+  ba.H = H;
+  cudaError_t e = launch_fwd2(fa, false, N, stream);
+  if (e != cudaSuccess) return fail_cuda(e, "checkpointing forward launch");
+  e = launch_bwd2(ba, false, N, stream);
+  if (e != cudaSuccess) return fail_cuda(e, "backward launch");
+  return WKV7_OK;
+}
+
+}  // namespace
 }  // namespace wkv7
 
 // ============================================================== C ABI ===
@@ -383,5 +494,14 @@ int wkv7_status(void* stream) {
 }
 
 const char* wkv7_last_error(void) { return t_last_error.c_str(); }
+
+int wkv7_backward_noalloc(const float* r, const float* w, const float* k, const float* v, const float* a,
+                          const float* b, const float* dy, const float* s_init, float* dr, float* dw, float* dk,
+                          float* dv, float* da, float* db, float* dS_init, int B, int T, int H, int N,
+                          void* stream) {
+  const float* in[7] = {r, w, k, v, a, b, dy};
+  float* const grads[6] = {dr, dw, dk, dv, da, db};
+  return backward_noalloc_impl(in, s_init, grads, dS_init, B, T, H, N, static_cast<cudaStream_t>(stream));
+}
 
 }  // extern "C"

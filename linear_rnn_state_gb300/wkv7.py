@@ -26,6 +26,7 @@ EXPORTS = {
     "wkv7_default_ckpt_every": 2,
     "wkv7_status": 1,
     "wkv7_last_error": 0,
+    "wkv7_backward_noalloc": 20,
 }
 
 
@@ -62,6 +63,8 @@ def load(path: str | None = None):
     lib.wkv7_status.restype = i
     lib.wkv7_last_error.argtypes = []
     lib.wkv7_last_error.restype = ctypes.c_char_p
+    lib.wkv7_backward_noalloc.argtypes = [vp] * 15 + [i] * 4 + [vp]
+    lib.wkv7_backward_noalloc.restype = i
     if path is None:
         _lib = lib
     return lib
@@ -97,6 +100,14 @@ def wkv7_backward_bf16(r, w, k, v, a, b, dy, s_init, ckpt, ckpt_every, dr, dw, d
                        B, T, H, N, stream):
     return load().wkv7_backward_bf16(r, w, k, v, a, b, dy, s_init, ckpt, ckpt_every, dr, dw, dk, dv, da, db,
                                      dS_init, B, T, H, N, stream)
+
+
+def wkv7_backward_noalloc(r, w, k, v, a, b, dy, s_init, dr, dw, dk, dv, da, db, dS_init, B, T, H, N, stream):
+    """Backward without any device allocation (fp32 inputs): checkpoints go to
+    the library's fixed 64 MiB scratch array. For callers that cannot allocate;
+    calls that overlap on the GPU race on the shared scratch."""
+    return load().wkv7_backward_noalloc(r, w, k, v, a, b, dy, s_init, dr, dw, dk, dv, da, db, dS_init,
+                                        B, T, H, N, stream)
 
 
 def wkv7_ckpt_bytes(B, T, H, N, ckpt_every) -> int:
