@@ -26,6 +26,34 @@ sys.path.insert(0, ROOT)
 METRIC = "WKV7 fwd+bwd tokens/s (B·T) at 1.5B shape; achieved % of roofline"
 FP32_LANES_PER_SM = 128  # Blackwell SM: 4 partitions x 32 FP32 lanes
 
+# DRAM bytes (read + write) per token-head of the backward kernel, from one ncu capture
+# (dram__bytes_read.sum + dram__bytes_write.sum at T=1024, divided by B*T*H; traffic grows in
+# proportion to T). It is valid only for the kernel sources it was taken on: a change to any of
+# them makes the report carry null instead.
+TRAFFIC = {
+    "kernel": "wkv7_bwd2_kernel",
+    "sources": ("wkv7_bwd2.cu", "wkv7_common.cuh", "wkv7_scaled.cuh", "wkv7_tmem.cuh", "wkv7_launch.h"),
+    "sha256": "4d02d49363ab928dcfad8694561f71071cbb9b5644b48d90d1bc6297f8a584a2",
+    "bytes_per_token_head": 412.262656e6 / 131072,
+}
+
+
+def sources_sha256(names) -> str:
+    import hashlib
+
+    h = hashlib.sha256()
+    for n in names:
+        with open(os.path.join(ROOT, "linear_rnn_state_gb300", "csrc", n), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()
+
+
+def measured_traffic(token_heads: int):
+    """Per-launch DRAM bytes of the dominant kernel, or None if its sources changed since."""
+    if not TRAFFIC["sha256"] or sources_sha256(TRAFFIC["sources"]) != TRAFFIC["sha256"]:
+        return None
+    return TRAFFIC["bytes_per_token_head"] * token_heads
+
 
 def _peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
@@ -337,7 +365,7 @@ def _report(args, wl, world, B, T, H, N, C, bf16, ms, fwd_ms, bwd_ms, e2e, ckpt,
                          % ((7 * BTH * N * (2 if bf16 else 4) + ckpt.numel() * 4 + 6 * BTH * N * 4) / 1e9)},
         "fwd_ms": fwd_ms, "bwd_ms": bwd_ms, "step_roofline_frac": t_roof / (ms * 1e-3),
         "roofline": {"bound": "alu", "achieved": achieved / 1e12, "peak": peak_flops / 1e12, "unit": "TFLOP/s",
-                     "frac": achieved / peak_flops, "traffic": None, "kernel": "wkv7_bwd_kernel",
+                     "frac": achieved / peak_flops, "traffic": measured_traffic(BTH), "kernel": TRAFFIC["kernel"],
                      "peak_source": f"{sms} SMs x {FP32_LANES_PER_SM} FP32 lanes x 2 x {peaks['sm_max_mhz']:.0f} MHz",
                      "hbm_gbs_achieved": b_bytes * BTH / (bwd_ms * 1e-3) / 1e9, "hbm_peak_gbs": peaks["hbm_gbs"]},
         "e2e": None if e2e is None else {
