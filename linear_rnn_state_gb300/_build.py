@@ -18,8 +18,8 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD_DIR = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libwkv7.so")
 
-SOURCES = ["wkv7_api.cu", "wkv7_fwd.cu", "wkv7_fwd2.cu", "wkv7_bwd.cu", "wkv7_bwd2.cu"]
-HEADERS = ["wkv7_common.cuh", "wkv7_launch.h", "wkv7_scaled.cuh", "wkv7_tmem.cuh"]
+SOURCES = ["wkv7_api.cu", "wkv7_fwd.cu", "wkv7_fwd2.cu", "wkv7_fwd3.cu", "wkv7_bwd.cu", "wkv7_bwd2.cu"]
+HEADERS = ["wkv7_common.cuh", "wkv7_launch.h", "wkv7_mma.cuh", "wkv7_scaled.cuh", "wkv7_tmem.cuh"]
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ARCH + ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-cudart", "shared",

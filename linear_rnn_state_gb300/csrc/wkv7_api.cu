@@ -197,7 +197,7 @@ int forward_impl(bool bf16, const void* const in[6], const float* s_init, void* 
   args.B = B;
   args.T = T;
   args.H = H;
-  cudaError_t e = launch_fwd2(args, bf16, N, stream);
+  cudaError_t e = use_chunked(bf16, N, ckpt ? C : kChunk) ? launch_fwd3(args, stream) : launch_fwd2(args, bf16, N, stream);
   if (e != cudaSuccess) return fail_cuda(e, "forward launch");
   return WKV7_OK;
 }
@@ -272,7 +272,7 @@ int backward_impl(bool bf16, const void* const in[7], const float* s_init, const
     fa.B = B;
     fa.T = T;
     fa.H = H;
-    e = launch_fwd2(fa, bf16, N, stream);
+    e = use_chunked(bf16, N, C_eff) ? launch_fwd3(fa, stream) : launch_fwd2(fa, bf16, N, stream);
     if (e != cudaSuccess) {
       cudaFreeAsync(ws, stream);
       return fail_cuda(e, "checkpointing forward launch");

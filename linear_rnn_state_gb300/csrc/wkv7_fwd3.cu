@@ -1,0 +1,450 @@
+// WKV7 forward scan on tensor cores (sm_103a): chunked form, bf16 inputs, N = 64.
+//
+// Same result as "rx_pretrain.c", rx_wkv7_forward_seq, per (b, h):
+//   sa = S a ;  S <- S diag(w) + v k^T + sa b^T ;  y = S r.
+// Over a chunk of L = 16 steps with start state S0 and c(t) = w(1)...w(t)
+// (chunk-relative, c(0) = 1), the column-scaled state S~ = S diag(1/c) turns
+// every step into a rank-2 update, and the chunk unrolls into small dense
+// products (time-major L x N matrices, rows = steps):
+//   A^ = a * c(t-1), R^ = r * c(t), K~ = k / c(t), B~ = b / c(t),
+//   Kb = k * c(L)/c(t), Bb = b * c(L)/c(t)
+//   Mka = A^ K~^T, Mba = A^ B~^T (strictly lower), Mkr = R^ K~^T, Mbr = R^ B~^T (lower)
+//   SA  = (I - Mba)^-1 (A^ S0^T + Mka V)            rows: sa(t)
+//   Y   = R^ S0^T + Mkr V + Mbr SA                   rows: y(t)
+//   S(L) = S0 diag(c(L)) + V^T Kb + SA^T Bb
+// (exact up to rounding; the reverse scan uses the same algebra). The
+// products run on tf32 tensor cores with fp32 accumulation; the state stays
+// fp32 in registers.
+//
+// One CTA per (b, h), eight warps in two groups working one chunk apart:
+//  - prep warps (4..7) turn the chunk's r, w, k, v, a, b (TMA tensor loads
+//    into a four-stage ring) into the scaled operands, the four L x L
+//    products and T = (I - Mba)^-1 (forward substitution, one warp), in a
+//    double-buffered operand block;
+//  - state warps (0..3) each own 16 rows i of S as mma accumulator tiles
+//    and compute S0 [A^ R^]^T, SA, Y and S(L) for the chunk the prep warps
+//    finished in the previous round, and write y and the checkpoints.
+// A chunk whose decays leave [1/16, 16] (or hold a NaN) is run step by step
+// in the direct form by the state warps, in fp32.
+#include "wkv7_launch.h"
+#include "wkv7_mma.cuh"
+#include "wkv7_scaled.cuh"
+
+namespace wkv7 {
+namespace {
+
+constexpr int kN = 64, kL = 16;
+constexpr int kLD64 = 72;  // row stride (floats) of 64-wide operands: conflict-free fragment loads
+constexpr int kLD16 = 24;  // row stride of 16-wide operands
+
+// Operand block of one chunk (tf32 values unless noted).
+struct Prep3 {
+  float X1[2 * kL * kLD64];  // rows 0..15: a^(t); rows 16..31: r^(t)   [t][j]
+  float VT[kN * kLD16];      // v(s)[i]                                   [i][s]
+  float KbT[kN * kLD16];     // k(s)[j] c(L)[j] / c(s)[j]                 [j][s]
+  float BbT[kN * kLD16];     // b(s)[j] c(L)[j] / c(s)[j]                 [j][s]
+  float M[4][kL * kLD16];    // Mka, Mba (strictly lower), Mkr, Mbr (lower) [t][s]
+  float Tinv[kL * kLD16];    // (I - Mba)^-1                              [t][s]
+  float cL[kN];              // c(L) (fp32)
+  int unsafe;
+  int pad_[31];
+};
+
+struct Fwd3Smem {
+  __nv_bfloat16 raw[4][6][kL * kN];  // TMA ring: r, w, k, v, a, b of one chunk per stage
+  Prep3 prep[2];
+  float X2[2 * kL * kLD64];  // rows 0..15: k~(s); rows 16..31: b~(s)   [s][j]
+  __nv_bfloat16 ys[kL * kN];  // y of the chunk [t][i]
+  uint64_t full[4];
+  int abort_flag;
+};
+
+constexpr int kStages = 4;
+constexpr int kThreads = 256;
+enum { V_R = 0, V_W = 1, V_K = 2, V_V = 3, V_A = 4, V_B = 5 };
+
+__device__ __forceinline__ float bf(const __nv_bfloat16* p) { return __bfloat162float(*p); }
+__device__ __forceinline__ float2 bf2(const __nv_bfloat16* p) {
+  return __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(p));
+}
+
+// ------------------------------------------------------------ prep warps ---
+// 128 threads; thread (j = ptid % 64, half = ptid / 64) forms column j of
+// steps 8*half .. 8*half+7.
+__device__ void prep_chunk(Fwd3Smem& sm, Prep3& P, int stage, int len, int ptid) {
+  const int pw = ptid >> 5, lane = ptid & 31, g = lane >> 2, t4 = lane & 3;
+  const __nv_bfloat16* rs = sm.raw[stage][0];
+  const int j = ptid & 63, half = ptid >> 6;
+  // decays of this thread's 8 steps (wm) and of the other 8 (wo); padding
+  // steps past the end of the sequence decay by 1
+  float wm[8], wo[8];
+  const int tm = 8 * half, to = 8 - tm;
+#pragma unroll
+  for (int e = 0; e < 8; ++e) {
+    wm[e] = tm + e < len ? bf(rs + V_W * kL * kN + (tm + e) * kN + j) : 1.f;
+    wo[e] = to + e < len ? bf(rs + V_W * kL * kN + (to + e) * kN + j) : 1.f;
+  }
+  bool unsafe = false;
+#pragma unroll
+  for (int e = 0; e < 8; ++e) unsafe |= !decay_is_safe(wm[e]);
+  float pm = 1.f, po = 1.f;
+#pragma unroll
+  for (int e = 0; e < 8; ++e) {
+    pm *= wm[e];
+    po *= wo[e];
+  }
+  const float p_first = half ? po : pm;  // w(1)...w(8), multiplied in step order
+  const float cL = half ? po * pm : pm * po;
+  float c = half ? p_first : 1.f;
+  if (half == 0) P.cL[j] = cL;
+  float vt[8], kbt[8], bbt[8];
+#pragma unroll
+  for (int e = 0; e < 8; ++e) {
+    const int t = tm + e;
+    const float cprev = c;
+    c *= wm[e];
+    const float ic = rcp_approx(c);
+    const int o = t * kN + j;
+    const float a = bf(rs + V_A * kL * kN + o), r = bf(rs + V_R * kL * kN + o);
+    const float k = bf(rs + V_K * kL * kN + o), b = bf(rs + V_B * kL * kN + o);
+    vt[e] = tf32r(bf(rs + V_V * kL * kN + o));
+    sm.X2[t * kLD64 + j] = tf32r(k * ic);
+    sm.X2[(kL + t) * kLD64 + j] = tf32r(b * ic);
+    P.X1[t * kLD64 + j] = tf32r(a * cprev);
+    P.X1[(kL + t) * kLD64 + j] = tf32r(r * c);
+    const float s = cL * ic;
+    kbt[e] = tf32r(k * s);
+    bbt[e] = tf32r(b * s);
+  }
+#pragma unroll
+  for (int q = 0; q < 2; ++q) {
+    const int o = j * kLD16 + 8 * half + 4 * q;
+    *reinterpret_cast<float4*>(P.VT + o) = make_float4(vt[4 * q], vt[4 * q + 1], vt[4 * q + 2], vt[4 * q + 3]);
+    *reinterpret_cast<float4*>(P.KbT + o) = make_float4(kbt[4 * q], kbt[4 * q + 1], kbt[4 * q + 2], kbt[4 * q + 3]);
+    *reinterpret_cast<float4*>(P.BbT + o) = make_float4(bbt[4 * q], bbt[4 * q + 1], bbt[4 * q + 2], bbt[4 * q + 3]);
+  }
+  unsafe = named_bar_or(1, 128, unsafe);
+  if (ptid == 0) P.unsafe = unsafe;
+  if (unsafe) return;
+
+  // Gram blocks: warp pw computes [A^ | R^](rows 16*(pw/2)) x [K~ | B~](rows 16*(pw%2))^T.
+  {
+    const int mt = pw >> 1, nb = pw & 1;
+    float acc[2][4];
+    zero4(acc[0]);
+    zero4(acc[1]);
+#pragma unroll
+    for (int kb = 0; kb < kN / 8; ++kb) {
+      uint32_t a[4];
+      frag_a(a, P.X1, kLD64, 16 * mt, 8 * kb, g, t4);
+#pragma unroll
+      for (int nt = 0; nt < 2; ++nt) {
+        uint32_t b0, b1;
+        frag_b(b0, b1, sm.X2, kLD64, 16 * nb + 8 * nt, 8 * kb, g, t4);
+        mma_tf32(acc[nt], a, b0, b1);
+      }
+    }
+    const bool strict = mt == 0;  // Mka, Mba: s < t; Mkr, Mbr: s <= t
+    float* M = P.M[pw];
+#pragma unroll
+    for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const int t = g + 8 * h, s = 8 * nt + 2 * t4;
+        const float x0 = (s < t || (!strict && s == t)) ? acc[nt][2 * h] : 0.f;
+        const float x1 = (s + 1 < t || (!strict && s + 1 == t)) ? acc[nt][2 * h + 1] : 0.f;
+        *reinterpret_cast<float2*>(M + t * kLD16 + s) = make_float2(tf32r(x0), tf32r(x1));
+      }
+  }
+  // T = (I - Mba)^-1 by forward substitution; warp 1 made Mba, so a warp
+  // barrier suffices. Lane s (< 16) owns column s.
+  if (pw == 1) {
+    __syncwarp();
+    const float* Mba = P.M[1];
+    const int s = lane & 15;
+    float col[kL];
+#pragma unroll
+    for (int t = 0; t < kL; ++t) {
+      float acc = t == s ? 1.f : 0.f;
+#pragma unroll
+      for (int u = 0; u < t; ++u) acc = fmaf(Mba[t * kLD16 + u], col[u], acc);
+      col[t] = acc;
+    }
+    if (lane < 16) {
+#pragma unroll
+      for (int t = 0; t < kL; ++t) P.Tinv[t * kLD16 + s] = tf32r(col[t]);
+    }
+  }
+}
+
+// ----------------------------------------------------------- state warps ---
+
+struct StateCtx {
+  float S[8][4];  // rows i0+g, i0+g+8; columns 8*nt + 2*t4 + {0, 1}
+  int i0, g, t4;
+};
+
+__device__ __forceinline__ void store_state(const StateCtx& c, float* dst) {
+#pragma unroll
+  for (int nt = 0; nt < 8; ++nt) {
+    const int col = 8 * nt + 2 * c.t4;
+    *reinterpret_cast<float2*>(dst + (c.i0 + c.g) * kN + col) = make_float2(c.S[nt][0], c.S[nt][1]);
+    *reinterpret_cast<float2*>(dst + (c.i0 + c.g + 8) * kN + col) = make_float2(c.S[nt][2], c.S[nt][3]);
+  }
+}
+
+// Chunk on tensor cores. Writes the chunk's y into ys.
+__device__ void state_chunk(StateCtx& c, Fwd3Smem& sm, const Prep3& P) {
+  const int g = c.g, t4 = c.t4, i0 = c.i0;
+  // PA = S0 A^^T (later + V^T Mka^T), PR = S0 R^^T (later + ...): [i][t]
+  float PA[2][4], PR[2][4];
+#pragma unroll
+  for (int q = 0; q < 2; ++q) {
+    zero4(PA[q]);
+    zero4(PR[q]);
+  }
+#pragma unroll
+  for (int kb = 0; kb < 8; ++kb) {
+    uint32_t a[4];
+    c2a(a, c.S[kb]);
+#pragma unroll
+    for (int q = 0; q < 2; ++q) {
+      uint32_t b0, b1;
+      frag_b(b0, b1, P.X1, kLD64, 8 * q, 8 * kb, g, t4);
+      mma_tf32(PA[q], a, b0, b1);
+      frag_b(b0, b1, P.X1, kLD64, kL + 8 * q, 8 * kb, g, t4);
+      mma_tf32(PR[q], a, b0, b1);
+    }
+  }
+  uint32_t av[2][4];  // V^T rows i0.., k = s
+  frag_a(av[0], P.VT, kLD16, i0, 0, g, t4);
+  frag_a(av[1], P.VT, kLD16, i0, 8, g, t4);
+#pragma unroll
+  for (int kb = 0; kb < 2; ++kb)
+#pragma unroll
+    for (int q = 0; q < 2; ++q) {
+      uint32_t b0, b1;
+      frag_b(b0, b1, P.M[0], kLD16, 8 * q, 8 * kb, g, t4);  // Mka
+      mma_tf32(PA[q], av[kb], b0, b1);
+      frag_b(b0, b1, P.M[2], kLD16, 8 * q, 8 * kb, g, t4);  // Mkr
+      mma_tf32(PR[q], av[kb], b0, b1);
+    }
+  // SA^T = PA T^T  [i][t]
+  float SA[2][4];
+  zero4(SA[0]);
+  zero4(SA[1]);
+#pragma unroll
+  for (int kb = 0; kb < 2; ++kb) {
+    uint32_t a[4];
+    c2a(a, PA[kb]);
+#pragma unroll
+    for (int q = 0; q < 2; ++q) {
+      uint32_t b0, b1;
+      frag_b(b0, b1, P.Tinv, kLD16, 8 * q, 8 * kb, g, t4);
+      mma_tf32(SA[q], a, b0, b1);
+    }
+  }
+  uint32_t asa[2][4];
+  c2a(asa[0], SA[0]);
+  c2a(asa[1], SA[1]);
+  // Y^T = PR + SA^T Mbr^T
+#pragma unroll
+  for (int kb = 0; kb < 2; ++kb)
+#pragma unroll
+    for (int q = 0; q < 2; ++q) {
+      uint32_t b0, b1;
+      frag_b(b0, b1, P.M[3], kLD16, 8 * q, 8 * kb, g, t4);
+      mma_tf32(PR[q], asa[kb], b0, b1);
+    }
+#pragma unroll
+  for (int q = 0; q < 2; ++q)
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const int i = i0 + g + 8 * h, t = 8 * q + 2 * t4;
+      sm.ys[t * kN + i] = __float2bfloat16_rn(PR[q][2 * h]);
+      sm.ys[(t + 1) * kN + i] = __float2bfloat16_rn(PR[q][2 * h + 1]);
+    }
+  // S(L) = S0 diag(c(L)) + V^T Kb + SA^T Bb
+#pragma unroll
+  for (int nt = 0; nt < 8; ++nt) {
+    const float2 cl = *reinterpret_cast<const float2*>(P.cL + 8 * nt + 2 * t4);
+    c.S[nt][0] *= cl.x;
+    c.S[nt][1] *= cl.y;
+    c.S[nt][2] *= cl.x;
+    c.S[nt][3] *= cl.y;
+  }
+#pragma unroll
+  for (int kb = 0; kb < 2; ++kb)
+#pragma unroll
+    for (int nt = 0; nt < 8; ++nt) {
+      uint32_t b0, b1;
+      frag_b(b0, b1, P.KbT, kLD16, 8 * nt, 8 * kb, g, t4);
+      mma_tf32(c.S[nt], av[kb], b0, b1);
+      frag_b(b0, b1, P.BbT, kLD16, 8 * nt, 8 * kb, g, t4);
+      mma_tf32(c.S[nt], asa[kb], b0, b1);
+    }
+}
+
+// Chunk in the direct form (any decay), fp32 on the CUDA cores.
+__device__ void state_chunk_direct(StateCtx& c, Fwd3Smem& sm, int stage, int len) {
+  const int g = c.g, t4 = c.t4, i0 = c.i0;
+  const __nv_bfloat16* rs = sm.raw[stage][0];
+  for (int t = 0; t < len; ++t) {
+    const __nv_bfloat16* row = rs + t * kN;
+    float s0 = 0.f, s1 = 0.f;
+#pragma unroll
+    for (int nt = 0; nt < 8; ++nt) {
+      const float2 a = bf2(row + V_A * kL * kN + 8 * nt + 2 * t4);
+      s0 = fmaf(c.S[nt][0], a.x, fmaf(c.S[nt][1], a.y, s0));
+      s1 = fmaf(c.S[nt][2], a.x, fmaf(c.S[nt][3], a.y, s1));
+    }
+    s0 += __shfl_xor_sync(0xffffffffu, s0, 1);
+    s0 += __shfl_xor_sync(0xffffffffu, s0, 2);
+    s1 += __shfl_xor_sync(0xffffffffu, s1, 1);
+    s1 += __shfl_xor_sync(0xffffffffu, s1, 2);
+    const float v0 = bf(row + V_V * kL * kN + i0 + g), v1 = bf(row + V_V * kL * kN + i0 + g + 8);
+    float y0 = 0.f, y1 = 0.f;
+#pragma unroll
+    for (int nt = 0; nt < 8; ++nt) {
+      const int col = 8 * nt + 2 * t4;
+      const float2 w = bf2(row + V_W * kL * kN + col), k = bf2(row + V_K * kL * kN + col);
+      const float2 b = bf2(row + V_B * kL * kN + col), r = bf2(row + V_R * kL * kN + col);
+      c.S[nt][0] = fmaf(s0, b.x, fmaf(c.S[nt][0], w.x, v0 * k.x));
+      c.S[nt][1] = fmaf(s0, b.y, fmaf(c.S[nt][1], w.y, v0 * k.y));
+      c.S[nt][2] = fmaf(s1, b.x, fmaf(c.S[nt][2], w.x, v1 * k.x));
+      c.S[nt][3] = fmaf(s1, b.y, fmaf(c.S[nt][3], w.y, v1 * k.y));
+      y0 = fmaf(c.S[nt][0], r.x, fmaf(c.S[nt][1], r.y, y0));
+      y1 = fmaf(c.S[nt][2], r.x, fmaf(c.S[nt][3], r.y, y1));
+    }
+    y0 += __shfl_xor_sync(0xffffffffu, y0, 1);
+    y0 += __shfl_xor_sync(0xffffffffu, y0, 2);
+    y1 += __shfl_xor_sync(0xffffffffu, y1, 1);
+    y1 += __shfl_xor_sync(0xffffffffu, y1, 2);
+    if (t4 == 0) {
+      sm.ys[t * kN + i0 + g] = __float2bfloat16_rn(y0);
+      sm.ys[t * kN + i0 + g + 8] = __float2bfloat16_rn(y1);
+    }
+  }
+}
+
+__global__ void __launch_bounds__(kThreads, 1) wkv7_fwd3_kernel(const __grid_constant__ FwdArgs args) {
+  extern __shared__ __align__(128) unsigned char smem_raw[];
+  Fwd3Smem& sm = *reinterpret_cast<Fwd3Smem*>(smem_raw);
+  const int T = args.T, H = args.H;
+  const int head = blockIdx.x, bi = head / H, hi = head % H;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const bool is_prep = warp >= 4;
+  const int ptid = tid - 128;
+  const int nchunks = (T + kL - 1) / kL;
+  constexpr int kStageBytes = 6 * kL * kN * 2;
+
+  auto issue = [&](int chunk) {
+    const int st = chunk % kStages;
+    mbar_arrive_expect_tx(&sm.full[st], kStageBytes);
+    for (int v = 0; v < 6; ++v) tma_load_4d(sm.raw[st][v], &args.map[v], &sm.full[st], 0, hi, chunk * kL, bi);
+  };
+  if (tid == 128) {
+    for (int s = 0; s < kStages; ++s) mbar_init(&sm.full[s], 1);
+    fence_mbar_init();
+    for (int v = 0; v < 6; ++v) prefetch_tensormap(&args.map[v]);
+    for (int ch = 0; ch < kStages && ch < nchunks; ++ch) issue(ch);
+  }
+  if (tid == 0) sm.abort_flag = 0;
+
+  StateCtx c;
+  c.g = lane >> 2;
+  c.t4 = lane & 3;
+  c.i0 = 16 * warp;
+  if (!is_prep) {
+#pragma unroll
+    for (int nt = 0; nt < 8; ++nt)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) c.S[nt][e] = 0.f;
+    if (args.s_init) {
+      const float* src = args.s_init + (size_t)head * kN * kN;
+#pragma unroll
+      for (int nt = 0; nt < 8; ++nt) {
+        const int col = 8 * nt + 2 * c.t4;
+        const float2 lo = *reinterpret_cast<const float2*>(src + (c.i0 + c.g) * kN + col);
+        const float2 hi2 = *reinterpret_cast<const float2*>(src + (c.i0 + c.g + 8) * kN + col);
+        c.S[nt][0] = lo.x;
+        c.S[nt][1] = lo.y;
+        c.S[nt][2] = hi2.x;
+        c.S[nt][3] = hi2.y;
+      }
+    }
+  }
+  __syncthreads();
+
+  // Prep warps wait for a stage together: the group agrees on the outcome, so
+  // its named barriers stay matched; a timeout raises the CTA's abort flag.
+  int waited = 0;  // chunks whose stage has landed (prep warps)
+  int issued = min(kStages, nchunks);  // chunks whose copy was started (thread 128)
+  auto wait_stage = [&](int chunk) -> bool {
+    const bool ok = mbar_wait_bounded(args.status, &sm.full[chunk % kStages], (chunk / kStages) & 1);
+    const bool bad = named_bar_or(1, 128, !ok);
+    if (bad) {
+      if (ptid == 0) sm.abort_flag = 1;
+      return false;
+    }
+    waited = chunk + 1;
+    return true;
+  };
+  auto chunk_len = [&](int chunk) { return min(kL, T - chunk * kL); };
+
+  if (is_prep && wait_stage(0)) prep_chunk(sm, sm.prep[0], 0, chunk_len(0), ptid);
+  __nv_bfloat16* y = static_cast<__nv_bfloat16*>(args.y);
+  const size_t vstep = (size_t)H * kN;
+  const size_t vbase = ((size_t)bi * T * H + hi) * kN;
+  float* ck_head = args.ckpt ? args.ckpt + (size_t)head * args.nck * kN * kN : nullptr;
+
+  bool aborted = __syncthreads_or(sm.abort_flag) != 0;
+  for (int n = 0; n < nchunks && !aborted; ++n) {
+    if (is_prep) {
+      if (n + 1 < nchunks && wait_stage(n + 1))
+        prep_chunk(sm, sm.prep[(n + 1) & 1], (n + 1) % kStages, chunk_len(n + 1), ptid);
+    } else {
+      const Prep3& P = sm.prep[n & 1];
+      const int t0 = n * kL, len = chunk_len(n);
+      if (ck_head && t0 % args.C == 0) store_state(c, ck_head + (size_t)(t0 / args.C) * kN * kN);
+      if (P.unsafe)
+        state_chunk_direct(c, sm, n % kStages, len);
+      else
+        state_chunk(c, sm, P);
+      named_bar(2, 128);
+      if (y) {
+        const int row = tid >> 3, piece = tid & 7;  // 16 rows x 8 pieces of 16 bytes
+        if (row < len)
+          *reinterpret_cast<uint4*>(y + vbase + (size_t)(t0 + row) * vstep + 8 * piece) =
+              *reinterpret_cast<const uint4*>(sm.ys + row * kN + 8 * piece);
+      }
+    }
+    aborted = __syncthreads_or(sm.abort_flag) != 0;
+    if (!aborted && tid == 128 && n + kStages < nchunks) {
+      fence_proxy_async_smem();
+      issue(n + kStages);
+      issued = n + kStages + 1;
+    }
+  }
+  if (aborted) {
+    // let the copies still in flight land before the CTA's shared memory is released
+    if (tid == 128)
+      for (int ch = waited; ch < issued; ++ch)
+        mbar_wait_bounded(nullptr, &sm.full[ch % kStages], (ch / kStages) & 1, 200000000ull);
+    __syncthreads();
+    return;
+  }
+  if (!is_prep && args.s_final) store_state(c, args.s_final + (size_t)head * kN * kN);
+}
+
+}  // namespace
+
+cudaError_t launch_fwd3(const FwdArgs& args, cudaStream_t stream) {
+  const size_t smem = sizeof(Fwd3Smem);
+  cudaError_t e = cudaFuncSetAttribute(wkv7_fwd3_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  wkv7_fwd3_kernel<<<(unsigned)(args.B * args.H), kThreads, smem, stream>>>(args);
+  return cudaGetLastError();
+}
+
+}  // namespace wkv7

@@ -46,6 +46,11 @@ int bwd_steps_per_stage(int N, bool bf16);
 
 cudaError_t launch_fwd(const FwdArgs& args, bool bf16, int N, cudaStream_t stream);
 cudaError_t launch_fwd2(const FwdArgs& args, bool bf16, int N, cudaStream_t stream);
+// Chunked tensor-core forward: bf16 inputs, N = 64, checkpoints (if any) at a
+// multiple of its 16-step chunk.
+cudaError_t launch_fwd3(const FwdArgs& args, cudaStream_t stream);
+constexpr int kChunk = 16;
+inline bool use_chunked(bool bf16, int N, int C) { return bf16 && N == 64 && C % kChunk == 0; }
 cudaError_t launch_bwd(const BwdArgs& args, bool bf16, int N, cudaStream_t stream);
 cudaError_t launch_bwd2(const BwdArgs& args, bool bf16, int N, cudaStream_t stream);
 int bwd2_steps_per_window(int N, bool bf16);
