@@ -31,8 +31,8 @@ FP32_LANES_PER_SM = 128  # Blackwell SM: 4 partitions x 32 FP32 lanes
 # proportion to T). It is valid only for the kernel sources it was taken on: a change to any of
 # them makes the report carry null instead.
 TRAFFIC = {
-    "kernel": "wkv7_bwd2_kernel",
-    "sources": ("wkv7_bwd2.cu", "wkv7_common.cuh", "wkv7_scaled.cuh", "wkv7_tmem.cuh", "wkv7_launch.h"),
+    "kernel": "wkv7_bwd3_kernel",
+    "sources": ("wkv7_bwd3.cu", "wkv7_common.cuh", "wkv7_scaled.cuh", "wkv7_mma.cuh", "wkv7_launch.h"),
     "sha256": "4d02d49363ab928dcfad8694561f71071cbb9b5644b48d90d1bc6297f8a584a2",
     "bytes_per_token_head": 412.262656e6 / 131072,
 }

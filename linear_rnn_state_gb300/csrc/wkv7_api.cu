@@ -299,7 +299,7 @@ int backward_impl(bool bf16, const void* const in[7], const float* s_init, const
   args.B = B;
   args.T = T;
   args.H = H;
-  cudaError_t e = launch_bwd2(args, bf16, N, stream);
+  cudaError_t e = (bf16 && N == 64 && C_eff == kChunk) ? launch_bwd3(args, stream) : launch_bwd2(args, bf16, N, stream);
   if (ws) {
     cudaError_t e2 = cudaFreeAsync(ws, stream);
     if (e == cudaSuccess && e2 != cudaSuccess) return fail_cuda(e2, "cudaFreeAsync(workspace)");

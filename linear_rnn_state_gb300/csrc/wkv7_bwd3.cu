@@ -1,0 +1,718 @@
+// WKV7 backward-through-time on tensor cores (sm_103a): chunked form, bf16
+// inputs, N = 64, checkpoints every 16 steps.
+//
+// Same result as "rx_pretrain.c", rx_wkv7_backward (the reverse scan of its
+// equations (1)-(3)): per (b, h), with G = dL/dS carried from the last step
+// back to the first,
+//   dr = S_t^T dy ; G += dy r^T ; dk = G^T v ; db = G^T sa ;
+//   dw = colsum(G o S_prev) ; dv = G k ; dsa = G b ; da = S_prev^T dsa ;
+//   G <- G diag(w) + dsa a^T ;  dS_init = G after the first step.
+// Over a chunk of L = 16 steps with checkpoint S0 (state before the chunk),
+// carry Gc (gradient w.r.t. the state after the chunk) and the scaled
+// operands of the forward (A^, R^, K~, B~, Kb, Bb, the products Mka, Mba,
+// Mkr, Mbr and T = (I - Mba)^-1, see the forward kernel), G(t) =
+// G~(t) diag(1/c(t)) with G~(t) = Gc diag(c(L)) + sum_{s>=t} dy r^^T +
+// sum_{s>t} dsa a^^T, and the reverse scan becomes (time-major, rows = steps)
+//   SA  = T (A^ S0^T + Mka V)                 (recomputed sa)
+//   DSA = T^T (Bb Gc^T + Mbr^T DY)            rows: dsa(t)
+//   DV  = Kb Gc^T + Mkr^T DY + Mka^T DSA
+//   DK~ = (V Gc) diag(c(L)) + triu(V DY^T) R^ + triu(V DSA^T, 1) A^,  dk = DK~ / c
+//   DB~ = (SA Gc) diag(c(L)) + triu(SA DY^T) R^ + triu(SA DSA^T, 1) A^, db = DB~ / c
+//   DR^ = DY S0 + tril(DY V^T) K~ + tril(DY SA^T) B~,                  dr = DR^ c
+//   DA^ = DSA S0 + tril(DSA V^T, -1) K~ + tril(DSA SA^T, -1) B~,       da = DA^ c(t-1)
+//   carry: Gc <- Gc diag(c(L)) + DY^T R^ + DSA^T A^
+// dw follows from the chunk's dependence on log c: with x = r dr - k dk -
+// b db + a da (per step and column),
+//   w(t) dw(t) = sum_{u>=t} x(u) - a(t) da(t) + colsum(Gc o S(L))
+//              = colsum(Gc' o S0) - sum_{u<t} x(u) - a(t) da(t)
+// (Gc' the carry out of the chunk; the colsum terms are the dependence of
+// the chunk-end state on c(L) and of the chunk start on nothing). The
+// kernel takes the first form for the last 8 steps and the second for the
+// first 8, so at most 8 terms are summed, and dw is exactly 0 where the
+// state before the step is. All products run on tf32 tensor cores
+// (mma.sync m16n8k8) with fp32 accumulation.
+//
+// One CTA per (b, h), eight warps, chunks in reverse order. Warps 0..3
+// ("state warps") own 16 rows i of the carry Gc as accumulator tiles and
+// produce sa, dsa, dv and the next carry; warps 4..7 ("prep warps") form the
+// scaled operands (TMA ring of r, w, k, v, a, b, dy), the L x L products and
+// T; then all eight warps produce dr, dk, db, da, dw for 8 columns each.
+// Checkpoints arrive by cp.async one chunk ahead. A chunk whose decays leave
+// [1/16, 16] (or hold a NaN) is run step by step in the direct form, fp32,
+// recomputing each S_prev from the checkpoint.
+#include "wkv7_launch.h"
+#include "wkv7_mma.cuh"
+#include "wkv7_scaled.cuh"
+
+namespace wkv7 {
+namespace {
+
+constexpr int kN = 64, kL = 16;
+constexpr int kLD64 = 72;  // row stride (floats) of 64-wide operands
+constexpr int kLD16 = 24;  // row stride of 16-wide operands
+constexpr int kStages = 3;
+constexpr int kThreads = 256;
+constexpr int kTile = kL * kN;
+enum { V_R = 0, V_W = 1, V_K = 2, V_V = 3, V_A = 4, V_B = 5, V_DY = 6 };
+
+struct Bwd3Smem {
+  __nv_bfloat16 raw[kStages][7][kTile];  // r, w, k, v, a, b, dy of one chunk per stage
+  // scaled operands of the chunk, tf32 values, [t][j] (V and DY: [t][i])
+  float Ah[kL * kLD64], Rh[kL * kLD64], Kt[kL * kLD64], Bt[kL * kLD64];
+  float Kb[kL * kLD64], Bb[kL * kLD64], Vs[kL * kLD64], DYs[kL * kLD64];
+  float cS[kTile], icS[kTile];  // c(t) and 1/c(t), fp32 [t][j]
+  float cL[kN], bnd[kN], bpart[kN];
+  float spart[4][kN];  // per state warp: column sums of (next carry o S0) over its rows
+  float M[4][kL * kLD16];  // Mka, Mba (strictly lower), Mkr, Mbr (lower)   [t][s]
+  float Tinv[kL * kLD16];  // (I - Mba)^-1                                    [t][s]
+  // triu(V DY^T), triu(V DSA^T, 1), triu(SA DY^T), triu(SA DSA^T, 1)      [t][s]
+  // (their transposes are the tril(...) factors); direct chunks reuse it
+  float U[4][kL * kLD16];
+  float SAs[kL * kLD64], DSAs[kL * kLD64];  // sa(t), dsa(t) [t][i] (tf32)
+  float GcS[kN * kLD64];                    // carry at the chunk end [i][j]
+  float S0s[3][kN * kLD64];                 // checkpoints [i][j]
+  float dvs[kTile];                         // dv of the chunk [t][i]
+  uint64_t full[kStages];
+  int unsafe, abort_flag;
+};
+
+__device__ __forceinline__ float bf(const __nv_bfloat16* p) { return __bfloat162float(*p); }
+__device__ __forceinline__ float2 bf2(const __nv_bfloat16* p) {
+  return __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(p));
+}
+
+// Scaled operands of a chunk. 128 prep threads; thread (j, half) forms
+// column j of steps 8*half .. 8*half+7. Returns (uniformly over the prep
+// warps) whether some decay leaves the range of the scaled form.
+__device__ bool prep_bwd(Bwd3Smem& sm, int stage, int len, int ptid) {
+  const __nv_bfloat16* rs = sm.raw[stage][0];
+  const int j = ptid & 63, half = ptid >> 6;
+  float wm[8], wo[8];
+  const int tm = 8 * half, to = 8 - tm;
+#pragma unroll
+  for (int e = 0; e < 8; ++e) {
+    wm[e] = tm + e < len ? bf(rs + V_W * kTile + (tm + e) * kN + j) : 1.f;
+    wo[e] = to + e < len ? bf(rs + V_W * kTile + (to + e) * kN + j) : 1.f;
+  }
+  bool unsafe = false;
+#pragma unroll
+  for (int e = 0; e < 8; ++e) unsafe |= !decay_is_safe(wm[e]);
+  unsafe = named_bar_or(1, 128, unsafe);
+  if (unsafe) return true;
+  float pm = 1.f, po = 1.f;
+#pragma unroll
+  for (int e = 0; e < 8; ++e) {
+    pm *= wm[e];
+    po *= wo[e];
+  }
+  const float cL = half ? po * pm : pm * po;
+  float c = half ? po : 1.f;
+  if (half == 0) sm.cL[j] = cL;
+#pragma unroll
+  for (int e = 0; e < 8; ++e) {
+    const int t = tm + e;
+    const float cprev = c;
+    c *= wm[e];
+    const float ic = rcp_approx(c);
+    const int o = t * kN + j, q = t * kLD64 + j;
+    const float a = bf(rs + V_A * kTile + o), r = bf(rs + V_R * kTile + o);
+    const float k = bf(rs + V_K * kTile + o), b = bf(rs + V_B * kTile + o);
+    sm.Ah[q] = tf32r(a * cprev);
+    sm.Rh[q] = tf32r(r * c);
+    sm.Kt[q] = tf32r(k * ic);
+    sm.Bt[q] = tf32r(b * ic);
+    const float s = cL * ic;
+    sm.Kb[q] = tf32r(k * s);
+    sm.Bb[q] = tf32r(b * s);
+    sm.Vs[q] = tf32r(bf(rs + V_V * kTile + o));
+    sm.DYs[q] = tf32r(bf(rs + V_DY * kTile + o));
+    sm.cS[o] = c;
+    sm.icS[o] = ic;
+  }
+  return false;
+}
+
+// acc = P Q^T for 16-row P, Q (ld kLD64, tf32 values), K = 64.
+__device__ __forceinline__ void gram16(float (&acc)[2][4], const float* P, const float* Q, int g, int t4) {
+  zero4(acc[0]);
+  zero4(acc[1]);
+#pragma unroll
+  for (int kb = 0; kb < kN / 8; ++kb) {
+    uint32_t a[4];
+    frag_a(a, P, kLD64, 0, 8 * kb, g, t4);
+#pragma unroll
+    for (int nt = 0; nt < 2; ++nt) {
+      uint32_t b0, b1;
+      frag_b(b0, b1, Q, kLD64, 8 * nt, 8 * kb, g, t4);
+      mma_tf32(acc[nt], a, b0, b1);
+    }
+  }
+}
+
+// Store a 16 x 16 accumulator as tf32, keeping (t, s) with
+// lower: s < t (+ s == t if incl); upper: s > t (+ s == t if incl).
+__device__ __forceinline__ void store_masked(const float (&acc)[2][4], float* dst, bool lower, bool incl, int g,
+                                             int t4) {
+#pragma unroll
+  for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const int t = g + 8 * h, s = 8 * nt + 2 * t4;
+      float x[2];
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        const int se = s + e;
+        const bool keep = lower ? (se < t || (incl && se == t)) : (se > t || (incl && se == t));
+        x[e] = keep ? acc[nt][2 * h + e] : 0.f;
+      }
+      *reinterpret_cast<float2*>(dst + t * kLD16 + s) = make_float2(tf32r(x[0]), tf32r(x[1]));
+    }
+}
+
+// --------------------------------------------------------- direct chunk ---
+// Step-by-step reverse scan of one chunk (state warps, fp32). G is the
+// carry in accumulator layout; S_prev of step t is recomputed from the
+// checkpoint.
+struct Outs {
+  float *dr, *dw, *dk, *dv, *da, *db;
+  size_t base;   // element offset of (b, t0, h, 0)
+  size_t vstep;  // elements between consecutive steps
+};
+
+__device__ __forceinline__ float quad_sum(float x) {
+  x += __shfl_xor_sync(0xffffffffu, x, 1);
+  return x + __shfl_xor_sync(0xffffffffu, x, 2);
+}
+__device__ __forceinline__ float col_sum(float x) {  // over the 8 row groups g of the warp
+  x += __shfl_xor_sync(0xffffffffu, x, 4);
+  x += __shfl_xor_sync(0xffffffffu, x, 8);
+  return x + __shfl_xor_sync(0xffffffffu, x, 16);
+}
+
+__device__ void direct_chunk_bwd(Bwd3Smem& sm, const float* S0, int stage, int len, const Outs& o, float (&G)[8][4],
+                                 int warp, int lane) {
+  const int g = lane >> 2, t4 = lane & 3, i0 = 16 * warp, tid = threadIdx.x;
+  const __nv_bfloat16* rs = sm.raw[stage][0];
+  float* red = &sm.U[0][0];  // [4 warps][5][64]
+  for (int t = len - 1; t >= 0; --t) {
+    float sp[8][4];
+#pragma unroll
+    for (int nt = 0; nt < 8; ++nt) {
+      const int col = 8 * nt + 2 * t4;
+      const float2 lo = *reinterpret_cast<const float2*>(S0 + (i0 + g) * kLD64 + col);
+      const float2 hi = *reinterpret_cast<const float2*>(S0 + (i0 + g + 8) * kLD64 + col);
+      sp[nt][0] = lo.x;
+      sp[nt][1] = lo.y;
+      sp[nt][2] = hi.x;
+      sp[nt][3] = hi.y;
+    }
+    float sa0 = 0.f, sa1 = 0.f;
+    for (int u = 0; u <= t; ++u) {
+      const __nv_bfloat16* row = rs + u * kN;
+      float s0 = 0.f, s1 = 0.f;
+#pragma unroll
+      for (int nt = 0; nt < 8; ++nt) {
+        const float2 a = bf2(row + V_A * kTile + 8 * nt + 2 * t4);
+        s0 = fmaf(sp[nt][0], a.x, fmaf(sp[nt][1], a.y, s0));
+        s1 = fmaf(sp[nt][2], a.x, fmaf(sp[nt][3], a.y, s1));
+      }
+      sa0 = quad_sum(s0);
+      sa1 = quad_sum(s1);
+      if (u == t) break;  // sp = S_prev(t), sa = sa(t)
+      const float v0 = bf(row + V_V * kTile + i0 + g), v1 = bf(row + V_V * kTile + i0 + g + 8);
+#pragma unroll
+      for (int nt = 0; nt < 8; ++nt) {
+        const int col = 8 * nt + 2 * t4;
+        const float2 w = bf2(row + V_W * kTile + col), k = bf2(row + V_K * kTile + col);
+        const float2 b = bf2(row + V_B * kTile + col);
+        sp[nt][0] = fmaf(sa0, b.x, fmaf(sp[nt][0], w.x, v0 * k.x));
+        sp[nt][1] = fmaf(sa0, b.y, fmaf(sp[nt][1], w.y, v0 * k.y));
+        sp[nt][2] = fmaf(sa1, b.x, fmaf(sp[nt][2], w.x, v1 * k.x));
+        sp[nt][3] = fmaf(sa1, b.y, fmaf(sp[nt][3], w.y, v1 * k.y));
+      }
+    }
+    const __nv_bfloat16* row = rs + t * kN;
+    const float v0 = bf(row + V_V * kTile + i0 + g), v1 = bf(row + V_V * kTile + i0 + g + 8);
+    const float dy0 = bf(row + V_DY * kTile + i0 + g), dy1 = bf(row + V_DY * kTile + i0 + g + 8);
+    // column partials: dr (from S_t), then G += dy r^T, dk, db, dw; row sums dv, dsa
+    float pr[8][2], pk[8][2], pb[8][2], pw[8][2];
+    float dv0 = 0.f, dv1 = 0.f, ds0 = 0.f, ds1 = 0.f;
+#pragma unroll
+    for (int nt = 0; nt < 8; ++nt) {
+      const int col = 8 * nt + 2 * t4;
+      const float2 w = bf2(row + V_W * kTile + col), k = bf2(row + V_K * kTile + col);
+      const float2 b = bf2(row + V_B * kTile + col), r = bf2(row + V_R * kTile + col);
+      const float wv[2] = {w.x, w.y}, kv[2] = {k.x, k.y}, bv[2] = {b.x, b.y}, rv[2] = {r.x, r.y};
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        const float st0 = fmaf(sa0, bv[e], fmaf(sp[nt][e], wv[e], v0 * kv[e]));
+        const float st1 = fmaf(sa1, bv[e], fmaf(sp[nt][2 + e], wv[e], v1 * kv[e]));
+        pr[nt][e] = fmaf(st0, dy0, st1 * dy1);
+        G[nt][e] = fmaf(dy0, rv[e], G[nt][e]);
+        G[nt][2 + e] = fmaf(dy1, rv[e], G[nt][2 + e]);
+        pk[nt][e] = fmaf(G[nt][e], v0, G[nt][2 + e] * v1);
+        pb[nt][e] = fmaf(G[nt][e], sa0, G[nt][2 + e] * sa1);
+        pw[nt][e] = fmaf(G[nt][e], sp[nt][e], G[nt][2 + e] * sp[nt][2 + e]);
+        dv0 = fmaf(G[nt][e], kv[e], dv0);
+        dv1 = fmaf(G[nt][2 + e], kv[e], dv1);
+        ds0 = fmaf(G[nt][e], bv[e], ds0);
+        ds1 = fmaf(G[nt][2 + e], bv[e], ds1);
+      }
+    }
+    dv0 = quad_sum(dv0);
+    dv1 = quad_sum(dv1);
+    ds0 = quad_sum(ds0);
+    ds1 = quad_sum(ds1);
+    if (t4 == 0) {
+      o.dv[o.base + (size_t)t * o.vstep + i0 + g] = dv0;
+      o.dv[o.base + (size_t)t * o.vstep + i0 + g + 8] = dv1;
+    }
+    // da = S_prev^T dsa; carry G <- G diag(w) + dsa a^T; column sums to shared memory
+#pragma unroll
+    for (int nt = 0; nt < 8; ++nt) {
+      const int col = 8 * nt + 2 * t4;
+      const float2 w = bf2(row + V_W * kTile + col), a = bf2(row + V_A * kTile + col);
+      const float wv[2] = {w.x, w.y}, av[2] = {a.x, a.y};
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        const float pa = fmaf(sp[nt][e], ds0, sp[nt][2 + e] * ds1);
+        G[nt][e] = fmaf(ds0, av[e], G[nt][e] * wv[e]);
+        G[nt][2 + e] = fmaf(ds1, av[e], G[nt][2 + e] * wv[e]);
+        const float sums[5] = {col_sum(pr[nt][e]), col_sum(pk[nt][e]), col_sum(pb[nt][e]), col_sum(pw[nt][e]),
+                               col_sum(pa)};
+        if (g == 0) {
+#pragma unroll
+          for (int q = 0; q < 5; ++q) red[(warp * 5 + q) * kN + col + e] = sums[q];
+        }
+      }
+    }
+    named_bar(2, 128);
+    for (int idx = tid; idx < 5 * kN; idx += 128) {
+      const int q = idx / kN, col = idx % kN;
+      const float x = red[q * kN + col] + red[(5 + q) * kN + col] + red[(10 + q) * kN + col] + red[(15 + q) * kN + col];
+      float* dst = q == 0 ? o.dr : q == 1 ? o.dk : q == 2 ? o.db : q == 3 ? o.dw : o.da;
+      dst[o.base + (size_t)t * o.vstep + col] = x;
+    }
+    named_bar(2, 128);
+  }
+}
+
+// ----------------------------------------------------------------- kernel ---
+
+__global__ void __launch_bounds__(kThreads, 1) wkv7_bwd3_kernel(const __grid_constant__ BwdArgs args) {
+  extern __shared__ __align__(128) unsigned char smem_raw[];
+  Bwd3Smem& sm = *reinterpret_cast<Bwd3Smem*>(smem_raw);
+  const int T = args.T, H = args.H;
+  const int head = blockIdx.x, bi = head / H, hi = head % H;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, g = lane >> 2, t4 = lane & 3;
+  const bool is_prep = warp >= 4;
+  const int ptid = tid - 128, pw = warp - 4;
+  const int i0 = 16 * warp;  // state warps: rows of the carry
+  const int nchunks = (T + kL - 1) / kL;
+  constexpr int kStageBytes = 7 * kTile * 2;
+  const float* ck_head = args.ckpt + (size_t)head * args.nck * kN * kN;
+
+  // chunks are visited in reverse; visit m handles chunk nchunks-1-m
+  auto issue = [&](int m) {
+    const int st = m % kStages, chunk = nchunks - 1 - m;
+    mbar_arrive_expect_tx(&sm.full[st], kStageBytes);
+    for (int v = 0; v < 7; ++v) tma_load_4d(sm.raw[st][v], &args.map[v], &sm.full[st], 0, hi, chunk * kL, bi);
+  };
+  // state warps copy checkpoint `chunk` into S0s[chunk % 3] (padded rows)
+  auto fetch_ckpt = [&](int chunk) {
+    const float* src = ck_head + (size_t)chunk * kN * kN;
+    float* dst = sm.S0s[chunk % 3];
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
+      const int idx = tid + 128 * q;  // 16-byte piece: row idx / 16, column 4 * (idx % 16)
+      cp_async16(dst + (idx >> 4) * kLD64 + 4 * (idx & 15), src + 4 * idx);
+    }
+    cp_async_commit();
+  };
+  if (tid == 128) {
+    for (int s = 0; s < kStages; ++s) mbar_init(&sm.full[s], 1);
+    fence_mbar_init();
+    for (int v = 0; v < 7; ++v) prefetch_tensormap(&args.map[v]);
+    for (int m = 0; m < kStages && m < nchunks; ++m) issue(m);
+  }
+  if (tid == 0) sm.abort_flag = 0;
+  float G[8][4];
+#pragma unroll
+  for (int nt = 0; nt < 8; ++nt) zero4(G[nt]);
+  if (!is_prep) fetch_ckpt(nchunks - 1);
+  __syncthreads();
+
+  int waited = 0, issued = min(kStages, nchunks);
+  const size_t vstep = (size_t)H * kN;
+  bool aborted = false;
+  for (int m = 0; m < nchunks; ++m) {
+    const int n = nchunks - 1 - m, st = m % kStages, t0 = n * kL, len = min(kL, T - t0);
+    const float* S0 = sm.S0s[n % 3];
+    // ---- A: checkpoint and carry to shared memory; prep of the chunk's operands
+    if (!is_prep) {
+      cp_async_wait_all();
+      if (n > 0) fetch_ckpt(n - 1);
+#pragma unroll
+      for (int nt = 0; nt < 8; ++nt) {
+        const int col = 8 * nt + 2 * t4;
+        *reinterpret_cast<float2*>(sm.GcS + (i0 + g) * kLD64 + col) = make_float2(G[nt][0], G[nt][1]);
+        *reinterpret_cast<float2*>(sm.GcS + (i0 + g + 8) * kLD64 + col) = make_float2(G[nt][2], G[nt][3]);
+      }
+    } else {
+      const bool ok = mbar_wait_bounded(args.status, &sm.full[st], (m / kStages) & 1);
+      if (named_bar_or(1, 128, !ok)) {
+        if (ptid == 0) sm.abort_flag = 1;
+      } else {
+        waited = m + 1;
+        const bool unsafe = prep_bwd(sm, st, len, ptid);
+        if (ptid == 0) sm.unsafe = unsafe;
+      }
+    }
+    if (__syncthreads_or(sm.abort_flag)) {
+      aborted = true;
+      break;
+    }
+    const Outs o{args.dr, args.dw, args.dk, args.dv, args.da, args.db, ((size_t)bi * T + t0) * vstep + (size_t)hi * kN,
+                 vstep};
+    if (sm.unsafe) {
+      if (!is_prep) direct_chunk_bwd(sm, S0, st, len, o, G, warp, lane);
+    } else {
+      // ---- B: L x L products and T (prep warps); first products of the state warps
+      float RSA[2][4], RDSA[2][4], RDV[2][4];
+      if (is_prep) {
+        float acc[2][4];
+        const int mt = pw >> 1, nb = pw & 1;
+        zero4(acc[0]);
+        zero4(acc[1]);
+#pragma unroll
+        for (int kb = 0; kb < kN / 8; ++kb) {
+          uint32_t a[4];
+          frag_a(a, mt ? sm.Rh : sm.Ah, kLD64, 0, 8 * kb, g, t4);
+#pragma unroll
+          for (int nt = 0; nt < 2; ++nt) {
+            uint32_t b0, b1;
+            frag_b(b0, b1, nb ? sm.Bt : sm.Kt, kLD64, 8 * nt, 8 * kb, g, t4);
+            mma_tf32(acc[nt], a, b0, b1);
+          }
+        }
+        store_masked(acc, sm.M[pw], true, mt == 1, g, t4);
+        if (pw == 1) {  // T = (I - Mba)^-1, lane s < 16 owns column s
+          __syncwarp();
+          const float* Mba = sm.M[1];
+          const int s = lane & 15;
+          float col[kL];
+#pragma unroll
+          for (int t = 0; t < kL; ++t) {
+            float x = t == s ? 1.f : 0.f;
+#pragma unroll
+            for (int u = 0; u < t; ++u) x = fmaf(Mba[t * kLD16 + u], col[u], x);
+            col[t] = x;
+          }
+          if (lane < 16) {
+#pragma unroll
+            for (int t = 0; t < kL; ++t) sm.Tinv[t * kLD16 + s] = tf32r(col[t]);
+          }
+        } else if (pw == 2) {  // U0 = triu(V DY^T)
+          gram16(acc, sm.Vs, sm.DYs, g, t4);
+          store_masked(acc, sm.U[0], false, true, g, t4);
+        }
+      } else {
+#pragma unroll
+        for (int q = 0; q < 2; ++q) {
+          zero4(RSA[q]);
+          zero4(RDSA[q]);
+          zero4(RDV[q]);
+        }
+#pragma unroll
+        for (int kb = 0; kb < 8; ++kb) {
+          uint32_t aS[4], aG[4];
+          frag_a_r(aS, S0, kLD64, i0, 8 * kb, g, t4);
+          c2a(aG, G[kb]);
+#pragma unroll
+          for (int q = 0; q < 2; ++q) {
+            uint32_t b0, b1;
+            frag_b(b0, b1, sm.Ah, kLD64, 8 * q, 8 * kb, g, t4);
+            mma_tf32(RSA[q], aS, b0, b1);
+            frag_b(b0, b1, sm.Bb, kLD64, 8 * q, 8 * kb, g, t4);
+            mma_tf32(RDSA[q], aG, b0, b1);
+            frag_b(b0, b1, sm.Kb, kLD64, 8 * q, 8 * kb, g, t4);
+            mma_tf32(RDV[q], aG, b0, b1);
+          }
+        }
+      }
+      __syncthreads();
+      // ---- C: sa, dsa, dv and the next carry (state warps); boundary term (prep warps)
+      if (!is_prep) {
+        uint32_t aV[2][4], aD[2][4];
+#pragma unroll
+        for (int kb = 0; kb < 2; ++kb) {
+          frag_a_t(aV[kb], sm.Vs, kLD64, i0, 8 * kb, g, t4);   // V^T
+          frag_a_t(aD[kb], sm.DYs, kLD64, i0, 8 * kb, g, t4);  // DY^T
+#pragma unroll
+          for (int q = 0; q < 2; ++q) {
+            uint32_t b0, b1;
+            frag_b(b0, b1, sm.M[0], kLD16, 8 * q, 8 * kb, g, t4);  // + V^T Mka^T
+            mma_tf32(RSA[q], aV[kb], b0, b1);
+            frag_b_t(b0, b1, sm.M[3], kLD16, 8 * q, 8 * kb, g, t4);  // + DY^T Mbr
+            mma_tf32(RDSA[q], aD[kb], b0, b1);
+            frag_b_t(b0, b1, sm.M[2], kLD16, 8 * q, 8 * kb, g, t4);  // + DY^T Mkr
+            mma_tf32(RDV[q], aD[kb], b0, b1);
+          }
+        }
+        float SA[2][4], DSA[2][4];
+#pragma unroll
+        for (int q = 0; q < 2; ++q) {
+          zero4(SA[q]);
+          zero4(DSA[q]);
+        }
+#pragma unroll
+        for (int kb = 0; kb < 2; ++kb) {
+          uint32_t a1[4], a2[4];
+          c2a(a1, RSA[kb]);
+          c2a(a2, RDSA[kb]);
+#pragma unroll
+          for (int q = 0; q < 2; ++q) {
+            uint32_t b0, b1;
+            frag_b(b0, b1, sm.Tinv, kLD16, 8 * q, 8 * kb, g, t4);  // SA^T = RSA T^T
+            mma_tf32(SA[q], a1, b0, b1);
+            frag_b_t(b0, b1, sm.Tinv, kLD16, 8 * q, 8 * kb, g, t4);  // DSA^T = RDSA T
+            mma_tf32(DSA[q], a2, b0, b1);
+          }
+        }
+        uint32_t aDS[2][4];
+        c2a(aDS[0], DSA[0]);
+        c2a(aDS[1], DSA[1]);
+#pragma unroll
+        for (int kb = 0; kb < 2; ++kb)
+#pragma unroll
+          for (int q = 0; q < 2; ++q) {
+            uint32_t b0, b1;
+            frag_b_t(b0, b1, sm.M[0], kLD16, 8 * q, 8 * kb, g, t4);  // DV^T += DSA^T Mka
+            mma_tf32(RDV[q], aDS[kb], b0, b1);
+          }
+#pragma unroll
+        for (int q = 0; q < 2; ++q)
+#pragma unroll
+          for (int h = 0; h < 2; ++h)
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+              const int i = i0 + g + 8 * h, t = 8 * q + 2 * t4 + e;
+              sm.SAs[t * kLD64 + i] = tf32r(SA[q][2 * h + e]);
+              sm.DSAs[t * kLD64 + i] = tf32r(DSA[q][2 * h + e]);
+              sm.dvs[t * kN + i] = RDV[q][2 * h + e];
+            }
+        // next carry: Gc diag(c(L)) + DY^T R^ + DSA^T A^
+#pragma unroll
+        for (int nt = 0; nt < 8; ++nt) {
+          const float2 cl = *reinterpret_cast<const float2*>(sm.cL + 8 * nt + 2 * t4);
+          G[nt][0] *= cl.x;
+          G[nt][1] *= cl.y;
+          G[nt][2] *= cl.x;
+          G[nt][3] *= cl.y;
+        }
+#pragma unroll
+        for (int kb = 0; kb < 2; ++kb)
+#pragma unroll
+          for (int nt = 0; nt < 8; ++nt) {
+            uint32_t b0, b1;
+            frag_b_t(b0, b1, sm.Rh, kLD64, 8 * nt, 8 * kb, g, t4);
+            mma_tf32(G[nt], aD[kb], b0, b1);
+            frag_b_t(b0, b1, sm.Ah, kLD64, 8 * nt, 8 * kb, g, t4);
+            mma_tf32(G[nt], aDS[kb], b0, b1);
+          }
+        // start anchor of the dw identity: colsum(next carry o S0), this warp's rows
+#pragma unroll
+        for (int nt = 0; nt < 8; ++nt) {
+          const int col = 8 * nt + 2 * t4;
+          const float2 s_lo = *reinterpret_cast<const float2*>(S0 + (i0 + g) * kLD64 + col);
+          const float2 s_hi = *reinterpret_cast<const float2*>(S0 + (i0 + g + 8) * kLD64 + col);
+          const float p0 = col_sum(fmaf(G[nt][0], s_lo.x, G[nt][2] * s_hi.x));
+          const float p1 = col_sum(fmaf(G[nt][1], s_lo.y, G[nt][3] * s_hi.y));
+          if (g == 0) *reinterpret_cast<float2*>(sm.spart[warp] + col) = make_float2(p0, p1);
+        }
+        named_bar(2, 128);
+        if (args.dv) {
+          const int p = tid & 15;
+#pragma unroll
+          for (int rr = 0; rr < 2; ++rr) {
+            const int t = (tid >> 4) + 8 * rr;
+            if (t < len)
+              *reinterpret_cast<float4*>(args.dv + o.base + (size_t)t * vstep + 4 * p) =
+                  *reinterpret_cast<const float4*>(sm.dvs + t * kN + 4 * p);
+          }
+        }
+      } else {
+        // boundary term colsum(Gc o S(L)); zero for the last chunk (Gc = 0)
+        const int j = ptid & 63, half = ptid >> 6;
+        float x = 0.f;
+        if (n + 1 < nchunks) {
+          const float* SL = sm.S0s[(n + 1) % 3];
+#pragma unroll 8
+          for (int i = 32 * half; i < 32 * half + 32; ++i) x = fmaf(sm.GcS[i * kLD64 + j], SL[i * kLD64 + j], x);
+        }
+        if (half) sm.bpart[j] = x;
+        named_bar(1, 128);
+        if (!half) sm.bnd[j] = x + sm.bpart[j];
+      }
+      __syncthreads();
+      // ---- D: remaining L x L products (prep warps); column products of every warp
+      if (is_prep && pw < 3) {
+        float acc[2][4];
+        gram16(acc, pw == 0 ? sm.Vs : sm.SAs, pw == 1 ? sm.DYs : sm.DSAs, g, t4);
+        store_masked(acc, sm.U[pw + 1], false, pw == 1, g, t4);  // U1, U3 strictly upper; U2 with diagonal
+      }
+      const int j0 = 8 * warp;
+      float bK[4], bB[4], bR[4], bA[4];
+      zero4(bK);
+      zero4(bB);
+      zero4(bR);
+      zero4(bA);
+#pragma unroll
+      for (int kb = 0; kb < 8; ++kb) {
+        uint32_t aV[4], aSA[4], aDY[4], aDSA[4], b0, b1, c0, c1;
+        frag_a(aV, sm.Vs, kLD64, 0, 8 * kb, g, t4);
+        frag_a(aSA, sm.SAs, kLD64, 0, 8 * kb, g, t4);
+        frag_a(aDY, sm.DYs, kLD64, 0, 8 * kb, g, t4);
+        frag_a(aDSA, sm.DSAs, kLD64, 0, 8 * kb, g, t4);
+        frag_b_t(b0, b1, sm.GcS, kLD64, j0, 8 * kb, g, t4);
+        frag_b_t(c0, c1, S0, kLD64, j0, 8 * kb, g, t4);
+        mma_tf32(bK, aV, b0, b1);
+        mma_tf32(bB, aSA, b0, b1);
+        mma_tf32(bR, aDY, c0, c1);
+        mma_tf32(bA, aDSA, c0, c1);
+      }
+      __syncthreads();
+      // ---- E: triangular terms, scaling, dw, stores (columns j0 .. j0+7)
+      {
+        const float2 cl = *reinterpret_cast<const float2*>(sm.cL + j0 + 2 * t4);
+        bK[0] *= cl.x;
+        bK[1] *= cl.y;
+        bK[2] *= cl.x;
+        bK[3] *= cl.y;
+        bB[0] *= cl.x;
+        bB[1] *= cl.y;
+        bB[2] *= cl.x;
+        bB[3] *= cl.y;
+#pragma unroll
+        for (int kb = 0; kb < 2; ++kb) {
+          uint32_t a[4], b0, b1;
+          frag_b_t(b0, b1, sm.Rh, kLD64, j0, 8 * kb, g, t4);
+          frag_a(a, sm.U[0], kLD16, 0, 8 * kb, g, t4);
+          mma_tf32(bK, a, b0, b1);
+          frag_a(a, sm.U[2], kLD16, 0, 8 * kb, g, t4);
+          mma_tf32(bB, a, b0, b1);
+          frag_b_t(b0, b1, sm.Ah, kLD64, j0, 8 * kb, g, t4);
+          frag_a(a, sm.U[1], kLD16, 0, 8 * kb, g, t4);
+          mma_tf32(bK, a, b0, b1);
+          frag_a(a, sm.U[3], kLD16, 0, 8 * kb, g, t4);
+          mma_tf32(bB, a, b0, b1);
+          frag_b_t(b0, b1, sm.Kt, kLD64, j0, 8 * kb, g, t4);
+          frag_a_t(a, sm.U[0], kLD16, 0, 8 * kb, g, t4);
+          mma_tf32(bR, a, b0, b1);
+          frag_a_t(a, sm.U[1], kLD16, 0, 8 * kb, g, t4);
+          mma_tf32(bA, a, b0, b1);
+          frag_b_t(b0, b1, sm.Bt, kLD64, j0, 8 * kb, g, t4);
+          frag_a_t(a, sm.U[2], kLD16, 0, 8 * kb, g, t4);
+          mma_tf32(bR, a, b0, b1);
+          frag_a_t(a, sm.U[3], kLD16, 0, 8 * kb, g, t4);
+          mma_tf32(bA, a, b0, b1);
+        }
+        const __nv_bfloat16* rs = sm.raw[st][0];
+        float dr[4], dk[4], db[4], da[4], x[4], ada[4];
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          const int t = g + 8 * h, col = j0 + 2 * t4;
+          const float2 c = *reinterpret_cast<const float2*>(sm.cS + t * kN + col);
+          const float2 ic = *reinterpret_cast<const float2*>(sm.icS + t * kN + col);
+          const float2 cp = t ? *reinterpret_cast<const float2*>(sm.cS + (t - 1) * kN + col) : make_float2(1.f, 1.f);
+          const float2 r = bf2(rs + V_R * kTile + t * kN + col), k = bf2(rs + V_K * kTile + t * kN + col);
+          const float2 b = bf2(rs + V_B * kTile + t * kN + col), a = bf2(rs + V_A * kTile + t * kN + col);
+          const float cv[2] = {c.x, c.y}, icv[2] = {ic.x, ic.y}, cpv[2] = {cp.x, cp.y};
+          const float rv[2] = {r.x, r.y}, kv[2] = {k.x, k.y}, bv[2] = {b.x, b.y}, av[2] = {a.x, a.y};
+#pragma unroll
+          for (int e = 0; e < 2; ++e) {
+            const int q = 2 * h + e;
+            dr[q] = bR[q] * cv[e];
+            dk[q] = bK[q] * icv[e];
+            db[q] = bB[q] * icv[e];
+            da[q] = bA[q] * cpv[e];
+            ada[q] = av[e] * da[q];
+            x[q] = rv[e] * dr[q] - kv[e] * dk[q] - bv[e] * db[q] + ada[q];
+          }
+        }
+        // w dw from the identity, anchored where fewer terms are summed:
+        // rows t < 8: colsum(next carry o S0) - sum_{u<t} x(u) - a(t) da(t);
+        // rows t >= 8: sum_{u>=t} x(u) - a(t) da(t) + colsum(Gc o S(L)).
+        float dw[4];
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          float hi2 = x[2 + e], lo = x[e];
+#pragma unroll
+          for (int d = 1; d < 8; d <<= 1) {
+            const float oh = __shfl_down_sync(0xffffffffu, hi2, 4 * d);
+            const float ol = __shfl_up_sync(0xffffffffu, lo, 4 * d);
+            if (g + d < 8) hi2 += oh;
+            if (g >= d) lo += ol;
+          }
+          const int col = j0 + 2 * t4 + e;
+          const float start = sm.spart[0][col] + sm.spart[1][col] + sm.spart[2][col] + sm.spart[3][col];
+          const float2 w0 = bf2(rs + V_W * kTile + g * kN + j0 + 2 * t4);
+          const float2 w1 = bf2(rs + V_W * kTile + (g + 8) * kN + j0 + 2 * t4);
+          dw[e] = (start - (lo - x[e]) - ada[e]) / (e ? w0.y : w0.x);
+          dw[2 + e] = (hi2 - ada[2 + e] + sm.bnd[col]) / (e ? w1.y : w1.x);
+        }
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          const int t = g + 8 * h;
+          if (t < len) {
+            const size_t off = o.base + (size_t)t * vstep + j0 + 2 * t4;
+            *reinterpret_cast<float2*>(args.dr + off) = make_float2(dr[2 * h], dr[2 * h + 1]);
+            *reinterpret_cast<float2*>(args.dk + off) = make_float2(dk[2 * h], dk[2 * h + 1]);
+            *reinterpret_cast<float2*>(args.db + off) = make_float2(db[2 * h], db[2 * h + 1]);
+            *reinterpret_cast<float2*>(args.da + off) = make_float2(da[2 * h], da[2 * h + 1]);
+            *reinterpret_cast<float2*>(args.dw + off) = make_float2(dw[2 * h], dw[2 * h + 1]);
+          }
+        }
+      }
+    }
+    // stage st is free; refill it with the chunk of visit m + kStages
+    if (__syncthreads_or(sm.abort_flag)) {
+      aborted = true;
+      break;
+    }
+    if (tid == 128 && m + kStages < nchunks) {
+      fence_proxy_async_smem();
+      issue(m + kStages);
+      issued = m + kStages + 1;
+    }
+  }
+  if (aborted) {
+    if (tid == 128)
+      for (int mm = waited; mm < issued; ++mm)
+        mbar_wait_bounded(nullptr, &sm.full[mm % kStages], (mm / kStages) & 1, 200000000ull);
+    if (!is_prep) cp_async_wait_all();
+    __syncthreads();
+    return;
+  }
+  if (!is_prep && args.dS_init) {
+    float* dst = args.dS_init + (size_t)head * kN * kN;
+#pragma unroll
+    for (int nt = 0; nt < 8; ++nt) {
+      const int col = 8 * nt + 2 * t4;
+      *reinterpret_cast<float2*>(dst + (i0 + g) * kN + col) = make_float2(G[nt][0], G[nt][1]);
+      *reinterpret_cast<float2*>(dst + (i0 + g + 8) * kN + col) = make_float2(G[nt][2], G[nt][3]);
+    }
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_bwd3(const BwdArgs& args, cudaStream_t stream) {
+  const size_t smem = sizeof(Bwd3Smem);
+  cudaError_t e = cudaFuncSetAttribute(wkv7_bwd3_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  wkv7_bwd3_kernel<<<(unsigned)(args.B * args.H), kThreads, smem, stream>>>(args);
+  return cudaGetLastError();
+}
+
+}  // namespace wkv7

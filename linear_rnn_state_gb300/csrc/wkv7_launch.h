@@ -49,6 +49,8 @@ cudaError_t launch_fwd2(const FwdArgs& args, bool bf16, int N, cudaStream_t stre
 // Chunked tensor-core forward: bf16 inputs, N = 64, checkpoints (if any) at a
 // multiple of its 16-step chunk.
 cudaError_t launch_fwd3(const FwdArgs& args, cudaStream_t stream);
+// Chunked tensor-core backward: bf16 inputs, N = 64, checkpoints every 16 steps.
+cudaError_t launch_bwd3(const BwdArgs& args, cudaStream_t stream);
 constexpr int kChunk = 16;
 inline bool use_chunked(bool bf16, int N, int C) { return bf16 && N == 64 && C % kChunk == 0; }
 cudaError_t launch_bwd(const BwdArgs& args, bool bf16, int N, cudaStream_t stream);

@@ -56,6 +56,35 @@ __device__ __forceinline__ void frag_b(uint32_t& b0, uint32_t& b1, const float* 
   b1 = __float_as_uint(v.y);
 }
 
+// A fragment as frag_a, from fp32 values that still need rounding to tf32.
+__device__ __forceinline__ void frag_a_r(uint32_t (&a)[4], const float* m, int ld, int r0, int k0, int g, int t) {
+  const float2 lo = *reinterpret_cast<const float2*>(m + (r0 + g) * ld + k0 + 2 * t);
+  const float2 hi = *reinterpret_cast<const float2*>(m + (r0 + g + 8) * ld + k0 + 2 * t);
+  a[0] = tf32_bits(lo.x);
+  a[2] = tf32_bits(lo.y);
+  a[1] = tf32_bits(hi.x);
+  a[3] = tf32_bits(hi.y);
+}
+
+// A fragment of A[m][k] read from storage laid out [k][m] (scalar loads),
+// rounded to tf32.
+__device__ __forceinline__ void frag_a_t(uint32_t (&a)[4], const float* m, int ld, int m0, int k0, int g, int t) {
+  const float* p = m + (k0 + 2 * t) * ld + m0 + g;
+  a[0] = tf32_bits(p[0]);
+  a[2] = tf32_bits(p[ld]);
+  a[1] = tf32_bits(p[8]);
+  a[3] = tf32_bits(p[ld + 8]);
+}
+
+// B fragment of B[k][n] read from storage laid out [k][n] (scalar loads),
+// rounded to tf32.
+__device__ __forceinline__ void frag_b_t(uint32_t& b0, uint32_t& b1, const float* m, int ld, int n0, int k0, int g,
+                                         int t) {
+  const float* p = m + (k0 + 2 * t) * ld + n0 + g;
+  b0 = tf32_bits(p[0]);
+  b1 = tf32_bits(p[ld]);
+}
+
 // Accumulator tile -> A fragment over the same columns (rounded to tf32).
 __device__ __forceinline__ void c2a(uint32_t (&a)[4], const float (&c)[4]) {
   a[0] = tf32_bits(c[0]);
@@ -65,6 +94,15 @@ __device__ __forceinline__ void c2a(uint32_t (&a)[4], const float (&c)[4]) {
 }
 
 __device__ __forceinline__ void zero4(float (&c)[4]) { c[0] = c[1] = c[2] = c[3] = 0.f; }
+
+// 16-byte asynchronous copy global -> shared (both addresses 16-byte aligned).
+__device__ __forceinline__ void cp_async16(void* dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(static_cast<uint32_t>(__cvta_generic_to_shared(dst))),
+               "l"(src)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
 
 // Named barrier over `count` threads (a multiple of 32).
 __device__ __forceinline__ void named_bar(int id, int count) {
