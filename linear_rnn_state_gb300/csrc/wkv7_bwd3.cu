@@ -48,8 +48,9 @@ namespace wkv7 {
 namespace {
 
 constexpr int kN = 64, kL = 16;
-constexpr int kLD64 = 72;  // row stride (floats) of 64-wide operands
+constexpr int kLD64 = 72;  // row stride (floats) of 64-wide operands read along k
 constexpr int kLD16 = 24;  // row stride of 16-wide operands
+constexpr int kLDT = 68;   // row stride of the carry, read only transposed
 constexpr int kStages = 3;
 constexpr int kThreads = 256;
 constexpr int kTile = kL * kN;
@@ -61,7 +62,8 @@ struct Bwd3Smem {
   float Ah[kL * kLD64], Rh[kL * kLD64], Kt[kL * kLD64], Bt[kL * kLD64];
   float Kb[kL * kLD64], Bb[kL * kLD64], Vs[kL * kLD64], DYs[kL * kLD64];
   float cS[kTile], icS[kTile];  // c(t) and 1/c(t), fp32 [t][j]
-  float cL[kN], bnd[kN], bpart[kN];
+  float cL[kN];
+  float bpart[4][kN];  // per state warp: column sums of (carry o S(L)) over its rows
   float spart[4][kN];  // per state warp: column sums of (next carry o S0) over its rows
   float M[4][kL * kLD16];  // Mka, Mba (strictly lower), Mkr, Mbr (lower)   [t][s]
   float Tinv[kL * kLD16];  // (I - Mba)^-1                                    [t][s]
@@ -69,7 +71,7 @@ struct Bwd3Smem {
   // (their transposes are the tril(...) factors); direct chunks reuse it
   float U[4][kL * kLD16];
   float SAs[kL * kLD64], DSAs[kL * kLD64];  // sa(t), dsa(t) [t][i] (tf32)
-  float GcS[kN * kLD64];                    // carry at the chunk end [i][j]
+  float GcS[kN * kLDT];                     // carry at the chunk end [i][j] (tf32)
   float S0s[3][kN * kLD64];                 // checkpoints [i][j]
   float dvs[kTile];                         // dv of the chunk [t][i]
   uint64_t full[kStages];
@@ -352,11 +354,24 @@ __global__ void __launch_bounds__(kThreads, 1) wkv7_bwd3_kernel(const __grid_con
     if (!is_prep) {
       cp_async_wait_all();
       if (n > 0) fetch_ckpt(n - 1);
+      // carry as a tf32 operand, and this warp's share of colsum(Gc o S(L))
+      // (S(L) = the next chunk's checkpoint; Gc = 0 after the last chunk)
+      const float* SL = sm.S0s[(n + 1) % 3];
 #pragma unroll
       for (int nt = 0; nt < 8; ++nt) {
         const int col = 8 * nt + 2 * t4;
-        *reinterpret_cast<float2*>(sm.GcS + (i0 + g) * kLD64 + col) = make_float2(G[nt][0], G[nt][1]);
-        *reinterpret_cast<float2*>(sm.GcS + (i0 + g + 8) * kLD64 + col) = make_float2(G[nt][2], G[nt][3]);
+        *reinterpret_cast<float2*>(sm.GcS + (i0 + g) * kLDT + col) = make_float2(tf32r(G[nt][0]), tf32r(G[nt][1]));
+        *reinterpret_cast<float2*>(sm.GcS + (i0 + g + 8) * kLDT + col) = make_float2(tf32r(G[nt][2]), tf32r(G[nt][3]));
+        float p0 = 0.f, p1 = 0.f;
+        if (m > 0) {
+          const float2 s_lo = *reinterpret_cast<const float2*>(SL + (i0 + g) * kLD64 + col);
+          const float2 s_hi = *reinterpret_cast<const float2*>(SL + (i0 + g + 8) * kLD64 + col);
+          p0 = fmaf(G[nt][0], s_lo.x, G[nt][2] * s_hi.x);
+          p1 = fmaf(G[nt][1], s_lo.y, G[nt][3] * s_hi.y);
+        }
+        p0 = col_sum(p0);
+        p1 = col_sum(p1);
+        if (g == 0) *reinterpret_cast<float2*>(sm.bpart[warp] + col) = make_float2(p0, p1);
       }
     } else {
       const bool ok = mbar_wait_bounded(args.status, &sm.full[st], (m / kStages) & 1);
@@ -541,18 +556,6 @@ __global__ void __launch_bounds__(kThreads, 1) wkv7_bwd3_kernel(const __grid_con
                   *reinterpret_cast<const float4*>(sm.dvs + t * kN + 4 * p);
           }
         }
-      } else {
-        // boundary term colsum(Gc o S(L)); zero for the last chunk (Gc = 0)
-        const int j = ptid & 63, half = ptid >> 6;
-        float x = 0.f;
-        if (n + 1 < nchunks) {
-          const float* SL = sm.S0s[(n + 1) % 3];
-#pragma unroll 8
-          for (int i = 32 * half; i < 32 * half + 32; ++i) x = fmaf(sm.GcS[i * kLD64 + j], SL[i * kLD64 + j], x);
-        }
-        if (half) sm.bpart[j] = x;
-        named_bar(1, 128);
-        if (!half) sm.bnd[j] = x + sm.bpart[j];
       }
       __syncthreads();
       // ---- D: remaining L x L products (prep warps); column products of every warp
@@ -574,8 +577,8 @@ __global__ void __launch_bounds__(kThreads, 1) wkv7_bwd3_kernel(const __grid_con
         frag_a(aSA, sm.SAs, kLD64, 0, 8 * kb, g, t4);
         frag_a(aDY, sm.DYs, kLD64, 0, 8 * kb, g, t4);
         frag_a(aDSA, sm.DSAs, kLD64, 0, 8 * kb, g, t4);
-        frag_b_t(b0, b1, sm.GcS, kLD64, j0, 8 * kb, g, t4);
-        frag_b_t(c0, c1, S0, kLD64, j0, 8 * kb, g, t4);
+        frag_b_t(b0, b1, sm.GcS, kLDT, j0, 8 * kb, g, t4);
+        frag_b_t_r(c0, c1, S0, kLD64, j0, 8 * kb, g, t4);
         mma_tf32(bK, aV, b0, b1);
         mma_tf32(bB, aSA, b0, b1);
         mma_tf32(bR, aDY, c0, c1);
@@ -658,8 +661,9 @@ __global__ void __launch_bounds__(kThreads, 1) wkv7_bwd3_kernel(const __grid_con
           const float start = sm.spart[0][col] + sm.spart[1][col] + sm.spart[2][col] + sm.spart[3][col];
           const float2 w0 = bf2(rs + V_W * kTile + g * kN + j0 + 2 * t4);
           const float2 w1 = bf2(rs + V_W * kTile + (g + 8) * kN + j0 + 2 * t4);
-          dw[e] = (start - (lo - x[e]) - ada[e]) / (e ? w0.y : w0.x);
-          dw[2 + e] = (hi2 - ada[2 + e] + sm.bnd[col]) / (e ? w1.y : w1.x);
+          dw[e] = (start - (lo - x[e]) - ada[e]) * rcp_approx(e ? w0.y : w0.x);
+          const float bnd = sm.bpart[0][col] + sm.bpart[1][col] + sm.bpart[2][col] + sm.bpart[3][col];
+          dw[2 + e] = (hi2 - ada[2 + e] + bnd) * rcp_approx(e ? w1.y : w1.x);
         }
 #pragma unroll
         for (int h = 0; h < 2; ++h) {

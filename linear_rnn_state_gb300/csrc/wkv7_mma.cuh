@@ -1,7 +1,11 @@
 // Warp-level tf32 tensor-core helpers for the chunked WKV7 kernels.
 //
 // Every product uses mma.sync m16n8k8 (tf32 inputs, fp32 accumulation) with
-// one fixed fragment convention. Within each 8-wide k block the hardware
+// one fixed fragment convention. Operands in shared memory use row strides
+// of 72 or 24 floats (= 8 mod 32): the float2 loads along k of each
+// half-warp then touch every bank once. A matrix read only transposed
+// (scalar loads down a column pair) uses 68 (= 4 mod 16) instead, which keeps
+// those loads conflict-free. Within each 8-wide k block the hardware
 // k slot q of lane (g = lane/4, t = lane%4) is bound to physical column
 //   slot t -> 2t,  slot t+4 -> 2t+1,
 // in both operands (the sum over k is order-free). Then
@@ -66,20 +70,28 @@ __device__ __forceinline__ void frag_a_r(uint32_t (&a)[4], const float* m, int l
   a[3] = tf32_bits(hi.y);
 }
 
-// A fragment of A[m][k] read from storage laid out [k][m] (scalar loads),
-// rounded to tf32.
+// A fragment of A[m][k] read from storage laid out [k][m] (scalar loads;
+// tf32 values).
 __device__ __forceinline__ void frag_a_t(uint32_t (&a)[4], const float* m, int ld, int m0, int k0, int g, int t) {
   const float* p = m + (k0 + 2 * t) * ld + m0 + g;
-  a[0] = tf32_bits(p[0]);
-  a[2] = tf32_bits(p[ld]);
-  a[1] = tf32_bits(p[8]);
-  a[3] = tf32_bits(p[ld + 8]);
+  a[0] = __float_as_uint(p[0]);
+  a[2] = __float_as_uint(p[ld]);
+  a[1] = __float_as_uint(p[8]);
+  a[3] = __float_as_uint(p[ld + 8]);
 }
 
-// B fragment of B[k][n] read from storage laid out [k][n] (scalar loads),
-// rounded to tf32.
+// B fragment of B[k][n] read from storage laid out [k][n] (scalar loads;
+// tf32 values).
 __device__ __forceinline__ void frag_b_t(uint32_t& b0, uint32_t& b1, const float* m, int ld, int n0, int k0, int g,
                                          int t) {
+  const float* p = m + (k0 + 2 * t) * ld + n0 + g;
+  b0 = __float_as_uint(p[0]);
+  b1 = __float_as_uint(p[ld]);
+}
+
+// frag_b_t from fp32 values that still need rounding to tf32.
+__device__ __forceinline__ void frag_b_t_r(uint32_t& b0, uint32_t& b1, const float* m, int ld, int n0, int k0, int g,
+                                           int t) {
   const float* p = m + (k0 + 2 * t) * ld + n0 + g;
   b0 = tf32_bits(p[0]);
   b1 = tf32_bits(p[ld]);
