@@ -33,8 +33,8 @@ FP32_LANES_PER_SM = 128  # Blackwell SM: 4 partitions x 32 FP32 lanes
 TRAFFIC = {
     "kernel": "wkv7_bwd3_kernel",
     "sources": ("wkv7_bwd3.cu", "wkv7_common.cuh", "wkv7_scaled.cuh", "wkv7_mma.cuh", "wkv7_launch.h"),
-    "sha256": "4d02d49363ab928dcfad8694561f71071cbb9b5644b48d90d1bc6297f8a584a2",
-    "bytes_per_token_head": 412.262656e6 / 131072,
+    "sha256": "8a78e1c25c92002105b001afecd1c4bf3ee4f52db8ac7935e74a5875f0049044",
+    "bytes_per_token_head": (251.771904e6 + 163.0528e6) / 131072,
 }
 
 
@@ -359,13 +359,18 @@ def _report(args, wl, world, B, T, H, N, C, bf16, ms, fwd_ms, bwd_ms, e2e, ckpt,
     line = {
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "vs_baseline": None, "dtype": "tf32" if (bf16 and N == 64) else "f32", "data": "synthetic",
+        "arithmetic": ("tf32 tensor-core products with fp32 accumulation; fp32 state, carry and element-wise math"
+                       if (bf16 and N == 64) else "fp32 throughout") + "; inputs, dy and y stored in " + wl.storage,
         "config": {"workload": wl.name if T == wl.T else f"{wl.name} (T={T})", "B": B, "T": T, "H": H, "N": N, "storage": wl.storage, "ckpt_every": C,
                    "l2": "no flush: inputs, checkpoints and gradients (%.1f GB) exceed the 129 MB L2"
                          % ((7 * BTH * N * (2 if bf16 else 4) + ckpt.numel() * 4 + 6 * BTH * N * 4) / 1e9)},
         "fwd_ms": fwd_ms, "bwd_ms": bwd_ms, "step_roofline_frac": t_roof / (ms * 1e-3),
         "roofline": {"bound": "alu", "achieved": achieved / 1e12, "peak": peak_flops / 1e12, "unit": "TFLOP/s",
                      "frac": achieved / peak_flops, "traffic": measured_traffic(BTH), "kernel": TRAFFIC["kernel"],
+                     "note": "algorithmic FLOP of the recurrence (24 N^2 per token-head, backward) against the FP32 "
+                             "CUDA-core peak, the roofline the metric names; the kernel forms them as tf32 "
+                             "tensor-core products",
                      "peak_source": f"{sms} SMs x {FP32_LANES_PER_SM} FP32 lanes x 2 x {peaks['sm_max_mhz']:.0f} MHz",
                      "hbm_gbs_achieved": b_bytes * BTH / (bwd_ms * 1e-3) / 1e9, "hbm_peak_gbs": peaks["hbm_gbs"]},
         "e2e": None if e2e is None else {
