@@ -32,12 +32,14 @@
 // state before the step is. All products run on tf32 tensor cores
 // (mma.sync m16n8k8) with fp32 accumulation.
 //
-// One CTA per (b, h), eight warps, chunks in reverse order. Warps 0..3
-// ("state warps") own 16 rows i of the carry Gc as accumulator tiles and
-// produce sa, dsa, dv and the next carry; warps 4..7 ("prep warps") form the
-// scaled operands (TMA ring of r, w, k, v, a, b, dy), the L x L products and
-// T; then all eight warps produce dr, dk, db, da, dw for 8 columns each.
-// Checkpoints arrive by cp.async one chunk ahead. A chunk whose decays leave
+// One CTA per (b, h), eight warps, chunks in reverse order, two-stage
+// software pipeline. While warps 0..3 ("state warps", each owning 16 rows i
+// of the carry Gc as accumulator tiles) run chunk n's carry chain (sa, dsa,
+// the next carry), warps 4..7 ("prep warps") form chunk n-1's scaled operands
+// (TMA ring of r, w, k, v, a, b, dy), its L x L products, T and triu(V DY^T)
+// in the other half of a double-buffered operand block. Then all eight warps
+// produce chunk n's dv, dr, dk, db, da, dw, 8 columns each. Checkpoints
+// arrive by cp.async one chunk ahead. A chunk whose decays leave
 // [1/16, 16] (or hold a NaN) is run step by step in the direct form, fp32,
 // recomputing each S_prev from the checkpoint.
 #include "wkv7_launch.h"
@@ -56,26 +58,33 @@ constexpr int kThreads = 256;
 constexpr int kTile = kL * kN;
 enum { V_R = 0, V_W = 1, V_K = 2, V_V = 3, V_A = 4, V_B = 5, V_DY = 6 };
 
+// Operands of one chunk, formed by the prep warps (tf32 values unless noted).
+struct OpB {
+  float Ah[kL * kLD64], Rh[kL * kLD64], Kt[kL * kLD64], Bt[kL * kLD64];  // [t][j]
+  float Kb[kL * kLD64], Bb[kL * kLD64], Vs[kL * kLD64], DYs[kL * kLD64];  // [t][j], V and DY [t][i]
+  float cS[kTile], icS[kTile];  // c(t) and 1/c(t), fp32 [t][j]
+  float cL[kN];                 // fp32
+  float M[4][kL * kLD16];       // Mka, Mba (strictly lower), Mkr, Mbr (lower)   [t][s]
+  float Tinv[kL * kLD16];       // (I - Mba)^-1                                  [t][s]
+  float U0[kL * kLD16];         // triu(V DY^T)                                 [t][s]
+  int unsafe;
+  int pad_[3];
+};
+
 struct Bwd3Smem {
   __nv_bfloat16 raw[kStages][7][kTile];  // r, w, k, v, a, b, dy of one chunk per stage
-  // scaled operands of the chunk, tf32 values, [t][j] (V and DY: [t][i])
-  float Ah[kL * kLD64], Rh[kL * kLD64], Kt[kL * kLD64], Bt[kL * kLD64];
-  float Kb[kL * kLD64], Bb[kL * kLD64], Vs[kL * kLD64], DYs[kL * kLD64];
-  float cS[kTile], icS[kTile];  // c(t) and 1/c(t), fp32 [t][j]
-  float cL[kN];
-  float bpart[4][kN];  // per state warp: column sums of (carry o S(L)) over its rows
-  float spart[4][kN];  // per state warp: column sums of (next carry o S0) over its rows
-  float M[4][kL * kLD16];  // Mka, Mba (strictly lower), Mkr, Mbr (lower)   [t][s]
-  float Tinv[kL * kLD16];  // (I - Mba)^-1                                    [t][s]
-  // triu(V DY^T), triu(V DSA^T, 1), triu(SA DY^T), triu(SA DSA^T, 1)      [t][s]
-  // (their transposes are the tril(...) factors); direct chunks reuse it
-  float U[4][kL * kLD16];
+  OpB op[2];
+  // triu(V DSA^T, 1), triu(SA DY^T), triu(SA DSA^T, 1) of the chunk in flight [t][s]
+  // (with triu(V DY^T) their transposes are the tril(...) factors)
+  float U[3][kL * kLD16];
   float SAs[kL * kLD64], DSAs[kL * kLD64];  // sa(t), dsa(t) [t][i] (tf32)
   float GcS[kN * kLDT];                     // carry at the chunk end [i][j] (tf32)
-  float S0s[3][kN * kLD64];                 // checkpoints [i][j]
-  float dvs[kTile];                         // dv of the chunk [t][i]
+  float S0s[2][kN * kLD64];                 // checkpoints [i][j]
+  float bpart[4][kN];  // per state warp: column sums of (carry o S(L)) over its rows
+  float spart[4][kN];  // per state warp: column sums of (next carry o S0) over its rows
+  float red[4 * 5 * kN];  // direct chunks: per-warp column partials
   uint64_t full[kStages];
-  int unsafe, abort_flag;
+  int abort_flag;
 };
 
 __device__ __forceinline__ float bf(const __nv_bfloat16* p) { return __bfloat162float(*p); }
@@ -86,8 +95,7 @@ __device__ __forceinline__ float2 bf2(const __nv_bfloat16* p) {
 // Scaled operands of a chunk. 128 prep threads; thread (j, half) forms
 // column j of steps 8*half .. 8*half+7. Returns (uniformly over the prep
 // warps) whether some decay leaves the range of the scaled form.
-__device__ bool prep_bwd(Bwd3Smem& sm, int stage, int len, int ptid) {
-  const __nv_bfloat16* rs = sm.raw[stage][0];
+__device__ bool prep_bwd(const __nv_bfloat16* rs, OpB& op, int len, int ptid) {
   const int j = ptid & 63, half = ptid >> 6;
   float wm[8], wo[8];
   const int tm = 8 * half, to = 8 - tm;
@@ -109,7 +117,7 @@ __device__ bool prep_bwd(Bwd3Smem& sm, int stage, int len, int ptid) {
   }
   const float cL = half ? po * pm : pm * po;
   float c = half ? po : 1.f;
-  if (half == 0) sm.cL[j] = cL;
+  if (half == 0) op.cL[j] = cL;
 #pragma unroll
   for (int e = 0; e < 8; ++e) {
     const int t = tm + e;
@@ -119,17 +127,17 @@ __device__ bool prep_bwd(Bwd3Smem& sm, int stage, int len, int ptid) {
     const int o = t * kN + j, q = t * kLD64 + j;
     const float a = bf(rs + V_A * kTile + o), r = bf(rs + V_R * kTile + o);
     const float k = bf(rs + V_K * kTile + o), b = bf(rs + V_B * kTile + o);
-    sm.Ah[q] = tf32r(a * cprev);
-    sm.Rh[q] = tf32r(r * c);
-    sm.Kt[q] = tf32r(k * ic);
-    sm.Bt[q] = tf32r(b * ic);
+    op.Ah[q] = tf32r(a * cprev);
+    op.Rh[q] = tf32r(r * c);
+    op.Kt[q] = tf32r(k * ic);
+    op.Bt[q] = tf32r(b * ic);
     const float s = cL * ic;
-    sm.Kb[q] = tf32r(k * s);
-    sm.Bb[q] = tf32r(b * s);
-    sm.Vs[q] = tf32r(bf(rs + V_V * kTile + o));
-    sm.DYs[q] = tf32r(bf(rs + V_DY * kTile + o));
-    sm.cS[o] = c;
-    sm.icS[o] = ic;
+    op.Kb[q] = tf32r(k * s);
+    op.Bb[q] = tf32r(b * s);
+    op.Vs[q] = tf32r(bf(rs + V_V * kTile + o));
+    op.DYs[q] = tf32r(bf(rs + V_DY * kTile + o));
+    op.cS[o] = c;
+    op.icS[o] = ic;
   }
   return false;
 }
@@ -171,6 +179,59 @@ __device__ __forceinline__ void store_masked(const float (&acc)[2][4], float* ds
     }
 }
 
+// Front half of a chunk (prep warps): wait for its inputs, form the operands,
+// the masked L x L products, T and triu(V DY^T). Returns false on a timeout.
+__device__ bool front_chunk(Bwd3Smem& sm, OpB& op, const __nv_bfloat16* rs, uint64_t* bar, uint32_t parity, int len,
+                            unsigned* status) {
+  const int ptid = threadIdx.x - 128, pw = ptid >> 5, lane = threadIdx.x & 31, g = lane >> 2, t4 = lane & 3;
+  const bool ok = mbar_wait_bounded(status, bar, parity);
+  if (named_bar_or(1, 128, !ok)) {
+    if (ptid == 0) sm.abort_flag = 1;
+    return false;
+  }
+  const bool unsafe = prep_bwd(rs, op, len, ptid);
+  if (ptid == 0) op.unsafe = unsafe;
+  if (unsafe) return true;
+  named_bar(1, 128);
+  float acc[2][4];
+  const int mt = pw >> 1, nb = pw & 1;
+  zero4(acc[0]);
+  zero4(acc[1]);
+#pragma unroll
+  for (int kb = 0; kb < kN / 8; ++kb) {
+    uint32_t a[4];
+    frag_a(a, mt ? op.Rh : op.Ah, kLD64, 0, 8 * kb, g, t4);
+#pragma unroll
+    for (int nt = 0; nt < 2; ++nt) {
+      uint32_t b0, b1;
+      frag_b(b0, b1, nb ? op.Bt : op.Kt, kLD64, 8 * nt, 8 * kb, g, t4);
+      mma_tf32(acc[nt], a, b0, b1);
+    }
+  }
+  store_masked(acc, op.M[pw], true, mt == 1, g, t4);
+  if (pw == 1) {  // T = (I - Mba)^-1, lane s < 16 owns column s
+    __syncwarp();
+    const float* Mba = op.M[1];
+    const int s = lane & 15;
+    float col[kL];
+#pragma unroll
+    for (int t = 0; t < kL; ++t) {
+      float x = t == s ? 1.f : 0.f;
+#pragma unroll
+      for (int u = 0; u < t; ++u) x = fmaf(Mba[t * kLD16 + u], col[u], x);
+      col[t] = x;
+    }
+    if (lane < 16) {
+#pragma unroll
+      for (int t = 0; t < kL; ++t) op.Tinv[t * kLD16 + s] = tf32r(col[t]);
+    }
+  } else if (pw == 2) {  // U0 = triu(V DY^T)
+    gram16(acc, op.Vs, op.DYs, g, t4);
+    store_masked(acc, op.U0, false, true, g, t4);
+  }
+  return true;
+}
+
 // --------------------------------------------------------- direct chunk ---
 // Step-by-step reverse scan of one chunk (state warps, fp32). G is the
 // carry in accumulator layout; S_prev of step t is recomputed from the
@@ -195,7 +256,7 @@ __device__ void direct_chunk_bwd(Bwd3Smem& sm, const float* S0, int stage, int l
                                  int warp, int lane) {
   const int g = lane >> 2, t4 = lane & 3, i0 = 16 * warp, tid = threadIdx.x;
   const __nv_bfloat16* rs = sm.raw[stage][0];
-  float* red = &sm.U[0][0];  // [4 warps][5][64]
+  float* red = sm.red;  // [4 warps][5][64]
   for (int t = len - 1; t >= 0; --t) {
     float sp[8][4];
 #pragma unroll
@@ -308,7 +369,7 @@ __global__ void __launch_bounds__(kThreads, 1) wkv7_bwd3_kernel(const __grid_con
   const int head = blockIdx.x, bi = head / H, hi = head % H;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, g = lane >> 2, t4 = lane & 3;
   const bool is_prep = warp >= 4;
-  const int ptid = tid - 128, pw = warp - 4;
+  const int pw = warp - 4;
   const int i0 = 16 * warp;  // state warps: rows of the carry
   const int nchunks = (T + kL - 1) / kL;
   constexpr int kStageBytes = 7 * kTile * 2;
@@ -320,10 +381,10 @@ __global__ void __launch_bounds__(kThreads, 1) wkv7_bwd3_kernel(const __grid_con
     mbar_arrive_expect_tx(&sm.full[st], kStageBytes);
     for (int v = 0; v < 7; ++v) tma_load_4d(sm.raw[st][v], &args.map[v], &sm.full[st], 0, hi, chunk * kL, bi);
   };
-  // state warps copy checkpoint `chunk` into S0s[chunk % 3] (padded rows)
+  // state warps copy checkpoint `chunk` into S0s[chunk % 2] (padded rows)
   auto fetch_ckpt = [&](int chunk) {
     const float* src = ck_head + (size_t)chunk * kN * kN;
-    float* dst = sm.S0s[chunk % 3];
+    float* dst = sm.S0s[chunk & 1];
 #pragma unroll
     for (int q = 0; q < 8; ++q) {
       const int idx = tid + 128 * q;  // 16-byte piece: row idx / 16, column 4 * (idx % 16)
@@ -347,16 +408,26 @@ __global__ void __launch_bounds__(kThreads, 1) wkv7_bwd3_kernel(const __grid_con
   int waited = 0, issued = min(kStages, nchunks);
   const size_t vstep = (size_t)H * kN;
   bool aborted = false;
-  for (int m = 0; m < nchunks; ++m) {
+  // front half of the first visited chunk
+  if (is_prep && nchunks > 0) {
+    const int n = nchunks - 1;
+    if (front_chunk(sm, sm.op[n & 1], sm.raw[0][0], &sm.full[0], 0, min(kL, T - n * kL), args.status)) waited = 1;
+  }
+  if (__syncthreads_or(sm.abort_flag)) aborted = true;
+
+  for (int m = 0; m < nchunks && !aborted; ++m) {
     const int n = nchunks - 1 - m, st = m % kStages, t0 = n * kL, len = min(kL, T - t0);
-    const float* S0 = sm.S0s[n % 3];
-    // ---- A: checkpoint and carry to shared memory; prep of the chunk's operands
+    OpB& op = sm.op[n & 1];
+    const float* S0 = sm.S0s[n & 1];
+    const bool unsafe = op.unsafe;
+    const Outs o{args.dr, args.dw, args.dk, args.dv, args.da, args.db, ((size_t)bi * T + t0) * vstep + (size_t)hi * kN,
+                 vstep};
+    // ================= P: carry chain of chunk n (state warps) || front half of chunk n-1 (prep warps)
     if (!is_prep) {
       cp_async_wait_all();
-      if (n > 0) fetch_ckpt(n - 1);
       // carry as a tf32 operand, and this warp's share of colsum(Gc o S(L))
       // (S(L) = the next chunk's checkpoint; Gc = 0 after the last chunk)
-      const float* SL = sm.S0s[(n + 1) % 3];
+      const float* SL = sm.S0s[(n + 1) & 1];
 #pragma unroll
       for (int nt = 0; nt < 8; ++nt) {
         const int col = 8 * nt + 2 * t4;
@@ -373,70 +444,16 @@ __global__ void __launch_bounds__(kThreads, 1) wkv7_bwd3_kernel(const __grid_con
         p1 = col_sum(p1);
         if (g == 0) *reinterpret_cast<float2*>(sm.bpart[warp] + col) = make_float2(p0, p1);
       }
-    } else {
-      const bool ok = mbar_wait_bounded(args.status, &sm.full[st], (m / kStages) & 1);
-      if (named_bar_or(1, 128, !ok)) {
-        if (ptid == 0) sm.abort_flag = 1;
+      named_bar(2, 128);  // S(L) read by every state warp before its buffer is refilled
+      if (n > 0) fetch_ckpt(n - 1);
+      if (unsafe) {
+        direct_chunk_bwd(sm, S0, st, len, o, G, warp, lane);
       } else {
-        waited = m + 1;
-        const bool unsafe = prep_bwd(sm, st, len, ptid);
-        if (ptid == 0) sm.unsafe = unsafe;
-      }
-    }
-    if (__syncthreads_or(sm.abort_flag)) {
-      aborted = true;
-      break;
-    }
-    const Outs o{args.dr, args.dw, args.dk, args.dv, args.da, args.db, ((size_t)bi * T + t0) * vstep + (size_t)hi * kN,
-                 vstep};
-    if (sm.unsafe) {
-      if (!is_prep) direct_chunk_bwd(sm, S0, st, len, o, G, warp, lane);
-    } else {
-      // ---- B: L x L products and T (prep warps); first products of the state warps
-      float RSA[2][4], RDSA[2][4], RDV[2][4];
-      if (is_prep) {
-        float acc[2][4];
-        const int mt = pw >> 1, nb = pw & 1;
-        zero4(acc[0]);
-        zero4(acc[1]);
-#pragma unroll
-        for (int kb = 0; kb < kN / 8; ++kb) {
-          uint32_t a[4];
-          frag_a(a, mt ? sm.Rh : sm.Ah, kLD64, 0, 8 * kb, g, t4);
-#pragma unroll
-          for (int nt = 0; nt < 2; ++nt) {
-            uint32_t b0, b1;
-            frag_b(b0, b1, nb ? sm.Bt : sm.Kt, kLD64, 8 * nt, 8 * kb, g, t4);
-            mma_tf32(acc[nt], a, b0, b1);
-          }
-        }
-        store_masked(acc, sm.M[pw], true, mt == 1, g, t4);
-        if (pw == 1) {  // T = (I - Mba)^-1, lane s < 16 owns column s
-          __syncwarp();
-          const float* Mba = sm.M[1];
-          const int s = lane & 15;
-          float col[kL];
-#pragma unroll
-          for (int t = 0; t < kL; ++t) {
-            float x = t == s ? 1.f : 0.f;
-#pragma unroll
-            for (int u = 0; u < t; ++u) x = fmaf(Mba[t * kLD16 + u], col[u], x);
-            col[t] = x;
-          }
-          if (lane < 16) {
-#pragma unroll
-            for (int t = 0; t < kL; ++t) sm.Tinv[t * kLD16 + s] = tf32r(col[t]);
-          }
-        } else if (pw == 2) {  // U0 = triu(V DY^T)
-          gram16(acc, sm.Vs, sm.DYs, g, t4);
-          store_masked(acc, sm.U[0], false, true, g, t4);
-        }
-      } else {
+        float RSA[2][4], RDSA[2][4];
 #pragma unroll
         for (int q = 0; q < 2; ++q) {
           zero4(RSA[q]);
           zero4(RDSA[q]);
-          zero4(RDV[q]);
         }
 #pragma unroll
         for (int kb = 0; kb < 8; ++kb) {
@@ -446,32 +463,24 @@ __global__ void __launch_bounds__(kThreads, 1) wkv7_bwd3_kernel(const __grid_con
 #pragma unroll
           for (int q = 0; q < 2; ++q) {
             uint32_t b0, b1;
-            frag_b(b0, b1, sm.Ah, kLD64, 8 * q, 8 * kb, g, t4);
+            frag_b(b0, b1, op.Ah, kLD64, 8 * q, 8 * kb, g, t4);
             mma_tf32(RSA[q], aS, b0, b1);
-            frag_b(b0, b1, sm.Bb, kLD64, 8 * q, 8 * kb, g, t4);
+            frag_b(b0, b1, op.Bb, kLD64, 8 * q, 8 * kb, g, t4);
             mma_tf32(RDSA[q], aG, b0, b1);
-            frag_b(b0, b1, sm.Kb, kLD64, 8 * q, 8 * kb, g, t4);
-            mma_tf32(RDV[q], aG, b0, b1);
           }
         }
-      }
-      __syncthreads();
-      // ---- C: sa, dsa, dv and the next carry (state warps); boundary term (prep warps)
-      if (!is_prep) {
         uint32_t aV[2][4], aD[2][4];
 #pragma unroll
         for (int kb = 0; kb < 2; ++kb) {
-          frag_a_t(aV[kb], sm.Vs, kLD64, i0, 8 * kb, g, t4);   // V^T
-          frag_a_t(aD[kb], sm.DYs, kLD64, i0, 8 * kb, g, t4);  // DY^T
+          frag_a_t(aV[kb], op.Vs, kLD64, i0, 8 * kb, g, t4);   // V^T
+          frag_a_t(aD[kb], op.DYs, kLD64, i0, 8 * kb, g, t4);  // DY^T
 #pragma unroll
           for (int q = 0; q < 2; ++q) {
             uint32_t b0, b1;
-            frag_b(b0, b1, sm.M[0], kLD16, 8 * q, 8 * kb, g, t4);  // + V^T Mka^T
+            frag_b(b0, b1, op.M[0], kLD16, 8 * q, 8 * kb, g, t4);  // + V^T Mka^T
             mma_tf32(RSA[q], aV[kb], b0, b1);
-            frag_b_t(b0, b1, sm.M[3], kLD16, 8 * q, 8 * kb, g, t4);  // + DY^T Mbr
+            frag_b_t(b0, b1, op.M[3], kLD16, 8 * q, 8 * kb, g, t4);  // + DY^T Mbr
             mma_tf32(RDSA[q], aD[kb], b0, b1);
-            frag_b_t(b0, b1, sm.M[2], kLD16, 8 * q, 8 * kb, g, t4);  // + DY^T Mkr
-            mma_tf32(RDV[q], aD[kb], b0, b1);
           }
         }
         float SA[2][4], DSA[2][4];
@@ -488,23 +497,15 @@ __global__ void __launch_bounds__(kThreads, 1) wkv7_bwd3_kernel(const __grid_con
 #pragma unroll
           for (int q = 0; q < 2; ++q) {
             uint32_t b0, b1;
-            frag_b(b0, b1, sm.Tinv, kLD16, 8 * q, 8 * kb, g, t4);  // SA^T = RSA T^T
+            frag_b(b0, b1, op.Tinv, kLD16, 8 * q, 8 * kb, g, t4);  // SA^T = RSA T^T
             mma_tf32(SA[q], a1, b0, b1);
-            frag_b_t(b0, b1, sm.Tinv, kLD16, 8 * q, 8 * kb, g, t4);  // DSA^T = RDSA T
+            frag_b_t(b0, b1, op.Tinv, kLD16, 8 * q, 8 * kb, g, t4);  // DSA^T = RDSA T
             mma_tf32(DSA[q], a2, b0, b1);
           }
         }
         uint32_t aDS[2][4];
         c2a(aDS[0], DSA[0]);
         c2a(aDS[1], DSA[1]);
-#pragma unroll
-        for (int kb = 0; kb < 2; ++kb)
-#pragma unroll
-          for (int q = 0; q < 2; ++q) {
-            uint32_t b0, b1;
-            frag_b_t(b0, b1, sm.M[0], kLD16, 8 * q, 8 * kb, g, t4);  // DV^T += DSA^T Mka
-            mma_tf32(RDV[q], aDS[kb], b0, b1);
-          }
 #pragma unroll
         for (int q = 0; q < 2; ++q)
 #pragma unroll
@@ -514,12 +515,11 @@ __global__ void __launch_bounds__(kThreads, 1) wkv7_bwd3_kernel(const __grid_con
               const int i = i0 + g + 8 * h, t = 8 * q + 2 * t4 + e;
               sm.SAs[t * kLD64 + i] = tf32r(SA[q][2 * h + e]);
               sm.DSAs[t * kLD64 + i] = tf32r(DSA[q][2 * h + e]);
-              sm.dvs[t * kN + i] = RDV[q][2 * h + e];
             }
         // next carry: Gc diag(c(L)) + DY^T R^ + DSA^T A^
 #pragma unroll
         for (int nt = 0; nt < 8; ++nt) {
-          const float2 cl = *reinterpret_cast<const float2*>(sm.cL + 8 * nt + 2 * t4);
+          const float2 cl = *reinterpret_cast<const float2*>(op.cL + 8 * nt + 2 * t4);
           G[nt][0] *= cl.x;
           G[nt][1] *= cl.y;
           G[nt][2] *= cl.x;
@@ -530,9 +530,9 @@ __global__ void __launch_bounds__(kThreads, 1) wkv7_bwd3_kernel(const __grid_con
 #pragma unroll
           for (int nt = 0; nt < 8; ++nt) {
             uint32_t b0, b1;
-            frag_b_t(b0, b1, sm.Rh, kLD64, 8 * nt, 8 * kb, g, t4);
+            frag_b_t(b0, b1, op.Rh, kLD64, 8 * nt, 8 * kb, g, t4);
             mma_tf32(G[nt], aD[kb], b0, b1);
-            frag_b_t(b0, b1, sm.Ah, kLD64, 8 * nt, 8 * kb, g, t4);
+            frag_b_t(b0, b1, op.Ah, kLD64, 8 * nt, 8 * kb, g, t4);
             mma_tf32(G[nt], aDS[kb], b0, b1);
           }
         // start anchor of the dw identity: colsum(next carry o S0), this warp's rows
@@ -545,24 +545,23 @@ __global__ void __launch_bounds__(kThreads, 1) wkv7_bwd3_kernel(const __grid_con
           const float p1 = col_sum(fmaf(G[nt][1], s_lo.y, G[nt][3] * s_hi.y));
           if (g == 0) *reinterpret_cast<float2*>(sm.spart[warp] + col) = make_float2(p0, p1);
         }
-        named_bar(2, 128);
-        if (args.dv) {
-          const int p = tid & 15;
-#pragma unroll
-          for (int rr = 0; rr < 2; ++rr) {
-            const int t = (tid >> 4) + 8 * rr;
-            if (t < len)
-              *reinterpret_cast<float4*>(args.dv + o.base + (size_t)t * vstep + 4 * p) =
-                  *reinterpret_cast<const float4*>(sm.dvs + t * kN + 4 * p);
-          }
-        }
       }
-      __syncthreads();
-      // ---- D: remaining L x L products (prep warps); column products of every warp
-      if (is_prep && pw < 3) {
+    } else if (n > 0) {
+      const int st1 = (m + 1) % kStages;
+      if (front_chunk(sm, sm.op[(n - 1) & 1], sm.raw[st1][0], &sm.full[st1], ((m + 1) / kStages) & 1,
+                      min(kL, T - (n - 1) * kL), args.status))
+        waited = m + 2;
+    }
+    if (__syncthreads_or(sm.abort_flag)) {
+      aborted = true;
+      break;
+    }
+    // ================= Q: outputs of chunk n (all warps, 8 columns each)
+    if (!unsafe) {
+      if (is_prep && pw < 3) {  // U1 = triu(V DSA^T, 1), U2 = triu(SA DY^T), U3 = triu(SA DSA^T, 1)
         float acc[2][4];
-        gram16(acc, pw == 0 ? sm.Vs : sm.SAs, pw == 1 ? sm.DYs : sm.DSAs, g, t4);
-        store_masked(acc, sm.U[pw + 1], false, pw == 1, g, t4);  // U1, U3 strictly upper; U2 with diagonal
+        gram16(acc, pw == 0 ? op.Vs : sm.SAs, pw == 1 ? op.DYs : sm.DSAs, g, t4);
+        store_masked(acc, sm.U[pw], false, pw == 1, g, t4);
       }
       const int j0 = 8 * warp;
       float bK[4], bB[4], bR[4], bA[4];
@@ -573,9 +572,9 @@ __global__ void __launch_bounds__(kThreads, 1) wkv7_bwd3_kernel(const __grid_con
 #pragma unroll
       for (int kb = 0; kb < 8; ++kb) {
         uint32_t aV[4], aSA[4], aDY[4], aDSA[4], b0, b1, c0, c1;
-        frag_a(aV, sm.Vs, kLD64, 0, 8 * kb, g, t4);
+        frag_a(aV, op.Vs, kLD64, 0, 8 * kb, g, t4);
         frag_a(aSA, sm.SAs, kLD64, 0, 8 * kb, g, t4);
-        frag_a(aDY, sm.DYs, kLD64, 0, 8 * kb, g, t4);
+        frag_a(aDY, op.DYs, kLD64, 0, 8 * kb, g, t4);
         frag_a(aDSA, sm.DSAs, kLD64, 0, 8 * kb, g, t4);
         frag_b_t(b0, b1, sm.GcS, kLDT, j0, 8 * kb, g, t4);
         frag_b_t_r(c0, c1, S0, kLD64, j0, 8 * kb, g, t4);
@@ -584,10 +583,39 @@ __global__ void __launch_bounds__(kThreads, 1) wkv7_bwd3_kernel(const __grid_con
         mma_tf32(bR, aDY, c0, c1);
         mma_tf32(bA, aDSA, c0, c1);
       }
-      __syncthreads();
-      // ---- E: triangular terms, scaling, dw, stores (columns j0 .. j0+7)
+      // dv (t x i, columns i = j0..j0+7) = Kb Gc^T + Mkr^T DY + Mka^T DSA
       {
-        const float2 cl = *reinterpret_cast<const float2*>(sm.cL + j0 + 2 * t4);
+        float bV[4];
+        zero4(bV);
+#pragma unroll
+        for (int kb = 0; kb < 8; ++kb) {
+          uint32_t a[4], b0, b1;
+          frag_a(a, op.Kb, kLD64, 0, 8 * kb, g, t4);
+          frag_b(b0, b1, sm.GcS, kLDT, j0, 8 * kb, g, t4);
+          mma_tf32(bV, a, b0, b1);
+        }
+#pragma unroll
+        for (int kb = 0; kb < 2; ++kb) {
+          uint32_t a[4], b0, b1;
+          frag_a_t(a, op.M[2], kLD16, 0, 8 * kb, g, t4);
+          frag_b_t(b0, b1, op.DYs, kLD64, j0, 8 * kb, g, t4);
+          mma_tf32(bV, a, b0, b1);
+          frag_a_t(a, op.M[0], kLD16, 0, 8 * kb, g, t4);
+          frag_b_t(b0, b1, sm.DSAs, kLD64, j0, 8 * kb, g, t4);
+          mma_tf32(bV, a, b0, b1);
+        }
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          const int t = g + 8 * h;
+          if (t < len)
+            *reinterpret_cast<float2*>(args.dv + o.base + (size_t)t * vstep + j0 + 2 * t4) =
+                make_float2(bV[2 * h], bV[2 * h + 1]);
+        }
+      }
+      __syncthreads();
+      // triangular terms, scaling, dw, stores (columns j0 .. j0+7)
+      {
+        const float2 cl = *reinterpret_cast<const float2*>(op.cL + j0 + 2 * t4);
         bK[0] *= cl.x;
         bK[1] *= cl.y;
         bK[2] *= cl.x;
@@ -596,28 +624,29 @@ __global__ void __launch_bounds__(kThreads, 1) wkv7_bwd3_kernel(const __grid_con
         bB[1] *= cl.y;
         bB[2] *= cl.x;
         bB[3] *= cl.y;
+        const float* Uq[4] = {op.U0, sm.U[0], sm.U[1], sm.U[2]};
 #pragma unroll
         for (int kb = 0; kb < 2; ++kb) {
           uint32_t a[4], b0, b1;
-          frag_b_t(b0, b1, sm.Rh, kLD64, j0, 8 * kb, g, t4);
-          frag_a(a, sm.U[0], kLD16, 0, 8 * kb, g, t4);
+          frag_b_t(b0, b1, op.Rh, kLD64, j0, 8 * kb, g, t4);
+          frag_a(a, Uq[0], kLD16, 0, 8 * kb, g, t4);
           mma_tf32(bK, a, b0, b1);
-          frag_a(a, sm.U[2], kLD16, 0, 8 * kb, g, t4);
+          frag_a(a, Uq[2], kLD16, 0, 8 * kb, g, t4);
           mma_tf32(bB, a, b0, b1);
-          frag_b_t(b0, b1, sm.Ah, kLD64, j0, 8 * kb, g, t4);
-          frag_a(a, sm.U[1], kLD16, 0, 8 * kb, g, t4);
+          frag_b_t(b0, b1, op.Ah, kLD64, j0, 8 * kb, g, t4);
+          frag_a(a, Uq[1], kLD16, 0, 8 * kb, g, t4);
           mma_tf32(bK, a, b0, b1);
-          frag_a(a, sm.U[3], kLD16, 0, 8 * kb, g, t4);
+          frag_a(a, Uq[3], kLD16, 0, 8 * kb, g, t4);
           mma_tf32(bB, a, b0, b1);
-          frag_b_t(b0, b1, sm.Kt, kLD64, j0, 8 * kb, g, t4);
-          frag_a_t(a, sm.U[0], kLD16, 0, 8 * kb, g, t4);
+          frag_b_t(b0, b1, op.Kt, kLD64, j0, 8 * kb, g, t4);
+          frag_a_t(a, Uq[0], kLD16, 0, 8 * kb, g, t4);
           mma_tf32(bR, a, b0, b1);
-          frag_a_t(a, sm.U[1], kLD16, 0, 8 * kb, g, t4);
+          frag_a_t(a, Uq[1], kLD16, 0, 8 * kb, g, t4);
           mma_tf32(bA, a, b0, b1);
-          frag_b_t(b0, b1, sm.Bt, kLD64, j0, 8 * kb, g, t4);
-          frag_a_t(a, sm.U[2], kLD16, 0, 8 * kb, g, t4);
+          frag_b_t(b0, b1, op.Bt, kLD64, j0, 8 * kb, g, t4);
+          frag_a_t(a, Uq[2], kLD16, 0, 8 * kb, g, t4);
           mma_tf32(bR, a, b0, b1);
-          frag_a_t(a, sm.U[3], kLD16, 0, 8 * kb, g, t4);
+          frag_a_t(a, Uq[3], kLD16, 0, 8 * kb, g, t4);
           mma_tf32(bA, a, b0, b1);
         }
         const __nv_bfloat16* rs = sm.raw[st][0];
@@ -625,9 +654,9 @@ __global__ void __launch_bounds__(kThreads, 1) wkv7_bwd3_kernel(const __grid_con
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
           const int t = g + 8 * h, col = j0 + 2 * t4;
-          const float2 c = *reinterpret_cast<const float2*>(sm.cS + t * kN + col);
-          const float2 ic = *reinterpret_cast<const float2*>(sm.icS + t * kN + col);
-          const float2 cp = t ? *reinterpret_cast<const float2*>(sm.cS + (t - 1) * kN + col) : make_float2(1.f, 1.f);
+          const float2 c = *reinterpret_cast<const float2*>(op.cS + t * kN + col);
+          const float2 ic = *reinterpret_cast<const float2*>(op.icS + t * kN + col);
+          const float2 cp = t ? *reinterpret_cast<const float2*>(op.cS + (t - 1) * kN + col) : make_float2(1.f, 1.f);
           const float2 r = bf2(rs + V_R * kTile + t * kN + col), k = bf2(rs + V_K * kTile + t * kN + col);
           const float2 b = bf2(rs + V_B * kTile + t * kN + col), a = bf2(rs + V_A * kTile + t * kN + col);
           const float cv[2] = {c.x, c.y}, icv[2] = {ic.x, ic.y}, cpv[2] = {cp.x, cp.y};
@@ -679,7 +708,7 @@ __global__ void __launch_bounds__(kThreads, 1) wkv7_bwd3_kernel(const __grid_con
         }
       }
     }
-    // stage st is free; refill it with the chunk of visit m + kStages
+    // the stage of chunk n is free (front half and outputs done); refill it
     if (__syncthreads_or(sm.abort_flag)) {
       aborted = true;
       break;
