@@ -62,10 +62,12 @@ enum { V_R = 0, V_W = 1, V_K = 2, V_V = 3, V_A = 4, V_B = 5, V_DY = 6 };
 struct OpB {
   float Ah[kL * kLD64], Rh[kL * kLD64], Kt[kL * kLD64], Bt[kL * kLD64];  // [t][j]
   float Kb[kL * kLD64], Bb[kL * kLD64], Vs[kL * kLD64], DYs[kL * kLD64];  // [t][j], V and DY [t][i]
-  float cS[kTile], icS[kTile];  // c(t) and 1/c(t), fp32 [t][j]
+  float Ah68[kL * kLDT];        // A^ again, stride 68 (read only as a transposed B operand)
+  float cS[kTile];              // c(t), fp32 [t][j]
   float cL[kN];                 // fp32
   float M[4][kL * kLD16];       // Mka, Mba (strictly lower), Mkr, Mbr (lower)   [t][s]
   float Tinv[kL * kLD16];       // (I - Mba)^-1                                  [t][s]
+  float TinvT[kL * kLD16];      // its transpose                                [s][t]
   float U0[kL * kLD16];         // triu(V DY^T)                                 [t][s]
   int unsafe;
   int pad_[3];
@@ -80,9 +82,10 @@ struct Bwd3Smem {
   float SAs[kL * kLD64], DSAs[kL * kLD64];  // sa(t), dsa(t) [t][i] (tf32)
   float GcS[kN * kLDT];                     // carry at the chunk end [i][j] (tf32)
   float S0s[2][kN * kLD64];                 // checkpoints [i][j]
-  float bpart[4][kN];  // per state warp: column sums of (carry o S(L)) over its rows
-  float spart[4][kN];  // per state warp: column sums of (next carry o S0) over its rows
-  float red[4 * 5 * kN];  // direct chunks: per-warp column partials
+  // per chunk parity and state warp: column sums over the warp's rows of
+  // (carry at the chunk start) o S0, i.e. colsum(G o S) at a chunk boundary;
+  // the end-anchor term of a chunk is the start-anchor term of the chunk after it
+  float spart[2][4][kN];
   uint64_t full[kStages];
   int abort_flag;
 };
@@ -103,6 +106,17 @@ __device__ bool prep_bwd(const __nv_bfloat16* rs, OpB& op, int len, int ptid) {
   for (int e = 0; e < 8; ++e) {
     wm[e] = tm + e < len ? bf(rs + V_W * kTile + (tm + e) * kN + j) : 1.f;
     wo[e] = to + e < len ? bf(rs + V_W * kTile + (to + e) * kN + j) : 1.f;
+  }
+  float av[8], rv[8], kv[8], bv[8], vv[8], dyv[8];
+#pragma unroll
+  for (int e = 0; e < 8; ++e) {
+    const int o = (tm + e) * kN + j;
+    av[e] = bf(rs + V_A * kTile + o);
+    rv[e] = bf(rs + V_R * kTile + o);
+    kv[e] = bf(rs + V_K * kTile + o);
+    bv[e] = bf(rs + V_B * kTile + o);
+    vv[e] = bf(rs + V_V * kTile + o);
+    dyv[e] = bf(rs + V_DY * kTile + o);
   }
   bool unsafe = false;
 #pragma unroll
@@ -125,19 +139,19 @@ __device__ bool prep_bwd(const __nv_bfloat16* rs, OpB& op, int len, int ptid) {
     c *= wm[e];
     const float ic = rcp_approx(c);
     const int o = t * kN + j, q = t * kLD64 + j;
-    const float a = bf(rs + V_A * kTile + o), r = bf(rs + V_R * kTile + o);
-    const float k = bf(rs + V_K * kTile + o), b = bf(rs + V_B * kTile + o);
-    op.Ah[q] = tf32r(a * cprev);
+    const float a = av[e], r = rv[e], k = kv[e], b = bv[e];
+    const float ah = tf32r(a * cprev);
+    op.Ah[q] = ah;
     op.Rh[q] = tf32r(r * c);
     op.Kt[q] = tf32r(k * ic);
     op.Bt[q] = tf32r(b * ic);
     const float s = cL * ic;
     op.Kb[q] = tf32r(k * s);
     op.Bb[q] = tf32r(b * s);
-    op.Vs[q] = tf32r(bf(rs + V_V * kTile + o));
-    op.DYs[q] = tf32r(bf(rs + V_DY * kTile + o));
+    op.Vs[q] = vv[e];  // bf16 values are tf32 values
+    op.DYs[q] = dyv[e];
+    op.Ah68[t * kLDT + j] = ah;
     op.cS[o] = c;
-    op.icS[o] = ic;
   }
   return false;
 }
@@ -223,7 +237,11 @@ __device__ bool front_chunk(Bwd3Smem& sm, OpB& op, const __nv_bfloat16* rs, uint
     }
     if (lane < 16) {
 #pragma unroll
-      for (int t = 0; t < kL; ++t) op.Tinv[t * kLD16 + s] = tf32r(col[t]);
+      for (int t = 0; t < kL; ++t) {
+        const float x = tf32r(col[t]);
+        op.Tinv[t * kLD16 + s] = x;
+        op.TinvT[s * kLD16 + t] = x;
+      }
     }
   } else if (pw == 2) {  // U0 = triu(V DY^T)
     gram16(acc, op.Vs, op.DYs, g, t4);
@@ -256,7 +274,7 @@ __device__ void direct_chunk_bwd(Bwd3Smem& sm, const float* S0, int stage, int l
                                  int warp, int lane) {
   const int g = lane >> 2, t4 = lane & 3, i0 = 16 * warp, tid = threadIdx.x;
   const __nv_bfloat16* rs = sm.raw[stage][0];
-  float* red = sm.red;  // [4 warps][5][64]
+  float* red = sm.SAs;  // [4 warps][5][64], in SAs and DSAs (unused by a direct chunk)
   for (int t = len - 1; t >= 0; --t) {
     float sp[8][4];
 #pragma unroll
@@ -402,7 +420,11 @@ __global__ void __launch_bounds__(kThreads, 1) wkv7_bwd3_kernel(const __grid_con
   float G[8][4];
 #pragma unroll
   for (int nt = 0; nt < 8; ++nt) zero4(G[nt]);
-  if (!is_prep) fetch_ckpt(nchunks - 1);
+  if (!is_prep) {
+    fetch_ckpt(nchunks - 1);
+    cp_async_wait_all();
+  }
+  (&sm.spart[nchunks & 1][0][0])[tid] = 0.f;  // the carry after the last chunk is zero
   __syncthreads();
 
   int waited = 0, issued = min(kStages, nchunks);
@@ -424,36 +446,23 @@ __global__ void __launch_bounds__(kThreads, 1) wkv7_bwd3_kernel(const __grid_con
                  vstep};
     // ================= P: carry chain of chunk n (state warps) || front half of chunk n-1 (prep warps)
     if (!is_prep) {
-      cp_async_wait_all();
-      // carry as a tf32 operand, and this warp's share of colsum(Gc o S(L))
-      // (S(L) = the next chunk's checkpoint; Gc = 0 after the last chunk)
-      const float* SL = sm.S0s[(n + 1) & 1];
+      // carry as a tf32 operand; S0 of this chunk is complete (waited before the last barrier)
 #pragma unroll
       for (int nt = 0; nt < 8; ++nt) {
         const int col = 8 * nt + 2 * t4;
         *reinterpret_cast<float2*>(sm.GcS + (i0 + g) * kLDT + col) = make_float2(tf32r(G[nt][0]), tf32r(G[nt][1]));
         *reinterpret_cast<float2*>(sm.GcS + (i0 + g + 8) * kLDT + col) = make_float2(tf32r(G[nt][2]), tf32r(G[nt][3]));
-        float p0 = 0.f, p1 = 0.f;
-        if (m > 0) {
-          const float2 s_lo = *reinterpret_cast<const float2*>(SL + (i0 + g) * kLD64 + col);
-          const float2 s_hi = *reinterpret_cast<const float2*>(SL + (i0 + g + 8) * kLD64 + col);
-          p0 = fmaf(G[nt][0], s_lo.x, G[nt][2] * s_hi.x);
-          p1 = fmaf(G[nt][1], s_lo.y, G[nt][3] * s_hi.y);
-        }
-        p0 = col_sum(p0);
-        p1 = col_sum(p1);
-        if (g == 0) *reinterpret_cast<float2*>(sm.bpart[warp] + col) = make_float2(p0, p1);
       }
-      named_bar(2, 128);  // S(L) read by every state warp before its buffer is refilled
-      if (n > 0) fetch_ckpt(n - 1);
+      if (n > 0) fetch_ckpt(n - 1);  // into the buffer of the chunk after this one, read last in its outputs
       if (unsafe) {
         direct_chunk_bwd(sm, S0, st, len, o, G, warp, lane);
       } else {
-        float RSA[2][4], RDSA[2][4];
+        float RSA[2][4], RDSA[2][4], DV[2][4];
 #pragma unroll
         for (int q = 0; q < 2; ++q) {
           zero4(RSA[q]);
           zero4(RDSA[q]);
+          zero4(DV[q]);
         }
 #pragma unroll
         for (int kb = 0; kb < 8; ++kb) {
@@ -467,19 +476,21 @@ __global__ void __launch_bounds__(kThreads, 1) wkv7_bwd3_kernel(const __grid_con
             mma_tf32(RSA[q], aS, b0, b1);
             frag_b(b0, b1, op.Bb, kLD64, 8 * q, 8 * kb, g, t4);
             mma_tf32(RDSA[q], aG, b0, b1);
+            frag_b(b0, b1, op.Kb, kLD64, 8 * q, 8 * kb, g, t4);  // dv^T: Gc Kb^T
+            mma_tf32(DV[q], aG, b0, b1);
           }
         }
         uint32_t aV[2][4], aD[2][4];
 #pragma unroll
         for (int kb = 0; kb < 2; ++kb) {
-          frag_a_t(aV[kb], op.Vs, kLD64, i0, 8 * kb, g, t4);   // V^T
-          frag_a_t(aD[kb], op.DYs, kLD64, i0, 8 * kb, g, t4);  // DY^T
+          frag_a_t(aV[kb], op.Vs, kLD64, i0, 8 * kb, g, t4);    // V^T
+          frag_a_ts(aD[kb], op.DYs, kLD64, i0, 8 * kb, g, t4);  // DY^T (hardware k order)
 #pragma unroll
           for (int q = 0; q < 2; ++q) {
             uint32_t b0, b1;
             frag_b(b0, b1, op.M[0], kLD16, 8 * q, 8 * kb, g, t4);  // + V^T Mka^T
             mma_tf32(RSA[q], aV[kb], b0, b1);
-            frag_b_t(b0, b1, op.M[3], kLD16, 8 * q, 8 * kb, g, t4);  // + DY^T Mbr
+            frag_b_ts(b0, b1, op.M[3], kLD16, 8 * q, 8 * kb, g, t4);  // + DY^T Mbr
             mma_tf32(RDSA[q], aD[kb], b0, b1);
           }
         }
@@ -499,13 +510,35 @@ __global__ void __launch_bounds__(kThreads, 1) wkv7_bwd3_kernel(const __grid_con
             uint32_t b0, b1;
             frag_b(b0, b1, op.Tinv, kLD16, 8 * q, 8 * kb, g, t4);  // SA^T = RSA T^T
             mma_tf32(SA[q], a1, b0, b1);
-            frag_b_t(b0, b1, op.Tinv, kLD16, 8 * q, 8 * kb, g, t4);  // DSA^T = RDSA T
+            frag_b(b0, b1, op.TinvT, kLD16, 8 * q, 8 * kb, g, t4);  // DSA^T = RDSA T
             mma_tf32(DSA[q], a2, b0, b1);
           }
         }
         uint32_t aDS[2][4];
         c2a(aDS[0], DSA[0]);
         c2a(aDS[1], DSA[1]);
+        // dv^T (rows i, columns t) += DY^T Mkr + DSA^T Mka
+#pragma unroll
+        for (int kb = 0; kb < 2; ++kb)
+#pragma unroll
+          for (int q = 0; q < 2; ++q) {
+            uint32_t b0, b1;
+            frag_b_ts(b0, b1, op.M[2], kLD16, 8 * q, 8 * kb, g, t4);
+            mma_tf32(DV[q], aD[kb], b0, b1);
+            frag_b_t(b0, b1, op.M[0], kLD16, 8 * q, 8 * kb, g, t4);
+            mma_tf32(DV[q], aDS[kb], b0, b1);
+          }
+#pragma unroll
+        for (int q = 0; q < 2; ++q)
+#pragma unroll
+          for (int e = 0; e < 2; ++e) {
+            const int t = 8 * q + 2 * t4 + e;
+            if (t < len) {
+              float* dst = args.dv + o.base + (size_t)t * vstep + i0 + g;
+              dst[0] = DV[q][e];
+              dst[8] = DV[q][2 + e];
+            }
+          }
 #pragma unroll
         for (int q = 0; q < 2; ++q)
 #pragma unroll
@@ -530,21 +563,21 @@ __global__ void __launch_bounds__(kThreads, 1) wkv7_bwd3_kernel(const __grid_con
 #pragma unroll
           for (int nt = 0; nt < 8; ++nt) {
             uint32_t b0, b1;
-            frag_b_t(b0, b1, op.Rh, kLD64, 8 * nt, 8 * kb, g, t4);
+            frag_b_ts(b0, b1, op.Rh, kLD64, 8 * nt, 8 * kb, g, t4);
             mma_tf32(G[nt], aD[kb], b0, b1);
-            frag_b_t(b0, b1, op.Ah, kLD64, 8 * nt, 8 * kb, g, t4);
+            frag_b_t(b0, b1, op.Ah68, kLDT, 8 * nt, 8 * kb, g, t4);
             mma_tf32(G[nt], aDS[kb], b0, b1);
           }
-        // start anchor of the dw identity: colsum(next carry o S0), this warp's rows
+      }
+      // start anchor of the dw identity: colsum(next carry o S0), this warp's rows
 #pragma unroll
-        for (int nt = 0; nt < 8; ++nt) {
-          const int col = 8 * nt + 2 * t4;
-          const float2 s_lo = *reinterpret_cast<const float2*>(S0 + (i0 + g) * kLD64 + col);
-          const float2 s_hi = *reinterpret_cast<const float2*>(S0 + (i0 + g + 8) * kLD64 + col);
-          const float p0 = col_sum(fmaf(G[nt][0], s_lo.x, G[nt][2] * s_hi.x));
-          const float p1 = col_sum(fmaf(G[nt][1], s_lo.y, G[nt][3] * s_hi.y));
-          if (g == 0) *reinterpret_cast<float2*>(sm.spart[warp] + col) = make_float2(p0, p1);
-        }
+      for (int nt = 0; nt < 8; ++nt) {
+        const int col = 8 * nt + 2 * t4;
+        const float2 s_lo = *reinterpret_cast<const float2*>(S0 + (i0 + g) * kLD64 + col);
+        const float2 s_hi = *reinterpret_cast<const float2*>(S0 + (i0 + g + 8) * kLD64 + col);
+        const float p0 = col_sum(fmaf(G[nt][0], s_lo.x, G[nt][2] * s_hi.x));
+        const float p1 = col_sum(fmaf(G[nt][1], s_lo.y, G[nt][3] * s_hi.y));
+        if (g == 0) *reinterpret_cast<float2*>(sm.spart[n & 1][warp] + col) = make_float2(p0, p1);
       }
     } else if (n > 0) {
       const int st1 = (m + 1) % kStages;
@@ -583,35 +616,6 @@ __global__ void __launch_bounds__(kThreads, 1) wkv7_bwd3_kernel(const __grid_con
         mma_tf32(bR, aDY, c0, c1);
         mma_tf32(bA, aDSA, c0, c1);
       }
-      // dv (t x i, columns i = j0..j0+7) = Kb Gc^T + Mkr^T DY + Mka^T DSA
-      {
-        float bV[4];
-        zero4(bV);
-#pragma unroll
-        for (int kb = 0; kb < 8; ++kb) {
-          uint32_t a[4], b0, b1;
-          frag_a(a, op.Kb, kLD64, 0, 8 * kb, g, t4);
-          frag_b(b0, b1, sm.GcS, kLDT, j0, 8 * kb, g, t4);
-          mma_tf32(bV, a, b0, b1);
-        }
-#pragma unroll
-        for (int kb = 0; kb < 2; ++kb) {
-          uint32_t a[4], b0, b1;
-          frag_a_t(a, op.M[2], kLD16, 0, 8 * kb, g, t4);
-          frag_b_t(b0, b1, op.DYs, kLD64, j0, 8 * kb, g, t4);
-          mma_tf32(bV, a, b0, b1);
-          frag_a_t(a, op.M[0], kLD16, 0, 8 * kb, g, t4);
-          frag_b_t(b0, b1, sm.DSAs, kLD64, j0, 8 * kb, g, t4);
-          mma_tf32(bV, a, b0, b1);
-        }
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          const int t = g + 8 * h;
-          if (t < len)
-            *reinterpret_cast<float2*>(args.dv + o.base + (size_t)t * vstep + j0 + 2 * t4) =
-                make_float2(bV[2 * h], bV[2 * h + 1]);
-        }
-      }
       __syncthreads();
       // triangular terms, scaling, dw, stores (columns j0 .. j0+7)
       {
@@ -633,20 +637,20 @@ __global__ void __launch_bounds__(kThreads, 1) wkv7_bwd3_kernel(const __grid_con
           mma_tf32(bK, a, b0, b1);
           frag_a(a, Uq[2], kLD16, 0, 8 * kb, g, t4);
           mma_tf32(bB, a, b0, b1);
-          frag_b_t(b0, b1, op.Ah, kLD64, j0, 8 * kb, g, t4);
+          frag_b_t(b0, b1, op.Ah68, kLDT, j0, 8 * kb, g, t4);
           frag_a(a, Uq[1], kLD16, 0, 8 * kb, g, t4);
           mma_tf32(bK, a, b0, b1);
           frag_a(a, Uq[3], kLD16, 0, 8 * kb, g, t4);
           mma_tf32(bB, a, b0, b1);
-          frag_b_t(b0, b1, op.Kt, kLD64, j0, 8 * kb, g, t4);
-          frag_a_t(a, Uq[0], kLD16, 0, 8 * kb, g, t4);
+          frag_b_ts(b0, b1, op.Kt, kLD64, j0, 8 * kb, g, t4);
+          frag_a_ts(a, Uq[0], kLD16, 0, 8 * kb, g, t4);
           mma_tf32(bR, a, b0, b1);
-          frag_a_t(a, Uq[1], kLD16, 0, 8 * kb, g, t4);
+          frag_a_ts(a, Uq[1], kLD16, 0, 8 * kb, g, t4);
           mma_tf32(bA, a, b0, b1);
-          frag_b_t(b0, b1, op.Bt, kLD64, j0, 8 * kb, g, t4);
-          frag_a_t(a, Uq[2], kLD16, 0, 8 * kb, g, t4);
+          frag_b_ts(b0, b1, op.Bt, kLD64, j0, 8 * kb, g, t4);
+          frag_a_ts(a, Uq[2], kLD16, 0, 8 * kb, g, t4);
           mma_tf32(bR, a, b0, b1);
-          frag_a_t(a, Uq[3], kLD16, 0, 8 * kb, g, t4);
+          frag_a_ts(a, Uq[3], kLD16, 0, 8 * kb, g, t4);
           mma_tf32(bA, a, b0, b1);
         }
         const __nv_bfloat16* rs = sm.raw[st][0];
@@ -655,7 +659,7 @@ __global__ void __launch_bounds__(kThreads, 1) wkv7_bwd3_kernel(const __grid_con
         for (int h = 0; h < 2; ++h) {
           const int t = g + 8 * h, col = j0 + 2 * t4;
           const float2 c = *reinterpret_cast<const float2*>(op.cS + t * kN + col);
-          const float2 ic = *reinterpret_cast<const float2*>(op.icS + t * kN + col);
+          const float2 ic = make_float2(rcp_approx(c.x), rcp_approx(c.y));
           const float2 cp = t ? *reinterpret_cast<const float2*>(op.cS + (t - 1) * kN + col) : make_float2(1.f, 1.f);
           const float2 r = bf2(rs + V_R * kTile + t * kN + col), k = bf2(rs + V_K * kTile + t * kN + col);
           const float2 b = bf2(rs + V_B * kTile + t * kN + col), a = bf2(rs + V_A * kTile + t * kN + col);
@@ -687,11 +691,13 @@ __global__ void __launch_bounds__(kThreads, 1) wkv7_bwd3_kernel(const __grid_con
             if (g >= d) lo += ol;
           }
           const int col = j0 + 2 * t4 + e;
-          const float start = sm.spart[0][col] + sm.spart[1][col] + sm.spart[2][col] + sm.spart[3][col];
+          const float(&sp)[4][kN] = sm.spart[n & 1];
+          const float start = sp[0][col] + sp[1][col] + sp[2][col] + sp[3][col];
           const float2 w0 = bf2(rs + V_W * kTile + g * kN + j0 + 2 * t4);
           const float2 w1 = bf2(rs + V_W * kTile + (g + 8) * kN + j0 + 2 * t4);
           dw[e] = (start - (lo - x[e]) - ada[e]) * rcp_approx(e ? w0.y : w0.x);
-          const float bnd = sm.bpart[0][col] + sm.bpart[1][col] + sm.bpart[2][col] + sm.bpart[3][col];
+          const float(&bp)[4][kN] = sm.spart[(n + 1) & 1];
+          const float bnd = bp[0][col] + bp[1][col] + bp[2][col] + bp[3][col];
           dw[2 + e] = (hi2 - ada[2 + e] + bnd) * rcp_approx(e ? w1.y : w1.x);
         }
 #pragma unroll
@@ -708,6 +714,8 @@ __global__ void __launch_bounds__(kThreads, 1) wkv7_bwd3_kernel(const __grid_con
         }
       }
     }
+    // S0 of the next chunk complete before the barrier makes it visible
+    if (!is_prep) cp_async_wait_all();
     // the stage of chunk n is free (front half and outputs done); refill it
     if (__syncthreads_or(sm.abort_flag)) {
       aborted = true;

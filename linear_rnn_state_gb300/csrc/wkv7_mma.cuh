@@ -33,7 +33,7 @@ __device__ __forceinline__ float tf32r(float x) { return __uint_as_float(tf32_bi
 
 // d += a * b for one 16x8x8 tile.
 __device__ __forceinline__ void mma_tf32(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
-  asm volatile(
+  asm(
       "mma.sync.aligned.m16n8k8.row.col.f32.tf32.tf32.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
       "{%0,%1,%2,%3};\n"
       : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
@@ -95,6 +95,25 @@ __device__ __forceinline__ void frag_b_t_r(uint32_t& b0, uint32_t& b1, const flo
   const float* p = m + (k0 + 2 * t) * ld + n0 + g;
   b0 = tf32_bits(p[0]);
   b1 = tf32_bits(p[ld]);
+}
+
+// Fragments in the hardware's own k order (slot t -> column t, slot t+4 ->
+// column t+4), for products whose two operands are both read transposed:
+// A[m][k] from storage [k][m] and B[k][n] from storage [k][n]. With a row
+// stride of 8 mod 32 (or 24 for 16-wide blocks) every such load is
+// conflict-free.
+__device__ __forceinline__ void frag_a_ts(uint32_t (&a)[4], const float* m, int ld, int m0, int k0, int g, int t) {
+  const float* p = m + (k0 + t) * ld + m0 + g;
+  a[0] = __float_as_uint(p[0]);
+  a[1] = __float_as_uint(p[8]);
+  a[2] = __float_as_uint(p[4 * ld]);
+  a[3] = __float_as_uint(p[4 * ld + 8]);
+}
+__device__ __forceinline__ void frag_b_ts(uint32_t& b0, uint32_t& b1, const float* m, int ld, int n0, int k0, int g,
+                                          int t) {
+  const float* p = m + (k0 + t) * ld + n0 + g;
+  b0 = __float_as_uint(p[0]);
+  b1 = __float_as_uint(p[4 * ld]);
 }
 
 // Accumulator tile -> A fragment over the same columns (rounded to tf32).
