@@ -84,6 +84,16 @@ __device__ void prep_chunk(Fwd3Smem& sm, Prep3& P, int stage, int len, int ptid)
     wm[e] = tm + e < len ? bf(rs + V_W * kL * kN + (tm + e) * kN + j) : 1.f;
     wo[e] = to + e < len ? bf(rs + V_W * kL * kN + (to + e) * kN + j) : 1.f;
   }
+  float av[8], rv[8], kv[8], bv[8], vt[8];
+#pragma unroll
+  for (int e = 0; e < 8; ++e) {
+    const int o = (tm + e) * kN + j;
+    av[e] = bf(rs + V_A * kL * kN + o);
+    rv[e] = bf(rs + V_R * kL * kN + o);
+    kv[e] = bf(rs + V_K * kL * kN + o);
+    bv[e] = bf(rs + V_B * kL * kN + o);
+    vt[e] = bf(rs + V_V * kL * kN + o);  // bf16 values are tf32 values
+  }
   bool unsafe = false;
 #pragma unroll
   for (int e = 0; e < 8; ++e) unsafe |= !decay_is_safe(wm[e]);
@@ -97,7 +107,7 @@ __device__ void prep_chunk(Fwd3Smem& sm, Prep3& P, int stage, int len, int ptid)
   const float cL = half ? po * pm : pm * po;
   float c = half ? p_first : 1.f;
   if (half == 0) P.cL[j] = cL;
-  float vt[8], kbt[8], bbt[8];
+  float kbt[8], bbt[8];
 #pragma unroll
   for (int e = 0; e < 8; ++e) {
     const int t = tm + e;
@@ -105,9 +115,7 @@ __device__ void prep_chunk(Fwd3Smem& sm, Prep3& P, int stage, int len, int ptid)
     c *= wm[e];
     const float ic = rcp_approx(c);
     const int o = t * kN + j;
-    const float a = bf(rs + V_A * kL * kN + o), r = bf(rs + V_R * kL * kN + o);
-    const float k = bf(rs + V_K * kL * kN + o), b = bf(rs + V_B * kL * kN + o);
-    vt[e] = tf32r(bf(rs + V_V * kL * kN + o));
+    const float a = av[e], r = rv[e], k = kv[e], b = bv[e];
     sm.X2[t * kLD64 + j] = tf32r(k * ic);
     sm.X2[(kL + t) * kLD64 + j] = tf32r(b * ic);
     P.X1[t * kLD64 + j] = tf32r(a * cprev);
