@@ -53,6 +53,7 @@ constexpr int kN = 64, kL = 16;
 constexpr int kLD64 = 72;  // row stride (floats) of 64-wide operands read along k
 constexpr int kLD16 = 24;  // row stride of 16-wide operands
 constexpr int kLDT = 68;   // row stride of the carry, read only transposed
+constexpr int kLDS = 72;   // row stride of the checkpoints
 constexpr int kStages = 3;
 constexpr int kThreads = 256;
 constexpr int kTile = kL * kN;
@@ -62,10 +63,11 @@ enum { V_R = 0, V_W = 1, V_K = 2, V_V = 3, V_A = 4, V_B = 5, V_DY = 6 };
 struct OpB {
   float Ah[kL * kLD64], Rh[kL * kLD64], Kt[kL * kLD64], Bt[kL * kLD64];  // [t][j]
   float Kb[kL * kLD64], Bb[kL * kLD64], Vs[kL * kLD64], DYs[kL * kLD64];  // [t][j], V and DY [t][i]
-  float Ah68[kL * kLDT];        // A^ again, stride 68 (read only as a transposed B operand)
+  float Ah68[kL * kLDT];        // A^ and R^ again, stride 68 (read only as transposed B operands)
+  float Rh68[kL * kLDT];
   float cS[kTile];              // c(t), fp32 [t][j]
   float cL[kN];                 // fp32
-  float M[4][kL * kLD16];       // Mka, Mba (strictly lower), Mkr, Mbr (lower)   [t][s]
+  float M[3][kL * kLD16];       // Mka (strictly lower), Mkr, Mbr (lower)          [t][s]
   float Tinv[kL * kLD16];       // (I - Mba)^-1                                  [t][s]
   float TinvT[kL * kLD16];      // its transpose                                [s][t]
   float U0[kL * kLD16];         // triu(V DY^T)                                 [t][s]
@@ -81,7 +83,7 @@ struct Bwd3Smem {
   float U[3][kL * kLD16];
   float SAs[kL * kLD64], DSAs[kL * kLD64];  // sa(t), dsa(t) [t][i] (tf32)
   float GcS[kN * kLDT];                     // carry at the chunk end [i][j] (tf32)
-  float S0s[2][kN * kLD64];                 // checkpoints [i][j]
+  float S0s[2][kN * kLDS];                  // checkpoints [i][j]
   // per chunk parity and state warp: column sums over the warp's rows of
   // (carry at the chunk start) o S0, i.e. colsum(G o S) at a chunk boundary;
   // the end-anchor term of a chunk is the start-anchor term of the chunk after it
@@ -142,7 +144,9 @@ __device__ bool prep_bwd(const __nv_bfloat16* rs, OpB& op, int len, int ptid) {
     const float a = av[e], r = rv[e], k = kv[e], b = bv[e];
     const float ah = tf32r(a * cprev);
     op.Ah[q] = ah;
-    op.Rh[q] = tf32r(r * c);
+    const float rh = tf32r(r * c);
+    op.Rh[q] = rh;
+    op.Rh68[t * kLDT + j] = rh;
     op.Kt[q] = tf32r(k * ic);
     op.Bt[q] = tf32r(b * ic);
     const float s = cL * ic;
@@ -222,10 +226,11 @@ __device__ bool front_chunk(Bwd3Smem& sm, OpB& op, const __nv_bfloat16* rs, uint
       mma_tf32(acc[nt], a, b0, b1);
     }
   }
-  store_masked(acc, op.M[pw], true, mt == 1, g, t4);
+  // Mba is needed only for T: it goes to U1's tile, which is free until the output phase
+  store_masked(acc, pw == 1 ? sm.U[0] : op.M[pw == 0 ? 0 : pw - 1], true, mt == 1, g, t4);
   if (pw == 1) {  // T = (I - Mba)^-1, lane s < 16 owns column s
     __syncwarp();
-    const float* Mba = op.M[1];
+    const float* Mba = sm.U[0];
     const int s = lane & 15;
     float col[kL];
 #pragma unroll
@@ -280,8 +285,8 @@ __device__ void direct_chunk_bwd(Bwd3Smem& sm, const float* S0, int stage, int l
 #pragma unroll
     for (int nt = 0; nt < 8; ++nt) {
       const int col = 8 * nt + 2 * t4;
-      const float2 lo = *reinterpret_cast<const float2*>(S0 + (i0 + g) * kLD64 + col);
-      const float2 hi = *reinterpret_cast<const float2*>(S0 + (i0 + g + 8) * kLD64 + col);
+      const float2 lo = *reinterpret_cast<const float2*>(S0 + (i0 + g) * kLDS + col);
+      const float2 hi = *reinterpret_cast<const float2*>(S0 + (i0 + g + 8) * kLDS + col);
       sp[nt][0] = lo.x;
       sp[nt][1] = lo.y;
       sp[nt][2] = hi.x;
@@ -406,7 +411,7 @@ __global__ void __launch_bounds__(kThreads, 1) wkv7_bwd3_kernel(const __grid_con
 #pragma unroll
     for (int q = 0; q < 8; ++q) {
       const int idx = tid + 128 * q;  // 16-byte piece: row idx / 16, column 4 * (idx % 16)
-      cp_async16(dst + (idx >> 4) * kLD64 + 4 * (idx & 15), src + 4 * idx);
+      cp_async16(dst + (idx >> 4) * kLDS + 4 * (idx & 15), src + 4 * idx);
     }
     cp_async_commit();
   };
@@ -467,7 +472,7 @@ __global__ void __launch_bounds__(kThreads, 1) wkv7_bwd3_kernel(const __grid_con
 #pragma unroll
         for (int kb = 0; kb < 8; ++kb) {
           uint32_t aS[4], aG[4];
-          frag_a_r(aS, S0, kLD64, i0, 8 * kb, g, t4);
+          frag_a_r(aS, S0, kLDS, i0, 8 * kb, g, t4);
           c2a(aG, G[kb]);
 #pragma unroll
           for (int q = 0; q < 2; ++q) {
@@ -490,7 +495,7 @@ __global__ void __launch_bounds__(kThreads, 1) wkv7_bwd3_kernel(const __grid_con
             uint32_t b0, b1;
             frag_b(b0, b1, op.M[0], kLD16, 8 * q, 8 * kb, g, t4);  // + V^T Mka^T
             mma_tf32(RSA[q], aV[kb], b0, b1);
-            frag_b_ts(b0, b1, op.M[3], kLD16, 8 * q, 8 * kb, g, t4);  // + DY^T Mbr
+            frag_b_ts(b0, b1, op.M[2], kLD16, 8 * q, 8 * kb, g, t4);  // + DY^T Mbr
             mma_tf32(RDSA[q], aD[kb], b0, b1);
           }
         }
@@ -523,7 +528,7 @@ __global__ void __launch_bounds__(kThreads, 1) wkv7_bwd3_kernel(const __grid_con
 #pragma unroll
           for (int q = 0; q < 2; ++q) {
             uint32_t b0, b1;
-            frag_b_ts(b0, b1, op.M[2], kLD16, 8 * q, 8 * kb, g, t4);
+            frag_b_ts(b0, b1, op.M[1], kLD16, 8 * q, 8 * kb, g, t4);
             mma_tf32(DV[q], aD[kb], b0, b1);
             frag_b_t(b0, b1, op.M[0], kLD16, 8 * q, 8 * kb, g, t4);
             mma_tf32(DV[q], aDS[kb], b0, b1);
@@ -573,8 +578,8 @@ __global__ void __launch_bounds__(kThreads, 1) wkv7_bwd3_kernel(const __grid_con
 #pragma unroll
       for (int nt = 0; nt < 8; ++nt) {
         const int col = 8 * nt + 2 * t4;
-        const float2 s_lo = *reinterpret_cast<const float2*>(S0 + (i0 + g) * kLD64 + col);
-        const float2 s_hi = *reinterpret_cast<const float2*>(S0 + (i0 + g + 8) * kLD64 + col);
+        const float2 s_lo = *reinterpret_cast<const float2*>(S0 + (i0 + g) * kLDS + col);
+        const float2 s_hi = *reinterpret_cast<const float2*>(S0 + (i0 + g + 8) * kLDS + col);
         const float p0 = col_sum(fmaf(G[nt][0], s_lo.x, G[nt][2] * s_hi.x));
         const float p1 = col_sum(fmaf(G[nt][1], s_lo.y, G[nt][3] * s_hi.y));
         if (g == 0) *reinterpret_cast<float2*>(sm.spart[n & 1][warp] + col) = make_float2(p0, p1);
@@ -596,121 +601,193 @@ __global__ void __launch_bounds__(kThreads, 1) wkv7_bwd3_kernel(const __grid_con
         gram16(acc, pw == 0 ? op.Vs : sm.SAs, pw == 1 ? op.DYs : sm.DSAs, g, t4);
         store_masked(acc, sm.U[pw], false, pw == 1, g, t4);
       }
-      const int j0 = 8 * warp;
-      float bK[4], bB[4], bR[4], bA[4];
-      zero4(bK);
-      zero4(bB);
-      zero4(bR);
-      zero4(bA);
+      // Column products, 8 warps: warp (grp, jb) covers columns j0 .. j0+15 of
+      // dk~, db~ (grp 0) or dr^, da^ (grp 1).
+      const int grp = warp >> 2, jb = warp & 3, j0 = 16 * jb;
+      float P0[2][4], P1[2][4];
+#pragma unroll
+      for (int nt = 0; nt < 2; ++nt) {
+        zero4(P0[nt]);
+        zero4(P1[nt]);
+      }
+      // sums over the rows i: V Gc, SA Gc (grp 0); DY S0, DSA S0 (grp 1)
+      const float* Bm = grp ? S0 : sm.GcS;  // (rounding the carry again leaves it unchanged)
+      const int ldb = grp ? kLDS : kLDT;
 #pragma unroll
       for (int kb = 0; kb < 8; ++kb) {
-        uint32_t aV[4], aSA[4], aDY[4], aDSA[4], b0, b1, c0, c1;
-        frag_a(aV, op.Vs, kLD64, 0, 8 * kb, g, t4);
-        frag_a(aSA, sm.SAs, kLD64, 0, 8 * kb, g, t4);
-        frag_a(aDY, op.DYs, kLD64, 0, 8 * kb, g, t4);
-        frag_a(aDSA, sm.DSAs, kLD64, 0, 8 * kb, g, t4);
-        frag_b_t(b0, b1, sm.GcS, kLDT, j0, 8 * kb, g, t4);
-        frag_b_t_r(c0, c1, S0, kLD64, j0, 8 * kb, g, t4);
-        mma_tf32(bK, aV, b0, b1);
-        mma_tf32(bB, aSA, b0, b1);
-        mma_tf32(bR, aDY, c0, c1);
-        mma_tf32(bA, aDSA, c0, c1);
+        uint32_t a0[4], a1[4];
+        frag_a(a0, grp ? op.DYs : op.Vs, kLD64, 0, 8 * kb, g, t4);
+        frag_a(a1, grp ? sm.DSAs : sm.SAs, kLD64, 0, 8 * kb, g, t4);
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt) {
+          uint32_t b0, b1;
+          frag_b_t_r(b0, b1, Bm, ldb, j0 + 8 * nt, 8 * kb, g, t4);
+          mma_tf32(P0[nt], a0, b0, b1);
+          mma_tf32(P1[nt], a1, b0, b1);
+        }
       }
       __syncthreads();
-      // triangular terms, scaling, dw, stores (columns j0 .. j0+7)
-      {
-        const float2 cl = *reinterpret_cast<const float2*>(op.cL + j0 + 2 * t4);
-        bK[0] *= cl.x;
-        bK[1] *= cl.y;
-        bK[2] *= cl.x;
-        bK[3] *= cl.y;
-        bB[0] *= cl.x;
-        bB[1] *= cl.y;
-        bB[2] *= cl.x;
-        bB[3] *= cl.y;
-        const float* Uq[4] = {op.U0, sm.U[0], sm.U[1], sm.U[2]};
+      // triangular terms (U0 = triu(V DY^T), U1 = triu(V DSA^T, 1), U2 = triu(SA DY^T), U3 = triu(SA DSA^T, 1)):
+      //   dk~ = (V Gc) c(L) + U0 R^ + U1 A^        db~ = (SA Gc) c(L) + U2 R^ + U3 A^
+      //   dr^ = DY S0 + U0^T K~ + U2^T B~          da^ = DSA S0 + U1^T K~ + U3^T B~
+      const float* Uq[4] = {op.U0, sm.U[0], sm.U[1], sm.U[2]};
+      if (grp == 0) {
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt) {
+          const float2 cl = *reinterpret_cast<const float2*>(op.cL + j0 + 8 * nt + 2 * t4);
+          P0[nt][0] *= cl.x;
+          P0[nt][1] *= cl.y;
+          P0[nt][2] *= cl.x;
+          P0[nt][3] *= cl.y;
+          P1[nt][0] *= cl.x;
+          P1[nt][1] *= cl.y;
+          P1[nt][2] *= cl.x;
+          P1[nt][3] *= cl.y;
+        }
 #pragma unroll
         for (int kb = 0; kb < 2; ++kb) {
-          uint32_t a[4], b0, b1;
-          frag_b_t(b0, b1, op.Rh, kLD64, j0, 8 * kb, g, t4);
-          frag_a(a, Uq[0], kLD16, 0, 8 * kb, g, t4);
-          mma_tf32(bK, a, b0, b1);
-          frag_a(a, Uq[2], kLD16, 0, 8 * kb, g, t4);
-          mma_tf32(bB, a, b0, b1);
-          frag_b_t(b0, b1, op.Ah68, kLDT, j0, 8 * kb, g, t4);
-          frag_a(a, Uq[1], kLD16, 0, 8 * kb, g, t4);
-          mma_tf32(bK, a, b0, b1);
-          frag_a(a, Uq[3], kLD16, 0, 8 * kb, g, t4);
-          mma_tf32(bB, a, b0, b1);
-          frag_b_ts(b0, b1, op.Kt, kLD64, j0, 8 * kb, g, t4);
-          frag_a_ts(a, Uq[0], kLD16, 0, 8 * kb, g, t4);
-          mma_tf32(bR, a, b0, b1);
-          frag_a_ts(a, Uq[1], kLD16, 0, 8 * kb, g, t4);
-          mma_tf32(bA, a, b0, b1);
-          frag_b_ts(b0, b1, op.Bt, kLD64, j0, 8 * kb, g, t4);
-          frag_a_ts(a, Uq[2], kLD16, 0, 8 * kb, g, t4);
-          mma_tf32(bR, a, b0, b1);
-          frag_a_ts(a, Uq[3], kLD16, 0, 8 * kb, g, t4);
-          mma_tf32(bA, a, b0, b1);
+          uint32_t u0[4], u1[4], u2[4], u3[4];
+          frag_a(u0, Uq[0], kLD16, 0, 8 * kb, g, t4);
+          frag_a(u1, Uq[1], kLD16, 0, 8 * kb, g, t4);
+          frag_a(u2, Uq[2], kLD16, 0, 8 * kb, g, t4);
+          frag_a(u3, Uq[3], kLD16, 0, 8 * kb, g, t4);
+#pragma unroll
+          for (int nt = 0; nt < 2; ++nt) {
+            uint32_t b0, b1;
+            frag_b_t(b0, b1, op.Rh68, kLDT, j0 + 8 * nt, 8 * kb, g, t4);
+            mma_tf32(P0[nt], u0, b0, b1);
+            mma_tf32(P1[nt], u2, b0, b1);
+            frag_b_t(b0, b1, op.Ah68, kLDT, j0 + 8 * nt, 8 * kb, g, t4);
+            mma_tf32(P0[nt], u1, b0, b1);
+            mma_tf32(P1[nt], u3, b0, b1);
+          }
         }
-        const __nv_bfloat16* rs = sm.raw[st][0];
-        float dr[4], dk[4], db[4], da[4], x[4], ada[4];
+      } else {
+#pragma unroll
+        for (int kb = 0; kb < 2; ++kb) {
+          uint32_t u0[4], u1[4], u2[4], u3[4];
+          frag_a_ts(u0, Uq[0], kLD16, 0, 8 * kb, g, t4);
+          frag_a_ts(u1, Uq[1], kLD16, 0, 8 * kb, g, t4);
+          frag_a_ts(u2, Uq[2], kLD16, 0, 8 * kb, g, t4);
+          frag_a_ts(u3, Uq[3], kLD16, 0, 8 * kb, g, t4);
+#pragma unroll
+          for (int nt = 0; nt < 2; ++nt) {
+            uint32_t b0, b1;
+            frag_b_ts(b0, b1, op.Kt, kLD64, j0 + 8 * nt, 8 * kb, g, t4);
+            mma_tf32(P0[nt], u0, b0, b1);
+            mma_tf32(P1[nt], u1, b0, b1);
+            frag_b_ts(b0, b1, op.Bt, kLD64, j0 + 8 * nt, 8 * kb, g, t4);
+            mma_tf32(P0[nt], u2, b0, b1);
+            mma_tf32(P1[nt], u3, b0, b1);
+          }
+        }
+      }
+      // unscale: dk = dk~ / c, db = db~ / c (grp 0); dr = dr^ c, da = da^ c(t-1) (grp 1); and this
+      // group's part of x = r dr - k dk - b db + a da
+      const __nv_bfloat16* rs = sm.raw[st][0];
+      float X[2][4], AD[2][4];
+#pragma unroll
+      for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
-          const int t = g + 8 * h, col = j0 + 2 * t4;
+          const int t = g + 8 * h, col = j0 + 8 * nt + 2 * t4;
           const float2 c = *reinterpret_cast<const float2*>(op.cS + t * kN + col);
-          const float2 ic = make_float2(rcp_approx(c.x), rcp_approx(c.y));
-          const float2 cp = t ? *reinterpret_cast<const float2*>(op.cS + (t - 1) * kN + col) : make_float2(1.f, 1.f);
-          const float2 r = bf2(rs + V_R * kTile + t * kN + col), k = bf2(rs + V_K * kTile + t * kN + col);
-          const float2 b = bf2(rs + V_B * kTile + t * kN + col), a = bf2(rs + V_A * kTile + t * kN + col);
-          const float cv[2] = {c.x, c.y}, icv[2] = {ic.x, ic.y}, cpv[2] = {cp.x, cp.y};
-          const float rv[2] = {r.x, r.y}, kv[2] = {k.x, k.y}, bv[2] = {b.x, b.y}, av[2] = {a.x, a.y};
+          if (grp == 0) {
+            const float2 k = bf2(rs + V_K * kTile + t * kN + col), b = bf2(rs + V_B * kTile + t * kN + col);
+            const float ic[2] = {rcp_approx(c.x), rcp_approx(c.y)}, kv[2] = {k.x, k.y}, bv[2] = {b.x, b.y};
 #pragma unroll
-          for (int e = 0; e < 2; ++e) {
-            const int q = 2 * h + e;
-            dr[q] = bR[q] * cv[e];
-            dk[q] = bK[q] * icv[e];
-            db[q] = bB[q] * icv[e];
-            da[q] = bA[q] * cpv[e];
-            ada[q] = av[e] * da[q];
-            x[q] = rv[e] * dr[q] - kv[e] * dk[q] - bv[e] * db[q] + ada[q];
+            for (int e = 0; e < 2; ++e) {
+              P0[nt][2 * h + e] *= ic[e];
+              P1[nt][2 * h + e] *= ic[e];
+              X[nt][2 * h + e] = -kv[e] * P0[nt][2 * h + e] - bv[e] * P1[nt][2 * h + e];
+              AD[nt][2 * h + e] = 0.f;
+            }
+          } else {
+            const float2 cp = t ? *reinterpret_cast<const float2*>(op.cS + (t - 1) * kN + col) : make_float2(1.f, 1.f);
+            const float2 r = bf2(rs + V_R * kTile + t * kN + col), a = bf2(rs + V_A * kTile + t * kN + col);
+            const float cv[2] = {c.x, c.y}, cpv[2] = {cp.x, cp.y}, rv[2] = {r.x, r.y}, av[2] = {a.x, a.y};
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+              P0[nt][2 * h + e] *= cv[e];
+              P1[nt][2 * h + e] *= cpv[e];
+              AD[nt][2 * h + e] = av[e] * P1[nt][2 * h + e];
+              X[nt][2 * h + e] = rv[e] * P0[nt][2 * h + e] + AD[nt][2 * h + e];
+            }
           }
         }
-        // w dw from the identity, anchored where fewer terms are summed:
-        // rows t < 8: colsum(next carry o S0) - sum_{u<t} x(u) - a(t) da(t);
-        // rows t >= 8: sum_{u>=t} x(u) - a(t) da(t) + colsum(Gc o S(L)).
-        float dw[4];
+      // exchange with the partner warp of the other group (same columns): grp 0 keeps
+      // dw of n-tile 0, grp 1 of n-tile 1. The carry tile is free in this phase.
+      float* XK = sm.GcS;                   // grp 0's x part, [t][j] stride 72
+      float* XR = sm.GcS + kL * kLD64;      // grp 1's x part
+      float* XA = sm.GcS + 2 * kL * kLD64;  // grp 1's a da
 #pragma unroll
-        for (int e = 0; e < 2; ++e) {
-          float hi2 = x[2 + e], lo = x[e];
-#pragma unroll
-          for (int d = 1; d < 8; d <<= 1) {
-            const float oh = __shfl_down_sync(0xffffffffu, hi2, 4 * d);
-            const float ol = __shfl_up_sync(0xffffffffu, lo, 4 * d);
-            if (g + d < 8) hi2 += oh;
-            if (g >= d) lo += ol;
-          }
-          const int col = j0 + 2 * t4 + e;
-          const float(&sp)[4][kN] = sm.spart[n & 1];
-          const float start = sp[0][col] + sp[1][col] + sp[2][col] + sp[3][col];
-          const float2 w0 = bf2(rs + V_W * kTile + g * kN + j0 + 2 * t4);
-          const float2 w1 = bf2(rs + V_W * kTile + (g + 8) * kN + j0 + 2 * t4);
-          dw[e] = (start - (lo - x[e]) - ada[e]) * rcp_approx(e ? w0.y : w0.x);
-          const float(&bp)[4][kN] = sm.spart[(n + 1) & 1];
-          const float bnd = bp[0][col] + bp[1][col] + bp[2][col] + bp[3][col];
-          dw[2 + e] = (hi2 - ada[2 + e] + bnd) * rcp_approx(e ? w1.y : w1.x);
+      for (int h = 0; h < 2; ++h) {
+        const int t = g + 8 * h;
+        if (grp == 0) {
+          *reinterpret_cast<float2*>(XK + t * kLD64 + j0 + 8 + 2 * t4) = make_float2(X[1][2 * h], X[1][2 * h + 1]);
+        } else {
+          *reinterpret_cast<float2*>(XR + t * kLD64 + j0 + 2 * t4) = make_float2(X[0][2 * h], X[0][2 * h + 1]);
+          *reinterpret_cast<float2*>(XA + t * kLD64 + j0 + 2 * t4) = make_float2(AD[0][2 * h], AD[0][2 * h + 1]);
         }
+      }
+      named_bar(3 + jb, 64);
+      const int nw = grp, jw = j0 + 8 * nw;  // this warp's dw columns jw .. jw+7
+      float xw[4], adw[4];
 #pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          const int t = g + 8 * h;
-          if (t < len) {
-            const size_t off = o.base + (size_t)t * vstep + j0 + 2 * t4;
-            *reinterpret_cast<float2*>(args.dr + off) = make_float2(dr[2 * h], dr[2 * h + 1]);
-            *reinterpret_cast<float2*>(args.dk + off) = make_float2(dk[2 * h], dk[2 * h + 1]);
-            *reinterpret_cast<float2*>(args.db + off) = make_float2(db[2 * h], db[2 * h + 1]);
-            *reinterpret_cast<float2*>(args.da + off) = make_float2(da[2 * h], da[2 * h + 1]);
-            *reinterpret_cast<float2*>(args.dw + off) = make_float2(dw[2 * h], dw[2 * h + 1]);
+      for (int h = 0; h < 2; ++h) {
+        const int t = g + 8 * h;
+        if (grp == 0) {
+          const float2 xr = *reinterpret_cast<const float2*>(XR + t * kLD64 + jw + 2 * t4);
+          const float2 xa = *reinterpret_cast<const float2*>(XA + t * kLD64 + jw + 2 * t4);
+          xw[2 * h] = X[0][2 * h] + xr.x;
+          xw[2 * h + 1] = X[0][2 * h + 1] + xr.y;
+          adw[2 * h] = xa.x;
+          adw[2 * h + 1] = xa.y;
+        } else {
+          const float2 xk = *reinterpret_cast<const float2*>(XK + t * kLD64 + jw + 2 * t4);
+          xw[2 * h] = X[1][2 * h] + xk.x;
+          xw[2 * h + 1] = X[1][2 * h + 1] + xk.y;
+          adw[2 * h] = AD[1][2 * h];
+          adw[2 * h + 1] = AD[1][2 * h + 1];
+        }
+      }
+      // w dw from the identity, anchored where fewer terms are summed:
+      // rows t < 8: colsum(next carry o S0) - sum_{u<t} x(u) - a(t) da(t);
+      // rows t >= 8: sum_{u>=t} x(u) - a(t) da(t) + colsum(Gc o S(L)).
+      float dw[4];
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        float hi2 = xw[2 + e], lo = xw[e];
+#pragma unroll
+        for (int d = 1; d < 8; d <<= 1) {
+          const float oh = __shfl_down_sync(0xffffffffu, hi2, 4 * d);
+          const float ol = __shfl_up_sync(0xffffffffu, lo, 4 * d);
+          if (g + d < 8) hi2 += oh;
+          if (g >= d) lo += ol;
+        }
+        const int col = jw + 2 * t4 + e;
+        const float(&sp)[4][kN] = sm.spart[n & 1];
+        const float start = sp[0][col] + sp[1][col] + sp[2][col] + sp[3][col];
+        const float(&bp)[4][kN] = sm.spart[(n + 1) & 1];
+        const float bnd = bp[0][col] + bp[1][col] + bp[2][col] + bp[3][col];
+        const float2 w0 = bf2(rs + V_W * kTile + g * kN + jw + 2 * t4);
+        const float2 w1 = bf2(rs + V_W * kTile + (g + 8) * kN + jw + 2 * t4);
+        dw[e] = (start - (lo - xw[e]) - adw[e]) * rcp_approx(e ? w0.y : w0.x);
+        dw[2 + e] = (hi2 - adw[2 + e] + bnd) * rcp_approx(e ? w1.y : w1.x);
+      }
+      float* out0 = grp ? args.dr : args.dk;
+      float* out1 = grp ? args.da : args.db;
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const int t = g + 8 * h;
+        if (t < len) {
+          const size_t off = o.base + (size_t)t * vstep + j0 + 2 * t4;
+#pragma unroll
+          for (int nt = 0; nt < 2; ++nt) {
+            *reinterpret_cast<float2*>(out0 + off + 8 * nt) = make_float2(P0[nt][2 * h], P0[nt][2 * h + 1]);
+            *reinterpret_cast<float2*>(out1 + off + 8 * nt) = make_float2(P1[nt][2 * h], P1[nt][2 * h + 1]);
           }
+          *reinterpret_cast<float2*>(args.dw + off + 8 * nw) = make_float2(dw[2 * h], dw[2 * h + 1]);
         }
       }
     }
