@@ -232,11 +232,20 @@ int backward_impl(bool bf16, const void* const in[7], const float* s_init, const
   rc = check_spans(ins, 9, outs, 7, 7, 6);
   if (rc) return rc;
 
-  if (!ckpt) {
+  // bf16 inputs at N = 64 with 16-step checkpoints take a chunked tensor-core
+  // backward: the fused one (one CTA per head) or, with WKV7_SPLIT_BACKWARD=1,
+  // the split one (carry chain + parallel output pass), which keeps the carry
+  // of every chunk in the workspace too.
+  const bool chunked = bf16 && N == 64 && C_eff == kChunk;
+  const char* split_env = std::getenv("WKV7_SPLIT_BACKWARD");
+  const bool split = chunked && split_env && split_env[0] == '1';
+  const size_t ck_ws = ckpt ? 0 : (ckpt_bytes(B, T, H, N, C_eff) + 255) / 256 * 256;
+  const size_t ws_bytes = ck_ws + (split ? bwd4_workspace_bytes(B, T, H) : 0);
+  if (ws_bytes) {
     // Fault injection for tests: make the workspace allocation fail.
     const char* inject = std::getenv("WKV7_FAIL_ALLOC");
     if (inject && inject[0] == '1')
-      return fail(WKV7_ERR_ALLOC, "checkpoint workspace allocation failed (injected by WKV7_FAIL_ALLOC)");
+      return fail(WKV7_ERR_ALLOC, "workspace allocation failed (injected by WKV7_FAIL_ALLOC)");
   }
 
   BwdArgs args;
@@ -245,13 +254,14 @@ int backward_impl(bool bf16, const void* const in[7], const float* s_init, const
     if ((rc = make_map(&args.map[v], in[v], bf16, B, T, H, N, KS))) return rc;
 
   float* ws = nullptr;
-  if (!ckpt) {
-    const size_t bytes = ckpt_bytes(B, T, H, N, C_eff);
-    cudaError_t e = cudaMallocAsync(reinterpret_cast<void**>(&ws), bytes, stream);
+  if (ws_bytes) {
+    cudaError_t e = cudaMallocAsync(reinterpret_cast<void**>(&ws), ws_bytes, stream);
     if (e != cudaSuccess) {
       cudaGetLastError();
-      return fail(WKV7_ERR_ALLOC, "checkpoint workspace of %zu bytes: %s", bytes, cudaGetErrorString(e));
+      return fail(WKV7_ERR_ALLOC, "backward workspace of %zu bytes: %s", ws_bytes, cudaGetErrorString(e));
     }
+  }
+  if (!ckpt) {
     FwdArgs fa;
     const int K = fwd_steps_per_stage(N, bf16);
     for (int v = 0; v < 6; ++v)
@@ -272,7 +282,7 @@ int backward_impl(bool bf16, const void* const in[7], const float* s_init, const
     fa.B = B;
     fa.T = T;
     fa.H = H;
-    e = use_chunked(bf16, N, C_eff) ? launch_fwd3(fa, stream) : launch_fwd2(fa, bf16, N, stream);
+    cudaError_t e = use_chunked(bf16, N, C_eff) ? launch_fwd3(fa, stream) : launch_fwd2(fa, bf16, N, stream);
     if (e != cudaSuccess) {
       cudaFreeAsync(ws, stream);
       return fail_cuda(e, "checkpointing forward launch");
@@ -294,12 +304,13 @@ int backward_impl(bool bf16, const void* const in[7], const float* s_init, const
   args.da = grads[4];
   args.db = grads[5];
   args.dS_init = dS_init;
+  args.carry = split ? ws + ck_ws / sizeof(float) : nullptr;
   args.C = C_eff;
   args.nck = (T + C_eff - 1) / C_eff;
   args.B = B;
   args.T = T;
   args.H = H;
-  cudaError_t e = (bf16 && N == 64 && C_eff == kChunk) ? launch_bwd3(args, stream) : launch_bwd2(args, bf16, N, stream);
+  cudaError_t e = split ? launch_bwd4(args, stream) : chunked ? launch_bwd3(args, stream) : launch_bwd2(args, bf16, N, stream);
   if (ws) {
     cudaError_t e2 = cudaFreeAsync(ws, stream);
     if (e == cudaSuccess && e2 != cudaSuccess) return fail_cuda(e2, "cudaFreeAsync(workspace)");

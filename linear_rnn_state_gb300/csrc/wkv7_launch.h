@@ -34,6 +34,7 @@ struct BwdArgs {
   float* da;
   float* db;
   float* dS_init;  // [B][H][N][N] or null
+  float* carry;    // split backward: [B*H][nchunks][N][N] carry after each chunk
   unsigned* status;
   int C, nck;
   int B, T, H;
@@ -51,6 +52,10 @@ cudaError_t launch_fwd2(const FwdArgs& args, bool bf16, int N, cudaStream_t stre
 cudaError_t launch_fwd3(const FwdArgs& args, cudaStream_t stream);
 // Chunked tensor-core backward: bf16 inputs, N = 64, checkpoints every 16 steps.
 cudaError_t launch_bwd3(const BwdArgs& args, cudaStream_t stream);
+// The same backward as a carry-chain kernel plus a parallel per-chunk output
+// kernel; needs args.carry, a workspace of bwd4_workspace_bytes.
+cudaError_t launch_bwd4(const BwdArgs& args, cudaStream_t stream);
+size_t bwd4_workspace_bytes(int B, int T, int H);
 constexpr int kChunk = 16;
 inline bool use_chunked(bool bf16, int N, int C) { return bf16 && N == 64 && C % kChunk == 0; }
 cudaError_t launch_bwd(const BwdArgs& args, bool bf16, int N, cudaStream_t stream);

@@ -19,8 +19,8 @@ GRADS = ("dr", "dw", "dk", "dv", "da", "db")
 REL_L2 = 2e-2
 
 
-@pytest.fixture(scope="module")
-def env():
+@pytest.fixture(scope="module", params=["fused", "split"])
+def env(request):
     if not torch.cuda.is_available():
         pytest.skip("no CUDA device")
     import __graft_entry__  # noqa: F401
@@ -30,7 +30,14 @@ def env():
     _build.build()
     wkv7.load()
     torch.cuda.set_device(0)
-    return oracle, inputs, wkv7
+    # the backward variant is chosen per call from the environment
+    import os
+    if request.param == "split":
+        os.environ["WKV7_SPLIT_BACKWARD"] = "1"
+    else:
+        os.environ.pop("WKV7_SPLIT_BACKWARD", None)
+    yield oracle, inputs, wkv7
+    os.environ.pop("WKV7_SPLIT_BACKWARD", None)
 
 
 def _bf16_bits(x):
