@@ -359,9 +359,11 @@ def _report(args, wl, world, B, T, H, N, C, bf16, ms, fwd_ms, bwd_ms, e2e, ckpt,
     line = {
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "tf32" if (bf16 and N == 64) else "f32", "data": "synthetic",
-        "arithmetic": ("tf32 tensor-core products with fp32 accumulation; fp32 state, carry and element-wise math"
-                       if (bf16 and N == 64) else "fp32 throughout") + "; inputs, dy and y stored in " + wl.storage,
+        "vs_baseline": None, "dtype": "bf16" if (bf16 and N == 64) else "f32", "data": "synthetic",
+        "arithmetic": ("tensor-core products with fp32 accumulation: tf32 operands in the forward and the backward's "
+                       "carry chain, bf16 operands in the backward's per-chunk gradient products; fp32 state, carry "
+                       "and element-wise math" if (bf16 and N == 64) else "fp32 throughout")
+                      + "; inputs, dy and y stored in " + wl.storage,
         "config": {"workload": wl.name if T == wl.T else f"{wl.name} (T={T})", "B": B, "T": T, "H": H, "N": N, "storage": wl.storage, "ckpt_every": C,
                    "l2": "no flush: inputs, checkpoints and gradients (%.1f GB) exceed the 129 MB L2"
                          % ((7 * BTH * N * (2 if bf16 else 4) + ckpt.numel() * 4 + 6 * BTH * N * 4) / 1e9)},
@@ -376,7 +378,7 @@ def _report(args, wl, world, B, T, H, N, C, bf16, ms, fwd_ms, bwd_ms, e2e, ckpt,
         "e2e": None if e2e is None else {
             "value": aggregate_tokens_per_s(world, B, T, e2e[0]), "unit": "tokens/s", "h2d_bytes_per_step": e2e[1],
             "d2h_bytes_per_step": e2e[2]},
-        "gpu_launches": 2 * args.steps,
+        "gpu_launches": (3 if (bf16 and N == 64) else 2) * args.steps,
         "clocks": clocks.summary(),
     }
     if cpu_v is not None:

@@ -233,12 +233,12 @@ int backward_impl(bool bf16, const void* const in[7], const float* s_init, const
   if (rc) return rc;
 
   // bf16 inputs at N = 64 with 16-step checkpoints take a chunked tensor-core
-  // backward: the fused one (one CTA per head) or, with WKV7_SPLIT_BACKWARD=1,
-  // the split one (carry chain + parallel output pass), which keeps the carry
-  // of every chunk in the workspace too.
+  // backward: the split one (carry chain + parallel output pass), which keeps
+  // the carry of every chunk in the workspace too, or, with
+  // WKV7_SPLIT_BACKWARD=0, the fused one (one CTA per head).
   const bool chunked = bf16 && N == 64 && C_eff == kChunk;
   const char* split_env = std::getenv("WKV7_SPLIT_BACKWARD");
-  const bool split = chunked && split_env && split_env[0] == '1';
+  const bool split = chunked && !(split_env && split_env[0] == '0');
   const size_t ck_ws = ckpt ? 0 : (ckpt_bytes(B, T, H, N, C_eff) + 255) / 256 * 256;
   const size_t ws_bytes = ck_ws + (split ? bwd4_workspace_bytes(B, T, H) : 0);
   if (ws_bytes) {
@@ -305,6 +305,7 @@ int backward_impl(bool bf16, const void* const in[7], const float* s_init, const
   args.db = grads[5];
   args.dS_init = dS_init;
   args.carry = split ? ws + ck_ws / sizeof(float) : nullptr;
+  for (int v = 0; v < 7; ++v) args.in[v] = in[v];
   args.C = C_eff;
   args.nck = (T + C_eff - 1) / C_eff;
   args.B = B;

@@ -26,14 +26,15 @@
 // Only the carry Gc is sequential over chunks, and it needs neither k, v
 // nor the state: DSA^T = Gc (T^T Bb)^T + DY^T (Mbr T). So the backward runs
 // as two kernels:
-//  * wkv7_bwd4_carry_kernel - one CTA per (b, h), chunks in reverse: eight
-//    "prep" warps form the next chunk's R^, A^, DY, T^T Bb and Mbr T while
-//    four "state" warps (16 rows of Gc each, as accumulator tiles) advance
-//    the carry with three small products. It stores Gc for every chunk (as
-//    tf32 values) and dS_init.
+//  * wkv7_bwd4_carry_kernel - one CTA per (b, h), chunks in reverse, a
+//    three-stage pipeline of warp groups: four "state" warps (16 rows of Gc
+//    each, as accumulator tiles) advance the carry through chunk n with three
+//    small products, four warps finish chunk n-1's T^T Bb and Mbr T, four
+//    form chunk n-2's scaled R^, A^, B~, Bb and DY. It stores Gc for every
+//    chunk (as bf16) and dS_init.
 //  * wkv7_bwd4_out_kernel - one CTA per (b, h, chunk), all independent: from
 //    the chunk's inputs, checkpoint and stored carry it forms every gradient
-//    of the chunk. Two CTAs share an SM. The dw anchors come from the
+//    of the chunk. Three CTAs share an SM. The dw anchors come from the
 //    chunk's own column products: with S(L) = S0 diag(c(L)) + V^T Kb + SA^T Bb,
 //      colsum(Gc o S(L)) = c(L) colsum(Gc o S0) + sum_t (Kb o V Gc + Bb o SA Gc)
 //      colsum(Gc' o S0)  = c(L) colsum(Gc o S0) + sum_t (R^ o DY S0 + A^ o DSA S0).
@@ -51,8 +52,6 @@ constexpr int kN = 64, kL = 16;
 constexpr int kLD64 = 72;  // row stride (floats) of 64-wide operands read along k
 constexpr int kLD16 = 24;  // row stride of 16-wide operands
 constexpr int kLDT = 68;   // row stride of operands read only as [k][n] B operands
-constexpr int kLDS = 72;   // row stride of checkpoints in the carry kernel (read along rows)
-constexpr int kLDG = 68;   // row stride of checkpoint and carry in the output kernel (read down columns)
 constexpr int kTile = kL * kN;
 constexpr int kThreads = 256;
 enum { V_R = 0, V_W = 1, V_K = 2, V_V = 3, V_A = 4, V_B = 5, V_DY = 6 };
@@ -62,6 +61,104 @@ __device__ __forceinline__ float2 bf2(const __nv_bfloat16* p) {
   return __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(p));
 }
 __device__ __forceinline__ float2 tf32r2(float2 x) { return make_float2(tf32r(x.x), tf32r(x.y)); }
+
+// ----------------------------------------------------------- bf16 operands ---
+
+constexpr int kB64 = 72;  // row stride (bf16 elements) of 64-wide tiles
+constexpr int kB16 = 24;  // row stride of 16-wide tiles
+typedef __nv_bfloat16 bf16_t;
+
+__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
+  uint32_t r;
+  asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+__device__ __forceinline__ float2 unpack_bf16(uint32_t u) {
+  return make_float2(__uint_as_float(u << 16), __uint_as_float(u & 0xFFFF0000u));
+}
+__device__ __forceinline__ void st_pair(bf16_t* p, float2 x) { *reinterpret_cast<uint32_t*>(p) = pack_bf16(x.x, x.y); }
+
+// d += a * b for one 16 x 8 x 16 tile (bf16 inputs, fp32 accumulation).
+__device__ __forceinline__ void mma16(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+  asm("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%0,%1,%2,%3};\n"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+__device__ __forceinline__ void ldsm4(uint32_t (&r)[4], const bf16_t* p) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(smem_addr(p)));
+}
+__device__ __forceinline__ void ldsm4t(uint32_t (&r)[4], const bf16_t* p) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(smem_addr(p)));
+}
+__device__ __forceinline__ void stsm4t(bf16_t* p, const uint32_t (&r)[4]) {
+  asm volatile("stmatrix.sync.aligned.m8n8.x4.trans.shared.b16 [%0], {%1,%2,%3,%4};" ::"r"(smem_addr(p)), "r"(r[0]),
+               "r"(r[1]), "r"(r[2]), "r"(r[3])
+               : "memory");
+}
+
+// Fragment loads for one k16 block. "A" is 16 rows (m) x 16 k, "B" two n8
+// tiles x 16 k (r[0], r[1] for columns n0 .. n0+7, r[2], r[3] for n0+8 ..).
+// Storage is row-major with stride ld; the suffix says how it is laid out:
+//   a_mk: A[m][k] stored [m][k];  a_km: stored [k][m] (transposed load)
+//   b_nk: B^T[n][k] stored [n][k]; b_kn: B[k][n] stored [k][n] (transposed load)
+__device__ __forceinline__ void a_mk(uint32_t (&r)[4], const bf16_t* s, int ld, int m0, int k0, int lane) {
+  ldsm4(r, s + (m0 + (lane & 7) + ((lane >> 3) & 1) * 8) * ld + k0 + (lane >> 4) * 8);
+}
+__device__ __forceinline__ void a_km(uint32_t (&r)[4], const bf16_t* s, int ld, int m0, int k0, int lane) {
+  ldsm4t(r, s + (k0 + (lane & 7) + (lane >> 4) * 8) * ld + m0 + ((lane >> 3) & 1) * 8);
+}
+__device__ __forceinline__ void b_nk(uint32_t (&r)[4], const bf16_t* s, int ld, int n0, int k0, int lane) {
+  ldsm4(r, s + (n0 + (lane & 7) + (lane >> 4) * 8) * ld + k0 + ((lane >> 3) & 1) * 8);
+}
+__device__ __forceinline__ void b_kn(uint32_t (&r)[4], const bf16_t* s, int ld, int n0, int k0, int lane) {
+  ldsm4t(r, s + (k0 + (lane & 7) + ((lane >> 3) & 1) * 8) * ld + n0 + (lane >> 4) * 8);
+}
+// Two accumulator tiles (columns k0 .. k0+7 and k0+8 .. k0+15 of 16 rows) as
+// the A fragment of a product over those 16 columns.
+__device__ __forceinline__ void c2a16(uint32_t (&a)[4], const float (&lo)[4], const float (&hi)[4]) {
+  a[0] = pack_bf16(lo[0], lo[1]);
+  a[1] = pack_bf16(lo[2], lo[3]);
+  a[2] = pack_bf16(hi[0], hi[1]);
+  a[3] = pack_bf16(hi[2], hi[3]);
+}
+// acc[nt] += A B over K = 16 * KB for two n8 tiles, A from [m][k], B from [n][k].
+template <int KB>
+__device__ __forceinline__ void mm_mk_nk(float (&acc)[2][4], const bf16_t* A, int lda, int m0, const bf16_t* Bt, int ldb,
+                                         int n0, int lane) {
+#pragma unroll
+  for (int kb = 0; kb < KB; ++kb) {
+    uint32_t a[4], b[4];
+    a_mk(a, A, lda, m0, 16 * kb, lane);
+    b_nk(b, Bt, ldb, n0, 16 * kb, lane);
+    mma16(acc[0], a, b[0], b[1]);
+    mma16(acc[1], a, b[2], b[3]);
+  }
+}
+// Store a 16 x 16 fp32 accumulator (tiles acc[0], acc[1]) as bf16 [t][s],
+// keeping lower: s < t (+ diagonal if incl), upper: s > t (+ diagonal if incl).
+__device__ __forceinline__ void store_masked16(const float (&acc)[2][4], bf16_t* dst, bool lower, bool incl, int g,
+                                               int t4) {
+#pragma unroll
+  for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const int t = g + 8 * h, s = 8 * nt + 2 * t4;
+      float x[2];
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        const int se = s + e;
+        const bool keep = lower ? (se < t || (incl && se == t)) : (se > t || (incl && se == t));
+        x[e] = keep ? acc[nt][2 * h + e] : 0.f;
+      }
+      st_pair(dst + t * kB16 + s, make_float2(x[0], x[1]));
+    }
+}
+
 
 // acc = P Q^T for 16-row P, Q (ld kLD64, tf32 values), K = 64.
 __device__ __forceinline__ void gram16(float (&acc)[2][4], const float* P, const float* Q, int g, int t4) {
@@ -151,9 +248,8 @@ __device__ __forceinline__ void fetch_state(float* dst, const float* src, int ti
 // ================================================================ carry ===
 
 enum { C_R = 0, C_W = 1, C_A = 2, C_B = 3, C_DY = 4 };  // vectors staged for the carry
-constexpr int kCarryStages = 3;
-constexpr int kCarryThreads = 384;  // warps 0-3: state; warps 4-11: prep
-constexpr int kPrepThreads = 256;
+constexpr int kCarryStages = 4;
+constexpr int kCarryThreads = 384;  // warps 0-3: state; 4-7: forming (F); 8-11: products (P)
 
 // Operands of one chunk for the carry update (tf32 values unless noted).
 struct OpC {
@@ -167,24 +263,28 @@ struct OpC {
   int pad_[3];
 };
 
+// Scaled operands only the products group reads (one set per chunk in flight).
+struct ScratchC {
+  float Ah[kL * kLD64], Bt[kL * kLD64];  // A^, B~ [t][j]
+  float Bb68[kL * kLDT];                 // Bb [t][j]
+};
+
 struct CarrySmem {
   __nv_bfloat16 raw[kCarryStages][5][kTile];  // r, w, a, b, dy of one chunk per stage
-  OpC op[2];
-  // prep scratch (one chunk at a time)
-  float Ah[kL * kLD64], Bt[kL * kLD64];                   // A^, B~ [t][j]
-  float Bb68[kL * kLDT];                                  // Bb [t][j]
+  OpC op[3];
+  ScratchC sc[2];
   float Mbr[kL * kLD16], Mba[kL * kLD16], TT[kL * kLD16];  // [t][s]; TT = T^T
   uint64_t full[kCarryStages];
   int abort_flag;
 };
 
-// Scaled operands of a chunk for the carry. 256 prep threads; thread
-// (lane, pw) forms columns 2 lane, 2 lane + 1 of steps 2 pw, 2 pw + 1. The
+// Forming group (128 threads): the scaled operands of a chunk. Thread
+// (lane, pf) forms columns 2 lane, 2 lane + 1 of steps 4 pf .. 4 pf + 3. The
 // running products c(t) are taken in step order from t = 0 in every thread
 // (the output kernel forms the same values). Returns (uniformly over the
-// prep warps) whether some decay leaves the range of the scaled form.
-__device__ bool prep_carry(CarrySmem& sm, const __nv_bfloat16* rs, OpC& op, int len, int ptid) {
-  const int lane = ptid & 31, pw = ptid >> 5, j = 2 * lane, t0 = 2 * pw;
+// group) whether some decay leaves the range of the scaled form.
+__device__ bool form_carry(ScratchC& sc, const __nv_bfloat16* rs, OpC& op, int len, int ftid) {
+  const int lane = ftid & 31, pf = ftid >> 5, j = 2 * lane, t0 = 4 * pf;
   bool safe = true;
   float2 cL = make_float2(1.f, 1.f), cpre = cL;  // cpre = c(t0 - 1)
 #pragma unroll
@@ -194,11 +294,11 @@ __device__ bool prep_carry(CarrySmem& sm, const __nv_bfloat16* rs, OpC& op, int 
     cL = fmul2(cL, w);
     if (t < t0) cpre = cL;
   }
-  if (named_bar_or(1, kPrepThreads, !safe)) return true;
-  if (pw == 0) *reinterpret_cast<float2*>(op.cL + j) = cL;
-  float2 wv[2], av[2], rv[2], bv[2], dyv[2];
+  if (named_bar_or(1, 128, !safe)) return true;
+  if (pf == 0) *reinterpret_cast<float2*>(op.cL + j) = cL;
+  float2 wv[4], av[4], rv[4], bv[4], dyv[4];
 #pragma unroll
-  for (int e = 0; e < 2; ++e) {
+  for (int e = 0; e < 4; ++e) {
     const int o = (t0 + e) * kN + j;
     wv[e] = t0 + e < len ? bf2(rs + C_W * kTile + o) : make_float2(1.f, 1.f);
     av[e] = bf2(rs + C_A * kTile + o);
@@ -208,63 +308,74 @@ __device__ bool prep_carry(CarrySmem& sm, const __nv_bfloat16* rs, OpC& op, int 
   }
   float2 c = cpre;
 #pragma unroll
-  for (int e = 0; e < 2; ++e) {
+  for (int e = 0; e < 4; ++e) {
     const int t = t0 + e, q = t * kLD64 + j, q68 = t * kLDT + j;
     const float2 cprev = c;
     c = fmul2(c, wv[e]);
     const float2 ic = make_float2(rcp_approx(c.x), rcp_approx(c.y));
     const float2 ah = tf32r2(fmul2(av[e], cprev));
-    *reinterpret_cast<float2*>(sm.Ah + q) = ah;
+    *reinterpret_cast<float2*>(sc.Ah + q) = ah;
     *reinterpret_cast<float2*>(op.Ah68 + q68) = ah;
     *reinterpret_cast<float2*>(op.Rh + q) = tf32r2(fmul2(rv[e], c));
-    *reinterpret_cast<float2*>(sm.Bt + q) = tf32r2(fmul2(bv[e], ic));
-    *reinterpret_cast<float2*>(sm.Bb68 + q68) = tf32r2(fmul2(bv[e], fmul2(cL, ic)));
+    *reinterpret_cast<float2*>(sc.Bt + q) = tf32r2(fmul2(bv[e], ic));
+    *reinterpret_cast<float2*>(sc.Bb68 + q68) = tf32r2(fmul2(bv[e], fmul2(cL, ic)));
     *reinterpret_cast<float2*>(op.DYs + q) = dyv[e];
   }
   return false;
 }
 
-// Prep warps: wait for a chunk's inputs, form its operands, Mbr, Mba, T,
-// T^T Bb and Mbr T. Returns false on a timeout.
-__device__ bool front_carry(CarrySmem& sm, OpC& op, const __nv_bfloat16* rs, uint64_t* bar, uint32_t parity, int len,
-                            unsigned* status) {
-  const int ptid = threadIdx.x - 128, pw = ptid >> 5, lane = threadIdx.x & 31, g = lane >> 2, t4 = lane & 3;
+// Forming group: wait for a chunk's inputs and form its operands. Returns
+// false on a timeout.
+__device__ bool front_form(CarrySmem& sm, ScratchC& sc, OpC& op, const __nv_bfloat16* rs, uint64_t* bar,
+                           uint32_t parity, int len, unsigned* status) {
+  const int ftid = threadIdx.x - 128;
   const bool ok = mbar_wait_bounded(status, bar, parity);
-  if (named_bar_or(1, kPrepThreads, !ok)) {
-    if (ptid == 0) sm.abort_flag = 1;
+  if (named_bar_or(1, 128, !ok)) {
+    if (ftid == 0) sm.abort_flag = 1;
     return false;
   }
-  const bool unsafe = prep_carry(sm, rs, op, len, ptid);
-  if (ptid == 0) op.unsafe = unsafe;
-  if (unsafe) return true;
-  named_bar(1, kPrepThreads);
-  if (pw < 2) {  // Mbr = R^ B~^T (with diagonal), Mba = A^ B~^T (strictly lower), then T
+  const bool unsafe = form_carry(sc, rs, op, len, ftid);
+  if (ftid == 0) op.unsafe = unsafe;
+  return true;
+}
+
+// Products group (128 threads): Mbr, Mba, T, T^T Bb and Mbr T of a formed chunk.
+__device__ void front_products(CarrySmem& sm, const ScratchC& sc, OpC& op) {
+  const int pp = (threadIdx.x >> 5) - 8, lane = threadIdx.x & 31, g = lane >> 2, t4 = lane & 3;
+  if (pp < 2) {  // Mbr = R^ B~^T (with diagonal), Mba = A^ B~^T (strictly lower), then T
     float acc[2][4];
-    gram16(acc, pw ? sm.Ah : op.Rh, sm.Bt, g, t4);
-    store_masked(acc, pw ? sm.Mba : sm.Mbr, true, pw == 0, g, t4);
-    if (pw == 1) {
+    gram16(acc, pp ? sc.Ah : op.Rh, sc.Bt, g, t4);
+    store_masked(acc, pp ? sm.Mba : sm.Mbr, true, pp == 0, g, t4);
+    if (pp == 1) {
       __syncwarp();
       unit_lower_inverse(sm.Mba, nullptr, sm.TT, lane);
     }
   }
-  named_bar(1, kPrepThreads);
-  {  // T^T Bb, n-tile pw
-    float acc[4];
-    zero4(acc);
+  named_bar(2, 128);
+  {  // T^T Bb, n-tiles 2 pp and 2 pp + 1
+    float acc[2][4];
+    zero4(acc[0]);
+    zero4(acc[1]);
 #pragma unroll
     for (int kb = 0; kb < 2; ++kb) {
-      uint32_t a[4], b0, b1;
+      uint32_t a[4];
       frag_a(a, sm.TT, kLD16, 0, 8 * kb, g, t4);
-      frag_b_t(b0, b1, sm.Bb68, kLDT, 8 * pw, 8 * kb, g, t4);
-      mma_tf32(acc, a, b0, b1);
+#pragma unroll
+      for (int nt = 0; nt < 2; ++nt) {
+        uint32_t b0, b1;
+        frag_b_t(b0, b1, sc.Bb68, kLDT, 8 * (2 * pp + nt), 8 * kb, g, t4);
+        mma_tf32(acc[nt], a, b0, b1);
+      }
     }
 #pragma unroll
-    for (int h = 0; h < 2; ++h)
-      *reinterpret_cast<float2*>(op.Btp + (g + 8 * h) * kLD64 + 8 * pw + 2 * t4) =
-          make_float2(tf32r(acc[2 * h]), tf32r(acc[2 * h + 1]));
+    for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+      for (int h = 0; h < 2; ++h)
+        *reinterpret_cast<float2*>(op.Btp + (g + 8 * h) * kLD64 + 8 * (2 * pp + nt) + 2 * t4) =
+            make_float2(tf32r(acc[nt][2 * h]), tf32r(acc[nt][2 * h + 1]));
   }
-  if (pw >= 6) {  // W = Mbr T, n-tile pw - 6
-    const int q = pw - 6;
+  if (pp >= 2) {  // W = Mbr T, n-tile pp - 2
+    const int q = pp - 2;
     float acc[4];
     zero4(acc);
 #pragma unroll
@@ -279,7 +390,6 @@ __device__ bool front_carry(CarrySmem& sm, OpC& op, const __nv_bfloat16* rs, uin
       *reinterpret_cast<float2*>(op.W + (g + 8 * h) * kLD16 + 8 * q + 2 * t4) =
           make_float2(tf32r(acc[2 * h]), tf32r(acc[2 * h + 1]));
   }
-  return true;
 }
 
 // One chunk of the carry (state warp, rows i0 .. i0+15 of G):
@@ -377,63 +487,83 @@ __global__ void __launch_bounds__(kCarryThreads, 1) wkv7_bwd4_carry_kernel(const
   const int T = args.T, H = args.H;
   const int head = blockIdx.x, bi = head / H, hi = head % H;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, g = lane >> 2, t4 = lane & 3;
-  const bool is_prep = warp >= 4;
-  const int i0 = 16 * warp;  // state warps: rows of the carry
+  const int role = warp < 4 ? 0 : warp < 8 ? 1 : 2;  // state, forming, products
+  const int i0 = 16 * warp;                          // state warps: rows of the carry
   const int nchunks = (T + kL - 1) / kL;
   constexpr int kStageBytes = 5 * kTile * 2;
-  float* carry_head = args.carry + (size_t)head * nchunks * kN * kN;
+  bf16_t* carry_head = reinterpret_cast<bf16_t*>(args.carry) + (size_t)head * nchunks * kN * kN;
 
-  // chunks are visited in reverse; visit m handles chunk nchunks-1-m
-  auto issue = [&](int m) {
-    const int st = m % kCarryStages, chunk = nchunks - 1 - m;
+  // Chunks are visited in reverse: visit v is chunk nchunks-1-v. In visit m the state warps
+  // advance the carry through chunk m, the products group finishes chunk m+1 and the
+  // forming group forms chunk m+2 (visit numbers); inputs arrive by TMA four visits ahead.
+  auto chunk_of = [&](int v) { return nchunks - 1 - v; };
+  auto len_of = [&](int v) { return min(kL, T - chunk_of(v) * kL); };
+  auto issue = [&](int v) {
+    const int st = v % kCarryStages;
     const int vmap[5] = {V_R, V_W, V_A, V_B, V_DY};
     mbar_arrive_expect_tx(&sm.full[st], kStageBytes);
-    for (int v = 0; v < 5; ++v) tma_load_4d(sm.raw[st][v], &args.map[vmap[v]], &sm.full[st], 0, hi, chunk * kL, bi);
+    for (int q = 0; q < 5; ++q)
+      tma_load_4d(sm.raw[st][q], &args.map[vmap[q]], &sm.full[st], 0, hi, chunk_of(v) * kL, bi);
+  };
+  int waited = 0, issued = 0;
+  auto form = [&](int v) {  // forming group; false on a timeout
+    const int c = chunk_of(v);
+    if (!front_form(sm, sm.sc[c & 1], sm.op[c % 3], sm.raw[v % kCarryStages][0], &sm.full[v % kCarryStages],
+                    (v / kCarryStages) & 1, len_of(v), args.status))
+      return false;
+    waited = v + 1;
+    return true;
+  };
+  auto products = [&](int v) {  // products group
+    const int c = chunk_of(v);
+    if (!sm.op[c % 3].unsafe) front_products(sm, sm.sc[c & 1], sm.op[c % 3]);
   };
   if (tid == 128) {
     for (int s = 0; s < kCarryStages; ++s) mbar_init(&sm.full[s], 1);
     fence_mbar_init();
-    for (int v = 0; v < 7; ++v) prefetch_tensormap(&args.map[v]);
-    for (int m = 0; m < kCarryStages && m < nchunks; ++m) issue(m);
+    for (int q = 0; q < 7; ++q) prefetch_tensormap(&args.map[q]);
+    for (int v = 0; v < kCarryStages && v < nchunks; ++v) issue(v);
   }
+  issued = min(kCarryStages, nchunks);
   if (tid == 0) sm.abort_flag = 0;
   float G[8][4];
 #pragma unroll
   for (int nt = 0; nt < 8; ++nt) zero4(G[nt]);
   __syncthreads();
 
-  int waited = 0, issued = min(kCarryStages, nchunks);
   bool aborted = false;
-  if (is_prep) {  // front half of the first visited chunk
-    const int n = nchunks - 1;
-    if (front_carry(sm, sm.op[n & 1], sm.raw[0][0], &sm.full[0], 0, min(kL, T - n * kL), args.status)) waited = 1;
-  }
+  // pipeline fill: form visits 0 and 1, products of visit 0
+  if (role == 1 && !form(0)) aborted = true;
   if (__syncthreads_or(sm.abort_flag)) aborted = true;
+  if (!aborted) {
+    if (role == 1 && nchunks > 1) form(1);
+    if (role == 2) products(0);
+    if (__syncthreads_or(sm.abort_flag)) aborted = true;
+  }
 
   for (int m = 0; m < nchunks && !aborted; ++m) {
-    const int n = nchunks - 1 - m, st = m % kCarryStages, len = min(kL, T - n * kL);
-    if (!is_prep) {
-      const OpC& op = sm.op[n & 1];
-      // the carry entering this chunk (gradient w.r.t. the state after it), as the tf32
+    const int n = chunk_of(m), st = m % kCarryStages;
+    if (role == 0) {
+      const OpC& op = sm.op[n % 3];
+      // the carry entering this chunk (gradient w.r.t. the state after it), as the bf16
       // operand the output kernel multiplies with
-      float* dst = carry_head + (size_t)n * kN * kN;
+      bf16_t* dst = carry_head + (size_t)n * kN * kN;
 #pragma unroll
       for (int nt = 0; nt < 8; ++nt) {
         const int col = 8 * nt + 2 * t4;
-        *reinterpret_cast<float2*>(dst + (i0 + g) * kN + col) = make_float2(tf32r(G[nt][0]), tf32r(G[nt][1]));
-        *reinterpret_cast<float2*>(dst + (i0 + g + 8) * kN + col) = make_float2(tf32r(G[nt][2]), tf32r(G[nt][3]));
+        *reinterpret_cast<uint32_t*>(dst + (i0 + g) * kN + col) = pack_bf16(G[nt][0], G[nt][1]);
+        *reinterpret_cast<uint32_t*>(dst + (i0 + g + 8) * kN + col) = pack_bf16(G[nt][2], G[nt][3]);
       }
       if (op.unsafe)
-        carry_direct(G, sm.raw[st][0], len, i0, g, t4);
+        carry_direct(G, sm.raw[st][0], len_of(m), i0, g, t4);
       else
         carry_chunk(G, op, i0, g, t4);
-    } else if (n > 0) {
-      const int st1 = (m + 1) % kCarryStages;
-      if (front_carry(sm, sm.op[(n - 1) & 1], sm.raw[st1][0], &sm.full[st1], ((m + 1) / kCarryStages) & 1,
-                      min(kL, T - (n - 1) * kL), args.status))
-        waited = m + 2;
+    } else if (role == 1) {
+      if (m + 2 < nchunks) form(m + 2);
+    } else {
+      if (m + 1 < nchunks) products(m + 1);
     }
-    // the stage of chunk n is free (front half and direct steps done); refill it
+    // the stage of visit m is free (formed two visits ago, direct steps done); refill it
     if (__syncthreads_or(sm.abort_flag)) {
       aborted = true;
       break;
@@ -441,17 +571,17 @@ __global__ void __launch_bounds__(kCarryThreads, 1) wkv7_bwd4_carry_kernel(const
     if (tid == 128 && m + kCarryStages < nchunks) {
       fence_proxy_async_smem();
       issue(m + kCarryStages);
-      issued = m + kCarryStages + 1;
     }
+    issued = min(m + 1 + kCarryStages, nchunks);
   }
   if (aborted) {
     if (tid == 128)
-      for (int mm = waited; mm < issued; ++mm)
-        mbar_wait_bounded(nullptr, &sm.full[mm % kCarryStages], (mm / kCarryStages) & 1, 200000000ull);
+      for (int v = waited; v < issued; ++v)
+        mbar_wait_bounded(nullptr, &sm.full[v % kCarryStages], (v / kCarryStages) & 1, 200000000ull);
     __syncthreads();
     return;
   }
-  if (!is_prep && args.dS_init) {
+  if (role == 0 && args.dS_init) {
     float* dst = args.dS_init + (size_t)head * kN * kN;
 #pragma unroll
     for (int nt = 0; nt < 8; ++nt) {
@@ -463,188 +593,163 @@ __global__ void __launch_bounds__(kCarryThreads, 1) wkv7_bwd4_carry_kernel(const
 }
 
 // =============================================================== output ===
-
-struct OpsB {  // phases A-B
-  float Ah[kL * kLD64], Rh[kL * kLD64], Kb[kL * kLD64], Bb[kL * kLD64];  // [t][j]
-};
-struct OpsD {  // phases C-E
-  float SAs[kL * kLD64], DSAs[kL * kLD64];  // sa(t), dsa(t) [t][i] (tf32)
-  // triu(V DY^T), triu(V DSA^T, 1), triu(SA DY^T), triu(SA DSA^T, 1) [t][s]
-  // (their transposes are the tril(...) factors)
-  float U[4][kL * kLD16];
-};
-struct OpsE {  // phases A-E
-  float Kt[kL * kLD64], Bt[kL * kLD64], Vs[kL * kLD64], DYs[kL * kLD64];  // [t][j], V and DY [t][i]
-  float Ah68[kL * kLDT], Rh68[kL * kLDT];                                 // A^, R^ [t][j]
-};
+//
+// The output kernel multiplies bf16 operands (mma.sync m16n8k16, fp32
+// accumulation): the inputs are bf16 already, the scaled operands, the
+// checkpoint and the carry are rounded to bf16 once, every sum is fp32.
+// Operands live once, row-major, in shared memory; ldmatrix (.trans where
+// the product reads a matrix down its columns) forms the fragments, so no
+// transposed copies are kept. Row strides of 72 (64-wide) and 24 (16-wide)
+// bf16 elements put the eight 16-byte rows of an 8 x 8 matrix on distinct
+// banks.
 
 struct OutSmem {
-  __nv_bfloat16 raw[7][kTile];  // r, w, k, v, a, b, dy of the chunk
-  float S0s[kN * kLDG];         // checkpoint [i][j]
-  float GcS[kN * kLDG];         // carry after the chunk [i][j] (tf32 values); the dw exchange later
+  bf16_t raw[7][kL * kB64];  // r, w, k, v, a, b, dy of the chunk [t][j] (V, DY: [t][i])
   union {
-    OpsB b;
-    OpsD d;
-    float red[4 * 5 * kN];  // column sums of a direct chunk
+    struct {
+      bf16_t S0[kN * kB64];  // checkpoint [i][j]
+      bf16_t Gc[kN * kB64];  // carry after the chunk [i][j]
+    } st;
+    float xch[3][kL * kLD64];  // the dw exchange, once the column products are done
+    float red[8 * 5 * kN];     // column sums of a direct chunk
   } u;
-  OpsE e;
-  float cS[kTile];                            // c(t) [t][j], fp32
-  float M[4][kL * kLD16];                     // Mka, Mkr, Mbr (with diagonal), Mba [t][s]
-  float Tinv[kL * kLD16], TinvT[kL * kLD16];  // T and T^T
-  float Epart[4][kN];                         // colsum(Gc o S0) over quarters of the rows
+  bf16_t Ah[kL * kB64], Rh[kL * kB64], Kt[kL * kB64], Bt[kL * kB64];  // [t][j]
+  bf16_t Kb[kL * kB64], Bb[kL * kB64];
+  bf16_t SA[kL * kB64], DSA[kL * kB64];  // sa(t), dsa(t) [t][i]
+  // Mka, Mkr, Mbr [t][s]; T = (I - Mba)^-1 [t][s]; U0 = triu(V DY^T), U1 = triu(V DSA^T, 1),
+  // U2 = triu(SA DY^T), U3 = triu(SA DSA^T, 1) [t][s]
+  bf16_t M[3][kL * kB16], Tm[kL * kB16], U[4][kL * kB16];
+  float Mba[kL * kLD16];  // fp32, for the substitution
+  float cS[kTile];        // c(t) [t][j], fp32
+  float Epart[4][kN];     // colsum(Gc o S0) over the rows of each row block
   float anc[2][kN];  // the chunk's parts of colsum(carry o state) at its start and end, without c(L) colsum(Gc o S0)
-  uint64_t bar;
-  int pad_[2];
 };
 
-// Step-by-step reverse scan of one chunk (warps 0..3, fp32): the carry
-// starts at the stored Gc, S_prev of step t is recomputed from the
-// checkpoint.
-__device__ void out_direct(OutSmem& sm, int len, const BwdArgs& args, size_t base, size_t vstep, int warp,
-                           int lane) {
-  const int g = lane >> 2, t4 = lane & 3, i0 = 16 * warp, tid = threadIdx.x;
-  const __nv_bfloat16* rs = sm.raw[0];
-  const float* S0 = sm.S0s;
-  float* red = sm.u.red;
-  float G[8][4];
+// Step-by-step reverse scan of one chunk (all eight warps, fp32; warp w owns
+// rows 8 w .. 8 w + 7 of the state and the carry, lane (g, t) row 8 w + g and
+// columns 8 nt + 2 t, + 1): the carry starts at the stored Gc, S_prev of step
+// t is recomputed from the checkpoint (fp32, read from global memory).
+__device__ void out_direct(OutSmem& sm, const float* S0, const bf16_t* Gcg, int len, const BwdArgs& args, size_t base,
+                           size_t vstep, int warp, int lane) {
+  const int g = lane >> 2, t4 = lane & 3, i = 8 * warp + g, tid = threadIdx.x;
+  const bf16_t* rs = sm.raw[0];
+  float* red = sm.u.red;  // [8 warps][5][64]
+  constexpr int RS = kL * kB64;
+  float G[8][2];
 #pragma unroll
   for (int nt = 0; nt < 8; ++nt) {
-    const int col = 8 * nt + 2 * t4;
-    const float2 lo = *reinterpret_cast<const float2*>(sm.GcS + (i0 + g) * kLDG + col);
-    const float2 hi = *reinterpret_cast<const float2*>(sm.GcS + (i0 + g + 8) * kLDG + col);
-    G[nt][0] = lo.x;
-    G[nt][1] = lo.y;
-    G[nt][2] = hi.x;
-    G[nt][3] = hi.y;
+    const float2 x = unpack_bf16(*reinterpret_cast<const uint32_t*>(Gcg + i * kN + 8 * nt + 2 * t4));
+    G[nt][0] = x.x;
+    G[nt][1] = x.y;
   }
   for (int t = len - 1; t >= 0; --t) {
-    float sp[8][4];
+    float sp[8][2];
 #pragma unroll
     for (int nt = 0; nt < 8; ++nt) {
-      const int col = 8 * nt + 2 * t4;
-      const float2 lo = *reinterpret_cast<const float2*>(S0 + (i0 + g) * kLDG + col);
-      const float2 hi = *reinterpret_cast<const float2*>(S0 + (i0 + g + 8) * kLDG + col);
-      sp[nt][0] = lo.x;
-      sp[nt][1] = lo.y;
-      sp[nt][2] = hi.x;
-      sp[nt][3] = hi.y;
+      const float2 x = *reinterpret_cast<const float2*>(S0 + i * kN + 8 * nt + 2 * t4);
+      sp[nt][0] = x.x;
+      sp[nt][1] = x.y;
     }
-    float sa0 = 0.f, sa1 = 0.f;
+    float sa = 0.f;
     for (int u = 0; u <= t; ++u) {
-      const __nv_bfloat16* row = rs + u * kN;
-      float s0 = 0.f, s1 = 0.f;
+      const bf16_t* row = rs + u * kB64;
+      float s = 0.f;
 #pragma unroll
       for (int nt = 0; nt < 8; ++nt) {
-        const float2 a = bf2(row + V_A * kTile + 8 * nt + 2 * t4);
-        s0 = fmaf(sp[nt][0], a.x, fmaf(sp[nt][1], a.y, s0));
-        s1 = fmaf(sp[nt][2], a.x, fmaf(sp[nt][3], a.y, s1));
+        const float2 a = bf2(row + V_A * RS + 8 * nt + 2 * t4);
+        s = fmaf(sp[nt][0], a.x, fmaf(sp[nt][1], a.y, s));
       }
-      sa0 = quad_sum(s0);
-      sa1 = quad_sum(s1);
+      sa = quad_sum(s);
       if (u == t) break;  // sp = S_prev(t), sa = sa(t)
-      const float v0 = bf(row + V_V * kTile + i0 + g), v1 = bf(row + V_V * kTile + i0 + g + 8);
+      const float v = bf(row + V_V * RS + i);
 #pragma unroll
       for (int nt = 0; nt < 8; ++nt) {
         const int col = 8 * nt + 2 * t4;
-        const float2 w = bf2(row + V_W * kTile + col), k = bf2(row + V_K * kTile + col);
-        const float2 b = bf2(row + V_B * kTile + col);
-        sp[nt][0] = fmaf(sa0, b.x, fmaf(sp[nt][0], w.x, v0 * k.x));
-        sp[nt][1] = fmaf(sa0, b.y, fmaf(sp[nt][1], w.y, v0 * k.y));
-        sp[nt][2] = fmaf(sa1, b.x, fmaf(sp[nt][2], w.x, v1 * k.x));
-        sp[nt][3] = fmaf(sa1, b.y, fmaf(sp[nt][3], w.y, v1 * k.y));
+        const float2 w = bf2(row + V_W * RS + col), k = bf2(row + V_K * RS + col), b = bf2(row + V_B * RS + col);
+        sp[nt][0] = fmaf(sa, b.x, fmaf(sp[nt][0], w.x, v * k.x));
+        sp[nt][1] = fmaf(sa, b.y, fmaf(sp[nt][1], w.y, v * k.y));
       }
     }
-    const __nv_bfloat16* row = rs + t * kN;
-    const float v0 = bf(row + V_V * kTile + i0 + g), v1 = bf(row + V_V * kTile + i0 + g + 8);
-    const float dy0 = bf(row + V_DY * kTile + i0 + g), dy1 = bf(row + V_DY * kTile + i0 + g + 8);
-    // column partials: dr (from S_t), then G += dy r^T, dk, db, dw; row sums dv, dsa
-    float pr[8][2], pk[8][2], pb[8][2], pw[8][2];
-    float dv0 = 0.f, dv1 = 0.f, ds0 = 0.f, ds1 = 0.f;
+    const bf16_t* row = rs + t * kB64;
+    const float v = bf(row + V_V * RS + i), dy = bf(row + V_DY * RS + i);
+    // column sums (over this warp's rows) of dr (from S_t), then G += dy r^T, dk, db, dw; row sums dv, dsa
+    float dv = 0.f, ds = 0.f;
 #pragma unroll
     for (int nt = 0; nt < 8; ++nt) {
       const int col = 8 * nt + 2 * t4;
-      const float2 w = bf2(row + V_W * kTile + col), k = bf2(row + V_K * kTile + col);
-      const float2 b = bf2(row + V_B * kTile + col), r = bf2(row + V_R * kTile + col);
+      const float2 w = bf2(row + V_W * RS + col), k = bf2(row + V_K * RS + col);
+      const float2 b = bf2(row + V_B * RS + col), r = bf2(row + V_R * RS + col);
       const float wv[2] = {w.x, w.y}, kv[2] = {k.x, k.y}, bv[2] = {b.x, b.y}, rv[2] = {r.x, r.y};
 #pragma unroll
       for (int e = 0; e < 2; ++e) {
-        const float st0 = fmaf(sa0, bv[e], fmaf(sp[nt][e], wv[e], v0 * kv[e]));
-        const float st1 = fmaf(sa1, bv[e], fmaf(sp[nt][2 + e], wv[e], v1 * kv[e]));
-        pr[nt][e] = fmaf(st0, dy0, st1 * dy1);
-        G[nt][e] = fmaf(dy0, rv[e], G[nt][e]);
-        G[nt][2 + e] = fmaf(dy1, rv[e], G[nt][2 + e]);
-        pk[nt][e] = fmaf(G[nt][e], v0, G[nt][2 + e] * v1);
-        pb[nt][e] = fmaf(G[nt][e], sa0, G[nt][2 + e] * sa1);
-        pw[nt][e] = fmaf(G[nt][e], sp[nt][e], G[nt][2 + e] * sp[nt][2 + e]);
-        dv0 = fmaf(G[nt][e], kv[e], dv0);
-        dv1 = fmaf(G[nt][2 + e], kv[e], dv1);
-        ds0 = fmaf(G[nt][e], bv[e], ds0);
-        ds1 = fmaf(G[nt][2 + e], bv[e], ds1);
+        const float st = fmaf(sa, bv[e], fmaf(sp[nt][e], wv[e], v * kv[e]));
+        G[nt][e] = fmaf(dy, rv[e], G[nt][e]);
+        const float sums[4] = {col_sum(st * dy), col_sum(G[nt][e] * v), col_sum(G[nt][e] * sa),
+                               col_sum(G[nt][e] * sp[nt][e])};
+        if (g == 0) {
+#pragma unroll
+          for (int q = 0; q < 4; ++q) red[(warp * 5 + q) * kN + col + e] = sums[q];
+        }
+        dv = fmaf(G[nt][e], kv[e], dv);
+        ds = fmaf(G[nt][e], bv[e], ds);
       }
     }
-    dv0 = quad_sum(dv0);
-    dv1 = quad_sum(dv1);
-    ds0 = quad_sum(ds0);
-    ds1 = quad_sum(ds1);
-    if (t4 == 0) {
-      args.dv[base + (size_t)t * vstep + i0 + g] = dv0;
-      args.dv[base + (size_t)t * vstep + i0 + g + 8] = dv1;
-    }
-    // da = S_prev^T dsa; carry G <- G diag(w) + dsa a^T; column sums to shared memory
+    dv = quad_sum(dv);
+    ds = quad_sum(ds);
+    if (t4 == 0) args.dv[base + (size_t)t * vstep + i] = dv;
+    // da = S_prev^T dsa; carry G <- G diag(w) + dsa a^T
 #pragma unroll
     for (int nt = 0; nt < 8; ++nt) {
       const int col = 8 * nt + 2 * t4;
-      const float2 w = bf2(row + V_W * kTile + col), a = bf2(row + V_A * kTile + col);
+      const float2 w = bf2(row + V_W * RS + col), a = bf2(row + V_A * RS + col);
       const float wv[2] = {w.x, w.y}, av[2] = {a.x, a.y};
 #pragma unroll
       for (int e = 0; e < 2; ++e) {
-        const float pa = fmaf(sp[nt][e], ds0, sp[nt][2 + e] * ds1);
-        G[nt][e] = fmaf(ds0, av[e], G[nt][e] * wv[e]);
-        G[nt][2 + e] = fmaf(ds1, av[e], G[nt][2 + e] * wv[e]);
-        const float sums[5] = {col_sum(pr[nt][e]), col_sum(pk[nt][e]), col_sum(pb[nt][e]), col_sum(pw[nt][e]),
-                               col_sum(pa)};
-        if (g == 0) {
-#pragma unroll
-          for (int q = 0; q < 5; ++q) red[(warp * 5 + q) * kN + col + e] = sums[q];
-        }
+        const float pa = col_sum(sp[nt][e] * ds);
+        G[nt][e] = fmaf(ds, av[e], G[nt][e] * wv[e]);
+        if (g == 0) red[(warp * 5 + 4) * kN + col + e] = pa;
       }
     }
-    named_bar(5, 128);
-    for (int idx = tid; idx < 5 * kN; idx += 128) {
+    __syncthreads();
+    for (int idx = tid; idx < 5 * kN; idx += kThreads) {
       const int q = idx / kN, col = idx % kN;
-      const float x = red[q * kN + col] + red[(5 + q) * kN + col] + red[(10 + q) * kN + col] + red[(15 + q) * kN + col];
+      float x = 0.f;
+#pragma unroll
+      for (int w8 = 0; w8 < 8; ++w8) x += red[(w8 * 5 + q) * kN + col];
       float* dst = q == 0 ? args.dr : q == 1 ? args.dk : q == 2 ? args.db : q == 3 ? args.dw : args.da;
       dst[base + (size_t)t * vstep + col] = x;
     }
-    named_bar(5, 128);
+    __syncthreads();
   }
 }
 
-// P0 += X M[:, j0 .. j0+15], P1 += Y M[:, j0 .. j0+15] for 16-row X, Y (stride
-// kLD64, tf32 values) and a 64 x 64 M (stride kLDG; fp32 values that need
-// rounding if kRound).
-template <bool kRound>
-__device__ __forceinline__ void column_products(float (&P0)[2][4], float (&P1)[2][4], const float* X, const float* Y,
-                                                const float* M, int j0, int g, int t4) {
+// T = (I - M)^-1 for a strictly lower 16 x 16 fp32 M (stride kLD16) by
+// forward substitution, one warp; lane s < 16 owns column s. Writes T
+// row-major as bf16.
+__device__ __forceinline__ void unit_lower_inverse16(const float* M, bf16_t* Tout, int lane) {
+  const int s = lane & 15;
+  float col[kL];
 #pragma unroll
-  for (int kb = 0; kb < 8; ++kb) {
-    uint32_t a0[4], a1[4];
-    frag_a(a0, X, kLD64, 0, 8 * kb, g, t4);
-    frag_a(a1, Y, kLD64, 0, 8 * kb, g, t4);
+  for (int t = 0; t < kL; ++t) {
+    float x = t == s ? 1.f : 0.f;
 #pragma unroll
-    for (int nt = 0; nt < 2; ++nt) {
-      uint32_t b0, b1;
-      if (kRound)
-        frag_b_t_r(b0, b1, M, kLDG, j0 + 8 * nt, 8 * kb, g, t4);
-      else
-        frag_b_t(b0, b1, M, kLDG, j0 + 8 * nt, 8 * kb, g, t4);
-      mma_tf32(P0[nt], a0, b0, b1);
-      mma_tf32(P1[nt], a1, b0, b1);
-    }
+    for (int u = 0; u < t; ++u) x = fmaf(M[t * kLD16 + u], col[u], x);
+    col[t] = x;
+  }
+  if (lane < 16) {
+#pragma unroll
+    for (int t = 0; t < kL; ++t) Tout[t * kB16 + s] = __float2bfloat16_rn(col[t]);
   }
 }
 
-__global__ void __launch_bounds__(kThreads, 2) wkv7_bwd4_out_kernel(const __grid_constant__ BwdArgs args) {
+// 16-byte asynchronous copy that writes zeros instead when `valid` is false.
+__device__ __forceinline__ void cp_async16_zfill(void* dst, const void* src, bool valid) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(smem_addr(dst)), "l"(src),
+               "r"(valid ? 16 : 0)
+               : "memory");
+}
+
+__global__ void __launch_bounds__(kThreads, 3) wkv7_bwd4_out_kernel(const __grid_constant__ BwdArgs args) {
   extern __shared__ __align__(128) unsigned char smem_raw[];
   OutSmem& sm = *reinterpret_cast<OutSmem*>(smem_raw);
   const int T = args.T, H = args.H, nchunks = (T + kL - 1) / kL;
@@ -652,87 +757,76 @@ __global__ void __launch_bounds__(kThreads, 2) wkv7_bwd4_out_kernel(const __grid
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, g = lane >> 2, t4 = lane & 3;
   const int t0 = n * kL, len = min(kL, T - t0);
   const size_t vstep = (size_t)H * kN, base = ((size_t)bi * T + t0) * vstep + (size_t)hi * kN;
+  const float* S0g = args.ckpt + ((size_t)head * args.nck + n) * kN * kN;
+  const bf16_t* Gcg = reinterpret_cast<const bf16_t*>(args.carry) + ((size_t)head * nchunks + n) * kN * kN;
+  constexpr int RS = kL * kB64;  // elements between staged vectors
 
-  // ---- loads: inputs by TMA, checkpoint and carry by cp.async
-  if (tid == 0) {
-    mbar_init(&sm.bar, 1);
-    fence_mbar_init();
-    mbar_arrive_expect_tx(&sm.bar, 7 * kTile * 2);
-    for (int v = 0; v < 7; ++v) tma_load_4d(sm.raw[v], &args.map[v], &sm.bar, 0, hi, t0, bi);
+  // ---- loads: the chunk's rows (zeros past T) and the carry by cp.async, the checkpoint through registers
+  for (int idx = tid; idx < 7 * kL * 8; idx += kThreads) {
+    const int v = idx / (kL * 8), t = (idx >> 3) % kL, c = idx & 7;
+    const bf16_t* src = static_cast<const bf16_t*>(args.in[v]) + base + (size_t)min(t, len - 1) * vstep + 8 * c;
+    cp_async16_zfill(sm.raw[v] + t * kB64 + 8 * c, src, t < len);
   }
-  fetch_state<kLDG, kThreads>(sm.S0s, args.ckpt + ((size_t)head * args.nck + n) * kN * kN, tid, true);
-  fetch_state<kLDG, kThreads>(sm.GcS, args.carry + ((size_t)head * nchunks + n) * kN * kN, tid, true);
-  __syncthreads();  // barrier initialised
-  const bool ok = mbar_wait_bounded(args.status, &sm.bar, 0);
+#pragma unroll
+  for (int q = 0; q < kN * 8 / kThreads; ++q) {
+    const int idx = tid + kThreads * q;  // row idx / 8, columns 8 (idx % 8) ..
+    cp_async16(sm.u.st.Gc + (idx >> 3) * kB64 + 8 * (idx & 7), Gcg + 8 * idx);
+  }
+  cp_async_commit();
+  float4 s0v[4];
+#pragma unroll
+  for (int q = 0; q < 4; ++q) s0v[q] = *reinterpret_cast<const float4*>(S0g + 4 * (tid + kThreads * q));
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    const int idx = tid + kThreads * q;  // row idx / 16, columns 4 (idx % 16) ..
+    *reinterpret_cast<uint2*>(sm.u.st.S0 + (idx >> 4) * kB64 + 4 * (idx & 15)) =
+        make_uint2(pack_bf16(s0v[q].x, s0v[q].y), pack_bf16(s0v[q].z, s0v[q].w));
+  }
   cp_async_wait_all();
-  if (__syncthreads_or(!ok)) {
-    if (tid == 0) mbar_wait_bounded(nullptr, &sm.bar, 0, 200000000ull);
-    __syncthreads();
-    return;
-  }
-  const __nv_bfloat16* rs = sm.raw[0];
+  __syncthreads();
+  const bf16_t* rs = sm.raw[0];
 
   // ---- A: scaled operands; thread (lane, warp) forms columns 2 lane, 2 lane + 1 of steps
   //      2 warp, 2 warp + 1 (running products c in step order from t = 0, as in the carry kernel)
   {
-    const int j = 2 * lane, t0 = 2 * warp;
+    const int j = 2 * lane, ta = 2 * warp;
     bool safe = true;
-    float2 cL = make_float2(1.f, 1.f), cpre = cL;  // cpre = c(t0 - 1)
+    float2 cL = make_float2(1.f, 1.f), cpre = cL;  // cpre = c(ta - 1)
 #pragma unroll
     for (int t = 0; t < kL; ++t) {
-      const float2 w = t < len ? bf2(rs + V_W * kTile + t * kN + j) : make_float2(1.f, 1.f);
+      const float2 w = t < len ? bf2(rs + V_W * RS + t * kB64 + j) : make_float2(1.f, 1.f);
       safe &= decay_is_safe(w.x) && decay_is_safe(w.y);
       cL = fmul2(cL, w);
-      if (t < t0) cpre = cL;
+      if (t < ta) cpre = cL;
     }
     if (__syncthreads_or(!safe)) {
-      if (warp < 4) out_direct(sm, len, args, base, vstep, warp, lane);
+      out_direct(sm, S0g, Gcg, len, args, base, vstep, warp, lane);
       return;
-    }
-    float2 wv[2], av[2], rv[2], kv[2], bv[2], vv[2], dyv[2];
-#pragma unroll
-    for (int e = 0; e < 2; ++e) {
-      const int o = (t0 + e) * kN + j;
-      wv[e] = t0 + e < len ? bf2(rs + V_W * kTile + o) : make_float2(1.f, 1.f);
-      av[e] = bf2(rs + V_A * kTile + o);
-      rv[e] = bf2(rs + V_R * kTile + o);
-      kv[e] = bf2(rs + V_K * kTile + o);
-      bv[e] = bf2(rs + V_B * kTile + o);
-      vv[e] = bf2(rs + V_V * kTile + o);
-      dyv[e] = bf2(rs + V_DY * kTile + o);
     }
     float2 c = cpre;
 #pragma unroll
     for (int e = 0; e < 2; ++e) {
-      const int t = t0 + e, o = t * kN + j, q = t * kLD64 + j, q68 = t * kLDT + j;
+      const int t = ta + e, q = t * kB64 + j;
+      const float2 w = t < len ? bf2(rs + V_W * RS + q) : make_float2(1.f, 1.f);
+      const float2 a = bf2(rs + V_A * RS + q), r = bf2(rs + V_R * RS + q);
+      const float2 k = bf2(rs + V_K * RS + q), b = bf2(rs + V_B * RS + q);
       const float2 cprev = c;
-      c = fmul2(c, wv[e]);
+      c = fmul2(c, w);
       const float2 ic = make_float2(rcp_approx(c.x), rcp_approx(c.y)), s = fmul2(cL, ic);
-      const float2 ah = tf32r2(fmul2(av[e], cprev)), rh = tf32r2(fmul2(rv[e], c));
-      *reinterpret_cast<float2*>(sm.u.b.Ah + q) = ah;
-      *reinterpret_cast<float2*>(sm.e.Ah68 + q68) = ah;
-      *reinterpret_cast<float2*>(sm.u.b.Rh + q) = rh;
-      *reinterpret_cast<float2*>(sm.e.Rh68 + q68) = rh;
-      *reinterpret_cast<float2*>(sm.e.Kt + q) = tf32r2(fmul2(kv[e], ic));
-      *reinterpret_cast<float2*>(sm.e.Bt + q) = tf32r2(fmul2(bv[e], ic));
-      *reinterpret_cast<float2*>(sm.u.b.Kb + q) = tf32r2(fmul2(kv[e], s));
-      *reinterpret_cast<float2*>(sm.u.b.Bb + q) = tf32r2(fmul2(bv[e], s));
-      *reinterpret_cast<float2*>(sm.e.Vs + q) = vv[e];  // bf16 values are tf32 values
-      *reinterpret_cast<float2*>(sm.e.DYs + q) = dyv[e];
-      *reinterpret_cast<float2*>(sm.cS + o) = c;
+      st_pair(sm.Ah + q, fmul2(a, cprev));
+      st_pair(sm.Rh + q, fmul2(r, c));
+      st_pair(sm.Kt + q, fmul2(k, ic));
+      st_pair(sm.Bt + q, fmul2(b, ic));
+      st_pair(sm.Kb + q, fmul2(k, s));
+      st_pair(sm.Bb + q, fmul2(b, s));
+      *reinterpret_cast<float2*>(sm.cS + t * kN + j) = c;
     }
-    // colsum(Gc o S0) over rows 16 q .. 16 q + 15, column j = tid % 64 (both anchors of dw start from it)
-    const int jc = tid & 63, q = tid >> 6;
-    float ep = 0.f;
-#pragma unroll
-    for (int i = 16 * q; i < 16 * q + 16; ++i) ep = fmaf(sm.GcS[i * kLDG + jc], sm.S0s[i * kLDG + jc], ep);
-    sm.Epart[q][jc] = ep;
   }
   __syncthreads();
 
-  // ---- B: L x L products and T (warps 0-3), the K = 64 parts of sa, dsa, dv
-  const int rb = warp & 3, r0 = 16 * rb;  // row block of the state-sized products
-  float X1[2][4], X2[2][4];               // warps 0-3: RDSA^T; warps 4-7: RSA^T, DV^T (rows i, columns t)
+  // ---- B: L x L products and T (warps 0-3), the K = 64 parts of sa, dsa, dv (rows i of block rb)
+  const int rb = warp & 3, r0 = 16 * rb;
+  float X1[2][4], X2[2][4];  // warps 0-3: RDSA^T; warps 4-7: RSA^T, DV^T (rows i, columns t)
 #pragma unroll
   for (int q = 0; q < 2; ++q) {
     zero4(X1[q]);
@@ -741,119 +835,87 @@ __global__ void __launch_bounds__(kThreads, 2) wkv7_bwd4_out_kernel(const __grid
   if (warp < 4) {
     // Mka = A^ K~^T, Mba = A^ B~^T (strictly lower); Mkr = R^ K~^T, Mbr = R^ B~^T (with diagonal)
     float acc[2][4];
-    gram16(acc, warp < 2 ? sm.u.b.Ah : sm.u.b.Rh, (warp & 1) ? sm.e.Bt : sm.e.Kt, g, t4);
-    store_masked(acc, sm.M[warp == 0 ? 0 : warp == 1 ? 3 : warp - 1], true, warp >= 2, g, t4);
+    zero4(acc[0]);
+    zero4(acc[1]);
+    mm_mk_nk<4>(acc, warp < 2 ? sm.Ah : sm.Rh, kB64, 0, (warp & 1) ? sm.Bt : sm.Kt, kB64, 0, lane);
     if (warp == 1) {
+#pragma unroll
+      for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          const int t = g + 8 * h, s = 8 * nt + 2 * t4;
+          sm.Mba[t * kLD16 + s] = s < t ? acc[nt][2 * h] : 0.f;
+          sm.Mba[t * kLD16 + s + 1] = s + 1 < t ? acc[nt][2 * h + 1] : 0.f;
+        }
       __syncwarp();
-      unit_lower_inverse(sm.M[3], sm.Tinv, sm.TinvT, lane);
+      unit_lower_inverse16(sm.Mba, sm.Tm, lane);
+    } else {
+      store_masked16(acc, sm.M[warp == 0 ? 0 : warp - 1], true, warp >= 2, g, t4);
     }
-#pragma unroll
-    for (int kb = 0; kb < 8; ++kb) {  // Gc Bb^T
-      uint32_t aG[4];
-      frag_a(aG, sm.GcS, kLDG, r0, 8 * kb, g, t4);
-#pragma unroll
-      for (int q = 0; q < 2; ++q) {
-        uint32_t b0, b1;
-        frag_b(b0, b1, sm.u.b.Bb, kLD64, 8 * q, 8 * kb, g, t4);
-        mma_tf32(X1[q], aG, b0, b1);
-      }
-    }
+    mm_mk_nk<4>(X1, sm.u.st.Gc, kB64, r0, sm.Bb, kB64, 0, lane);  // Gc Bb^T
   } else {
+    mm_mk_nk<4>(X1, sm.u.st.S0, kB64, r0, sm.Ah, kB64, 0, lane);  // S0 A^T
+    mm_mk_nk<4>(X2, sm.u.st.Gc, kB64, r0, sm.Kb, kB64, 0, lane);  // Gc Kb^T
+    // this row block's part of colsum(Gc o S0), columns 2 lane, 2 lane + 1
+    float2 ep = make_float2(0.f, 0.f);
 #pragma unroll
-    for (int kb = 0; kb < 8; ++kb) {  // S0 A^T, Gc Kb^T
-      uint32_t aS[4], aG[4];
-      frag_a_r(aS, sm.S0s, kLDG, r0, 8 * kb, g, t4);
-      frag_a(aG, sm.GcS, kLDG, r0, 8 * kb, g, t4);
-#pragma unroll
-      for (int q = 0; q < 2; ++q) {
-        uint32_t b0, b1;
-        frag_b(b0, b1, sm.u.b.Ah, kLD64, 8 * q, 8 * kb, g, t4);
-        mma_tf32(X1[q], aS, b0, b1);
-        frag_b(b0, b1, sm.u.b.Kb, kLD64, 8 * q, 8 * kb, g, t4);
-        mma_tf32(X2[q], aG, b0, b1);
-      }
+    for (int i = r0; i < r0 + 16; ++i) {
+      const float2 gc = bf2(sm.u.st.Gc + i * kB64 + 2 * lane), s0 = bf2(sm.u.st.S0 + i * kB64 + 2 * lane);
+      ep = ffma2(gc, s0, ep);
+    }
+    *reinterpret_cast<float2*>(&sm.Epart[rb][2 * lane]) = ep;
+    if (warp == 4) {  // U0 = triu(V DY^T)
+      float acc[2][4];
+      zero4(acc[0]);
+      zero4(acc[1]);
+      mm_mk_nk<4>(acc, sm.raw[V_V], kB64, 0, sm.raw[V_DY], kB64, 0, lane);
+      store_masked16(acc, sm.U[0], false, true, g, t4);
     }
   }
   __syncthreads();
 
   // ---- C: DSA^T = (Gc Bb^T + DY^T Mbr) T (warps 0-3); SA^T = (S0 A^T + V^T Mka^T) T^T and
-  //      DV^T += DY^T Mkr (warps 4-7). SAs/DSAs overwrite operands of phase B.
+  //      DV^T += DY^T Mkr (warps 4-7); sa and dsa stored as bf16 [t][i]
   {
-    uint32_t aD[2][4];
-#pragma unroll
-    for (int kb = 0; kb < 2; ++kb) frag_a_ts(aD[kb], sm.e.DYs, kLD64, r0, 8 * kb, g, t4);  // DY^T
+    uint32_t aD[4], b[4], p[4];
+    a_km(aD, sm.raw[V_DY], kB64, r0, 0, lane);  // DY^T
     float Y[2][4];
     zero4(Y[0]);
     zero4(Y[1]);
     if (warp < 4) {
-#pragma unroll
-      for (int kb = 0; kb < 2; ++kb)
-#pragma unroll
-        for (int q = 0; q < 2; ++q) {
-          uint32_t b0, b1;
-          frag_b_ts(b0, b1, sm.M[2], kLD16, 8 * q, 8 * kb, g, t4);
-          mma_tf32(X1[q], aD[kb], b0, b1);
-        }
-#pragma unroll
-      for (int kb = 0; kb < 2; ++kb) {
-        uint32_t a2[4];
-        c2a(a2, X1[kb]);
-#pragma unroll
-        for (int q = 0; q < 2; ++q) {
-          uint32_t b0, b1;
-          frag_b(b0, b1, sm.TinvT, kLD16, 8 * q, 8 * kb, g, t4);
-          mma_tf32(Y[q], a2, b0, b1);
-        }
-      }
+      b_kn(b, sm.M[2], kB16, 0, 0, lane);  // Mbr
+      mma16(X1[0], aD, b[0], b[1]);
+      mma16(X1[1], aD, b[2], b[3]);
+      c2a16(p, X1[0], X1[1]);
+      b_kn(b, sm.Tm, kB16, 0, 0, lane);  // T
+      mma16(Y[0], p, b[0], b[1]);
+      mma16(Y[1], p, b[2], b[3]);
     } else {
-#pragma unroll
-      for (int kb = 0; kb < 2; ++kb) {
-        uint32_t aV[4];
-        frag_a_t(aV, sm.e.Vs, kLD64, r0, 8 * kb, g, t4);  // V^T
-#pragma unroll
-        for (int q = 0; q < 2; ++q) {
-          uint32_t b0, b1;
-          frag_b(b0, b1, sm.M[0], kLD16, 8 * q, 8 * kb, g, t4);
-          mma_tf32(X1[q], aV, b0, b1);
-          frag_b_ts(b0, b1, sm.M[1], kLD16, 8 * q, 8 * kb, g, t4);
-          mma_tf32(X2[q], aD[kb], b0, b1);
-        }
-      }
-#pragma unroll
-      for (int kb = 0; kb < 2; ++kb) {
-        uint32_t a1[4];
-        c2a(a1, X1[kb]);
-#pragma unroll
-        for (int q = 0; q < 2; ++q) {
-          uint32_t b0, b1;
-          frag_b(b0, b1, sm.Tinv, kLD16, 8 * q, 8 * kb, g, t4);
-          mma_tf32(Y[q], a1, b0, b1);
-        }
-      }
+      uint32_t aV[4];
+      a_km(aV, sm.raw[V_V], kB64, r0, 0, lane);  // V^T
+      b_nk(b, sm.M[0], kB16, 0, 0, lane);        // Mka^T
+      mma16(X1[0], aV, b[0], b[1]);
+      mma16(X1[1], aV, b[2], b[3]);
+      b_kn(b, sm.M[1], kB16, 0, 0, lane);  // Mkr
+      mma16(X2[0], aD, b[0], b[1]);
+      mma16(X2[1], aD, b[2], b[3]);
+      c2a16(p, X1[0], X1[1]);
+      b_nk(b, sm.Tm, kB16, 0, 0, lane);  // T^T
+      mma16(Y[0], p, b[0], b[1]);
+      mma16(Y[1], p, b[2], b[3]);
     }
-    float* dst = warp < 4 ? sm.u.d.DSAs : sm.u.d.SAs;
-#pragma unroll
-    for (int q = 0; q < 2; ++q)
-#pragma unroll
-      for (int h = 0; h < 2; ++h)
-#pragma unroll
-        for (int e = 0; e < 2; ++e) dst[(8 * q + 2 * t4 + e) * kLD64 + r0 + g + 8 * h] = tf32r(Y[q][2 * h + e]);
+    c2a16(p, Y[0], Y[1]);
+    stsm4t((warp < 4 ? sm.DSA : sm.SA) + ((lane & 7) + (lane >> 4) * 8) * kB64 + r0 + ((lane >> 3) & 1) * 8, p);
   }
   __syncthreads();
 
-  // ---- D: DV^T += DSA^T Mka and dv (warps 4-7); the four triangular L x L factors (warps 0-3)
+  // ---- D: DV^T += DSA^T Mka and dv (warps 4-7); triu(V DSA^T, 1), triu(SA DY^T), triu(SA DSA^T, 1) (warps 1-3)
   if (warp >= 4) {
-#pragma unroll
-    for (int kb = 0; kb < 2; ++kb) {
-      uint32_t aS[4];
-      frag_a_t(aS, sm.u.d.DSAs, kLD64, r0, 8 * kb, g, t4);  // DSA^T
-#pragma unroll
-      for (int q = 0; q < 2; ++q) {
-        uint32_t b0, b1;
-        frag_b_t(b0, b1, sm.M[0], kLD16, 8 * q, 8 * kb, g, t4);
-        mma_tf32(X2[q], aS, b0, b1);
-      }
-    }
+    uint32_t aS[4], b[4];
+    a_km(aS, sm.DSA, kB64, r0, 0, lane);  // DSA^T
+    b_kn(b, sm.M[0], kB16, 0, 0, lane);   // Mka
+    mma16(X2[0], aS, b[0], b[1]);
+    mma16(X2[1], aS, b[2], b[3]);
 #pragma unroll
     for (int q = 0; q < 2; ++q)
 #pragma unroll
@@ -865,11 +927,12 @@ __global__ void __launch_bounds__(kThreads, 2) wkv7_bwd4_out_kernel(const __grid
           dst[8] = X2[q][2 + e];
         }
       }
-  } else {
-    // U0 = triu(V DY^T), U1 = triu(V DSA^T, 1), U2 = triu(SA DY^T), U3 = triu(SA DSA^T, 1)
+  } else if (warp >= 1) {
     float acc[2][4];
-    gram16(acc, warp < 2 ? sm.e.Vs : sm.u.d.SAs, (warp & 1) ? sm.u.d.DSAs : sm.e.DYs, g, t4);
-    store_masked(acc, sm.u.d.U[warp], false, (warp & 1) == 0, g, t4);
+    zero4(acc[0]);
+    zero4(acc[1]);
+    mm_mk_nk<4>(acc, warp == 1 ? sm.raw[V_V] : sm.SA, kB64, 0, warp == 2 ? sm.raw[V_DY] : sm.DSA, kB64, 0, lane);
+    store_masked16(acc, sm.U[warp], false, warp == 2, g, t4);
   }
   __syncthreads();
 
@@ -882,18 +945,28 @@ __global__ void __launch_bounds__(kThreads, 2) wkv7_bwd4_out_kernel(const __grid
     zero4(P0[nt]);
     zero4(P1[nt]);
   }
-  // sums over the rows i: V Gc, SA Gc (grp 0); DY S0, DSA S0 (grp 1)
-  if (grp == 0)
-    column_products<false>(P0, P1, sm.e.Vs, sm.u.d.SAs, sm.GcS, j0, g, t4);
-  else
-    column_products<true>(P0, P1, sm.e.DYs, sm.u.d.DSAs, sm.S0s, j0, g, t4);
+  {  // sums over the rows i: V Gc, SA Gc (grp 0); DY S0, DSA S0 (grp 1)
+    const bf16_t* Bm = grp ? sm.u.st.S0 : sm.u.st.Gc;
+    const bf16_t* X = grp ? sm.raw[V_DY] : sm.raw[V_V];
+    const bf16_t* Y = grp ? sm.DSA : sm.SA;
+#pragma unroll
+    for (int kb = 0; kb < 4; ++kb) {
+      uint32_t a0[4], a1[4], b[4];
+      a_mk(a0, X, kB64, 0, 16 * kb, lane);
+      a_mk(a1, Y, kB64, 0, 16 * kb, lane);
+      b_kn(b, Bm, kB64, j0, 16 * kb, lane);
+      mma16(P0[0], a0, b[0], b[1]);
+      mma16(P0[1], a0, b[2], b[3]);
+      mma16(P1[0], a1, b[0], b[1]);
+      mma16(P1[1], a1, b[2], b[3]);
+    }
+  }
   {
     // This warp's part of the dw anchors, from the column products (c(L) colsum(Gc o S0) is
     // added later):
     //   colsum(Gc o S(L)) = c(L) colsum(Gc o S0) + sum_t (Kb o V Gc + Bb o SA Gc)       (grp 0)
     //   colsum(Gc' o S0)  = c(L) colsum(Gc o S0) + sum_t (R^ o DY S0 + A^ o DSA S0)     (grp 1)
     // with S(L) = S0 diag(c(L)) + V^T Kb + SA^T Bb and Gc' = Gc diag(c(L)) + DY^T R^ + DSA^T A^.
-    const __nv_bfloat16* rs0 = sm.raw[0];
     float v[4];
 #pragma unroll
     for (int nt = 0; nt < 2; ++nt) {
@@ -904,12 +977,12 @@ __global__ void __launch_bounds__(kThreads, 2) wkv7_bwd4_out_kernel(const __grid
         const int t = g + 8 * h;
         const float2 c = *reinterpret_cast<const float2*>(sm.cS + t * kN + col);
         if (grp == 0) {
-          const float2 k = bf2(rs0 + V_K * kTile + t * kN + col), b = bf2(rs0 + V_B * kTile + t * kN + col);
+          const float2 k = bf2(rs + V_K * RS + t * kB64 + col), b = bf2(rs + V_B * RS + t * kB64 + col);
           acc.x += fmaf(k.x, P0[nt][2 * h], b.x * P1[nt][2 * h]) * rcp_approx(c.x);
           acc.y += fmaf(k.y, P0[nt][2 * h + 1], b.y * P1[nt][2 * h + 1]) * rcp_approx(c.y);
         } else {
           const float2 cp = t ? *reinterpret_cast<const float2*>(sm.cS + (t - 1) * kN + col) : make_float2(1.f, 1.f);
-          const float2 r = bf2(rs0 + V_R * kTile + t * kN + col), a = bf2(rs0 + V_A * kTile + t * kN + col);
+          const float2 r = bf2(rs + V_R * RS + t * kB64 + col), a = bf2(rs + V_A * RS + t * kB64 + col);
           acc.x += fmaf(r.x * c.x, P0[nt][2 * h], a.x * cp.x * P1[nt][2 * h]);
           acc.y += fmaf(r.y * c.y, P0[nt][2 * h + 1], a.y * cp.y * P1[nt][2 * h + 1]);
         }
@@ -919,8 +992,8 @@ __global__ void __launch_bounds__(kThreads, 2) wkv7_bwd4_out_kernel(const __grid
     }
     // sum over the 8 row groups: reduce-scatter over xor 16 (n-tile), 8 (column parity), then 4
     const bool up16 = (g & 4) != 0, up8 = (g & 2) != 0;
-    float x0 = (up16 ? v[2] : v[0]) + __shfl_xor_sync(0xffffffffu, up16 ? v[0] : v[2], 16);
-    float x1 = (up16 ? v[3] : v[1]) + __shfl_xor_sync(0xffffffffu, up16 ? v[1] : v[3], 16);
+    const float x0 = (up16 ? v[2] : v[0]) + __shfl_xor_sync(0xffffffffu, up16 ? v[0] : v[2], 16);
+    const float x1 = (up16 ? v[3] : v[1]) + __shfl_xor_sync(0xffffffffu, up16 ? v[1] : v[3], 16);
     float y = (up8 ? x1 : x0) + __shfl_xor_sync(0xffffffffu, up8 ? x0 : x1, 8);
     y += __shfl_xor_sync(0xffffffffu, y, 4);
     if ((g & 1) == 0) {
@@ -929,64 +1002,54 @@ __global__ void __launch_bounds__(kThreads, 2) wkv7_bwd4_out_kernel(const __grid
       sm.anc[grp ? 0 : 1][col] = grp ? y : cl * y;
     }
   }
-  __syncthreads();  // the carry tile is free from here on (the dw exchange below)
+  __syncthreads();  // checkpoint and carry tiles are free from here on (the dw exchange below)
   // triangular terms (U0 = triu(V DY^T), U1 = triu(V DSA^T, 1), U2 = triu(SA DY^T), U3 = triu(SA DSA^T, 1)):
   //   dk~ = (V Gc) c(L) + U0 R^ + U1 A^        db~ = (SA Gc) c(L) + U2 R^ + U3 A^
   //   dr^ = DY S0 + U0^T K~ + U2^T B~          da^ = DSA S0 + U1^T K~ + U3^T B~
-  const float* U0 = sm.u.d.U[0];
-  const float* U1 = sm.u.d.U[1];
-  const float* U2 = sm.u.d.U[2];
-  const float* U3 = sm.u.d.U[3];
-  if (grp == 0) {
-#pragma unroll
-    for (int nt = 0; nt < 2; ++nt) {
-      // c(L) = c(15), the last row of cS
-      const float2 cl = *reinterpret_cast<const float2*>(sm.cS + (kL - 1) * kN + j0 + 8 * nt + 2 * t4);
-      P0[nt][0] *= cl.x;
-      P0[nt][1] *= cl.y;
-      P0[nt][2] *= cl.x;
-      P0[nt][3] *= cl.y;
-      P1[nt][0] *= cl.x;
-      P1[nt][1] *= cl.y;
-      P1[nt][2] *= cl.x;
-      P1[nt][3] *= cl.y;
-    }
-#pragma unroll
-    for (int kb = 0; kb < 2; ++kb) {
-      uint32_t u0[4], u1[4], u2[4], u3[4];
-      frag_a(u0, U0, kLD16, 0, 8 * kb, g, t4);
-      frag_a(u1, U1, kLD16, 0, 8 * kb, g, t4);
-      frag_a(u2, U2, kLD16, 0, 8 * kb, g, t4);
-      frag_a(u3, U3, kLD16, 0, 8 * kb, g, t4);
+  {
+    uint32_t u0[4], u1[4], u2[4], u3[4], b[4];
+    if (grp == 0) {
 #pragma unroll
       for (int nt = 0; nt < 2; ++nt) {
-        uint32_t b0, b1;
-        frag_b_t(b0, b1, sm.e.Rh68, kLDT, j0 + 8 * nt, 8 * kb, g, t4);
-        mma_tf32(P0[nt], u0, b0, b1);
-        mma_tf32(P1[nt], u2, b0, b1);
-        frag_b_t(b0, b1, sm.e.Ah68, kLDT, j0 + 8 * nt, 8 * kb, g, t4);
-        mma_tf32(P0[nt], u1, b0, b1);
-        mma_tf32(P1[nt], u3, b0, b1);
+        const float2 cl = *reinterpret_cast<const float2*>(sm.cS + (kL - 1) * kN + j0 + 8 * nt + 2 * t4);
+        P0[nt][0] *= cl.x;
+        P0[nt][1] *= cl.y;
+        P0[nt][2] *= cl.x;
+        P0[nt][3] *= cl.y;
+        P1[nt][0] *= cl.x;
+        P1[nt][1] *= cl.y;
+        P1[nt][2] *= cl.x;
+        P1[nt][3] *= cl.y;
       }
-    }
-  } else {
-#pragma unroll
-    for (int kb = 0; kb < 2; ++kb) {
-      uint32_t u0[4], u1[4], u2[4], u3[4];
-      frag_a_ts(u0, U0, kLD16, 0, 8 * kb, g, t4);
-      frag_a_ts(u1, U1, kLD16, 0, 8 * kb, g, t4);
-      frag_a_ts(u2, U2, kLD16, 0, 8 * kb, g, t4);
-      frag_a_ts(u3, U3, kLD16, 0, 8 * kb, g, t4);
-#pragma unroll
-      for (int nt = 0; nt < 2; ++nt) {
-        uint32_t b0, b1;
-        frag_b_ts(b0, b1, sm.e.Kt, kLD64, j0 + 8 * nt, 8 * kb, g, t4);
-        mma_tf32(P0[nt], u0, b0, b1);
-        mma_tf32(P1[nt], u1, b0, b1);
-        frag_b_ts(b0, b1, sm.e.Bt, kLD64, j0 + 8 * nt, 8 * kb, g, t4);
-        mma_tf32(P0[nt], u2, b0, b1);
-        mma_tf32(P1[nt], u3, b0, b1);
-      }
+      a_mk(u0, sm.U[0], kB16, 0, 0, lane);
+      a_mk(u1, sm.U[1], kB16, 0, 0, lane);
+      a_mk(u2, sm.U[2], kB16, 0, 0, lane);
+      a_mk(u3, sm.U[3], kB16, 0, 0, lane);
+      b_kn(b, sm.Rh, kB64, j0, 0, lane);
+      mma16(P0[0], u0, b[0], b[1]);
+      mma16(P0[1], u0, b[2], b[3]);
+      mma16(P1[0], u2, b[0], b[1]);
+      mma16(P1[1], u2, b[2], b[3]);
+      b_kn(b, sm.Ah, kB64, j0, 0, lane);
+      mma16(P0[0], u1, b[0], b[1]);
+      mma16(P0[1], u1, b[2], b[3]);
+      mma16(P1[0], u3, b[0], b[1]);
+      mma16(P1[1], u3, b[2], b[3]);
+    } else {
+      a_km(u0, sm.U[0], kB16, 0, 0, lane);
+      a_km(u1, sm.U[1], kB16, 0, 0, lane);
+      a_km(u2, sm.U[2], kB16, 0, 0, lane);
+      a_km(u3, sm.U[3], kB16, 0, 0, lane);
+      b_kn(b, sm.Kt, kB64, j0, 0, lane);
+      mma16(P0[0], u0, b[0], b[1]);
+      mma16(P0[1], u0, b[2], b[3]);
+      mma16(P1[0], u1, b[0], b[1]);
+      mma16(P1[1], u1, b[2], b[3]);
+      b_kn(b, sm.Bt, kB64, j0, 0, lane);
+      mma16(P0[0], u2, b[0], b[1]);
+      mma16(P0[1], u2, b[2], b[3]);
+      mma16(P1[0], u3, b[0], b[1]);
+      mma16(P1[1], u3, b[2], b[3]);
     }
   }
   // unscale: dk = dk~ / c, db = db~ / c (grp 0); dr = dr^ c, da = da^ c(t-1) (grp 1); and this
@@ -999,7 +1062,7 @@ __global__ void __launch_bounds__(kThreads, 2) wkv7_bwd4_out_kernel(const __grid
       const int t = g + 8 * h, col = j0 + 8 * nt + 2 * t4;
       const float2 c = *reinterpret_cast<const float2*>(sm.cS + t * kN + col);
       if (grp == 0) {
-        const float2 k = bf2(rs + V_K * kTile + t * kN + col), b = bf2(rs + V_B * kTile + t * kN + col);
+        const float2 k = bf2(rs + V_K * RS + t * kB64 + col), b = bf2(rs + V_B * RS + t * kB64 + col);
         const float ic[2] = {rcp_approx(c.x), rcp_approx(c.y)}, kv[2] = {k.x, k.y}, bv[2] = {b.x, b.y};
 #pragma unroll
         for (int e = 0; e < 2; ++e) {
@@ -1010,7 +1073,7 @@ __global__ void __launch_bounds__(kThreads, 2) wkv7_bwd4_out_kernel(const __grid
         }
       } else {
         const float2 cp = t ? *reinterpret_cast<const float2*>(sm.cS + (t - 1) * kN + col) : make_float2(1.f, 1.f);
-        const float2 r = bf2(rs + V_R * kTile + t * kN + col), a = bf2(rs + V_A * kTile + t * kN + col);
+        const float2 r = bf2(rs + V_R * RS + t * kB64 + col), a = bf2(rs + V_A * RS + t * kB64 + col);
         const float cv[2] = {c.x, c.y}, cpv[2] = {cp.x, cp.y}, rv[2] = {r.x, r.y}, av[2] = {a.x, a.y};
 #pragma unroll
         for (int e = 0; e < 2; ++e) {
@@ -1023,9 +1086,9 @@ __global__ void __launch_bounds__(kThreads, 2) wkv7_bwd4_out_kernel(const __grid
     }
   // exchange with the partner warp of the other group (same columns): grp 0 keeps
   // dw of n-tile 0, grp 1 of n-tile 1
-  float* XK = sm.GcS;                   // grp 0's x part, [t][j] stride 72
-  float* XR = sm.GcS + kL * kLD64;      // grp 1's x part
-  float* XA = sm.GcS + 2 * kL * kLD64;  // grp 1's a da
+  float* XK = sm.u.xch[0];  // grp 0's x part, [t][j] stride 72
+  float* XR = sm.u.xch[1];  // grp 1's x part
+  float* XA = sm.u.xch[2];  // grp 1's a da
 #pragma unroll
   for (int h = 0; h < 2; ++h) {
     const int t = g + 8 * h;
@@ -1072,8 +1135,8 @@ __global__ void __launch_bounds__(kThreads, 2) wkv7_bwd4_out_kernel(const __grid
       if (g >= d) lo += ol;
     }
     const int col = jw + 2 * t4 + e;
-    const float2 w0 = bf2(rs + V_W * kTile + g * kN + jw + 2 * t4);
-    const float2 w1 = bf2(rs + V_W * kTile + (g + 8) * kN + jw + 2 * t4);
+    const float2 w0 = bf2(rs + V_W * RS + g * kB64 + jw + 2 * t4);
+    const float2 w1 = bf2(rs + V_W * RS + (g + 8) * kB64 + jw + 2 * t4);
     const float cge = sm.cS[(kL - 1) * kN + col] * (sm.Epart[0][col] + sm.Epart[1][col] + sm.Epart[2][col] + sm.Epart[3][col]);
     dw[e] = (cge + sm.anc[0][col] - (lo - xw[e]) - adw[e]) * rcp_approx(e ? w0.y : w0.x);
     dw[2 + e] = (hi2 - adw[2 + e] + cge + sm.anc[1][col]) * rcp_approx(e ? w1.y : w1.x);
@@ -1099,7 +1162,7 @@ __global__ void __launch_bounds__(kThreads, 2) wkv7_bwd4_out_kernel(const __grid
 
 size_t bwd4_workspace_bytes(int B, int T, int H) {
   const size_t nchunks = ((size_t)T + kL - 1) / kL, heads = (size_t)B * H;
-  return heads * nchunks * kN * kN * sizeof(float);
+  return heads * nchunks * kN * kN * sizeof(__nv_bfloat16);
 }
 
 cudaError_t launch_bwd4(const BwdArgs& args, cudaStream_t stream) {

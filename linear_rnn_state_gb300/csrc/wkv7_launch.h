@@ -34,7 +34,8 @@ struct BwdArgs {
   float* da;
   float* db;
   float* dS_init;  // [B][H][N][N] or null
-  float* carry;    // split backward: [B*H][nchunks][N][N] carry after each chunk
+  const void* in[7];  // r, w, k, v, a, b, dy ([B][T][H][N], the input type)
+  void* carry;        // split backward: [B*H][nchunks][N][N] carry after each chunk (bf16)
   unsigned* status;
   int C, nck;
   int B, T, H;

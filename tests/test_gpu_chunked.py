@@ -32,10 +32,7 @@ def env(request):
     torch.cuda.set_device(0)
     # the backward variant is chosen per call from the environment
     import os
-    if request.param == "split":
-        os.environ["WKV7_SPLIT_BACKWARD"] = "1"
-    else:
-        os.environ.pop("WKV7_SPLIT_BACKWARD", None)
+    os.environ["WKV7_SPLIT_BACKWARD"] = "1" if request.param == "split" else "0"
     yield oracle, inputs, wkv7
     os.environ.pop("WKV7_SPLIT_BACKWARD", None)
 
