@@ -274,33 +274,40 @@ struct CarrySmem {
   OpC op[3];
   ScratchC sc[2];
   float Mbr[kL * kLD16], Mba[kL * kLD16], TT[kL * kLD16];  // [t][s]; TT = T^T
+  float Pc[4][kN];                                         // products of the decays of four-step blocks
   uint64_t full[kCarryStages];
   int abort_flag;
 };
 
 // Forming group (128 threads): the scaled operands of a chunk. Thread
 // (lane, pf) forms columns 2 lane, 2 lane + 1 of steps 4 pf .. 4 pf + 3. The
-// running products c(t) are taken in step order from t = 0 in every thread
-// (the output kernel forms the same values). Returns (uniformly over the
-// group) whether some decay leaves the range of the scaled form.
-__device__ bool form_carry(ScratchC& sc, const __nv_bfloat16* rs, OpC& op, int len, int ftid) {
+// running products c(t) are taken per block of four steps and the blocks'
+// products chained in step order. Returns (uniformly over the group) whether
+// some decay leaves the range of the scaled form.
+__device__ bool form_carry(ScratchC& sc, float (&Pc)[4][kN], const __nv_bfloat16* rs, OpC& op, int len, int ftid) {
   const int lane = ftid & 31, pf = ftid >> 5, j = 2 * lane, t0 = 4 * pf;
-  bool safe = true;
-  float2 cL = make_float2(1.f, 1.f), cpre = cL;  // cpre = c(t0 - 1)
-#pragma unroll
-  for (int t = 0; t < kL; ++t) {
-    const float2 w = t < len ? bf2(rs + C_W * kTile + t * kN + j) : make_float2(1.f, 1.f);
-    safe &= decay_is_safe(w.x) && decay_is_safe(w.y);
-    cL = fmul2(cL, w);
-    if (t < t0) cpre = cL;
-  }
-  if (named_bar_or(1, 128, !safe)) return true;
-  if (pf == 0) *reinterpret_cast<float2*>(op.cL + j) = cL;
   float2 wv[4], av[4], rv[4], bv[4], dyv[4];
+  bool safe = true;
+  float2 pb = make_float2(1.f, 1.f);
 #pragma unroll
   for (int e = 0; e < 4; ++e) {
     const int o = (t0 + e) * kN + j;
     wv[e] = t0 + e < len ? bf2(rs + C_W * kTile + o) : make_float2(1.f, 1.f);
+    safe &= decay_is_safe(wv[e].x) && decay_is_safe(wv[e].y);
+    pb = fmul2(pb, wv[e]);
+  }
+  *reinterpret_cast<float2*>(&Pc[pf][j]) = pb;
+  if (named_bar_or(1, 128, !safe)) return true;
+  float2 cL = make_float2(1.f, 1.f), cpre = cL;  // cpre = c(t0 - 1)
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    cL = fmul2(cL, *reinterpret_cast<const float2*>(&Pc[q][j]));
+    if (q < pf) cpre = cL;
+  }
+  if (pf == 0) *reinterpret_cast<float2*>(op.cL + j) = cL;
+#pragma unroll
+  for (int e = 0; e < 4; ++e) {
+    const int o = (t0 + e) * kN + j;
     av[e] = bf2(rs + C_A * kTile + o);
     rv[e] = bf2(rs + C_R * kTile + o);
     bv[e] = bf2(rs + C_B * kTile + o);
@@ -334,7 +341,7 @@ __device__ bool front_form(CarrySmem& sm, ScratchC& sc, OpC& op, const __nv_bflo
     if (ftid == 0) sm.abort_flag = 1;
     return false;
   }
-  const bool unsafe = form_carry(sc, rs, op, len, ftid);
+  const bool unsafe = form_carry(sc, sm.Pc, rs, op, len, ftid);
   if (ftid == 0) op.unsafe = unsafe;
   return true;
 }
@@ -622,6 +629,8 @@ struct OutSmem {
   float Mba[kL * kLD16];  // fp32, for the substitution
   float cS[kTile];        // c(t) [t][j], fp32
   float Epart[4][kN];     // colsum(Gc o S0) over the rows of each row block
+  float Ppart[8][kN];     // products of the decays of steps 2 q, 2 q + 1
+  float cLs[kN];          // c(L) = product of the chunk's decays
   float anc[2][kN];  // the chunk's parts of colsum(carry o state) at its start and end, without c(L) colsum(Gc o S0)
 };
 
@@ -787,27 +796,32 @@ __global__ void __launch_bounds__(kThreads, 3) wkv7_bwd4_out_kernel(const __grid
   const bf16_t* rs = sm.raw[0];
 
   // ---- A: scaled operands; thread (lane, warp) forms columns 2 lane, 2 lane + 1 of steps
-  //      2 warp, 2 warp + 1 (running products c in step order from t = 0, as in the carry kernel)
+  //      2 warp, 2 warp + 1. The running products c(t) are taken per pair of steps and the
+  //      pairs' products chained in step order.
   {
     const int j = 2 * lane, ta = 2 * warp;
-    bool safe = true;
-    float2 cL = make_float2(1.f, 1.f), cpre = cL;  // cpre = c(ta - 1)
+    float2 wv[2];
 #pragma unroll
-    for (int t = 0; t < kL; ++t) {
-      const float2 w = t < len ? bf2(rs + V_W * RS + t * kB64 + j) : make_float2(1.f, 1.f);
-      safe &= decay_is_safe(w.x) && decay_is_safe(w.y);
-      cL = fmul2(cL, w);
-      if (t < ta) cpre = cL;
-    }
+    for (int e = 0; e < 2; ++e) wv[e] = ta + e < len ? bf2(rs + V_W * RS + (ta + e) * kB64 + j) : make_float2(1.f, 1.f);
+    const bool safe = decay_is_safe(wv[0].x) && decay_is_safe(wv[0].y) && decay_is_safe(wv[1].x) &&
+                      decay_is_safe(wv[1].y);
+    *reinterpret_cast<float2*>(&sm.Ppart[warp][j]) = fmul2(wv[0], wv[1]);
     if (__syncthreads_or(!safe)) {
       out_direct(sm, S0g, Gcg, len, args, base, vstep, warp, lane);
       return;
     }
+    float2 cL = make_float2(1.f, 1.f), cpre = cL;  // cpre = c(ta - 1)
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
+      cL = fmul2(cL, *reinterpret_cast<const float2*>(&sm.Ppart[q][j]));
+      if (q < warp) cpre = cL;
+    }
+    if (warp == 0) *reinterpret_cast<float2*>(&sm.cLs[j]) = cL;
     float2 c = cpre;
 #pragma unroll
     for (int e = 0; e < 2; ++e) {
       const int t = ta + e, q = t * kB64 + j;
-      const float2 w = t < len ? bf2(rs + V_W * RS + q) : make_float2(1.f, 1.f);
+      const float2 w = wv[e];
       const float2 a = bf2(rs + V_A * RS + q), r = bf2(rs + V_R * RS + q);
       const float2 k = bf2(rs + V_K * RS + q), b = bf2(rs + V_B * RS + q);
       const float2 cprev = c;
@@ -961,6 +975,26 @@ __global__ void __launch_bounds__(kThreads, 3) wkv7_bwd4_out_kernel(const __grid
       mma16(P1[1], a1, b[2], b[3]);
     }
   }
+  // per element (t, j) of this warp: grp 0: 1/c, k, b; grp 1: c, c(t-1), r, a
+  float2 q0[2][2], q1[2][2], q2[2][2], q3[2][2];
+#pragma unroll
+  for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const int t = g + 8 * h, col = j0 + 8 * nt + 2 * t4;
+      const float2 c = *reinterpret_cast<const float2*>(sm.cS + t * kN + col);
+      if (grp == 0) {
+        q0[nt][h] = make_float2(rcp_approx(c.x), rcp_approx(c.y));
+        q1[nt][h] = bf2(rs + V_K * RS + t * kB64 + col);
+        q2[nt][h] = bf2(rs + V_B * RS + t * kB64 + col);
+        q3[nt][h] = make_float2(0.f, 0.f);
+      } else {
+        q0[nt][h] = c;
+        q1[nt][h] = t ? *reinterpret_cast<const float2*>(sm.cS + (t - 1) * kN + col) : make_float2(1.f, 1.f);
+        q2[nt][h] = bf2(rs + V_R * RS + t * kB64 + col);
+        q3[nt][h] = bf2(rs + V_A * RS + t * kB64 + col);
+      }
+    }
   {
     // This warp's part of the dw anchors, from the column products (c(L) colsum(Gc o S0) is
     // added later):
@@ -970,22 +1004,14 @@ __global__ void __launch_bounds__(kThreads, 3) wkv7_bwd4_out_kernel(const __grid
     float v[4];
 #pragma unroll
     for (int nt = 0; nt < 2; ++nt) {
-      const int col = j0 + 8 * nt + 2 * t4;
       float2 acc = make_float2(0.f, 0.f);
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
-        const int t = g + 8 * h;
-        const float2 c = *reinterpret_cast<const float2*>(sm.cS + t * kN + col);
-        if (grp == 0) {
-          const float2 k = bf2(rs + V_K * RS + t * kB64 + col), b = bf2(rs + V_B * RS + t * kB64 + col);
-          acc.x += fmaf(k.x, P0[nt][2 * h], b.x * P1[nt][2 * h]) * rcp_approx(c.x);
-          acc.y += fmaf(k.y, P0[nt][2 * h + 1], b.y * P1[nt][2 * h + 1]) * rcp_approx(c.y);
-        } else {
-          const float2 cp = t ? *reinterpret_cast<const float2*>(sm.cS + (t - 1) * kN + col) : make_float2(1.f, 1.f);
-          const float2 r = bf2(rs + V_R * RS + t * kB64 + col), a = bf2(rs + V_A * RS + t * kB64 + col);
-          acc.x += fmaf(r.x * c.x, P0[nt][2 * h], a.x * cp.x * P1[nt][2 * h]);
-          acc.y += fmaf(r.y * c.y, P0[nt][2 * h + 1], a.y * cp.y * P1[nt][2 * h + 1]);
-        }
+        // grp 0: Kb = k c(L) / c, Bb = b c(L) / c (c(L) applied after the sum); grp 1: R^ = r c, A^ = a c(t-1)
+        const float2 m0 = grp ? fmul2(q2[nt][h], q0[nt][h]) : fmul2(q1[nt][h], q0[nt][h]);
+        const float2 m1 = grp ? fmul2(q3[nt][h], q1[nt][h]) : fmul2(q2[nt][h], q0[nt][h]);
+        acc = ffma2(m0, make_float2(P0[nt][2 * h], P0[nt][2 * h + 1]), acc);
+        acc = ffma2(m1, make_float2(P1[nt][2 * h], P1[nt][2 * h + 1]), acc);
       }
       v[2 * nt] = acc.x;
       v[2 * nt + 1] = acc.y;
@@ -998,7 +1024,7 @@ __global__ void __launch_bounds__(kThreads, 3) wkv7_bwd4_out_kernel(const __grid
     y += __shfl_xor_sync(0xffffffffu, y, 4);
     if ((g & 1) == 0) {
       const int col = j0 + 8 * (up16 ? 1 : 0) + 2 * t4 + (up8 ? 1 : 0);
-      const float cl = sm.cS[(kL - 1) * kN + col];
+      const float cl = sm.cLs[col];
       sm.anc[grp ? 0 : 1][col] = grp ? y : cl * y;
     }
   }
@@ -1011,7 +1037,7 @@ __global__ void __launch_bounds__(kThreads, 3) wkv7_bwd4_out_kernel(const __grid
     if (grp == 0) {
 #pragma unroll
       for (int nt = 0; nt < 2; ++nt) {
-        const float2 cl = *reinterpret_cast<const float2*>(sm.cS + (kL - 1) * kN + j0 + 8 * nt + 2 * t4);
+        const float2 cl = *reinterpret_cast<const float2*>(sm.cLs + j0 + 8 * nt + 2 * t4);
         P0[nt][0] *= cl.x;
         P0[nt][1] *= cl.y;
         P0[nt][2] *= cl.x;
@@ -1059,11 +1085,9 @@ __global__ void __launch_bounds__(kThreads, 3) wkv7_bwd4_out_kernel(const __grid
   for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
-      const int t = g + 8 * h, col = j0 + 8 * nt + 2 * t4;
-      const float2 c = *reinterpret_cast<const float2*>(sm.cS + t * kN + col);
       if (grp == 0) {
-        const float2 k = bf2(rs + V_K * RS + t * kB64 + col), b = bf2(rs + V_B * RS + t * kB64 + col);
-        const float ic[2] = {rcp_approx(c.x), rcp_approx(c.y)}, kv[2] = {k.x, k.y}, bv[2] = {b.x, b.y};
+        const float ic[2] = {q0[nt][h].x, q0[nt][h].y}, kv[2] = {q1[nt][h].x, q1[nt][h].y},
+                    bv[2] = {q2[nt][h].x, q2[nt][h].y};
 #pragma unroll
         for (int e = 0; e < 2; ++e) {
           P0[nt][2 * h + e] *= ic[e];
@@ -1072,9 +1096,8 @@ __global__ void __launch_bounds__(kThreads, 3) wkv7_bwd4_out_kernel(const __grid
           AD[nt][2 * h + e] = 0.f;
         }
       } else {
-        const float2 cp = t ? *reinterpret_cast<const float2*>(sm.cS + (t - 1) * kN + col) : make_float2(1.f, 1.f);
-        const float2 r = bf2(rs + V_R * RS + t * kB64 + col), a = bf2(rs + V_A * RS + t * kB64 + col);
-        const float cv[2] = {c.x, c.y}, cpv[2] = {cp.x, cp.y}, rv[2] = {r.x, r.y}, av[2] = {a.x, a.y};
+        const float cv[2] = {q0[nt][h].x, q0[nt][h].y}, cpv[2] = {q1[nt][h].x, q1[nt][h].y},
+                    rv[2] = {q2[nt][h].x, q2[nt][h].y}, av[2] = {q3[nt][h].x, q3[nt][h].y};
 #pragma unroll
         for (int e = 0; e < 2; ++e) {
           P0[nt][2 * h + e] *= cv[e];
@@ -1137,7 +1160,7 @@ __global__ void __launch_bounds__(kThreads, 3) wkv7_bwd4_out_kernel(const __grid
     const int col = jw + 2 * t4 + e;
     const float2 w0 = bf2(rs + V_W * RS + g * kB64 + jw + 2 * t4);
     const float2 w1 = bf2(rs + V_W * RS + (g + 8) * kB64 + jw + 2 * t4);
-    const float cge = sm.cS[(kL - 1) * kN + col] * (sm.Epart[0][col] + sm.Epart[1][col] + sm.Epart[2][col] + sm.Epart[3][col]);
+    const float cge = sm.cLs[col] * (sm.Epart[0][col] + sm.Epart[1][col] + sm.Epart[2][col] + sm.Epart[3][col]);
     dw[e] = (cge + sm.anc[0][col] - (lo - xw[e]) - adw[e]) * rcp_approx(e ? w0.y : w0.x);
     dw[2 + e] = (hi2 - adw[2 + e] + cge + sm.anc[1][col]) * rcp_approx(e ? w1.y : w1.x);
   }
