@@ -160,43 +160,6 @@ __device__ __forceinline__ void store_masked16(const float (&acc)[2][4], bf16_t*
 }
 
 
-// acc = P Q^T for 16-row P, Q (ld kLD64, tf32 values), K = 64.
-__device__ __forceinline__ void gram16(float (&acc)[2][4], const float* P, const float* Q, int g, int t4) {
-  zero4(acc[0]);
-  zero4(acc[1]);
-#pragma unroll
-  for (int kb = 0; kb < kN / 8; ++kb) {
-    uint32_t a[4];
-    frag_a(a, P, kLD64, 0, 8 * kb, g, t4);
-#pragma unroll
-    for (int nt = 0; nt < 2; ++nt) {
-      uint32_t b0, b1;
-      frag_b(b0, b1, Q, kLD64, 8 * nt, 8 * kb, g, t4);
-      mma_tf32(acc[nt], a, b0, b1);
-    }
-  }
-}
-
-// Store a 16 x 16 accumulator as tf32, keeping (t, s) with
-// lower: s < t (+ s == t if incl); upper: s > t (+ s == t if incl).
-__device__ __forceinline__ void store_masked(const float (&acc)[2][4], float* dst, bool lower, bool incl, int g,
-                                             int t4) {
-#pragma unroll
-  for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-    for (int h = 0; h < 2; ++h) {
-      const int t = g + 8 * h, s = 8 * nt + 2 * t4;
-      float x[2];
-#pragma unroll
-      for (int e = 0; e < 2; ++e) {
-        const int se = s + e;
-        const bool keep = lower ? (se < t || (incl && se == t)) : (se > t || (incl && se == t));
-        x[e] = keep ? acc[nt][2 * h + e] : 0.f;
-      }
-      *reinterpret_cast<float2*>(dst + t * kLD16 + s) = make_float2(tf32r(x[0]), tf32r(x[1]));
-    }
-}
-
 // T = (I - M)^-1 for a strictly lower 16 x 16 M (stride kLD16) by forward
 // substitution, one warp; lane s < 16 owns column s. Writes T (row-major)
 // and/or its transpose as tf32 values.
@@ -263,17 +226,18 @@ struct OpC {
   int pad_[3];
 };
 
-// Scaled operands only the products group reads (one set per chunk in flight).
+// Per chunk in flight between the forming and the products group.
 struct ScratchC {
   float Ah[kL * kLD64], Bt[kL * kLD64];  // A^, B~ [t][j]
   float Bb68[kL * kLDT];                 // Bb [t][j]
+  float Mbr[kL * kLD16], Mba[kL * kLD16];  // R^ B~^T (with diagonal), A^ B~^T (strictly lower) [t][s]
 };
 
 struct CarrySmem {
   __nv_bfloat16 raw[kCarryStages][5][kTile];  // r, w, a, b, dy of one chunk per stage
   OpC op[3];
   ScratchC sc[2];
-  float Mbr[kL * kLD16], Mba[kL * kLD16], TT[kL * kLD16];  // [t][s]; TT = T^T
+  float TT[kL * kLD16];  // T^T, T = (I - Mba)^-1
   float Pc[4][kN];                                         // products of the decays of four-step blocks
   uint64_t full[kCarryStages];
   int abort_flag;
@@ -343,21 +307,36 @@ __device__ bool front_form(CarrySmem& sm, ScratchC& sc, OpC& op, const __nv_bflo
   }
   const bool unsafe = form_carry(sc, sm.Pc, rs, op, len, ftid);
   if (ftid == 0) op.unsafe = unsafe;
+  if (unsafe) return true;
+  named_bar(1, 128);
+  // n-tile (pf % 2) of Mbr = R^ B~^T (pf < 2) or Mba = A^ B~^T (pf >= 2)
+  const int pf = ftid >> 5, lane = ftid & 31, g = lane >> 2, t4 = lane & 3, nt = pf & 1;
+  const bool is_ba = pf >= 2;
+  const float* P = is_ba ? sc.Ah : op.Rh;
+  float acc[4];
+  zero4(acc);
+#pragma unroll
+  for (int kb = 0; kb < kN / 8; ++kb) {
+    uint32_t a[4], b0, b1;
+    frag_a(a, P, kLD64, 0, 8 * kb, g, t4);
+    frag_b(b0, b1, sc.Bt, kLD64, 8 * nt, 8 * kb, g, t4);
+    mma_tf32(acc, a, b0, b1);
+  }
+  float* M = is_ba ? sc.Mba : sc.Mbr;
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    const int t = g + 8 * h, s = 8 * nt + 2 * t4;
+    const bool k0 = is_ba ? s < t : s <= t, k1 = is_ba ? s + 1 < t : s + 1 <= t;
+    *reinterpret_cast<float2*>(M + t * kLD16 + s) =
+        make_float2(k0 ? tf32r(acc[2 * h]) : 0.f, k1 ? tf32r(acc[2 * h + 1]) : 0.f);
+  }
   return true;
 }
 
-// Products group (128 threads): Mbr, Mba, T, T^T Bb and Mbr T of a formed chunk.
+// Products group (128 threads): T, T^T Bb and Mbr T of a formed chunk.
 __device__ void front_products(CarrySmem& sm, const ScratchC& sc, OpC& op) {
   const int pp = (threadIdx.x >> 5) - 8, lane = threadIdx.x & 31, g = lane >> 2, t4 = lane & 3;
-  if (pp < 2) {  // Mbr = R^ B~^T (with diagonal), Mba = A^ B~^T (strictly lower), then T
-    float acc[2][4];
-    gram16(acc, pp ? sc.Ah : op.Rh, sc.Bt, g, t4);
-    store_masked(acc, pp ? sm.Mba : sm.Mbr, true, pp == 0, g, t4);
-    if (pp == 1) {
-      __syncwarp();
-      unit_lower_inverse(sm.Mba, nullptr, sm.TT, lane);
-    }
-  }
+  if (pp == 0) unit_lower_inverse(sc.Mba, nullptr, sm.TT, lane);
   named_bar(2, 128);
   {  // T^T Bb, n-tiles 2 pp and 2 pp + 1
     float acc[2][4];
@@ -388,7 +367,7 @@ __device__ void front_products(CarrySmem& sm, const ScratchC& sc, OpC& op) {
 #pragma unroll
     for (int kb = 0; kb < 2; ++kb) {
       uint32_t a[4], b0, b1;
-      frag_a(a, sm.Mbr, kLD16, 0, 8 * kb, g, t4);
+      frag_a(a, sc.Mbr, kLD16, 0, 8 * kb, g, t4);
       frag_b(b0, b1, sm.TT, kLD16, 8 * q, 8 * kb, g, t4);
       mma_tf32(acc, a, b0, b1);
     }
