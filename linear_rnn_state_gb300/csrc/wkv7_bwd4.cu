@@ -606,7 +606,7 @@ struct OutSmem {
   // U2 = triu(SA DY^T), U3 = triu(SA DSA^T, 1) [t][s]
   bf16_t M[3][kL * kB16], Tm[kL * kB16], U[4][kL * kB16];
   float Mba[kL * kLD16];  // fp32, for the substitution
-  float cS[kTile];        // c(t) [t][j], fp32
+  float cS[kL * kLD64];   // c(t) [t][j], fp32
   float Epart[4][kN];     // colsum(Gc o S0) over the rows of each row block
   float Ppart[8][kN];     // products of the decays of steps 2 q, 2 q + 1
   float cLs[kN];          // c(L) = product of the chunk's decays
@@ -812,7 +812,7 @@ __global__ void __launch_bounds__(kThreads, 3) wkv7_bwd4_out_kernel(const __grid
       st_pair(sm.Bt + q, fmul2(b, ic));
       st_pair(sm.Kb + q, fmul2(k, s));
       st_pair(sm.Bb + q, fmul2(b, s));
-      *reinterpret_cast<float2*>(sm.cS + t * kN + j) = c;
+      *reinterpret_cast<float2*>(sm.cS + t * kLD64 + j) = c;
     }
   }
   __syncthreads();
@@ -955,26 +955,29 @@ __global__ void __launch_bounds__(kThreads, 3) wkv7_bwd4_out_kernel(const __grid
     }
   }
   // per element (t, j) of this warp: grp 0: 1/c, k, b; grp 1: c, c(t-1), r, a
-  float2 q0[2][2], q1[2][2], q2[2][2], q3[2][2];
+  auto load_q = [&](float2 (&q0)[2][2], float2 (&q1)[2][2], float2 (&q2)[2][2], float2 (&q3)[2][2]) {
 #pragma unroll
-  for (int nt = 0; nt < 2; ++nt)
+    for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
-    for (int h = 0; h < 2; ++h) {
-      const int t = g + 8 * h, col = j0 + 8 * nt + 2 * t4;
-      const float2 c = *reinterpret_cast<const float2*>(sm.cS + t * kN + col);
-      if (grp == 0) {
-        q0[nt][h] = make_float2(rcp_approx(c.x), rcp_approx(c.y));
-        q1[nt][h] = bf2(rs + V_K * RS + t * kB64 + col);
-        q2[nt][h] = bf2(rs + V_B * RS + t * kB64 + col);
-        q3[nt][h] = make_float2(0.f, 0.f);
-      } else {
-        q0[nt][h] = c;
-        q1[nt][h] = t ? *reinterpret_cast<const float2*>(sm.cS + (t - 1) * kN + col) : make_float2(1.f, 1.f);
-        q2[nt][h] = bf2(rs + V_R * RS + t * kB64 + col);
-        q3[nt][h] = bf2(rs + V_A * RS + t * kB64 + col);
+      for (int h = 0; h < 2; ++h) {
+        const int t = g + 8 * h, col = j0 + 8 * nt + 2 * t4;
+        const float2 c = *reinterpret_cast<const float2*>(sm.cS + t * kLD64 + col);
+        if (grp == 0) {
+          q0[nt][h] = make_float2(rcp_approx(c.x), rcp_approx(c.y));
+          q1[nt][h] = bf2(rs + V_K * RS + t * kB64 + col);
+          q2[nt][h] = bf2(rs + V_B * RS + t * kB64 + col);
+          q3[nt][h] = make_float2(0.f, 0.f);
+        } else {
+          q0[nt][h] = c;
+          q1[nt][h] = t ? *reinterpret_cast<const float2*>(sm.cS + (t - 1) * kLD64 + col) : make_float2(1.f, 1.f);
+          q2[nt][h] = bf2(rs + V_R * RS + t * kB64 + col);
+          q3[nt][h] = bf2(rs + V_A * RS + t * kB64 + col);
+        }
       }
-    }
+  };
   {
+    float2 q0[2][2], q1[2][2], q2[2][2], q3[2][2];
+    load_q(q0, q1, q2, q3);
     // This warp's part of the dw anchors, from the column products (c(L) colsum(Gc o S0) is
     // added later):
     //   colsum(Gc o S(L)) = c(L) colsum(Gc o S0) + sum_t (Kb o V Gc + Bb o SA Gc)       (grp 0)
@@ -1060,6 +1063,8 @@ __global__ void __launch_bounds__(kThreads, 3) wkv7_bwd4_out_kernel(const __grid
   // unscale: dk = dk~ / c, db = db~ / c (grp 0); dr = dr^ c, da = da^ c(t-1) (grp 1); and this
   // group's part of x = r dr - k dk - b db + a da
   float X[2][4], AD[2][4];
+  float2 q0[2][2], q1[2][2], q2[2][2], q3[2][2];
+  load_q(q0, q1, q2, q3);
 #pragma unroll
   for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
@@ -1086,76 +1091,48 @@ __global__ void __launch_bounds__(kThreads, 3) wkv7_bwd4_out_kernel(const __grid
         }
       }
     }
-  // exchange with the partner warp of the other group (same columns): grp 0 keeps
-  // dw of n-tile 0, grp 1 of n-tile 1
-  float* XK = sm.u.xch[0];  // grp 0's x part, [t][j] stride 72
-  float* XR = sm.u.xch[1];  // grp 1's x part
-  float* XA = sm.u.xch[2];  // grp 1's a da
-#pragma unroll
-  for (int h = 0; h < 2; ++h) {
-    const int t = g + 8 * h;
-    if (grp == 0) {
-      *reinterpret_cast<float2*>(XK + t * kLD64 + j0 + 8 + 2 * t4) = make_float2(X[1][2 * h], X[1][2 * h + 1]);
-    } else {
-      *reinterpret_cast<float2*>(XR + t * kLD64 + j0 + 2 * t4) = make_float2(X[0][2 * h], X[0][2 * h + 1]);
-      *reinterpret_cast<float2*>(XA + t * kLD64 + j0 + 2 * t4) = make_float2(AD[0][2 * h], AD[0][2 * h + 1]);
-    }
-  }
-  named_bar(1 + jb, 64);
-  const int nw = grp, jw = j0 + 8 * nw;  // this warp's dw columns jw .. jw+7
-  float xw[4], adw[4];
-#pragma unroll
-  for (int h = 0; h < 2; ++h) {
-    const int t = g + 8 * h;
-    if (grp == 0) {
-      const float2 xr = *reinterpret_cast<const float2*>(XR + t * kLD64 + jw + 2 * t4);
-      const float2 xa = *reinterpret_cast<const float2*>(XA + t * kLD64 + jw + 2 * t4);
-      xw[2 * h] = X[0][2 * h] + xr.x;
-      xw[2 * h + 1] = X[0][2 * h + 1] + xr.y;
-      adw[2 * h] = xa.x;
-      adw[2 * h + 1] = xa.y;
-    } else {
-      const float2 xk = *reinterpret_cast<const float2*>(XK + t * kLD64 + jw + 2 * t4);
-      xw[2 * h] = X[1][2 * h] + xk.x;
-      xw[2 * h + 1] = X[1][2 * h + 1] + xk.y;
-      adw[2 * h] = AD[1][2 * h];
-      adw[2 * h + 1] = AD[1][2 * h + 1];
-    }
-  }
-  // w dw from the identity, anchored where fewer terms are summed:
-  // rows t < 8: colsum(carry at the chunk start o S0) - sum_{u<t} x(u) - a(t) da(t);
-  // rows t >= 8: sum_{u>=t} x(u) - a(t) da(t) + colsum(carry at the chunk end o S(L)).
-  float dw[4];
-#pragma unroll
-  for (int e = 0; e < 2; ++e) {
-    float hi2 = xw[2 + e], lo = xw[e];
-#pragma unroll
-    for (int d = 1; d < 8; d <<= 1) {
-      const float oh = __shfl_down_sync(0xffffffffu, hi2, 4 * d);
-      const float ol = __shfl_up_sync(0xffffffffu, lo, 4 * d);
-      if (g + d < 8) hi2 += oh;
-      if (g >= d) lo += ol;
-    }
-    const int col = jw + 2 * t4 + e;
-    const float2 w0 = bf2(rs + V_W * RS + g * kB64 + jw + 2 * t4);
-    const float2 w1 = bf2(rs + V_W * RS + (g + 8) * kB64 + jw + 2 * t4);
-    const float cge = sm.cLs[col] * (sm.Epart[0][col] + sm.Epart[1][col] + sm.Epart[2][col] + sm.Epart[3][col]);
-    dw[e] = (cge + sm.anc[0][col] - (lo - xw[e]) - adw[e]) * rcp_approx(e ? w0.y : w0.x);
-    dw[2 + e] = (hi2 - adw[2 + e] + cge + sm.anc[1][col]) * rcp_approx(e ? w1.y : w1.x);
-  }
+  // this warp's outputs, and its part of x for dw: grp 0 -k dk - b db, grp 1 r dr + a da and a da
+  float* XK = sm.u.xch[0];  // [t][j] stride 72
+  float* XR = sm.u.xch[1];
+  float* XA = sm.u.xch[2];
   float* out0 = grp ? args.dr : args.dk;
   float* out1 = grp ? args.da : args.db;
 #pragma unroll
   for (int h = 0; h < 2; ++h) {
     const int t = g + 8 * h;
-    if (t < len) {
-      const size_t off = base + (size_t)t * vstep + j0 + 2 * t4;
 #pragma unroll
-      for (int nt = 0; nt < 2; ++nt) {
-        *reinterpret_cast<float2*>(out0 + off + 8 * nt) = make_float2(P0[nt][2 * h], P0[nt][2 * h + 1]);
-        *reinterpret_cast<float2*>(out1 + off + 8 * nt) = make_float2(P1[nt][2 * h], P1[nt][2 * h + 1]);
+    for (int nt = 0; nt < 2; ++nt) {
+      const int col = j0 + 8 * nt + 2 * t4;
+      *reinterpret_cast<float2*>((grp ? XR : XK) + t * kLD64 + col) = make_float2(X[nt][2 * h], X[nt][2 * h + 1]);
+      if (grp) *reinterpret_cast<float2*>(XA + t * kLD64 + col) = make_float2(AD[nt][2 * h], AD[nt][2 * h + 1]);
+      if (t < len) {
+        const size_t off = base + (size_t)t * vstep + col;
+        *reinterpret_cast<float2*>(out0 + off) = make_float2(P0[nt][2 * h], P0[nt][2 * h + 1]);
+        *reinterpret_cast<float2*>(out1 + off) = make_float2(P1[nt][2 * h], P1[nt][2 * h + 1]);
       }
-      *reinterpret_cast<float2*>(args.dw + off + 8 * nw) = make_float2(dw[2 * h], dw[2 * h + 1]);
+    }
+  }
+  __syncthreads();
+  // w dw from the identity, one thread per column, anchored where fewer terms are summed:
+  //   t < 8:  colsum(carry at the chunk start o S0) - sum_{u<t} x(u) - a(t) da(t)
+  //   t >= 8: sum_{u>=t} x(u) - a(t) da(t) + colsum(carry at the chunk end o S(L))
+  if (tid < kN) {
+    const int col = tid;
+    const float cge = sm.cLs[col] * (sm.Epart[0][col] + sm.Epart[1][col] + sm.Epart[2][col] + sm.Epart[3][col]);
+    float run = cge + sm.anc[0][col];  // start anchor, minus the x of the steps before t
+#pragma unroll
+    for (int t = 0; t < kL / 2; ++t) {
+      const float x = XK[t * kLD64 + col] + XR[t * kLD64 + col];
+      const float v = (run - XA[t * kLD64 + col]) * rcp_approx(bf(rs + V_W * RS + t * kB64 + col));
+      if (t < len) args.dw[base + (size_t)t * vstep + col] = v;
+      run -= x;
+    }
+    run = cge + sm.anc[1][col];  // end anchor, plus the x of the steps from t on
+#pragma unroll
+    for (int t = kL - 1; t >= kL / 2; --t) {
+      run += XK[t * kLD64 + col] + XR[t * kLD64 + col];
+      const float v = (run - XA[t * kLD64 + col]) * rcp_approx(bf(rs + V_W * RS + t * kB64 + col));
+      if (t < len) args.dw[base + (size_t)t * vstep + col] = v;
     }
   }
 }
