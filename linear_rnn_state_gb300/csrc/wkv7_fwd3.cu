@@ -16,14 +16,15 @@
 // products run on tf32 tensor cores with fp32 accumulation; the state stays
 // fp32 in registers.
 //
-// One CTA per (b, h), eight warps in two groups working one chunk apart:
-//  - prep warps (4..7) turn the chunk's r, w, k, v, a, b (TMA tensor loads
-//    into a four-stage ring) into the scaled operands, the four L x L
-//    products and T = (I - Mba)^-1 (forward substitution, one warp), in a
-//    double-buffered operand block;
+// One CTA per (b, h), twelve warps in three groups working one chunk apart:
+//  - forming warps (4..7) turn chunk n+2's r, w, k, v, a, b (TMA tensor loads
+//    into a four-stage ring) into the scaled operands;
+//  - products warps (8..11) make chunk n+1's four L x L products and
+//    T = (I - Mba)^-1 (forward substitution, one warp);
 //  - state warps (0..3) each own 16 rows i of S as mma accumulator tiles
-//    and compute S0 [A^ R^]^T, SA, Y and S(L) for the chunk the prep warps
-//    finished in the previous round, and write y and the checkpoints.
+//    and compute S0 [A^ R^]^T, SA, Y and S(L) for chunk n, and write y and
+//    the checkpoints.
+// Operand blocks rotate over three buffers.
 // A chunk whose decays leave [1/16, 16] (or hold a NaN) is run step by step
 // in the direct form by the state warps, in fp32.
 #include "wkv7_launch.h"
@@ -52,15 +53,15 @@ struct Prep3 {
 
 struct Fwd3Smem {
   __nv_bfloat16 raw[4][6][kL * kN];  // TMA ring: r, w, k, v, a, b of one chunk per stage
-  Prep3 prep[2];
-  float X2[2 * kL * kLD64];  // rows 0..15: k~(s); rows 16..31: b~(s)   [s][j]
+  Prep3 prep[3];
+  float X2[2][2 * kL * kLD64];  // per chunk in flight: rows 0..15: k~(s); rows 16..31: b~(s)   [s][j]
   __nv_bfloat16 ys[kL * kN];  // y of the chunk [t][i]
   uint64_t full[4];
   int abort_flag;
 };
 
 constexpr int kStages = 4;
-constexpr int kThreads = 256;
+constexpr int kThreads = 384;  // warps 0-3: state; 4-7: forming; 8-11: products
 enum { V_R = 0, V_W = 1, V_K = 2, V_V = 3, V_A = 4, V_B = 5 };
 
 __device__ __forceinline__ float bf(const __nv_bfloat16* p) { return __bfloat162float(*p); }
@@ -68,11 +69,10 @@ __device__ __forceinline__ float2 bf2(const __nv_bfloat16* p) {
   return __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(p));
 }
 
-// ------------------------------------------------------------ prep warps ---
+// ---------------------------------------------------------- forming group ---
 // 128 threads; thread (j = ptid % 64, half = ptid / 64) forms column j of
 // steps 8*half .. 8*half+7.
-__device__ void prep_chunk(Fwd3Smem& sm, Prep3& P, int stage, int len, int ptid) {
-  const int pw = ptid >> 5, lane = ptid & 31, g = lane >> 2, t4 = lane & 3;
+__device__ void form_chunk(Fwd3Smem& sm, Prep3& P, float* X2, int stage, int len, int ptid) {
   const __nv_bfloat16* rs = sm.raw[stage][0];
   const int j = ptid & 63, half = ptid >> 6;
   // decays of this thread's 8 steps (wm) and of the other 8 (wo); padding
@@ -116,8 +116,8 @@ __device__ void prep_chunk(Fwd3Smem& sm, Prep3& P, int stage, int len, int ptid)
     const float ic = rcp_approx(c);
     const int o = t * kN + j;
     const float a = av[e], r = rv[e], k = kv[e], b = bv[e];
-    sm.X2[t * kLD64 + j] = tf32r(k * ic);
-    sm.X2[(kL + t) * kLD64 + j] = tf32r(b * ic);
+    X2[t * kLD64 + j] = tf32r(k * ic);
+    X2[(kL + t) * kLD64 + j] = tf32r(b * ic);
     P.X1[t * kLD64 + j] = tf32r(a * cprev);
     P.X1[(kL + t) * kLD64 + j] = tf32r(r * c);
     const float s = cL * ic;
@@ -133,8 +133,13 @@ __device__ void prep_chunk(Fwd3Smem& sm, Prep3& P, int stage, int len, int ptid)
   }
   unsafe = named_bar_or(1, 128, unsafe);
   if (ptid == 0) P.unsafe = unsafe;
-  if (unsafe) return;
+}
 
+// --------------------------------------------------------- products group ---
+// The four L x L products and T of a formed chunk (128 threads; skipped by the
+// caller for a chunk in the direct form).
+__device__ void gram_chunk(Prep3& P, const float* X2, int gtid) {
+  const int pw = gtid >> 5, lane = gtid & 31, g = lane >> 2, t4 = lane & 3;
   // Gram blocks: warp pw computes [A^ | R^](rows 16*(pw/2)) x [K~ | B~](rows 16*(pw%2))^T.
   {
     const int mt = pw >> 1, nb = pw & 1;
@@ -148,7 +153,7 @@ __device__ void prep_chunk(Fwd3Smem& sm, Prep3& P, int stage, int len, int ptid)
 #pragma unroll
       for (int nt = 0; nt < 2; ++nt) {
         uint32_t b0, b1;
-        frag_b(b0, b1, sm.X2, kLD64, 16 * nb + 8 * nt, 8 * kb, g, t4);
+        frag_b(b0, b1, X2, kLD64, 16 * nb + 8 * nt, 8 * kb, g, t4);
         mma_tf32(acc[nt], a, b0, b1);
       }
     }
@@ -341,11 +346,14 @@ __global__ void __launch_bounds__(kThreads, 1) wkv7_fwd3_kernel(const __grid_con
   const int T = args.T, H = args.H;
   const int head = blockIdx.x, bi = head / H, hi = head % H;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const bool is_prep = warp >= 4;
-  const int ptid = tid - 128;
+  const int role = warp < 4 ? 0 : warp < 8 ? 1 : 2;  // state, forming, products
+  const int ftid = tid - 128, gtid = tid - 256;
   const int nchunks = (T + kL - 1) / kL;
   constexpr int kStageBytes = 6 * kL * kN * 2;
 
+  // Chunk n: the state warps run it in round n, the products group makes its
+  // L x L products and T in round n-1, the forming group forms it in round
+  // n-2; its inputs arrive by TMA four rounds ahead (a four-stage ring).
   auto issue = [&](int chunk) {
     const int st = chunk % kStages;
     mbar_arrive_expect_tx(&sm.full[st], kStageBytes);
@@ -363,7 +371,7 @@ __global__ void __launch_bounds__(kThreads, 1) wkv7_fwd3_kernel(const __grid_con
   c.g = lane >> 2;
   c.t4 = lane & 3;
   c.i0 = 16 * warp;
-  if (!is_prep) {
+  if (role == 0) {
 #pragma unroll
     for (int nt = 0; nt < 8; ++nt)
 #pragma unroll
@@ -384,35 +392,46 @@ __global__ void __launch_bounds__(kThreads, 1) wkv7_fwd3_kernel(const __grid_con
   }
   __syncthreads();
 
-  // Prep warps wait for a stage together: the group agrees on the outcome, so
-  // its named barriers stay matched; a timeout raises the CTA's abort flag.
-  int waited = 0;  // chunks whose stage has landed (prep warps)
+  // The forming group waits for a stage together: the group agrees on the
+  // outcome, so its named barriers stay matched; a timeout raises the CTA's
+  // abort flag.
+  int waited = 0;  // chunks whose stage has landed (forming group)
   int issued = min(kStages, nchunks);  // chunks whose copy was started (thread 128)
-  auto wait_stage = [&](int chunk) -> bool {
+  auto chunk_len = [&](int chunk) { return min(kL, T - chunk * kL); };
+  auto form = [&](int chunk) {
     const bool ok = mbar_wait_bounded(args.status, &sm.full[chunk % kStages], (chunk / kStages) & 1);
-    const bool bad = named_bar_or(1, 128, !ok);
-    if (bad) {
-      if (ptid == 0) sm.abort_flag = 1;
-      return false;
+    if (named_bar_or(1, 128, !ok)) {
+      if (ftid == 0) sm.abort_flag = 1;
+      return;
     }
     waited = chunk + 1;
-    return true;
+    form_chunk(sm, sm.prep[chunk % 3], sm.X2[chunk & 1], chunk % kStages, chunk_len(chunk), ftid);
   };
-  auto chunk_len = [&](int chunk) { return min(kL, T - chunk * kL); };
+  auto grams = [&](int chunk) {
+    Prep3& P = sm.prep[chunk % 3];
+    if (!P.unsafe) gram_chunk(P, sm.X2[chunk & 1], gtid);
+  };
 
-  if (is_prep && wait_stage(0)) prep_chunk(sm, sm.prep[0], 0, chunk_len(0), ptid);
+  // pipeline fill: form chunks 0 and 1, products of chunk 0
+  if (role == 1) form(0);
+  bool aborted = __syncthreads_or(sm.abort_flag) != 0;
+  if (!aborted) {
+    if (role == 1 && nchunks > 1) form(1);
+    if (role == 2) grams(0);
+    aborted = __syncthreads_or(sm.abort_flag) != 0;
+  }
   __nv_bfloat16* y = static_cast<__nv_bfloat16*>(args.y);
   const size_t vstep = (size_t)H * kN;
   const size_t vbase = ((size_t)bi * T * H + hi) * kN;
   float* ck_head = args.ckpt ? args.ckpt + (size_t)head * args.nck * kN * kN : nullptr;
 
-  bool aborted = __syncthreads_or(sm.abort_flag) != 0;
   for (int n = 0; n < nchunks && !aborted; ++n) {
-    if (is_prep) {
-      if (n + 1 < nchunks && wait_stage(n + 1))
-        prep_chunk(sm, sm.prep[(n + 1) & 1], (n + 1) % kStages, chunk_len(n + 1), ptid);
+    if (role == 1) {
+      if (n + 2 < nchunks) form(n + 2);
+    } else if (role == 2) {
+      if (n + 1 < nchunks) grams(n + 1);
     } else {
-      const Prep3& P = sm.prep[n & 1];
+      const Prep3& P = sm.prep[n % 3];
       const int t0 = n * kL, len = chunk_len(n);
       if (ck_head && t0 % args.C == 0) store_state(c, ck_head + (size_t)(t0 / args.C) * kN * kN);
       if (P.unsafe)
@@ -427,6 +446,7 @@ __global__ void __launch_bounds__(kThreads, 1) wkv7_fwd3_kernel(const __grid_con
               *reinterpret_cast<const uint4*>(sm.ys + row * kN + 8 * piece);
       }
     }
+    // the stage of chunk n is free (formed two rounds ago, direct steps done); refill it
     aborted = __syncthreads_or(sm.abort_flag) != 0;
     if (!aborted && tid == 128 && n + kStages < nchunks) {
       fence_proxy_async_smem();
@@ -442,7 +462,7 @@ __global__ void __launch_bounds__(kThreads, 1) wkv7_fwd3_kernel(const __grid_con
     __syncthreads();
     return;
   }
-  if (!is_prep && args.s_final) store_state(c, args.s_final + (size_t)head * kN * kN);
+  if (role == 0 && args.s_final) store_state(c, args.s_final + (size_t)head * kN * kN);
 }
 
 }  // namespace
