@@ -26,15 +26,16 @@ sys.path.insert(0, ROOT)
 METRIC = "WKV7 fwd+bwd tokens/s (B·T) at 1.5B shape; achieved % of roofline"
 FP32_LANES_PER_SM = 128  # Blackwell SM: 4 partitions x 32 FP32 lanes
 
-# DRAM bytes (read + write) per token-head of the backward kernel, from one ncu capture
-# (dram__bytes_read.sum + dram__bytes_write.sum at T=1024, divided by B*T*H; traffic grows in
-# proportion to T). It is valid only for the kernel sources it was taken on: a change to any of
-# them makes the report carry null instead.
+# The backward call (wkv7_backward_bf16) launches two kernels: the carry chain and the
+# per-chunk output pass. DRAM bytes (read + write) per token-head of the two together, from one
+# ncu capture (dram__bytes_read.sum + dram__bytes_write.sum at T=1024, divided by B*T*H;
+# traffic grows in proportion to T). It is valid only for the kernel sources it was taken on: a
+# change to any of them makes the report carry null instead.
 TRAFFIC = {
-    "kernel": "wkv7_bwd3_kernel",
-    "sources": ("wkv7_bwd3.cu", "wkv7_common.cuh", "wkv7_scaled.cuh", "wkv7_mma.cuh", "wkv7_launch.h"),
-    "sha256": "8a78e1c25c92002105b001afecd1c4bf3ee4f52db8ac7935e74a5875f0049044",
-    "bytes_per_token_head": (251.771904e6 + 163.0528e6) / 131072,
+    "kernel": "wkv7_bwd4_carry_kernel + wkv7_bwd4_out_kernel (one wkv7_backward_bf16 call)",
+    "sources": ("wkv7_bwd4.cu", "wkv7_common.cuh", "wkv7_scaled.cuh", "wkv7_mma.cuh", "wkv7_launch.h"),
+    "sha256": "ea577be540009499cb1e8859ae9c26f8a81b82bfb0464ae156da03d710eba032",
+    "bytes_per_token_head": (83.958272e6 + 26.309888e6 + 318.859008e6 + 165.179648e6) / 131072,
 }
 
 
@@ -370,9 +371,10 @@ def _report(args, wl, world, B, T, H, N, C, bf16, ms, fwd_ms, bwd_ms, e2e, ckpt,
         "fwd_ms": fwd_ms, "bwd_ms": bwd_ms, "step_roofline_frac": t_roof / (ms * 1e-3),
         "roofline": {"bound": "alu", "achieved": achieved / 1e12, "peak": peak_flops / 1e12, "unit": "TFLOP/s",
                      "frac": achieved / peak_flops, "traffic": measured_traffic(BTH), "kernel": TRAFFIC["kernel"],
-                     "note": "algorithmic FLOP of the recurrence (24 N^2 per token-head, backward) against the FP32 "
-                             "CUDA-core peak, the roofline the metric names; the kernel forms them as tf32 "
-                             "tensor-core products",
+                     "note": "the backward call (its two kernels, timed together with CUDA events around the "
+                             "call): algorithmic FLOP of the recurrence (24 N^2 per token-head) against the FP32 "
+                             "CUDA-core peak, the roofline the metric names; the kernels form them as tensor-core "
+                             "products (tf32 in the carry chain, bf16 in the output pass)",
                      "peak_source": f"{sms} SMs x {FP32_LANES_PER_SM} FP32 lanes x 2 x {peaks['sm_max_mhz']:.0f} MHz",
                      "hbm_gbs_achieved": b_bytes * BTH / (bwd_ms * 1e-3) / 1e9, "hbm_peak_gbs": peaks["hbm_gbs"]},
         "e2e": None if e2e is None else {

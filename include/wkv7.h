@@ -99,8 +99,17 @@ int wkv7_backward(const float* r, const float* w, const float* k, const float* v
                   int ckpt_every, float* dr, float* dw, float* dk, float* dv, float* da, float* db,
                   float* dS_init, int B, int T, int H, int N, void* stream);
 
-/* Backward with bfloat16 r, w, k, v, a, b and dy; checkpoints, s_init, every
- * gradient and the arithmetic are fp32. */
+/* Backward with bfloat16 r, w, k, v, a, b and dy; checkpoints, s_init and every
+ * gradient are fp32, as are the state, the carried gradient and every sum.
+ * At N = 64 with 16-step checkpoints the chunked tensor-core form runs: the
+ * carried gradient G at every chunk boundary is computed first (one sequential
+ * pass per (b, h)) and kept in a workspace of B*H*ceil(T/16)*N*N bf16 values,
+ * then every chunk's gradients are formed independently; the workspace is taken
+ * with cudaMallocAsync on `stream` and freed on it after the call (together with
+ * the checkpoint workspace when ckpt is NULL), so WKV7_ERR_ALLOC can also be
+ * returned when ckpt is given. Setting the environment variable
+ * WKV7_SPLIT_BACKWARD=0 selects a fused form instead (one pass per (b, h), no
+ * carry workspace). */
 int wkv7_backward_bf16(const wkv7_bf16* r, const wkv7_bf16* w, const wkv7_bf16* k, const wkv7_bf16* v,
                        const wkv7_bf16* a, const wkv7_bf16* b, const wkv7_bf16* dy, const float* s_init,
                        const float* ckpt, int ckpt_every, float* dr, float* dw, float* dk, float* dv,

@@ -109,6 +109,16 @@ def test_backward_workspace_allocation_failure_is_reported(lib, monkeypatch):
     assert "WKV7_FAIL_ALLOC" in lib.last_error()
 
 
+def test_chunked_backward_reports_carry_workspace_failure(lib, monkeypatch):
+    # bf16 inputs at N = 64 with 16-step checkpoints keep the carry of every chunk in a
+    # workspace even when the checkpoints are given
+    monkeypatch.setenv("WKV7_FAIL_ALLOC", "1")
+    monkeypatch.delenv("WKV7_SPLIT_BACKWARD", raising=False)
+    rc = lib.wkv7_backward_bf16(*_bwd_args(T=32, N=64, C=16))
+    assert rc == lib.ERR_ALLOC
+    assert "WKV7_FAIL_ALLOC" in lib.last_error()
+
+
 def test_empty_problems_need_no_device(lib):
     # B*H == 0: nothing to do, every buffer may be NULL.
     assert lib.wkv7_forward(*([None] * 10), 4, 0, 8, 3, 16, None) == lib.OK
