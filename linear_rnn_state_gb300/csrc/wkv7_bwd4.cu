@@ -238,7 +238,8 @@ struct CarrySmem {
   OpC op[3];
   ScratchC sc[2];
   float TT[kL * kLD16];  // T^T, T = (I - Mba)^-1
-  float Pc[4][kN];                                         // products of the decays of four-step blocks
+  float Pc[4][kN];
+  bf16_t gst[2][kN * 72];  // carries on their way out (state warps write, products warps store)                                         // products of the decays of four-step blocks
   uint64_t full[kCarryStages];
   int abort_flag;
 };
@@ -467,6 +468,16 @@ __device__ void carry_direct(float (&G)[8][4], const __nv_bfloat16* rs, int len,
   }
 }
 
+// A staged 64 x 64 bf16 carry (rows of 72) to global memory, 128 threads, whole rows per
+// instruction.
+__device__ __forceinline__ void flush_carry(const bf16_t* src, bf16_t* dst, int ptid) {
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    const int idx = ptid + 128 * q;  // row idx / 8, columns 8 (idx % 8) ..
+    *reinterpret_cast<uint4*>(dst + 8 * idx) = *reinterpret_cast<const uint4*>(src + (idx >> 3) * 72 + 8 * (idx & 7));
+  }
+}
+
 __global__ void __launch_bounds__(kCarryThreads, 1) wkv7_bwd4_carry_kernel(const __grid_constant__ BwdArgs args) {
   extern __shared__ __align__(128) unsigned char smem_raw[];
   CarrySmem& sm = *reinterpret_cast<CarrySmem*>(smem_raw);
@@ -532,13 +543,13 @@ __global__ void __launch_bounds__(kCarryThreads, 1) wkv7_bwd4_carry_kernel(const
     if (role == 0) {
       const OpC& op = sm.op[n % 3];
       // the carry entering this chunk (gradient w.r.t. the state after it), as the bf16
-      // operand the output kernel multiplies with
-      bf16_t* dst = carry_head + (size_t)n * kN * kN;
+      // operand the output kernel multiplies with; the products group stores it next round
+      bf16_t* dst = sm.gst[m & 1];
 #pragma unroll
       for (int nt = 0; nt < 8; ++nt) {
         const int col = 8 * nt + 2 * t4;
-        *reinterpret_cast<uint32_t*>(dst + (i0 + g) * kN + col) = pack_bf16(G[nt][0], G[nt][1]);
-        *reinterpret_cast<uint32_t*>(dst + (i0 + g + 8) * kN + col) = pack_bf16(G[nt][2], G[nt][3]);
+        *reinterpret_cast<uint32_t*>(dst + (i0 + g) * 72 + col) = pack_bf16(G[nt][0], G[nt][1]);
+        *reinterpret_cast<uint32_t*>(dst + (i0 + g + 8) * 72 + col) = pack_bf16(G[nt][2], G[nt][3]);
       }
       if (op.unsafe)
         carry_direct(G, sm.raw[st][0], len_of(m), i0, g, t4);
@@ -548,6 +559,7 @@ __global__ void __launch_bounds__(kCarryThreads, 1) wkv7_bwd4_carry_kernel(const
       if (m + 2 < nchunks) form(m + 2);
     } else {
       if (m + 1 < nchunks) products(m + 1);
+      if (m > 0) flush_carry(sm.gst[(m - 1) & 1], carry_head + (size_t)chunk_of(m - 1) * kN * kN, tid - 256);
     }
     // the stage of visit m is free (formed two visits ago, direct steps done); refill it
     if (__syncthreads_or(sm.abort_flag)) {
@@ -567,6 +579,7 @@ __global__ void __launch_bounds__(kCarryThreads, 1) wkv7_bwd4_carry_kernel(const
     __syncthreads();
     return;
   }
+  if (role == 2) flush_carry(sm.gst[(nchunks - 1) & 1], carry_head, tid - 256);  // chunk 0's
   if (role == 0 && args.dS_init) {
     float* dst = args.dS_init + (size_t)head * kN * kN;
 #pragma unroll

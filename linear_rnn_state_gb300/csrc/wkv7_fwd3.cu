@@ -56,6 +56,7 @@ struct Fwd3Smem {
   Prep3 prep[3];
   float X2[2][2 * kL * kLD64];  // per chunk in flight: rows 0..15: k~(s); rows 16..31: b~(s)   [s][j]
   __nv_bfloat16 ys[kL * kN];  // y of the chunk [t][i]
+  float ck[2][kN * kLD64];     // checkpoints on their way out (state warps write, products warps store)
   uint64_t full[4];
   int abort_flag;
 };
@@ -196,6 +197,25 @@ struct StateCtx {
   float S[8][4];  // rows i0+g, i0+g+8; columns 8*nt + 2*t4 + {0, 1}
   int i0, g, t4;
 };
+
+// The state into a staging tile (rows of kLD64 floats).
+__device__ __forceinline__ void stage_state(const StateCtx& c, float* dst) {
+#pragma unroll
+  for (int nt = 0; nt < 8; ++nt) {
+    const int col = 8 * nt + 2 * c.t4;
+    *reinterpret_cast<float2*>(dst + (c.i0 + c.g) * kLD64 + col) = make_float2(c.S[nt][0], c.S[nt][1]);
+    *reinterpret_cast<float2*>(dst + (c.i0 + c.g + 8) * kLD64 + col) = make_float2(c.S[nt][2], c.S[nt][3]);
+  }
+}
+
+// A staged 64 x 64 state to global memory (128 threads, whole rows per instruction).
+__device__ __forceinline__ void flush_state(const float* src, float* dst, int ptid) {
+#pragma unroll
+  for (int q = 0; q < 8; ++q) {
+    const int idx = ptid + 128 * q;  // row idx / 16, columns 4 (idx % 16) ..
+    *reinterpret_cast<float4*>(dst + 4 * idx) = *reinterpret_cast<const float4*>(src + (idx >> 4) * kLD64 + 4 * (idx & 15));
+  }
+}
 
 __device__ __forceinline__ void store_state(const StateCtx& c, float* dst) {
 #pragma unroll
@@ -430,10 +450,13 @@ __global__ void __launch_bounds__(kThreads, 1) wkv7_fwd3_kernel(const __grid_con
       if (n + 2 < nchunks) form(n + 2);
     } else if (role == 2) {
       if (n + 1 < nchunks) grams(n + 1);
+      // the checkpoint the state warps staged in the previous round
+      if (ck_head && n > 0 && ((n - 1) * kL) % args.C == 0)
+        flush_state(sm.ck[(n - 1) & 1], ck_head + (size_t)((n - 1) * kL / args.C) * kN * kN, gtid);
     } else {
       const Prep3& P = sm.prep[n % 3];
       const int t0 = n * kL, len = chunk_len(n);
-      if (ck_head && t0 % args.C == 0) store_state(c, ck_head + (size_t)(t0 / args.C) * kN * kN);
+      if (ck_head && t0 % args.C == 0) stage_state(c, sm.ck[n & 1]);
       if (P.unsafe)
         state_chunk_direct(c, sm, n % kStages, len);
       else
@@ -462,6 +485,9 @@ __global__ void __launch_bounds__(kThreads, 1) wkv7_fwd3_kernel(const __grid_con
     __syncthreads();
     return;
   }
+  // the last staged checkpoint
+  if (role == 2 && ck_head && nchunks > 0 && ((nchunks - 1) * kL) % args.C == 0)
+    flush_state(sm.ck[(nchunks - 1) & 1], ck_head + (size_t)((nchunks - 1) * kL / args.C) * kN * kN, gtid);
   if (role == 0 && args.s_final) store_state(c, args.s_final + (size_t)head * kN * kN);
 }
 
