@@ -1126,26 +1126,21 @@ __global__ void __launch_bounds__(kThreads, 3) wkv7_bwd4_out_kernel(const __grid
     }
   }
   __syncthreads();
-  // w dw from the identity, one thread per column, anchored where fewer terms are summed:
+  // w dw from the identity, anchored where fewer terms are summed, thread (column, half):
   //   t < 8:  colsum(carry at the chunk start o S0) - sum_{u<t} x(u) - a(t) da(t)
   //   t >= 8: sum_{u>=t} x(u) - a(t) da(t) + colsum(carry at the chunk end o S(L))
-  if (tid < kN) {
-    const int col = tid;
+  if (tid < 2 * kN) {
+    const int col = tid & 63, upper = tid >> 6;
     const float cge = sm.cLs[col] * (sm.Epart[0][col] + sm.Epart[1][col] + sm.Epart[2][col] + sm.Epart[3][col]);
-    float run = cge + sm.anc[0][col];  // start anchor, minus the x of the steps before t
+    float run = cge + sm.anc[upper][col];
 #pragma unroll
-    for (int t = 0; t < kL / 2; ++t) {
+    for (int e = 0; e < kL / 2; ++e) {
+      const int t = upper ? kL - 1 - e : e;
       const float x = XK[t * kLD64 + col] + XR[t * kLD64 + col];
+      if (upper) run += x;  // end anchor plus the x of the steps from t on
       const float v = (run - XA[t * kLD64 + col]) * rcp_approx(bf(rs + V_W * RS + t * kB64 + col));
       if (t < len) args.dw[base + (size_t)t * vstep + col] = v;
-      run -= x;
-    }
-    run = cge + sm.anc[1][col];  // end anchor, plus the x of the steps from t on
-#pragma unroll
-    for (int t = kL - 1; t >= kL / 2; --t) {
-      run += XK[t * kLD64 + col] + XR[t * kLD64 + col];
-      const float v = (run - XA[t * kLD64 + col]) * rcp_approx(bf(rs + V_W * RS + t * kB64 + col));
-      if (t < len) args.dw[base + (size_t)t * vstep + col] = v;
+      if (!upper) run -= x;  // start anchor minus the x of the steps before t
     }
   }
 }

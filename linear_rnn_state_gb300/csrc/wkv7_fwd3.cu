@@ -55,7 +55,7 @@ struct Fwd3Smem {
   __nv_bfloat16 raw[4][6][kL * kN];  // TMA ring: r, w, k, v, a, b of one chunk per stage
   Prep3 prep[3];
   float X2[2][2 * kL * kLD64];  // per chunk in flight: rows 0..15: k~(s); rows 16..31: b~(s)   [s][j]
-  __nv_bfloat16 ys[kL * kN];  // y of the chunk [t][i]
+  __nv_bfloat16 ys[2][kL * kN];  // y of the chunk [t][i], on its way out (state warps write, products warps store)
   float ck[2][kN * kLD64];     // checkpoints on their way out (state warps write, products warps store)
   uint64_t full[4];
   int abort_flag;
@@ -196,6 +196,7 @@ __device__ void gram_chunk(Prep3& P, const float* X2, int gtid) {
 struct StateCtx {
   float S[8][4];  // rows i0+g, i0+g+8; columns 8*nt + 2*t4 + {0, 1}
   int i0, g, t4;
+  int yb;  // which y staging buffer this round writes
 };
 
 // The state into a staging tile (rows of kLD64 floats).
@@ -215,6 +216,15 @@ __device__ __forceinline__ void flush_state(const float* src, float* dst, int pt
     const int idx = ptid + 128 * q;  // row idx / 16, columns 4 (idx % 16) ..
     *reinterpret_cast<float4*>(dst + 4 * idx) = *reinterpret_cast<const float4*>(src + (idx >> 4) * kLD64 + 4 * (idx & 15));
   }
+}
+
+// A chunk's staged y rows ([t][i] bf16) to global memory: 128 threads, 16 rows x 8 pieces of
+// 16 bytes, rows past the end of the sequence skipped.
+__device__ __forceinline__ void flush_y(const __nv_bfloat16* src, __nv_bfloat16* dst, size_t vstep, int len, int ptid) {
+  const int row = ptid >> 3, piece = ptid & 7;
+  if (row < len)
+    *reinterpret_cast<uint4*>(dst + (size_t)row * vstep + 8 * piece) =
+        *reinterpret_cast<const uint4*>(src + row * kN + 8 * piece);
 }
 
 __device__ __forceinline__ void store_state(const StateCtx& c, float* dst) {
@@ -294,8 +304,8 @@ __device__ void state_chunk(StateCtx& c, Fwd3Smem& sm, const Prep3& P) {
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
       const int i = i0 + g + 8 * h, t = 8 * q + 2 * t4;
-      sm.ys[t * kN + i] = __float2bfloat16_rn(PR[q][2 * h]);
-      sm.ys[(t + 1) * kN + i] = __float2bfloat16_rn(PR[q][2 * h + 1]);
+      sm.ys[c.yb][t * kN + i] = __float2bfloat16_rn(PR[q][2 * h]);
+      sm.ys[c.yb][(t + 1) * kN + i] = __float2bfloat16_rn(PR[q][2 * h + 1]);
     }
   // S(L) = S0 diag(c(L)) + V^T Kb + SA^T Bb
 #pragma unroll
@@ -354,8 +364,8 @@ __device__ void state_chunk_direct(StateCtx& c, Fwd3Smem& sm, int stage, int len
     y1 += __shfl_xor_sync(0xffffffffu, y1, 1);
     y1 += __shfl_xor_sync(0xffffffffu, y1, 2);
     if (t4 == 0) {
-      sm.ys[t * kN + i0 + g] = __float2bfloat16_rn(y0);
-      sm.ys[t * kN + i0 + g + 8] = __float2bfloat16_rn(y1);
+      sm.ys[c.yb][t * kN + i0 + g] = __float2bfloat16_rn(y0);
+      sm.ys[c.yb][t * kN + i0 + g + 8] = __float2bfloat16_rn(y1);
     }
   }
 }
@@ -450,24 +460,21 @@ __global__ void __launch_bounds__(kThreads, 1) wkv7_fwd3_kernel(const __grid_con
       if (n + 2 < nchunks) form(n + 2);
     } else if (role == 2) {
       if (n + 1 < nchunks) grams(n + 1);
-      // the checkpoint the state warps staged in the previous round
-      if (ck_head && n > 0 && ((n - 1) * kL) % args.C == 0)
-        flush_state(sm.ck[(n - 1) & 1], ck_head + (size_t)((n - 1) * kL / args.C) * kN * kN, gtid);
+      // the checkpoint and the y rows the state warps staged in the previous round
+      if (n > 0) {
+        if (ck_head && ((n - 1) * kL) % args.C == 0)
+          flush_state(sm.ck[(n - 1) & 1], ck_head + (size_t)((n - 1) * kL / args.C) * kN * kN, gtid);
+        if (y) flush_y(sm.ys[(n - 1) & 1], y + vbase + (size_t)(n - 1) * kL * vstep, vstep, chunk_len(n - 1), gtid);
+      }
     } else {
       const Prep3& P = sm.prep[n % 3];
       const int t0 = n * kL, len = chunk_len(n);
       if (ck_head && t0 % args.C == 0) stage_state(c, sm.ck[n & 1]);
+      c.yb = n & 1;
       if (P.unsafe)
         state_chunk_direct(c, sm, n % kStages, len);
       else
         state_chunk(c, sm, P);
-      named_bar(2, 128);
-      if (y) {
-        const int row = tid >> 3, piece = tid & 7;  // 16 rows x 8 pieces of 16 bytes
-        if (row < len)
-          *reinterpret_cast<uint4*>(y + vbase + (size_t)(t0 + row) * vstep + 8 * piece) =
-              *reinterpret_cast<const uint4*>(sm.ys + row * kN + 8 * piece);
-      }
     }
     // the stage of chunk n is free (formed two rounds ago, direct steps done); refill it
     aborted = __syncthreads_or(sm.abort_flag) != 0;
@@ -485,9 +492,12 @@ __global__ void __launch_bounds__(kThreads, 1) wkv7_fwd3_kernel(const __grid_con
     __syncthreads();
     return;
   }
-  // the last staged checkpoint
-  if (role == 2 && ck_head && nchunks > 0 && ((nchunks - 1) * kL) % args.C == 0)
-    flush_state(sm.ck[(nchunks - 1) & 1], ck_head + (size_t)((nchunks - 1) * kL / args.C) * kN * kN, gtid);
+  // the last staged checkpoint and y rows
+  if (role == 2 && nchunks > 0) {
+    const int n = nchunks - 1;
+    if (ck_head && (n * kL) % args.C == 0) flush_state(sm.ck[n & 1], ck_head + (size_t)(n * kL / args.C) * kN * kN, gtid);
+    if (y) flush_y(sm.ys[n & 1], y + vbase + (size_t)n * kL * vstep, vstep, chunk_len(n), gtid);
+  }
   if (role == 0 && args.s_final) store_state(c, args.s_final + (size_t)head * kN * kN);
 }
 
