@@ -296,6 +296,28 @@ __device__ bool form_carry(ScratchC& sc, float (&Pc)[4][kN], const __nv_bfloat16
   return false;
 }
 
+// n-tile nt of P Q^T (16 x 16, K = 64, tf32 values, stride kLD64) stored to M
+// (stride kLD16) as tf32, masked to s < t (strict) or s <= t.
+__device__ __forceinline__ void gram_tile(float* M, const float* P, const float* Q, int nt, bool strict, int lane) {
+  const int g = lane >> 2, t4 = lane & 3;
+  float acc[4];
+  zero4(acc);
+#pragma unroll
+  for (int kb = 0; kb < kN / 8; ++kb) {
+    uint32_t a[4], b0, b1;
+    frag_a(a, P, kLD64, 0, 8 * kb, g, t4);
+    frag_b(b0, b1, Q, kLD64, 8 * nt, 8 * kb, g, t4);
+    mma_tf32(acc, a, b0, b1);
+  }
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    const int t = g + 8 * h, s = 8 * nt + 2 * t4;
+    const bool k0 = strict ? s < t : s <= t, k1 = strict ? s + 1 < t : s + 1 <= t;
+    *reinterpret_cast<float2*>(M + t * kLD16 + s) =
+        make_float2(k0 ? tf32r(acc[2 * h]) : 0.f, k1 ? tf32r(acc[2 * h + 1]) : 0.f);
+  }
+}
+
 // Forming group: wait for a chunk's inputs and form its operands. Returns
 // false on a timeout.
 __device__ bool front_form(CarrySmem& sm, ScratchC& sc, OpC& op, const __nv_bfloat16* rs, uint64_t* bar,
@@ -310,34 +332,18 @@ __device__ bool front_form(CarrySmem& sm, ScratchC& sc, OpC& op, const __nv_bflo
   if (ftid == 0) op.unsafe = unsafe;
   if (unsafe) return true;
   named_bar(1, 128);
-  // n-tile (pf % 2) of Mbr = R^ B~^T (pf < 2) or Mba = A^ B~^T (pf >= 2)
-  const int pf = ftid >> 5, lane = ftid & 31, g = lane >> 2, t4 = lane & 3, nt = pf & 1;
-  const bool is_ba = pf >= 2;
-  const float* P = is_ba ? sc.Ah : op.Rh;
-  float acc[4];
-  zero4(acc);
-#pragma unroll
-  for (int kb = 0; kb < kN / 8; ++kb) {
-    uint32_t a[4], b0, b1;
-    frag_a(a, P, kLD64, 0, 8 * kb, g, t4);
-    frag_b(b0, b1, sc.Bt, kLD64, 8 * nt, 8 * kb, g, t4);
-    mma_tf32(acc, a, b0, b1);
-  }
-  float* M = is_ba ? sc.Mba : sc.Mbr;
-#pragma unroll
-  for (int h = 0; h < 2; ++h) {
-    const int t = g + 8 * h, s = 8 * nt + 2 * t4;
-    const bool k0 = is_ba ? s < t : s <= t, k1 = is_ba ? s + 1 < t : s + 1 <= t;
-    *reinterpret_cast<float2*>(M + t * kLD16 + s) =
-        make_float2(k0 ? tf32r(acc[2 * h]) : 0.f, k1 ? tf32r(acc[2 * h + 1]) : 0.f);
-  }
+  // n-tile pf - 2 of Mba = A^ B~^T (warps 2, 3); the products group makes Mbr
+  const int pf = ftid >> 5;
+  if (pf >= 2) gram_tile(sc.Mba, sc.Ah, sc.Bt, pf - 2, true, ftid & 31);
   return true;
 }
 
-// Products group (128 threads): T, T^T Bb and Mbr T of a formed chunk.
-__device__ void front_products(CarrySmem& sm, const ScratchC& sc, OpC& op) {
+// Products group (128 threads): T, Mbr = R^ B~^T (with diagonal), T^T Bb and Mbr T of a
+// formed chunk.
+__device__ void front_products(CarrySmem& sm, ScratchC& sc, OpC& op) {
   const int pp = (threadIdx.x >> 5) - 8, lane = threadIdx.x & 31, g = lane >> 2, t4 = lane & 3;
   if (pp == 0) unit_lower_inverse(sc.Mba, nullptr, sm.TT, lane);
+  else if (pp <= 2) gram_tile(sc.Mbr, op.Rh, sc.Bt, pp - 1, false, lane);
   named_bar(2, 128);
   {  // T^T Bb, n-tiles 2 pp and 2 pp + 1
     float acc[2][4];
@@ -515,7 +521,10 @@ __global__ void __launch_bounds__(kCarryThreads, 1) wkv7_bwd4_carry_kernel(const
     const int c = chunk_of(v);
     if (!sm.op[c % 3].unsafe) front_products(sm, sm.sc[c & 1], sm.op[c % 3]);
   };
-  if (tid == 128) {
+  // TMA copies are issued by a products-group thread (that group has the most slack); the
+  // forming group waits for them
+  constexpr int kIssuer = 352;
+  if (tid == kIssuer) {
     for (int s = 0; s < kCarryStages; ++s) mbar_init(&sm.full[s], 1);
     fence_mbar_init();
     for (int q = 0; q < 7; ++q) prefetch_tensormap(&args.map[q]);
@@ -566,7 +575,7 @@ __global__ void __launch_bounds__(kCarryThreads, 1) wkv7_bwd4_carry_kernel(const
       aborted = true;
       break;
     }
-    if (tid == 128 && m + kCarryStages < nchunks) {
+    if (tid == kIssuer && m + kCarryStages < nchunks) {
       fence_proxy_async_smem();
       issue(m + kCarryStages);
     }

@@ -389,7 +389,9 @@ __global__ void __launch_bounds__(kThreads, 1) wkv7_fwd3_kernel(const __grid_con
     mbar_arrive_expect_tx(&sm.full[st], kStageBytes);
     for (int v = 0; v < 6; ++v) tma_load_4d(sm.raw[st][v], &args.map[v], &sm.full[st], 0, hi, chunk * kL, bi);
   };
-  if (tid == 128) {
+  // TMA copies are issued by the forming group's first thread
+  constexpr int kIssuer = 128;
+  if (tid == kIssuer) {
     for (int s = 0; s < kStages; ++s) mbar_init(&sm.full[s], 1);
     fence_mbar_init();
     for (int v = 0; v < 6; ++v) prefetch_tensormap(&args.map[v]);
@@ -426,7 +428,7 @@ __global__ void __launch_bounds__(kThreads, 1) wkv7_fwd3_kernel(const __grid_con
   // outcome, so its named barriers stay matched; a timeout raises the CTA's
   // abort flag.
   int waited = 0;  // chunks whose stage has landed (forming group)
-  int issued = min(kStages, nchunks);  // chunks whose copy was started (thread 128)
+  int issued = min(kStages, nchunks);  // chunks whose copy was started (every thread keeps count)
   auto chunk_len = [&](int chunk) { return min(kL, T - chunk * kL); };
   auto form = [&](int chunk) {
     const bool ok = mbar_wait_bounded(args.status, &sm.full[chunk % kStages], (chunk / kStages) & 1);
@@ -478,11 +480,11 @@ __global__ void __launch_bounds__(kThreads, 1) wkv7_fwd3_kernel(const __grid_con
     }
     // the stage of chunk n is free (formed two rounds ago, direct steps done); refill it
     aborted = __syncthreads_or(sm.abort_flag) != 0;
-    if (!aborted && tid == 128 && n + kStages < nchunks) {
+    if (!aborted && tid == kIssuer && n + kStages < nchunks) {
       fence_proxy_async_smem();
       issue(n + kStages);
-      issued = n + kStages + 1;
     }
+    if (!aborted) issued = min(n + 1 + kStages, nchunks);
   }
   if (aborted) {
     // let the copies still in flight land before the CTA's shared memory is released
