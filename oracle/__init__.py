@@ -52,7 +52,7 @@ class Oracle:
             fwd.argtypes = [p] * 9 + [i] * 5
             fwd.restype = i
             bwd = getattr(lib, f"oracle_wkv7_backward_{suffix}")
-            bwd.argtypes = [p] * 15 + [i] * 5
+            bwd.argtypes = [p] * 16 + [i] * 5
             bwd.restype = i
         self.lib = lib
 
@@ -72,17 +72,20 @@ class Oracle:
             raise RuntimeError(f"oracle forward failed with status {rc}")
         return y, s_final
 
-    def backward(self, r, w, k, v, a, b, dy, s_init=None, *, nthreads: int = 0, dtype=np.float64):
+    def backward(self, r, w, k, v, a, b, dy, s_init=None, dS_final=None, *, nthreads: int = 0,
+                 dtype=np.float64):
         """Backward-through-time. Returns dict dr, dw, dk, dv, da, db ([B][T][H][N])
-        and dS_init ([B][H][N][N]) in ``dtype``. No gradient enters through s_final.
+        and dS_init ([B][H][N][N]) in ``dtype``. dS_final ([B][H][N][N]) is the
+        gradient entering through s_final; None means none (zeros).
         """
         r, w, k, v, a, b, dy = (_prep(x, dtype) for x in (r, w, k, v, a, b, dy))
         s_init = _prep(s_init, dtype)
+        dS_final = _prep(dS_final, dtype)
         B, T, H, N = r.shape
         out = {n: np.empty_like(r) for n in ("dr", "dw", "dk", "dv", "da", "db")}
         out["dS_init"] = np.empty((B, H, N, N), dtype=dtype)
         fn = self.lib.oracle_wkv7_backward_f64 if dtype == np.float64 else self.lib.oracle_wkv7_backward_f32
-        args = [_ptr(x, dtype) for x in (r, w, k, v, a, b, dy, s_init)]
+        args = [_ptr(x, dtype) for x in (r, w, k, v, a, b, dy, s_init, dS_final)]
         args += [_ptr(out[n], dtype) for n in ("dr", "dw", "dk", "dv", "da", "db", "dS_init")]
         rc = fn(*args, B, T, H, N, nthreads)
         if rc != 0:

@@ -16,8 +16,12 @@
 //     S_ij <- S_ij w_j + v_i k_j + sa_i b_j
 //     y_i  = sum_j S_ij r_j                       (post-update state)
 //
-//   backward, G = dL/dS starts at zero (no gradient flows into s_final),
-//   t = T-1 .. 0, with S_prev the state before step t and S_t after it:
+//   backward, G = dL/dS starts at the gradient of the final state: zero in
+//   the C file (no loss term reads s_final), or a given dS_final when the
+//   sequence is one segment of a longer one (the Mamba-3 page's
+//   "serial_recalculated/backward.rs" takes that final-state gradient as an
+//   input in the same way); t = T-1 .. 0, with S_prev the state before step t
+//   and S_t after it:
 //     (1) dr_j = sum_i S_t_ij dy_i ;  G_ij += dy_i r_j
 //     (2) dk_j = sum_i G_ij v_i ;  db_j = sum_i G_ij sa_i ;
 //         dw_j = sum_i G_ij S_prev_ij   (w is the effective decay itself)
@@ -101,7 +105,7 @@ template <typename F>
 struct HeadGrads { F* dr; F* dw; F* dk; F* dv; F* da; F* db; };
 
 template <typename F>
-void backward_head(const HeadView<F>& hv, const F* s_init, const HeadGrads<F>& g,
+void backward_head(const HeadView<F>& hv, const F* s_init, const F* dS_final, const HeadGrads<F>& g,
                    F* dS_init, int T, int N) {
   const std::size_t NN = static_cast<std::size_t>(N) * N;
   // states[t] = state before step t (t = 0..T-1); states[T] = final state.
@@ -119,6 +123,7 @@ void backward_head(const HeadView<F>& hv, const F* s_init, const HeadGrads<F>& g
   }
 
   std::vector<F> G(NN, F(0)), dsa(N);
+  if (dS_final) std::memcpy(G.data(), dS_final, NN * sizeof(F));
   for (int t = T - 1; t >= 0; --t) {
     const std::size_t o = t * hv.stride;
     const F* r = hv.r + o; const F* w = hv.w + o; const F* k = hv.k + o;
@@ -217,8 +222,8 @@ int forward_all(const F* r, const F* w, const F* k, const F* v, const F* a, cons
 
 template <typename F>
 int backward_all(const F* r, const F* w, const F* k, const F* v, const F* a, const F* b,
-                 const F* dy, const F* s_init, F* dr, F* dw, F* dk, F* dv, F* da, F* db,
-                 F* dS_init, int B, int T, int H, int N, int nthreads) {
+                 const F* dy, const F* s_init, const F* dS_final, F* dr, F* dw, F* dk, F* dv,
+                 F* da, F* db, F* dS_init, int B, int T, int H, int N, int nthreads) {
   if (!r || !w || !k || !v || !a || !b || !dy) return -2;
   if (!dr || !dw || !dk || !dv || !da || !db) return -2;
   if (B <= 0 || T <= 0 || H <= 0 || N <= 0) return -2;
@@ -228,7 +233,7 @@ int backward_all(const F* r, const F* w, const F* k, const F* v, const F* a, con
     HeadView<F> hv = head_view<F>(r, w, k, v, a, b, dy, bi, hi, T, H, N);
     const std::size_t off = (static_cast<std::size_t>(bi) * T * H + hi) * N;
     HeadGrads<F> g{dr + off, dw + off, dk + off, dv + off, da + off, db + off};
-    backward_head(hv, s_init ? s_init + hd * NN : nullptr, g,
+    backward_head(hv, s_init ? s_init + hd * NN : nullptr, dS_final ? dS_final + hd * NN : nullptr, g,
                   dS_init ? dS_init + hd * NN : nullptr, T, N);
   });
 }
@@ -237,8 +242,9 @@ int backward_all(const F* r, const F* w, const F* k, const F* v, const F* a, con
 
 extern "C" {
 
-// All pointers are host memory. s_init may be NULL (zero initial state);
-// y, s_final and dS_init may be NULL (not written). Returns 0, -1 when a
+// All pointers are host memory. s_init may be NULL (zero initial state),
+// dS_final may be NULL (no gradient into the final state); y, s_final and
+// dS_init may be NULL (not written). Returns 0, -1 when a
 // cache cannot be allocated, -2 on an invalid argument. nthreads <= 0 uses
 // every hardware thread.
 int oracle_wkv7_forward_f64(const double* r, const double* w, const double* k,
@@ -250,10 +256,11 @@ int oracle_wkv7_forward_f64(const double* r, const double* w, const double* k,
 
 int oracle_wkv7_backward_f64(const double* r, const double* w, const double* k,
                              const double* v, const double* a, const double* b,
-                             const double* dy, const double* s_init, double* dr, double* dw,
-                             double* dk, double* dv, double* da, double* db,
-                             double* dS_init, int B, int T, int H, int N, int nthreads) {
-  return backward_all(r, w, k, v, a, b, dy, s_init, dr, dw, dk, dv, da, db, dS_init,
+                             const double* dy, const double* s_init, const double* dS_final,
+                             double* dr, double* dw, double* dk, double* dv, double* da,
+                             double* db, double* dS_init, int B, int T, int H, int N,
+                             int nthreads) {
+  return backward_all(r, w, k, v, a, b, dy, s_init, dS_final, dr, dw, dk, dv, da, db, dS_init,
                       B, T, H, N, nthreads);
 }
 
@@ -265,10 +272,10 @@ int oracle_wkv7_forward_f32(const float* r, const float* w, const float* k, cons
 
 int oracle_wkv7_backward_f32(const float* r, const float* w, const float* k, const float* v,
                              const float* a, const float* b, const float* dy,
-                             const float* s_init, float* dr, float* dw, float* dk, float* dv,
-                             float* da, float* db, float* dS_init, int B, int T, int H, int N,
-                             int nthreads) {
-  return backward_all(r, w, k, v, a, b, dy, s_init, dr, dw, dk, dv, da, db, dS_init,
+                             const float* s_init, const float* dS_final, float* dr, float* dw,
+                             float* dk, float* dv, float* da, float* db, float* dS_init, int B,
+                             int T, int H, int N, int nthreads) {
+  return backward_all(r, w, k, v, a, b, dy, s_init, dS_final, dr, dw, dk, dv, da, db, dS_init,
                       B, T, H, N, nthreads);
 }
 

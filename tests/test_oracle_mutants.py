@@ -46,6 +46,10 @@ MUTANTS = {
     "dS_init_not_written": (
         "if (dS_init) std::memcpy(dS_init, G.data(), NN * sizeof(F));",
         "if (dS_init) std::memset(dS_init, 0, NN * sizeof(F));"),
+    "dS_final_ignored": ("if (dS_final) std::memcpy(G.data(), dS_final, NN * sizeof(F));", ""),
+    "dS_final_transposed": (
+        "if (dS_final) std::memcpy(G.data(), dS_final, NN * sizeof(F));",
+        "if (dS_final) for (int i = 0; i < N; ++i) for (int j = 0; j < N; ++j) G[i * N + j] = dS_final[j * N + i];"),
 }
 
 # Cheapest first; the run stops at the first pin that fails.
@@ -58,6 +62,8 @@ PIN_TESTS = [
     pins.test_structure_causality_linearity_zero_b,
     pins.test_row_permutation_equivariance,
     pins.test_finite_differences_sampled_tiny_workload,
+    pins.test_final_state_gradient_euler_identity,
+    pins.test_final_state_gradient_finite_differences,
     pins.test_exact_rational_forward_and_gradients,
 ]
 

@@ -286,3 +286,67 @@ def test_backward_heads_matches_whole_run(oracle_mod, gen_mod):
         for n in GRAD_OF.values():
             np.testing.assert_array_equal(gh[n][p], g[n][bi, :, hi])
         np.testing.assert_array_equal(gh["dS_init"][p], g["dS_init"][bi, hi])
+
+
+# ------------------------------------- gradient entering through s_final ----
+# A sequence cut into segments: the gradient of the loss w.r.t. a segment's
+# final state (dS_final) is the next segment's dS_init. Pinned by finite
+# differences of L = <dy, y> + <dS_final, s_final>, by composing two segments
+# and by Euler's identity for (v, s_init).
+
+def _loss_final(oracle, ins, s_init, dy, dsf):
+    y, sf = oracle.forward(*ins, s_init)
+    return float(np.sum(dy * y) + np.sum(dsf * sf))
+
+
+def test_final_state_gradient_finite_differences(oracle_mod, gen_mod):
+    ins, dy, s0 = _inputs(gen_mod, 1, 5, 2, 3, seed=21, s_init_std=0.6)
+    dsf = np.random.default_rng(21).standard_normal(s0.shape)
+    g = oracle_mod.backward(*ins, dy, s0, dsf)
+    h = 1e-5
+    coords = [(n, idx) for n in ORDER for idx in np.ndindex(ins[0].shape)]
+    coords += [("s_init", idx) for idx in np.ndindex(s0.shape)]
+    for name, idx in coords:
+        if name == "s_init":
+            base, gval = s0, g["dS_init"][idx]
+        else:
+            base, gval = ins[ORDER.index(name)], g[GRAD_OF[name]][idx]
+        old = base[idx]
+        base[idx] = old + h
+        lp = _loss_final(oracle_mod, ins, s0, dy, dsf)
+        base[idx] = old - h
+        lm = _loss_final(oracle_mod, ins, s0, dy, dsf)
+        base[idx] = old
+        fd = (lp - lm) / (2 * h)
+        assert abs(fd - gval) <= 1e-7 * max(1.0, abs(gval)), (name, idx, fd, gval)
+
+
+def test_final_state_gradient_composes_segments(oracle_mod, gen_mod):
+    """Backward over [0, T) with dS_final equals the backward of [T1, T) with
+    dS_final followed by the backward of [0, T1) with the first one's dS_init
+    as its dS_final (each segment starting from the state the forward reached)."""
+    ins, dy, s0 = _inputs(gen_mod, 2, 23, 2, 5, seed=22, s_init_std=0.4)
+    dsf = np.random.default_rng(22).standard_normal(s0.shape)
+    full = oracle_mod.backward(*ins, dy, s0, dsf)
+    T1 = 9
+    first = [x[:, :T1].copy() for x in ins]
+    second = [x[:, T1:].copy() for x in ins]
+    _, s_mid = oracle_mod.forward(*first, s0)
+    g2 = oracle_mod.backward(*second, dy[:, T1:].copy(), s_mid, dsf)
+    g1 = oracle_mod.backward(*first, dy[:, :T1].copy(), s0, g2["dS_init"])
+    for n in GRAD_OF.values():
+        np.testing.assert_allclose(np.concatenate([g1[n], g2[n]], axis=1), full[n], rtol=1e-12, atol=1e-13)
+    np.testing.assert_allclose(g1["dS_init"], full["dS_init"], rtol=1e-12, atol=1e-13)
+
+
+def test_final_state_gradient_euler_identity(oracle_mod, gen_mod):
+    """y and s_final are jointly linear in (v, s_init), so
+    sum <dv, v> + <dS_init, s_init> = <dy, y> + <dS_final, s_final>; with dy = 0
+    nothing flows into r."""
+    ins, dy, s0 = _inputs(gen_mod, 2, 12, 3, 6, seed=23, s_init_std=0.5)
+    dsf = np.random.default_rng(23).standard_normal(s0.shape)
+    g = oracle_mod.backward(*ins, dy, s0, dsf)
+    lhs = np.sum(g["dv"] * ins[3]) + np.sum(g["dS_init"] * s0)
+    assert lhs == pytest.approx(_loss_final(oracle_mod, ins, s0, dy, dsf), rel=1e-12)
+    g0 = oracle_mod.backward(*ins, np.zeros_like(dy), s0, dsf)
+    assert np.all(g0["dr"] == 0.0)
