@@ -115,6 +115,31 @@ int wkv7_backward_bf16(const wkv7_bf16* r, const wkv7_bf16* w, const wkv7_bf16* 
                        const float* ckpt, int ckpt_every, float* dr, float* dw, float* dk, float* dv,
                        float* da, float* db, float* dS_init, int B, int T, int H, int N, void* stream);
 
+/*
+ * Backward of one segment of a longer sequence: as wkv7_backward (and
+ * wkv7_backward_bf16), with the gradient of the loss w.r.t. the segment's
+ * final state entering the reverse scan (the scan of "rx_pretrain.c" starts
+ * its carry at zero; the Mamba-3 page's "serial_recalculated/backward.rs"
+ * takes this final-state gradient as an input). Cutting a sequence at T1, the
+ * segment [T1, T) is run first with the whole sequence's dS_final and
+ * s_init = the state the forward reached at T1; its dS_init is then the
+ * dS_final of the segment [0, T1).
+ *   dS_final   [B][H][N][N] fp32 gradient entering through the final state, or
+ *              NULL for zeros (then identical to wkv7_backward). An input: it
+ *              must not overlap an output.
+ * With T = 0, dS_init = dS_final. Other arguments, layouts, workspaces and
+ * status codes as wkv7_backward / wkv7_backward_bf16.
+ */
+int wkv7_backward_segment(const float* r, const float* w, const float* k, const float* v, const float* a,
+                          const float* b, const float* dy, const float* s_init, const float* dS_final,
+                          const float* ckpt, int ckpt_every, float* dr, float* dw, float* dk, float* dv,
+                          float* da, float* db, float* dS_init, int B, int T, int H, int N, void* stream);
+int wkv7_backward_segment_bf16(const wkv7_bf16* r, const wkv7_bf16* w, const wkv7_bf16* k, const wkv7_bf16* v,
+                               const wkv7_bf16* a, const wkv7_bf16* b, const wkv7_bf16* dy, const float* s_init,
+                               const float* dS_final, const float* ckpt, int ckpt_every, float* dr, float* dw,
+                               float* dk, float* dv, float* da, float* db, float* dS_init, int B, int T, int H,
+                               int N, void* stream);
+
 /* Bytes of the checkpoint buffer: B*H*ceil(T/ckpt_every)*N*N*4, or 0 for an
  * invalid size. */
 size_t wkv7_ckpt_bytes(int B, int T, int H, int N, int ckpt_every);

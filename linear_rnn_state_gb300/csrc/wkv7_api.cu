@@ -204,8 +204,8 @@ int forward_impl(bool bf16, const void* const in[6], const float* s_init, void* 
 
 // ----------------------------------------------------------- backward ---
 
-int backward_impl(bool bf16, const void* const in[7], const float* s_init, const float* ckpt, int C,
-                  float* const grads[6], float* dS_init, int B, int T, int H, int N, cudaStream_t stream) {
+int backward_impl(bool bf16, const void* const in[7], const float* s_init, const float* dS_final, const float* ckpt,
+                  int C, float* const grads[6], float* dS_init, int B, int T, int H, int N, cudaStream_t stream) {
   int rc = check_dims(B, T, H, N);
   if (rc) return rc;
   if (ckpt && C < 1) return fail(WKV7_ERR_INVALID, "ckpt_every must be >= 1 (got %d)", C);
@@ -214,22 +214,25 @@ int backward_impl(bool bf16, const void* const in[7], const float* s_init, const
   const size_t vec = (size_t)B * T * H * N * es;
   const size_t gvec = (size_t)B * T * H * N * 4;
   const size_t st = (size_t)B * H * N * N * 4;
-  const Span ins[9] = {{in[0], vec, "r"},  {in[1], vec, "w"},     {in[2], vec, "k"},
+  const Span ins[10] = {{in[0], vec, "r"},  {in[1], vec, "w"},     {in[2], vec, "k"},
                        {in[3], vec, "v"},  {in[4], vec, "a"},     {in[5], vec, "b"},
-                       {in[6], vec, "dy"}, {s_init, st, "s_init"}, {ckpt, ckpt ? ckpt_bytes(B, T, H, N, C) : 0, "ckpt"}};
+                       {in[6], vec, "dy"}, {s_init, st, "s_init"}, {ckpt, ckpt ? ckpt_bytes(B, T, H, N, C) : 0, "ckpt"},
+                       {dS_final, st, "dS_final"}};
   const Span outs[7] = {{grads[0], gvec, "dr"}, {grads[1], gvec, "dw"}, {grads[2], gvec, "dk"},
                         {grads[3], gvec, "dv"}, {grads[4], gvec, "da"}, {grads[5], gvec, "db"},
                         {dS_init, st, "dS_init"}};
   // Empty problems: no step runs, so the carried gradient stays zero.
   if ((size_t)B * H == 0) return WKV7_OK;
-  if (T == 0) {
-    rc = check_spans(ins + 7, 1, outs + 6, 1, 0, 0);
+  if (T == 0) {  // no step: the gradient of the initial state is the one entering the final state
+    const Span states[2] = {ins[7], ins[9]};
+    rc = check_spans(states, 2, outs + 6, 1, 0, 0);
     if (rc) return rc;
     if (!dS_init) return WKV7_OK;
-    cudaError_t e = cudaMemsetAsync(dS_init, 0, st, stream);
+    cudaError_t e = dS_final ? cudaMemcpyAsync(dS_init, dS_final, st, cudaMemcpyDeviceToDevice, stream)
+                             : cudaMemsetAsync(dS_init, 0, st, stream);
     return e == cudaSuccess ? WKV7_OK : fail_cuda(e, "empty backward");
   }
-  rc = check_spans(ins, 9, outs, 7, 7, 6);
+  rc = check_spans(ins, 10, outs, 7, 7, 6);
   if (rc) return rc;
 
   // bf16 inputs at N = 64 with 16-step checkpoints take a chunked tensor-core
@@ -304,6 +307,7 @@ int backward_impl(bool bf16, const void* const in[7], const float* s_init, const
   args.da = grads[4];
   args.db = grads[5];
   args.dS_init = dS_init;
+  args.dS_final = dS_final;
   args.carry = split ? ws + ck_ws / sizeof(float) : nullptr;
   for (int v = 0; v < 7; ++v) args.in[v] = in[v];
   args.C = C_eff;
@@ -407,6 +411,7 @@ int backward_noalloc_impl(const float* const in[7], const float* s_init, float* 
   fa.T = T;
   fa.H = H;
   BwdArgs ba;
+  ba.dS_final = nullptr;
   for (int v = 0; v < 7; ++v)
     if ((rc = make_map(&ba.map[v], in[v], false, B, T, H, N, bwd2_steps_per_window(N, false)))) return rc;
   if ((rc = make_ckpt_map(&ba.ckmap, scratch, B, H, N, fa.nck))) return rc;
@@ -463,7 +468,28 @@ int wkv7_backward(const float* r, const float* w, const float* k, const float* v
                   float* dS_init, int B, int T, int H, int N, void* stream) {
   const void* in[7] = {r, w, k, v, a, b, dy};
   float* const grads[6] = {dr, dw, dk, dv, da, db};
-  return backward_impl(false, in, s_init, ckpt, ckpt_every, grads, dS_init, B, T, H, N,
+  return backward_impl(false, in, s_init, nullptr, ckpt, ckpt_every, grads, dS_init, B, T, H, N,
+                       static_cast<cudaStream_t>(stream));
+}
+
+int wkv7_backward_segment(const float* r, const float* w, const float* k, const float* v, const float* a,
+                          const float* b, const float* dy, const float* s_init, const float* dS_final,
+                          const float* ckpt, int ckpt_every, float* dr, float* dw, float* dk, float* dv, float* da,
+                          float* db, float* dS_init, int B, int T, int H, int N, void* stream) {
+  const void* in[7] = {r, w, k, v, a, b, dy};
+  float* const grads[6] = {dr, dw, dk, dv, da, db};
+  return backward_impl(false, in, s_init, dS_final, ckpt, ckpt_every, grads, dS_init, B, T, H, N,
+                       static_cast<cudaStream_t>(stream));
+}
+
+int wkv7_backward_segment_bf16(const wkv7_bf16* r, const wkv7_bf16* w, const wkv7_bf16* k, const wkv7_bf16* v,
+                               const wkv7_bf16* a, const wkv7_bf16* b, const wkv7_bf16* dy, const float* s_init,
+                               const float* dS_final, const float* ckpt, int ckpt_every, float* dr, float* dw,
+                               float* dk, float* dv, float* da, float* db, float* dS_init, int B, int T, int H,
+                               int N, void* stream) {
+  const void* in[7] = {r, w, k, v, a, b, dy};
+  float* const grads[6] = {dr, dw, dk, dv, da, db};
+  return backward_impl(true, in, s_init, dS_final, ckpt, ckpt_every, grads, dS_init, B, T, H, N,
                        static_cast<cudaStream_t>(stream));
 }
 
@@ -473,7 +499,7 @@ int wkv7_backward_bf16(const wkv7_bf16* r, const wkv7_bf16* w, const wkv7_bf16* 
                        float* da, float* db, float* dS_init, int B, int T, int H, int N, void* stream) {
   const void* in[7] = {r, w, k, v, a, b, dy};
   float* const grads[6] = {dr, dw, dk, dv, da, db};
-  return backward_impl(true, in, s_init, ckpt, ckpt_every, grads, dS_init, B, T, H, N,
+  return backward_impl(true, in, s_init, nullptr, ckpt, ckpt_every, grads, dS_init, B, T, H, N,
                        static_cast<cudaStream_t>(stream));
 }
 

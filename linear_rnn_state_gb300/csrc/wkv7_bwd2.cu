@@ -214,11 +214,18 @@ __global__ void __launch_bounds__(Bwd2Cfg<TIn, N, R, E, KS>::THREADS, 1)
   static_assert(SG >= 1 && KS % SG == 0 && NQ <= 32 && Cfg::THREADS % NQ == 0, "prologue mapping");
   const int pq = tid % NQ, pg = tid / NQ;
 
+  // the carry after the last step: the gradient entering through the final state (or zero)
   float2 Gt[R][NP];
 #pragma unroll
   for (int i = 0; i < R; ++i)
 #pragma unroll
-    for (int p = 0; p < NP; ++p) Gt[i][p] = make_float2(0.f, 0.f);
+    for (int m = 0; m < Q; ++m) {
+      const float4 g4 = args.dS_final
+                            ? ld_f4(args.dS_final + ((size_t)head * N + row0 + i) * N + colq(m))
+                            : make_float4(0.f, 0.f, 0.f, 0.f);
+      Gt[i][2 * m] = make_float2(g4.x, g4.y);
+      Gt[i][2 * m + 1] = make_float2(g4.z, g4.w);
+    }
   float2 S[R][NP];
   bool completed = true;
 

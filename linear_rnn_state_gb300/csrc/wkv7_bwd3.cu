@@ -422,9 +422,23 @@ __global__ void __launch_bounds__(kThreads, 1) wkv7_bwd3_kernel(const __grid_con
     for (int m = 0; m < kStages && m < nchunks; ++m) issue(m);
   }
   if (tid == 0) sm.abort_flag = 0;
+  // the carry after the last chunk: the gradient entering through the final state (or zero)
   float G[8][4];
 #pragma unroll
   for (int nt = 0; nt < 8; ++nt) zero4(G[nt]);
+  if (args.dS_final && warp < 4) {
+    const float* src = args.dS_final + (size_t)head * kN * kN;
+#pragma unroll
+    for (int nt = 0; nt < 8; ++nt) {
+      const int col = 8 * nt + 2 * t4;
+      const float2 lo = *reinterpret_cast<const float2*>(src + (i0 + g) * kN + col);
+      const float2 hi = *reinterpret_cast<const float2*>(src + (i0 + g + 8) * kN + col);
+      G[nt][0] = lo.x;
+      G[nt][1] = lo.y;
+      G[nt][2] = hi.x;
+      G[nt][3] = hi.y;
+    }
+  }
   if (!is_prep) {
     fetch_ckpt(nchunks - 1);
     cp_async_wait_all();
@@ -769,7 +783,11 @@ __global__ void __launch_bounds__(kThreads, 1) wkv7_bwd3_kernel(const __grid_con
         const float(&sp)[4][kN] = sm.spart[n & 1];
         const float start = sp[0][col] + sp[1][col] + sp[2][col] + sp[3][col];
         const float(&bp)[4][kN] = sm.spart[(n + 1) & 1];
-        const float bnd = bp[0][col] + bp[1][col] + bp[2][col] + bp[3][col];
+        float bnd = bp[0][col] + bp[1][col] + bp[2][col] + bp[3][col];
+        // after the last chunk the state is not at hand: with a gradient entering through it,
+        // take the end anchor from the identity end = start - sum of x over the chunk
+        const float xtot = __shfl_sync(0xffffffffu, lo, 28 + t4) + __shfl_sync(0xffffffffu, hi2, t4);
+        if (n == nchunks - 1 && args.dS_final) bnd = start - xtot;
         const float2 w0 = bf2(rs + V_W * kTile + g * kN + jw + 2 * t4);
         const float2 w1 = bf2(rs + V_W * kTile + (g + 8) * kN + jw + 2 * t4);
         dw[e] = (start - (lo - xw[e]) - adw[e]) * rcp_approx(e ? w0.y : w0.x);

@@ -532,9 +532,23 @@ __global__ void __launch_bounds__(kCarryThreads, 1) wkv7_bwd4_carry_kernel(const
   }
   issued = min(kCarryStages, nchunks);
   if (tid == 0) sm.abort_flag = 0;
+  // the carry after the last chunk: the gradient entering through the final state (or zero)
   float G[8][4];
 #pragma unroll
   for (int nt = 0; nt < 8; ++nt) zero4(G[nt]);
+  if (args.dS_final && warp < 4) {
+    const float* src = args.dS_final + (size_t)head * kN * kN;
+#pragma unroll
+    for (int nt = 0; nt < 8; ++nt) {
+      const int col = 8 * nt + 2 * t4;
+      const float2 lo = *reinterpret_cast<const float2*>(src + (i0 + g) * kN + col);
+      const float2 hi = *reinterpret_cast<const float2*>(src + (i0 + g + 8) * kN + col);
+      G[nt][0] = lo.x;
+      G[nt][1] = lo.y;
+      G[nt][2] = hi.x;
+      G[nt][3] = hi.y;
+    }
+  }
   __syncthreads();
 
   bool aborted = false;

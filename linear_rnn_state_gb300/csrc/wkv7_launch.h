@@ -33,7 +33,8 @@ struct BwdArgs {
   float* dv;
   float* da;
   float* db;
-  float* dS_init;  // [B][H][N][N] or null
+  float* dS_init;         // [B][H][N][N] or null
+  const float* dS_final;  // [B][H][N][N] gradient entering through the final state, or null (zeros)
   const void* in[7];  // r, w, k, v, a, b, dy ([B][T][H][N], the input type)
   void* carry;        // split backward: [B*H][nchunks][N][N] carry after each chunk (bf16)
   unsigned* status;

@@ -22,6 +22,8 @@ EXPORTS = {
     "wkv7_forward_bf16": 16,
     "wkv7_backward": 22,
     "wkv7_backward_bf16": 22,
+    "wkv7_backward_segment": 23,
+    "wkv7_backward_segment_bf16": 23,
     "wkv7_ckpt_bytes": 5,
     "wkv7_default_ckpt_every": 2,
     "wkv7_status": 1,
@@ -53,7 +55,10 @@ def load(path: str | None = None):
     lib.wkv7_forward_bf16.argtypes = [vp] * 10 + [i] * 5 + [vp]
     lib.wkv7_backward.argtypes = [vp] * 9 + [i] + [vp] * 7 + [i] * 4 + [vp]
     lib.wkv7_backward_bf16.argtypes = [vp] * 9 + [i] + [vp] * 7 + [i] * 4 + [vp]
-    for f in ("wkv7_forward", "wkv7_forward_bf16", "wkv7_backward", "wkv7_backward_bf16"):
+    lib.wkv7_backward_segment.argtypes = [vp] * 10 + [i] + [vp] * 7 + [i] * 4 + [vp]
+    lib.wkv7_backward_segment_bf16.argtypes = [vp] * 10 + [i] + [vp] * 7 + [i] * 4 + [vp]
+    for f in ("wkv7_forward", "wkv7_forward_bf16", "wkv7_backward", "wkv7_backward_bf16", "wkv7_backward_segment",
+              "wkv7_backward_segment_bf16"):
         getattr(lib, f).restype = i
     lib.wkv7_ckpt_bytes.argtypes = [i] * 5
     lib.wkv7_ckpt_bytes.restype = sz
@@ -100,6 +105,20 @@ def wkv7_backward_bf16(r, w, k, v, a, b, dy, s_init, ckpt, ckpt_every, dr, dw, d
                        B, T, H, N, stream):
     return load().wkv7_backward_bf16(r, w, k, v, a, b, dy, s_init, ckpt, ckpt_every, dr, dw, dk, dv, da, db,
                                      dS_init, B, T, H, N, stream)
+
+
+def wkv7_backward_segment(r, w, k, v, a, b, dy, s_init, dS_final, ckpt, ckpt_every, dr, dw, dk, dv, da, db,
+                          dS_init, B, T, H, N, stream):
+    """wkv7_backward_segment (include/wkv7.h): pointers as ints."""
+    return load().wkv7_backward_segment(r, w, k, v, a, b, dy, s_init, dS_final, ckpt, ckpt_every, dr, dw, dk, dv,
+                                        da, db, dS_init, B, T, H, N, stream)
+
+
+def wkv7_backward_segment_bf16(r, w, k, v, a, b, dy, s_init, dS_final, ckpt, ckpt_every, dr, dw, dk, dv, da, db,
+                               dS_init, B, T, H, N, stream):
+    """wkv7_backward_segment_bf16 (include/wkv7.h): pointers as ints."""
+    return load().wkv7_backward_segment_bf16(r, w, k, v, a, b, dy, s_init, dS_final, ckpt, ckpt_every, dr, dw, dk,
+                                             dv, da, db, dS_init, B, T, H, N, stream)
 
 
 def wkv7_backward_noalloc(r, w, k, v, a, b, dy, s_init, dr, dw, dk, dv, da, db, dS_init, B, T, H, N, stream):
@@ -167,9 +186,11 @@ def forward(r, w, k, v, a, b, s_init=None, *, ckpt_every: int | None = None, wan
 
 
 def backward(r, w, k, v, a, b, dy, s_init=None, ckpt=None, ckpt_every: int = 0, *, want_dS_init: bool = True,
-             stream=None):
+             dS_final=None, stream=None):
     """Backward-through-time. Returns dict dr, dw, dk, dv, da, db (float32
-    [B][T][H][N]) and dS_init (float32 [B][H][N][N] or None)."""
+    [B][T][H][N]) and dS_init (float32 [B][H][N][N] or None). dS_final
+    (float32 [B][H][N][N]) is the gradient entering through the final state
+    (None: zero)."""
     import torch
 
     bf16 = _inputs_dtype(r)
@@ -177,8 +198,8 @@ def backward(r, w, k, v, a, b, dy, s_init=None, ckpt=None, ckpt_every: int = 0, 
     dev = r.device
     g = {n: torch.empty((B, T, H, N), dtype=torch.float32, device=dev) for n in ("dr", "dw", "dk", "dv", "da", "db")}
     g["dS_init"] = torch.empty((B, H, N, N), dtype=torch.float32, device=dev) if want_dS_init else None
-    fn = wkv7_backward_bf16 if bf16 else wkv7_backward
-    _check(fn(*(_addr(x) for x in (r, w, k, v, a, b, dy, s_init, ckpt)), ckpt_every,
+    fn = wkv7_backward_segment_bf16 if bf16 else wkv7_backward_segment
+    _check(fn(*(_addr(x) for x in (r, w, k, v, a, b, dy, s_init, dS_final, ckpt)), ckpt_every,
               *(_addr(g[n]) for n in ("dr", "dw", "dk", "dv", "da", "db", "dS_init")), B, T, H, N, _stream(stream)))
     return g
 
