@@ -34,8 +34,8 @@ FP32_LANES_PER_SM = 128  # Blackwell SM: 4 partitions x 32 FP32 lanes
 TRAFFIC = {
     "kernel": "wkv7_bwd4_carry_kernel + wkv7_bwd4_out_kernel (one wkv7_backward_bf16 call)",
     "sources": ("wkv7_bwd4.cu", "wkv7_common.cuh", "wkv7_scaled.cuh", "wkv7_mma.cuh", "wkv7_launch.h"),
-    "sha256": "ea577be540009499cb1e8859ae9c26f8a81b82bfb0464ae156da03d710eba032",
-    "bytes_per_token_head": (83.958272e6 + 26.309888e6 + 318.859008e6 + 165.179648e6) / 131072,
+    "sha256": "fb18ca88265d753a1257bcc936b0a530a54b591d18b244b14116a2d543dd89db",
+    "bytes_per_token_head": (83.964416e6 + 28.879104e6 + 318.864128e6 + 165.230592e6) / 131072,
 }
 
 
