@@ -1,4 +1,4 @@
-"""Seeded synthetic inputs for the WKV7 scan.
+"""Seeded synthetic inputs for the WKV7 scan and the RWKV-8 recurrence.
 
 A module of its own: it draws random numbers and shapes them into the scan's
 inputs, and holds none of the recurrence's arithmetic. The CUDA path and the
@@ -51,6 +51,9 @@ def _load():
         lib.wkv7_gen_normal_at.restype = ctypes.c_double
         lib.wkv7_gen_bf16_rne.argtypes = [ctypes.c_double]
         lib.wkv7_gen_bf16_rne.restype = ctypes.c_uint16
+        dp = ctypes.POINTER(ctypes.c_double)
+        lib.rwkv8_gen_inputs.argtypes = [ctypes.c_uint64] + [i] * 6 + [dp] * 6 + [ctypes.c_double] + [dp] * 2 + [i]
+        lib.rwkv8_gen_inputs.restype = i
         _lib = lib
     return _lib
 
@@ -87,3 +90,39 @@ def as_f64(x: np.ndarray, storage: str) -> np.ndarray:
     if storage == "bf16":
         return bf16_bits_to_f64(x)
     return np.asarray(x, dtype=np.float64)
+
+
+def generate_rwkv8(B: int, T: int, H: int, Hv: int, L: int, E: int, storage: str = "f32",
+                   state_std: float | None = None, boundary: bool = False, seed: int = 0,
+                   nthreads: int = 0) -> dict:
+    """Inputs of the RWKV-8 normalized recurrence (value semantics and draw
+    order in ``wkv7_gen.c``, rwkv8_gen_inputs): q [B][H][T][L], v [B][Hv][T][E],
+    decay [H][L], dy [B][H][T][E]; with ``state_std`` also rho_init and
+    rho_norm_init, with ``boundary`` also d_rho_final and d_rho_norm_final
+    (else those keys hold None). Drawn in double and rounded once to
+    ``storage`` ("f64" or "f32")."""
+    if storage not in ("f64", "f32"):
+        raise ValueError("storage must be f64 or f32")
+    lib = _load()
+    dp = ctypes.POINTER(ctypes.c_double)
+    arr = {
+        "q": np.empty((B, H, T, L)), "v": np.empty((B, Hv, T, E)), "decay": np.empty((H, L)),
+        "dy": np.empty((B, H, T, E)),
+        "rho_init": np.empty((B, H, L, E)) if state_std is not None else None,
+        "rho_norm_init": np.empty((B, H, L)) if state_std is not None else None,
+        "d_rho_final": np.empty((B, H, L, E)) if boundary else None,
+        "d_rho_norm_final": np.empty((B, H, L)) if boundary else None,
+    }
+
+    def ptr(x):
+        return None if x is None else x.ctypes.data_as(dp)
+
+    rc = lib.rwkv8_gen_inputs(
+        ctypes.c_uint64(seed), B, T, H, Hv, L, E, ptr(arr["q"]), ptr(arr["v"]), ptr(arr["decay"]),
+        ptr(arr["dy"]), ptr(arr["rho_init"]), ptr(arr["rho_norm_init"]), float(state_std or 0.0),
+        ptr(arr["d_rho_final"]), ptr(arr["d_rho_norm_final"]), nthreads)
+    if rc != 0:
+        raise RuntimeError(f"rwkv8_gen_inputs failed with status {rc}")
+    if storage == "f32":
+        arr = {k: None if x is None else x.astype(np.float32) for k, x in arr.items()}
+    return arr

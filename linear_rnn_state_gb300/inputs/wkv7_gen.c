@@ -1,5 +1,6 @@
 /*
- * Seeded synthetic inputs for the WKV7 scan (r, w, k, v, a, b, dy, s_init).
+ * Seeded synthetic inputs for the WKV7 scan (r, w, k, v, a, b, dy, s_init)
+ * and, at the end of the file, for the RWKV-8 normalized recurrence.
  *
  * This module draws random numbers and shapes them into the six recurrence
  * inputs, the upstream gradient dy and the optional initial state. It holds
@@ -185,4 +186,98 @@ int wkv7_gen_inputs(uint64_t seed, int B, int T, int H, int N, int kind,
   fill_worker(&jobs[0]);
   for (int i = 1; i <= started; ++i) pthread_join(tids[i], NULL);
   return rc;
+}
+
+/*
+ * Seeded synthetic inputs for the RWKV-8 normalized recurrence (the
+ * burn_dragon_kernel page "src/sequence/rwkv8/backward.rs"), in double.
+ *
+ * Value semantics (the page gives no value ranges; these are readings):
+ *   q      = max(n, 0)                        non-negative query weights
+ *   v      = n / sqrt(E)
+ *   decay  = exp(-0.606531 * sigmoid(z))       the RWKV-7 decay range (0.545, 1)
+ *   dy     = n
+ *   rho_init      = std * n        (optional)
+ *   rho_norm_init = std * |n|      (optional; a running sum of q is >= 0)
+ *   d_rho_final   = n, d_rho_norm_final = n   (optional)
+ * Streams, in this order, each as long as its array: q [B][H][T][L],
+ * v [B][Hv][T][E], z [H][L], dy [B][H][T][E], rho_init [B][H][L][E],
+ * rho_norm_init [B][H][L], d_rho_final [B][H][L][E], d_rho_norm_final
+ * [B][H][L]; stream s starts at normal number (sum of the earlier lengths),
+ * so every array is the same whichever optional arrays are asked for.
+ */
+typedef struct {
+  uint64_t seed, base;
+  double *out;
+  size_t begin, end;
+  int kind; /* 0 plain normal, 1 max(n, 0), 2 n * scale, 3 |n| * scale, 4 decay */
+  double scale;
+} rwkv8_job;
+
+static void *rwkv8_worker(void *arg) {
+  rwkv8_job *J = (rwkv8_job *)arg;
+  for (size_t f = J->begin; f < J->end; ++f) {
+    const double n = wkv7_gen_normal_at(J->seed, J->base + f);
+    double x;
+    switch (J->kind) {
+      case 1: x = n > 0.0 ? n : 0.0; break;
+      case 2: x = n * J->scale; break;
+      case 3: x = fabs(n) * J->scale; break;
+      case 4: x = exp(-WDECAY_COEFF * sigmoid(n)); break;
+      default: x = n; break;
+    }
+    J->out[f] = x;
+  }
+  return NULL;
+}
+
+static int rwkv8_fill(uint64_t seed, uint64_t base, double *out, size_t count, int kind, double scale,
+                      int nthreads) {
+  if (!out || count == 0) return 0;
+  rwkv8_job jobs[256];
+  pthread_t tids[256];
+  if ((size_t)nthreads > count) nthreads = (int)count;
+  for (int i = 0; i < nthreads; ++i) {
+    jobs[i].seed = seed; jobs[i].base = base; jobs[i].out = out;
+    jobs[i].begin = count * i / nthreads; jobs[i].end = count * (i + 1) / nthreads;
+    jobs[i].kind = kind; jobs[i].scale = scale;
+  }
+  int started = 0, rc = 0;
+  for (int i = 1; i < nthreads; ++i) {
+    if (pthread_create(&tids[i], NULL, rwkv8_worker, &jobs[i]) != 0) { rc = -1; break; }
+    started = i;
+  }
+  rwkv8_worker(&jobs[0]);
+  for (int i = 1; i <= started; ++i) pthread_join(tids[i], NULL);
+  return rc;
+}
+
+/*
+ * Fill the RWKV-8 inputs. q, v, decay and dy are required; the four state
+ * arrays may be NULL (not drawn). Returns 0, -2 on an invalid argument or -1
+ * if a thread cannot start. nthreads <= 0 uses every online core.
+ */
+int rwkv8_gen_inputs(uint64_t seed, int B, int T, int H, int Hv, int L, int E, double *q, double *v,
+                     double *decay, double *dy, double *rho_init, double *rho_norm_init, double state_std,
+                     double *d_rho_final, double *d_rho_norm_final, int nthreads) {
+  if (B <= 0 || T <= 0 || H <= 0 || L <= 0 || E <= 0 || (Hv != 1 && Hv != H)) return -2;
+  if (!q || !v || !decay || !dy) return -2;
+  if (nthreads <= 0) {
+    long n = sysconf(_SC_NPROCESSORS_ONLN);
+    nthreads = n > 0 ? (int)n : 1;
+  }
+  if (nthreads > 256) nthreads = 256;
+  const uint64_t nq = (uint64_t)B * H * T * L, nv = (uint64_t)B * Hv * T * E, nz = (uint64_t)H * L;
+  const uint64_t ny = (uint64_t)B * H * T * E, ns = (uint64_t)B * H * L * E, nn = (uint64_t)B * H * L;
+  uint64_t base = 0;
+  int rc = 0;
+  rc |= rwkv8_fill(seed, base, q, nq, 1, 1.0, nthreads); base += nq;
+  rc |= rwkv8_fill(seed, base, v, nv, 2, 1.0 / sqrt((double)E), nthreads); base += nv;
+  rc |= rwkv8_fill(seed, base, decay, nz, 4, 1.0, nthreads); base += nz;
+  rc |= rwkv8_fill(seed, base, dy, ny, 0, 1.0, nthreads); base += ny;
+  rc |= rwkv8_fill(seed, base, rho_init, ns, 2, state_std, nthreads); base += ns;
+  rc |= rwkv8_fill(seed, base, rho_norm_init, nn, 3, state_std, nthreads); base += nn;
+  rc |= rwkv8_fill(seed, base, d_rho_final, ns, 0, 1.0, nthreads); base += ns;
+  rc |= rwkv8_fill(seed, base, d_rho_norm_final, nn, 0, 1.0, nthreads);
+  return rc ? -1 : 0;
 }
