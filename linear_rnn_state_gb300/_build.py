@@ -18,8 +18,9 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD_DIR = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libwkv7.so")
 
-SOURCES = ["wkv7_api.cu", "wkv7_fwd.cu", "wkv7_fwd2.cu", "wkv7_fwd3.cu", "wkv7_bwd.cu", "wkv7_bwd2.cu", "wkv7_bwd3.cu", "wkv7_bwd4.cu"]
-HEADERS = ["wkv7_common.cuh", "wkv7_launch.h", "wkv7_mma.cuh", "wkv7_scaled.cuh", "wkv7_tmem.cuh"]
+SOURCES = ["wkv7_api.cu", "wkv7_fwd.cu", "wkv7_fwd2.cu", "wkv7_fwd3.cu", "wkv7_bwd.cu", "wkv7_bwd2.cu", "wkv7_bwd3.cu", "wkv7_bwd4.cu", "rwkv8_api.cu",
+           "rwkv8_fwd.cu", "rwkv8_bwd.cu"]
+HEADERS = ["wkv7_common.cuh", "wkv7_launch.h", "wkv7_mma.cuh", "wkv7_scaled.cuh", "wkv7_tmem.cuh", "rwkv8_launch.h"]
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ARCH + ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-cudart", "shared",
@@ -47,7 +48,7 @@ def _stale(target: str, deps) -> bool:
 def build(force: bool = False, verbose: bool = False, extra_flags=()) -> str:
     """Compile every .cu to an object (in parallel) and link libwkv7.so."""
     os.makedirs(BUILD_DIR, exist_ok=True)
-    headers = [os.path.join(CSRC, h) for h in HEADERS] + [os.path.join(INCLUDE, "wkv7.h")]
+    headers = [os.path.join(CSRC, h) for h in HEADERS] + [os.path.join(INCLUDE, h) for h in ("wkv7.h", "rwkv8.h")]
     objs, jobs = [], []
     for src in SOURCES:
         s = os.path.join(CSRC, src)

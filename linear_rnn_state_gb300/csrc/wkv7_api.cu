@@ -326,6 +326,10 @@ int backward_impl(bool bf16, const void* const in[7], const float* s_init, const
 
 }  // namespace
 
+// Error hook for the other entry points of the library (rwkv8_api.cu): the
+// message goes to the same thread-local slot wkv7_last_error() reads.
+int api_fail(int code, const char* msg) { return fail(code, "%s", msg); }
+
 // ======================================== backward without allocation ===
 //
 // For callers that cannot allocate device memory: code running inside a

@@ -7,6 +7,9 @@
 
 namespace wkv7 {
 
+// Records `msg` as the calling thread's last error and returns `code`.
+int api_fail(int code, const char* msg);
+
 // Forward kernel arguments. The tensor maps describe r, w, k, v, a, b as
 // 4-D tensors (N, H, T, B) with a box of (N, 1, K, 1): K steps of one head.
 struct FwdArgs {

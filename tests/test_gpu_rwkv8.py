@@ -1,0 +1,162 @@
+"""GPU parity of the RWKV-8 normalized recurrence (include/rwkv8.h) against the
+fp64 oracle (oracle/rwkv8_oracle.py), called through the C ABI.
+
+Inputs are the seeded synthetic ones of linear_rnn_state_gb300.inputs
+(generate_rwkv8), rounded to fp32; the oracle consumes exactly those values.
+The bar is the fp32 one of this library, element by element:
+|gpu - ref| <= 1e-4 (1 + |ref|) for y, the final states, dq, dv and the
+initial-state gradients. ddecay is a sum over batch and time of terms of both
+signs, so one entry can be much smaller than the terms it sums; it is held to
+|gpu - ref| <= 1e-4 (1 + |ref| + S) with S the mean |ref| over its latents
+(the scale of the summands, which fp32 summation error follows).
+"""
+import importlib.util
+import os
+
+import numpy as np
+import pytest
+
+pytestmark = pytest.mark.gpu
+
+torch = pytest.importorskip("torch")
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def env():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import __graft_entry__  # noqa: F401
+    from linear_rnn_state_gb300 import _build, inputs, rwkv8
+
+    _build.build()
+    rwkv8.load()
+    spec = importlib.util.spec_from_file_location("rwkv8_oracle", os.path.join(ROOT, "oracle", "rwkv8_oracle.py"))
+    orc = importlib.util.module_from_spec(spec)
+    spec.loader.exec_module(orc)
+    torch.cuda.set_device(0)
+    return orc, inputs, rwkv8
+
+
+def _close(name, got, ref, scale=0.0):
+    got = np.asarray(got, dtype=np.float64)
+    assert got.shape == ref.shape, (name, got.shape, ref.shape)
+    assert np.all(np.isfinite(got)), name
+    err = np.abs(got - ref) / (1.0 + np.abs(ref) + scale)
+    assert err.max() <= 1e-4, f"{name}: max scaled error {err.max():.3e}"
+
+
+def _dev(x):
+    return None if x is None else torch.from_numpy(np.ascontiguousarray(x)).cuda()
+
+
+def _run(env, B, T, H, Hv, seed, state=False, boundary=False, use_ckpt=True):
+    orc, inputs, rwkv8 = env
+    d = inputs.generate_rwkv8(B, T, H, Hv, 64, 64, "f32", state_std=0.1 if state else None, boundary=boundary,
+                              seed=seed)
+    t = {k: _dev(x) for k, x in d.items()}
+    y, rf, nf, ck = rwkv8.forward(t["q"], t["v"], t["decay"], t["rho_init"], t["rho_norm_init"], want_ckpt=use_ckpt)
+    g = rwkv8.backward(t["q"], t["v"], t["decay"], t["dy"], t["rho_init"], t["rho_norm_init"], ck,
+                       d_rho_final=t["d_rho_final"], d_rho_norm_final=t["d_rho_norm_final"])
+    torch.cuda.synchronize()
+    o = {k: None if x is None else x.astype(np.float64) for k, x in d.items()}
+    y_ref, rf_ref, nf_ref = orc.forward(o["q"], o["v"], o["decay"], o["rho_init"], o["rho_norm_init"])
+    g_ref = orc.backward(o["q"], o["v"], o["decay"], o["dy"], o["rho_init"], o["rho_norm_init"], o["d_rho_final"],
+                         o["d_rho_norm_final"])
+    tag = f"B={B} T={T} H={H} Hv={Hv}"
+    _close(f"y {tag}", y.cpu().numpy(), y_ref)
+    _close(f"rho_final {tag}", rf.cpu().numpy(), rf_ref)
+    _close(f"rho_norm_final {tag}", nf.cpu().numpy(), nf_ref)
+    for k in ("dq", "dv", "d_rho_init", "d_rho_norm_init"):
+        _close(f"{k} {tag}", g[k].cpu().numpy(), g_ref[k])
+    _close(f"ddecay {tag}", g["ddecay"].cpu().numpy(), g_ref["ddecay"], float(np.abs(g_ref["ddecay"]).mean()))
+    return g
+
+
+@pytest.mark.parametrize("B,T,H,Hv", [(2, 16, 3, 3), (2, 45, 3, 1), (1, 130, 2, 2), (2, 1, 2, 2), (1, 33, 1, 1)])
+def test_rwkv8_parity(env, B, T, H, Hv):
+    _run(env, B, T, H, Hv, seed=100 + T)
+
+
+@pytest.mark.parametrize("Hv", [1, 3])
+def test_rwkv8_parity_with_states_and_boundary(env, Hv):
+    _run(env, 2, 70, 3, Hv, seed=7, state=True, boundary=True)
+
+
+def test_rwkv8_backward_without_checkpoints_matches(env):
+    """ckpt = NULL makes the library run the forward itself: the same kernels
+    on the same inputs, so the gradients are bit-identical."""
+    _, inputs, rwkv8 = env
+    d = inputs.generate_rwkv8(2, 50, 2, 2, 64, 64, "f32", state_std=0.1, seed=3)
+    t = {k: _dev(x) for k, x in d.items()}
+    _, _, _, ck = rwkv8.forward(t["q"], t["v"], t["decay"], t["rho_init"], t["rho_norm_init"])
+    g1 = rwkv8.backward(t["q"], t["v"], t["decay"], t["dy"], t["rho_init"], t["rho_norm_init"], ck)
+    g2 = rwkv8.backward(t["q"], t["v"], t["decay"], t["dy"], t["rho_init"], t["rho_norm_init"], None)
+    torch.cuda.synchronize()
+    for k in g1:
+        assert torch.equal(g1[k], g2[k]), k
+
+
+def test_rwkv8_empty_sequence(env):
+    _, inputs, rwkv8 = env
+    d = inputs.generate_rwkv8(2, 1, 2, 2, 64, 64, "f32", state_std=0.1, boundary=True, seed=4)
+    t = {k: _dev(x) for k, x in d.items()}
+    q0, v0, dy0 = (torch.empty((2, 2, 0, 64), device="cuda") for _ in range(3))
+    y, rf, nf, _ = rwkv8.forward(q0, v0, t["decay"], t["rho_init"], t["rho_norm_init"], want_ckpt=False)
+    g = rwkv8.backward(q0, v0, t["decay"], dy0, t["rho_init"], t["rho_norm_init"], None,
+                       d_rho_final=t["d_rho_final"], d_rho_norm_final=t["d_rho_norm_final"])
+    torch.cuda.synchronize()
+    assert torch.equal(rf, t["rho_init"]) and torch.equal(nf, t["rho_norm_init"])
+    assert torch.equal(g["d_rho_init"], t["d_rho_final"]) and torch.equal(g["d_rho_norm_init"], t["d_rho_norm_final"])
+    assert torch.count_nonzero(g["ddecay"]) == 0
+
+
+def test_rwkv8_segments_compose(env):
+    """Backward of [T1, T) with the final-state gradients, then of [0, T1) with
+    the initial-state gradients it returned, equals the whole sequence's."""
+    _, inputs, rwkv8 = env
+    B, T, H, T1 = 2, 96, 2, 40
+    d = inputs.generate_rwkv8(B, T, H, H, 64, 64, "f32", boundary=True, seed=5)
+    t = {k: _dev(x) for k, x in d.items()}
+    full = rwkv8.backward(t["q"], t["v"], t["decay"], t["dy"], None, None, None, d_rho_final=t["d_rho_final"],
+                          d_rho_norm_final=t["d_rho_norm_final"])
+    a = {k: t[k][:, :, :T1].contiguous() for k in ("q", "v", "dy")}
+    z = {k: t[k][:, :, T1:].contiguous() for k in ("q", "v", "dy")}
+    _, r_mid, n_mid, _ = rwkv8.forward(a["q"], a["v"], t["decay"], want_ckpt=False)
+    g2 = rwkv8.backward(z["q"], z["v"], t["decay"], z["dy"], r_mid, n_mid, None, d_rho_final=t["d_rho_final"],
+                        d_rho_norm_final=t["d_rho_norm_final"])
+    g1 = rwkv8.backward(a["q"], a["v"], t["decay"], a["dy"], None, None, None, d_rho_final=g2["d_rho_init"],
+                        d_rho_norm_final=g2["d_rho_norm_init"])
+    torch.cuda.synchronize()
+    for k in ("dq", "dv"):
+        got = torch.cat([g1[k], g2[k]], dim=2).cpu().numpy()
+        _close(k, got, full[k].cpu().numpy().astype(np.float64))
+    _close("ddecay", (g1["ddecay"] + g2["ddecay"]).cpu().numpy(), full["ddecay"].cpu().numpy().astype(np.float64),
+           float(np.abs(full["ddecay"].cpu().numpy()).mean()))
+
+
+def test_rwkv8_full_size_sampled(env):
+    """The benchmark's workload (B=4, T=4096, H=32, one value row per head,
+    L = E = 64) in the same launch configuration; the oracle recomputes every
+    output of the heads of one h (all four batch rows, so ddecay[h] is whole)."""
+    orc, inputs, rwkv8 = env
+    B, T, H = 4, 4096, 32
+    d = inputs.generate_rwkv8(B, T, H, H, 64, 64, "f32", seed=0)
+    t = {k: _dev(x) for k, x in d.items()}
+    y, rf, nf, ck = rwkv8.forward(t["q"], t["v"], t["decay"])
+    g = rwkv8.backward(t["q"], t["v"], t["decay"], t["dy"], None, None, ck)
+    torch.cuda.synchronize()
+    for h in (0, 31):
+        sl = (slice(None), slice(h, h + 1))
+        o = {k: d[k][sl].astype(np.float64) for k in ("q", "v", "dy")}
+        dec = d["decay"][h:h + 1].astype(np.float64)
+        y_ref, rf_ref, nf_ref = orc.forward(o["q"], o["v"], dec)
+        g_ref = orc.backward(o["q"], o["v"], dec, o["dy"])
+        _close(f"y h={h}", y[sl].cpu().numpy(), y_ref)
+        _close(f"rho_final h={h}", rf[sl].cpu().numpy(), rf_ref)
+        _close(f"rho_norm_final h={h}", nf[sl].cpu().numpy(), nf_ref)
+        for k in ("dq", "dv", "d_rho_init", "d_rho_norm_init"):
+            _close(f"{k} h={h}", g[k][sl].cpu().numpy(), g_ref[k])
+        _close(f"ddecay h={h}", g["ddecay"][h:h + 1].cpu().numpy(), g_ref["ddecay"],
+               float(np.abs(g_ref["ddecay"]).mean()))
