@@ -390,6 +390,213 @@ def _report(args, wl, world, B, T, H, N, C, bf16, ms, fwd_ms, bwd_ms, e2e, ckpt,
     return 0
 
 
+# ------------------------------------------------------------------ RWKV-8 ---
+# `--workload rwkv8`: the RWKV-8 normalized recurrence (include/rwkv8.h), fp32,
+# B=4, T=4096, H=32 heads of L = E = 64 with one value row per head. The pages
+# give no sizes for it; this reuses the RWKV-7 layer's B, T, H and head size.
+
+RWKV8_METRIC = "RWKV-8 normalized recurrence fwd+bwd tokens/s (B·T), B=4 T=4096 H=32 L=E=64 fp32; achieved % of roofline"
+RWKV8_SHAPE = {"B": 4, "T": 4096, "H": 32, "Hv": 32, "L": 64, "E": 64}
+
+# DRAM bytes per token-head of one rwkv8_backward call (its kernel and the ddecay sum), from one
+# ncu capture at T=1024 (dram__bytes_read.sum + dram__bytes_write.sum / (B*T*H)); null once the
+# kernel sources change.
+RWKV8_TRAFFIC = {
+    "kernel": "rwkv8_bwd_kernel (one rwkv8_backward call)",
+    "sources": ("rwkv8_bwd.cu", "rwkv8_launch.h"),
+    "sha256": "dacfc9de14f0afc7bc640910bc0341364b06d62de03e3da0b3199eb485f6c91e",
+    "bytes_per_token_head": (237.072128e6 + 49.760512e6) / 131072,
+}
+
+
+def _rwkv8_work_per_token_head(L, E, C=16):
+    """Algorithmic FLOP and bytes per token-head (fwd, bwd) of the RWKV-8
+    recurrence, from its step-by-step definition: forward 3 L E multiply-adds
+    (readout, decay, q v^T), backward 6 L E (carry decay, U dy^T, <rho, dy>,
+    G v, G^T q, G . rho), each 2 FLOP. Bytes: forward reads q, v and writes y
+    and 1/C of a checkpoint (rho and rho_norm); backward reads q, v, dy and
+    the checkpoint share and writes dq and dv (fp32 throughout)."""
+    ck = 4 * (L * E + L) / C
+    return 6 * L * E, 12 * L * E, 4 * (L + 2 * E) + ck, 4 * (L + 2 * E) + ck + 4 * (L + E)
+
+
+def _rwkv8_oracle_sample(d, heads, T):
+    """Time the RWKV-8 oracle (fwd + bwd, fp64) on the first `heads` heads of
+    batch row 0, each over the whole sequence."""
+    import importlib.util
+
+    import numpy as np
+
+    spec = importlib.util.spec_from_file_location("rwkv8_oracle", os.path.join(ROOT, "oracle", "rwkv8_oracle.py"))
+    orc = importlib.util.module_from_spec(spec)
+    spec.loader.exec_module(orc)
+    sl = (slice(0, 1), slice(0, heads))
+    o = {k: d[k][sl].astype(np.float64) for k in ("q", "v", "dy")}
+    dec = d["decay"][:heads].astype(np.float64)
+    t0 = time.perf_counter()
+    orc.forward(o["q"], o["v"], dec)
+    orc.backward(o["q"], o["v"], dec, o["dy"])
+    dt = time.perf_counter() - t0
+    return T * heads / RWKV8_SHAPE["H"] / dt, dt
+
+
+def run_rwkv8(args):
+    world, rank, local = _dist()
+    if args.impl == "reference":
+        if rank != 0:
+            return 0
+        from linear_rnn_state_gb300 import inputs
+
+        sh = RWKV8_SHAPE
+        d = inputs.generate_rwkv8(1, sh["T"], sh["H"], sh["Hv"], sh["L"], sh["E"], "f32", seed=0)
+        heads = 8
+        for _ in range(args.warmup):
+            _rwkv8_oracle_sample(d, heads, sh["T"])
+        times = [_rwkv8_oracle_sample(d, heads, sh["T"])[1] for _ in range(args.steps)]
+        value = sh["T"] * heads / sh["H"] * len(times) / sum(times)
+        line = {
+            "metric": RWKV8_METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": 1000 * sum(times) / len(times), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic", "impl": "reference",
+            "config": {"workload": "rwkv8-4x4096x32-l64e64-f32", **sh},
+            "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": 1, "kind": "oracle",
+                             "sample": f"{heads} of {sh['B'] * sh['H']} heads, full T={sh['T']}, fwd+bwd fp64 "
+                                       "per step (numpy, one thread)"},
+            "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        }
+        print(json.dumps(line), flush=True)
+        return 0
+
+    import torch
+
+    from linear_rnn_state_gb300 import inputs, rwkv8, wkv7
+
+    torch.cuda.set_device(local)
+    dist = _init_pg(world, "nccl")
+    rwkv8.load()
+    dev = torch.device("cuda", local)
+    sh = dict(RWKV8_SHAPE)
+    if args.T:
+        sh["T"] = args.T
+    B, T, H, Hv, L, E = (sh[k] for k in ("B", "T", "H", "Hv", "L", "E"))
+    d = inputs.generate_rwkv8(B, T, H, Hv, L, E, "f32", seed=shard_seed(rank))
+    t_in = {k: torch.from_numpy(d[k]).to(dev) for k in ("q", "v", "decay", "dy")}
+    f32 = dict(dtype=torch.float32, device=dev)
+    y = torch.empty((B, H, T, E), **f32)
+    rf, nf = torch.empty((B, H, L, E), **f32), torch.empty((B, H, L), **f32)
+    ckpt = torch.empty(rwkv8.rwkv8_ckpt_bytes(B, T, H, L, E) // 4, **f32)
+    g = {"dq": torch.empty((B, H, T, L), **f32), "dv": torch.empty((B, Hv, T, E), **f32),
+         "ddecay": torch.empty((H, L), **f32), "d_rho_init": torch.empty((B, H, L, E), **f32),
+         "d_rho_norm_init": torch.empty((B, H, L), **f32)}
+    stream = torch.cuda.current_stream()
+    sp = stream.cuda_stream
+    fargs = [t_in["q"].data_ptr(), t_in["v"].data_ptr(), t_in["decay"].data_ptr(), None, None, y.data_ptr(),
+             rf.data_ptr(), nf.data_ptr(), ckpt.data_ptr(), B, T, H, Hv, L, E, sp]
+    bargs = [t_in["q"].data_ptr(), t_in["v"].data_ptr(), t_in["decay"].data_ptr(), t_in["dy"].data_ptr(), None, None,
+             None, None, ckpt.data_ptr()] + [g[k].data_ptr() for k in g] + [B, T, H, Hv, L, E, sp]
+
+    def step(ev=None):
+        if ev is not None:
+            ev[0].record(stream)
+        rc = rwkv8.rwkv8_forward(*fargs)
+        if ev is not None:
+            ev[1].record(stream)
+        rc2 = rwkv8.rwkv8_backward(*bargs)
+        if ev is not None:
+            ev[2].record(stream)
+        if rc or rc2:
+            raise RuntimeError(wkv7.last_error())
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    events = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clocks:
+        start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        start.record(stream)
+        for k in range(args.steps):
+            step(events[k])
+        end.record(stream)
+        torch.cuda.synchronize()
+    if dist:
+        dist.barrier()
+    ms = reduce_max(start.elapsed_time(end) / args.steps, dist, dev)
+    fwd_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in events)
+    bwd_ms = statistics.mean(e[1].elapsed_time(e[2]) for e in events)
+
+    e2e = None
+    if not args.no_e2e:
+        host_in = {k: torch.from_numpy(d[k]).pin_memory() for k in ("q", "v", "dy")}
+        host_out = {k: torch.empty(x.shape, dtype=torch.float32).pin_memory() for k, x in g.items()}
+        host_y = torch.empty(y.shape, dtype=torch.float32).pin_memory()
+        h2d = sum(x.numel() * 4 for x in host_in.values())
+        d2h = sum(x.numel() * 4 for x in host_out.values()) + host_y.numel() * 4
+
+        def e2e_step():
+            for k in host_in:
+                t_in[k].copy_(host_in[k], non_blocking=True)
+            step()
+            host_y.copy_(y, non_blocking=True)
+            for k in g:
+                host_out[k].copy_(g[k], non_blocking=True)
+
+        e2e_step()
+        torch.cuda.synchronize()
+        n = max(1, min(args.steps, 5))
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(n):
+            e2e_step()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        e2e = (reduce_max(e0.elapsed_time(e1) / n, dist, dev), h2d, d2h)
+    if rank != 0:
+        return 0
+
+    peaks = _peaks()
+    BTH = B * T * H
+    f_flop, b_flop, f_bytes, b_bytes = _rwkv8_work_per_token_head(L, E)
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    peak_flops = sms * FP32_LANES_PER_SM * 2 * peaks["sm_max_mhz"] * 1e6
+    achieved = b_flop * BTH / (bwd_ms * 1e-3)
+    t_roof = max((f_flop + b_flop) * BTH / peak_flops, (f_bytes + b_bytes) * BTH / (peaks["hbm_gbs"] * 1e9))
+    traffic = None
+    if RWKV8_TRAFFIC["sha256"] and sources_sha256(RWKV8_TRAFFIC["sources"]) == RWKV8_TRAFFIC["sha256"]:
+        traffic = RWKV8_TRAFFIC["bytes_per_token_head"] * BTH
+    line = {
+        "metric": RWKV8_METRIC, "value": aggregate_tokens_per_s(world, B, T, ms), "unit": "tokens/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "arithmetic": "fp32 FFMA on the CUDA cores throughout",
+        "config": {"workload": "rwkv8-4x4096x32-l64e64-f32" if T == RWKV8_SHAPE["T"] else f"rwkv8 (T={T})", **sh,
+                   "ckpt_every": 16,
+                   "l2": "no flush: inputs, checkpoints and gradients (%.1f GB) exceed the 129 MB L2"
+                         % ((3 * BTH * 64 * 4 + ckpt.numel() * 4 + 3 * BTH * 64 * 4) / 1e9)},
+        "fwd_ms": fwd_ms, "bwd_ms": bwd_ms, "step_roofline_frac": t_roof / (ms * 1e-3),
+        "roofline": {"bound": "alu", "achieved": achieved / 1e12, "peak": peak_flops / 1e12, "unit": "TFLOP/s",
+                     "frac": achieved / peak_flops, "traffic": traffic, "kernel": RWKV8_TRAFFIC["kernel"],
+                     "note": "the backward call timed with CUDA events around it: algorithmic FLOP of the "
+                             "recurrence (12 L E per token-head) against the FP32 CUDA-core peak",
+                     "peak_source": f"{sms} SMs x {FP32_LANES_PER_SM} FP32 lanes x 2 x {peaks['sm_max_mhz']:.0f} MHz",
+                     "hbm_gbs_achieved": b_bytes * BTH / (bwd_ms * 1e-3) / 1e9, "hbm_peak_gbs": peaks["hbm_gbs"]},
+        "e2e": None if e2e is None else {
+            "value": aggregate_tokens_per_s(world, B, T, e2e[0]), "unit": "tokens/s", "h2d_bytes_per_step": e2e[1],
+            "d2h_bytes_per_step": e2e[2]},
+        "gpu_launches": (2 if Hv == H else 3) * args.steps + args.steps,
+        "clocks": clocks.summary(),
+    }
+    if not args.no_cpu_baseline and T == RWKV8_SHAPE["T"]:
+        heads = 16
+        v, dt = _rwkv8_oracle_sample(d, heads, T)
+        line["cpu_baseline"] = {"value": v, "unit": "tokens/s", "cores": 1, "kind": "oracle",
+                                "sample": f"{heads} of {B * H} heads, full T={T}, fwd+bwd fp64 ({dt:.1f} s, numpy)"}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -399,7 +606,11 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true", help="skip the timed oracle sample")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end measurement")
     ap.add_argument("--T", type=int, default=0, help="override T (profiler captures of a smaller case)")
+    ap.add_argument("--workload", choices=["wkv7", "rwkv8"], default="wkv7",
+                    help="wkv7: the RWKV-7 1.5B-shaped layer (default); rwkv8: the RWKV-8 recurrence")
     args = ap.parse_args()
+    if args.workload == "rwkv8":
+        return run_rwkv8(args)
     if args.impl == "reference":
         return run_reference(args)
     return run_gpu(args)

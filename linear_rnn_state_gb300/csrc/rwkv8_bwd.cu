@@ -71,6 +71,29 @@ __device__ __forceinline__ void cp_async16(void* dst, const void* src) {
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
 __device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
 
+// Sum of a 4 x 4 tile over the four lanes that share it (lane bits 3 and 4,
+// kq = lane >> 3), leaving row kq of the sum in `out`: a reduce-scatter in two
+// exchange steps instead of an all-reduce of all sixteen values.
+__device__ __forceinline__ void reduce_scatter4(const float (&a)[4][4], int kq, float (&out)[4]) {
+  const bool hi = (kq & 2) != 0;
+  float k2[2][4];
+#pragma unroll
+  for (int ii = 0; ii < 2; ++ii)
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const float keep = hi ? a[2 + ii][j] : a[ii][j];
+      const float send = hi ? a[ii][j] : a[2 + ii][j];
+      k2[ii][j] = keep + __shfl_xor_sync(0xffffffffu, send, 16);
+    }
+  const bool odd = (kq & 1) != 0;
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const float keep = odd ? k2[1][j] : k2[0][j];
+    const float send = odd ? k2[0][j] : k2[1][j];
+    out[j] = keep + __shfl_xor_sync(0xffffffffu, send, 8);
+  }
+}
+
 __device__ __forceinline__ float dot4(const float4 a, const float4 b) {
   return fmaf(a.x, b.x, fmaf(a.y, b.y, fmaf(a.z, b.z, a.w * b.w)));
 }
@@ -140,7 +163,7 @@ __device__ __forceinline__ void chunk_elements(BwdSmem& sm, int buf, int l, int 
       if (s > tau) G = fmaf(pcol[s - 1 - tau] * ucol[s], sm.M[s][tau], G);
     if (tau < len) G = fmaf(sm.pw[len - 1 - tau][l], wv, G);
     const float n = sm.NB[tau][l];
-    const float g = R / (n + kEps);
+    const float g = __fdividef(R, n + kEps);  // denominator >= 1e-6
     gq[j] = g;
     gv[j] = G;
     nb[j] = n;
@@ -313,22 +336,14 @@ __global__ void __launch_bounds__(kThreads, 1) rwkv8_bwd_kernel(const Args a) {
             aw[i][j] += dot4(vv[i], gv[j]);
           }
       }
-#pragma unroll
-      for (int i = 0; i < 4; ++i)
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          ar[i][j] += __shfl_xor_sync(0xffffffffu, ar[i][j], 8);
-          ar[i][j] += __shfl_xor_sync(0xffffffffu, ar[i][j], 16);
-          aw[i][j] += __shfl_xor_sync(0xffffffffu, aw[i][j], 8);
-          aw[i][j] += __shfl_xor_sync(0xffffffffu, aw[i][j], 16);
-        }
-      // lane group kq stores row 4 rt + kq
+      // lane group kq keeps and stores row 4 rt + kq
+      float vr[4], vw[4];
+      reduce_scatter4(ar, kq, vr);
+      reduce_scatter4(aw, kq, vw);
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
-        const float vr = kq == 0 ? ar[0][j] : kq == 1 ? ar[1][j] : kq == 2 ? ar[2][j] : ar[3][j];
-        const float vw = kq == 0 ? aw[0][j] : kq == 1 ? aw[1][j] : kq == 2 ? aw[2][j] : aw[3][j];
-        sm.R0[4 * rt + kq][ec + 16 * j] = vr;
-        sm.W[4 * rt + kq][ec + 16 * j] = vw;
+        sm.R0[4 * rt + kq][ec + 16 * j] = vr[j];
+        sm.W[4 * rt + kq][ec + 16 * j] = vw[j];
       }
     }
     {
@@ -354,7 +369,7 @@ __global__ void __launch_bounds__(kThreads, 1) rwkv8_bwd_kernel(const Args a) {
         const int tau = 4 * seg + j;
         const float nbv = fmaf(sm.pw[j][l_s], start, loc[j]);
         const float sq = sm.sqp[0][tau] + sm.sqp[1][tau] + kEps;
-        const float u = x[j] / (sq * (nbv + kEps));
+        const float u = __fdividef(x[j], sq * (nbv + kEps));  // denominator >= 1e-12
         sm.NB[tau][l_s] = nbv;
         sm.U[tau][l_s] = u;
         sm.Ut[tau][l_s] = u * sm.pw[tau][l_s];
@@ -429,15 +444,7 @@ __global__ void __launch_bounds__(kThreads, 1) rwkv8_bwd_kernel(const Args a) {
           }
         }
       }
-#pragma unroll
-      for (int i = 0; i < 4; ++i)
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          acc[i][j] += __shfl_xor_sync(0xffffffffu, acc[i][j], 8);
-          acc[i][j] += __shfl_xor_sync(0xffffffffu, acc[i][j], 16);
-        }
-#pragma unroll
-      for (int j = 0; j < 4; ++j) dv4[j] = kq == 0 ? acc[0][j] : kq == 1 ? acc[1][j] : kq == 2 ? acc[2][j] : acc[3][j];
+      reduce_scatter4(acc, kq, dv4);
     }
     __syncthreads();  // A, g_n and the row sums complete; every read of G done
 
@@ -450,8 +457,9 @@ __global__ void __launch_bounds__(kThreads, 1) rwkv8_bwd_kernel(const Args a) {
     }
     {
       const int tau = 4 * rt + kq;
+      // A[s][tau] is zero for s <= tau; the warp's rows start at 4 rt
 #pragma unroll 4
-      for (int s = 0; s < kC; ++s) {
+      for (int s = 4 * rt + 1; s < kC; ++s) {
         const float al = sm.A[s][tau];
         const float4 dd = *reinterpret_cast<const float4*>(&sm.dys[buf][s][4 * ec]);
         dv4[0] = fmaf(al, dd.x, dv4[0]);

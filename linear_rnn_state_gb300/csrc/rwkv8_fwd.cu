@@ -55,6 +55,29 @@ __device__ __forceinline__ void cp_async16(void* dst, const void* src) {
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
 __device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
 
+// Sum of a 4 x 4 tile over the four lanes that share it (lane bits 3 and 4,
+// kq = lane >> 3), leaving row kq of the sum in `out`: a reduce-scatter in two
+// exchange steps instead of an all-reduce of all sixteen values.
+__device__ __forceinline__ void reduce_scatter4(const float (&a)[4][4], int kq, float (&out)[4]) {
+  const bool hi = (kq & 2) != 0;
+  float k2[2][4];
+#pragma unroll
+  for (int ii = 0; ii < 2; ++ii)
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const float keep = hi ? a[2 + ii][j] : a[ii][j];
+      const float send = hi ? a[ii][j] : a[2 + ii][j];
+      k2[ii][j] = keep + __shfl_xor_sync(0xffffffffu, send, 16);
+    }
+  const bool odd = (kq & 1) != 0;
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const float keep = odd ? k2[1][j] : k2[0][j];
+    const float send = odd ? k2[0][j] : k2[1][j];
+    out[j] = keep + __shfl_xor_sync(0xffffffffu, send, 8);
+  }
+}
+
 // Copies chunk `c` of q and v into buffer `buf`; rows past the end of the
 // sequence are zero-filled. Each thread moves one 16-byte piece of each.
 __device__ __forceinline__ void load_chunk(FwdSmem& sm, int buf, const float* qh, const float* vh, int c, int T,
@@ -179,7 +202,7 @@ __global__ void __launch_bounds__(kThreads, 1) rwkv8_fwd_kernel(const Args a) {
         const int tau = 4 * seg + j;
         const float nb = fmaf(sm.pw[j][l_s], start, loc[j]);
         const float sq = sm.sqp[0][tau] + sm.sqp[1][tau] + kEps;
-        const float u = x[j] / (sq * (nb + kEps));
+        const float u = __fdividef(x[j], sq * (nb + kEps));  // denominator >= 1e-12
         sm.U[tau][l_s] = u;
         sm.UtT[l_s][tau] = u * sm.pw[tau][l_s];
         sm.Qt[tau][l_s] = tau < len ? x[j] * sm.pw[len - 1 - tau][l_s] : 0.f;
@@ -226,23 +249,16 @@ __global__ void __launch_bounds__(kThreads, 1) rwkv8_fwd_kernel(const Args a) {
 #pragma unroll
         for (int j = 0; j < 4; ++j) acc[i][j] = fmaf(uu[i], ss[j], acc[i][j]);
     }
-#pragma unroll
-    for (int i = 0; i < 4; ++i)
-#pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        acc[i][j] += __shfl_xor_sync(0xffffffffu, acc[i][j], 8);
-        acc[i][j] += __shfl_xor_sync(0xffffffffu, acc[i][j], 16);
-      }
+    float yv[4];
+    reduce_scatter4(acc, kq, yv);
     __syncthreads();  // A complete; every read of rho0 done
 
     // ---- phase 4: y = readout + A v, then rho <- d^len rho + Qt^T v
     {
       const int tau = 4 * rt + kq;
-      float yv[4];
-#pragma unroll
-      for (int j = 0; j < 4; ++j) yv[j] = kq == 0 ? acc[0][j] : kq == 1 ? acc[1][j] : kq == 2 ? acc[2][j] : acc[3][j];
+      // A[tau][s] is zero for s >= tau; the warp's rows end at 4 rt + 3
 #pragma unroll 4
-      for (int s = 0; s < kC; ++s) {
+      for (int s = 0; s < 4 * rt + 3; ++s) {
         const float al = sm.A[tau][s];
         const float4 vv = *reinterpret_cast<const float4*>(&sm.vs[buf][s][4 * ec]);
         yv[0] = fmaf(al, vv.x, yv[0]);
