@@ -404,8 +404,8 @@ RWKV8_SHAPE = {"B": 4, "T": 4096, "H": 32, "Hv": 32, "L": 64, "E": 64}
 RWKV8_TRAFFIC = {
     "kernel": "rwkv8_bwd_kernel (one rwkv8_backward call)",
     "sources": ("rwkv8_bwd.cu", "rwkv8_launch.h"),
-    "sha256": "dacfc9de14f0afc7bc640910bc0341364b06d62de03e3da0b3199eb485f6c91e",
-    "bytes_per_token_head": (237.072128e6 + 49.760512e6) / 131072,
+    "sha256": "bbac91591701afffdac1b01fa81faf7c6f74bd9ac4bb72866b2e99791fcc8ecf",
+    "bytes_per_token_head": (237.090304e6 + 49.826304e6) / 131072,
 }
 
 
