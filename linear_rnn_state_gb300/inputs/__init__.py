@@ -54,6 +54,8 @@ def _load():
         dp = ctypes.POINTER(ctypes.c_double)
         lib.rwkv8_gen_inputs.argtypes = [ctypes.c_uint64] + [i] * 6 + [dp] * 6 + [ctypes.c_double] + [dp] * 2 + [i]
         lib.rwkv8_gen_inputs.restype = i
+        lib.wkv7_gen_logits.argtypes = [ctypes.c_uint64, i, i, i, i, i, vp]
+        lib.wkv7_gen_logits.restype = i
         _lib = lib
     return _lib
 
@@ -78,6 +80,17 @@ def generate(B: int, T: int, H: int, N: int, storage: str = "f64", s_init_std: f
         raise RuntimeError(f"wkv7_gen_inputs failed with status {rc}")
     out["s_init"] = s_init
     return out
+
+
+def generate_logits(B: int, T: int, H: int, N: int, storage: str = "f64", seed: int = 0) -> np.ndarray:
+    """The decay logits z [B][T][H][N] behind generate()'s w (same seed):
+    w = exp(-0.606531 sigmoid(z)). bf16 storage returns uint16 bit patterns."""
+    lib = _load()
+    z = np.empty((B, T, H, N), dtype=NP_STORAGE[storage])
+    rc = lib.wkv7_gen_logits(ctypes.c_uint64(seed), B, T, H, N, KIND[storage], z.ctypes.data_as(ctypes.c_void_p))
+    if rc != 0:
+        raise RuntimeError(f"wkv7_gen_logits failed with status {rc}")
+    return z
 
 
 def bf16_bits_to_f64(u16: np.ndarray) -> np.ndarray:

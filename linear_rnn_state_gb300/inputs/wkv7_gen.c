@@ -281,3 +281,16 @@ int rwkv8_gen_inputs(uint64_t seed, int B, int T, int H, int Hv, int L, int E, d
   rc |= rwkv8_fill(seed, base, d_rho_norm_final, nn, 0, 1.0, nthreads);
   return rc ? -1 : 0;
 }
+
+/*
+ * The decay logits z [B][T][H][N] behind the w that wkv7_gen_inputs draws
+ * (stream 3 of the same seed: w = exp(-0.606531 sigmoid(z)) there), rounded
+ * once to the requested storage kind, for callers that pass the decay as
+ * logits. Returns 0, or -2 on an invalid argument.
+ */
+int wkv7_gen_logits(uint64_t seed, int B, int T, int H, int N, int kind, void *z) {
+  if (B <= 0 || T <= 0 || H <= 0 || N <= 0 || N > 256 || kind < 0 || kind > 2 || !z) return -2;
+  const uint64_t M = (uint64_t)B * T * H * N;
+  for (uint64_t f = 0; f < M; ++f) store(z, kind, (size_t)f, wkv7_gen_normal_at(seed, 3 * M + f));
+  return 0;
+}

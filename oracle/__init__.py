@@ -144,3 +144,34 @@ def backward(*args, **kw):
 
 def backward_heads(*args, **kw):
     return _get().backward_heads(*args, **kw)
+
+
+# ----------------------------------------------- decay given as logits ---
+# The RWKV-7 time-mix ("rx_pretrain.c", tm_pre_forward) forms the decay from a
+# logit z (its w0 + tanh(shw w1) w2) as w = exp(-RX_WDECAY_COEFF * sigmoid(z)),
+# and its backward turns dw into the logit's gradient through
+# dsig = dw * w * (-RX_WDECAY_COEFF), dz = dsig * sigmoid(z) * (1 - sigmoid(z)).
+# These two functions are that chain around the scan, in float64.
+
+WDECAY_COEFF = 0.606531  # RX_WDECAY_COEFF of "rx_pretrain.c"
+
+
+def decay_from_logit(z):
+    """w = exp(-0.606531 * sigmoid(z)), elementwise, float64."""
+    z = np.asarray(z, dtype=np.float64)
+    return np.exp(-WDECAY_COEFF / (1.0 + np.exp(-z)))
+
+
+def forward_logit(r, z, k, v, a, b, s_init=None, **kw):
+    """forward() with the decay given as logits z."""
+    return forward(r, decay_from_logit(z), k, v, a, b, s_init, **kw)
+
+
+def backward_logit(r, z, k, v, a, b, dy, s_init=None, dS_final=None, **kw):
+    """backward() with the decay given as logits z: returns dz in place of dw."""
+    z = np.asarray(z, dtype=np.float64)
+    w = decay_from_logit(z)
+    g = backward(r, w, k, v, a, b, dy, s_init, dS_final, **kw)
+    sig = 1.0 / (1.0 + np.exp(-z))
+    g["dz"] = g.pop("dw") * w * (-WDECAY_COEFF) * sig * (1.0 - sig)
+    return g
