@@ -33,9 +33,10 @@ FP32_LANES_PER_SM = 128  # Blackwell SM: 4 partitions x 32 FP32 lanes
 # change to any of them makes the report carry null instead.
 TRAFFIC = {
     "kernel": "wkv7_bwd4_carry_kernel + wkv7_bwd4_out_kernel (one wkv7_backward_bf16 call)",
-    "sources": ("wkv7_bwd4.cu", "wkv7_common.cuh", "wkv7_scaled.cuh", "wkv7_mma.cuh", "wkv7_launch.h"),
-    "sha256": "fb18ca88265d753a1257bcc936b0a530a54b591d18b244b14116a2d543dd89db",
-    "bytes_per_token_head": (83.964416e6 + 28.879104e6 + 318.864128e6 + 165.230592e6) / 131072,
+    "sources": ("wkv7_bwd4.cu", "wkv7_common.cuh", "wkv7_scaled.cuh", "wkv7_mma.cuh", "wkv7_launch.h",
+                "wkv7_decay.cuh"),
+    "sha256": "aecc441d270f7a7a20b07d5b4e11eb03b7295a981ac7e4814d56ecefa08a8163",
+    "bytes_per_token_head": (83.991552e6 + 28.238080e6 + 318.861568e6 + 161.771776e6) / 131072,
 }
 
 
@@ -242,6 +243,9 @@ def run_gpu(args):
     C = wkv7.wkv7_default_ckpt_every(N, bf16)
     names = ("r", "w", "k", "v", "a", "b", "dy")
     d = inputs.generate(B, T, H, N, wl.storage, wl.s_init_std, seed=shard_seed(rank))
+    logit = args.workload == "wkv7-logit"  # the decay given as logits z, w formed in the kernels
+    if logit:
+        d["w"] = inputs.generate_logits(B, T, H, N, wl.storage, seed=shard_seed(rank))
 
     def to_dev(x):
         t = torch.from_numpy(x)
@@ -263,6 +267,11 @@ def run_gpu(args):
                                                            C, B, T, H, N, sp]
     bwd_args = [t_in[n].data_ptr() for n in names] + [None, ckpt.data_ptr(), C] + [
         grads[n].data_ptr() for n in ("dr", "dw", "dk", "dv", "da", "db")] + [dS.data_ptr(), B, T, H, N, sp]
+    if logit:
+        if not (bf16 and N == 64 and C == 16):
+            raise RuntimeError("the decay-logit workload needs bf16 inputs, N = 64 and 16-step checkpoints")
+        fwd, bwd = wkv7.wkv7_forward_logit_bf16, wkv7.wkv7_backward_logit_bf16
+        bwd_args = bwd_args[:8] + [None] + bwd_args[8:]  # dS_final: none
 
     def step(ev=None):
         if ev is not None:
@@ -355,7 +364,8 @@ def _report(args, wl, world, B, T, H, N, C, bf16, ms, fwd_ms, bwd_ms, e2e, ckpt,
     achieved = b_flop * BTH / (bwd_ms * 1e-3)
     t_roof = max((f_flop + b_flop) * BTH / peak_flops, (f_bytes + b_bytes) * BTH / (peaks["hbm_gbs"] * 1e9))
     value = aggregate_tokens_per_s(world, B, T, ms)
-    cpu_v, cpu_cores, cpu_P, cpu_dt = cpu_baseline_sample(wl, d, B * H) if not args.no_cpu_baseline and T == wl.T \
+    with_cpu = not args.no_cpu_baseline and T == wl.T and args.workload == "wkv7"  # the oracle takes w, not logits
+    cpu_v, cpu_cores, cpu_P, cpu_dt = cpu_baseline_sample(wl, d, B * H) if with_cpu \
         else (None, 0, 0, 0.0)
     line = {
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
@@ -365,7 +375,8 @@ def _report(args, wl, world, B, T, H, N, C, bf16, ms, fwd_ms, bwd_ms, e2e, ckpt,
                        "carry chain, bf16 operands in the backward's per-chunk gradient products; fp32 state, carry "
                        "and element-wise math" if (bf16 and N == 64) else "fp32 throughout")
                       + "; inputs, dy and y stored in " + wl.storage,
-        "config": {"workload": wl.name if T == wl.T else f"{wl.name} (T={T})", "B": B, "T": T, "H": H, "N": N, "storage": wl.storage, "ckpt_every": C,
+        "config": {"workload": (wl.name + ("-decay-logits" if args.workload == "wkv7-logit" else ""))
+                   if T == wl.T else f"{wl.name} (T={T})", "B": B, "T": T, "H": H, "N": N, "storage": wl.storage, "ckpt_every": C,
                    "l2": "no flush: inputs, checkpoints and gradients (%.1f GB) exceed the 129 MB L2"
                          % ((7 * BTH * N * (2 if bf16 else 4) + ckpt.numel() * 4 + 6 * BTH * N * 4) / 1e9)},
         "fwd_ms": fwd_ms, "bwd_ms": bwd_ms, "step_roofline_frac": t_roof / (ms * 1e-3),
@@ -606,8 +617,9 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true", help="skip the timed oracle sample")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end measurement")
     ap.add_argument("--T", type=int, default=0, help="override T (profiler captures of a smaller case)")
-    ap.add_argument("--workload", choices=["wkv7", "rwkv8"], default="wkv7",
-                    help="wkv7: the RWKV-7 1.5B-shaped layer (default); rwkv8: the RWKV-8 recurrence")
+    ap.add_argument("--workload", choices=["wkv7", "wkv7-logit", "rwkv8"], default="wkv7",
+                    help="wkv7: the RWKV-7 1.5B-shaped layer (default); wkv7-logit: the same with the decay "
+                         "given as logits and formed inside the kernels; rwkv8: the RWKV-8 recurrence")
     args = ap.parse_args()
     if args.workload == "rwkv8":
         return run_rwkv8(args)

@@ -140,6 +140,28 @@ int wkv7_backward_segment_bf16(const wkv7_bf16* r, const wkv7_bf16* w, const wkv
                                float* dk, float* dv, float* da, float* db, float* dS_init, int B, int T, int H,
                                int N, void* stream);
 
+/*
+ * The decay given as logits (bfloat16 inputs, N = 64, 16-step checkpoints).
+ * The RWKV-7 time-mix ("rx_pretrain.c", tm_pre_forward) forms the decay from a
+ * logit z as w = exp(-0.606531 sigmoid(z)) (RX_WDECAY_COEFF); these calls take
+ * z [B][T][H][N] in the place of w and form w in fp32 inside the scan kernels
+ * where the decay tile is read, so w never exists in memory. The backward
+ * returns dz = dL/dz (its backward's chain dw w (-0.606531) sigmoid(z)
+ * (1 - sigmoid(z))) in the place of dw, and always runs the split chunked form
+ * (WKV7_SPLIT_BACKWARD is not read). Other arguments, layouts, workspaces and
+ * status codes as wkv7_forward_bf16 and wkv7_backward_segment_bf16; N other
+ * than 64, or checkpoints with an interval other than 16, return
+ * WKV7_ERR_INVALID.
+ */
+int wkv7_forward_logit_bf16(const wkv7_bf16* r, const wkv7_bf16* z, const wkv7_bf16* k, const wkv7_bf16* v,
+                            const wkv7_bf16* a, const wkv7_bf16* b, const float* s_init, wkv7_bf16* y,
+                            float* s_final, float* ckpt, int ckpt_every, int B, int T, int H, int N, void* stream);
+int wkv7_backward_logit_bf16(const wkv7_bf16* r, const wkv7_bf16* z, const wkv7_bf16* k, const wkv7_bf16* v,
+                             const wkv7_bf16* a, const wkv7_bf16* b, const wkv7_bf16* dy, const float* s_init,
+                             const float* dS_final, const float* ckpt, int ckpt_every, float* dr, float* dz,
+                             float* dk, float* dv, float* da, float* db, float* dS_init, int B, int T, int H, int N,
+                             void* stream);
+
 /* Bytes of the checkpoint buffer: B*H*ceil(T/ckpt_every)*N*N*4, or 0 for an
  * invalid size. */
 size_t wkv7_ckpt_bytes(int B, int T, int H, int N, int ckpt_every);

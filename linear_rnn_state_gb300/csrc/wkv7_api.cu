@@ -158,10 +158,12 @@ int status_word(unsigned** out) {
 // ------------------------------------------------------------ forward ---
 
 int forward_impl(bool bf16, const void* const in[6], const float* s_init, void* y, float* s_final,
-                 float* ckpt, int C, int B, int T, int H, int N, cudaStream_t stream) {
+                 float* ckpt, int C, int B, int T, int H, int N, cudaStream_t stream, bool logit = false) {
   int rc = check_dims(B, T, H, N);
   if (rc) return rc;
   if (ckpt && C < 1) return fail(WKV7_ERR_INVALID, "ckpt_every must be >= 1 (got %d)", C);
+  if (logit && (N != 64 || (ckpt && C != kChunk)))
+    return fail(WKV7_ERR_INVALID, "decay logits need N = 64 and ckpt_every = %d (got N = %d, %d)", kChunk, N, C);
   const size_t es = bf16 ? 2 : 4;
   const size_t vec = (size_t)B * T * H * N * es;
   const size_t st = (size_t)B * H * N * N * 4;
@@ -192,6 +194,7 @@ int forward_impl(bool bf16, const void* const in[6], const float* s_init, void* 
   args.y = y;
   args.s_final = s_final;
   args.ckpt = ckpt;
+  args.w_logit = logit ? 1 : 0;
   args.C = ckpt ? C : 1;
   args.nck = ckpt ? (T + C - 1) / C : 0;
   args.B = B;
@@ -205,11 +208,14 @@ int forward_impl(bool bf16, const void* const in[6], const float* s_init, void* 
 // ----------------------------------------------------------- backward ---
 
 int backward_impl(bool bf16, const void* const in[7], const float* s_init, const float* dS_final, const float* ckpt,
-                  int C, float* const grads[6], float* dS_init, int B, int T, int H, int N, cudaStream_t stream) {
+                  int C, float* const grads[6], float* dS_init, int B, int T, int H, int N, cudaStream_t stream,
+                  bool logit = false) {
   int rc = check_dims(B, T, H, N);
   if (rc) return rc;
   if (ckpt && C < 1) return fail(WKV7_ERR_INVALID, "ckpt_every must be >= 1 (got %d)", C);
   const int C_eff = ckpt ? C : (C >= 1 ? C : bwd2_steps_per_window(N, bf16));
+  if (logit && (N != 64 || C_eff != kChunk))
+    return fail(WKV7_ERR_INVALID, "decay logits need N = 64 and ckpt_every = %d (got N = %d, %d)", kChunk, N, C_eff);
   const size_t es = bf16 ? 2 : 4;
   const size_t vec = (size_t)B * T * H * N * es;
   const size_t gvec = (size_t)B * T * H * N * 4;
@@ -241,7 +247,8 @@ int backward_impl(bool bf16, const void* const in[7], const float* s_init, const
   // WKV7_SPLIT_BACKWARD=0, the fused one (one CTA per head).
   const bool chunked = bf16 && N == 64 && C_eff == kChunk;
   const char* split_env = std::getenv("WKV7_SPLIT_BACKWARD");
-  const bool split = chunked && !(split_env && split_env[0] == '0');
+  // decay logits run only in the split form
+  const bool split = chunked && (logit || !(split_env && split_env[0] == '0'));
   const size_t ck_ws = ckpt ? 0 : (ckpt_bytes(B, T, H, N, C_eff) + 255) / 256 * 256;
   const size_t ws_bytes = ck_ws + (split ? bwd4_workspace_bytes(B, T, H) : 0);
   if (ws_bytes) {
@@ -280,6 +287,7 @@ int backward_impl(bool bf16, const void* const in[7], const float* s_init, const
     fa.y = nullptr;
     fa.s_final = nullptr;
     fa.ckpt = ws;
+    fa.w_logit = logit ? 1 : 0;
     fa.C = C_eff;
     fa.nck = (T + C_eff - 1) / C_eff;
     fa.B = B;
@@ -308,6 +316,7 @@ int backward_impl(bool bf16, const void* const in[7], const float* s_init, const
   args.db = grads[5];
   args.dS_init = dS_init;
   args.dS_final = dS_final;
+  args.w_logit = logit ? 1 : 0;
   args.carry = split ? ws + ck_ws / sizeof(float) : nullptr;
   for (int v = 0; v < 7; ++v) args.in[v] = in[v];
   args.C = C_eff;
@@ -505,6 +514,25 @@ int wkv7_backward_bf16(const wkv7_bf16* r, const wkv7_bf16* w, const wkv7_bf16* 
   float* const grads[6] = {dr, dw, dk, dv, da, db};
   return backward_impl(true, in, s_init, nullptr, ckpt, ckpt_every, grads, dS_init, B, T, H, N,
                        static_cast<cudaStream_t>(stream));
+}
+
+int wkv7_forward_logit_bf16(const wkv7_bf16* r, const wkv7_bf16* z, const wkv7_bf16* k, const wkv7_bf16* v,
+                            const wkv7_bf16* a, const wkv7_bf16* b, const float* s_init, wkv7_bf16* y,
+                            float* s_final, float* ckpt, int ckpt_every, int B, int T, int H, int N, void* stream) {
+  const void* in[6] = {r, z, k, v, a, b};
+  return forward_impl(true, in, s_init, y, s_final, ckpt, ckpt_every, B, T, H, N,
+                      static_cast<cudaStream_t>(stream), true);
+}
+
+int wkv7_backward_logit_bf16(const wkv7_bf16* r, const wkv7_bf16* z, const wkv7_bf16* k, const wkv7_bf16* v,
+                             const wkv7_bf16* a, const wkv7_bf16* b, const wkv7_bf16* dy, const float* s_init,
+                             const float* dS_final, const float* ckpt, int ckpt_every, float* dr, float* dz,
+                             float* dk, float* dv, float* da, float* db, float* dS_init, int B, int T, int H, int N,
+                             void* stream) {
+  const void* in[7] = {r, z, k, v, a, b, dy};
+  float* const grads[6] = {dr, dz, dk, dv, da, db};
+  return backward_impl(true, in, s_init, dS_final, ckpt, ckpt_every, grads, dS_init, B, T, H, N,
+                       static_cast<cudaStream_t>(stream), true);
 }
 
 size_t wkv7_ckpt_bytes(int B, int T, int H, int N, int ckpt_every) {

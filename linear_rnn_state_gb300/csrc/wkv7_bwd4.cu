@@ -41,6 +41,7 @@
 // All products run on tf32 tensor cores (mma.sync m16n8k8) with fp32
 // accumulation. A chunk whose decays leave [1/16, 16] (or hold a NaN) is run
 // step by step in fp32 by both kernels.
+#include "wkv7_decay.cuh"
 #include "wkv7_launch.h"
 #include "wkv7_mma.cuh"
 #include "wkv7_scaled.cuh"
@@ -249,6 +250,7 @@ struct CarrySmem {
 // running products c(t) are taken per block of four steps and the blocks'
 // products chained in step order. Returns (uniformly over the group) whether
 // some decay leaves the range of the scaled form.
+template <bool kLogit>
 __device__ bool form_carry(ScratchC& sc, float (&Pc)[4][kN], const __nv_bfloat16* rs, OpC& op, int len, int ftid) {
   const int lane = ftid & 31, pf = ftid >> 5, j = 2 * lane, t0 = 4 * pf;
   float2 wv[4], av[4], rv[4], bv[4], dyv[4];
@@ -257,7 +259,7 @@ __device__ bool form_carry(ScratchC& sc, float (&Pc)[4][kN], const __nv_bfloat16
 #pragma unroll
   for (int e = 0; e < 4; ++e) {
     const int o = (t0 + e) * kN + j;
-    wv[e] = t0 + e < len ? bf2(rs + C_W * kTile + o) : make_float2(1.f, 1.f);
+    wv[e] = t0 + e < len ? decay_value2<kLogit>(bf2(rs + C_W * kTile + o)) : make_float2(1.f, 1.f);
     safe &= decay_is_safe(wv[e].x) && decay_is_safe(wv[e].y);
     pb = fmul2(pb, wv[e]);
   }
@@ -320,6 +322,7 @@ __device__ __forceinline__ void gram_tile(float* M, const float* P, const float*
 
 // Forming group: wait for a chunk's inputs and form its operands. Returns
 // false on a timeout.
+template <bool kLogit>
 __device__ bool front_form(CarrySmem& sm, ScratchC& sc, OpC& op, const __nv_bfloat16* rs, uint64_t* bar,
                            uint32_t parity, int len, unsigned* status) {
   const int ftid = threadIdx.x - 128;
@@ -328,7 +331,7 @@ __device__ bool front_form(CarrySmem& sm, ScratchC& sc, OpC& op, const __nv_bflo
     if (ftid == 0) sm.abort_flag = 1;
     return false;
   }
-  const bool unsafe = form_carry(sc, sm.Pc, rs, op, len, ftid);
+  const bool unsafe = form_carry<kLogit>(sc, sm.Pc, rs, op, len, ftid);
   if (ftid == 0) op.unsafe = unsafe;
   if (unsafe) return true;
   named_bar(1, 128);
@@ -444,6 +447,7 @@ __device__ __forceinline__ void carry_chunk(float (&G)[8][4], const OpC& op, int
 
 // The same chunk step by step in fp32 (a chunk outside the scaled form's
 // range): G += dy r^T ; dsa = G b ; G <- G diag(w) + dsa a^T.
+template <bool kLogit>
 __device__ void carry_direct(float (&G)[8][4], const __nv_bfloat16* rs, int len, int i0, int g, int t4) {
   for (int t = len - 1; t >= 0; --t) {
     const __nv_bfloat16* row = rs + t * kN;
@@ -465,7 +469,7 @@ __device__ void carry_direct(float (&G)[8][4], const __nv_bfloat16* rs, int len,
 #pragma unroll
     for (int nt = 0; nt < 8; ++nt) {
       const int col = 8 * nt + 2 * t4;
-      const float2 w = bf2(row + C_W * kTile + col), a = bf2(row + C_A * kTile + col);
+      const float2 w = decay_value2<kLogit>(bf2(row + C_W * kTile + col)), a = bf2(row + C_A * kTile + col);
       G[nt][0] = fmaf(ds0, a.x, G[nt][0] * w.x);
       G[nt][1] = fmaf(ds0, a.y, G[nt][1] * w.y);
       G[nt][2] = fmaf(ds1, a.x, G[nt][2] * w.x);
@@ -484,6 +488,7 @@ __device__ __forceinline__ void flush_carry(const bf16_t* src, bf16_t* dst, int 
   }
 }
 
+template <bool kLogit>
 __global__ void __launch_bounds__(kCarryThreads, 1) wkv7_bwd4_carry_kernel(const __grid_constant__ BwdArgs args) {
   extern __shared__ __align__(128) unsigned char smem_raw[];
   CarrySmem& sm = *reinterpret_cast<CarrySmem*>(smem_raw);
@@ -511,7 +516,7 @@ __global__ void __launch_bounds__(kCarryThreads, 1) wkv7_bwd4_carry_kernel(const
   int waited = 0, issued = 0;
   auto form = [&](int v) {  // forming group; false on a timeout
     const int c = chunk_of(v);
-    if (!front_form(sm, sm.sc[c & 1], sm.op[c % 3], sm.raw[v % kCarryStages][0], &sm.full[v % kCarryStages],
+    if (!front_form<kLogit>(sm, sm.sc[c & 1], sm.op[c % 3], sm.raw[v % kCarryStages][0], &sm.full[v % kCarryStages],
                     (v / kCarryStages) & 1, len_of(v), args.status))
       return false;
     waited = v + 1;
@@ -575,7 +580,7 @@ __global__ void __launch_bounds__(kCarryThreads, 1) wkv7_bwd4_carry_kernel(const
         *reinterpret_cast<uint32_t*>(dst + (i0 + g + 8) * 72 + col) = pack_bf16(G[nt][2], G[nt][3]);
       }
       if (op.unsafe)
-        carry_direct(G, sm.raw[st][0], len_of(m), i0, g, t4);
+        carry_direct<kLogit>(G, sm.raw[st][0], len_of(m), i0, g, t4);
       else
         carry_chunk(G, op, i0, g, t4);
     } else if (role == 1) {
@@ -653,6 +658,7 @@ struct OutSmem {
 // rows 8 w .. 8 w + 7 of the state and the carry, lane (g, t) row 8 w + g and
 // columns 8 nt + 2 t, + 1): the carry starts at the stored Gc, S_prev of step
 // t is recomputed from the checkpoint (fp32, read from global memory).
+template <bool kLogit>
 __device__ void out_direct(OutSmem& sm, const float* S0, const bf16_t* Gcg, int len, const BwdArgs& args, size_t base,
                            size_t vstep, int warp, int lane) {
   const int g = lane >> 2, t4 = lane & 3, i = 8 * warp + g, tid = threadIdx.x;
@@ -689,7 +695,8 @@ __device__ void out_direct(OutSmem& sm, const float* S0, const bf16_t* Gcg, int 
 #pragma unroll
       for (int nt = 0; nt < 8; ++nt) {
         const int col = 8 * nt + 2 * t4;
-        const float2 w = bf2(row + V_W * RS + col), k = bf2(row + V_K * RS + col), b = bf2(row + V_B * RS + col);
+        const float2 w = decay_value2<kLogit>(bf2(row + V_W * RS + col)), k = bf2(row + V_K * RS + col),
+                     b = bf2(row + V_B * RS + col);
         sp[nt][0] = fmaf(sa, b.x, fmaf(sp[nt][0], w.x, v * k.x));
         sp[nt][1] = fmaf(sa, b.y, fmaf(sp[nt][1], w.y, v * k.y));
       }
@@ -701,7 +708,7 @@ __device__ void out_direct(OutSmem& sm, const float* S0, const bf16_t* Gcg, int 
 #pragma unroll
     for (int nt = 0; nt < 8; ++nt) {
       const int col = 8 * nt + 2 * t4;
-      const float2 w = bf2(row + V_W * RS + col), k = bf2(row + V_K * RS + col);
+      const float2 w = decay_value2<kLogit>(bf2(row + V_W * RS + col)), k = bf2(row + V_K * RS + col);
       const float2 b = bf2(row + V_B * RS + col), r = bf2(row + V_R * RS + col);
       const float wv[2] = {w.x, w.y}, kv[2] = {k.x, k.y}, bv[2] = {b.x, b.y}, rv[2] = {r.x, r.y};
 #pragma unroll
@@ -725,7 +732,7 @@ __device__ void out_direct(OutSmem& sm, const float* S0, const bf16_t* Gcg, int 
 #pragma unroll
     for (int nt = 0; nt < 8; ++nt) {
       const int col = 8 * nt + 2 * t4;
-      const float2 w = bf2(row + V_W * RS + col), a = bf2(row + V_A * RS + col);
+      const float2 w = decay_value2<kLogit>(bf2(row + V_W * RS + col)), a = bf2(row + V_A * RS + col);
       const float wv[2] = {w.x, w.y}, av[2] = {a.x, a.y};
 #pragma unroll
       for (int e = 0; e < 2; ++e) {
@@ -741,6 +748,12 @@ __device__ void out_direct(OutSmem& sm, const float* S0, const bf16_t* Gcg, int 
 #pragma unroll
       for (int w8 = 0; w8 < 8; ++w8) x += red[(w8 * 5 + q) * kN + col];
       float* dst = q == 0 ? args.dr : q == 1 ? args.dk : q == 2 ? args.db : q == 3 ? args.dw : args.da;
+      if constexpr (kLogit) {
+        if (q == 3) {  // dL/dz from dL/dw
+          const float z = bf(rs + V_W * RS + t * kB64 + col);
+          x = logit_grad_from_wdw(x * decay_value<true>(z), z);
+        }
+      }
       dst[base + (size_t)t * vstep + col] = x;
     }
     __syncthreads();
@@ -773,6 +786,7 @@ __device__ __forceinline__ void cp_async16_zfill(void* dst, const void* src, boo
                : "memory");
 }
 
+template <bool kLogit>
 __global__ void __launch_bounds__(kThreads, 3) wkv7_bwd4_out_kernel(const __grid_constant__ BwdArgs args) {
   extern __shared__ __align__(128) unsigned char smem_raw[];
   OutSmem& sm = *reinterpret_cast<OutSmem*>(smem_raw);
@@ -817,12 +831,13 @@ __global__ void __launch_bounds__(kThreads, 3) wkv7_bwd4_out_kernel(const __grid
     const int j = 2 * lane, ta = 2 * warp;
     float2 wv[2];
 #pragma unroll
-    for (int e = 0; e < 2; ++e) wv[e] = ta + e < len ? bf2(rs + V_W * RS + (ta + e) * kB64 + j) : make_float2(1.f, 1.f);
+    for (int e = 0; e < 2; ++e)
+      wv[e] = ta + e < len ? decay_value2<kLogit>(bf2(rs + V_W * RS + (ta + e) * kB64 + j)) : make_float2(1.f, 1.f);
     const bool safe = decay_is_safe(wv[0].x) && decay_is_safe(wv[0].y) && decay_is_safe(wv[1].x) &&
                       decay_is_safe(wv[1].y);
     *reinterpret_cast<float2*>(&sm.Ppart[warp][j]) = fmul2(wv[0], wv[1]);
     if (__syncthreads_or(!safe)) {
-      out_direct(sm, S0g, Gcg, len, args, base, vstep, warp, lane);
+      out_direct<kLogit>(sm, S0g, Gcg, len, args, base, vstep, warp, lane);
       return;
     }
     float2 cL = make_float2(1.f, 1.f), cpre = cL;  // cpre = c(ta - 1)
@@ -1161,7 +1176,11 @@ __global__ void __launch_bounds__(kThreads, 3) wkv7_bwd4_out_kernel(const __grid
       const int t = upper ? kL - 1 - e : e;
       const float x = XK[t * kLD64 + col] + XR[t * kLD64 + col];
       if (upper) run += x;  // end anchor plus the x of the steps from t on
-      const float v = (run - XA[t * kLD64 + col]) * rcp_approx(bf(rs + V_W * RS + t * kB64 + col));
+      float v;
+      if constexpr (kLogit)  // dL/dz straight from w dw: no division by w
+        v = logit_grad_from_wdw(run - XA[t * kLD64 + col], bf(rs + V_W * RS + t * kB64 + col));
+      else
+        v = (run - XA[t * kLD64 + col]) * rcp_approx(bf(rs + V_W * RS + t * kB64 + col));
       if (t < len) args.dw[base + (size_t)t * vstep + col] = v;
       if (!upper) run -= x;  // start anchor minus the x of the steps before t
     }
@@ -1175,18 +1194,24 @@ size_t bwd4_workspace_bytes(int B, int T, int H) {
   return heads * nchunks * kN * kN * sizeof(__nv_bfloat16);
 }
 
-cudaError_t launch_bwd4(const BwdArgs& args, cudaStream_t stream) {
+template <bool kLogit>
+cudaError_t launch_bwd4_impl(const BwdArgs& args, cudaStream_t stream) {
   const size_t smem_c = sizeof(CarrySmem), smem_o = sizeof(OutSmem);
-  cudaError_t e = cudaFuncSetAttribute(wkv7_bwd4_carry_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_c);
+  cudaError_t e =
+      cudaFuncSetAttribute(wkv7_bwd4_carry_kernel<kLogit>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_c);
   if (e != cudaSuccess) return e;
-  e = cudaFuncSetAttribute(wkv7_bwd4_out_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_o);
+  e = cudaFuncSetAttribute(wkv7_bwd4_out_kernel<kLogit>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_o);
   if (e != cudaSuccess) return e;
   const unsigned heads = (unsigned)(args.B * args.H), nchunks = (unsigned)((args.T + kL - 1) / kL);
-  wkv7_bwd4_carry_kernel<<<heads, kCarryThreads, smem_c, stream>>>(args);
+  wkv7_bwd4_carry_kernel<kLogit><<<heads, kCarryThreads, smem_c, stream>>>(args);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  wkv7_bwd4_out_kernel<<<heads * nchunks, kThreads, smem_o, stream>>>(args);
+  wkv7_bwd4_out_kernel<kLogit><<<heads * nchunks, kThreads, smem_o, stream>>>(args);
   return cudaGetLastError();
+}
+
+cudaError_t launch_bwd4(const BwdArgs& args, cudaStream_t stream) {
+  return args.w_logit ? launch_bwd4_impl<true>(args, stream) : launch_bwd4_impl<false>(args, stream);
 }
 
 }  // namespace wkv7

@@ -27,6 +27,7 @@
 // Operand blocks rotate over three buffers.
 // A chunk whose decays leave [1/16, 16] (or hold a NaN) is run step by step
 // in the direct form by the state warps, in fp32.
+#include "wkv7_decay.cuh"
 #include "wkv7_launch.h"
 #include "wkv7_mma.cuh"
 #include "wkv7_scaled.cuh"
@@ -47,6 +48,7 @@ struct Prep3 {
   float M[4][kL * kLD16];    // Mka, Mba (strictly lower), Mkr, Mbr (lower) [t][s]
   float Tinv[kL * kLD16];    // (I - Mba)^-1                              [t][s]
   float cL[kN];              // c(L) (fp32)
+  float ph[2][kN];           // decay logits: product of each half's 8 decays
   int unsafe;
   int pad_[31];
 };
@@ -73,6 +75,7 @@ __device__ __forceinline__ float2 bf2(const __nv_bfloat16* p) {
 // ---------------------------------------------------------- forming group ---
 // 128 threads; thread (j = ptid % 64, half = ptid / 64) forms column j of
 // steps 8*half .. 8*half+7.
+template <bool kLogit>
 __device__ void form_chunk(Fwd3Smem& sm, Prep3& P, float* X2, int stage, int len, int ptid) {
   const __nv_bfloat16* rs = sm.raw[stage][0];
   const int j = ptid & 63, half = ptid >> 6;
@@ -82,8 +85,8 @@ __device__ void form_chunk(Fwd3Smem& sm, Prep3& P, float* X2, int stage, int len
   const int tm = 8 * half, to = 8 - tm;
 #pragma unroll
   for (int e = 0; e < 8; ++e) {
-    wm[e] = tm + e < len ? bf(rs + V_W * kL * kN + (tm + e) * kN + j) : 1.f;
-    wo[e] = to + e < len ? bf(rs + V_W * kL * kN + (to + e) * kN + j) : 1.f;
+    wm[e] = tm + e < len ? decay_value<kLogit>(bf(rs + V_W * kL * kN + (tm + e) * kN + j)) : 1.f;
+    if constexpr (!kLogit) wo[e] = to + e < len ? bf(rs + V_W * kL * kN + (to + e) * kN + j) : 1.f;
   }
   float av[8], rv[8], kv[8], bv[8], vt[8];
 #pragma unroll
@@ -102,7 +105,14 @@ __device__ void form_chunk(Fwd3Smem& sm, Prep3& P, float* X2, int stage, int len
 #pragma unroll
   for (int e = 0; e < 8; ++e) {
     pm *= wm[e];
-    po *= wo[e];
+    if constexpr (!kLogit) po *= wo[e];
+  }
+  if constexpr (kLogit) {
+    // each half forms its own decays once (three MUFU operations per logit)
+    // and takes the other half's product from shared memory
+    P.ph[half][j] = pm;
+    named_bar(1, 128);
+    po = P.ph[half ^ 1][j];
   }
   const float p_first = half ? po : pm;  // w(1)...w(8), multiplied in step order
   const float cL = half ? po * pm : pm * po;
@@ -329,6 +339,7 @@ __device__ void state_chunk(StateCtx& c, Fwd3Smem& sm, const Prep3& P) {
 }
 
 // Chunk in the direct form (any decay), fp32 on the CUDA cores.
+template <bool kLogit>
 __device__ void state_chunk_direct(StateCtx& c, Fwd3Smem& sm, int stage, int len) {
   const int g = c.g, t4 = c.t4, i0 = c.i0;
   const __nv_bfloat16* rs = sm.raw[stage][0];
@@ -350,7 +361,7 @@ __device__ void state_chunk_direct(StateCtx& c, Fwd3Smem& sm, int stage, int len
 #pragma unroll
     for (int nt = 0; nt < 8; ++nt) {
       const int col = 8 * nt + 2 * t4;
-      const float2 w = bf2(row + V_W * kL * kN + col), k = bf2(row + V_K * kL * kN + col);
+      const float2 w = decay_value2<kLogit>(bf2(row + V_W * kL * kN + col)), k = bf2(row + V_K * kL * kN + col);
       const float2 b = bf2(row + V_B * kL * kN + col), r = bf2(row + V_R * kL * kN + col);
       c.S[nt][0] = fmaf(s0, b.x, fmaf(c.S[nt][0], w.x, v0 * k.x));
       c.S[nt][1] = fmaf(s0, b.y, fmaf(c.S[nt][1], w.y, v0 * k.y));
@@ -370,6 +381,7 @@ __device__ void state_chunk_direct(StateCtx& c, Fwd3Smem& sm, int stage, int len
   }
 }
 
+template <bool kLogit>
 __global__ void __launch_bounds__(kThreads, 1) wkv7_fwd3_kernel(const __grid_constant__ FwdArgs args) {
   extern __shared__ __align__(128) unsigned char smem_raw[];
   Fwd3Smem& sm = *reinterpret_cast<Fwd3Smem*>(smem_raw);
@@ -437,7 +449,7 @@ __global__ void __launch_bounds__(kThreads, 1) wkv7_fwd3_kernel(const __grid_con
       return;
     }
     waited = chunk + 1;
-    form_chunk(sm, sm.prep[chunk % 3], sm.X2[chunk & 1], chunk % kStages, chunk_len(chunk), ftid);
+    form_chunk<kLogit>(sm, sm.prep[chunk % 3], sm.X2[chunk & 1], chunk % kStages, chunk_len(chunk), ftid);
   };
   auto grams = [&](int chunk) {
     Prep3& P = sm.prep[chunk % 3];
@@ -474,7 +486,7 @@ __global__ void __launch_bounds__(kThreads, 1) wkv7_fwd3_kernel(const __grid_con
       if (ck_head && t0 % args.C == 0) stage_state(c, sm.ck[n & 1]);
       c.yb = n & 1;
       if (P.unsafe)
-        state_chunk_direct(c, sm, n % kStages, len);
+        state_chunk_direct<kLogit>(c, sm, n % kStages, len);
       else
         state_chunk(c, sm, P);
     }
@@ -505,12 +517,18 @@ __global__ void __launch_bounds__(kThreads, 1) wkv7_fwd3_kernel(const __grid_con
 
 }  // namespace
 
-cudaError_t launch_fwd3(const FwdArgs& args, cudaStream_t stream) {
+template <bool kLogit>
+cudaError_t launch_fwd3_impl(const FwdArgs& args, cudaStream_t stream) {
   const size_t smem = sizeof(Fwd3Smem);
-  cudaError_t e = cudaFuncSetAttribute(wkv7_fwd3_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  cudaError_t e =
+      cudaFuncSetAttribute(wkv7_fwd3_kernel<kLogit>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  wkv7_fwd3_kernel<<<(unsigned)(args.B * args.H), kThreads, smem, stream>>>(args);
+  wkv7_fwd3_kernel<kLogit><<<(unsigned)(args.B * args.H), kThreads, smem, stream>>>(args);
   return cudaGetLastError();
+}
+
+cudaError_t launch_fwd3(const FwdArgs& args, cudaStream_t stream) {
+  return args.w_logit ? launch_fwd3_impl<true>(args, stream) : launch_fwd3_impl<false>(args, stream);
 }
 
 }  // namespace wkv7

@@ -19,6 +19,7 @@ struct FwdArgs {
   float* s_final;       // [B][H][N][N] or null
   float* ckpt;          // [B][H][nck][N][N] or null
   unsigned* status;     // device status word (timeout flag)
+  int w_logit = 0;      // 1: the w tiles hold logits z, w = exp(-0.606531 sigmoid(z)) (chunked kernels only)
   int C;                // checkpoint interval (steps)
   int nck;              // ceil(T / C)
   int B, T, H;
@@ -41,6 +42,7 @@ struct BwdArgs {
   const void* in[7];  // r, w, k, v, a, b, dy ([B][T][H][N], the input type)
   void* carry;        // split backward: [B*H][nchunks][N][N] carry after each chunk (bf16)
   unsigned* status;
+  int w_logit = 0;    // 1: the w tiles hold logits z and dw receives dL/dz (split backward only)
   int C, nck;
   int B, T, H;
 };

@@ -29,6 +29,8 @@ EXPORTS = {
     "wkv7_status": 1,
     "wkv7_last_error": 0,
     "wkv7_backward_noalloc": 20,
+    "wkv7_forward_logit_bf16": 16,
+    "wkv7_backward_logit_bf16": 23,
 }
 
 
@@ -70,6 +72,10 @@ def load(path: str | None = None):
     lib.wkv7_last_error.restype = ctypes.c_char_p
     lib.wkv7_backward_noalloc.argtypes = [vp] * 15 + [i] * 4 + [vp]
     lib.wkv7_backward_noalloc.restype = i
+    lib.wkv7_forward_logit_bf16.argtypes = [vp] * 10 + [i] * 5 + [vp]
+    lib.wkv7_forward_logit_bf16.restype = i
+    lib.wkv7_backward_logit_bf16.argtypes = [vp] * 10 + [i] + [vp] * 7 + [i] * 4 + [vp]
+    lib.wkv7_backward_logit_bf16.restype = i
     if path is None:
         _lib = lib
     return lib
@@ -127,6 +133,18 @@ def wkv7_backward_noalloc(r, w, k, v, a, b, dy, s_init, dr, dw, dk, dv, da, db, 
     calls that overlap on the GPU race on the shared scratch."""
     return load().wkv7_backward_noalloc(r, w, k, v, a, b, dy, s_init, dr, dw, dk, dv, da, db, dS_init,
                                         B, T, H, N, stream)
+
+
+def wkv7_forward_logit_bf16(r, z, k, v, a, b, s_init, y, s_final, ckpt, ckpt_every, B, T, H, N, stream):
+    """wkv7_forward_logit_bf16 (include/wkv7.h): the decay given as logits z."""
+    return load().wkv7_forward_logit_bf16(r, z, k, v, a, b, s_init, y, s_final, ckpt, ckpt_every, B, T, H, N, stream)
+
+
+def wkv7_backward_logit_bf16(r, z, k, v, a, b, dy, s_init, dS_final, ckpt, ckpt_every, dr, dz, dk, dv, da, db,
+                             dS_init, B, T, H, N, stream):
+    """wkv7_backward_logit_bf16 (include/wkv7.h): returns dz in the place of dw."""
+    return load().wkv7_backward_logit_bf16(r, z, k, v, a, b, dy, s_init, dS_final, ckpt, ckpt_every, dr, dz, dk, dv,
+                                           da, db, dS_init, B, T, H, N, stream)
 
 
 def wkv7_ckpt_bytes(B, T, H, N, ckpt_every) -> int:
@@ -201,6 +219,37 @@ def backward(r, w, k, v, a, b, dy, s_init=None, ckpt=None, ckpt_every: int = 0, 
     fn = wkv7_backward_segment_bf16 if bf16 else wkv7_backward_segment
     _check(fn(*(_addr(x) for x in (r, w, k, v, a, b, dy, s_init, dS_final, ckpt)), ckpt_every,
               *(_addr(g[n]) for n in ("dr", "dw", "dk", "dv", "da", "db", "dS_init")), B, T, H, N, _stream(stream)))
+    return g
+
+
+def forward_logit(r, z, k, v, a, b, s_init=None, *, want_ckpt: bool = True, stream=None):
+    """forward() with the decay given as logits z (bfloat16 tensors, N = 64):
+    w = exp(-0.606531 sigmoid(z)) is formed inside the kernels. Returns
+    (y, s_final, ckpt, 16)."""
+    import torch
+
+    B, T, H, N = r.shape
+    dev = r.device
+    y = torch.empty_like(r)
+    s_final = torch.empty((B, H, N, N), dtype=torch.float32, device=dev)
+    ckpt = torch.empty((B, H, (T + 15) // 16, N, N), dtype=torch.float32, device=dev) if want_ckpt else None
+    _check(wkv7_forward_logit_bf16(*(_addr(x) for x in (r, z, k, v, a, b, s_init, y, s_final, ckpt)), 16, B, T, H, N,
+                                   _stream(stream)))
+    return y, s_final, ckpt, 16
+
+
+def backward_logit(r, z, k, v, a, b, dy, s_init=None, ckpt=None, *, dS_final=None, stream=None):
+    """backward() with the decay given as logits z: returns dict dr, dz, dk,
+    dv, da, db and dS_init."""
+    import torch
+
+    B, T, H, N = r.shape
+    dev = r.device
+    g = {n: torch.empty((B, T, H, N), dtype=torch.float32, device=dev) for n in ("dr", "dz", "dk", "dv", "da", "db")}
+    g["dS_init"] = torch.empty((B, H, N, N), dtype=torch.float32, device=dev)
+    _check(wkv7_backward_logit_bf16(*(_addr(x) for x in (r, z, k, v, a, b, dy, s_init, dS_final, ckpt)), 16,
+                                    *(_addr(g[n]) for n in ("dr", "dz", "dk", "dv", "da", "db", "dS_init")), B, T, H,
+                                    N, _stream(stream)))
     return g
 
 

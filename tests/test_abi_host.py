@@ -126,3 +126,17 @@ def test_empty_problems_need_no_device(lib):
     # T == 0 without a final state / dS_init to write
     assert lib.wkv7_forward(*([None] * 10), 4, 2, 0, 3, 16, None) == lib.OK
     assert lib.wkv7_backward(*([None] * 9), 4, *([None] * 7), 2, 0, 3, 16, None) == lib.OK
+
+
+def test_logit_entries_reject_unsupported_shapes(lib):
+    """The decay-as-logits calls run only the N = 64, 16-step chunked kernels."""
+    fwd = _fwd_args(N=32, C=16)
+    assert lib.wkv7_forward_logit_bf16(*fwd) == lib.ERR_INVALID
+    assert "logits" in lib.last_error()
+    fwd = _fwd_args(N=64, C=8)
+    assert lib.wkv7_forward_logit_bf16(*fwd) == lib.ERR_INVALID
+    ptrs = [FAKE + i * 64 * MB for i in range(17)]
+    bwd = ptrs[:10] + [8] + ptrs[10:17] + [1, 8, 1, 64, None]
+    assert lib.wkv7_backward_logit_bf16(*bwd) == lib.ERR_INVALID
+    bwd = ptrs[:10] + [16] + ptrs[10:17] + [1, 8, 1, 32, None]
+    assert lib.wkv7_backward_logit_bf16(*bwd) == lib.ERR_INVALID
