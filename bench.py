@@ -91,6 +91,15 @@ def reduce_max(value: float, dist, device=None) -> float:
     return t.item()
 
 
+def allreduce_param_grad(t, dist):
+    """Sum of a parameter gradient over ranks (in place); identity on one
+    process. The RWKV-8 decay is one parameter shared by every batch row, so
+    ranks that shard the batch add their ddecay: the path's one exchange."""
+    if dist is not None:
+        dist.all_reduce(t, op=dist.ReduceOp.SUM)
+    return t
+
+
 def aggregate_tokens_per_s(world: int, B: int, T: int, ms_per_step: float) -> float:
     """Tokens of all ranks (each B*T per step) per second of the slowest rank."""
     return world * B * T / (ms_per_step * 1e-3)
@@ -492,6 +501,8 @@ def run_rwkv8(args):
     B, T, H, Hv, L, E = (sh[k] for k in ("B", "T", "H", "Hv", "L", "E"))
     d = inputs.generate_rwkv8(B, T, H, Hv, L, E, "f32", seed=shard_seed(rank))
     t_in = {k: torch.from_numpy(d[k]).to(dev) for k in ("q", "v", "decay", "dy")}
+    if dist:  # the decay is a parameter: one copy for every rank (rank 0's)
+        dist.broadcast(t_in["decay"], src=0)
     f32 = dict(dtype=torch.float32, device=dev)
     y = torch.empty((B, H, T, E), **f32)
     rf, nf = torch.empty((B, H, L, E), **f32), torch.empty((B, H, L), **f32)
@@ -513,6 +524,7 @@ def run_rwkv8(args):
         if ev is not None:
             ev[1].record(stream)
         rc2 = rwkv8.rwkv8_backward(*bargs)
+        allreduce_param_grad(g["ddecay"], dist)
         if ev is not None:
             ev[2].record(stream)
         if rc or rc2:

@@ -72,3 +72,52 @@ def test_single_process_reduction_is_identity():
     assert bench.reduce_max(3.5, None) == 3.5
     assert bench.aggregate_tokens_per_s(1, 4, 4096, 2.0) == pytest.approx(4 * 4096 / 2e-3)
     assert np.isfinite(bench.aggregate_tokens_per_s(8, 4, 4096, 1.0))
+
+
+def _rwkv8_worker(rank, world, port, q):
+    import torch
+    import torch.distributed as dist
+
+    sys.path.insert(0, ROOT)
+    import bench
+    from tests.test_rwkv8_oracle import load_oracle
+    from linear_rnn_state_gb300 import inputs
+
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port), RANK=str(rank), WORLD_SIZE=str(world))
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    try:
+        orc = load_oracle()
+        shards = [inputs.generate_rwkv8(1, 12, 2, 2, 4, 3, "f64", seed=bench.shard_seed(r)) for r in range(world)]
+        mine = shards[rank]
+        # the decay is one parameter: every rank draws the same one (seed 0's)
+        decay = shards[0]["decay"]
+        g = orc.backward(mine["q"], mine["v"], decay, mine["dy"])
+        t = torch.from_numpy(g["ddecay"].copy())
+        bench.allreduce_param_grad(t, dist)
+        full = {k: np.concatenate([sh[k] for sh in shards], axis=0) for k in ("q", "v", "dy")}
+        ref = orc.backward(full["q"], full["v"], decay, full["dy"])["ddecay"]
+        q.put((rank, float(np.abs(t.numpy() - ref).max()), float(np.abs(ref).max())))
+    finally:
+        dist.destroy_process_group()
+
+
+def test_rwkv8_decay_gradient_is_summed_over_batch_shards():
+    """Ranks that shard the batch add their ddecay; the sum equals the
+    gradient of the whole batch (ddecay is additive over batch rows)."""
+    import multiprocessing as mp
+    import socket
+
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        port = s.getsockname()[1]
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    procs = [ctx.Process(target=_rwkv8_worker, args=(r, 2, port, q)) for r in range(2)]
+    for p in procs:
+        p.start()
+    for p in procs:
+        p.join(timeout=120)
+        assert p.exitcode == 0
+    for _ in range(2):
+        rank, err, scale = q.get(timeout=10)
+        assert err <= 1e-12 * (1 + scale), (rank, err)
