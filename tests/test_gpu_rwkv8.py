@@ -160,3 +160,39 @@ def test_rwkv8_full_size_sampled(env):
             _close(f"{k} h={h}", g[k][sl].cpu().numpy(), g_ref[k])
         _close(f"ddecay h={h}", g["ddecay"][h:h + 1].cpu().numpy(), g_ref["ddecay"],
                float(np.abs(g_ref["ddecay"]).mean()))
+
+
+@pytest.mark.parametrize("case", ["decay_zero", "decay_one", "zero_query_rows", "mixed_decay"])
+def test_rwkv8_degenerate_inputs(env, case):
+    """Decay exactly 0 (only the previous step is seen) or 1 (plain prefix
+    sums), query rows of zeros (their weights are 0 / EPS = 0), and a decay
+    that mixes 0, 1 and tiny values across latents."""
+    orc, inputs, rwkv8 = env
+    B, T, H = 2, 40, 2
+    d = inputs.generate_rwkv8(B, T, H, H, 64, 64, "f32", state_std=0.1, boundary=True, seed=90)
+    if case == "decay_zero":
+        d["decay"][:] = 0.0
+    elif case == "decay_one":
+        d["decay"][:] = 1.0
+    elif case == "zero_query_rows":
+        d["q"][:, :, 5:9, :] = 0.0
+        d["q"][:, :, 20, :] = 0.0
+    else:
+        d["decay"][:, 0::3] = 0.0
+        d["decay"][:, 1::3] = 1.0
+        d["decay"][:, 2::6] = 1e-30
+    t = {k: _dev(x) for k, x in d.items()}
+    y, rf, nf, ck = rwkv8.forward(t["q"], t["v"], t["decay"], t["rho_init"], t["rho_norm_init"])
+    g = rwkv8.backward(t["q"], t["v"], t["decay"], t["dy"], t["rho_init"], t["rho_norm_init"], ck,
+                       d_rho_final=t["d_rho_final"], d_rho_norm_final=t["d_rho_norm_final"])
+    torch.cuda.synchronize()
+    o = {k: None if x is None else x.astype(np.float64) for k, x in d.items()}
+    y_ref, rf_ref, nf_ref = orc.forward(o["q"], o["v"], o["decay"], o["rho_init"], o["rho_norm_init"])
+    g_ref = orc.backward(o["q"], o["v"], o["decay"], o["dy"], o["rho_init"], o["rho_norm_init"], o["d_rho_final"],
+                         o["d_rho_norm_final"])
+    _close(f"y {case}", y.cpu().numpy(), y_ref)
+    _close(f"rho_final {case}", rf.cpu().numpy(), rf_ref)
+    _close(f"rho_norm_final {case}", nf.cpu().numpy(), nf_ref)
+    for k in ("dq", "dv", "d_rho_init", "d_rho_norm_init"):
+        _close(f"{k} {case}", g[k].cpu().numpy(), g_ref[k])
+    _close(f"ddecay {case}", g["ddecay"].cpu().numpy(), g_ref["ddecay"], float(np.abs(g_ref["ddecay"]).mean()))
