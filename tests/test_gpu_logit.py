@@ -112,3 +112,19 @@ def test_logit_full_size_sampled(env):
         _rel(f"s_final ({bi},{hi})", sf[bi:bi + 1, hi:hi + 1].cpu().numpy(), sf_ref)
         for n in ("dr", "dz", "dk", "dv", "da", "db"):
             _rel(f"{n} ({bi},{hi})", g[n][bi:bi + 1, :, hi:hi + 1].cpu().numpy(), g_ref[n])
+
+
+def test_logit_backward_ignores_the_fused_form_switch(env, monkeypatch):
+    """WKV7_SPLIT_BACKWARD=0 selects the fused backward for decays given as w;
+    the logit call runs the split form regardless, with the same results."""
+    _, inputs, wkv7 = env
+    d = _data(inputs, 1, 40, 2, seed=71, state=False)
+    t = {n: _dev(d[n]) for n in NAMES + ("dy",)}
+    _, _, ck, _ = wkv7.forward_logit(*(t[n] for n in NAMES))
+    monkeypatch.delenv("WKV7_SPLIT_BACKWARD", raising=False)
+    g1 = wkv7.backward_logit(*(t[n] for n in NAMES), t["dy"], None, ck)
+    monkeypatch.setenv("WKV7_SPLIT_BACKWARD", "0")
+    g2 = wkv7.backward_logit(*(t[n] for n in NAMES), t["dy"], None, ck)
+    wkv7.status()
+    for n in g1:
+        assert torch.equal(g1[n], g2[n]), n
