@@ -35,8 +35,8 @@ TRAFFIC = {
     "kernel": "wkv7_bwd4_carry_kernel + wkv7_bwd4_out_kernel (one wkv7_backward_bf16 call)",
     "sources": ("wkv7_bwd4.cu", "wkv7_common.cuh", "wkv7_scaled.cuh", "wkv7_mma.cuh", "wkv7_launch.h",
                 "wkv7_decay.cuh"),
-    "sha256": "aecc441d270f7a7a20b07d5b4e11eb03b7295a981ac7e4814d56ecefa08a8163",
-    "bytes_per_token_head": (83.991552e6 + 28.238080e6 + 318.861568e6 + 161.771776e6) / 131072,
+    "sha256": "2839c5c5fcca5f0eff6628780eaf6130067c1c34af703861af3059028417ef4f",
+    "bytes_per_token_head": (83.953664e6 + 28.174848e6 + 318.850048e6 + 162.109952e6) / 131072,
 }
 
 
@@ -281,6 +281,20 @@ def run_gpu(args):
             raise RuntimeError("the decay-logit workload needs bf16 inputs, N = 64 and 16-step checkpoints")
         fwd, bwd = wkv7.wkv7_forward_logit_bf16, wkv7.wkv7_backward_logit_bf16
         bwd_args = bwd_args[:8] + [None] + bwd_args[8:]  # dS_final: none
+    if args.workload == "wkv7-epilogue":
+        # the forward with the group-norm + bonus epilogue fused (out, nv and stats written);
+        # the backward call is the scan's alone (the epilogue's backward is not built)
+        import numpy as np
+
+        rng = np.random.default_rng(0)
+        epi_p = [torch.from_numpy(x.astype(np.float32)).to(dev) for x in (
+            rng.uniform(0.5, 1.5, (H, N)), 0.1 * rng.standard_normal((H, N)), 0.5 * rng.standard_normal((H, N)))]
+        nv = torch.empty_like(y)
+        stats = torch.empty((B, T, H, 2), dtype=torch.float32, device=dev)
+        fwd = wkv7.wkv7_forward_epilogue_bf16
+        fwd_args = fwd_args[:7] + [x.data_ptr() for x in epi_p] + [y.data_ptr(), nv.data_ptr(), stats.data_ptr(),
+                                                                    s_final.data_ptr(), ckpt.data_ptr(), C, 0, B, T,
+                                                                    H, N, sp]
 
     def step(ev=None):
         if ev is not None:
@@ -373,7 +387,7 @@ def _report(args, wl, world, B, T, H, N, C, bf16, ms, fwd_ms, bwd_ms, e2e, ckpt,
     achieved = b_flop * BTH / (bwd_ms * 1e-3)
     t_roof = max((f_flop + b_flop) * BTH / peak_flops, (f_bytes + b_bytes) * BTH / (peaks["hbm_gbs"] * 1e9))
     value = aggregate_tokens_per_s(world, B, T, ms)
-    with_cpu = not args.no_cpu_baseline and T == wl.T and args.workload == "wkv7"  # the oracle takes w, not logits
+    with_cpu = not args.no_cpu_baseline and T == wl.T and args.workload == "wkv7"  # the plain scan's oracle
     cpu_v, cpu_cores, cpu_P, cpu_dt = cpu_baseline_sample(wl, d, B * H) if with_cpu \
         else (None, 0, 0, 0.0)
     line = {
@@ -384,7 +398,8 @@ def _report(args, wl, world, B, T, H, N, C, bf16, ms, fwd_ms, bwd_ms, e2e, ckpt,
                        "carry chain, bf16 operands in the backward's per-chunk gradient products; fp32 state, carry "
                        "and element-wise math" if (bf16 and N == 64) else "fp32 throughout")
                       + "; inputs, dy and y stored in " + wl.storage,
-        "config": {"workload": (wl.name + ("-decay-logits" if args.workload == "wkv7-logit" else ""))
+        "config": {"workload": (wl.name + {"wkv7-logit": "-decay-logits", "wkv7-epilogue": "-fused-epilogue-forward"}.get(
+                       args.workload, ""))
                    if T == wl.T else f"{wl.name} (T={T})", "B": B, "T": T, "H": H, "N": N, "storage": wl.storage, "ckpt_every": C,
                    "l2": "no flush: inputs, checkpoints and gradients (%.1f GB) exceed the 129 MB L2"
                          % ((7 * BTH * N * (2 if bf16 else 4) + ckpt.numel() * 4 + 6 * BTH * N * 4) / 1e9)},
@@ -403,6 +418,12 @@ def _report(args, wl, world, B, T, H, N, C, bf16, ms, fwd_ms, bwd_ms, e2e, ckpt,
         "gpu_launches": (3 if (bf16 and N == 64) else 2) * args.steps,
         "clocks": clocks.summary(),
     }
+    if args.workload == "wkv7-epilogue":
+        line["note"] = ("forward with the group-norm + bonus epilogue fused (out, normalized y and per-row stats "
+                        "written in the place of y); the backward call is the scan's alone, the epilogue's backward "
+                        "is not built")
+    elif args.workload == "wkv7-logit":
+        line["note"] = "the decay given as logits z and formed inside the scan kernels; dz returned in the place of dw"
     if cpu_v is not None:
         line["cpu_baseline"] = {"value": cpu_v, "unit": "tokens/s", "cores": cpu_cores, "kind": "oracle",
                                 "sample": f"{cpu_P} of {B * H} (b,h) heads, full T={T}, fwd+bwd fp64 ({cpu_dt:.1f} s)"}
@@ -629,9 +650,11 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true", help="skip the timed oracle sample")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end measurement")
     ap.add_argument("--T", type=int, default=0, help="override T (profiler captures of a smaller case)")
-    ap.add_argument("--workload", choices=["wkv7", "wkv7-logit", "rwkv8"], default="wkv7",
+    ap.add_argument("--workload", choices=["wkv7", "wkv7-logit", "wkv7-epilogue", "rwkv8"], default="wkv7",
                     help="wkv7: the RWKV-7 1.5B-shaped layer (default); wkv7-logit: the same with the decay "
-                         "given as logits and formed inside the kernels; rwkv8: the RWKV-8 recurrence")
+                         "given as logits and formed inside the kernels; wkv7-epilogue: the forward with the "
+                         "group-norm + bonus epilogue fused (the backward call is the scan's alone); rwkv8: the "
+                         "RWKV-8 recurrence")
     args = ap.parse_args()
     if args.workload == "rwkv8":
         return run_rwkv8(args)

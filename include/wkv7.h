@@ -162,6 +162,28 @@ int wkv7_backward_logit_bf16(const wkv7_bf16* r, const wkv7_bf16* z, const wkv7_
                              float* dk, float* dv, float* da, float* db, float* dS_init, int B, int T, int H, int N,
                              void* stream);
 
+/*
+ * Forward with the time-mix epilogue fused into the scan ("rx_pretrain.c":
+ * gn_forward after rx_wkv7_forward_seq, and the bonus term): for every step
+ * and head, with y the scan's output row of N channels,
+ *     mean, var over the N channels;  rstd = 1 / sqrt(var + 64e-5)
+ *     bonus = sum_j r_j k_j r_k[j]
+ *     out = (y - mean) rstd ln_w + ln_b + bonus v
+ * bfloat16 inputs at N = 64 (16-step checkpoints if ckpt is given);
+ * decay_is_logit != 0 takes logits z in the place of w, as
+ * wkv7_forward_logit_bf16. ln_w, ln_b, r_k: [H][N] fp32 (required).
+ *   out    [B][T][H][N] bf16 (required; y itself is not written).
+ *   nv     [B][T][H][N] bf16 normalized y, (y - mean) rstd, or NULL.
+ *   stats  [B][T][H][2] fp32 (rstd, bonus) per row, or NULL.
+ * s_final and ckpt as wkv7_forward_bf16 (the scan's state, unchanged by the
+ * epilogue). N other than 64 returns WKV7_ERR_INVALID.
+ */
+int wkv7_forward_epilogue_bf16(const wkv7_bf16* r, const wkv7_bf16* w, const wkv7_bf16* k, const wkv7_bf16* v,
+                               const wkv7_bf16* a, const wkv7_bf16* b, const float* s_init, const float* ln_w,
+                               const float* ln_b, const float* r_k, wkv7_bf16* out, wkv7_bf16* nv, float* stats,
+                               float* s_final, float* ckpt, int ckpt_every, int decay_is_logit, int B, int T, int H,
+                               int N, void* stream);
+
 /* Bytes of the checkpoint buffer: B*H*ceil(T/ckpt_every)*N*N*4, or 0 for an
  * invalid size. */
 size_t wkv7_ckpt_bytes(int B, int T, int H, int N, int ckpt_every);

@@ -157,13 +157,23 @@ int status_word(unsigned** out) {
 
 // ------------------------------------------------------------ forward ---
 
+// The epilogue of wkv7_forward_epilogue_bf16 (null for the plain forward).
+struct Epilogue {
+  const float *ln_w, *ln_b, *r_k;
+  void* nv;
+  float* stats;
+};
+
 int forward_impl(bool bf16, const void* const in[6], const float* s_init, void* y, float* s_final,
-                 float* ckpt, int C, int B, int T, int H, int N, cudaStream_t stream, bool logit = false) {
+                 float* ckpt, int C, int B, int T, int H, int N, cudaStream_t stream, bool logit = false,
+                 const Epilogue* epi = nullptr) {
   int rc = check_dims(B, T, H, N);
   if (rc) return rc;
   if (ckpt && C < 1) return fail(WKV7_ERR_INVALID, "ckpt_every must be >= 1 (got %d)", C);
   if (logit && (N != 64 || (ckpt && C != kChunk)))
     return fail(WKV7_ERR_INVALID, "decay logits need N = 64 and ckpt_every = %d (got N = %d, %d)", kChunk, N, C);
+  if (epi && (N != 64 || (ckpt && C != kChunk)))
+    return fail(WKV7_ERR_INVALID, "the epilogue needs N = 64 and ckpt_every = %d (got N = %d, %d)", kChunk, N, C);
   const size_t es = bf16 ? 2 : 4;
   const size_t vec = (size_t)B * T * H * N * es;
   const size_t st = (size_t)B * H * N * N * 4;
@@ -184,6 +194,15 @@ int forward_impl(bool bf16, const void* const in[6], const float* s_init, void* 
   }
   rc = check_spans(ins, 7, outs, 3, 6, 0);
   if (rc) return rc;
+  if (epi) {
+    const size_t par = (size_t)H * N * 4;
+    const Span eins[10] = {ins[0], ins[1], ins[2], ins[3], ins[4], ins[5], ins[6],
+                           {epi->ln_w, par, "ln_w"}, {epi->ln_b, par, "ln_b"}, {epi->r_k, par, "r_k"}};
+    const Span eouts[5] = {outs[0], outs[1], outs[2], {epi->nv, vec, "nv"},
+                           {epi->stats, (size_t)B * T * H * 2 * 4, "stats"}};
+    if ((rc = check_spans(eins, 10, eouts, 5, 6, 1))) return rc;
+    if (!epi->ln_w || !epi->ln_b || !epi->r_k) return fail(WKV7_ERR_INVALID, "ln_w, ln_b and r_k are required");
+  }
 
   FwdArgs args;
   const int K = fwd_steps_per_stage(N, bf16);
@@ -195,6 +214,14 @@ int forward_impl(bool bf16, const void* const in[6], const float* s_init, void* 
   args.s_final = s_final;
   args.ckpt = ckpt;
   args.w_logit = logit ? 1 : 0;
+  if (epi) {
+    args.epilogue = 1;
+    args.ln_w = epi->ln_w;
+    args.ln_b = epi->ln_b;
+    args.r_k = epi->r_k;
+    args.nv = epi->nv;
+    args.stats = epi->stats;
+  }
   args.C = ckpt ? C : 1;
   args.nck = ckpt ? (T + C - 1) / C : 0;
   args.B = B;
@@ -522,6 +549,17 @@ int wkv7_forward_logit_bf16(const wkv7_bf16* r, const wkv7_bf16* z, const wkv7_b
   const void* in[6] = {r, z, k, v, a, b};
   return forward_impl(true, in, s_init, y, s_final, ckpt, ckpt_every, B, T, H, N,
                       static_cast<cudaStream_t>(stream), true);
+}
+
+int wkv7_forward_epilogue_bf16(const wkv7_bf16* r, const wkv7_bf16* w, const wkv7_bf16* k, const wkv7_bf16* v,
+                               const wkv7_bf16* a, const wkv7_bf16* b, const float* s_init, const float* ln_w,
+                               const float* ln_b, const float* r_k, wkv7_bf16* out, wkv7_bf16* nv, float* stats,
+                               float* s_final, float* ckpt, int ckpt_every, int decay_is_logit, int B, int T, int H,
+                               int N, void* stream) {
+  const void* in[6] = {r, w, k, v, a, b};
+  const Epilogue epi{ln_w, ln_b, r_k, nv, stats};
+  return forward_impl(true, in, s_init, out, s_final, ckpt, ckpt_every, B, T, H, N,
+                      static_cast<cudaStream_t>(stream), decay_is_logit != 0, &epi);
 }
 
 int wkv7_backward_logit_bf16(const wkv7_bf16* r, const wkv7_bf16* z, const wkv7_bf16* k, const wkv7_bf16* v,

@@ -58,6 +58,12 @@ struct Fwd3Smem {
   Prep3 prep[3];
   float X2[2][2 * kL * kLD64];  // per chunk in flight: rows 0..15: k~(s); rows 16..31: b~(s)   [s][j]
   __nv_bfloat16 ys[2][kL * kN];  // y of the chunk [t][i], on its way out (state warps write, products warps store)
+  // epilogue: the head's ln_w, ln_b, r_k; per chunk (ring of 4, written by the forming
+  // group two rounds before the state warps run the chunk, read by the products group the
+  // round after) the bonus partials of the two 32-column halves and the v rows
+  float epi[3][kN];
+  float epi_sp[4][2][kL];
+  __nv_bfloat16 epi_v[4][kL * kN];
   float ck[2][kN * kLD64];     // checkpoints on their way out (state warps write, products warps store)
   uint64_t full[4];
   int abort_flag;
@@ -75,8 +81,8 @@ __device__ __forceinline__ float2 bf2(const __nv_bfloat16* p) {
 // ---------------------------------------------------------- forming group ---
 // 128 threads; thread (j = ptid % 64, half = ptid / 64) forms column j of
 // steps 8*half .. 8*half+7.
-template <bool kLogit>
-__device__ void form_chunk(Fwd3Smem& sm, Prep3& P, float* X2, int stage, int len, int ptid) {
+template <bool kLogit, bool kEpi>
+__device__ void form_chunk(Fwd3Smem& sm, Prep3& P, float* X2, int stage, int len, int ptid, int eslot) {
   const __nv_bfloat16* rs = sm.raw[stage][0];
   const int j = ptid & 63, half = ptid >> 6;
   // decays of this thread's 8 steps (wm) and of the other 8 (wo); padding
@@ -97,6 +103,28 @@ __device__ void form_chunk(Fwd3Smem& sm, Prep3& P, float* X2, int stage, int len
     kv[e] = bf(rs + V_K * kL * kN + o);
     bv[e] = bf(rs + V_B * kL * kN + o);
     vt[e] = bf(rs + V_V * kL * kN + o);  // bf16 values are tf32 values
+  }
+  if constexpr (kEpi) {
+    // the epilogue's bonus sum_j r_j k_j r_k[j] of each step, over this warp's 32 columns,
+    // reduce-scattered over the lanes (lane bits 4, 3, 2 pick the step), and the v rows
+    const int lane = ptid & 31;
+    const float rk = sm.epi[2][j];
+    float p[8], q4[4], q2[2];
+#pragma unroll
+    for (int e = 0; e < 8; ++e) p[e] = rv[e] * kv[e] * rk;
+    const bool b4 = lane & 16, b3 = lane & 8, b2 = lane & 4;
+#pragma unroll
+    for (int u = 0; u < 4; ++u)
+      q4[u] = (b4 ? p[4 + u] : p[u]) + __shfl_xor_sync(0xffffffffu, b4 ? p[u] : p[4 + u], 16);
+#pragma unroll
+    for (int u = 0; u < 2; ++u)
+      q2[u] = (b3 ? q4[2 + u] : q4[u]) + __shfl_xor_sync(0xffffffffu, b3 ? q4[u] : q4[2 + u], 8);
+    float sum = (b2 ? q2[1] : q2[0]) + __shfl_xor_sync(0xffffffffu, b2 ? q2[0] : q2[1], 4);
+    sum += __shfl_xor_sync(0xffffffffu, sum, 2);
+    sum += __shfl_xor_sync(0xffffffffu, sum, 1);
+    if ((lane & 3) == 0) sm.epi_sp[eslot][j >> 5][tm + 4 * (b4 ? 1 : 0) + 2 * (b3 ? 1 : 0) + (b2 ? 1 : 0)] = sum;
+#pragma unroll
+    for (int e = 0; e < 8; ++e) sm.epi_v[eslot][(tm + e) * kN + j] = rs[V_V * kL * kN + (tm + e) * kN + j];
   }
   bool unsafe = false;
 #pragma unroll
@@ -381,7 +409,70 @@ __device__ void state_chunk_direct(StateCtx& c, Fwd3Smem& sm, int stage, int len
   }
 }
 
-template <bool kLogit>
+// The chunk's staged y rows through the time-mix epilogue ("rx_pretrain.c":
+// gn_forward and the bonus) to global memory: for every step t and head, with
+// mean and var over the N channels and rstd = 1 / sqrt(var + 64e-5),
+//   out = (y - mean) rstd ln_w + ln_b + (sum_j r_j k_j r_k[j]) v,
+// plus (y - mean) rstd to args.nv and (rstd, bonus) to args.stats when given.
+// The products group, eight threads per row (eight channels each); the bonus
+// partials and v rows were staged by the forming group.
+__device__ void flush_epilogue(const Fwd3Smem& sm, const FwdArgs& args, int m, size_t vbase, size_t vstep, int len,
+                               int ptid) {
+  const int t = ptid >> 3, i0 = 8 * (ptid & 7), es = m % 4;
+  auto load8 = [](const __nv_bfloat16* p, float (&x)[8]) {
+    const uint4 u = *reinterpret_cast<const uint4*>(p);
+    const uint32_t wv[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&wv[q]));
+      x[2 * q] = f.x;
+      x[2 * q + 1] = f.y;
+    }
+  };
+  float y[8], v[8];
+  load8(&sm.ys[m & 1][t * kN + i0], y);
+  load8(&sm.epi_v[es][t * kN + i0], v);
+  float sum = 0.f;
+#pragma unroll
+  for (int e = 0; e < 8; ++e) sum += y[e];
+#pragma unroll
+  for (int o = 1; o < 8; o <<= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+  const float mean = sum * (1.f / kN);
+  float sq = 0.f;
+#pragma unroll
+  for (int e = 0; e < 8; ++e) {
+    y[e] -= mean;
+    sq = fmaf(y[e], y[e], sq);
+  }
+#pragma unroll
+  for (int o = 1; o < 8; o <<= 1) sq += __shfl_xor_sync(0xffffffffu, sq, o);
+  const float rstd = rsqrtf(sq * (1.f / kN) + 64e-5f);
+  const float bon = sm.epi_sp[es][0][t] + sm.epi_sp[es][1][t];
+  uint32_t po[4], pn[4];
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    float o2[2], n2[2];
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const int e = 2 * q + h;
+      n2[h] = y[e] * rstd;
+      o2[h] = fmaf(n2[h], sm.epi[0][i0 + e], fmaf(bon, v[e], sm.epi[1][i0 + e]));
+    }
+    const __nv_bfloat162 bo = __floats2bfloat162_rn(o2[0], o2[1]), bn = __floats2bfloat162_rn(n2[0], n2[1]);
+    po[q] = *reinterpret_cast<const uint32_t*>(&bo);
+    pn[q] = *reinterpret_cast<const uint32_t*>(&bn);
+  }
+  if (t < len) {
+    const size_t off = vbase + ((size_t)m * kL + t) * vstep + i0;
+    *reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(args.y) + off) = make_uint4(po[0], po[1], po[2], po[3]);
+    if (args.nv)
+      *reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(args.nv) + off) = make_uint4(pn[0], pn[1], pn[2], pn[3]);
+    if (args.stats && (ptid & 7) == 0)
+      *reinterpret_cast<float2*>(args.stats + 2 * (off / kN)) = make_float2(rstd, bon);
+  }
+}
+
+template <bool kLogit, bool kEpi>
 __global__ void __launch_bounds__(kThreads, 1) wkv7_fwd3_kernel(const __grid_constant__ FwdArgs args) {
   extern __shared__ __align__(128) unsigned char smem_raw[];
   Fwd3Smem& sm = *reinterpret_cast<Fwd3Smem*>(smem_raw);
@@ -410,6 +501,12 @@ __global__ void __launch_bounds__(kThreads, 1) wkv7_fwd3_kernel(const __grid_con
     for (int ch = 0; ch < kStages && ch < nchunks; ++ch) issue(ch);
   }
   if (tid == 0) sm.abort_flag = 0;
+  if constexpr (kEpi) {
+    for (int i = tid; i < 3 * kN; i += kThreads) {
+      const float* src = i < kN ? args.ln_w : i < 2 * kN ? args.ln_b : args.r_k;
+      sm.epi[i / kN][i % kN] = src[(size_t)hi * kN + i % kN];
+    }
+  }
 
   StateCtx c;
   c.g = lane >> 2;
@@ -449,7 +546,8 @@ __global__ void __launch_bounds__(kThreads, 1) wkv7_fwd3_kernel(const __grid_con
       return;
     }
     waited = chunk + 1;
-    form_chunk<kLogit>(sm, sm.prep[chunk % 3], sm.X2[chunk & 1], chunk % kStages, chunk_len(chunk), ftid);
+    form_chunk<kLogit, kEpi>(sm, sm.prep[chunk % 3], sm.X2[chunk & 1], chunk % kStages, chunk_len(chunk), ftid,
+                             chunk % 4);
   };
   auto grams = [&](int chunk) {
     Prep3& P = sm.prep[chunk % 3];
@@ -478,7 +576,10 @@ __global__ void __launch_bounds__(kThreads, 1) wkv7_fwd3_kernel(const __grid_con
       if (n > 0) {
         if (ck_head && ((n - 1) * kL) % args.C == 0)
           flush_state(sm.ck[(n - 1) & 1], ck_head + (size_t)((n - 1) * kL / args.C) * kN * kN, gtid);
-        if (y) flush_y(sm.ys[(n - 1) & 1], y + vbase + (size_t)(n - 1) * kL * vstep, vstep, chunk_len(n - 1), gtid);
+        if constexpr (kEpi)
+          flush_epilogue(sm, args, n - 1, vbase, vstep, chunk_len(n - 1), gtid);
+        else if (y)
+          flush_y(sm.ys[(n - 1) & 1], y + vbase + (size_t)(n - 1) * kL * vstep, vstep, chunk_len(n - 1), gtid);
       }
     } else {
       const Prep3& P = sm.prep[n % 3];
@@ -510,25 +611,30 @@ __global__ void __launch_bounds__(kThreads, 1) wkv7_fwd3_kernel(const __grid_con
   if (role == 2 && nchunks > 0) {
     const int n = nchunks - 1;
     if (ck_head && (n * kL) % args.C == 0) flush_state(sm.ck[n & 1], ck_head + (size_t)(n * kL / args.C) * kN * kN, gtid);
-    if (y) flush_y(sm.ys[n & 1], y + vbase + (size_t)n * kL * vstep, vstep, chunk_len(n), gtid);
+    if constexpr (kEpi)
+      flush_epilogue(sm, args, n, vbase, vstep, chunk_len(n), gtid);
+    else if (y)
+      flush_y(sm.ys[n & 1], y + vbase + (size_t)n * kL * vstep, vstep, chunk_len(n), gtid);
   }
   if (role == 0 && args.s_final) store_state(c, args.s_final + (size_t)head * kN * kN);
 }
 
 }  // namespace
 
-template <bool kLogit>
+template <bool kLogit, bool kEpi>
 cudaError_t launch_fwd3_impl(const FwdArgs& args, cudaStream_t stream) {
   const size_t smem = sizeof(Fwd3Smem);
   cudaError_t e =
-      cudaFuncSetAttribute(wkv7_fwd3_kernel<kLogit>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+      cudaFuncSetAttribute(wkv7_fwd3_kernel<kLogit, kEpi>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  wkv7_fwd3_kernel<kLogit><<<(unsigned)(args.B * args.H), kThreads, smem, stream>>>(args);
+  wkv7_fwd3_kernel<kLogit, kEpi><<<(unsigned)(args.B * args.H), kThreads, smem, stream>>>(args);
   return cudaGetLastError();
 }
 
 cudaError_t launch_fwd3(const FwdArgs& args, cudaStream_t stream) {
-  return args.w_logit ? launch_fwd3_impl<true>(args, stream) : launch_fwd3_impl<false>(args, stream);
+  if (args.epilogue)
+    return args.w_logit ? launch_fwd3_impl<true, true>(args, stream) : launch_fwd3_impl<false, true>(args, stream);
+  return args.w_logit ? launch_fwd3_impl<true, false>(args, stream) : launch_fwd3_impl<false, false>(args, stream);
 }
 
 }  // namespace wkv7

@@ -20,6 +20,13 @@ struct FwdArgs {
   float* ckpt;          // [B][H][nck][N][N] or null
   unsigned* status;     // device status word (timeout flag)
   int w_logit = 0;      // 1: the w tiles hold logits z, w = exp(-0.606531 sigmoid(z)) (chunked kernels only)
+  // epilogue (chunked forward only): y <- group_norm(y) ln_w + ln_b + (sum r k r_k) v per head
+  int epilogue = 0;
+  const float* ln_w = nullptr;  // [H][N]
+  const float* ln_b = nullptr;  // [H][N]
+  const float* r_k = nullptr;   // [H][N]
+  void* nv = nullptr;           // [B][T][H][N] normalized y (input type), or null
+  float* stats = nullptr;       // [B][T][H][2] (rstd, bonus), or null
   int C;                // checkpoint interval (steps)
   int nck;              // ceil(T / C)
   int B, T, H;

@@ -31,6 +31,7 @@ EXPORTS = {
     "wkv7_backward_noalloc": 20,
     "wkv7_forward_logit_bf16": 16,
     "wkv7_backward_logit_bf16": 23,
+    "wkv7_forward_epilogue_bf16": 22,
 }
 
 
@@ -76,6 +77,8 @@ def load(path: str | None = None):
     lib.wkv7_forward_logit_bf16.restype = i
     lib.wkv7_backward_logit_bf16.argtypes = [vp] * 10 + [i] + [vp] * 7 + [i] * 4 + [vp]
     lib.wkv7_backward_logit_bf16.restype = i
+    lib.wkv7_forward_epilogue_bf16.argtypes = [vp] * 15 + [i] * 6 + [vp]
+    lib.wkv7_forward_epilogue_bf16.restype = i
     if path is None:
         _lib = lib
     return lib
@@ -251,6 +254,32 @@ def backward_logit(r, z, k, v, a, b, dy, s_init=None, ckpt=None, *, dS_final=Non
                                     *(_addr(g[n]) for n in ("dr", "dz", "dk", "dv", "da", "db", "dS_init")), B, T, H,
                                     N, _stream(stream)))
     return g
+
+
+def wkv7_forward_epilogue_bf16(r, w, k, v, a, b, s_init, ln_w, ln_b, r_k, out, nv, stats, s_final, ckpt,
+                               ckpt_every, decay_is_logit, B, T, H, N, stream):
+    """wkv7_forward_epilogue_bf16 (include/wkv7.h): pointers as ints."""
+    return load().wkv7_forward_epilogue_bf16(r, w, k, v, a, b, s_init, ln_w, ln_b, r_k, out, nv, stats, s_final, ckpt,
+                                             ckpt_every, decay_is_logit, B, T, H, N, stream)
+
+
+def forward_epilogue(r, w, k, v, a, b, ln_w, ln_b, r_k, s_init=None, *, decay_is_logit: bool = False,
+                     want_ckpt: bool = True, stream=None):
+    """Forward with the group-norm + bonus epilogue fused (bfloat16 tensors,
+    N = 64). Returns (out, nv, stats, s_final, ckpt)."""
+    import torch
+
+    B, T, H, N = r.shape
+    dev = r.device
+    out = torch.empty_like(r)
+    nv = torch.empty_like(r)
+    stats = torch.empty((B, T, H, 2), dtype=torch.float32, device=dev)
+    s_final = torch.empty((B, H, N, N), dtype=torch.float32, device=dev)
+    ckpt = torch.empty((B, H, (T + 15) // 16, N, N), dtype=torch.float32, device=dev) if want_ckpt else None
+    _check(wkv7_forward_epilogue_bf16(*(_addr(x) for x in (r, w, k, v, a, b, s_init, ln_w, ln_b, r_k, out, nv, stats,
+                                                           s_final, ckpt)), 16, int(decay_is_logit), B, T, H, N,
+                                      _stream(stream)))
+    return out, nv, stats, s_final, ckpt
 
 
 def status(stream=None) -> None:

@@ -140,3 +140,16 @@ def test_logit_entries_reject_unsupported_shapes(lib):
     assert lib.wkv7_backward_logit_bf16(*bwd) == lib.ERR_INVALID
     bwd = ptrs[:10] + [16] + ptrs[10:17] + [1, 8, 1, 32, None]
     assert lib.wkv7_backward_logit_bf16(*bwd) == lib.ERR_INVALID
+
+
+def test_epilogue_entry_rejects_unsupported_shapes_and_missing_parameters(lib):
+    p = [FAKE + i * 64 * MB for i in range(15)]
+    # r w k v a b s_init ln_w ln_b r_k out nv stats s_final ckpt, ckpt_every, logit, B, T, H, N, stream
+    assert lib.wkv7_forward_epilogue_bf16(*p, 16, 0, 1, 8, 1, 32, None) == lib.ERR_INVALID
+    assert lib.wkv7_forward_epilogue_bf16(*p, 8, 0, 1, 8, 1, 64, None) == lib.ERR_INVALID
+    q = list(p)
+    q[7] = None  # ln_w
+    assert lib.wkv7_forward_epilogue_bf16(*q, 16, 0, 1, 8, 1, 64, None) == lib.ERR_INVALID
+    q = list(p)
+    q[11] = FAKE + 16  # nv overlapping r
+    assert lib.wkv7_forward_epilogue_bf16(*q, 16, 0, 1, 8, 1, 64, None) == lib.ERR_INVALID
