@@ -282,8 +282,8 @@ def run_gpu(args):
         fwd, bwd = wkv7.wkv7_forward_logit_bf16, wkv7.wkv7_backward_logit_bf16
         bwd_args = bwd_args[:8] + [None] + bwd_args[8:]  # dS_final: none
     if args.workload == "wkv7-epilogue":
-        # the forward with the group-norm + bonus epilogue fused (out, nv and stats written);
-        # the backward call is the scan's alone (the epilogue's backward is not built)
+        # the forward with the group-norm + bonus epilogue fused (out, nv and stats written) and
+        # its backward (the group-norm gradient pass, the scan's backward, the bonus terms)
         import numpy as np
 
         rng = np.random.default_rng(0)
@@ -295,6 +295,12 @@ def run_gpu(args):
         fwd_args = fwd_args[:7] + [x.data_ptr() for x in epi_p] + [y.data_ptr(), nv.data_ptr(), stats.data_ptr(),
                                                                     s_final.data_ptr(), ckpt.data_ptr(), C, 0, B, T,
                                                                     H, N, sp]
+        pgrads = [torch.empty((H, N), dtype=torch.float32, device=dev) for _ in range(3)]
+        bwd = wkv7.wkv7_backward_epilogue_bf16
+        bwd_args = [t_in[n].data_ptr() for n in names] + [nv.data_ptr(), stats.data_ptr(), epi_p[0].data_ptr(),
+                                                          epi_p[2].data_ptr(), None, None, ckpt.data_ptr(), C, 0] + [
+            grads[n].data_ptr() for n in ("dr", "dw", "dk", "dv", "da", "db")] + [dS.data_ptr()] + [
+            x.data_ptr() for x in pgrads] + [B, T, H, N, sp]
 
     def step(ev=None):
         if ev is not None:
@@ -398,7 +404,7 @@ def _report(args, wl, world, B, T, H, N, C, bf16, ms, fwd_ms, bwd_ms, e2e, ckpt,
                        "carry chain, bf16 operands in the backward's per-chunk gradient products; fp32 state, carry "
                        "and element-wise math" if (bf16 and N == 64) else "fp32 throughout")
                       + "; inputs, dy and y stored in " + wl.storage,
-        "config": {"workload": (wl.name + {"wkv7-logit": "-decay-logits", "wkv7-epilogue": "-fused-epilogue-forward"}.get(
+        "config": {"workload": (wl.name + {"wkv7-logit": "-decay-logits", "wkv7-epilogue": "-with-epilogue"}.get(
                        args.workload, ""))
                    if T == wl.T else f"{wl.name} (T={T})", "B": B, "T": T, "H": H, "N": N, "storage": wl.storage, "ckpt_every": C,
                    "l2": "no flush: inputs, checkpoints and gradients (%.1f GB) exceed the 129 MB L2"
@@ -415,13 +421,13 @@ def _report(args, wl, world, B, T, H, N, C, bf16, ms, fwd_ms, bwd_ms, e2e, ckpt,
         "e2e": None if e2e is None else {
             "value": aggregate_tokens_per_s(world, B, T, e2e[0]), "unit": "tokens/s", "h2d_bytes_per_step": e2e[1],
             "d2h_bytes_per_step": e2e[2]},
-        "gpu_launches": (3 if (bf16 and N == 64) else 2) * args.steps,
+        "gpu_launches": (6 if args.workload == "wkv7-epilogue" else 3 if (bf16 and N == 64) else 2) * args.steps,
         "clocks": clocks.summary(),
     }
     if args.workload == "wkv7-epilogue":
         line["note"] = ("forward with the group-norm + bonus epilogue fused (out, normalized y and per-row stats "
-                        "written in the place of y); the backward call is the scan's alone, the epilogue's backward "
-                        "is not built")
+                        "written in the place of y); backward of the epilogue and the scan: a group-norm gradient "
+                        "pass, the scan's backward, the bonus terms and the parameters' gradients")
     elif args.workload == "wkv7-logit":
         line["note"] = "the decay given as logits z and formed inside the scan kernels; dz returned in the place of dw"
     if cpu_v is not None:
@@ -652,8 +658,8 @@ def main():
     ap.add_argument("--T", type=int, default=0, help="override T (profiler captures of a smaller case)")
     ap.add_argument("--workload", choices=["wkv7", "wkv7-logit", "wkv7-epilogue", "rwkv8"], default="wkv7",
                     help="wkv7: the RWKV-7 1.5B-shaped layer (default); wkv7-logit: the same with the decay "
-                         "given as logits and formed inside the kernels; wkv7-epilogue: the forward with the "
-                         "group-norm + bonus epilogue fused (the backward call is the scan's alone); rwkv8: the "
+                         "given as logits and formed inside the kernels; wkv7-epilogue: the same step with the "
+                         "group-norm + bonus epilogue (fused into the forward) and its backward; rwkv8: the "
                          "RWKV-8 recurrence")
     args = ap.parse_args()
     if args.workload == "rwkv8":

@@ -184,6 +184,30 @@ int wkv7_forward_epilogue_bf16(const wkv7_bf16* r, const wkv7_bf16* w, const wkv
                                float* s_final, float* ckpt, int ckpt_every, int decay_is_logit, int B, int T, int H,
                                int N, void* stream);
 
+/*
+ * Backward of wkv7_forward_epilogue_bf16: the gradients of sum <dout, out>.
+ *   dout        [B][T][H][N] bf16, the gradient of the epilogue's output.
+ *   nv, stats   the normalized y and (rstd, bonus) rows the forward wrote.
+ *   ln_w, r_k   [H][N] fp32, the forward's parameters (ln_b does not enter).
+ *   dr, dw (dz with decay_is_logit), dk, dv, da, db, dS_init: as
+ *               wkv7_backward_segment_bf16, with the bonus term's parts of
+ *               dr, dk, dv included.
+ *   dln_w, dln_b, dr_k  [H][N] fp32, summed over b and t (required).
+ * The group-norm gradient that is the scan's upstream gradient,
+ *     dy = rstd (dout ln_w - mean(dout ln_w) - nv mean(dout ln_w nv)),
+ * is formed by a pass before the scan's backward into a bf16 workspace (with
+ * the per-row gradient of the bonus); a pass after it adds the bonus terms to
+ * dr, dk, dv. Workspaces from cudaMallocAsync on `stream` (WKV7_ERR_ALLOC);
+ * N other than 64, or checkpoints with an interval other than 16, return
+ * WKV7_ERR_INVALID.
+ */
+int wkv7_backward_epilogue_bf16(const wkv7_bf16* r, const wkv7_bf16* w, const wkv7_bf16* k, const wkv7_bf16* v,
+                                const wkv7_bf16* a, const wkv7_bf16* b, const wkv7_bf16* dout, const wkv7_bf16* nv,
+                                const float* stats, const float* ln_w, const float* r_k, const float* s_init,
+                                const float* dS_final, const float* ckpt, int ckpt_every, int decay_is_logit,
+                                float* dr, float* dw, float* dk, float* dv, float* da, float* db, float* dS_init,
+                                float* dln_w, float* dln_b, float* dr_k, int B, int T, int H, int N, void* stream);
+
 /* Bytes of the checkpoint buffer: B*H*ceil(T/ckpt_every)*N*N*4, or 0 for an
  * invalid size. */
 size_t wkv7_ckpt_bytes(int B, int T, int H, int N, int ckpt_every);

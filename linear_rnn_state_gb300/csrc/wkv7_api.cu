@@ -10,6 +10,7 @@
 
 #include "wkv7.h"
 #include "wkv7_common.cuh"
+#include "wkv7_epilogue.h"
 #include "wkv7_launch.h"
 
 namespace wkv7 {
@@ -560,6 +561,78 @@ int wkv7_forward_epilogue_bf16(const wkv7_bf16* r, const wkv7_bf16* w, const wkv
   const Epilogue epi{ln_w, ln_b, r_k, nv, stats};
   return forward_impl(true, in, s_init, out, s_final, ckpt, ckpt_every, B, T, H, N,
                       static_cast<cudaStream_t>(stream), decay_is_logit != 0, &epi);
+}
+
+int wkv7_backward_epilogue_bf16(const wkv7_bf16* r, const wkv7_bf16* w, const wkv7_bf16* k, const wkv7_bf16* v,
+                                const wkv7_bf16* a, const wkv7_bf16* b, const wkv7_bf16* dout, const wkv7_bf16* nv,
+                                const float* stats, const float* ln_w, const float* r_k, const float* s_init,
+                                const float* dS_final, const float* ckpt, int ckpt_every, int decay_is_logit,
+                                float* dr, float* dw, float* dk, float* dv, float* da, float* db, float* dS_init,
+                                float* dln_w, float* dln_b, float* dr_k, int B, int T, int H, int N, void* stream) {
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  int rc = check_dims(B, T, H, N);
+  if (rc) return rc;
+  if (N != 64 || (ckpt && ckpt_every != kChunk))
+    return fail(WKV7_ERR_INVALID, "the epilogue needs N = 64 and ckpt_every = %d (got N = %d, %d)", kChunk, N,
+                ckpt_every);
+  const size_t vec = (size_t)B * T * H * N * 2, rows = (size_t)B * T * H, par = (size_t)H * N * 4;
+  const Span ins[6] = {{dout, vec, "dout"}, {nv, vec, "nv"}, {stats, rows * 8, "stats"},
+                       {ln_w, par, "ln_w"}, {r_k, par, "r_k"}, {r, vec, "r"}};
+  const Span outs[3] = {{dln_w, par, "dln_w"}, {dln_b, par, "dln_b"}, {dr_k, par, "dr_k"}};
+  if ((size_t)H == 0) return WKV7_OK;
+  if ((rc = check_spans(ins, 6, outs, 3, (size_t)B * T ? 6 : 0, 3))) return rc;
+  if ((size_t)B * T == 0) {  // no row: the parameters' gradients are empty sums
+    for (float* p : {dln_w, dln_b, dr_k}) {
+      cudaError_t e = cudaMemsetAsync(p, 0, par, s);
+      if (e != cudaSuccess) return fail_cuda(e, "epilogue clear");
+    }
+    const void* in[7] = {r, w, k, v, a, b, dout};
+    float* const grads[6] = {dr, dw, dk, dv, da, db};
+    return backward_impl(true, in, s_init, dS_final, ckpt, ckpt_every, grads, dS_init, B, T, H, N, s,
+                         decay_is_logit != 0);
+  }
+  const int nblk = epi_blocks(B, T);
+  const size_t dy_bytes = (vec + 255) / 256 * 256, db_bytes = (rows * 4 + 255) / 256 * 256;
+  const size_t ws_bytes = dy_bytes + db_bytes + (size_t)H * nblk * 3 * N * 4;
+  const char* inject = std::getenv("WKV7_FAIL_ALLOC");
+  if (inject && inject[0] == '1') return fail(WKV7_ERR_ALLOC, "workspace allocation failed (injected by WKV7_FAIL_ALLOC)");
+  unsigned char* ws = nullptr;
+  cudaError_t e = cudaMallocAsync(reinterpret_cast<void**>(&ws), ws_bytes, s);
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    return fail(WKV7_ERR_ALLOC, "epilogue workspace of %zu bytes: %s", ws_bytes, cudaGetErrorString(e));
+  }
+  EpiBwdArgs ea;
+  ea.dout = reinterpret_cast<const __nv_bfloat16*>(dout);
+  ea.nv = reinterpret_cast<const __nv_bfloat16*>(nv);
+  ea.r = reinterpret_cast<const __nv_bfloat16*>(r);
+  ea.k = reinterpret_cast<const __nv_bfloat16*>(k);
+  ea.v = reinterpret_cast<const __nv_bfloat16*>(v);
+  ea.stats = stats;
+  ea.ln_w = ln_w;
+  ea.r_k = r_k;
+  ea.dy = reinterpret_cast<__nv_bfloat16*>(ws);
+  ea.dbon = reinterpret_cast<float*>(ws + dy_bytes);
+  ea.part = reinterpret_cast<float*>(ws + dy_bytes + db_bytes);
+  ea.dr = dr, ea.dk = dk, ea.dv = dv;
+  ea.dln_w = dln_w, ea.dln_b = dln_b, ea.dr_k = dr_k;
+  ea.B = B, ea.T = T, ea.H = H;
+  e = launch_epi_grad(ea, s);
+  if (e != cudaSuccess) {
+    cudaFreeAsync(ws, s);
+    return fail_cuda(e, "epilogue gradient launch");
+  }
+  const void* in[7] = {r, w, k, v, a, b, ea.dy};
+  float* const grads[6] = {dr, dw, dk, dv, da, db};
+  rc = backward_impl(true, in, s_init, dS_final, ckpt, ckpt_every, grads, dS_init, B, T, H, N, s,
+                     decay_is_logit != 0);
+  if (rc == WKV7_OK) {  // the bonus terms into dr, dk, dv, and the parameters' gradients
+    e = launch_epi_finish(ea, s);
+    if (e != cudaSuccess) rc = fail_cuda(e, "epilogue bonus launch");
+  }
+  cudaError_t e2 = cudaFreeAsync(ws, s);
+  if (rc == WKV7_OK && e2 != cudaSuccess) return fail_cuda(e2, "cudaFreeAsync(epilogue workspace)");
+  return rc;
 }
 
 int wkv7_backward_logit_bf16(const wkv7_bf16* r, const wkv7_bf16* z, const wkv7_bf16* k, const wkv7_bf16* v,

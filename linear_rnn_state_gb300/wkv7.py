@@ -32,6 +32,7 @@ EXPORTS = {
     "wkv7_forward_logit_bf16": 16,
     "wkv7_backward_logit_bf16": 23,
     "wkv7_forward_epilogue_bf16": 22,
+    "wkv7_backward_epilogue_bf16": 31,
 }
 
 
@@ -79,6 +80,8 @@ def load(path: str | None = None):
     lib.wkv7_backward_logit_bf16.restype = i
     lib.wkv7_forward_epilogue_bf16.argtypes = [vp] * 15 + [i] * 6 + [vp]
     lib.wkv7_forward_epilogue_bf16.restype = i
+    lib.wkv7_backward_epilogue_bf16.argtypes = [vp] * 14 + [i, i] + [vp] * 10 + [i] * 4 + [vp]
+    lib.wkv7_backward_epilogue_bf16.restype = i
     if path is None:
         _lib = lib
     return lib
@@ -280,6 +283,35 @@ def forward_epilogue(r, w, k, v, a, b, ln_w, ln_b, r_k, s_init=None, *, decay_is
                                                            s_final, ckpt)), 16, int(decay_is_logit), B, T, H, N,
                                       _stream(stream)))
     return out, nv, stats, s_final, ckpt
+
+
+def wkv7_backward_epilogue_bf16(r, w, k, v, a, b, dout, nv, stats, ln_w, r_k, s_init, dS_final, ckpt, ckpt_every,
+                                decay_is_logit, dr, dw, dk, dv, da, db, dS_init, dln_w, dln_b, dr_k, B, T, H, N,
+                                stream):
+    """wkv7_backward_epilogue_bf16 (include/wkv7.h): pointers as ints."""
+    return load().wkv7_backward_epilogue_bf16(r, w, k, v, a, b, dout, nv, stats, ln_w, r_k, s_init, dS_final, ckpt,
+                                              ckpt_every, decay_is_logit, dr, dw, dk, dv, da, db, dS_init, dln_w,
+                                              dln_b, dr_k, B, T, H, N, stream)
+
+
+def backward_epilogue(r, w, k, v, a, b, dout, nv, stats, ln_w, r_k, s_init=None, ckpt=None, *,
+                      decay_is_logit: bool = False, dS_final=None, stream=None):
+    """Backward of forward_epilogue. Returns dict dr, dw (or dz), dk, dv, da,
+    db, dS_init, dln_w, dln_b, dr_k."""
+    import torch
+
+    B, T, H, N = r.shape
+    dev = r.device
+    dwn = "dz" if decay_is_logit else "dw"
+    g = {n: torch.empty((B, T, H, N), dtype=torch.float32, device=dev) for n in ("dr", dwn, "dk", "dv", "da", "db")}
+    g["dS_init"] = torch.empty((B, H, N, N), dtype=torch.float32, device=dev)
+    for n in ("dln_w", "dln_b", "dr_k"):
+        g[n] = torch.empty((H, N), dtype=torch.float32, device=dev)
+    _check(wkv7_backward_epilogue_bf16(
+        *(_addr(x) for x in (r, w, k, v, a, b, dout, nv, stats, ln_w, r_k, s_init, dS_final, ckpt)), 16,
+        int(decay_is_logit), *(_addr(g[n]) for n in ("dr", dwn, "dk", "dv", "da", "db", "dS_init", "dln_w", "dln_b",
+                                                    "dr_k")), B, T, H, N, _stream(stream)))
+    return g
 
 
 def status(stream=None) -> None:

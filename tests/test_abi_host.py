@@ -153,3 +153,15 @@ def test_epilogue_entry_rejects_unsupported_shapes_and_missing_parameters(lib):
     q = list(p)
     q[11] = FAKE + 16  # nv overlapping r
     assert lib.wkv7_forward_epilogue_bf16(*q, 16, 0, 1, 8, 1, 64, None) == lib.ERR_INVALID
+
+
+def test_epilogue_backward_entry_checks(lib, monkeypatch):
+    p = [FAKE + i * 64 * MB for i in range(14)]
+    g = [FAKE + (20 + i) * 64 * MB for i in range(10)]
+    # N = 32 is not supported; a missing dln_w is refused; a failing workspace is reported
+    assert lib.wkv7_backward_epilogue_bf16(*p, 16, 0, *g, 1, 8, 1, 32, None) == lib.ERR_INVALID
+    q = list(g)
+    q[7] = None
+    assert lib.wkv7_backward_epilogue_bf16(*p, 16, 0, *q, 1, 8, 1, 64, None) == lib.ERR_INVALID
+    monkeypatch.setenv("WKV7_FAIL_ALLOC", "1")
+    assert lib.wkv7_backward_epilogue_bf16(*p, 16, 0, *g, 1, 8, 1, 64, None) == lib.ERR_ALLOC

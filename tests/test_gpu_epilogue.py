@@ -97,3 +97,35 @@ def test_epilogue_parity(env, T, logit):
 
 def test_epilogue_full_size_sampled(env):
     _run(env, 4, 4096, 32, seed=0, logit=True, state=False, check_heads=[(0, 0), (3, 31)])
+
+
+@pytest.mark.parametrize("T", [16, 45, 130])
+@pytest.mark.parametrize("logit", [False, True])
+def test_epilogue_backward_parity(env, T, logit):
+    """wkv7_backward_epilogue_bf16 against the chained oracles: the epilogue's
+    backward gives the scan's dy and the bonus and parameter gradients, the
+    scan's backward the rest; dr, dk, dv are the sums of both."""
+    oracle, epi, inputs, wkv7 = env
+    B, H = 2, 3
+    d = dict(inputs.generate(B, T, H, 64, "bf16", 0.1, seed=120 + T))
+    if logit:
+        d["w"] = inputs.generate_logits(B, T, H, 64, "bf16", seed=120 + T)
+    t = {n: torch.from_numpy(d[n]).view(torch.bfloat16).cuda() for n in NAMES + ("dy",)}
+    s0 = torch.from_numpy(d["s_init"].astype(np.float32)).cuda()
+    ln_w, ln_b, r_k = _params(H, 7 + T)
+    pt = [torch.from_numpy(x).cuda() for x in (ln_w, ln_b, r_k)]
+    out, nv, stats, sf, ck = wkv7.forward_epilogue(*(t[n] for n in NAMES), *pt, s0, decay_is_logit=logit)
+    g = wkv7.backward_epilogue(*(t[n] for n in NAMES), t["dy"], nv, stats, pt[0], pt[2], s0, ck,
+                               decay_is_logit=logit)
+    wkv7.status()
+    o = {n: inputs.as_f64(d[n], "bf16") for n in NAMES + ("dy",)}
+    s064 = d["s_init"].astype(np.float32).astype(np.float64)
+    y_ref, _ = (oracle.forward_logit if logit else oracle.forward)(*(o[n] for n in NAMES), s064)
+    ge = epi.backward(o["dy"], y_ref, o["r"], o["k"], o["v"], ln_w, ln_b, r_k)
+    gs = (oracle.backward_logit if logit else oracle.backward)(*(o[n] for n in NAMES), ge["dy"], s064)
+    dwn = "dz" if logit else "dw"
+    ref = {"dr": gs["dr"] + ge["dr"], "dk": gs["dk"] + ge["dk"], "dv": gs["dv"] + ge["dv"], dwn: gs[dwn],
+           "da": gs["da"], "db": gs["db"], "dS_init": gs["dS_init"], "dln_w": ge["dln_w"], "dln_b": ge["dln_b"],
+           "dr_k": ge["dr_k"]}
+    for n, r in ref.items():
+        _rel(f"{n} T={T} logit={logit}", g[n].cpu().numpy(), r)
