@@ -272,43 +272,51 @@ def run_gpu(args):
     sp = stream.cuda_stream
     fwd = wkv7.wkv7_forward_bf16 if bf16 else wkv7.wkv7_forward
     bwd = wkv7.wkv7_backward_bf16 if bf16 else wkv7.wkv7_backward
-    fwd_args = [t_in[n].data_ptr() for n in names[:6]] + [None, y.data_ptr(), s_final.data_ptr(), ckpt.data_ptr(),
-                                                           C, B, T, H, N, sp]
-    bwd_args = [t_in[n].data_ptr() for n in names] + [None, ckpt.data_ptr(), C] + [
-        grads[n].data_ptr() for n in ("dr", "dw", "dk", "dv", "da", "db")] + [dS.data_ptr(), B, T, H, N, sp]
     if logit:
         if not (bf16 and N == 64 and C == 16):
             raise RuntimeError("the decay-logit workload needs bf16 inputs, N = 64 and 16-step checkpoints")
         fwd, bwd = wkv7.wkv7_forward_logit_bf16, wkv7.wkv7_backward_logit_bf16
-        bwd_args = bwd_args[:8] + [None] + bwd_args[8:]  # dS_final: none
-    if args.workload == "wkv7-epilogue":
+    epilogue = args.workload == "wkv7-epilogue"
+    if epilogue:
         # the forward with the group-norm + bonus epilogue fused (out, nv and stats written) and
         # its backward (the group-norm gradient pass, the scan's backward, the bonus terms)
-        import numpy as np
-
         rng = np.random.default_rng(0)
         epi_p = [torch.from_numpy(x.astype(np.float32)).to(dev) for x in (
             rng.uniform(0.5, 1.5, (H, N)), 0.1 * rng.standard_normal((H, N)), 0.5 * rng.standard_normal((H, N)))]
         nv = torch.empty_like(y)
         stats = torch.empty((B, T, H, 2), dtype=torch.float32, device=dev)
-        fwd = wkv7.wkv7_forward_epilogue_bf16
-        fwd_args = fwd_args[:7] + [x.data_ptr() for x in epi_p] + [y.data_ptr(), nv.data_ptr(), stats.data_ptr(),
-                                                                    s_final.data_ptr(), ckpt.data_ptr(), C, 0, B, T,
-                                                                    H, N, sp]
         pgrads = [torch.empty((H, N), dtype=torch.float32, device=dev) for _ in range(3)]
-        bwd = wkv7.wkv7_backward_epilogue_bf16
-        bwd_args = [t_in[n].data_ptr() for n in names] + [nv.data_ptr(), stats.data_ptr(), epi_p[0].data_ptr(),
-                                                          epi_p[2].data_ptr(), None, None, ckpt.data_ptr(), C, 0] + [
-            grads[n].data_ptr() for n in ("dr", "dw", "dk", "dv", "da", "db")] + [dS.data_ptr()] + [
-            x.data_ptr() for x in pgrads] + [B, T, H, N, sp]
+        fwd, bwd = wkv7.wkv7_forward_epilogue_bf16, wkv7.wkv7_backward_epilogue_bf16
 
-    def step(ev=None):
+    def build_args(tin, yb, gb, dSb):
+        """The forward's and backward's C arguments on one set of input and
+        output buffers (the checkpoints, s_final and the epilogue's nv and
+        stats are written and read within a step, so every set shares them)."""
+        g6 = [gb[n].data_ptr() for n in ("dr", "dw", "dk", "dv", "da", "db")]
+        if epilogue:
+            fa = [tin[n].data_ptr() for n in names[:6]] + [None] + [x.data_ptr() for x in epi_p] + [
+                yb.data_ptr(), nv.data_ptr(), stats.data_ptr(), s_final.data_ptr(), ckpt.data_ptr(), C, 0, B, T, H,
+                N, sp]
+            ba = [tin[n].data_ptr() for n in names] + [nv.data_ptr(), stats.data_ptr(), epi_p[0].data_ptr(),
+                                                       epi_p[2].data_ptr(), None, None, ckpt.data_ptr(), C, 0] + g6 + [
+                dSb.data_ptr()] + [x.data_ptr() for x in pgrads] + [B, T, H, N, sp]
+            return fa, ba
+        fa = [tin[n].data_ptr() for n in names[:6]] + [None, yb.data_ptr(), s_final.data_ptr(), ckpt.data_ptr(),
+                                                       C, B, T, H, N, sp]
+        ba = [tin[n].data_ptr() for n in names] + [None, ckpt.data_ptr(), C] + g6 + [dSb.data_ptr(), B, T, H, N, sp]
+        if logit:
+            ba = ba[:8] + [None] + ba[8:]  # dS_final: none
+        return fa, ba
+
+    fwd_args, bwd_args = build_args(t_in, y, grads, dS)
+
+    def step(ev=None, fa=None, ba=None):
         if ev is not None:
             ev[0].record(stream)
-        rc = fwd(*fwd_args)
+        rc = fwd(*(fa or fwd_args))
         if ev is not None:
             ev[1].record(stream)
-        rc2 = bwd(*bwd_args)
+        rc2 = bwd(*(ba or bwd_args))
         if ev is not None:
             ev[2].record(stream)
         if rc or rc2:
@@ -339,15 +347,19 @@ def run_gpu(args):
     if args.no_e2e:
         e2e_ms = None
     else:
-        e2e_ms = _e2e(args, d, names, t_in, grads, y, dS, bf16, tdt, step, stream, dist, dev)
+        e2e_ms = _e2e(args, d, names, t_in, grads, y, dS, bf16, tdt, step, build_args, stream, dist, dev)
     if rank != 0:
         return 0
     return _report(args, wl, world, B, T, H, N, C, bf16, ms, fwd_ms, bwd_ms, e2e_ms, ckpt, d, clocks, dev)
 
 
-def _e2e(args, d, names, t_in, grads, y, dS, bf16, tdt, step, stream, dist, dev):
-    """End-to-end step through the C ABI with pinned host buffers: copy the
-    step's inputs in, run forward + backward, copy every output back."""
+def _e2e(args, d, names, t_in, grads, y, dS, bf16, tdt, step, build_args, stream, dist, dev):
+    """End-to-end steps through the C ABI with pinned host buffers: every step
+    copies its inputs in, runs forward + backward and copies every output
+    back. Steps are pipelined over two sets of device buffers: step k's
+    host-to-device copies (one copy stream) overlap step k-1's compute, and
+    its device-to-host copies (another stream) overlap step k+1's, ordered by
+    events so that no buffer is rewritten before it has been read."""
     import torch
 
     host_in = {n: torch.from_numpy(d[n]).pin_memory() for n in names}
@@ -357,28 +369,51 @@ def _e2e(args, d, names, t_in, grads, y, dS, bf16, tdt, step, stream, dist, dev)
     h2d = sum(x.numel() * x.element_size() for x in host_in.values())
     d2h = sum(x.numel() * x.element_size() for x in host_out.values()) + host_y.numel() * host_y.element_size() \
         + host_dS.numel() * 4
+    sets = [(t_in, grads, y, dS)]
+    t1 = {n: torch.empty_like(t_in[n]) for n in names}
+    g1 = {n: torch.empty_like(grads[n]) for n in grads}
+    sets.append((t1, g1, torch.empty_like(y), torch.empty_like(dS)))
+    set_args = [build_args(tin, yb, gb, dSb) for tin, gb, yb, dSb in sets]
+    s_in, s_out = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
+    n_steps = max(2, min(args.steps, 6))
 
-    def e2e_step():
-        for n in names:
-            dst = t_in[n].view(torch.int16) if bf16 else t_in[n]
-            src = host_in[n].view(torch.int16) if bf16 else host_in[n]
-            dst.copy_(src, non_blocking=True)
-        step()
-        for n in grads:
-            host_out[n].copy_(grads[n], non_blocking=True)
-        host_y.copy_(y, non_blocking=True)
-        host_dS.copy_(dS, non_blocking=True)
+    def run(k, ev_in, ev_done, ev_out):
+        tin, gb, yb, dSb = sets[k % 2]
+        if k >= 2:
+            s_in.wait_event(ev_done[k - 2])  # step k-2 has read this set's inputs
+        with torch.cuda.stream(s_in):
+            for n in names:
+                dst = tin[n].view(torch.int16) if bf16 else tin[n]
+                src = host_in[n].view(torch.int16) if bf16 else host_in[n]
+                dst.copy_(src, non_blocking=True)
+        ev_in[k].record(s_in)
+        stream.wait_event(ev_in[k])
+        if k >= 2:
+            stream.wait_event(ev_out[k - 2])  # step k-2's outputs have left this set
+        step(fa=set_args[k % 2][0], ba=set_args[k % 2][1])
+        ev_done[k].record(stream)
+        s_out.wait_event(ev_done[k])
+        with torch.cuda.stream(s_out):
+            for n in gb:
+                host_out[n].copy_(gb[n], non_blocking=True)
+            host_y.copy_(yb, non_blocking=True)
+            host_dS.copy_(dSb, non_blocking=True)
+        ev_out[k].record(s_out)
 
-    e2e_steps = max(1, min(args.steps, 5))
-    e2e_step()
+    def events(n):
+        return [torch.cuda.Event() for _ in range(n)]
+
+    run(0, *(events(1) for _ in range(3)))  # warm-up of the copy paths
     torch.cuda.synchronize()
+    ev_in, ev_done, ev_out = events(n_steps), events(n_steps), events(n_steps)
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for _ in range(e2e_steps):
-        e2e_step()
-    e1.record(stream)
+    e0.record(s_in)
+    for k in range(n_steps):
+        run(k, ev_in, ev_done, ev_out)
+    s_in.wait_event(ev_out[n_steps - 1])
+    e1.record(s_in)
     torch.cuda.synchronize()
-    e2e_ms = reduce_max(e0.elapsed_time(e1) / e2e_steps, dist, dev)
+    e2e_ms = reduce_max(e0.elapsed_time(e1) / n_steps, dist, dev)
     return e2e_ms, h2d, d2h
 
 
