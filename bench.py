@@ -480,14 +480,14 @@ def _report(args, wl, world, B, T, H, N, C, bf16, ms, fwd_ms, bwd_ms, e2e, ckpt,
 RWKV8_METRIC = "RWKV-8 normalized recurrence fwd+bwd tokens/s (B·T), B=4 T=4096 H=32 L=E=64 fp32; achieved % of roofline"
 RWKV8_SHAPE = {"B": 4, "T": 4096, "H": 32, "Hv": 32, "L": 64, "E": 64}
 
-# DRAM bytes per token-head of one rwkv8_backward call (its kernel and the ddecay sum), from one
+# DRAM bytes per token-head of one rwkv8_backward call (its kernel; the ddecay sum moves 32 KB), from one
 # ncu capture at T=1024 (dram__bytes_read.sum + dram__bytes_write.sum / (B*T*H)); null once the
 # kernel sources change.
 RWKV8_TRAFFIC = {
     "kernel": "rwkv8_bwd_kernel (one rwkv8_backward call)",
     "sources": ("rwkv8_bwd.cu", "rwkv8_launch.h"),
-    "sha256": "bbac91591701afffdac1b01fa81faf7c6f74bd9ac4bb72866b2e99791fcc8ecf",
-    "bytes_per_token_head": (237.090304e6 + 49.826304e6) / 131072,
+    "sha256": "b03718f14002a3d822decece8bbc3a53d86c81c7b71b6f81396feef18a60800f",
+    "bytes_per_token_head": (237.082624e6 + 46.064896e6) / 131072,
 }
 
 
@@ -655,7 +655,8 @@ def run_rwkv8(args):
         "metric": RWKV8_METRIC, "value": aggregate_tokens_per_s(world, B, T, ms), "unit": "tokens/s",
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
-        "arithmetic": "fp32 FFMA on the CUDA cores throughout",
+        "arithmetic": "fp32 FFMA on the CUDA cores; the forward's chain and readout products on the tensor cores "
+                      "in split tf32 (three tf32 products per fp32 product, fp32 accumulation)",
         "config": {"workload": "rwkv8-4x4096x32-l64e64-f32" if T == RWKV8_SHAPE["T"] else f"rwkv8 (T={T})", **sh,
                    "ckpt_every": 16,
                    "l2": "no flush: inputs, checkpoints and gradients (%.1f GB) exceed the 129 MB L2"
@@ -670,7 +671,10 @@ def run_rwkv8(args):
         "e2e": None if e2e is None else {
             "value": aggregate_tokens_per_s(world, B, T, e2e[0]), "unit": "tokens/s", "h2d_bytes_per_step": e2e[1],
             "d2h_bytes_per_step": e2e[2]},
-        "gpu_launches": (2 if Hv == H else 3) * args.steps + args.steps,
+        # forward: the chain and the per-chunk readout (one kernel with RWKV8_SEQUENTIAL=1); backward: its
+        # kernel, the ddecay sum over b and, for a shared value row, one dv sum per batch row
+        "gpu_launches": ((1 if os.environ.get("RWKV8_SEQUENTIAL") == "1" else 2) + 2 + (B if Hv == 1 and H > 1 else 0))
+                        * args.steps,
         "clocks": clocks.summary(),
     }
     if not args.no_cpu_baseline and T == RWKV8_SHAPE["T"]:

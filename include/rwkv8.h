@@ -25,7 +25,8 @@
  * decay [H][L]; y, dy [B][H][T][E]; rho states [B][H][L][E]; rho_norm states
  * [B][H][L]. All fp32, row-major.
  *
- * Sizes: L = E = 64 (the kernels' tile), B, H >= 1 or 0, T >= 0. Every pointer
+ * Sizes: L = E = 64 (the kernels' tile), B, H >= 1 or 0 with B * H < 2^28,
+ * T >= 0 with B * H * T * L * 4 < 2^46. Every pointer
  * is device memory owned by the caller, 16-byte aligned; outputs are
  * overwritten and must not overlap an input or another output. An invalid
  * argument returns WKV7_ERR_INVALID before anything is enqueued.
@@ -61,7 +62,13 @@ size_t rwkv8_ckpt_bytes(int B, int T, int H, int L, int E);
  *   rho_final          [B][H][L][E] or NULL (skipped).
  *   rho_norm_final     [B][H][L] or NULL (skipped).
  *   ckpt               rwkv8_ckpt_bytes(...) bytes for rwkv8_backward, or NULL.
- * Returns WKV7_OK, WKV7_ERR_INVALID or WKV7_ERR_CUDA.
+ * The state chain between chunks runs first and writes the state before
+ * every chunk into ckpt; y of every chunk is then made from it. With ckpt
+ * NULL those states go to a workspace taken with cudaMallocAsync on the
+ * stream (WKV7_ERR_ALLOC if that fails). RWKV8_SEQUENTIAL=1 in the
+ * environment selects one pass per (b, h) through its chunks instead, which
+ * needs no workspace; the results agree to fp32 rounding.
+ * Returns WKV7_OK, WKV7_ERR_INVALID, WKV7_ERR_ALLOC or WKV7_ERR_CUDA.
  */
 int rwkv8_forward(const float* q, const float* v, const float* decay, const float* rho_init,
                   const float* rho_norm_init, float* y, float* rho_final, float* rho_norm_final, float* ckpt,

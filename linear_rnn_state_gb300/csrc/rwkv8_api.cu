@@ -28,7 +28,7 @@ int check_dims(int B, int T, int H, int Hv, int L, int E) {
   if (L != kL || E != kE) return fail(WKV7_ERR_INVALID, "L and E must be 64 (got %d, %d)", L, E);
   if (Hv != 1 && Hv != H) return fail(WKV7_ERR_INVALID, "value heads must be 1 or H (got %d, H = %d)", Hv, H);
   const unsigned long long heads = (unsigned long long)B * H;
-  if (heads >= (1ull << 31)) return fail(WKV7_ERR_INVALID, "B*H too large");
+  if (heads >= (1ull << 28)) return fail(WKV7_ERR_INVALID, "B*H too large");
   if (heads * (unsigned long long)T * kL * 4ull >= (1ull << 46)) return fail(WKV7_ERR_INVALID, "B*H*T too large");
   return WKV7_OK;
 }
@@ -60,6 +60,37 @@ int check_spans(const Span* ins, int nin, const Span* outs, int nout, int requir
     for (int q = 0; q < o; ++q)
       if (overlaps(outs[o], outs[q])) return fail(WKV7_ERR_INVALID, "%s overlaps output %s", outs[o].name, outs[q].name);
   }
+  return WKV7_OK;
+}
+
+// RWKV8_SEQUENTIAL=1 selects the kernels that walk each (b, h) through its
+// chunks in one CTA; by default the chains run alone and the per-chunk work
+// runs for every chunk at once.
+bool sequential() {
+  const char* s = std::getenv("RWKV8_SEQUENTIAL");
+  return s && s[0] == '1';
+}
+
+// A stream-ordered workspace (WKV7_FAIL_ALLOC=1 makes the allocation fail, for tests).
+int take_workspace(unsigned char** ws, size_t bytes, cudaStream_t stream) {
+  const char* inject = std::getenv("WKV7_FAIL_ALLOC");
+  if (inject && inject[0] == '1')
+    return fail(WKV7_ERR_ALLOC, "workspace allocation failed (injected by WKV7_FAIL_ALLOC)");
+  cudaError_t e = cudaMallocAsync(reinterpret_cast<void**>(ws), bytes, stream);
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    *ws = nullptr;
+    return fail(WKV7_ERR_ALLOC, "workspace of %zu bytes: %s", bytes, cudaGetErrorString(e));
+  }
+  return WKV7_OK;
+}
+
+// Frees a workspace (if any) after the launches that use it, reporting the
+// first launch error `e` or the free's own.
+int release_workspace(unsigned char* ws, cudaError_t e, const char* what, cudaStream_t stream) {
+  const cudaError_t e2 = ws ? cudaFreeAsync(ws, stream) : cudaSuccess;
+  if (e != cudaSuccess) return fail(WKV7_ERR_CUDA, "%s launch: %s", what, cudaGetErrorString(e));
+  if (e2 != cudaSuccess) return fail(WKV7_ERR_CUDA, "cudaFreeAsync(workspace): %s", cudaGetErrorString(e2));
   return WKV7_OK;
 }
 
@@ -101,9 +132,21 @@ int forward_impl(const float* q, const float* v, const float* decay, const float
   a.q = q, a.v = v, a.decay = decay, a.rho_init = rho_init, a.rho_norm_init = rho_norm_init;
   a.y = y, a.rho_final = rho_final, a.rho_norm_final = rho_norm_final, a.ckpt = ckpt;
   a.B = B, a.T = T, a.H = H, a.Hv = Hv;
-  cudaError_t e = launch_forward(a, stream);
-  if (e != cudaSuccess) return fail(WKV7_ERR_CUDA, "forward launch: %s", cudaGetErrorString(e));
-  return WKV7_OK;
+  if (sequential()) {
+    cudaError_t e = launch_forward(a, stream);
+    if (e != cudaSuccess) return fail(WKV7_ERR_CUDA, "forward launch: %s", cudaGetErrorString(e));
+    return WKV7_OK;
+  }
+  // The per-chunk readout starts from the checkpoints: without a buffer from
+  // the caller they go to a workspace.
+  unsigned char* ws = nullptr;
+  if (y && !ckpt) {
+    if ((rc = take_workspace(&ws, ckpt_bytes(B, T, H), stream))) return rc;
+    a.ckpt = reinterpret_cast<float*>(ws);
+  }
+  cudaError_t e = launch_state(a, stream);
+  if (e == cudaSuccess && y) e = launch_forward_chunks(a, stream);
+  return release_workspace(ws, e, "forward", stream);
 }
 
 int backward_impl(const float* q, const float* v, const float* decay, const float* dy, const float* rho_init,
@@ -161,7 +204,7 @@ int backward_impl(const float* q, const float* v, const float* decay, const floa
     f.rho_init = rho_init, f.rho_norm_init = rho_norm_init;
     f.ckpt = reinterpret_cast<float*>(ws);
     f.y = nullptr;  // checkpoints only
-    e = launch_forward(f, stream);
+    e = sequential() ? launch_forward(f, stream) : launch_state(f, stream);
     if (e != cudaSuccess) {
       cudaFreeAsync(ws, stream);
       return fail(WKV7_ERR_CUDA, "checkpointing forward launch: %s", cudaGetErrorString(e));

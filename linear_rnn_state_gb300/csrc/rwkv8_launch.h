@@ -29,7 +29,12 @@ __host__ __device__ inline size_t nchunks(int T) { return (size_t)((T + kC - 1) 
 // Float offset of the rho_norm checkpoints inside the checkpoint buffer.
 __host__ __device__ inline size_t ckpt_norm_offset(int B, int T, int H) { return (size_t)B * H * nchunks(T) * kL * kE; }
 
+// One CTA per (b, h) through all chunks (RWKV8_SEQUENTIAL=1).
 cudaError_t launch_forward(const Args& a, cudaStream_t s);
+// The chain alone: checkpoints (if ckpt is set) and final states, no y.
+cudaError_t launch_state(const Args& a, cudaStream_t s);
+// y of every chunk at once from the checkpoints in a.ckpt.
+cudaError_t launch_forward_chunks(const Args& a, cudaStream_t s);
 cudaError_t launch_backward(const Args& a, cudaStream_t s);
 // out[i] = sum over g of in[g * stride + i], g = 0 .. groups-1, for i in [0, n).
 cudaError_t launch_group_sum(const float* in, float* out, size_t n, size_t stride, int groups, cudaStream_t s);

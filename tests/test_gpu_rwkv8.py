@@ -3,6 +3,9 @@ fp64 oracle (oracle/rwkv8_oracle.py), called through the C ABI.
 
 Inputs are the seeded synthetic ones of linear_rnn_state_gb300.inputs
 (generate_rwkv8), rounded to fp32; the oracle consumes exactly those values.
+Both launch forms are checked: by default the chains between chunks run alone
+and the per-chunk work for all chunks at once; RWKV8_SEQUENTIAL=1 walks each
+(b, h) through its chunks in one CTA.
 The bar is the fp32 one of this library, element by element:
 |gpu - ref| <= 1e-4 (1 + |ref|) for y, the final states, dq, dv and the
 initial-state gradients. ddecay is a sum over batch and time of terms of both
@@ -74,14 +77,29 @@ def _run(env, B, T, H, Hv, seed, state=False, boundary=False, use_ckpt=True):
     return g
 
 
+VARIANTS = ["chunked", "sequential"]
+
+
+def _variant(monkeypatch, variant):
+    if variant == "sequential":
+        monkeypatch.setenv("RWKV8_SEQUENTIAL", "1")
+    else:
+        monkeypatch.delenv("RWKV8_SEQUENTIAL", raising=False)
+
+
+@pytest.mark.parametrize("variant", VARIANTS)
 @pytest.mark.parametrize("B,T,H,Hv", [(2, 16, 3, 3), (2, 45, 3, 1), (1, 130, 2, 2), (2, 1, 2, 2), (1, 33, 1, 1)])
-def test_rwkv8_parity(env, B, T, H, Hv):
+def test_rwkv8_parity(env, B, T, H, Hv, variant, monkeypatch):
+    _variant(monkeypatch, variant)
     _run(env, B, T, H, Hv, seed=100 + T)
 
 
+@pytest.mark.parametrize("variant", VARIANTS)
 @pytest.mark.parametrize("Hv", [1, 3])
-def test_rwkv8_parity_with_states_and_boundary(env, Hv):
+def test_rwkv8_parity_with_states_and_boundary(env, Hv, variant, monkeypatch):
+    _variant(monkeypatch, variant)
     _run(env, 2, 70, 3, Hv, seed=7, state=True, boundary=True)
+    _run(env, 1, 70, 3, Hv, seed=8, state=True, boundary=True, use_ckpt=False)
 
 
 def test_rwkv8_backward_without_checkpoints_matches(env):
@@ -162,11 +180,13 @@ def test_rwkv8_full_size_sampled(env):
                float(np.abs(g_ref["ddecay"]).mean()))
 
 
+@pytest.mark.parametrize("variant", VARIANTS)
 @pytest.mark.parametrize("case", ["decay_zero", "decay_one", "zero_query_rows", "mixed_decay"])
-def test_rwkv8_degenerate_inputs(env, case):
+def test_rwkv8_degenerate_inputs(env, case, variant, monkeypatch):
     """Decay exactly 0 (only the previous step is seen) or 1 (plain prefix
     sums), query rows of zeros (their weights are 0 / EPS = 0), and a decay
     that mixes 0, 1 and tiny values across latents."""
+    _variant(monkeypatch, variant)
     orc, inputs, rwkv8 = env
     B, T, H = 2, 40, 2
     d = inputs.generate_rwkv8(B, T, H, H, 64, 64, "f32", state_std=0.1, boundary=True, seed=90)
@@ -196,3 +216,25 @@ def test_rwkv8_degenerate_inputs(env, case):
     for k in ("dq", "dv", "d_rho_init", "d_rho_norm_init"):
         _close(f"{k} {case}", g[k].cpu().numpy(), g_ref[k])
     _close(f"ddecay {case}", g["ddecay"].cpu().numpy(), g_ref["ddecay"], float(np.abs(g_ref["ddecay"]).mean()))
+
+
+def test_rwkv8_launch_forms_agree(env, monkeypatch):
+    """The two launch forms on one input of several chunks and a ragged tail:
+    the forward's y, final states and checkpoints, and every gradient, agree
+    to fp32 rounding (the chain sums its terms in another order)."""
+    _, inputs, rwkv8 = env
+    d = inputs.generate_rwkv8(2, 77, 3, 3, 64, 64, "f32", state_std=0.1, boundary=True, seed=12)
+    t = {k: _dev(x) for k, x in d.items()}
+    out = {}
+    for variant in VARIANTS:
+        _variant(monkeypatch, variant)
+        f = rwkv8.forward(t["q"], t["v"], t["decay"], t["rho_init"], t["rho_norm_init"])
+        g = rwkv8.backward(t["q"], t["v"], t["decay"], t["dy"], t["rho_init"], t["rho_norm_init"], f[3],
+                           d_rho_final=t["d_rho_final"], d_rho_norm_final=t["d_rho_norm_final"])
+        torch.cuda.synchronize()
+        out[variant] = dict(zip(("y", "rho_final", "rho_norm_final", "ckpt"), f), **g)
+    a, b = out["chunked"], out["sequential"]
+    for k in a:
+        ref = b[k].cpu().numpy().astype(np.float64)
+        scale = float(np.abs(ref).mean()) if k == "ddecay" else 0.0
+        _close(f"{k} chunked vs sequential", a[k].cpu().numpy(), ref, scale)

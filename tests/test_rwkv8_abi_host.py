@@ -95,6 +95,15 @@ def test_backward_workspace_failure_is_reported(lib, monkeypatch):
     assert "WKV7_FAIL_ALLOC" in lib.wkv7.last_error()
 
 
+def test_forward_checkpoint_workspace_failure_is_reported(lib, monkeypatch):
+    # without a checkpoint buffer the per-chunk readout needs a workspace for the chunk states
+    monkeypatch.setenv("WKV7_FAIL_ALLOC", "1")
+    monkeypatch.delenv("RWKV8_SEQUENTIAL", raising=False)
+    rc = lib.rwkv8_forward(*_args(FWD_NAMES, ckpt=None))
+    assert rc == -1
+    assert "WKV7_FAIL_ALLOC" in lib.wkv7.last_error()
+
+
 def test_empty_problems_need_no_device(lib):
     # B*H == 0: nothing to do, every buffer may be NULL
     assert lib.rwkv8_forward(*([None] * 9), 0, 8, 2, 2, 64, 64, None) == 0
