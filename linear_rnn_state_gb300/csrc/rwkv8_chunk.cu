@@ -30,24 +30,12 @@ namespace {
 using wkv7::cp_async16;
 using wkv7::cp_async_commit;
 using wkv7::cp_async_wait_all;
-using wkv7::mma_tf32;
 
 constexpr int kThreads = 256;
 constexpr int kP = 72;   // row pitch of rho0 and v (8 mod 32: conflict-free B fragments)
 constexpr int kUT = 68;  // row pitch of U d^tau (4 mod 32: conflict-free A fragments and row stores)
 constexpr int kAP = 20;  // row pitch of A (conflict-free A fragments)
 
-// d += a b in split tf32 (the two small cross terms first).
-__device__ __forceinline__ void mma_split(float (&d)[4], const float (&a)[4], float b0, float b1) {
-  uint32_t ah[4], al[4], bh0, bl0, bh1, bl1;
-#pragma unroll
-  for (int i = 0; i < 4; ++i) split_tf32(a[i], ah[i], al[i]);
-  split_tf32(b0, bh0, bl0);
-  split_tf32(b1, bh1, bl1);
-  mma_tf32(d, al, bh0, bh1);
-  mma_tf32(d, ah, bl0, bl1);
-  mma_tf32(d, ah, bh0, bh1);
-}
 
 
 // The A role: the 120 pairs (at, as), as < at, in four rounds; in round r
