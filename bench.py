@@ -347,57 +347,50 @@ def run_gpu(args):
     if args.no_e2e:
         e2e_ms = None
     else:
-        e2e_ms = _e2e(args, d, names, t_in, grads, y, dS, bf16, tdt, step, build_args, stream, dist, dev)
+        e2e_ms = _e2e(args, d, names, t_in, grads, y, dS, step, build_args, stream, dist, dev)
     if rank != 0:
         return 0
     return _report(args, wl, world, B, T, H, N, C, bf16, ms, fwd_ms, bwd_ms, e2e_ms, ckpt, d, clocks, dev)
 
 
-def _e2e(args, d, names, t_in, grads, y, dS, bf16, tdt, step, build_args, stream, dist, dev):
+def _pipelined_e2e(args, host_in, sets, step_on, stream, dist, dev):
     """End-to-end steps through the C ABI with pinned host buffers: every step
     copies its inputs in, runs forward + backward and copies every output
-    back. Steps are pipelined over two sets of device buffers: step k's
-    host-to-device copies (one copy stream) overlap step k-1's compute, and
-    its device-to-host copies (another stream) overlap step k+1's, ordered by
-    events so that no buffer is rewritten before it has been read."""
+    back. `sets` holds two (device inputs, device outputs) buffer sets keyed
+    like `host_in`; `step_on(i)` enqueues one step on set i. Steps alternate
+    between the sets: step k's host-to-device copies (one copy stream)
+    overlap step k-1's compute, and its device-to-host copies (another
+    stream) overlap step k+1's, ordered by events so that no buffer is
+    rewritten before it has been read. Returns (ms per step, bytes in, bytes
+    out per step)."""
     import torch
 
-    host_in = {n: torch.from_numpy(d[n]).pin_memory() for n in names}
-    host_out = {n: torch.empty(grads[n].shape, dtype=torch.float32).pin_memory() for n in grads}
-    host_y = torch.empty(y.shape, dtype=tdt).pin_memory()
-    host_dS = torch.empty(dS.shape, dtype=torch.float32).pin_memory()
+    host_out = {n: torch.empty(x.shape, dtype=x.dtype).pin_memory() for n, x in sets[0][1].items()}
     h2d = sum(x.numel() * x.element_size() for x in host_in.values())
-    d2h = sum(x.numel() * x.element_size() for x in host_out.values()) + host_y.numel() * host_y.element_size() \
-        + host_dS.numel() * 4
-    sets = [(t_in, grads, y, dS)]
-    t1 = {n: torch.empty_like(t_in[n]) for n in names}
-    g1 = {n: torch.empty_like(grads[n]) for n in grads}
-    sets.append((t1, g1, torch.empty_like(y), torch.empty_like(dS)))
-    set_args = [build_args(tin, yb, gb, dSb) for tin, gb, yb, dSb in sets]
+    d2h = sum(x.numel() * x.element_size() for x in host_out.values())
     s_in, s_out = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
     n_steps = max(2, min(args.steps, 6))
 
     def run(k, ev_in, ev_done, ev_out):
-        tin, gb, yb, dSb = sets[k % 2]
+        dev_in, dev_out = sets[k % 2]
         if k >= 2:
             s_in.wait_event(ev_done[k - 2])  # step k-2 has read this set's inputs
         with torch.cuda.stream(s_in):
-            for n in names:
-                dst = tin[n].view(torch.int16) if bf16 else tin[n]
-                src = host_in[n].view(torch.int16) if bf16 else host_in[n]
+            for n, src in host_in.items():
+                dst = dev_in[n]
+                if dst.dtype != src.dtype:  # bf16 buffers take the raw 16-bit host words
+                    dst, src = dst.view(torch.int16), src.view(torch.int16)
                 dst.copy_(src, non_blocking=True)
         ev_in[k].record(s_in)
         stream.wait_event(ev_in[k])
         if k >= 2:
             stream.wait_event(ev_out[k - 2])  # step k-2's outputs have left this set
-        step(fa=set_args[k % 2][0], ba=set_args[k % 2][1])
+        step_on(k % 2)
         ev_done[k].record(stream)
         s_out.wait_event(ev_done[k])
         with torch.cuda.stream(s_out):
-            for n in gb:
-                host_out[n].copy_(gb[n], non_blocking=True)
-            host_y.copy_(yb, non_blocking=True)
-            host_dS.copy_(dSb, non_blocking=True)
+            for n, x in dev_out.items():
+                host_out[n].copy_(x, non_blocking=True)
         ev_out[k].record(s_out)
 
     def events(n):
@@ -413,8 +406,22 @@ def _e2e(args, d, names, t_in, grads, y, dS, bf16, tdt, step, build_args, stream
     s_in.wait_event(ev_out[n_steps - 1])
     e1.record(s_in)
     torch.cuda.synchronize()
-    e2e_ms = reduce_max(e0.elapsed_time(e1) / n_steps, dist, dev)
-    return e2e_ms, h2d, d2h
+    return reduce_max(e0.elapsed_time(e1) / n_steps, dist, dev), h2d, d2h
+
+
+def _e2e(args, d, names, t_in, grads, y, dS, step, build_args, stream, dist, dev):
+    """The WKV7 step end to end (see _pipelined_e2e): inputs in, every gradient,
+    y and dS_init out."""
+    import torch
+
+    host_in = {n: torch.from_numpy(d[n]).pin_memory() for n in names}
+    t1 = {n: torch.empty_like(t_in[n]) for n in names}
+    g1 = {n: torch.empty_like(grads[n]) for n in grads}
+    y1, dS1 = torch.empty_like(y), torch.empty_like(dS)
+    sets = [(t_in, {**grads, "y": y, "dS_init": dS}), (t1, {**g1, "y": y1, "dS_init": dS1})]
+    set_args = [build_args(t_in, y, grads, dS), build_args(t1, y1, g1, dS1)]
+    return _pipelined_e2e(args, host_in, sets, lambda i: step(fa=set_args[i][0], ba=set_args[i][1]), stream, dist,
+                          dev)
 
 
 def _report(args, wl, world, B, T, H, N, C, bf16, ms, fwd_ms, bwd_ms, e2e, ckpt, d, clocks, dev):
@@ -614,30 +621,32 @@ def run_rwkv8(args):
 
     e2e = None
     if not args.no_e2e:
-        host_in = {k: torch.from_numpy(d[k]).pin_memory() for k in ("q", "v", "dy")}
-        host_out = {k: torch.empty(x.shape, dtype=torch.float32).pin_memory() for k, x in g.items()}
-        host_y = torch.empty(y.shape, dtype=torch.float32).pin_memory()
-        h2d = sum(x.numel() * 4 for x in host_in.values())
-        d2h = sum(x.numel() * 4 for x in host_out.values()) + host_y.numel() * 4
+        # inputs q, v, dy in and y and every gradient out, pipelined over two buffer sets (the decay
+        # is a parameter and stays resident; checkpoints and final states never leave the device)
+        names = ("q", "v", "dy")
+        host_in = {k: torch.from_numpy(d[k]).pin_memory() for k in names}
+        t1 = {k: torch.empty_like(t_in[k]) for k in names}
+        g1 = {k: torch.empty_like(x) for k, x in g.items()}
+        sets = [({k: t_in[k] for k in names}, {**g, "y": y}), (t1, {**g1, "y": torch.empty_like(y)})]
 
-        def e2e_step():
-            for k in host_in:
-                t_in[k].copy_(host_in[k], non_blocking=True)
-            step()
-            host_y.copy_(y, non_blocking=True)
-            for k in g:
-                host_out[k].copy_(g[k], non_blocking=True)
+        def set_args(i):
+            tin, out = sets[i]
+            fa = [tin["q"].data_ptr(), tin["v"].data_ptr(), t_in["decay"].data_ptr(), None, None,
+                  out["y"].data_ptr(), rf.data_ptr(), nf.data_ptr(), ckpt.data_ptr(), B, T, H, Hv, L, E, sp]
+            ba = [tin["q"].data_ptr(), tin["v"].data_ptr(), t_in["decay"].data_ptr(), tin["dy"].data_ptr(), None,
+                  None, None, None, ckpt.data_ptr()] + [out[k].data_ptr() for k in g] + [B, T, H, Hv, L, E, sp]
+            return fa, ba
 
-        e2e_step()
-        torch.cuda.synchronize()
-        n = max(1, min(args.steps, 5))
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record(stream)
-        for _ in range(n):
-            e2e_step()
-        e1.record(stream)
-        torch.cuda.synchronize()
-        e2e = (reduce_max(e0.elapsed_time(e1) / n, dist, dev), h2d, d2h)
+        pargs = [set_args(0), set_args(1)]
+
+        def step_on(i):
+            rc = rwkv8.rwkv8_forward(*pargs[i][0])
+            rc2 = rwkv8.rwkv8_backward(*pargs[i][1])
+            allreduce_param_grad(sets[i][1]["ddecay"], dist)
+            if rc or rc2:
+                raise RuntimeError(wkv7.last_error())
+
+        e2e = _pipelined_e2e(args, host_in, sets, step_on, stream, dist, dev)
     if rank != 0:
         return 0
 
