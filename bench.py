@@ -18,6 +18,7 @@ import os
 import statistics
 import subprocess
 import sys
+import tempfile
 import time
 
 ROOT = os.path.dirname(os.path.abspath(__file__))
@@ -121,14 +122,21 @@ class ClockSampler:
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
-    def __init__(self, device_index: int):
+    def __init__(self, device_index: int, path: str | None = None):
+        """`path`: where the raw samples go ("{rank}" is replaced by the device
+        index); a temporary file when None."""
         self.dev = device_index
         self.proc = None
-        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_rank{device_index}.csv")
+        if path:
+            self.path = path.replace("{rank}", str(device_index))
+        else:
+            fd, self.path = tempfile.mkstemp(prefix=f"clocks_rank{device_index}_", suffix=".csv")
+            os.close(fd)
 
     def __enter__(self):
         try:
-            os.makedirs(os.path.dirname(self.path), exist_ok=True)
+            if os.path.dirname(self.path):
+                os.makedirs(os.path.dirname(self.path), exist_ok=True)
             self.fh = open(self.path, "w")
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits", "-lms", "200",
@@ -329,7 +337,7 @@ def run_gpu(args):
     if dist:
         dist.barrier()
     torch.cuda.synchronize()
-    with ClockSampler(local) as clocks:
+    with ClockSampler(local, args.clock_csv) as clocks:
         start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         start.record(stream)
         for k in range(args.steps):
@@ -606,7 +614,7 @@ def run_rwkv8(args):
     if dist:
         dist.barrier()
     torch.cuda.synchronize()
-    with ClockSampler(local) as clocks:
+    with ClockSampler(local, args.clock_csv) as clocks:
         start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         start.record(stream)
         for k in range(args.steps):
@@ -701,6 +709,9 @@ def main():
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["gb300", "reference"], default="gb300")
+    ap.add_argument("--clock-csv", default=None,
+                    help="file for the raw nvidia-smi samples of the timed region ({rank} = device index); "
+                         "a temporary file by default")
     ap.add_argument("--no-cpu-baseline", action="store_true", help="skip the timed oracle sample")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end measurement")
     ap.add_argument("--T", type=int, default=0, help="override T (profiler captures of a smaller case)")
