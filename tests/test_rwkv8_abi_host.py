@@ -60,6 +60,7 @@ BAD = [
     ("value_heads", {"Hv": 3}),
     ("negative_T", {"T": -1}),
     ("y_overlaps_q", {"y": FAKE + 16}),
+    ("too_many_heads", {"B": 1 << 14, "H": 1 << 14, "Hv": 1 << 14}),  # B * H must stay below 2^28
 ]
 
 
