@@ -16,8 +16,10 @@
 // only elementwise, so the chain between chunks is one multiply-add per state
 // element; the rest of a chunk is independent work.
 //
-// One CTA of 256 threads per (b, h) runs the chunks in order, fp32 FFMA on
-// the CUDA cores. The state lives in registers (a 4 x 4 tile per thread) with
+// This is the one-pass form (RWKV8_SEQUENTIAL=1; by default the chain runs
+// alone in rwkv8_state.cu and the readout per chunk in rwkv8_chunk.cu). One
+// CTA of 256 threads per (b, h) runs the chunks in order, fp32 FFMA on the
+// CUDA cores. The state lives in registers (a 4 x 4 tile per thread) with
 // a copy in shared memory for the readout product; the next chunk's q and v
 // are copied in with cp.async while the current one is processed. The state
 // before every chunk (and n) is written out as the backward's checkpoint.
