@@ -20,7 +20,10 @@ and the backward, with Gc the gradient of the state after the chunk,
     DA^ = DSA S0 + tril(DSA V^T, -1) K~ + tril(DSA SA^T, -1) B~,        da = DA^ c(t-1)
     Gc' = Gc diag(c_L) + DY^T R^ + DSA^T A^                     (the carry)
     w dw = colsum(Gc' o S0) - sum_{u<t} x(u) - a da,  x = r dr - k dk - b db + a da
-         = sum_{u>=t} x(u) - a da + colsum(Gc o S_end)          (both anchors).
+         = sum_{u>=t} x(u) - a da + colsum(Gc o S_end)          (both anchors),
+with the anchors from the chunk's own column products
+    colsum(Gc o S_end) = c_L colsum(Gc o S0) + sum_t (Kb o V Gc + Bb o SA Gc)
+    colsum(Gc' o S0)   = c_L colsum(Gc o S0) + sum_t (R^ o DY S0 + A^ o DSA S0).
 
 RWKV-8 ("src/sequence/rwkv8/backward.rs", burn_dragon_kernel): the chunk
 closed forms with non-negative powers of the fixed decay d only
@@ -85,6 +88,10 @@ def wkv7_chunk_backward(S0, r, w, k, v, a, b, dy, Gc):
     dk, db, dr, da = DKt / c, DBt / c, DRh * c, DAh * cprev
     Gc_prev = Gc * cL[None, :] + dy.T @ Rh + DSA.T @ Ah
     x = r * dr - k * dk - b * db + a * da
+    # the output kernel takes both anchors from the chunk's own column products
+    base = cL * (Gc * S0).sum(axis=0)
+    _rel("colsum(Gc o S_end)", base + (Kb * (v @ Gc) + Bb * (SA @ Gc)).sum(axis=0), (Gc * S_end).sum(axis=0), 1e-10)
+    _rel("colsum(Gc' o S0)", base + (Rh * (dy @ S0) + Ah * (DSA @ S0)).sum(axis=0), (Gc_prev * S0).sum(axis=0), 1e-10)
     start = (Gc_prev * S0).sum(axis=0) - np.vstack([np.zeros((1, x.shape[1])), np.cumsum(x, axis=0)[:-1]]) - a * da
     end = np.cumsum(x[::-1], axis=0)[::-1] - a * da + (Gc * S_end).sum(axis=0)
     return dr, start / w, end / w, dk, DV, da, db, Gc_prev
