@@ -36,7 +36,7 @@ TRAFFIC = {
     "kernel": "wkv7_bwd4_carry_kernel + wkv7_bwd4_out_kernel (one wkv7_backward_bf16 call)",
     "sources": ("wkv7_bwd4.cu", "wkv7_common.cuh", "wkv7_scaled.cuh", "wkv7_mma.cuh", "wkv7_launch.h",
                 "wkv7_decay.cuh"),
-    "sha256": "2839c5c5fcca5f0eff6628780eaf6130067c1c34af703861af3059028417ef4f",
+    "sha256": "b6d7e74b628bf65c30e012a75aecaec35f20f0a6021bcd5a59138e697919a2ec",
     "bytes_per_token_head": (83.953664e6 + 28.174848e6 + 318.850048e6 + 162.109952e6) / 131072,
 }
 

@@ -18,7 +18,7 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD_DIR = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libwkv7.so")
 
-SOURCES = ["wkv7_api.cu", "wkv7_fwd.cu", "wkv7_fwd2.cu", "wkv7_fwd3.cu", "wkv7_bwd.cu", "wkv7_bwd2.cu", "wkv7_bwd3.cu", "wkv7_bwd4.cu", "rwkv8_api.cu",
+SOURCES = ["wkv7_api.cu", "wkv7_fwd2.cu", "wkv7_fwd3.cu", "wkv7_bwd2.cu", "wkv7_bwd3.cu", "wkv7_bwd4.cu", "rwkv8_api.cu",
            "rwkv8_fwd.cu", "rwkv8_bwd.cu", "rwkv8_state.cu", "rwkv8_chunk.cu", "wkv7_epilogue.cu"]
 HEADERS = ["wkv7_common.cuh", "wkv7_launch.h", "wkv7_mma.cuh", "wkv7_scaled.cuh", "wkv7_tmem.cuh", "wkv7_decay.cuh",
            "wkv7_epilogue.h", "rwkv8_launch.h", "rwkv8_split.cuh"]

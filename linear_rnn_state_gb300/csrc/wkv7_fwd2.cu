@@ -400,6 +400,13 @@ int fwd2_box_steps(int N, bool bf16) {
   return 16;
 }
 
+// Steps per TMA box of the forward kernels' input rows (both forms stage 16).
+int fwd_steps_per_stage(int N, bool bf16) {
+  (void)N;
+  (void)bf16;
+  return 16;
+}
+
 cudaError_t launch_fwd2(const FwdArgs& args, bool bf16, int N, cudaStream_t stream) {
   if (bf16) {
     switch (N) {

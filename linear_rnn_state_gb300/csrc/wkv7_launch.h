@@ -54,12 +54,9 @@ struct BwdArgs {
   int B, T, H;
 };
 
-// Steps per TMA box for each kernel (the K / KS template parameter chosen
-// for this N and input type).
+// Steps per TMA box of the forward kernels' input rows.
 int fwd_steps_per_stage(int N, bool bf16);
-int bwd_steps_per_stage(int N, bool bf16);
 
-cudaError_t launch_fwd(const FwdArgs& args, bool bf16, int N, cudaStream_t stream);
 cudaError_t launch_fwd2(const FwdArgs& args, bool bf16, int N, cudaStream_t stream);
 // Chunked tensor-core forward: bf16 inputs, N = 64, checkpoints (if any) at a
 // multiple of its 16-step chunk.
@@ -72,7 +69,6 @@ cudaError_t launch_bwd4(const BwdArgs& args, cudaStream_t stream);
 size_t bwd4_workspace_bytes(int B, int T, int H);
 constexpr int kChunk = 16;
 inline bool use_chunked(bool bf16, int N, int C) { return bf16 && N == 64 && C % kChunk == 0; }
-cudaError_t launch_bwd(const BwdArgs& args, bool bf16, int N, cudaStream_t stream);
 cudaError_t launch_bwd2(const BwdArgs& args, bool bf16, int N, cudaStream_t stream);
 int bwd2_steps_per_window(int N, bool bf16);
 
