@@ -252,3 +252,58 @@ def test_rwkv8_chunk_algebra_matches_the_oracle(T, C):
     _rel("ddecay", dd, g_ref["ddecay"][0], 1e-10)
     _rel("d_rho_init", G, g_ref["d_rho_init"][0, 0])
     _rel("d_rho_norm_init", Gn, g_ref["d_rho_norm_init"][0, 0])
+
+
+def test_rwkv8_backward_splits_into_chains_and_chunks():
+    """The backward split the way the forward is: the carried G of every column
+    block alone (G_start = d^len G15 + (U d^s)^T DY over the block's columns),
+    Gn as the sum over blocks of partial chains built from each block's part
+    of R (g_n is linear in R), then every chunk's gradients from its (G15,
+    Gn15) alone. Against the oracle; the algebra a split backward kernel rests on."""
+    orc = _load_rwkv8_oracle()
+    rng = np.random.default_rng(5)
+    T, C, L, E, NB = 37, 8, 6, 8, 4
+    W = E // NB
+    q = np.maximum(rng.standard_normal((T, L)), 0.0)
+    v, dy = rng.standard_normal((T, E)), rng.standard_normal((T, E))
+    d = np.exp(-0.606531 / (1 + np.exp(-rng.standard_normal(L))))
+    rho_i, n_i = 0.1 * rng.standard_normal((L, E)), 0.1 * np.abs(rng.standard_normal(L))
+    dG, dGn = rng.standard_normal((L, E)), rng.standard_normal(L)
+    g_ref = orc.backward(q[None, None], v[None, None], d[None], dy[None, None], rho_i[None, None],
+                         n_i[None, None], dG[None, None], dGn[None, None])
+    chunks = [slice(t0, min(T, t0 + C)) for t0 in range(0, T, C)]
+    starts, rho, n = [], rho_i, n_i
+    for sl in chunks:
+        starts.append((rho, n))
+        _, rho, n = rwkv8_chunk_forward(rho, n, q[sl], v[sl], d)
+    # the chains alone, per column block
+    G15, Gn15 = [None] * len(chunks), [None] * len(chunks)
+    Gb = [dG[:, cb * W:(cb + 1) * W].copy() for cb in range(NB)]
+    Gnp = [dGn.copy() if cb == 0 else np.zeros(L) for cb in range(NB)]
+    for ci in reversed(range(len(chunks))):
+        sl = chunks[ci]
+        rho0, n0 = starts[ci]
+        ln = sl.stop - sl.start
+        G15[ci], Gn15[ci] = np.hstack(Gb), sum(Gnp)
+        pw = _pw(d, ln)
+        nb = _norm_before(n0, q[sl], pw)
+        U = q[sl] / (q[sl].sum(axis=1, keepdims=True) + EPS) / (nb + EPS)
+        for cb in range(NB):
+            cs = slice(cb * W, (cb + 1) * W)
+            Mp, R0p = dy[sl][:, cs] @ v[sl][:, cs].T, dy[sl][:, cs] @ rho0[:, cs].T
+            Rp = np.array([pw[t] * R0p[t] + sum(pw[t - 1 - s] * q[sl][s] * Mp[t, s] for s in range(t))
+                           for t in range(ln)])
+            Gnp[cb] = pw[ln] * Gnp[cb] + (pw[:ln] * (-U * Rp / (nb + EPS))).sum(axis=0)
+            Gb[cb] = pw[ln][:, None] * Gb[cb] + (U * pw[:ln]).T @ dy[sl][:, cs]
+    _rel("d_rho_init", np.hstack(Gb), g_ref["d_rho_init"][0, 0])
+    _rel("d_rho_norm_init", sum(Gnp), g_ref["d_rho_norm_init"][0, 0])
+    # every chunk from its own (G15, Gn15)
+    dq, dv, dd = [], [], np.zeros(L)
+    for ci, sl in enumerate(chunks):
+        a, b, c, _, _ = rwkv8_chunk_backward(*starts[ci], q[sl], v[sl], d, dy[sl], G15[ci], Gn15[ci])
+        dq.append(a)
+        dv.append(b)
+        dd = dd + c
+    _rel("dq", np.vstack(dq), g_ref["dq"][0, 0])
+    _rel("dv", np.vstack(dv), g_ref["dv"][0, 0])
+    _rel("ddecay", dd, g_ref["ddecay"][0], 1e-10)
