@@ -13,6 +13,7 @@ change).
 
 Run from the repository root: python tests/golden/make_golden.py
 """
+import importlib.util
 import json
 import os
 import sys
@@ -33,11 +34,10 @@ def cases():
     import oracle
     from linear_rnn_state_gb300 import inputs
 
-    spec = __import__("importlib.util").util
     def load(name):
-        s = spec.spec_from_file_location(name, os.path.join(ROOT, "oracle", f"{name}.py"))
-        m = spec.module_from_spec(s)
-        s.loader.exec_module(m)
+        spec = importlib.util.spec_from_file_location(name, os.path.join(ROOT, "oracle", f"{name}.py"))
+        m = importlib.util.module_from_spec(spec)
+        spec.loader.exec_module(m)
         return m
 
     r8, epi = load("rwkv8_oracle"), load("epilogue_oracle")
