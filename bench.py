@@ -41,6 +41,30 @@ TRAFFIC = {
 }
 
 
+# The fp32 backward (wkv7_backward at N = 64) runs one kernel; its DRAM bytes per token-head from
+# one ncu capture, null until taken (and once its sources change).
+TRAFFIC_FP32 = {
+    "kernel": "wkv7_bwd2_kernel (one wkv7_backward call, fp32 inputs)",
+    "sources": ("wkv7_bwd2.cu", "wkv7_common.cuh", "wkv7_scaled.cuh", "wkv7_tmem.cuh", "wkv7_launch.h"),
+    "sha256": "",
+    "N": 64,
+    "bytes_per_token_head": None,
+}
+
+
+def configs_bench_workload() -> str:
+    from linear_rnn_state_gb300 import configs
+
+    return configs.BENCH_WORKLOAD
+
+
+def measured_traffic_fp32(token_heads: int, N: int):
+    t = TRAFFIC_FP32
+    if not t["sha256"] or N != t["N"] or sources_sha256(t["sources"]) != t["sha256"]:
+        return None
+    return t["bytes_per_token_head"] * token_heads
+
+
 def sources_sha256(names) -> str:
     import hashlib
 
@@ -79,6 +103,17 @@ def _dist():
 def shard_seed(rank: int) -> int:
     """Each rank scans its own batch: the generator is seeded with the rank."""
     return rank
+
+
+def head_shard(B: int, H: int, rank: int, world: int):
+    """The (b, h) heads rank `rank` of `world` owns when one batch of B x H
+    heads is split across ranks: a contiguous run of the B*H heads in (b, h)
+    order, as even as the division allows. Heads are independent (each runs
+    its own scan and its own backward), so a split by (b, h) needs no
+    exchange; this is the only split the path uses."""
+    n = B * H
+    lo, hi = rank * n // world, (rank + 1) * n // world
+    return [(i // H, i % H) for i in range(lo, hi)]
 
 
 def reduce_max(value: float, dist, device=None) -> float:
@@ -189,16 +224,31 @@ def _work_per_token_head(N, C, in_bytes):
     return f_flop, b_flop, f_bytes, b_bytes
 
 
+# Host memory the timed oracle sample may hold: its backward keeps every state of a
+# head (T N^2 doubles) while it walks back, one head per thread.
+ORACLE_SAMPLE_BYTES = 16e9
+
+
+def cpu_sample_heads(wl, cores):
+    """How many (b, h) heads the timed oracle sample takes: every head, unless
+    their state histories would not fit the host-memory budget (the 65536-step
+    workload), then as many as fit, at most one per core."""
+    per_head = wl.T * wl.N * wl.N * 8
+    fit = max(1, int(ORACLE_SAMPLE_BYTES // per_head))
+    return wl.B * wl.H if fit >= min(wl.B * wl.H, cores) else min(fit, cores)
+
+
 def cpu_baseline_sample(wl, d, heads, nthreads=0):
     """Time the oracle (fwd + bwd, fp64) on the first `heads` (b, h) heads of
-    the workload, each over its whole sequence, on every host core."""
+    the workload, each over its whole sequence, on every host core (at most
+    one thread per head)."""
     import numpy as np
 
     import oracle
     from linear_rnn_state_gb300 import inputs
 
-    cores = nthreads or len(os.sched_getaffinity(0))
     P = min(wl.B * wl.H, heads)
+    cores = min(nthreads or len(os.sched_getaffinity(0)), P)
     heads = [(i // wl.H, i % wl.H) for i in range(P)]
     o = {n: inputs.as_f64(d[n], wl.storage) for n in ("r", "w", "k", "v", "a", "b", "dy")}
     sel = {n: np.stack([o[n][bi, :, hi, :] for bi, hi in heads])[:, :, None, :] for n in o}
@@ -216,14 +266,16 @@ def run_reference(args):
         return 0
     from linear_rnn_state_gb300 import configs, inputs
 
-    wl = configs.WORKLOADS[configs.BENCH_WORKLOAD]
+    wl = configs.WORKLOADS[args.shape]
     d = inputs.generate(wl.B, wl.T, wl.H, wl.N, wl.storage, wl.s_init_std, seed=0)
-    # each step: the whole workload (every (b, h) head over its full sequence)
+    # each step: the whole workload (every (b, h) head over its full sequence), or on the
+    # 65536-step workload the heads whose state histories fit the host-memory budget
+    P = cpu_sample_heads(wl, len(os.sched_getaffinity(0)))
     for _ in range(args.warmup):
-        cpu_baseline_sample(wl, d, wl.B * wl.H)
+        cpu_baseline_sample(wl, d, P)
     times, toks = [], 0.0
     for _ in range(args.steps):
-        v, used, P, dt = cpu_baseline_sample(wl, d, wl.B * wl.H)
+        v, used, P, dt = cpu_baseline_sample(wl, d, P)
         times.append(dt)
         toks += wl.T * P / wl.H
     value = toks / sum(times)
@@ -252,12 +304,15 @@ def run_gpu(args):
     dist = _init_pg(world, "nccl")
     wkv7.load()
     dev = torch.device("cuda", local)
-    wl = configs.WORKLOADS[configs.BENCH_WORKLOAD]
+    wl = configs.WORKLOADS[args.shape]
     B, T, H, N = wl.B, wl.T, wl.H, wl.N
     if args.T:  # shorter sequence of the same layer shape, for profiler captures
         T = args.T
     bf16 = wl.storage == "bf16"
-    C = wkv7.wkv7_default_ckpt_every(N, bf16)
+    if args.workload != "wkv7" and not bf16:
+        raise RuntimeError(f"--workload {args.workload} runs on bf16 inputs only")
+    # bf16 at N = 64: the chunked kernels' 16-step checkpoints; fp32: the workload's interval
+    C = wkv7.wkv7_default_ckpt_every(N, bf16) if bf16 else wl.ckpt_every
     names = ("r", "w", "k", "v", "a", "b", "dy")
     d = inputs.generate(B, T, H, N, wl.storage, wl.s_init_std, seed=shard_seed(rank))
     logit = args.workload == "wkv7-logit"  # the decay given as logits z, w formed in the kernels
@@ -444,15 +499,18 @@ def _report(args, wl, world, B, T, H, N, C, bf16, ms, fwd_ms, bwd_ms, e2e, ckpt,
     t_roof = max((f_flop + b_flop) * BTH / peak_flops, (f_bytes + b_bytes) * BTH / (peaks["hbm_gbs"] * 1e9))
     value = aggregate_tokens_per_s(world, B, T, ms)
     with_cpu = not args.no_cpu_baseline and T == wl.T and args.workload == "wkv7"  # the plain scan's oracle
-    cpu_v, cpu_cores, cpu_P, cpu_dt = cpu_baseline_sample(wl, d, B * H) if with_cpu \
-        else (None, 0, 0, 0.0)
+    cpu_v, cpu_cores, cpu_P, cpu_dt = cpu_baseline_sample(
+        wl, d, cpu_sample_heads(wl, len(os.sched_getaffinity(0)))) if with_cpu else (None, 0, 0, 0.0)
+    chunked = bf16 and N == 64
     line = {
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16" if (bf16 and N == 64) else "f32", "data": "synthetic",
         "arithmetic": ("tensor-core products with fp32 accumulation: tf32 operands in the forward and the backward's "
-                       "carry chain, bf16 operands in the backward's per-chunk gradient products; fp32 state, carry "
-                       "and element-wise math" if (bf16 and N == 64) else "fp32 throughout")
+                       "carry chain (the fp32 state and carry rounded to tf32 where they enter a product), bf16 "
+                       "operands in the backward's per-chunk gradient products (the carry stored as bf16 between "
+                       "the two backward kernels, the fp32 checkpoint rounded to bf16 there); fp32 accumulation, "
+                       "state and element-wise math" if chunked else "fp32 FMA throughout (scalar kernels)")
                       + "; inputs, dy and y stored in " + wl.storage,
         "config": {"workload": (wl.name + {"wkv7-logit": "-decay-logits", "wkv7-epilogue": "-with-epilogue"}.get(
                        args.workload, ""))
@@ -461,11 +519,15 @@ def _report(args, wl, world, B, T, H, N, C, bf16, ms, fwd_ms, bwd_ms, e2e, ckpt,
                          % ((7 * BTH * N * (2 if bf16 else 4) + ckpt.numel() * 4 + 6 * BTH * N * 4) / 1e9)},
         "fwd_ms": fwd_ms, "bwd_ms": bwd_ms, "step_roofline_frac": t_roof / (ms * 1e-3),
         "roofline": {"bound": "alu", "achieved": achieved / 1e12, "peak": peak_flops / 1e12, "unit": "TFLOP/s",
-                     "frac": achieved / peak_flops, "traffic": measured_traffic(BTH), "kernel": TRAFFIC["kernel"],
-                     "note": "the backward call (its two kernels, timed together with CUDA events around the "
-                             "call): algorithmic FLOP of the recurrence (24 N^2 per token-head) against the FP32 "
-                             "CUDA-core peak, the roofline the metric names; the kernels form them as tensor-core "
-                             "products (tf32 in the carry chain, bf16 in the output pass)",
+                     "frac": achieved / peak_flops,
+                     "traffic": measured_traffic(BTH) if chunked else measured_traffic_fp32(BTH, N),
+                     "kernel": TRAFFIC["kernel"] if chunked else TRAFFIC_FP32["kernel"],
+                     "note": ("the backward call (its two kernels, timed together with CUDA events around the "
+                              "call): algorithmic FLOP of the recurrence (24 N^2 per token-head) against the FP32 "
+                              "CUDA-core peak, the roofline the metric names; the kernels form them as tensor-core "
+                              "products (tf32 in the carry chain, bf16 in the output pass)") if chunked else
+                             ("the backward call (one kernel, timed with CUDA events around the call): algorithmic "
+                              "FLOP of the recurrence (24 N^2 per token-head) against the FP32 CUDA-core peak"),
                      "peak_source": f"{sms} SMs x {FP32_LANES_PER_SM} FP32 lanes x 2 x {peaks['sm_max_mhz']:.0f} MHz",
                      "hbm_gbs_achieved": b_bytes * BTH / (bwd_ms * 1e-3) / 1e9, "hbm_peak_gbs": peaks["hbm_gbs"]},
         "e2e": None if e2e is None else {
@@ -480,6 +542,9 @@ def _report(args, wl, world, B, T, H, N, C, bf16, ms, fwd_ms, bwd_ms, e2e, ckpt,
                         "pass, the scan's backward, the bonus terms and the parameters' gradients")
     elif args.workload == "wkv7-logit":
         line["note"] = "the decay given as logits z and formed inside the scan kernels; dz returned in the place of dw"
+    if wl.name != configs_bench_workload():
+        line["note"] = (f"the {wl.name} workload (B={B}, T={T}, H={H}, N={N}, {wl.storage}); the metric's own "
+                        "workload is the default run")
     if cpu_v is not None:
         line["cpu_baseline"] = {"value": cpu_v, "unit": "tokens/s", "cores": cpu_cores, "kind": "oracle",
                                 "sample": f"{cpu_P} of {B * H} (b,h) heads, full T={T}, fwd+bwd fp64 ({cpu_dt:.1f} s)"}
@@ -720,7 +785,16 @@ def main():
                          "given as logits and formed inside the kernels; wkv7-epilogue: the same step with the "
                          "group-norm + bonus epilogue (fused into the forward) and its backward; rwkv8: the "
                          "RWKV-8 recurrence")
+    ap.add_argument("--shape", default=None,
+                    help="WKV7 workload by name (linear_rnn_state_gb300/configs.py): rwkv7-1.5b-layer-bf16 "
+                         "(default, the metric's), rwkv7-0.1b-layer-fp32, long-carry-fp32, small-fp32-carry, "
+                         "tiny-fp32")
     args = ap.parse_args()
+    from linear_rnn_state_gb300 import configs
+
+    args.shape = args.shape or configs.BENCH_WORKLOAD
+    if args.shape not in configs.WORKLOADS:
+        ap.error(f"unknown --shape {args.shape}; one of {', '.join(configs.WORKLOADS)}")
     if args.workload == "rwkv8":
         return run_rwkv8(args)
     if args.impl == "reference":

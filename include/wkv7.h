@@ -73,7 +73,14 @@ int wkv7_forward(const float* r, const float* w, const float* k, const float* v,
                  int ckpt_every, int B, int T, int H, int N, void* stream);
 
 /* Forward scan with bfloat16 r, w, k, v, a, b and y; the state, s_init,
- * s_final and the checkpoints stay fp32 and the arithmetic is fp32. */
+ * s_final and the checkpoints are fp32 in memory.
+ * Arithmetic. At N = 64 with checkpoints every multiple of 16 steps (or none)
+ * the chunked tensor-core form runs: every product is a tensor-core product
+ * with tf32 operands (10-bit mantissa) and fp32 accumulation, and the carried
+ * state, held and decayed in fp32, is rounded to tf32 where it enters one;
+ * the element-wise work (decay products, the triangular solve) is fp32. The
+ * bfloat16 y is rounded once from the fp32 result. Other N or checkpoint
+ * intervals run fp32 FMA throughout. */
 int wkv7_forward_bf16(const wkv7_bf16* r, const wkv7_bf16* w, const wkv7_bf16* k, const wkv7_bf16* v,
                       const wkv7_bf16* a, const wkv7_bf16* b, const float* s_init, wkv7_bf16* y,
                       float* s_final, float* ckpt, int ckpt_every, int B, int T, int H, int N,
@@ -100,16 +107,21 @@ int wkv7_backward(const float* r, const float* w, const float* k, const float* v
                   float* dS_init, int B, int T, int H, int N, void* stream);
 
 /* Backward with bfloat16 r, w, k, v, a, b and dy; checkpoints, s_init and every
- * gradient are fp32, as are the state, the carried gradient and every sum.
- * At N = 64 with 16-step checkpoints the chunked tensor-core form runs: the
- * carried gradient G at every chunk boundary is computed first (one sequential
- * pass per (b, h)) and kept in a workspace of B*H*ceil(T/16)*N*N bf16 values,
- * then every chunk's gradients are formed independently; the workspace is taken
- * with cudaMallocAsync on `stream` and freed on it after the call (together with
+ * gradient are fp32 in memory.
+ * At N = 64 with 16-step checkpoints the chunked tensor-core form runs, split
+ * in two passes. The carried gradient G at every chunk boundary is computed
+ * first (one sequential pass per (b, h): tf32 operands, fp32 accumulation, G
+ * carried in fp32) and stored as bfloat16 in a workspace of
+ * B*H*ceil(T/16)*N*N values. Then every chunk's gradients are formed
+ * independently with bfloat16 operands and fp32 accumulation: the chunk's
+ * inputs, its stored bfloat16 carry and its fp32 checkpoint rounded once to
+ * bfloat16; the decay scaling, the triangular solve and the dw sums are fp32.
+ * (Measured relative L2 error of the gradients against an fp64 reference at
+ * 4 x 4096 x 32 heads: 2e-3 to 5e-3.) The workspace is taken with
+ * cudaMallocAsync on `stream` and freed on it after the call (together with
  * the checkpoint workspace when ckpt is NULL), so WKV7_ERR_ALLOC can also be
- * returned when ckpt is given. Setting the environment variable
- * WKV7_SPLIT_BACKWARD=0 selects a fused form instead (one pass per (b, h), no
- * carry workspace). */
+ * returned when ckpt is given. wkv7_backward_fused_bf16 runs the other form.
+ * Other N or checkpoint intervals run fp32 FMA throughout. */
 int wkv7_backward_bf16(const wkv7_bf16* r, const wkv7_bf16* w, const wkv7_bf16* k, const wkv7_bf16* v,
                        const wkv7_bf16* a, const wkv7_bf16* b, const wkv7_bf16* dy, const float* s_init,
                        const float* ckpt, int ckpt_every, float* dr, float* dw, float* dk, float* dv,
@@ -141,14 +153,30 @@ int wkv7_backward_segment_bf16(const wkv7_bf16* r, const wkv7_bf16* w, const wkv
                                int N, void* stream);
 
 /*
+ * The fused chunked backward (bfloat16 inputs, N = 64, 16-step checkpoints or
+ * ckpt NULL): one pass per (b, h) over the chunks in reverse, with tf32
+ * operands and fp32 accumulation in every product and the carried gradient
+ * kept in fp32 (relative L2 error of the gradients about 5e-4, against 2e-3
+ * to 5e-3 for the split form), and no carry workspace; slower than the split
+ * form when B*H is below a few times the SM count. Arguments, layouts and
+ * status codes as wkv7_backward_segment_bf16; N other than 64 or an interval
+ * other than 16 return WKV7_ERR_INVALID.
+ */
+int wkv7_backward_fused_bf16(const wkv7_bf16* r, const wkv7_bf16* w, const wkv7_bf16* k, const wkv7_bf16* v,
+                             const wkv7_bf16* a, const wkv7_bf16* b, const wkv7_bf16* dy, const float* s_init,
+                             const float* dS_final, const float* ckpt, int ckpt_every, float* dr, float* dw,
+                             float* dk, float* dv, float* da, float* db, float* dS_init, int B, int T, int H, int N,
+                             void* stream);
+
+/*
  * The decay given as logits (bfloat16 inputs, N = 64, 16-step checkpoints).
  * The RWKV-7 time-mix ("rx_pretrain.c", tm_pre_forward) forms the decay from a
  * logit z as w = exp(-0.606531 sigmoid(z)) (RX_WDECAY_COEFF); these calls take
  * z [B][T][H][N] in the place of w and form w in fp32 inside the scan kernels
  * where the decay tile is read, so w never exists in memory. The backward
  * returns dz = dL/dz (its backward's chain dw w (-0.606531) sigmoid(z)
- * (1 - sigmoid(z))) in the place of dw, and always runs the split chunked form
- * (WKV7_SPLIT_BACKWARD is not read). Other arguments, layouts, workspaces and
+ * (1 - sigmoid(z))) in the place of dw, and runs the split chunked form, with
+ * the arithmetic of wkv7_backward_bf16. Other arguments, layouts, workspaces and
  * status codes as wkv7_forward_bf16 and wkv7_backward_segment_bf16; N other
  * than 64, or checkpoints with an interval other than 16, return
  * WKV7_ERR_INVALID.

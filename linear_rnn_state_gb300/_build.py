@@ -3,6 +3,11 @@
 The translation units compile in parallel, then link into one shared library
 that uses the shared CUDA runtime (the same libcudart.so.13 PyTorch loads, so
 both see the same current device).
+
+It also links the debug build, libwkv7_debug.so: the same objects except the
+C ABI and the scalar forward, recompiled with WKV7_DEBUG (1 ms mbarrier wait
+limit, and the hook of include/wkv7_debug.h that lets a test make a wait run
+out). Only the tests of the timeout path load it.
 """
 from __future__ import annotations
 
@@ -17,6 +22,8 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD_DIR = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libwkv7.so")
+DEBUG_LIB = os.path.join(PKG, "libwkv7_debug.so")
+DEBUG_SOURCES = ["wkv7_api.cu", "wkv7_fwd2.cu"]  # recompiled with -DWKV7_DEBUG for the debug build
 
 SOURCES = ["wkv7_api.cu", "wkv7_fwd2.cu", "wkv7_fwd3.cu", "wkv7_bwd2.cu", "wkv7_bwd3.cu", "wkv7_bwd4.cu", "rwkv8_api.cu",
            "rwkv8_fwd.cu", "rwkv8_bwd.cu", "rwkv8_state.cu", "rwkv8_chunk.cu", "wkv7_epilogue.cu"]
@@ -49,14 +56,20 @@ def _stale(target: str, deps) -> bool:
 def build(force: bool = False, verbose: bool = False, extra_flags=()) -> str:
     """Compile every .cu to an object (in parallel) and link libwkv7.so."""
     os.makedirs(BUILD_DIR, exist_ok=True)
-    headers = [os.path.join(CSRC, h) for h in HEADERS] + [os.path.join(INCLUDE, h) for h in ("wkv7.h", "rwkv8.h")]
-    objs, jobs = [], []
+    headers = [os.path.join(CSRC, h) for h in HEADERS] + [os.path.join(INCLUDE, h)
+                                                          for h in ("wkv7.h", "rwkv8.h", "wkv7_debug.h")]
+    objs, dobjs, jobs = [], [], []
     for src in SOURCES:
         s = os.path.join(CSRC, src)
         o = os.path.join(BUILD_DIR, src.replace(".cu", ".o"))
         objs.append(o)
         if force or _stale(o, [s] + headers):
             jobs.append([nvcc(), *NVCC_FLAGS, *extra_flags, "-c", s, "-o", o])
+        if src in DEBUG_SOURCES:
+            o = os.path.join(BUILD_DIR, src.replace(".cu", ".debug.o"))
+            if force or _stale(o, [s] + headers):
+                jobs.append([nvcc(), *NVCC_FLAGS, *extra_flags, "-DWKV7_DEBUG", "-c", s, "-o", o])
+        dobjs.append(o)
 
     def run(cmd):
         res = subprocess.run(cmd, capture_output=True, text=True)
@@ -67,11 +80,12 @@ def build(force: bool = False, verbose: bool = False, extra_flags=()) -> str:
 
     with ThreadPoolExecutor(max_workers=max(1, len(jobs))) as ex:
         list(ex.map(run, jobs))
-    if force or jobs or _stale(LIB, objs):
-        tmp = LIB + f".tmp{os.getpid()}"
-        run([nvcc(), *ARCH, "-shared", "-cudart", "shared", "-o", tmp, *objs,
-             "-Xlinker", f"-rpath,{_cuda_lib_dir()}"])
-        os.replace(tmp, LIB)
+    for lib, parts in ((LIB, objs), (DEBUG_LIB, dobjs)):
+        if force or jobs or _stale(lib, parts):
+            tmp = lib + f".tmp{os.getpid()}"
+            run([nvcc(), *ARCH, "-shared", "-cudart", "shared", "-o", tmp, *parts,
+                 "-Xlinker", f"-rpath,{_cuda_lib_dir()}"])
+            os.replace(tmp, lib)
     return LIB
 
 

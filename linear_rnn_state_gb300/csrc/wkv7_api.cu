@@ -2,6 +2,7 @@
 // the backward's optional checkpoint workspace, and the device status word.
 #include <cudaTypedefs.h>
 
+#include <atomic>
 #include <cstdarg>
 #include <cstdio>
 #include <cstdlib>
@@ -9,6 +10,9 @@
 #include <string>
 
 #include "wkv7.h"
+#ifdef WKV7_DEBUG
+#include "wkv7_debug.h"
+#endif
 #include "wkv7_common.cuh"
 #include "wkv7_epilogue.h"
 #include "wkv7_launch.h"
@@ -156,6 +160,11 @@ int status_word(unsigned** out) {
   return WKV7_OK;
 }
 
+#ifdef WKV7_DEBUG
+// Debug build: set by wkv7_debug_skip_last_load (include/wkv7_debug.h).
+std::atomic<int> g_debug_skip_last_load{0};
+#endif
+
 // ------------------------------------------------------------ forward ---
 
 // The epilogue of wkv7_forward_epilogue_bf16 (null for the plain forward).
@@ -223,6 +232,9 @@ int forward_impl(bool bf16, const void* const in[6], const float* s_init, void* 
     args.nv = epi->nv;
     args.stats = epi->stats;
   }
+#ifdef WKV7_DEBUG
+  args.debug_skip_last_load = g_debug_skip_last_load.load();
+#endif
   args.C = ckpt ? C : 1;
   args.nck = ckpt ? (T + C - 1) / C : 0;
   args.B = B;
@@ -235,15 +247,22 @@ int forward_impl(bool bf16, const void* const in[6], const float* s_init, void* 
 
 // ----------------------------------------------------------- backward ---
 
+// Which chunked backward runs for bf16 inputs at N = 64 with 16-step
+// checkpoints: the split pair (default) or the fused one-pass kernel.
+enum class BwdForm { kAuto, kFused };
+
 int backward_impl(bool bf16, const void* const in[7], const float* s_init, const float* dS_final, const float* ckpt,
                   int C, float* const grads[6], float* dS_init, int B, int T, int H, int N, cudaStream_t stream,
-                  bool logit = false) {
+                  bool logit = false, BwdForm form = BwdForm::kAuto) {
   int rc = check_dims(B, T, H, N);
   if (rc) return rc;
   if (ckpt && C < 1) return fail(WKV7_ERR_INVALID, "ckpt_every must be >= 1 (got %d)", C);
   const int C_eff = ckpt ? C : (C >= 1 ? C : bwd2_steps_per_window(N, bf16));
   if (logit && (N != 64 || C_eff != kChunk))
     return fail(WKV7_ERR_INVALID, "decay logits need N = 64 and ckpt_every = %d (got N = %d, %d)", kChunk, N, C_eff);
+  if (form == BwdForm::kFused && (N != 64 || C_eff != kChunk))
+    return fail(WKV7_ERR_INVALID, "the fused backward needs N = 64 and ckpt_every = %d (got N = %d, %d)", kChunk, N,
+                C_eff);
   const size_t es = bf16 ? 2 : 4;
   const size_t vec = (size_t)B * T * H * N * es;
   const size_t gvec = (size_t)B * T * H * N * 4;
@@ -271,12 +290,10 @@ int backward_impl(bool bf16, const void* const in[7], const float* s_init, const
 
   // bf16 inputs at N = 64 with 16-step checkpoints take a chunked tensor-core
   // backward: the split one (carry chain + parallel output pass), which keeps
-  // the carry of every chunk in the workspace too, or, with
-  // WKV7_SPLIT_BACKWARD=0, the fused one (one CTA per head).
+  // the carry of every chunk in the workspace too, or, when the caller asks
+  // for it (wkv7_backward_fused_bf16), the fused one (one CTA per head).
   const bool chunked = bf16 && N == 64 && C_eff == kChunk;
-  const char* split_env = std::getenv("WKV7_SPLIT_BACKWARD");
-  // decay logits run only in the split form
-  const bool split = chunked && (logit || !(split_env && split_env[0] == '0'));
+  const bool split = chunked && form != BwdForm::kFused;
   const size_t ck_ws = ckpt ? 0 : (ckpt_bytes(B, T, H, N, C_eff) + 255) / 256 * 256;
   const size_t ws_bytes = ck_ws + (split ? bwd4_workspace_bytes(B, T, H) : 0);
   if (ws_bytes) {
@@ -544,6 +561,17 @@ int wkv7_backward_bf16(const wkv7_bf16* r, const wkv7_bf16* w, const wkv7_bf16* 
                        static_cast<cudaStream_t>(stream));
 }
 
+int wkv7_backward_fused_bf16(const wkv7_bf16* r, const wkv7_bf16* w, const wkv7_bf16* k, const wkv7_bf16* v,
+                             const wkv7_bf16* a, const wkv7_bf16* b, const wkv7_bf16* dy, const float* s_init,
+                             const float* dS_final, const float* ckpt, int ckpt_every, float* dr, float* dw,
+                             float* dk, float* dv, float* da, float* db, float* dS_init, int B, int T, int H, int N,
+                             void* stream) {
+  const void* in[7] = {r, w, k, v, a, b, dy};
+  float* const grads[6] = {dr, dw, dk, dv, da, db};
+  return backward_impl(true, in, s_init, dS_final, ckpt, ckpt_every, grads, dS_init, B, T, H, N,
+                       static_cast<cudaStream_t>(stream), false, BwdForm::kFused);
+}
+
 int wkv7_forward_logit_bf16(const wkv7_bf16* r, const wkv7_bf16* z, const wkv7_bf16* k, const wkv7_bf16* v,
                             const wkv7_bf16* a, const wkv7_bf16* b, const float* s_init, wkv7_bf16* y,
                             float* s_final, float* ckpt, int ckpt_every, int B, int T, int H, int N, void* stream) {
@@ -675,6 +703,13 @@ int wkv7_status(void* stream) {
 }
 
 const char* wkv7_last_error(void) { return t_last_error.c_str(); }
+
+#ifdef WKV7_DEBUG
+int wkv7_debug_skip_last_load(int on) {
+  g_debug_skip_last_load.store(on ? 1 : 0);
+  return WKV7_OK;
+}
+#endif
 
 int wkv7_backward_noalloc(const float* r, const float* w, const float* k, const float* v, const float* a,
                           const float* b, const float* dy, const float* s_init, float* dr, float* dw, float* dk,

@@ -38,9 +38,13 @@
 //    chunk's own column products: with S(L) = S0 diag(c(L)) + V^T Kb + SA^T Bb,
 //      colsum(Gc o S(L)) = c(L) colsum(Gc o S0) + sum_t (Kb o V Gc + Bb o SA Gc)
 //      colsum(Gc' o S0)  = c(L) colsum(Gc o S0) + sum_t (R^ o DY S0 + A^ o DSA S0).
-// All products run on tf32 tensor cores (mma.sync m16n8k8) with fp32
-// accumulation. A chunk whose decays leave [1/16, 16] (or hold a NaN) is run
-// step by step in fp32 by both kernels.
+// Arithmetic: every product accumulates in fp32. The carry kernel's products
+// take tf32 operands (mma.sync m16n8k8) and carry Gc in fp32, storing it as
+// bf16 for the output kernel. The output kernel's products take bf16 operands
+// (mma.sync m16n8k16): the chunk's inputs, the stored bf16 carry, and the fp32
+// checkpoint rounded once to bf16; its scaling, triangular solve and dw sums
+// are fp32. A chunk whose decays leave [1/16, 16] (or hold a NaN) is run step
+// by step in fp32 by both kernels.
 #include "wkv7_decay.cuh"
 #include "wkv7_launch.h"
 #include "wkv7_mma.cuh"

@@ -78,11 +78,19 @@ __device__ __forceinline__ uint64_t globaltimer_ns() {
   return t;
 }
 
+// How long a kernel waits on an mbarrier before it gives up: about 2 s, or
+// 1 ms in the debug build (WKV7_DEBUG), whose tests make a wait run out.
+#ifdef WKV7_DEBUG
+constexpr uint64_t kWaitLimitNs = 1000000ull;
+#else
+constexpr uint64_t kWaitLimitNs = 2000000000ull;
+#endif
+
 // Wait for the phase with the given parity to complete, giving up after
 // about `limit_ns` nanoseconds. On timeout the status word records it and the
 // function returns false; the caller then leaves the kernel.
 __device__ __forceinline__ bool mbar_wait_bounded(unsigned* status, uint64_t* bar, uint32_t parity,
-                                                  uint64_t limit_ns = 2000000000ull) {
+                                                  uint64_t limit_ns = kWaitLimitNs) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t start = globaltimer_ns();
   for (uint32_t spin = 1;; ++spin) {

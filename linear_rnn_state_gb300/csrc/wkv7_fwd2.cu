@@ -107,6 +107,12 @@ __global__ void __launch_bounds__(Fwd2Cfg<TIn, N, R, E, K>::THREADS)
   }
   __syncthreads();
   auto issue = [&](int chunk, int st) {
+#ifdef WKV7_DEBUG
+    // The timeout test's hook: no load for the last chunk. Every earlier
+    // chunk has been waited for by then, so nothing is in flight when that
+    // wait gives up and the CTA leaves.
+    if (args.debug_skip_last_load && chunk == nchunks - 1) return;
+#endif
     mbar_arrive_expect_tx(&full[st], Cfg::RAW_STAGE_BYTES);
     TIn* dst = raw + st * Cfg::RAW_STAGE;
     for (int v = 0; v < Cfg::NVEC; ++v) tma_load_4d(dst + v * RV, &args.map[v], &full[st], 0, hi, chunk * K, bi);

@@ -30,6 +30,10 @@ struct FwdArgs {
   int C;                // checkpoint interval (steps)
   int nck;              // ceil(T / C)
   int B, T, H;
+  // Debug build only (WKV7_DEBUG): 1 makes the scalar forward issue no load
+  // (and no expected-byte count) for its last chunk, so the wait for that
+  // chunk runs out with nothing in flight. Ignored by every other build.
+  int debug_skip_last_load = 0;
 };
 
 // Backward kernel arguments. Tensor maps for r, w, k, v, a, b, dy with a box

@@ -31,6 +31,7 @@ EXPORTS = {
     "wkv7_backward_noalloc": 20,
     "wkv7_forward_logit_bf16": 16,
     "wkv7_backward_logit_bf16": 23,
+    "wkv7_backward_fused_bf16": 23,
     "wkv7_forward_epilogue_bf16": 22,
     "wkv7_backward_epilogue_bf16": 31,
 }
@@ -78,6 +79,8 @@ def load(path: str | None = None):
     lib.wkv7_forward_logit_bf16.restype = i
     lib.wkv7_backward_logit_bf16.argtypes = [vp] * 10 + [i] + [vp] * 7 + [i] * 4 + [vp]
     lib.wkv7_backward_logit_bf16.restype = i
+    lib.wkv7_backward_fused_bf16.argtypes = [vp] * 10 + [i] + [vp] * 7 + [i] * 4 + [vp]
+    lib.wkv7_backward_fused_bf16.restype = i
     lib.wkv7_forward_epilogue_bf16.argtypes = [vp] * 15 + [i] * 6 + [vp]
     lib.wkv7_forward_epilogue_bf16.restype = i
     lib.wkv7_backward_epilogue_bf16.argtypes = [vp] * 14 + [i, i] + [vp] * 10 + [i] * 4 + [vp]
@@ -131,6 +134,13 @@ def wkv7_backward_segment_bf16(r, w, k, v, a, b, dy, s_init, dS_final, ckpt, ckp
     """wkv7_backward_segment_bf16 (include/wkv7.h): pointers as ints."""
     return load().wkv7_backward_segment_bf16(r, w, k, v, a, b, dy, s_init, dS_final, ckpt, ckpt_every, dr, dw, dk,
                                              dv, da, db, dS_init, B, T, H, N, stream)
+
+
+def wkv7_backward_fused_bf16(r, w, k, v, a, b, dy, s_init, dS_final, ckpt, ckpt_every, dr, dw, dk, dv, da, db,
+                             dS_init, B, T, H, N, stream):
+    """wkv7_backward_fused_bf16 (include/wkv7.h): the one-pass chunked backward."""
+    return load().wkv7_backward_fused_bf16(r, w, k, v, a, b, dy, s_init, dS_final, ckpt, ckpt_every, dr, dw, dk, dv,
+                                           da, db, dS_init, B, T, H, N, stream)
 
 
 def wkv7_backward_noalloc(r, w, k, v, a, b, dy, s_init, dr, dw, dk, dv, da, db, dS_init, B, T, H, N, stream):
@@ -210,11 +220,12 @@ def forward(r, w, k, v, a, b, s_init=None, *, ckpt_every: int | None = None, wan
 
 
 def backward(r, w, k, v, a, b, dy, s_init=None, ckpt=None, ckpt_every: int = 0, *, want_dS_init: bool = True,
-             dS_final=None, stream=None):
+             dS_final=None, fused: bool = False, stream=None):
     """Backward-through-time. Returns dict dr, dw, dk, dv, da, db (float32
     [B][T][H][N]) and dS_init (float32 [B][H][N][N] or None). dS_final
     (float32 [B][H][N][N]) is the gradient entering through the final state
-    (None: zero)."""
+    (None: zero). fused=True runs wkv7_backward_fused_bf16 (bfloat16 inputs,
+    N = 64, 16-step checkpoints)."""
     import torch
 
     bf16 = _inputs_dtype(r)
@@ -223,6 +234,8 @@ def backward(r, w, k, v, a, b, dy, s_init=None, ckpt=None, ckpt_every: int = 0, 
     g = {n: torch.empty((B, T, H, N), dtype=torch.float32, device=dev) for n in ("dr", "dw", "dk", "dv", "da", "db")}
     g["dS_init"] = torch.empty((B, H, N, N), dtype=torch.float32, device=dev) if want_dS_init else None
     fn = wkv7_backward_segment_bf16 if bf16 else wkv7_backward_segment
+    if fused:
+        fn = wkv7_backward_fused_bf16
     _check(fn(*(_addr(x) for x in (r, w, k, v, a, b, dy, s_init, dS_final, ckpt)), ckpt_every,
               *(_addr(g[n]) for n in ("dr", "dw", "dk", "dv", "da", "db", "dS_init")), B, T, H, N, _stream(stream)))
     return g

@@ -37,6 +37,22 @@ def test_exports_every_declared_function(lib):
     assert sorted(lib.EXPORTS) == declared
 
 
+def test_debug_hook_only_in_the_debug_build(lib):
+    """include/wkv7_debug.h's entry point is exported by libwkv7_debug.so
+    alone; the product library does not carry it."""
+    from linear_rnn_state_gb300 import _build
+
+    text = re.sub(r"/\*.*?\*/", "", open(os.path.join(ROOT, "include", "wkv7_debug.h")).read(), flags=re.S)
+    names = sorted(set(re.findall(r"\b(wkv7_\w+)\s*\(", text)))
+    assert names == ["wkv7_debug_skip_last_load"]
+    dbg = lib.load(_build.DEBUG_LIB)
+    for n in names:
+        assert hasattr(dbg, n)
+        assert not hasattr(lib.load(), n)
+    for n in lib.EXPORTS:  # the debug build is otherwise the same library
+        assert hasattr(dbg, n)
+
+
 def test_missing_library_fails_loudly(lib):
     with pytest.raises(RuntimeError, match="not built"):
         lib.load("/nonexistent/libwkv7.so")
@@ -113,10 +129,21 @@ def test_chunked_backward_reports_carry_workspace_failure(lib, monkeypatch):
     # bf16 inputs at N = 64 with 16-step checkpoints keep the carry of every chunk in a
     # workspace even when the checkpoints are given
     monkeypatch.setenv("WKV7_FAIL_ALLOC", "1")
-    monkeypatch.delenv("WKV7_SPLIT_BACKWARD", raising=False)
     rc = lib.wkv7_backward_bf16(*_bwd_args(T=32, N=64, C=16))
     assert rc == lib.ERR_ALLOC
     assert "WKV7_FAIL_ALLOC" in lib.last_error()
+
+
+def test_fused_backward_rejects_unsupported_shapes(lib):
+    """The fused backward exists only in the chunked form: N = 64, 16-step
+    checkpoints."""
+    a = list(_bwd_args(T=32, N=32, C=16))
+    a.insert(8, None)  # dS_final
+    assert lib.wkv7_backward_fused_bf16(*a) == lib.ERR_INVALID
+    assert "fused" in lib.last_error()
+    a = list(_bwd_args(T=32, N=64, C=8))
+    a.insert(8, None)
+    assert lib.wkv7_backward_fused_bf16(*a) == lib.ERR_INVALID
 
 
 def test_empty_problems_need_no_device(lib):

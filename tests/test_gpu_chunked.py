@@ -1,14 +1,19 @@
 """GPU parity of the chunked tensor-core kernels (bf16 inputs, N = 64,
-checkpoints every multiple of 16 steps) against the fp64 oracle.
+checkpoints every multiple of 16 steps) against the fp64 oracle, for both
+backward forms: the split one (wkv7_backward_bf16) and the fused one
+(wkv7_backward_fused_bf16).
 
-Bar: per output tensor, ||gpu - ref||_2 / ||ref||_2 <= 2e-2 (the bf16-input
-tolerance); the oracle reads exactly the bf16 values stored on the GPU.
-Cases span several 16-step chunks, ragged tails, a carried initial state,
-and chunks whose decays leave the range of the scaled form (w = 0, w > 16),
-which the kernels run in the direct form.
+Bar (parity_bars.check_bf16): relative L2 <= 2e-2 over each output tensor and
+over each of its (b, h, 16-step chunk) blocks, plus an element-wise guard;
+the oracle reads exactly the bf16 values stored on the GPU. Cases span
+several 16-step chunks, ragged tails, a carried initial state, and chunks
+whose decays leave the range of the scaled form (w = 0, w > 16), which the
+kernels run in the direct form.
 """
 import numpy as np
 import pytest
+
+from parity_bars import check_bf16
 
 pytestmark = pytest.mark.gpu
 
@@ -16,7 +21,6 @@ torch = pytest.importorskip("torch")
 
 NAMES = ("r", "w", "k", "v", "a", "b")
 GRADS = ("dr", "dw", "dk", "dv", "da", "db")
-REL_L2 = 2e-2
 
 
 @pytest.fixture(scope="module", params=["fused", "split"])
@@ -30,11 +34,7 @@ def env(request):
     _build.build()
     wkv7.load()
     torch.cuda.set_device(0)
-    # the backward variant is chosen per call from the environment
-    import os
-    os.environ["WKV7_SPLIT_BACKWARD"] = "1" if request.param == "split" else "0"
-    yield oracle, inputs, wkv7
-    os.environ.pop("WKV7_SPLIT_BACKWARD", None)
+    return oracle, inputs, wkv7, request.param == "fused"
 
 
 def _bf16_bits(x):
@@ -44,43 +44,39 @@ def _bf16_bits(x):
     return u.astype(np.uint16)
 
 
-def _rel(got, ref):
-    got = np.asarray(got, dtype=np.float64)
-    return np.linalg.norm(got - ref) / max(np.linalg.norm(ref), 1e-30)
-
-
 def _check(env, d, C, s_init_std=None, use_ckpt=True, label=""):
-    oracle, inputs, wkv7 = env
+    oracle, inputs, wkv7, fused = env
     dev = torch.device("cuda:0")
     t = {n: torch.from_numpy(d[n]).view(torch.bfloat16).to(dev) for n in NAMES + ("dy",)}
     s0_np = None if d.get("s_init") is None else d["s_init"].astype(np.float32)
     s0 = None if s0_np is None else torch.from_numpy(s0_np).to(dev)
     y, s_final, ckpt, C = wkv7.forward(*(t[n] for n in NAMES), s0, ckpt_every=C, want_ckpt=use_ckpt)
-    g = wkv7.backward(*(t[n] for n in NAMES), t["dy"], s0, ckpt if use_ckpt else None, C if use_ckpt else 0)
+    # the fused form exists for 16-step checkpoints; longer intervals run the scalar kernels
+    g = wkv7.backward(*(t[n] for n in NAMES), t["dy"], s0, ckpt if use_ckpt else None, C if use_ckpt else 0,
+                      fused=fused and (C == 16 or not use_ckpt))
     wkv7.status()
     o = {n: inputs.as_f64(d[n], "bf16") for n in NAMES + ("dy",)}
     s0_64 = None if s0_np is None else s0_np.astype(np.float64)
     y_ref, sf_ref = oracle.forward(*(o[n] for n in NAMES), s0_64)
     g_ref = oracle.backward(*(o[n] for n in NAMES), o["dy"], s0_64)
-    pairs = [("y", y.float().cpu().numpy(), y_ref), ("s_final", s_final.cpu().numpy(), sf_ref)]
-    pairs += [(n, g[n].cpu().numpy(), g_ref[n]) for n in GRADS + ("dS_init",)]
-    for name, got, ref in pairs:
-        assert np.all(np.isfinite(got)), f"{name}{label}: non-finite values"
-        rel = _rel(got, ref)
-        assert rel <= REL_L2, f"{name}{label}: relative L2 error {rel:.3e}"
+    check_bf16(f"y{label}", y.float().cpu().numpy(), y_ref)
+    check_bf16(f"s_final{label}", s_final.cpu().numpy(), sf_ref, "state")
+    for n in GRADS:
+        check_bf16(f"{n}{label}", g[n].cpu().numpy(), g_ref[n])
+    check_bf16(f"dS_init{label}", g["dS_init"].cpu().numpy(), g_ref["dS_init"], "state")
     return y, s_final, ckpt
 
 
 @pytest.mark.parametrize("T", [1, 15, 16, 17, 130, 300])
 def test_chunked_ragged_lengths(env, T):
-    _, inputs, _ = env
+    inputs = env[1]
     d = inputs.generate(2, T, 3, 64, "bf16", None, seed=11)
     _check(env, d, 16, label=f" (T={T})")
 
 
 @pytest.mark.parametrize("C,use_ckpt", [(16, True), (32, True), (48, True), (16, False)])
 def test_chunked_checkpoint_intervals_and_carried_state(env, C, use_ckpt):
-    _, inputs, _ = env
+    inputs = env[1]
     d = inputs.generate(2, 200, 2, 64, "bf16", 0.1, seed=12)
     _check(env, d, C, use_ckpt=use_ckpt, label=f" (C={C}, ckpt={use_ckpt})")
 
@@ -88,7 +84,7 @@ def test_chunked_checkpoint_intervals_and_carried_state(env, C, use_ckpt):
 def test_chunked_direct_form_chunks(env):
     """Chunks with w = 0 or w > 16 in some columns run step by step; the
     chunks around them stay on the scaled form."""
-    _, inputs, _ = env
+    inputs = env[1]
     d = dict(inputs.generate(1, 100, 2, 64, "bf16", 0.1, seed=13))
     w = inputs.as_f64(d["w"], "bf16").copy()
     w[0, 32:48, 0, :] = 0.0  # head 0: a whole chunk that forgets
@@ -100,7 +96,7 @@ def test_chunked_direct_form_chunks(env):
 
 def test_chunked_outputs_overwritten(env):
     """Poisoned (NaN) outputs: every element is written."""
-    _, inputs, wkv7 = env
+    _, inputs, wkv7, fused = env
     dev = torch.device("cuda:0")
     B, T, H, N, C = 1, 45, 3, 64, 16
     d = inputs.generate(B, T, H, N, "bf16", None, seed=14)
@@ -113,8 +109,9 @@ def test_chunked_outputs_overwritten(env):
                                   ck.data_ptr(), C, B, T, H, N, stream) == 0
     g = {n: torch.full((B, T, H, N), float("nan"), device=dev) for n in GRADS}
     dS = torch.full((B, H, N, N), float("nan"), device=dev)
-    assert wkv7.wkv7_backward_bf16(*(t[n].data_ptr() for n in NAMES), t["dy"].data_ptr(), None, ck.data_ptr(), C,
-                                   *(g[n].data_ptr() for n in GRADS), dS.data_ptr(), B, T, H, N, stream) == 0
+    bwd = wkv7.wkv7_backward_fused_bf16 if fused else wkv7.wkv7_backward_segment_bf16
+    assert bwd(*(t[n].data_ptr() for n in NAMES), t["dy"].data_ptr(), None, None, ck.data_ptr(), C,
+               *(g[n].data_ptr() for n in GRADS), dS.data_ptr(), B, T, H, N, stream) == 0
     wkv7.status()
     for x in [y, sf, ck, dS] + list(g.values()):
         assert torch.isfinite(x).all()
@@ -123,7 +120,7 @@ def test_chunked_outputs_overwritten(env):
 def test_chunked_checkpoints_are_states(env):
     """Checkpoint c is the state before step 16c: a forward over the first 16c
     steps ends in exactly that state (same chunks, same arithmetic)."""
-    _, inputs, wkv7 = env
+    _, inputs, wkv7, fused = env
     dev = torch.device("cuda:0")
     B, T, H, N, C = 1, 70, 2, 64, 16
     d = inputs.generate(B, T, H, N, "bf16", 0.1, seed=15)

@@ -1,14 +1,19 @@
 """Parity at the full sizes of the three large workloads, in the launch
 configuration the benchmark times.
 
-The oracle cannot run these whole, so it recomputes a sample of (b, h) heads
-in full (every step, every output of those heads) and the rest is checked
-through properties that hold at any size: every output finite and the
-per-row identity dr_t . r_t = dy_t . y_t (y is linear in r_t, which enters
-nowhere else).
+The two 4096-step workloads are checked whole: the fp64 oracle recomputes
+every output of every (b, h) head on the host cores (about a second), and
+every element is held to the bar (fp32 inputs |gpu - ref| <= 1e-4 (1 + |ref|);
+bf16 inputs parity_bars.check_bf16, per tensor, per (b, h, 16-step chunk) and
+per element). For the 65536-step workload the oracle recomputes a sample of
+heads in full, and the rest is checked through properties that hold at any
+size: every output finite and the per-row identity dr_t . r_t = dy_t . y_t
+(y is linear in r_t, which enters nowhere else).
 """
 import numpy as np
 import pytest
+
+from parity_bars import check_bf16
 
 pytestmark = [pytest.mark.gpu, pytest.mark.slow]
 
@@ -32,15 +37,15 @@ def env():
     return oracle, inputs, wkv7, configs
 
 
-def _check(name, got, ref, storage):
+def _check(name, got, ref, storage, kind="seq"):
     got = np.asarray(got, dtype=np.float64)
     assert np.all(np.isfinite(got)), name
     if storage == "bf16":
-        rel = np.linalg.norm(got - ref) / max(np.linalg.norm(ref), 1e-30)
-        assert rel <= 2e-2, f"{name}: relative L2 error {rel:.3e}"
+        check_bf16(name, got, ref, kind)
     else:
         err = np.abs(got - ref) / (1.0 + np.abs(ref))
-        assert err.max() <= 1e-4, f"{name}: max scaled error {err.max():.3e}"
+        i = np.unravel_index(np.argmax(err), err.shape)
+        assert err.max() <= 1e-4, f"{name}: max scaled error {err.max():.3e} at {i}"
 
 
 @pytest.mark.parametrize("name", ["rwkv7-0.1b-layer-fp32", "rwkv7-1.5b-layer-bf16", "long-carry-fp32"])
@@ -72,16 +77,24 @@ def test_full_size_workload(env, name):
         assert torch.isfinite(g[n]).all(), n
     assert torch.isfinite(yf).all()
 
-    # sampled heads in full against the oracle
-    heads = [(0, 0), (B - 1, H - 1), (B // 2, H // 2)]
-    if T >= 65536:
-        heads = heads[:2]
     o = {n: inputs.as_f64(d[n], st) for n in NAMES + ("dy",)}
-    y_ref, sf_ref, g_ref = oracle.backward_heads(*(o[n] for n in NAMES), o["dy"],
-                                                  None if s0_np is None else s0_np.astype(np.float64), heads)
+    s064 = None if s0_np is None else s0_np.astype(np.float64)
+    if T <= 4096:  # every head, every output, against the oracle
+        y_ref, sf_ref = oracle.forward(*(o[n] for n in NAMES), s064)
+        g_ref = oracle.backward(*(o[n] for n in NAMES), o["dy"], s064)
+        _check("y", yf.cpu().numpy(), y_ref, st)
+        _check("s_final", s_final.cpu().numpy(), sf_ref, st, "state")
+        for n in GRADS:
+            _check(n, g[n].cpu().numpy(), g_ref[n], st)
+        _check("dS_init", g["dS_init"].cpu().numpy(), g_ref["dS_init"], st, "state")
+        return
+
+    # sampled heads in full against the oracle
+    heads = [(0, 0), (B - 1, H - 1)]
+    y_ref, sf_ref, g_ref = oracle.backward_heads(*(o[n] for n in NAMES), o["dy"], s064, heads)
     for p, (bi, hi) in enumerate(heads):
         _check(f"y[{bi},{hi}]", y[bi, :, hi].float().cpu().numpy(), y_ref[p], st)
-        _check(f"s_final[{bi},{hi}]", s_final[bi, hi].cpu().numpy(), sf_ref[p], st)
+        _check(f"s_final[{bi},{hi}]", s_final[bi, hi].cpu().numpy(), sf_ref[p], st, "state")
         for n in GRADS:
             _check(f"{n}[{bi},{hi}]", g[n][bi, :, hi].cpu().numpy(), g_ref[n][p], st)
-        _check(f"dS_init[{bi},{hi}]", g["dS_init"][bi, hi].cpu().numpy(), g_ref["dS_init"][p], st)
+        _check(f"dS_init[{bi},{hi}]", g["dS_init"][bi, hi].cpu().numpy(), g_ref["dS_init"][p], st, "state")

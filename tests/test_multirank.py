@@ -57,6 +57,87 @@ def test_two_gloo_ranks_agree_on_the_slowest_rank():
     assert s0 != s1  # each rank scans its own batch
 
 
+def _shard_worker(rank, world, port, q):
+    """Each rank runs the oracle's forward and backward on its own (b, h)
+    heads of one shared batch; rank 0 gathers the pieces."""
+    import torch.distributed as dist
+
+    sys.path.insert(0, ROOT)
+    import bench
+    import oracle
+    from linear_rnn_state_gb300 import inputs
+
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port), RANK=str(rank), WORLD_SIZE=str(world))
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    try:
+        B, T, H, N = 3, 40, 3, 16
+        d = inputs.generate(B, T, H, N, "f32", 0.1, seed=5)  # one batch, the same on every rank
+        mine = bench.head_shard(B, H, rank, world)
+        o = {n: d[n].astype(np.float64) for n in ("r", "w", "k", "v", "a", "b", "dy")}
+        y, sf, g = oracle.backward_heads(*(o[n] for n in ("r", "w", "k", "v", "a", "b", "dy")),
+                                         d["s_init"].astype(np.float64), mine, nthreads=1)
+        piece = {"heads": mine, "y": y, "s_final": sf, **g}
+        pieces = [None] * world
+        dist.all_gather_object(pieces, piece)
+        if rank == 0:
+            q.put(pieces)
+    finally:
+        dist.destroy_process_group()
+
+
+def test_head_shards_concatenate_to_the_whole_batch_bit_for_bit():
+    """Splitting one batch by (b, h) heads across two gloo ranks: the pieces
+    cover every head once and, put together, equal the whole-batch oracle run
+    bit for bit, so the split needs no exchange between ranks."""
+    import multiprocessing as mp
+    import socket
+
+    sys.path.insert(0, ROOT)
+    import bench
+    import oracle
+    from linear_rnn_state_gb300 import inputs
+
+    oracle.build()
+    inputs.build()
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        port = s.getsockname()[1]
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    procs = [ctx.Process(target=_shard_worker, args=(r, 2, port, q)) for r in range(2)]
+    for p in procs:
+        p.start()
+    pieces = q.get(timeout=120)
+    for p in procs:
+        p.join(timeout=120)
+        assert p.exitcode == 0
+    B, T, H, N = 3, 40, 3, 16
+    heads = [hd for pc in pieces for hd in pc["heads"]]
+    assert sorted(heads) == [(b, h) for b in range(B) for h in range(H)]
+    assert len(pieces[0]["heads"]) and len(pieces[1]["heads"])
+    d = inputs.generate(B, T, H, N, "f32", 0.1, seed=5)
+    o = {n: d[n].astype(np.float64) for n in ("r", "w", "k", "v", "a", "b", "dy")}
+    s0 = d["s_init"].astype(np.float64)
+    y, sf = oracle.forward(*(o[n] for n in ("r", "w", "k", "v", "a", "b")), s0, nthreads=1)
+    g = oracle.backward(*(o[n] for n in ("r", "w", "k", "v", "a", "b", "dy")), s0, nthreads=1)
+    for pc in pieces:
+        for p, (bi, hi) in enumerate(pc["heads"]):
+            assert np.array_equal(pc["y"][p], y[bi, :, hi])
+            assert np.array_equal(pc["s_final"][p], sf[bi, hi])
+            assert np.array_equal(pc["dS_init"][p], g["dS_init"][bi, hi])
+            for n in ("dr", "dw", "dk", "dv", "da", "db"):
+                assert np.array_equal(pc[n][p], g[n][bi, :, hi]), (n, bi, hi)
+
+
+def test_head_shard_is_a_partition():
+    sys.path.insert(0, ROOT)
+    import bench
+
+    for B, H, world in ((4, 32, 8), (1, 40, 3), (3, 3, 2), (1, 1, 4)):
+        got = [hd for r in range(world) for hd in bench.head_shard(B, H, r, world)]
+        assert got == [(b, h) for b in range(B) for h in range(H)]
+
+
 def test_reference_arm_runs_on_rank_zero_only():
     env = dict(os.environ, RANK="1", WORLD_SIZE="2", LOCAL_RANK="1")
     out = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference", "--steps", "1",

@@ -4,10 +4,14 @@ Some callers of this library cannot allocate device memory: code recording a
 CUDA graph that must not contain allocation nodes, or a framework that owns
 every device byte through its own allocator. wkv7_backward_noalloc serves
 them: its own checkpointing forward writes into a fixed scratch array of the
-library instead of a cudaMallocAsync workspace. This file checks it, through
-the C ABI, against the allocating wkv7_backward on the same inputs, on two
-calls in a row (the scratch keeps whatever the previous call left in it), and
-that a problem larger than the scratch is refused. Collected last on purpose.
+library instead of a cudaMallocAsync workspace.
+
+This file checks it through the C ABI against the fp64 oracle, element by
+element at the fp32 bar, and against the allocating wkv7_backward, on two
+calls in a row of different shapes: the second call's checkpoints land on
+scratch that the first call left holding other data, which the second must
+overwrite before it reads. It also checks that a problem larger than the
+scratch is refused. Collected last on purpose.
 """
 import numpy as np
 import pytest
@@ -18,7 +22,7 @@ torch = pytest.importorskip("torch")
 
 NAMES = ("r", "w", "k", "v", "a", "b")
 GRADS = ("dr", "dw", "dk", "dv", "da", "db")
-TOL = 1e-4  # the fp32 parity bar used by every GPU test: |x - ref| <= TOL * (1 + |ref|)
+TOL = 1e-4  # the fp32 parity bar of every GPU test: |x - ref| <= TOL * (1 + |ref|)
 
 
 @pytest.fixture(scope="module")
@@ -26,48 +30,51 @@ def env():
     if not torch.cuda.is_available():
         pytest.skip("no CUDA device")
     import __graft_entry__  # noqa: F401
+    import oracle
     from linear_rnn_state_gb300 import _build, inputs, wkv7
 
     _build.build()
     wkv7.load()
     torch.cuda.set_device(0)
-    return inputs, wkv7
+    return oracle, inputs, wkv7
 
 
-def _case(inputs, seed, B=2, T=300, H=4, N=64):
+def _assert_close(name, got, ref):
+    got = np.asarray(got, dtype=np.float64)
+    err = np.abs(got - ref) / (1.0 + np.abs(ref))
+    i = np.unravel_index(np.argmax(err), err.shape)
+    assert err.max() <= TOL, f"{name}: max scaled error {err.max():.3e} at {i}: {got[i]} vs {ref[i]}"
+
+
+@pytest.mark.parametrize("shapes", [((1, 97, 3, 64), (2, 300, 4, 64)), ((2, 300, 4, 64), (1, 40, 2, 32))])
+def test_noalloc_backward_matches_the_oracle_on_two_calls(env, shapes):
+    oracle, inputs, wkv7 = env
     dev = torch.device("cuda:0")
-    d = inputs.generate(B, T, H, N, "f32", 0.1, seed=seed)
-    t = {n: torch.from_numpy(d[n]).to(dev) for n in NAMES + ("dy",)}
-    t["s_init"] = torch.from_numpy(d["s_init"].astype(np.float32)).to(dev)
-    return t
-
-
-def _close(got, ref):
-    got = got.double()
-    ref = ref.double()
-    return bool(((got - ref).abs() <= TOL * (1.0 + ref.abs())).all())
-
-
-def test_noalloc_backward_matches_the_allocating_backward_twice(env):
-    inputs, wkv7 = env
     stream = torch.cuda.current_stream().cuda_stream
-    for call, seed in enumerate((21, 22)):
-        t = _case(inputs, seed)
-        B, T, H, N = t["r"].shape
-        ref = wkv7.backward(*(t[n] for n in NAMES), t["dy"], t["s_init"], None, 0)
-        out = {n: torch.full((B, T, H, N), float("nan"), device=t["r"].device) for n in GRADS}
-        out["dS_init"] = torch.full((B, H, N, N), float("nan"), device=t["r"].device)
-        rc = wkv7.wkv7_backward_noalloc(*(t[n].data_ptr() for n in NAMES), t["dy"].data_ptr(),
-                                        t["s_init"].data_ptr(), *(out[n].data_ptr() for n in GRADS),
-                                        out["dS_init"].data_ptr(), B, T, H, N, stream)
+    for call, (B, T, H, N) in enumerate(shapes):
+        d = inputs.generate(B, T, H, N, "f32", 0.1, seed=21 + call)
+        t = {n: torch.from_numpy(d[n]).to(dev) for n in NAMES + ("dy",)}
+        s0_np = d["s_init"].astype(np.float32)
+        s0 = torch.from_numpy(s0_np).to(dev)
+        out = {n: torch.full((B, T, H, N), float("nan"), device=dev) for n in GRADS}
+        out["dS_init"] = torch.full((B, H, N, N), float("nan"), device=dev)
+        rc = wkv7.wkv7_backward_noalloc(*(t[n].data_ptr() for n in NAMES), t["dy"].data_ptr(), s0.data_ptr(),
+                                        *(out[n].data_ptr() for n in GRADS), out["dS_init"].data_ptr(),
+                                        B, T, H, N, stream)
         assert rc == wkv7.OK, wkv7.last_error()
         wkv7.status()
+        o = {n: d[n].astype(np.float64) for n in NAMES + ("dy",)}
+        ref = oracle.backward(*(o[n] for n in NAMES), o["dy"], s0_np.astype(np.float64))
+        alloc = wkv7.backward(*(t[n] for n in NAMES), t["dy"], s0, None, 0)
+        wkv7.status()
         for n in GRADS + ("dS_init",):
-            assert _close(out[n], ref[n]), f"call {call}: {n} differs from wkv7_backward"
+            got = out[n].cpu().numpy()
+            _assert_close(f"call {call} {n} vs the oracle", got, ref[n])
+            _assert_close(f"call {call} {n} vs wkv7_backward", got, alloc[n].cpu().numpy().astype(np.float64))
 
 
 def test_noalloc_refuses_problems_beyond_its_scratch(env):
-    _, wkv7 = env
+    wkv7 = env[2]
     fake = [0x7F0000000000 + i * (1 << 36) for i in range(15)]  # aligned, never dereferenced
     rc = wkv7.wkv7_backward_noalloc(*fake, 1, 65536, 40, 64, None)
     assert rc == wkv7.ERR_INVALID
