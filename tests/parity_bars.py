@@ -26,16 +26,18 @@ chunk is near zero.
 TAU comes from the rounding model of the chunked kernels: operands rounded to
 bf16 (unit roundoff 2^-8) enter a chain of a few tensor-core products with
 fp32 accumulation; an fp64 model of those roundings gives an element error of
-RMS about 4.5e-3 of the element's scale (|ref| + its chunk's rms). A test
-compares at most about 2e8 elements, whose largest Gaussian deviate is about
-sqrt(2 ln 2e8) = 6.2 standard deviations: 6.2 * 4.5e-3 = 2.8e-2, and twice that
-is TAU = 0.06. dw (and dz, its chain to the logit) is formed from the identity
-w dw = anchor - sum x - a da, whose up to eight terms x = r dr - k dk - b db +
-a da are each about three times w dw itself, so its errors are about three
-times larger against its own scale: TAU_IDENTITY = 0.2. Largest values seen
-over the GPU suite and the whole 4 x 4096 x 32 workload: 0.035 and 0.107.
-Either bar still fails an element that is wrong by its own size (a sign flip
-scores 2 |ref| / (|ref| + rms), near 1).
+RMS about 4.5e-3 of the element's scale (|ref| + its chunk's rms). The error is
+not spread evenly: the worst chunk's relative error runs about twice the
+tensor's (measured: 8e-3 against 4.3e-3 on the whole 4 x 4096 x 32 workload),
+so sigma = 9e-3 there. A test compares at most about 2e8 elements, whose
+largest Gaussian deviate is about sqrt(2 ln 2e8) = 6.2 standard deviations:
+6.2 * 9e-3 = 5.6e-2, rounded up to TAU = 0.1. dw (and dz, its chain to the
+logit) is formed from the identity w dw = anchor - sum x - a da, whose up to
+eight terms x = r dr - k dk - b db + a da are each several times w dw itself,
+so its errors are larger against its own scale: TAU_IDENTITY = 0.2. Largest
+values seen over the GPU suite and every element of the whole workload:
+0.057 (da) and 0.107 (dw). Either bar still fails an element that is wrong by
+its own size (a sign flip scores 2 |ref| / (|ref| + rms), near 1).
 
 Near-zero tensors: a reference that is exactly zero (dw at T = 1 from a zero
 state) requires the GPU value to be zero as well.
@@ -51,7 +53,7 @@ import os
 import numpy as np
 
 REL_L2 = 2e-2
-TAU = 0.06
+TAU = 0.1
 TAU_IDENTITY = 0.2  # dw and dz
 FLOOR = 0.1
 CHUNK = 16
