@@ -24,6 +24,13 @@ extern "C" {
  * Process-wide; returns WKV7_OK. */
 int wkv7_debug_skip_last_load(int on);
 
+/* which = 1: the split backward's per-chunk output pass runs the kernel whose
+ * products are tcgen05.mma on tensor memory (persistent, four CTAs per SM)
+ * instead of the default one on warp-level mma.sync products (which = 0); the
+ * results agree to rounding. For side-by-side timing and parity; the product
+ * library always runs the default. Process-wide; returns WKV7_OK. */
+int wkv7_debug_out_kernel(int which);
+
 #ifdef __cplusplus
 }
 #endif

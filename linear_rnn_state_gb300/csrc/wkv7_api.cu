@@ -108,8 +108,10 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 }
 
 // [B][T][H][N] tensor as a 4-D map (N, H, T, B) with a box of `steps` rows of
-// one head.
-int make_map(CUtensorMap* map, const void* base, bool bf16, int B, int T, int H, int N, int steps) {
+// one head; `swizzle128` lays the box out in shared memory with 128-byte
+// swizzling (rows of N = 64 bf16 elements, as the tensor cores read them).
+int make_map(CUtensorMap* map, const void* base, bool bf16, int B, int T, int H, int N, int steps,
+             bool swizzle128 = false) {
   auto enc = encode_fn();
   if (!enc) return fail(WKV7_ERR_CUDA, "cuTensorMapEncodeTiled is unavailable");
   const cuuint64_t es = bf16 ? 2 : 4;
@@ -119,9 +121,25 @@ int make_map(CUtensorMap* map, const void* base, bool bf16, int B, int T, int H,
   cuuint32_t estr[4] = {1, 1, 1, 1};
   CUresult r = enc(map, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4,
                    const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                   CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+                   swizzle128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) return fail(WKV7_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", (int)r);
+  return WKV7_OK;
+}
+
+// The split backward's carry workspace [B*H*nchunks][64][64] bf16 as a 3-D map
+// (64, 64, B*H*nchunks), one carry per box, 128-byte swizzled.
+int make_carry_map(CUtensorMap* map, const void* carry, size_t nblocks) {
+  auto enc = encode_fn();
+  if (!enc) return fail(WKV7_ERR_CUDA, "cuTensorMapEncodeTiled is unavailable");
+  cuuint64_t dims[3] = {64, 64, (cuuint64_t)nblocks};
+  cuuint64_t strides[2] = {64 * 2, 64 * 64 * 2};
+  cuuint32_t box[3] = {64, 64, 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(carry), dims, strides, box, estr,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(WKV7_ERR_CUDA, "cuTensorMapEncodeTiled (carry) failed (%d)", (int)r);
   return WKV7_OK;
 }
 
@@ -163,6 +181,7 @@ int status_word(unsigned** out) {
 #ifdef WKV7_DEBUG
 // Debug build: set by wkv7_debug_skip_last_load (include/wkv7_debug.h).
 std::atomic<int> g_debug_skip_last_load{0};
+std::atomic<int> g_debug_out_kernel{0};
 #endif
 
 // ------------------------------------------------------------ forward ---
@@ -363,6 +382,17 @@ int backward_impl(bool bf16, const void* const in[7], const float* s_init, const
   args.dS_final = dS_final;
   args.w_logit = logit ? 1 : 0;
   args.carry = split ? ws + ck_ws / sizeof(float) : nullptr;
+#ifdef WKV7_DEBUG
+  args.out_kernel = g_debug_out_kernel.load();
+#endif
+  if (split) {
+    for (int v = 0; v < 7 && rc == WKV7_OK; ++v) rc = make_map(&args.swmap[v], in[v], true, B, T, H, N, kChunk, true);
+    if (rc == WKV7_OK) rc = make_carry_map(&args.gcmap, args.carry, (size_t)B * H * ((T + kChunk - 1) / kChunk));
+    if (rc) {
+      cudaFreeAsync(ws, stream);
+      return rc;
+    }
+  }
   for (int v = 0; v < 7; ++v) args.in[v] = in[v];
   args.C = C_eff;
   args.nck = (T + C_eff - 1) / C_eff;
@@ -707,6 +737,11 @@ const char* wkv7_last_error(void) { return t_last_error.c_str(); }
 #ifdef WKV7_DEBUG
 int wkv7_debug_skip_last_load(int on) {
   g_debug_skip_last_load.store(on ? 1 : 0);
+  return WKV7_OK;
+}
+
+int wkv7_debug_out_kernel(int which) {
+  g_debug_out_kernel.store(which == 1 ? 1 : 0);
   return WKV7_OK;
 }
 #endif

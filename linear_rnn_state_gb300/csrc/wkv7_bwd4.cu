@@ -49,6 +49,7 @@
 #include "wkv7_launch.h"
 #include "wkv7_mma.cuh"
 #include "wkv7_scaled.cuh"
+#include "wkv7_tmem.cuh"
 
 namespace wkv7 {
 namespace {
@@ -662,12 +663,12 @@ struct OutSmem {
 // rows 8 w .. 8 w + 7 of the state and the carry, lane (g, t) row 8 w + g and
 // columns 8 nt + 2 t, + 1): the carry starts at the stored Gc, S_prev of step
 // t is recomputed from the checkpoint (fp32, read from global memory).
+// `rs` holds the chunk's r, w, k, v, a, b, dy rows ([t][j], row stride kB64,
+// kL * kB64 elements apart); `red` is 8 * 5 * kN floats of scratch.
 template <bool kLogit>
-__device__ void out_direct(OutSmem& sm, const float* S0, const bf16_t* Gcg, int len, const BwdArgs& args, size_t base,
-                           size_t vstep, int warp, int lane) {
-  const int g = lane >> 2, t4 = lane & 3, i = 8 * warp + g, tid = threadIdx.x;
-  const bf16_t* rs = sm.raw[0];
-  float* red = sm.u.red;  // [8 warps][5][64]
+__device__ void out_direct(const bf16_t* rs, float* red, const float* S0, const bf16_t* Gcg, int len,
+                           const BwdArgs& args, size_t base, size_t vstep, int warp, int lane) {
+  const int g = lane >> 2, t4 = lane & 3, i = 8 * warp + g, tid = threadIdx.x;  // red: [8 warps][5][64]
   constexpr int RS = kL * kB64;
   float G[8][2];
 #pragma unroll
@@ -841,7 +842,7 @@ __global__ void __launch_bounds__(kThreads, 3) wkv7_bwd4_out_kernel(const __grid
                       decay_is_safe(wv[1].y);
     *reinterpret_cast<float2*>(&sm.Ppart[warp][j]) = fmul2(wv[0], wv[1]);
     if (__syncthreads_or(!safe)) {
-      out_direct<kLogit>(sm, S0g, Gcg, len, args, base, vstep, warp, lane);
+      out_direct<kLogit>(sm.raw[0], sm.u.red, S0g, Gcg, len, args, base, vstep, warp, lane);
       return;
     }
     float2 cL = make_float2(1.f, 1.f), cpre = cL;  // cpre = c(ta - 1)
@@ -1191,6 +1192,641 @@ __global__ void __launch_bounds__(kThreads, 3) wkv7_bwd4_out_kernel(const __grid
   }
 }
 
+
+// ========================================== output kernel on tcgen05 ===
+//
+// The same per-chunk output pass as wkv7_bwd4_out_kernel, with every product
+// on the 5th-generation tensor cores: tcgen05.mma kind::f16 (bf16 operands,
+// fp32 accumulators in tensor memory), issued by one thread, operands read
+// by the tensor core from shared memory through matrix descriptors. The
+// chunk's rows and its carry arrive by TMA (cp.async.bulk.tensor) straight
+// into the 128-byte-swizzled layout the descriptors describe. Five rounds of
+// products, each followed by the threads reading the accumulators back (rows
+// i of the state or columns j, as tensor-memory lanes):
+//   1. Gram blocks [A^; R^] [K~; B~]^T                                (M = 64)
+//   2. [S0; Gc] [Bb; Kb; A^]^T + [V^T; DY^T] (Mka, [Mbr | Mkr]):
+//      S0 A^T + V^T Mka^T, Gc Bb^T + DY^T Mbr, Gc Kb^T + DY^T Mkr      (M = 128)
+//   3. the same rounds' SA and DSA parts times T^T and T: SA^T, DSA^T   (M = 128)
+//   4. DV^T += DSA^T Mka; the triangular factors [V; SA; DY; DSA] [DY; DSA]^T
+//      (M = 64); the column products [S0^T; Gc^T] [V; SA; DY; DSA]^T    (M = 128)
+//   5. the triangular terms [K~^T; R^T] U + [B~^T; A^T] U'              (M = 128)
+// T = (I - Mba)^-1 is formed by one warp from the Gram rows it holds while
+// round 2 runs. Each tile is stored once and read K-major or MN-major
+// (transposed) as a product needs it. 128 tensor-memory columns per CTA,
+// three CTAs per SM.
+
+namespace tcout {
+
+constexpr int kThreads = 256;
+constexpr int kCtasPerSm = 4;
+constexpr uint32_t kTmemCols = 128;
+
+// Shared memory (byte offsets from a 1024-byte-aligned base). 128B-swizzled
+// tiles of rows of 64 bf16 (128 bytes), 16 rows (2 KB) or 64 rows (8 KB).
+// Tiles whose lifetimes do not overlap share space (noted at each).
+enum : uint32_t {
+  OFF_S0 = 0x0000,   // checkpoint [i][j] (rounded to bf16); after round 4: U tiles, dw exchange
+  OFF_GC = 0x2000,   // carry after the chunk [i][j] (TMA); follows S0
+  OFF_UA = 0x0000,   // (after round 4) [U0 | U1] rows p (columns 0-15, 16-31)
+  OFF_UB = 0x0800,   // (after round 4) [U2 | U3]
+  OFF_XK = 0x1000,   // (after round 5) the dw exchange XK, XR, XA [16][64] fp32 (12 KB)
+  OFF_KT = 0x4000,   // K~ = k / c [t][j]
+  OFF_BT = 0x4800,   // B~ = b / c
+  OFF_BB = 0x5000,   // Bb = b c(L) / c
+  OFF_KB = 0x5800,   // Kb = k c(L) / c
+  OFF_PA = 0x5000,   // (after round 2) [SA_pre; DSA_pre], then [.; DSA^T]: 128 x 16 bf16, unswizzled core-matrix layout
+  OFF_AH = 0x6000,   // A^ = a c(t - 1)
+  OFF_RH = 0x6800,   // R^ = r c
+  OFF_V = 0x7000,    // v [t][i] (TMA)
+  OFF_SA = 0x7800,   // sa [t][i]
+  OFF_DY = 0x8000,   // dy [t][i] (TMA)
+  OFF_DSA = 0x8800,  // dsa [t][i]; before phase 3: the Mba rows [16][16] fp32 for T
+  OFF_MA = 0x9000,   // Mka [t][s]; before phase 1: the decay pair products [8][64] fp32
+  OFF_MB = 0x9800,   // [Mbr | Mkr] rows s
+  OFF_X = 0x9800,    // (after round 2) T^T: row s = column s of T
+  OFF_RAW = 0xA000,  // r, w, k, a, b [t][j] (TMA, plain row-major), 2 KB apart
+  OFF_EPART = 0xC800,  // colsum(Gc o S0), one partial per warp [8][64] fp32
+  OFF_ANC = 0xD000,    // the chunk's parts of the dw anchors [start, end][half][64] fp32
+  OFF_CL = 0xD400,     // c(L) [64] fp32
+  OFF_C7 = 0xD500,     // c(7) [64] fp32, the running decay product after the first 8 steps
+  OFF_BAR = 0xD600,    // two mbarriers and the tensor-memory address
+  SMEM_USED = 0xD640,
+};
+// A chunk run step by step: its rows with padded stride (16,128 B) and the
+// reduction scratch (10,240 B) from OFF_S0, below every tile the copy reads.
+constexpr uint32_t kSmemBytes = SMEM_USED + 1024;  // + alignment slack
+constexpr uint32_t OFF_RED = 0x3F00;
+enum { RAW_R = 0, RAW_W = 1, RAW_K = 2, RAW_A = 3, RAW_B = 4 };
+
+// Byte offset of element (row, col) in a 128B-swizzled tile of 64-element
+// rows (the tile 1024-byte aligned): 16-byte chunks permuted by row mod 8.
+__device__ __forceinline__ uint32_t swz(int row, int col) {
+  return (uint32_t)(row * 128 + ((((col >> 3) ^ row) & 7) << 4) + ((col & 7) << 1));
+}
+// Byte offset of element (t, j) in a plain row-major tile of 64-element rows
+// (the chunk's r, w, k, a, b, which only the threads read).
+__device__ __forceinline__ uint32_t rowo(int t, int j) { return (uint32_t)(t * 128 + j * 2); }
+// Byte offset of element (r, c) in a 16-column tile in the unswizzled
+// core-matrix layout (8 x 8 blocks of 128 contiguous bytes).
+__device__ __forceinline__ uint32_t core16(int r, int c) {
+  return (uint32_t)(((r >> 3) * 2 + (c >> 3)) * 128 + (r & 7) * 16 + (c & 7) * 2);
+}
+
+// Shared-memory matrix descriptor (sm_100 form): start, leading and stride
+// byte offsets (>> 4), descriptor version 1, layout type (2 = 128B swizzle,
+// 0 = none).
+__device__ __forceinline__ uint64_t sdesc(uint32_t addr, uint32_t lbo, uint32_t sbo, uint32_t layout) {
+  return (uint64_t)((addr >> 4) & 0x3FFFu) | ((uint64_t)((lbo >> 4) & 0x3FFFu) << 16) |
+         ((uint64_t)((sbo >> 4) & 0x3FFFu) << 32) | ((uint64_t)1 << 46) | ((uint64_t)layout << 61);
+}
+// K-major 128B-swizzled operand (rows of 64 elements, 8-row groups 1024 bytes
+// apart), K step ks of 16 elements.
+__device__ __forceinline__ uint64_t desc_k(uint32_t addr, int ks) { return sdesc(addr + 32u * ks, 16, 1024, 2); }
+// MN-major 128B-swizzled operand: stored [k][mn] with 64 mn per row; atoms of
+// 64 (M or N) x 8 (K), the next 64 along M or N `lbo` bytes on; K step ks.
+__device__ __forceinline__ uint64_t desc_mn(uint32_t addr, uint32_t lbo, int ks) {
+  return sdesc(addr + 2048u * ks, lbo, 1024, 2);
+}
+// K-major unswizzled 16-column operand (core16 layout), K = 16.
+__device__ __forceinline__ uint64_t desc_k16(uint32_t addr) { return sdesc(addr, 128, 256, 0); }
+// Instruction descriptor, kind::f16: fp32 accumulator, bf16 A and B, A/B
+// MN-major flags, N and M.
+__host__ __device__ constexpr uint32_t idesc(int M, int N, int a_mn, int b_mn) {
+  return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)a_mn << 15) | ((uint32_t)b_mn << 16) |
+         ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+}
+// D[tmem] (+)= A[smem] B[smem]^T
+__device__ __forceinline__ void mma(uint32_t d, uint64_t a, uint64_t b, uint32_t id, bool acc) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}" ::"r"(d),
+      "l"(a), "l"(b), "r"(id), "r"((uint32_t)acc)
+      : "memory");
+}
+__device__ __forceinline__ void commit(uint64_t* bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_addr(bar))
+               : "memory");
+}
+__device__ __forceinline__ void ld8(uint32_t taddr, float (&v)[8]) { tmem_ld<8>(taddr, v); }
+__device__ __forceinline__ void ld16(uint32_t taddr, float (&v)[16]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, "
+      "[%16];"
+      : "=f"(v[0]), "=f"(v[1]), "=f"(v[2]), "=f"(v[3]), "=f"(v[4]), "=f"(v[5]), "=f"(v[6]), "=f"(v[7]), "=f"(v[8]),
+        "=f"(v[9]), "=f"(v[10]), "=f"(v[11]), "=f"(v[12]), "=f"(v[13]), "=f"(v[14]), "=f"(v[15])
+      : "r"(taddr)
+      : "memory");
+}
+__device__ __forceinline__ float bfs(const unsigned char* sb, uint32_t off) {
+  return __bfloat162float(*reinterpret_cast<const bf16_t*>(sb + off));
+}
+__device__ __forceinline__ float2 bfs2(const unsigned char* sb, uint32_t off) {
+  return __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(sb + off));
+}
+__device__ __forceinline__ void sts_bf(unsigned char* sb, uint32_t off, float x) {
+  *reinterpret_cast<bf16_t*>(sb + off) = __float2bfloat16_rn(x);
+}
+// Every thread waits for the phase; all leave together, false if any gave up
+// (after draining: a second bounded wait).
+__device__ __forceinline__ bool cta_wait(unsigned* status, uint64_t* bar, uint32_t parity) {
+  bool ok = mbar_wait_bounded(status, bar, parity);
+  if (!ok) mbar_wait_bounded(status, bar, parity);
+  return __syncthreads_and(ok) != 0;
+}
+// Smem writes by the threads become visible to the tensor core's reads, and
+// tensor-memory reads finish before the next product is issued.
+__device__ __forceinline__ void to_mma_sync() {
+  fence_proxy_async_smem();
+  tmem_fence_before_sync();
+  __syncthreads();
+  tmem_fence_after_sync();
+}
+
+// The v, dy and carry tiles of `task` (one of the two arrivals of the load barrier's phase).
+__device__ __forceinline__ void issue_loads_vdg(unsigned char* sb, const BwdArgs& args, int task, int nchunks,
+                                                uint64_t* bar) {
+  const int head = task / nchunks, n = task % nchunks, bi = head / args.H, hi = head % args.H;
+  mbar_arrive_expect_tx(bar, 2 * 2048 + 8192);
+  tma_load_4d(sb + OFF_V, &args.swmap[3], bar, 0, hi, n * kL, bi);
+  tma_load_4d(sb + OFF_DY, &args.swmap[6], bar, 0, hi, n * kL, bi);
+  tma_load_3d(sb + OFF_GC, &args.gcmap, bar, 0, 0, task);
+}
+// The r, w, k, a, b rows of `task`, row-major (the other arrival).
+__device__ __forceinline__ void issue_loads_raw(unsigned char* sb, const BwdArgs& args, int task, int nchunks,
+                                                uint64_t* bar) {
+  const int head = task / nchunks, n = task % nchunks, bi = head / args.H, hi = head % args.H;
+  mbar_arrive_expect_tx(bar, 5 * 2048);
+  const int vec[5] = {0, 1, 2, 4, 5};  // r w k a b
+#pragma unroll
+  for (int q = 0; q < 5; ++q) tma_load_4d(sb + OFF_RAW + 0x800 * q, &args.map[vec[q]], bar, 0, hi, n * kL, bi);
+}
+// The checkpoint S0 (fp32 [i][j]) rounded to bf16 into its swizzled tile, four float4 per thread.
+__device__ __forceinline__ void stage_checkpoint(unsigned char* sb, const float* S0g, int tid) {
+  float4 x[4];
+#pragma unroll
+  for (int q = 0; q < 4; ++q) x[q] = *reinterpret_cast<const float4*>(S0g + 4 * (tid + kThreads * q));
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    const int idx = tid + kThreads * q, i = idx >> 4, c4 = idx & 15;
+    *reinterpret_cast<uint2*>(sb + OFF_S0 + swz(i, 4 * c4)) = make_uint2(pack_bf16(x[q].x, x[q].y), pack_bf16(x[q].z, x[q].w));
+  }
+}
+
+// One chunk (task = (b, h) head * nchunks + chunk). The load barrier completes once per
+// task (ld_it counts them), the product barrier five times per task run on the tensor
+// cores (mma_it counts those) and never for a chunk run step by step. Returns 1 for a
+// tensor-core task, 0 for a step-by-step one, -1 if a wait gave up (the CTA then leaves).
+template <bool kLogit>
+__device__ __forceinline__ int body(unsigned char* sb, uint32_t tb, const BwdArgs& args, int task, int ld_it,
+                                    int mma_it) {
+  const int T = args.T, H = args.H, nchunks = (T + kL - 1) / kL;
+  const int head = task / nchunks, n = task % nchunks, bi = head / H, hi = head % H;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int t0 = n * kL, len = min(kL, T - t0);
+  const size_t vstep = (size_t)H * kN, base = ((size_t)bi * T + t0) * vstep + (size_t)hi * kN;
+  const float* S0g = args.ckpt + ((size_t)head * args.nck + n) * kN * kN;
+  const bf16_t* Gcg = reinterpret_cast<const bf16_t*>(args.carry) + ((size_t)head * nchunks + n) * kN * kN;
+  const uint32_t sa_ = smem_addr(sb);
+  uint64_t* bar_load = reinterpret_cast<uint64_t*>(sb + OFF_BAR);
+  uint64_t* bar_mma = bar_load + 1;
+  float* c7s = reinterpret_cast<float*>(sb + OFF_C7);
+  float* cLs = reinterpret_cast<float*>(sb + OFF_CL);
+  float* Epart = reinterpret_cast<float*>(sb + OFF_EPART);
+  float* anc = reinterpret_cast<float*>(sb + OFF_ANC);
+  const unsigned char* raw = sb + OFF_RAW;
+  // this warp's quarter of tensor-memory lanes
+  const uint32_t tq = tb + ((uint32_t)(32 * (warp & 3)) << 16);
+
+  // ---- loads: the chunk's rows and its carry by TMA (rows past T read as zeros), the
+  //      checkpoint rounded to bf16
+  if (tid == 0) {
+    issue_loads_vdg(sb, args, task, nchunks, bar_load);
+    issue_loads_raw(sb, args, task, nchunks, bar_load);
+  }
+  stage_checkpoint(sb, S0g, tid);
+  // five product rounds per task: round r (from 0) waits on parity par ^ (r & 1)
+  const uint32_t par = (uint32_t)mma_it & 1u;
+  if (!cta_wait(args.status, bar_load, (uint32_t)ld_it & 1u)) return -1;
+  {  // colsum(Gc o S0) of the bf16 tiles: thread rows tid / 16 + 16 q, columns 4 (tid % 16) ..;
+     // then lanes l, l ^ 16 (the same columns); one partial per warp and column
+    float4 e = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const int idx = tid + kThreads * q, i = idx >> 4, c4 = idx & 15;
+      const uint2 gv = *reinterpret_cast<const uint2*>(sb + OFF_GC + swz(i, 4 * c4));
+      const uint2 sv = *reinterpret_cast<const uint2*>(sb + OFF_S0 + swz(i, 4 * c4));
+      const float2 g0 = unpack_bf16(gv.x), g1 = unpack_bf16(gv.y), s0 = unpack_bf16(sv.x), s1 = unpack_bf16(sv.y);
+      e.x = fmaf(g0.x, s0.x, e.x);
+      e.y = fmaf(g0.y, s0.y, e.y);
+      e.z = fmaf(g1.x, s1.x, e.z);
+      e.w = fmaf(g1.y, s1.y, e.w);
+    }
+    e.x += __shfl_xor_sync(0xffffffffu, e.x, 16);
+    e.y += __shfl_xor_sync(0xffffffffu, e.y, 16);
+    e.z += __shfl_xor_sync(0xffffffffu, e.z, 16);
+    e.w += __shfl_xor_sync(0xffffffffu, e.w, 16);
+    if (lane < 16) *reinterpret_cast<float4*>(Epart + warp * kN + 4 * lane) = e;
+  }
+
+  // ---- A: scaled operands; thread (lane, warp) forms columns 2 lane, 2 lane + 1 of steps
+  //      2 warp, 2 warp + 1 (the pairs' decay products chained in step order)
+  {
+    const int j = 2 * lane, ta = 2 * warp;
+    float* Ppart = reinterpret_cast<float*>(sb + OFF_MA);  // [8][64]
+    float2 wv[2];
+#pragma unroll
+    for (int e = 0; e < 2; ++e)
+      wv[e] = ta + e < len ? decay_value2<kLogit>(bfs2(raw + RAW_W * 0x800, rowo(ta + e, j))) : make_float2(1.f, 1.f);
+    const bool safe = decay_is_safe(wv[0].x) && decay_is_safe(wv[0].y) && decay_is_safe(wv[1].x) &&
+                      decay_is_safe(wv[1].y);
+    *reinterpret_cast<float2*>(&Ppart[warp * kN + j]) = fmul2(wv[0], wv[1]);
+    if (__syncthreads_or(!safe)) {
+      // A chunk whose decays leave the scaled form's range: step by step, from the rows
+      // copied with the padded stride of out_direct into the (dead) checkpoint and carry
+      // tiles, which no source tile overlaps.
+      const uint32_t src[7] = {OFF_RAW + 0x000, OFF_RAW + 0x800, OFF_RAW + 0x1000, OFF_V, OFF_RAW + 0x1800,
+                               OFF_RAW + 0x2000, OFF_DY};
+      bf16_t* pad = reinterpret_cast<bf16_t*>(sb + OFF_S0);
+#pragma unroll 1
+      for (int v = 0; v < 7; ++v)
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          const int e = 4 * (tid + kThreads * h), t = e >> 6, c = e & 63;
+          *reinterpret_cast<uint2*>(pad + v * kL * kB64 + t * kB64 + c) =
+              *reinterpret_cast<const uint2*>(sb + src[v] + ((v == 3 || v == 6) ? swz(t, c) : rowo(t, c)));
+        }
+      __syncthreads();
+      out_direct<kLogit>(pad, reinterpret_cast<float*>(sb + OFF_RED), S0g, Gcg, len, args, base, vstep, warp, lane);
+      return 0;
+    }
+    float2 cL = make_float2(1.f, 1.f), cpre = cL;  // cpre = c(ta - 1)
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
+      cL = fmul2(cL, *reinterpret_cast<const float2*>(&Ppart[q * kN + j]));
+      if (q < warp) cpre = cL;
+    }
+    if (warp == 0) *reinterpret_cast<float2*>(&cLs[j]) = cL;
+    if (warp == 4) *reinterpret_cast<float2*>(&c7s[j]) = cpre;  // c(7)
+    float2 c = cpre;
+#pragma unroll
+    for (int e = 0; e < 2; ++e) {
+      const int t = ta + e;
+      const uint32_t o = swz(t, j), ro = rowo(t, j);
+      const float2 w = wv[e];
+      const float2 a = bfs2(raw + RAW_A * 0x800, ro), r = bfs2(raw + RAW_R * 0x800, ro);
+      const float2 k = bfs2(raw + RAW_K * 0x800, ro), b = bfs2(raw + RAW_B * 0x800, ro);
+      const float2 cprev = c;
+      c = fmul2(c, w);
+      const float2 ic = make_float2(rcp_approx(c.x), rcp_approx(c.y)), sc = fmul2(cL, ic);
+      *reinterpret_cast<uint32_t*>(sb + OFF_AH + o) = pack_bf16(a.x * cprev.x, a.y * cprev.y);
+      *reinterpret_cast<uint32_t*>(sb + OFF_RH + o) = pack_bf16(r.x * c.x, r.y * c.y);
+      *reinterpret_cast<uint32_t*>(sb + OFF_KT + o) = pack_bf16(k.x * ic.x, k.y * ic.y);
+      *reinterpret_cast<uint32_t*>(sb + OFF_BT + o) = pack_bf16(b.x * ic.x, b.y * ic.y);
+      *reinterpret_cast<uint32_t*>(sb + OFF_KB + o) = pack_bf16(k.x * sc.x, k.y * sc.y);
+      *reinterpret_cast<uint32_t*>(sb + OFF_BB + o) = pack_bf16(b.x * sc.x, b.y * sc.y);
+    }
+  }
+  to_mma_sync();
+
+  // ---- round 1: the Gram blocks (columns 0-31, M = 64: lanes 0-15 A^, 32-47 R^; columns
+  //      0-15 = . K~^T, 16-31 = . B~^T): Mka, Mba (lanes 0-15), Mkr, Mbr (lanes 32-47)
+  if (tid == 0) {
+#pragma unroll
+    for (int ks = 0; ks < 4; ++ks)
+      mma(tb, desc_k(sa_ + OFF_AH, ks), desc_k(sa_ + OFF_KT, ks), idesc(64, 32, 0, 0), ks > 0);
+    commit(bar_mma);
+  }
+  if (!cta_wait(args.status, bar_mma, par)) return -1;
+  tmem_fence_after_sync();
+
+  // ---- phase 1: Mka rows (masked s < t) to the tile Mka [t][s]; [Mbr | Mkr] rows (s <= t) to
+  //      [Mbr | Mkr] [s][.]; warp 0 keeps the Mba rows for T
+  if (warp < 2) {
+    float g[32];
+    ld16(tq, *reinterpret_cast<float(*)[16]>(&g[0]));
+    ld16(tq + 16, *reinterpret_cast<float(*)[16]>(&g[16]));
+    tmem_wait_ld();
+    if (lane < 16) {
+      const int t = lane;
+      uint32_t pk[16];
+      if (warp == 0) {
+        float* mba = reinterpret_cast<float*>(sb + OFF_DSA);  // Mba rows, fp32, for T
+#pragma unroll
+        for (int q = 0; q < 4; ++q)
+          *reinterpret_cast<float4*>(mba + t * 16 + 4 * q) =
+              make_float4(4 * q < t ? g[16 + 4 * q] : 0.f, 4 * q + 1 < t ? g[17 + 4 * q] : 0.f,
+                          4 * q + 2 < t ? g[18 + 4 * q] : 0.f, 4 * q + 3 < t ? g[19 + 4 * q] : 0.f);
+#pragma unroll
+        for (int s = 0; s < 16; s += 2) pk[s / 2] = pack_bf16(s < t ? g[s] : 0.f, s + 1 < t ? g[s + 1] : 0.f);
+#pragma unroll
+        for (int c = 0; c < 2; ++c)
+          *reinterpret_cast<uint4*>(sb + OFF_MA + swz(t, 8 * c)) =
+              make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
+      } else {
+#pragma unroll
+        for (int s = 0; s < 16; s += 2) {
+          pk[s / 2] = pack_bf16(s <= t ? g[16 + s] : 0.f, s + 1 <= t ? g[16 + s + 1] : 0.f);  // Mbr
+          pk[8 + s / 2] = pack_bf16(s <= t ? g[s] : 0.f, s + 1 <= t ? g[s + 1] : 0.f);       // Mkr
+        }
+#pragma unroll
+        for (int c = 0; c < 4; ++c)
+          *reinterpret_cast<uint4*>(sb + OFF_MB + swz(t, 8 * c)) =
+              make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
+      }
+    }
+  }
+  to_mma_sync();
+
+  // ---- round 2 (columns 32-79, M = 128; B = [Bb; Kb; A^]): rows 0-63 (S0) columns 64-79 =
+  //      SA_pre^T = S0 A^T + V^T Mka^T; rows 64-127 (Gc) columns 32-47 = DSA_pre^T = Gc Bb^T +
+  //      DY^T Mbr, columns 48-63 = DV_pre^T = Gc Kb^T + DY^T Mkr
+  if (tid == 0) {
+#pragma unroll
+    for (int ks = 0; ks < 4; ++ks)
+      mma(tb + 32, desc_k(sa_ + OFF_S0, ks), desc_k(sa_ + OFF_BB, ks), idesc(128, 48, 0, 0), ks > 0);
+    mma(tb + 64, desc_mn(sa_ + OFF_V, OFF_DY - OFF_V, 0), desc_k(sa_ + OFF_MA, 0), idesc(128, 16, 1, 0), true);
+    mma(tb + 32, desc_mn(sa_ + OFF_V, OFF_DY - OFF_V, 0), desc_mn(sa_ + OFF_MB, 8192, 0), idesc(128, 32, 1, 1), true);
+    commit(bar_mma);
+  }
+  float col[kL];  // warp 0: column (lane & 15) of T
+  if (warp == 0) {  // meanwhile: T = (I - Mba)^-1, lane s owning column s (rows of Mba broadcast)
+    const int s = lane & 15;
+    const float* mba = reinterpret_cast<const float*>(sb + OFF_DSA);
+#pragma unroll
+    for (int t = 0; t < kL; ++t) {
+      float m[16];
+#pragma unroll
+      for (int q = 0; q < (t + 3) / 4; ++q) {
+        const float4 r4 = *reinterpret_cast<const float4*>(mba + t * 16 + 4 * q);
+        m[4 * q] = r4.x;
+        m[4 * q + 1] = r4.y;
+        m[4 * q + 2] = r4.z;
+        m[4 * q + 3] = r4.w;
+      }
+      float x = t == s ? 1.f : 0.f;
+#pragma unroll
+      for (int u = 0; u < t; ++u) x = fmaf(m[u], col[u], x);
+      col[t] = x;
+    }
+  }
+  if (!cta_wait(args.status, bar_mma, par ^ 1u)) return -1;
+  tmem_fence_after_sync();
+
+  // ---- phase 2: T^T rows over [Mbr | Mkr] (read by round 2); SA_pre (rows 0-63) and
+  //      DSA_pre (rows 64-127) to the A tile [i][t] over Bb, Kb (read by round 2)
+  if (warp == 0 && lane < 16) {  // row s of T^T
+    const int s = lane;
+    uint32_t pk[8];
+#pragma unroll
+    for (int t = 0; t < kL; t += 2) pk[t / 2] = pack_bf16(col[t], col[t + 1]);
+#pragma unroll
+    for (int c = 0; c < 2; ++c)
+      *reinterpret_cast<uint4*>(sb + OFF_X + swz(s, 8 * c)) = make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
+  }
+  if (warp < 4) {
+    float v[16];
+    ld16(tq + (warp < 2 ? 64 : 32), v);
+    tmem_wait_ld();
+    const int r = 32 * warp + lane;
+    uint32_t pk[8];
+#pragma unroll
+    for (int t = 0; t < kL; t += 2) pk[t / 2] = pack_bf16(v[t], v[t + 1]);
+    *reinterpret_cast<uint4*>(sb + OFF_PA + core16(r, 0)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+    *reinterpret_cast<uint4*>(sb + OFF_PA + core16(r, 8)) = make_uint4(pk[4], pk[5], pk[6], pk[7]);
+  }
+  to_mma_sync();
+
+  // ---- round 3 (columns 0-31, M = 128): columns 0-15 rows 0-63 = SA^T = SA_pre^T T^T
+  //      (T^T read MN-major); columns 16-31 rows 64-127 = DSA^T = DSA_pre^T T (K-major)
+  if (tid == 0) {
+    mma(tb, desc_k16(sa_ + OFF_PA), desc_mn(sa_ + OFF_X, 8192, 0), idesc(128, 16, 0, 1), false);
+    mma(tb + 16, desc_k16(sa_ + OFF_PA), desc_k(sa_ + OFF_X, 0), idesc(128, 16, 0, 0), false);
+    commit(bar_mma);
+  }
+  if (!cta_wait(args.status, bar_mma, par)) return -1;
+  tmem_fence_after_sync();
+
+  // ---- phase 3: sa, dsa to bf16 tiles [t][i]; dsa^T also to rows 64-127 of the A tile.
+  //      Warps 0, 1 / 4, 5: sa steps 0-7 / 8-15; warps 2, 3 / 6, 7: dsa steps 0-7 / 8-15.
+  {
+    const int i = lane + 32 * (warp & 1), tbeg = warp >= 4 ? 8 : 0;
+    float v[8];
+    ld8(tq + ((warp & 2) ? 16 : 0) + tbeg, v);
+    tmem_wait_ld();
+    const uint32_t dst = (warp & 2) ? OFF_DSA : OFF_SA;
+#pragma unroll
+    for (int e = 0; e < 8; ++e) sts_bf(sb + dst, swz(tbeg + e, i), v[e]);
+    if (warp & 2) {
+      *reinterpret_cast<uint4*>(sb + OFF_PA + core16(64 + i, tbeg)) =
+          make_uint4(pack_bf16(v[0], v[1]), pack_bf16(v[2], v[3]), pack_bf16(v[4], v[5]), pack_bf16(v[6], v[7]));
+    }
+  }
+  to_mma_sync();
+
+  // ---- round 4: DV^T += DSA^T Mka (columns 48-63, rows 64-127; Mka read MN-major); the
+  //      triangular factors (columns 0-31, M = 64: lanes 0-15 V, 32-47 SA; columns 0-15 =
+  //      . DY^T, 16-31 = . DSA^T); the column products (columns 64-127, M = 128: rows 0-63
+  //      S0^T, 64-127 Gc^T; columns 64-79 . V^T, 80-95 . SA^T, 96-111 . DY^T, 112-127 . DSA^T)
+  if (tid == 0) {
+    mma(tb + 48, desc_k16(sa_ + OFF_PA), desc_mn(sa_ + OFF_MA, 8192, 0), idesc(128, 16, 0, 1), true);
+#pragma unroll
+    for (int ks = 0; ks < 4; ++ks)
+      mma(tb, desc_k(sa_ + OFF_V, ks), desc_k(sa_ + OFF_DY, ks), idesc(64, 32, 0, 0), ks > 0);
+#pragma unroll
+    for (int ks = 0; ks < 4; ++ks)
+      mma(tb + 64, desc_mn(sa_ + OFF_S0, OFF_GC - OFF_S0, ks), desc_k(sa_ + OFF_V, ks), idesc(128, 64, 1, 0), ks > 0);
+    commit(bar_mma);
+  }
+  if (!cta_wait(args.status, bar_mma, par ^ 1u)) return -1;
+  tmem_fence_after_sync();
+
+  // ---- phase 4: U0 = triu(V DY^T), U1 = triu(V DSA^T, 1) into [U0 | U1] rows p; U2 =
+  //      triu(SA DY^T), U3 = triu(SA DSA^T, 1) into [U2 | U3]; dv out
+  if (warp < 2) {
+    float v[32];
+    ld16(tq, *reinterpret_cast<float(*)[16]>(&v[0]));
+    ld16(tq + 16, *reinterpret_cast<float(*)[16]>(&v[16]));
+    tmem_wait_ld();
+    if (lane < 16) {
+      const int p = lane;
+      uint32_t pk[16];
+#pragma unroll
+      for (int q = 0; q < 16; q += 2) {
+        pk[q / 2] = pack_bf16(q >= p ? v[q] : 0.f, q + 1 >= p ? v[q + 1] : 0.f);
+        pk[8 + q / 2] = pack_bf16(q > p ? v[16 + q] : 0.f, q + 1 > p ? v[16 + q + 1] : 0.f);
+      }
+      unsigned char* dst = sb + (warp == 0 ? OFF_UA : OFF_UB);
+#pragma unroll
+      for (int c = 0; c < 4; ++c)
+        *reinterpret_cast<uint4*>(dst + swz(p, 8 * c)) = make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
+    }
+  } else if (warp >= 6) {  // dv (rows 64-127 = i, columns 48-63)
+    const int i = lane + 32 * (warp & 1);
+    float v[16];
+    ld16(tq + 48, v);
+    tmem_wait_ld();
+#pragma unroll
+    for (int t = 0; t < kL; ++t)
+      if (t < len) args.dv[base + (size_t)t * vstep + i] = v[t];
+  }
+  to_mma_sync();
+
+  // ---- round 5: the triangular terms. Columns 0-31 (rows 64-127): (U0 R^ + U1 A^)^T and
+  //      (U2 R^ + U3 A^)^T; columns 32-63 (rows 0-63): (U0^T K~ + U2^T B~)^T and
+  //      (U1^T K~ + U3^T B~)^T
+  if (tid == 0) {
+    mma(tb, desc_mn(sa_ + OFF_KT, OFF_RH - OFF_KT, 0), desc_k(sa_ + OFF_UA, 0), idesc(128, 32, 1, 0), false);
+    mma(tb, desc_mn(sa_ + OFF_BT, OFF_AH - OFF_BT, 0), desc_k(sa_ + OFF_UA, 1), idesc(128, 32, 1, 0), true);
+    mma(tb + 32, desc_mn(sa_ + OFF_KT, OFF_RH - OFF_KT, 0), desc_mn(sa_ + OFF_UA, 8192, 0), idesc(128, 32, 1, 1), false);
+    mma(tb + 32, desc_mn(sa_ + OFF_BT, OFF_AH - OFF_BT, 0), desc_mn(sa_ + OFF_UB, 8192, 0), idesc(128, 32, 1, 1), true);
+    commit(bar_mma);
+  }
+  if (!cta_wait(args.status, bar_mma, par)) return -1;
+  tmem_fence_after_sync();
+
+  // ---- E: the gradients, thread = column j, warp w and w + 4 take steps 0-7 and 8-15;
+  //      warps 2, 3, 6, 7 dk, db (rows 64-127), warps 0, 1, 4, 5 dr, da (rows 0-63); and the
+  //      chunk's parts of the dw anchors over those steps (anc [grp][half][64]):
+  //      end   c(L) sum_t (k V Gc + b SA Gc) / c        start  sum_t (r c DY S0 + a c(t-1) DSA S0)
+  float* XK = reinterpret_cast<float*>(sb + OFF_XK);  // [t][j]: -k dk - b db
+  float* XR = XK + kL * kN;                          // r dr + a da
+  float* XA = XR + kL * kN;                          // a da
+  {
+    const int j = lane + 32 * (warp & 1), h = warp >> 2, tbeg = 8 * h;
+    float p0[8], p1[8], y0[8], y1[8];
+    // c(t) of this column for the steps tbeg - 1 .. tbeg + 7, as the forming warps formed it
+    float cc[9];
+    cc[0] = h ? c7s[j] : 1.f;
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+      const int t = tbeg + e;
+      const float w = t < len ? decay_value<kLogit>(__bfloat162float(
+                                    *reinterpret_cast<const bf16_t*>(raw + RAW_W * 0x800 + rowo(t, j))))
+                              : 1.f;
+      cc[e + 1] = cc[e] * w;
+    }
+    if (warp & 2) {  // dk, db
+      ld8(tq + 64 + tbeg, p0);  // (V Gc)^T
+      ld8(tq + 80 + tbeg, p1);  // (SA Gc)^T
+      ld8(tq + tbeg, y0);
+      ld8(tq + 16 + tbeg, y1);
+      tmem_wait_ld();
+      const float cl = cLs[j];
+      float an = 0.f;
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        const int t = tbeg + e;
+        const float ic = rcp_approx(cc[e + 1]);
+        const float kv = bfs(raw + RAW_K * 0x800, rowo(t, j)), bv = bfs(raw + RAW_B * 0x800, rowo(t, j));
+        an = fmaf(kv * ic, p0[e], fmaf(bv * ic, p1[e], an));
+        const float dk = fmaf(cl, p0[e], y0[e]) * ic, db = fmaf(cl, p1[e], y1[e]) * ic;
+        XK[t * kN + j] = -kv * dk - bv * db;
+        if (t < len) {
+          args.dk[base + (size_t)t * vstep + j] = dk;
+          args.db[base + (size_t)t * vstep + j] = db;
+        }
+      }
+      anc[(2 + h) * kN + j] = cl * an;
+    } else {  // dr, da
+      ld8(tq + 96 + tbeg, p0);   // (DY S0)^T
+      ld8(tq + 112 + tbeg, p1);  // (DSA S0)^T
+      ld8(tq + 32 + tbeg, y0);
+      ld8(tq + 48 + tbeg, y1);
+      tmem_wait_ld();
+      float an = 0.f;
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        const int t = tbeg + e;
+        const float c = cc[e + 1], cp = cc[e];
+        const float rv = bfs(raw + RAW_R * 0x800, rowo(t, j)), av = bfs(raw + RAW_A * 0x800, rowo(t, j));
+        an = fmaf(rv * c, p0[e], fmaf(av * cp, p1[e], an));
+        const float dr = (p0[e] + y0[e]) * c, da = (p1[e] + y1[e]) * cp;
+        const float ad = av * da;
+        XR[t * kN + j] = fmaf(rv, dr, ad);
+        XA[t * kN + j] = ad;
+        if (t < len) {
+          args.dr[base + (size_t)t * vstep + j] = dr;
+          args.da[base + (size_t)t * vstep + j] = da;
+        }
+      }
+      anc[h * kN + j] = an;
+    }
+  }
+  __syncthreads();
+  // w dw from the identity, anchored where fewer terms are summed; thread (column, quarter
+  // of the steps q), the quarters' partial sums of x taken from the steps between:
+  //   t < 8:  colsum(carry at the chunk start o S0) - sum_{u<t} x(u) - a(t) da(t)
+  //   t >= 8: sum_{u>=t} x(u) - a(t) da(t) + colsum(carry at the chunk end o S(L))
+  {
+    const int col = tid & 63, q = tid >> 6, upper = q >> 1;
+    float eg = 0.f;
+#pragma unroll
+    for (int w8 = 0; w8 < 8; ++w8) eg += Epart[w8 * kN + col];
+    const float cge = cLs[col] * eg;
+    float run = cge + anc[2 * upper * kN + col] + anc[(2 * upper + 1) * kN + col];
+    if (q == 1) {
+#pragma unroll
+      for (int u = 0; u < 4; ++u) run -= XK[u * kN + col] + XR[u * kN + col];
+    } else if (q == 2) {
+#pragma unroll
+      for (int u = 12; u < kL; ++u) run += XK[u * kN + col] + XR[u * kN + col];
+    }
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const int t = upper ? 4 * q + 3 - e : 4 * q + e;
+      const float x = XK[t * kN + col] + XR[t * kN + col];
+      if (upper) run += x;
+      const float wraw = bfs(raw + RAW_W * 0x800, rowo(t, col));
+      float v;
+      if constexpr (kLogit)
+        v = logit_grad_from_wdw(run - XA[t * kN + col], wraw);
+      else
+        v = (run - XA[t * kN + col]) * rcp_approx(wraw);
+      if (t < len) args.dw[base + (size_t)t * vstep + col] = v;
+      if (!upper) run -= x;
+    }
+  }
+  return 1;
+}
+
+template <bool kLogit>
+__global__ void __launch_bounds__(kThreads, kCtasPerSm) wkv7_bwd4_tc_kernel(const __grid_constant__ BwdArgs args, int ntasks) {
+  extern __shared__ __align__(1024) unsigned char smem_raw[];
+  unsigned char* sb = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sb + OFF_BAR);
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(sb + OFF_BAR + 16);
+  const int warp = threadIdx.x >> 5;
+  if (threadIdx.x == 0) {
+    mbar_init(bars, 2);  // loads: two arrivals per task (v, dy, carry; the rows)
+    mbar_init(bars + 1, 1);
+    fence_mbar_init();
+#pragma unroll
+    for (int v = 0; v < 7; ++v) prefetch_tensormap(&args.swmap[v]);
+    prefetch_tensormap(&args.gcmap);
+  }
+  if (warp == 0) tmem_alloc(tslot, kTmemCols);
+  tmem_fence_before_sync();
+  __syncthreads();
+  tmem_fence_after_sync();
+  const uint32_t tb = *tslot;
+  // Persistent: this CTA takes tasks blockIdx.x, + gridDim.x, ...
+  int ld_it = 0, mma_it = 0;
+  for (int task = blockIdx.x; task < ntasks; task += gridDim.x) {
+    const int r = body<kLogit>(sb, tb, args, task, ld_it, mma_it);
+    if (r < 0) break;
+    ld_it += 1;
+    mma_it += r;
+    // every thread's reads of this task's tiles are ordered before the next task's TMA
+    // writes (another proxy) land in them
+    fence_proxy_async_smem();
+    __syncthreads();
+  }
+  tmem_fence_before_sync();
+  __syncthreads();
+  if (warp == 0) tmem_dealloc(tb, kTmemCols);
+}
+
+}  // namespace tcout
+
 }  // namespace
 
 size_t bwd4_workspace_bytes(int B, int T, int H) {
@@ -1210,7 +1846,18 @@ cudaError_t launch_bwd4_impl(const BwdArgs& args, cudaStream_t stream) {
   wkv7_bwd4_carry_kernel<kLogit><<<heads, kCarryThreads, smem_c, stream>>>(args);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  wkv7_bwd4_out_kernel<kLogit><<<heads * nchunks, kThreads, smem_o, stream>>>(args);
+  if (args.out_kernel != 1) {
+    wkv7_bwd4_out_kernel<kLogit><<<heads * nchunks, kThreads, smem_o, stream>>>(args);
+    return cudaGetLastError();
+  }
+  e = cudaFuncSetAttribute(tcout::wkv7_bwd4_tc_kernel<kLogit>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           (int)tcout::kSmemBytes);
+  if (e != cudaSuccess) return e;
+  int dev = 0, sms = 0;
+  if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
+  if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
+  const unsigned ntasks = heads * nchunks, grid = std::min<unsigned>(ntasks, (unsigned)tcout::kCtasPerSm * (unsigned)sms);
+  tcout::wkv7_bwd4_tc_kernel<kLogit><<<grid, tcout::kThreads, tcout::kSmemBytes, stream>>>(args, (int)ntasks);
   return cudaGetLastError();
 }
 

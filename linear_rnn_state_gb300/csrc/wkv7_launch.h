@@ -52,6 +52,12 @@ struct BwdArgs {
   const float* dS_final;  // [B][H][N][N] gradient entering through the final state, or null (zeros)
   const void* in[7];  // r, w, k, v, a, b, dy ([B][T][H][N], the input type)
   void* carry;        // split backward: [B*H][nchunks][N][N] carry after each chunk (bf16)
+  // Split backward's tensor-core output kernel: the seven vectors as maps with a
+  // (N, 1, 16, 1) box in 128-byte-swizzled shared-memory layout, and the carry
+  // workspace as (N, N, B*H*nchunks) with an (N, N, 1) box, also swizzled.
+  CUtensorMap swmap[7];
+  CUtensorMap gcmap;
+  int out_kernel = 0;  // split backward's output pass: 0 the mma.sync kernel, 1 the tcgen05 one
   unsigned* status;
   int w_logit = 0;    // 1: the w tiles hold logits z and dw receives dL/dz (split backward only)
   int C, nck;

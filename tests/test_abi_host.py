@@ -44,7 +44,7 @@ def test_debug_hook_only_in_the_debug_build(lib):
 
     text = re.sub(r"/\*.*?\*/", "", open(os.path.join(ROOT, "include", "wkv7_debug.h")).read(), flags=re.S)
     names = sorted(set(re.findall(r"\b(wkv7_\w+)\s*\(", text)))
-    assert names == ["wkv7_debug_skip_last_load"]
+    assert names == ["wkv7_debug_out_kernel", "wkv7_debug_skip_last_load"]
     dbg = lib.load(_build.DEBUG_LIB)
     for n in names:
         assert hasattr(dbg, n)
