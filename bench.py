@@ -533,13 +533,14 @@ def _report(args, wl, world, B, T, H, N, C, bf16, ms, fwd_ms, bwd_ms, e2e, ckpt,
         "e2e": None if e2e is None else {
             "value": aggregate_tokens_per_s(world, B, T, e2e[0]), "unit": "tokens/s", "h2d_bytes_per_step": e2e[1],
             "d2h_bytes_per_step": e2e[2]},
-        "gpu_launches": (6 if args.workload == "wkv7-epilogue" else 3 if (bf16 and N == 64) else 2) * args.steps,
+        "gpu_launches": (4 if args.workload == "wkv7-epilogue" else 3 if (bf16 and N == 64) else 2) * args.steps,
         "clocks": clocks.summary(),
     }
     if args.workload == "wkv7-epilogue":
         line["note"] = ("forward with the group-norm + bonus epilogue fused (out, normalized y and per-row stats "
-                        "written in the place of y); backward of the epilogue and the scan: a group-norm gradient "
-                        "pass, the scan's backward, the bonus terms and the parameters' gradients")
+                        "written in the place of y); backward with the epilogue's gradient fused into the scan's "
+                        "split backward (dy formed where the carry and output kernels read it, the bonus terms "
+                        "added to the output pass's stores) plus one small kernel summing the parameters' terms")
     elif args.workload == "wkv7-logit":
         line["note"] = "the decay given as logits z and formed inside the scan kernels; dz returned in the place of dw"
     if wl.name != configs_bench_workload():

@@ -223,11 +223,12 @@ int wkv7_forward_epilogue_bf16(const wkv7_bf16* r, const wkv7_bf16* w, const wkv
  *   dln_w, dln_b, dr_k  [H][N] fp32, summed over b and t (required).
  * The group-norm gradient that is the scan's upstream gradient,
  *     dy = rstd (dout ln_w - mean(dout ln_w) - nv mean(dout ln_w nv)),
- * is formed by a pass before the scan's backward into a bf16 workspace (with
- * the per-row gradient of the bonus); a pass after it adds the bonus terms to
- * dr, dk, dv. Workspaces from cudaMallocAsync on `stream` (WKV7_ERR_ALLOC);
- * N other than 64, or checkpoints with an interval other than 16, return
- * WKV7_ERR_INVALID.
+ * is formed inside the scan's split backward where its kernels read dy (rounded
+ * to bf16, as the scan's dy is), and the output pass adds the bonus terms to
+ * dr, dk, dv as it stores them; each chunk's parameter terms go to a workspace
+ * of B*H*ceil(T/16)*3*N floats (cudaMallocAsync on `stream`, WKV7_ERR_ALLOC)
+ * that a last small kernel sums in a fixed order. N other than 64, or
+ * checkpoints with an interval other than 16, return WKV7_ERR_INVALID.
  */
 int wkv7_backward_epilogue_bf16(const wkv7_bf16* r, const wkv7_bf16* w, const wkv7_bf16* k, const wkv7_bf16* v,
                                 const wkv7_bf16* a, const wkv7_bf16* b, const wkv7_bf16* dout, const wkv7_bf16* nv,

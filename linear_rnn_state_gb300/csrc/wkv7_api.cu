@@ -14,7 +14,6 @@
 #include "wkv7_debug.h"
 #endif
 #include "wkv7_common.cuh"
-#include "wkv7_epilogue.h"
 #include "wkv7_launch.h"
 
 namespace wkv7 {
@@ -270,9 +269,18 @@ int forward_impl(bool bf16, const void* const in[6], const float* s_init, void* 
 // checkpoints: the split pair (default) or the fused one-pass kernel.
 enum class BwdForm { kAuto, kFused };
 
+// The epilogue's backward fused into the split backward (wkv7_backward_epilogue_bf16):
+// in[6] is then dout, and these are the epilogue's other inputs and the per-chunk
+// parameter terms' workspace.
+struct EpiBwd {
+  const void* nv;
+  const float *stats, *ln_w, *r_k;
+  float* part;
+};
+
 int backward_impl(bool bf16, const void* const in[7], const float* s_init, const float* dS_final, const float* ckpt,
                   int C, float* const grads[6], float* dS_init, int B, int T, int H, int N, cudaStream_t stream,
-                  bool logit = false, BwdForm form = BwdForm::kAuto) {
+                  bool logit = false, BwdForm form = BwdForm::kAuto, const EpiBwd* eb = nullptr) {
   int rc = check_dims(B, T, H, N);
   if (rc) return rc;
   if (ckpt && C < 1) return fail(WKV7_ERR_INVALID, "ckpt_every must be >= 1 (got %d)", C);
@@ -385,6 +393,19 @@ int backward_impl(bool bf16, const void* const in[7], const float* s_init, const
 #ifdef WKV7_DEBUG
   args.out_kernel = g_debug_out_kernel.load();
 #endif
+  if (eb) {
+    if (!split) {
+      if (ws) cudaFreeAsync(ws, stream);
+      return fail(WKV7_ERR_INVALID, "the epilogue's backward runs in the split chunked form only");
+    }
+    args.epilogue = 1;
+    args.epi_nv = eb->nv;
+    args.epi_stats = eb->stats;
+    args.epi_ln_w = eb->ln_w;
+    args.epi_r_k = eb->r_k;
+    args.epi_part = eb->part;
+    rc = make_map(&args.map_nv, eb->nv, true, B, T, H, N, KS);
+  }
   if (split) {
     for (int v = 0; v < 7 && rc == WKV7_OK; ++v) rc = make_map(&args.swmap[v], in[v], true, B, T, H, N, kChunk, true);
     if (rc == WKV7_OK) rc = make_carry_map(&args.gcmap, args.carry, (size_t)B * H * ((T + kChunk - 1) / kChunk));
@@ -639,56 +660,35 @@ int wkv7_backward_epilogue_bf16(const wkv7_bf16* r, const wkv7_bf16* w, const wk
   const Span outs[3] = {{dln_w, par, "dln_w"}, {dln_b, par, "dln_b"}, {dr_k, par, "dr_k"}};
   if ((size_t)H == 0) return WKV7_OK;
   if ((rc = check_spans(ins, 6, outs, 3, (size_t)B * T ? 6 : 0, 3))) return rc;
+  const void* in[7] = {r, w, k, v, a, b, dout};
+  float* const grads[6] = {dr, dw, dk, dv, da, db};
   if ((size_t)B * T == 0) {  // no row: the parameters' gradients are empty sums
     for (float* p : {dln_w, dln_b, dr_k}) {
       cudaError_t e = cudaMemsetAsync(p, 0, par, s);
       if (e != cudaSuccess) return fail_cuda(e, "epilogue clear");
     }
-    const void* in[7] = {r, w, k, v, a, b, dout};
-    float* const grads[6] = {dr, dw, dk, dv, da, db};
     return backward_impl(true, in, s_init, dS_final, ckpt, ckpt_every, grads, dS_init, B, T, H, N, s,
                          decay_is_logit != 0);
   }
-  const int nblk = epi_blocks(B, T);
-  const size_t dy_bytes = (vec + 255) / 256 * 256, db_bytes = (rows * 4 + 255) / 256 * 256;
-  const size_t ws_bytes = dy_bytes + db_bytes + (size_t)H * nblk * 3 * N * 4;
+  // every chunk's parameter terms: [B][H][nchunks][3][N] fp32
+  const int nchunks = (T + kChunk - 1) / kChunk;
+  const size_t ws_bytes = (size_t)B * H * nchunks * 3 * N * 4;
   const char* inject = std::getenv("WKV7_FAIL_ALLOC");
   if (inject && inject[0] == '1') return fail(WKV7_ERR_ALLOC, "workspace allocation failed (injected by WKV7_FAIL_ALLOC)");
-  unsigned char* ws = nullptr;
-  cudaError_t e = cudaMallocAsync(reinterpret_cast<void**>(&ws), ws_bytes, s);
+  float* part = nullptr;
+  cudaError_t e = cudaMallocAsync(reinterpret_cast<void**>(&part), ws_bytes, s);
   if (e != cudaSuccess) {
     cudaGetLastError();
     return fail(WKV7_ERR_ALLOC, "epilogue workspace of %zu bytes: %s", ws_bytes, cudaGetErrorString(e));
   }
-  EpiBwdArgs ea;
-  ea.dout = reinterpret_cast<const __nv_bfloat16*>(dout);
-  ea.nv = reinterpret_cast<const __nv_bfloat16*>(nv);
-  ea.r = reinterpret_cast<const __nv_bfloat16*>(r);
-  ea.k = reinterpret_cast<const __nv_bfloat16*>(k);
-  ea.v = reinterpret_cast<const __nv_bfloat16*>(v);
-  ea.stats = stats;
-  ea.ln_w = ln_w;
-  ea.r_k = r_k;
-  ea.dy = reinterpret_cast<__nv_bfloat16*>(ws);
-  ea.dbon = reinterpret_cast<float*>(ws + dy_bytes);
-  ea.part = reinterpret_cast<float*>(ws + dy_bytes + db_bytes);
-  ea.dr = dr, ea.dk = dk, ea.dv = dv;
-  ea.dln_w = dln_w, ea.dln_b = dln_b, ea.dr_k = dr_k;
-  ea.B = B, ea.T = T, ea.H = H;
-  e = launch_epi_grad(ea, s);
-  if (e != cudaSuccess) {
-    cudaFreeAsync(ws, s);
-    return fail_cuda(e, "epilogue gradient launch");
+  const EpiBwd eb{nv, stats, ln_w, r_k, part};
+  rc = backward_impl(true, in, s_init, dS_final, ckpt, ckpt_every, grads, dS_init, B, T, H, N, s, decay_is_logit != 0,
+                     BwdForm::kAuto, &eb);
+  if (rc == WKV7_OK) {
+    e = launch_epi_params(part, dln_w, dln_b, dr_k, B, H, nchunks, s);
+    if (e != cudaSuccess) rc = fail_cuda(e, "epilogue parameter sums");
   }
-  const void* in[7] = {r, w, k, v, a, b, ea.dy};
-  float* const grads[6] = {dr, dw, dk, dv, da, db};
-  rc = backward_impl(true, in, s_init, dS_final, ckpt, ckpt_every, grads, dS_init, B, T, H, N, s,
-                     decay_is_logit != 0);
-  if (rc == WKV7_OK) {  // the bonus terms into dr, dk, dv, and the parameters' gradients
-    e = launch_epi_finish(ea, s);
-    if (e != cudaSuccess) rc = fail_cuda(e, "epilogue bonus launch");
-  }
-  cudaError_t e2 = cudaFreeAsync(ws, s);
+  cudaError_t e2 = cudaFreeAsync(part, s);
   if (rc == WKV7_OK && e2 != cudaSuccess) return fail_cuda(e2, "cudaFreeAsync(epilogue workspace)");
   return rc;
 }

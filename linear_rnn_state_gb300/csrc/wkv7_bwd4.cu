@@ -216,7 +216,7 @@ __device__ __forceinline__ void fetch_state(float* dst, const float* src, int ti
 
 // ================================================================ carry ===
 
-enum { C_R = 0, C_W = 1, C_A = 2, C_B = 3, C_DY = 4 };  // vectors staged for the carry
+enum { C_R = 0, C_W = 1, C_A = 2, C_B = 3, C_DY = 4, C_NV = 5 };  // vectors staged for the carry (nv: epilogue)
 constexpr int kCarryStages = 4;
 constexpr int kCarryThreads = 384;  // warps 0-3: state; 4-7: forming (F); 8-11: products (P)
 
@@ -240,7 +240,7 @@ struct ScratchC {
 };
 
 struct CarrySmem {
-  __nv_bfloat16 raw[kCarryStages][5][kTile];  // r, w, a, b, dy of one chunk per stage
+  __nv_bfloat16 raw[kCarryStages][6][kTile];  // r, w, a, b, dy (or dout), nv (epilogue) of one chunk per stage
   OpC op[3];
   ScratchC sc[2];
   float TT[kL * kLD16];  // T^T, T = (I - Mba)^-1
@@ -250,15 +250,44 @@ struct CarrySmem {
   int abort_flag;
 };
 
+// Sum over the 32 lanes (xor 16, 8, 4, 2, 1).
+__device__ __forceinline__ float warp_sum(float x) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
+  return x;
+}
+
+// The time-mix epilogue's group-norm backward for one row (step) of one head, as the 32
+// lanes of a warp hold it (lane l: channels 2 l, 2 l + 1): from the gradient of the
+// epilogue's output d and the normalized output nv, the scan's upstream gradient
+//     dn = d ln_w ;  dy = rstd (dn - mean(dn) - nv mean(dn nv)),
+// rounded to bf16 (the scan's dy is bf16).
+__device__ __forceinline__ __nv_bfloat162 gn_backward_row(float2 d, float2 nv, float2 lw, float rstd) {
+  const float dn0 = d.x * lw.x, dn1 = d.y * lw.y;
+  const float s1 = warp_sum(dn0 + dn1);
+  const float s2 = warp_sum(fmaf(dn0, nv.x, dn1 * nv.y));
+  const float m1 = s1 * (1.f / kN), m2 = s2 * (1.f / kN);
+  return __floats2bfloat162_rn(rstd * (dn0 - m1 - nv.x * m2), rstd * (dn1 - m1 - nv.y * m2));
+}
+
 // Forming group (128 threads): the scaled operands of a chunk. Thread
 // (lane, pf) forms columns 2 lane, 2 lane + 1 of steps 4 pf .. 4 pf + 3. The
 // running products c(t) are taken per block of four steps and the blocks'
 // products chained in step order. Returns (uniformly over the group) whether
 // some decay leaves the range of the scaled form.
-template <bool kLogit>
-__device__ bool form_carry(ScratchC& sc, float (&Pc)[4][kN], const __nv_bfloat16* rs, OpC& op, int len, int ftid) {
+template <bool kLogit, bool kEpi>
+__device__ bool form_carry(ScratchC& sc, float (&Pc)[4][kN], __nv_bfloat16* rs, OpC& op, int len, int ftid,
+                           const float* epi_rstd, float2 epi_lw) {
   const int lane = ftid & 31, pf = ftid >> 5, j = 2 * lane, t0 = 4 * pf;
   float2 wv[4], av[4], rv[4], bv[4], dyv[4];
+  if constexpr (kEpi) {  // epilogue: the stage holds dout and nv; dy replaces dout (the step-by-step path reads it)
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const int o = (t0 + e) * kN + j;
+      *reinterpret_cast<__nv_bfloat162*>(rs + C_DY * kTile + o) =
+          gn_backward_row(bf2(rs + C_DY * kTile + o), bf2(rs + C_NV * kTile + o), epi_lw, epi_rstd[e]);
+    }
+  }
   bool safe = true;
   float2 pb = make_float2(1.f, 1.f);
 #pragma unroll
@@ -327,16 +356,16 @@ __device__ __forceinline__ void gram_tile(float* M, const float* P, const float*
 
 // Forming group: wait for a chunk's inputs and form its operands. Returns
 // false on a timeout.
-template <bool kLogit>
-__device__ bool front_form(CarrySmem& sm, ScratchC& sc, OpC& op, const __nv_bfloat16* rs, uint64_t* bar,
-                           uint32_t parity, int len, unsigned* status) {
+template <bool kLogit, bool kEpi>
+__device__ bool front_form(CarrySmem& sm, ScratchC& sc, OpC& op, __nv_bfloat16* rs, uint64_t* bar,
+                           uint32_t parity, int len, unsigned* status, const float* epi_rstd, float2 epi_lw) {
   const int ftid = threadIdx.x - 128;
   const bool ok = mbar_wait_bounded(status, bar, parity);
   if (named_bar_or(1, 128, !ok)) {
     if (ftid == 0) sm.abort_flag = 1;
     return false;
   }
-  const bool unsafe = form_carry<kLogit>(sc, sm.Pc, rs, op, len, ftid);
+  const bool unsafe = form_carry<kLogit, kEpi>(sc, sm.Pc, rs, op, len, ftid, epi_rstd, epi_lw);
   if (ftid == 0) op.unsafe = unsafe;
   if (unsafe) return true;
   named_bar(1, 128);
@@ -493,7 +522,7 @@ __device__ __forceinline__ void flush_carry(const bf16_t* src, bf16_t* dst, int 
   }
 }
 
-template <bool kLogit>
+template <bool kLogit, bool kEpi>
 __global__ void __launch_bounds__(kCarryThreads, 1) wkv7_bwd4_carry_kernel(const __grid_constant__ BwdArgs args) {
   extern __shared__ __align__(128) unsigned char smem_raw[];
   CarrySmem& sm = *reinterpret_cast<CarrySmem*>(smem_raw);
@@ -503,7 +532,8 @@ __global__ void __launch_bounds__(kCarryThreads, 1) wkv7_bwd4_carry_kernel(const
   const int role = warp < 4 ? 0 : warp < 8 ? 1 : 2;  // state, forming, products
   const int i0 = 16 * warp;                          // state warps: rows of the carry
   const int nchunks = (T + kL - 1) / kL;
-  constexpr int kStageBytes = 5 * kTile * 2;
+  const int nvec = kEpi ? 6 : 5;
+  const uint32_t stage_bytes = (uint32_t)(nvec * kTile * 2);
   bf16_t* carry_head = reinterpret_cast<bf16_t*>(args.carry) + (size_t)head * nchunks * kN * kN;
 
   // Chunks are visited in reverse: visit v is chunk nchunks-1-v. In visit m the state warps
@@ -514,15 +544,37 @@ __global__ void __launch_bounds__(kCarryThreads, 1) wkv7_bwd4_carry_kernel(const
   auto issue = [&](int v) {
     const int st = v % kCarryStages;
     const int vmap[5] = {V_R, V_W, V_A, V_B, V_DY};
-    mbar_arrive_expect_tx(&sm.full[st], kStageBytes);
+    mbar_arrive_expect_tx(&sm.full[st], stage_bytes);
     for (int q = 0; q < 5; ++q)
       tma_load_4d(sm.raw[st][q], &args.map[vmap[q]], &sm.full[st], 0, hi, chunk_of(v) * kL, bi);
+    if constexpr (kEpi) tma_load_4d(sm.raw[st][C_NV], &args.map_nv, &sm.full[st], 0, hi, chunk_of(v) * kL, bi);
   };
+  // Epilogue: the forming threads' rstd (rows 4 pf .. 4 pf + 3 of the chunk they form next),
+  // requested a visit ahead, and ln_w of their two channels.
+  float rs_next[4] = {0.f, 0.f, 0.f, 0.f}, rs_cur[4];
+  float2 epi_lw = make_float2(0.f, 0.f);
+  auto load_rstd = [&](int v) {
+    const int t0 = chunk_of(v) * kL + 4 * ((tid - 128) >> 5);
+#pragma unroll
+    for (int e = 0; e < 4; ++e)
+      rs_next[e] = t0 + e < T ? args.epi_stats[2 * (((size_t)bi * T + t0 + e) * H + hi)] : 0.f;
+  };
+  if (kEpi && role == 1) {
+    epi_lw = *reinterpret_cast<const float2*>(args.epi_ln_w + (size_t)hi * kN + 2 * (lane));
+    load_rstd(0);
+  }
   int waited = 0, issued = 0;
   auto form = [&](int v) {  // forming group; false on a timeout
     const int c = chunk_of(v);
-    if (!front_form<kLogit>(sm, sm.sc[c & 1], sm.op[c % 3], sm.raw[v % kCarryStages][0], &sm.full[v % kCarryStages],
-                    (v / kCarryStages) & 1, len_of(v), args.status))
+    const float* rst = nullptr;
+    if constexpr (kEpi) {
+#pragma unroll
+      for (int e = 0; e < 4; ++e) rs_cur[e] = rs_next[e];
+      if (v + 1 < nchunks) load_rstd(v + 1);
+      rst = rs_cur;
+    }
+    if (!front_form<kLogit, kEpi>(sm, sm.sc[c & 1], sm.op[c % 3], sm.raw[v % kCarryStages][0], &sm.full[v % kCarryStages],
+                            (v / kCarryStages) & 1, len_of(v), args.status, rst, epi_lw))
       return false;
     waited = v + 1;
     return true;
@@ -538,6 +590,7 @@ __global__ void __launch_bounds__(kCarryThreads, 1) wkv7_bwd4_carry_kernel(const
     for (int s = 0; s < kCarryStages; ++s) mbar_init(&sm.full[s], 1);
     fence_mbar_init();
     for (int q = 0; q < 7; ++q) prefetch_tensormap(&args.map[q]);
+    if (kEpi) prefetch_tensormap(&args.map_nv);
     for (int v = 0; v < kCarryStages && v < nchunks; ++v) issue(v);
   }
   issued = min(kCarryStages, nchunks);
@@ -658,6 +711,48 @@ struct OutSmem {
   float cLs[kN];          // c(L) = product of the chunk's decays
   float anc[2][kN];  // the chunk's parts of colsum(carry o state) at its start and end, without c(L) colsum(Gc o S0)
 };
+
+// Extra shared memory of the output pass with the epilogue's backward fused (after OutSmem).
+struct OutEpiSmem {
+  bf16_t dout[kL * kB64];  // the gradient of the epilogue's output [t][i]
+  bf16_t nv[kL * kB64];    // the normalized y [t][i]
+  float stat[kL][2];       // (rstd, bonus) per step
+  float dbon[kL];          // gradient of each step's bonus: sum_i dout_i v_i
+  float lnw[kN], rk[kN];
+};
+
+// The epilogue's bonus terms for the chunk's stored dr, dk, dv (a chunk run step by step:
+// added to what out_direct wrote): dr += dbon k r_k, dk += dbon r r_k, dv += dout bonus.
+__device__ void epi_bonus_direct(const OutEpiSmem& ep, const bf16_t* rs, int len, const BwdArgs& args, size_t base,
+                                 size_t vstep) {
+  constexpr int RS = kL * kB64;
+  for (int idx = threadIdx.x; idx < len * kN; idx += kThreads) {
+    const int t = idx / kN, c = idx % kN;
+    const size_t off = base + (size_t)t * vstep + c;
+    const float db = ep.dbon[t];
+    args.dr[off] += db * bf(rs + V_K * RS + t * kB64 + c) * ep.rk[c];
+    args.dk[off] += db * bf(rs + V_R * RS + t * kB64 + c) * ep.rk[c];
+    args.dv[off] += bf(ep.dout + t * kB64 + c) * ep.stat[t][1];
+  }
+}
+
+// This chunk's terms of the epilogue's parameter gradients, from every thread's partial
+// sums over its steps (columns 2 lane, 2 lane + 1): sum_t dout nv, sum_t dout,
+// sum_t dbon r k, summed over the warps in order into epi_part.
+__device__ void epi_params_chunk(float* scratch, const float (&pp)[3][2], const BwdArgs& args, int head, int n,
+                                 int nchunks) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+#pragma unroll
+  for (int q = 0; q < 3; ++q)
+    *reinterpret_cast<float2*>(scratch + (warp * 3 + q) * kN + 2 * lane) = make_float2(pp[q][0], pp[q][1]);
+  __syncthreads();
+  for (int i = threadIdx.x; i < 3 * kN; i += kThreads) {
+    float x = 0.f;
+#pragma unroll
+    for (int w8 = 0; w8 < 8; ++w8) x += scratch[w8 * 3 * kN + i];
+    args.epi_part[((size_t)head * nchunks + n) * 3 * kN + i] = x;
+  }
+}
 
 // Step-by-step reverse scan of one chunk (all eight warps, fp32; warp w owns
 // rows 8 w .. 8 w + 7 of the state and the carry, lane (g, t) row 8 w + g and
@@ -791,10 +886,12 @@ __device__ __forceinline__ void cp_async16_zfill(void* dst, const void* src, boo
                : "memory");
 }
 
-template <bool kLogit>
+template <bool kLogit, bool kEpi>
 __global__ void __launch_bounds__(kThreads, 3) wkv7_bwd4_out_kernel(const __grid_constant__ BwdArgs args) {
   extern __shared__ __align__(128) unsigned char smem_raw[];
   OutSmem& sm = *reinterpret_cast<OutSmem*>(smem_raw);
+  OutEpiSmem& ep = *reinterpret_cast<OutEpiSmem*>(smem_raw + sizeof(OutSmem));  // epilogue only
+  constexpr bool epi = kEpi;
   const int T = args.T, H = args.H, nchunks = (T + kL - 1) / kL;
   const int head = blockIdx.x / nchunks, n = blockIdx.x % nchunks, bi = head / H, hi = head % H;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, g = lane >> 2, t4 = lane & 3;
@@ -804,11 +901,25 @@ __global__ void __launch_bounds__(kThreads, 3) wkv7_bwd4_out_kernel(const __grid
   const bf16_t* Gcg = reinterpret_cast<const bf16_t*>(args.carry) + ((size_t)head * nchunks + n) * kN * kN;
   constexpr int RS = kL * kB64;  // elements between staged vectors
 
-  // ---- loads: the chunk's rows (zeros past T) and the carry by cp.async, the checkpoint through registers
-  for (int idx = tid; idx < 7 * kL * 8; idx += kThreads) {
+  // ---- loads: the chunk's rows (zeros past T) and the carry by cp.async, the checkpoint through registers.
+  //      Epilogue: dout (in the place of dy) and nv to their own tiles, dy is formed below.
+  for (int idx = tid; idx < (epi ? 8 : 7) * kL * 8; idx += kThreads) {
     const int v = idx / (kL * 8), t = (idx >> 3) % kL, c = idx & 7;
-    const bf16_t* src = static_cast<const bf16_t*>(args.in[v]) + base + (size_t)min(t, len - 1) * vstep + 8 * c;
-    cp_async16_zfill(sm.raw[v] + t * kB64 + 8 * c, src, t < len);
+    const bf16_t* src = static_cast<const bf16_t*>(v == 7 ? args.epi_nv : args.in[v]) + base +
+                        (size_t)min(t, len - 1) * vstep + 8 * c;
+    bf16_t* dst = !epi || v < V_DY ? sm.raw[v] : v == V_DY ? ep.dout : ep.nv;
+    cp_async16_zfill(dst + t * kB64 + 8 * c, src, t < len);
+  }
+  if (epi) {
+    if (tid < kL) {
+      const float2 st = tid < len ? *reinterpret_cast<const float2*>(args.epi_stats + 2 * (((size_t)bi * T + t0 + tid) * H + hi))
+                                  : make_float2(0.f, 0.f);
+      ep.stat[tid][0] = st.x;
+      ep.stat[tid][1] = st.y;
+    } else if (tid >= 64 && tid < 64 + kN) {
+      ep.lnw[tid - 64] = args.epi_ln_w[(size_t)hi * kN + tid - 64];
+      ep.rk[tid - 64] = args.epi_r_k[(size_t)hi * kN + tid - 64];
+    }
   }
 #pragma unroll
   for (int q = 0; q < kN * 8 / kThreads; ++q) {
@@ -828,6 +939,28 @@ __global__ void __launch_bounds__(kThreads, 3) wkv7_bwd4_out_kernel(const __grid
   cp_async_wait_all();
   __syncthreads();
   const bf16_t* rs = sm.raw[0];
+  // Epilogue: the scan's dy (rows of the step pairs 2 warp, 2 warp + 1, lane's channels
+  // 2 lane, 2 lane + 1), each step's dbon, and this thread's parameter terms.
+  float pp[3][2] = {{0.f, 0.f}, {0.f, 0.f}, {0.f, 0.f}};
+  if (epi) {
+    const int j = 2 * lane;
+    const float2 lw = make_float2(ep.lnw[j], ep.lnw[j + 1]);
+#pragma unroll
+    for (int e = 0; e < 2; ++e) {
+      const int t = 2 * warp + e, q = t * kB64 + j;
+      const float2 d = bf2(ep.dout + q), nv = bf2(ep.nv + q), v = bf2(rs + V_V * RS + q);
+      *reinterpret_cast<__nv_bfloat162*>(sm.raw[V_DY] + q) = gn_backward_row(d, nv, lw, ep.stat[t][0]);
+      const float dbon = warp_sum(fmaf(d.x, v.x, d.y * v.y));
+      if (lane == 0) ep.dbon[t] = dbon;
+      const float2 r = bf2(rs + V_R * RS + q), k = bf2(rs + V_K * RS + q);
+      pp[0][0] = fmaf(d.x, nv.x, pp[0][0]);
+      pp[0][1] = fmaf(d.y, nv.y, pp[0][1]);
+      pp[1][0] += d.x;
+      pp[1][1] += d.y;
+      pp[2][0] = fmaf(dbon, r.x * k.x, pp[2][0]);
+      pp[2][1] = fmaf(dbon, r.y * k.y, pp[2][1]);
+    }
+  }
 
   // ---- A: scaled operands; thread (lane, warp) forms columns 2 lane, 2 lane + 1 of steps
   //      2 warp, 2 warp + 1. The running products c(t) are taken per pair of steps and the
@@ -843,6 +976,10 @@ __global__ void __launch_bounds__(kThreads, 3) wkv7_bwd4_out_kernel(const __grid
     *reinterpret_cast<float2*>(&sm.Ppart[warp][j]) = fmul2(wv[0], wv[1]);
     if (__syncthreads_or(!safe)) {
       out_direct<kLogit>(sm.raw[0], sm.u.red, S0g, Gcg, len, args, base, vstep, warp, lane);
+      if (epi) {
+        epi_bonus_direct(ep, rs, len, args, base, vstep);
+        epi_params_chunk(sm.u.red, pp, args, head, n, nchunks);
+      }
       return;
     }
     float2 cL = make_float2(1.f, 1.f), cpre = cL;  // cpre = c(ta - 1)
@@ -972,8 +1109,13 @@ __global__ void __launch_bounds__(kThreads, 3) wkv7_bwd4_out_kernel(const __grid
         const int t = 8 * q + 2 * t4 + e;
         if (t < len) {
           float* dst = args.dv + base + (size_t)t * vstep + r0 + g;
-          dst[0] = X2[q][e];
-          dst[8] = X2[q][2 + e];
+          float x0 = X2[q][e], x1 = X2[q][2 + e];
+          if (epi) {  // + dout bonus
+            x0 = fmaf(bf(ep.dout + t * kB64 + r0 + g), ep.stat[t][1], x0);
+            x1 = fmaf(bf(ep.dout + t * kB64 + r0 + g + 8), ep.stat[t][1], x1);
+          }
+          dst[0] = x0;
+          dst[8] = x1;
         }
       }
   } else if (warp >= 1) {
@@ -1163,7 +1305,14 @@ __global__ void __launch_bounds__(kThreads, 3) wkv7_bwd4_out_kernel(const __grid
       if (grp) *reinterpret_cast<float2*>(XA + t * kLD64 + col) = make_float2(AD[nt][2 * h], AD[nt][2 * h + 1]);
       if (t < len) {
         const size_t off = base + (size_t)t * vstep + col;
-        *reinterpret_cast<float2*>(out0 + off) = make_float2(P0[nt][2 * h], P0[nt][2 * h + 1]);
+        float2 o0 = make_float2(P0[nt][2 * h], P0[nt][2 * h + 1]);
+        if (epi) {  // the bonus terms: dk += dbon r r_k (grp 0), dr += dbon k r_k (grp 1)
+          const float db = ep.dbon[t];
+          const float2 x = bf2(rs + (grp ? V_K : V_R) * RS + t * kB64 + col);
+          o0.x = fmaf(db * x.x, ep.rk[col], o0.x);
+          o0.y = fmaf(db * x.y, ep.rk[col + 1], o0.y);
+        }
+        *reinterpret_cast<float2*>(out0 + off) = o0;
         *reinterpret_cast<float2*>(out1 + off) = make_float2(P1[nt][2 * h], P1[nt][2 * h + 1]);
       }
     }
@@ -1189,6 +1338,10 @@ __global__ void __launch_bounds__(kThreads, 3) wkv7_bwd4_out_kernel(const __grid
       if (t < len) args.dw[base + (size_t)t * vstep + col] = v;
       if (!upper) run -= x;  // start anchor minus the x of the steps before t
     }
+  }
+  if (epi) {
+    __syncthreads();  // the dw exchange is read; its space takes the parameter terms
+    epi_params_chunk(sm.u.xch[0], pp, args, head, n, nchunks);
   }
 }
 
@@ -1834,20 +1987,21 @@ size_t bwd4_workspace_bytes(int B, int T, int H) {
   return heads * nchunks * kN * kN * sizeof(__nv_bfloat16);
 }
 
-template <bool kLogit>
+template <bool kLogit, bool kEpi>
 cudaError_t launch_bwd4_impl(const BwdArgs& args, cudaStream_t stream) {
-  const size_t smem_c = sizeof(CarrySmem), smem_o = sizeof(OutSmem);
-  cudaError_t e =
-      cudaFuncSetAttribute(wkv7_bwd4_carry_kernel<kLogit>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_c);
-  if (e != cudaSuccess) return e;
-  e = cudaFuncSetAttribute(wkv7_bwd4_out_kernel<kLogit>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_o);
+  const size_t smem_c = sizeof(CarrySmem), smem_o = sizeof(OutSmem) + (kEpi ? sizeof(OutEpiSmem) : 0);
+  cudaError_t e = cudaFuncSetAttribute(wkv7_bwd4_carry_kernel<kLogit, kEpi>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_c);
   if (e != cudaSuccess) return e;
   const unsigned heads = (unsigned)(args.B * args.H), nchunks = (unsigned)((args.T + kL - 1) / kL);
-  wkv7_bwd4_carry_kernel<kLogit><<<heads, kCarryThreads, smem_c, stream>>>(args);
+  wkv7_bwd4_carry_kernel<kLogit, kEpi><<<heads, kCarryThreads, smem_c, stream>>>(args);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  if (args.out_kernel != 1) {
-    wkv7_bwd4_out_kernel<kLogit><<<heads * nchunks, kThreads, smem_o, stream>>>(args);
+  if (args.out_kernel != 1 || kEpi) {
+    e = cudaFuncSetAttribute(wkv7_bwd4_out_kernel<kLogit, kEpi>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)smem_o);
+    if (e != cudaSuccess) return e;
+    wkv7_bwd4_out_kernel<kLogit, kEpi><<<heads * nchunks, kThreads, smem_o, stream>>>(args);
     return cudaGetLastError();
   }
   e = cudaFuncSetAttribute(tcout::wkv7_bwd4_tc_kernel<kLogit>, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -1862,7 +2016,9 @@ cudaError_t launch_bwd4_impl(const BwdArgs& args, cudaStream_t stream) {
 }
 
 cudaError_t launch_bwd4(const BwdArgs& args, cudaStream_t stream) {
-  return args.w_logit ? launch_bwd4_impl<true>(args, stream) : launch_bwd4_impl<false>(args, stream);
+  if (args.epilogue)
+    return args.w_logit ? launch_bwd4_impl<true, true>(args, stream) : launch_bwd4_impl<false, true>(args, stream);
+  return args.w_logit ? launch_bwd4_impl<true, false>(args, stream) : launch_bwd4_impl<false, false>(args, stream);
 }
 
 }  // namespace wkv7

@@ -58,6 +58,18 @@ struct BwdArgs {
   CUtensorMap swmap[7];
   CUtensorMap gcmap;
   int out_kernel = 0;  // split backward's output pass: 0 the mma.sync kernel, 1 the tcgen05 one
+  // Backward of the time-mix epilogue fused into the split backward (mma.sync output pass):
+  // the dy vector (map[6], in[6]) holds dout, the gradient of the epilogue's output, and the
+  // kernels form the scan's dy = rstd (dn - mean(dn) - nv mean(dn nv)), dn = dout ln_w, where
+  // they read it; the output pass also adds the bonus terms to dr, dk, dv and writes each
+  // chunk's parameter terms.
+  int epilogue = 0;
+  CUtensorMap map_nv;          // nv [B][T][H][N] bf16, box (N, 1, 16, 1)
+  const void* epi_nv = nullptr;
+  const float* epi_stats = nullptr;  // [B][T][H][2] (rstd, bonus)
+  const float* epi_ln_w = nullptr;   // [H][N]
+  const float* epi_r_k = nullptr;    // [H][N]
+  float* epi_part = nullptr;         // [B][H][nchunks][3][N]: sum_t dout nv, sum_t dout, sum_t dbon r k
   unsigned* status;
   int w_logit = 0;    // 1: the w tiles hold logits z and dw receives dL/dz (split backward only)
   int C, nck;
@@ -77,6 +89,9 @@ cudaError_t launch_bwd3(const BwdArgs& args, cudaStream_t stream);
 // kernel; needs args.carry, a workspace of bwd4_workspace_bytes.
 cudaError_t launch_bwd4(const BwdArgs& args, cudaStream_t stream);
 size_t bwd4_workspace_bytes(int B, int T, int H);
+// dln_w, dln_b, dr_k [H][N] from the output pass's per-chunk terms, summed in a fixed order.
+cudaError_t launch_epi_params(const float* part, float* dln_w, float* dln_b, float* dr_k, int B, int H, int nchunks,
+                              cudaStream_t stream);
 constexpr int kChunk = 16;
 inline bool use_chunked(bool bf16, int N, int C) { return bf16 && N == 64 && C % kChunk == 0; }
 cudaError_t launch_bwd2(const BwdArgs& args, bool bf16, int N, cudaStream_t stream);
