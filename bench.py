@@ -35,20 +35,21 @@ FP32_LANES_PER_SM = 128  # Blackwell SM: 4 partitions x 32 FP32 lanes
 TRAFFIC = {
     "kernel": "wkv7_bwd4_carry_kernel + wkv7_bwd4_out_kernel (one wkv7_backward_bf16 call)",
     "sources": ("wkv7_bwd4.cu", "wkv7_common.cuh", "wkv7_scaled.cuh", "wkv7_mma.cuh", "wkv7_launch.h",
-                "wkv7_decay.cuh"),
-    "sha256": "b6d7e74b628bf65c30e012a75aecaec35f20f0a6021bcd5a59138e697919a2ec",
-    "bytes_per_token_head": (83.953664e6 + 28.174848e6 + 318.850048e6 + 162.109952e6) / 131072,
+                "wkv7_decay.cuh", "wkv7_tmem.cuh"),
+    "sha256": "19536b6bd69788d0742498ac2300cefb7d7f19e6c539777052b5d1524ab3689d",
+    "bytes_per_token_head": (83.953920e6 + 28.895744e6 + 318.861056e6 + 161.701376e6) / 131072,
 }
 
 
 # The fp32 backward (wkv7_backward at N = 64) runs one kernel; its DRAM bytes per token-head from
-# one ncu capture, null until taken (and once its sources change).
+# one ncu capture at the 8 x 4096 x 12 workload (dram__bytes_read.sum + dram__bytes_write.sum of
+# one launch / (B*T*H)), null once its sources change.
 TRAFFIC_FP32 = {
     "kernel": "wkv7_bwd2_kernel (one wkv7_backward call, fp32 inputs)",
     "sources": ("wkv7_bwd2.cu", "wkv7_common.cuh", "wkv7_scaled.cuh", "wkv7_tmem.cuh", "wkv7_launch.h"),
-    "sha256": "",
+    "sha256": "eed32800391914dce60eb7b191285669bca86d5bcf4aa6e18465af8b80d628a2",
     "N": 64,
-    "bytes_per_token_head": None,
+    "bytes_per_token_head": (1107.634432e6 + 571.360768e6) / 393216,
 }
 
 
