@@ -53,6 +53,7 @@ extern "C" {
 #define WKV7_ERR_INVALID (-2) /* bad pointer, size, alignment or overlap */
 #define WKV7_ERR_CUDA (-3)    /* a CUDA launch or runtime call failed */
 #define WKV7_ERR_TIMEOUT (-4) /* a kernel gave up a bounded wait (wkv7_status) */
+#define WKV7_ERR_BOUNDS (-5)  /* debug build only: a kernel skipped an access outside its buffer (wkv7_status) */
 
 /* bfloat16 values are passed as their 16-bit patterns. */
 typedef uint16_t wkv7_bf16;
@@ -248,7 +249,10 @@ int wkv7_default_ckpt_every(int N, int bf16);
 
 /* Waits for `stream`, then reports (and clears) what the kernels flagged on
  * the current device: WKV7_OK, WKV7_ERR_TIMEOUT when a bounded wait inside a
- * kernel gave up, or WKV7_ERR_CUDA for a CUDA error. */
+ * kernel gave up, WKV7_ERR_BOUNDS when (in the debug build, which checks every
+ * plain global load and store of the scan kernels against the buffer it
+ * belongs to) a kernel found an index outside its buffer and skipped that
+ * access, or WKV7_ERR_CUDA for a CUDA error. */
 int wkv7_status(void* stream);
 
 /* Message of the calling thread's last failed call ("" if none). */

@@ -4,10 +4,11 @@ The translation units compile in parallel, then link into one shared library
 that uses the shared CUDA runtime (the same libcudart.so.13 PyTorch loads, so
 both see the same current device).
 
-It also links the debug build, libwkv7_debug.so: the same objects except the
-C ABI and the scalar forward, recompiled with WKV7_DEBUG (1 ms mbarrier wait
-limit, and the hook of include/wkv7_debug.h that lets a test make a wait run
-out). Only the tests of the timeout path load it.
+It also links the debug build, libwkv7_debug.so: the same objects, the C ABI
+and the WKV7 scan kernels recompiled with WKV7_DEBUG (every plain global load
+and store checked against its buffer, 1 ms mbarrier wait limit, and the hooks
+of include/wkv7_debug.h). Only the tests of those checks and of the timeout
+path load it.
 """
 from __future__ import annotations
 
@@ -23,7 +24,8 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD_DIR = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libwkv7.so")
 DEBUG_LIB = os.path.join(PKG, "libwkv7_debug.so")
-DEBUG_SOURCES = ["wkv7_api.cu", "wkv7_fwd2.cu"]  # recompiled with -DWKV7_DEBUG for the debug build
+DEBUG_SOURCES = ["wkv7_api.cu", "wkv7_fwd2.cu", "wkv7_fwd3.cu", "wkv7_bwd2.cu", "wkv7_bwd3.cu",
+                 "wkv7_bwd4.cu"]  # recompiled with -DWKV7_DEBUG for the debug build
 
 SOURCES = ["wkv7_api.cu", "wkv7_fwd2.cu", "wkv7_fwd3.cu", "wkv7_bwd2.cu", "wkv7_bwd3.cu", "wkv7_bwd4.cu", "rwkv8_api.cu",
            "rwkv8_fwd.cu", "rwkv8_bwd.cu", "rwkv8_state.cu", "rwkv8_chunk.cu", "wkv7_epilogue.cu"]

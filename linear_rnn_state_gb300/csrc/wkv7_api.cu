@@ -178,10 +178,55 @@ int status_word(unsigned** out) {
 }
 
 #ifdef WKV7_DEBUG
-// Debug build: set by wkv7_debug_skip_last_load (include/wkv7_debug.h).
+// Debug build: set by the hooks of include/wkv7_debug.h.
 std::atomic<int> g_debug_skip_last_load{0};
 std::atomic<int> g_debug_out_kernel{0};
+std::atomic<size_t> g_debug_extent_cut{0};
 #endif
+
+// The extent of a buffer as the kernels check it in the debug build: its size,
+// less the bytes wkv7_debug_cut_extents asked to cut off its end.
+Extent extent(const void* p, size_t bytes) {
+#ifdef WKV7_DEBUG
+  const size_t cut = g_debug_extent_cut.load();
+  bytes = bytes > cut ? bytes - cut : 0;
+#endif
+  return Extent{p, p ? bytes : 0};
+}
+
+// The buffers of a forward launch, as the api validated them; the checkpoint
+// buffer holds ck_bytes.
+void set_extents(FwdArgs& a, int N, bool bf16, size_t ck_bytes) {
+  const size_t vec = (size_t)a.B * a.T * a.H * N, st = (size_t)a.B * a.H * N * N * 4, par = (size_t)a.H * N * 4;
+  a.ext.y = extent(a.y, vec * (bf16 ? 2 : 4));
+  a.ext.nv = extent(a.nv, vec * 2);
+  a.ext.stats = extent(a.stats, (size_t)a.B * a.T * a.H * 2 * 4);
+  a.ext.s_init = extent(a.s_init, st);
+  a.ext.s_final = extent(a.s_final, st);
+  a.ext.ckpt = extent(a.ckpt, ck_bytes);
+  a.ext.ln_w = extent(a.ln_w, par);
+  a.ext.ln_b = extent(a.ln_b, par);
+  a.ext.r_k = extent(a.r_k, par);
+}
+
+// The buffers of a backward launch; the checkpoints take ck_bytes.
+void set_extents(BwdArgs& a, int N, bool bf16, size_t ck_bytes) {
+  const size_t vec = (size_t)a.B * a.T * a.H * N, st = (size_t)a.B * a.H * N * N * 4, par = (size_t)a.H * N * 4;
+  const size_t nchunks = ((size_t)a.T + kChunk - 1) / kChunk;
+  for (int v = 0; v < 7; ++v) a.ext.in[v] = extent(a.in[v], vec * (bf16 ? 2 : 4));
+  a.ext.in[7] = extent(a.epi_nv, vec * 2);
+  a.ext.ckpt = extent(a.ckpt, ck_bytes);
+  a.ext.carry = extent(a.carry, a.carry ? bwd4_workspace_bytes(a.B, a.T, a.H) : 0);
+  float* const g[6] = {a.dr, a.dw, a.dk, a.dv, a.da, a.db};
+  Extent* const x[6] = {&a.ext.dr, &a.ext.dw, &a.ext.dk, &a.ext.dv, &a.ext.da, &a.ext.db};
+  for (int q = 0; q < 6; ++q) *x[q] = extent(g[q], vec * 4);
+  a.ext.dS_init = extent(a.dS_init, st);
+  a.ext.dS_final = extent(a.dS_final, st);
+  a.ext.stats = extent(a.epi_stats, (size_t)a.B * a.T * a.H * 2 * 4);
+  a.ext.ln_w = extent(a.epi_ln_w, par);
+  a.ext.r_k = extent(a.epi_r_k, par);
+  a.ext.part = extent(a.epi_part, (size_t)a.B * a.H * nchunks * 3 * N * 4);
+}
 
 // ------------------------------------------------------------ forward ---
 
@@ -258,6 +303,7 @@ int forward_impl(bool bf16, const void* const in[6], const float* s_init, void* 
   args.B = B;
   args.T = T;
   args.H = H;
+  set_extents(args, N, bf16, ckpt ? ckpt_bytes(B, T, H, N, C) : 0);
   cudaError_t e = use_chunked(bf16, N, ckpt ? C : kChunk) ? launch_fwd3(args, stream) : launch_fwd2(args, bf16, N, stream);
   if (e != cudaSuccess) return fail_cuda(e, "forward launch");
   return WKV7_OK;
@@ -365,6 +411,7 @@ int backward_impl(bool bf16, const void* const in[7], const float* s_init, const
     fa.B = B;
     fa.T = T;
     fa.H = H;
+    set_extents(fa, N, bf16, ckpt_bytes(B, T, H, N, C_eff));
     cudaError_t e = use_chunked(bf16, N, C_eff) ? launch_fwd3(fa, stream) : launch_fwd2(fa, bf16, N, stream);
     if (e != cudaSuccess) {
       cudaFreeAsync(ws, stream);
@@ -420,6 +467,7 @@ int backward_impl(bool bf16, const void* const in[7], const float* s_init, const
   args.B = B;
   args.T = T;
   args.H = H;
+  set_extents(args, N, bf16, ckpt_bytes(B, T, H, N, C_eff));
   cudaError_t e = split ? launch_bwd4(args, stream) : chunked ? launch_bwd3(args, stream) : launch_bwd2(args, bf16, N, stream);
   if (ws) {
     cudaError_t e2 = cudaFreeAsync(ws, stream);
@@ -538,6 +586,9 @@ int backward_noalloc_impl(const float* const in[7], const float* s_init, float* 
   ba.B = B;
   ba.T = T;
   ba.H = H;
+  for (int v = 0; v < 7; ++v) ba.in[v] = in[v];
+  set_extents(fa, N, false, bytes);
+  set_extents(ba, N, false, bytes);
   cudaError_t e = launch_fwd2(fa, false, N, stream);
   if (e != cudaSuccess) return fail_cuda(e, "checkpointing forward launch");
   e = launch_bwd2(ba, false, N, stream);
@@ -728,6 +779,7 @@ int wkv7_status(void* stream) {
     e = cudaMemcpy(word, &zero, sizeof zero, cudaMemcpyHostToDevice);
     if (e != cudaSuccess) return fail_cuda(e, "clearing the status word");
     if (host & STATUS_TIMEOUT) return fail(WKV7_ERR_TIMEOUT, "a kernel gave up a bounded wait");
+    if (host & STATUS_BOUNDS) return fail(WKV7_ERR_BOUNDS, "a kernel skipped an access outside its buffer");
   }
   return WKV7_OK;
 }
@@ -742,6 +794,11 @@ int wkv7_debug_skip_last_load(int on) {
 
 int wkv7_debug_out_kernel(int which) {
   g_debug_out_kernel.store(which == 1 ? 1 : 0);
+  return WKV7_OK;
+}
+
+int wkv7_debug_cut_extents(size_t bytes) {
+  g_debug_extent_cut.store(bytes);
   return WKV7_OK;
 }
 #endif

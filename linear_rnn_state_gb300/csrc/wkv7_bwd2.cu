@@ -220,8 +220,9 @@ __global__ void __launch_bounds__(Bwd2Cfg<TIn, N, R, E, KS>::THREADS, 1)
   for (int i = 0; i < R; ++i)
 #pragma unroll
     for (int m = 0; m < Q; ++m) {
-      const float4 g4 = args.dS_final
-                            ? ld_f4(args.dS_final + ((size_t)head * N + row0 + i) * N + colq(m))
+      const float* src = args.dS_final + ((size_t)head * N + row0 + i) * N + colq(m);
+      const float4 g4 = args.dS_final && in_extent(args.status, args.ext.dS_final, reinterpret_cast<const float4*>(src))
+                            ? ld_f4(src)
                             : make_float4(0.f, 0.f, 0.f, 0.f);
       Gt[i][2 * m] = make_float2(g4.x, g4.y);
       Gt[i][2 * m + 1] = make_float2(g4.z, g4.w);
@@ -587,8 +588,8 @@ __global__ void __launch_bounds__(Bwd2Cfg<TIn, N, R, E, KS>::THREADS, 1)
         }
         {
           const float dvv = rowsum_scatter<G, R>(pdv, cg);
-          if (l < len && row_writer<G, R>(cg))
-            args.dv[vbase + (size_t)(start + l) * vstep + row0 + row_of_lane<G, R>(cg)] = dvv;
+          float* p = args.dv + vbase + (size_t)(start + l) * vstep + row0 + row_of_lane<G, R>(cg);
+          if (l < len && row_writer<G, R>(cg) && in_extent(args.status, args.ext.dv, p)) *p = dvv;
         }
         // da partials (S~_prev^T dsa) and the carry G~ += dsa a^ (direct: G = G w + dsa a)
         constexpr int NV2 = (E + RGN - 1) / RGN * RGN;
@@ -668,14 +669,15 @@ __global__ void __launch_bounds__(Bwd2Cfg<TIn, N, R, E, KS>::THREADS, 1)
           }
         const size_t go = vbase + (size_t)(start + l) * vstep + col;
         const float4 cw = make_float4(cp.x * il.x, cp.y * il.y, cp.z * il.z, cp.w * il.w);
-        auto put = [&](float* out, const float4& a, const float4& sc) {
-          *reinterpret_cast<float4*>(out + go) = make_float4(a.x * sc.x, a.y * sc.y, a.z * sc.z, a.w * sc.w);
+        auto put = [&](float* out, const Extent& x, const float4& a, const float4& sc) {
+          float4* p = reinterpret_cast<float4*>(out + go);
+          if (in_extent(args.status, x, p)) *p = make_float4(a.x * sc.x, a.y * sc.y, a.z * sc.z, a.w * sc.w);
         };
-        put(args.dr, acc[0], cl);
-        put(args.dk, acc[1], il);
-        put(args.db, acc[2], il);
-        put(args.dw, acc[3], cw);
-        put(args.da, acc[4], cp);
+        put(args.dr, args.ext.dr, acc[0], cl);
+        put(args.dk, args.ext.dk, acc[1], il);
+        put(args.db, args.ext.db, acc[2], il);
+        put(args.dw, args.ext.dw, acc[3], cw);
+        put(args.da, args.ext.da, acc[4], cp);
       }
     }
     if (!w_next(cur)) break;
@@ -685,9 +687,11 @@ __global__ void __launch_bounds__(Bwd2Cfg<TIn, N, R, E, KS>::THREADS, 1)
 #pragma unroll
     for (int i = 0; i < R; ++i)
 #pragma unroll
-      for (int m = 0; m < Q; ++m)
-        *reinterpret_cast<float4*>(args.dS_init + ((size_t)head * N + row0 + i) * N + colq(m)) =
-            make_float4(Gt[i][2 * m].x, Gt[i][2 * m].y, Gt[i][2 * m + 1].x, Gt[i][2 * m + 1].y);
+      for (int m = 0; m < Q; ++m) {
+        float4* p = reinterpret_cast<float4*>(args.dS_init + ((size_t)head * N + row0 + i) * N + colq(m));
+        if (in_extent(args.status, args.ext.dS_init, p))
+          *p = make_float4(Gt[i][2 * m].x, Gt[i][2 * m].y, Gt[i][2 * m + 1].x, Gt[i][2 * m + 1].y);
+      }
   }
   tmem_fence_before_sync();
   __syncthreads();

@@ -263,6 +263,8 @@ struct Outs {
   float *dr, *dw, *dk, *dv, *da, *db;
   size_t base;   // element offset of (b, t0, h, 0)
   size_t vstep;  // elements between consecutive steps
+  const BwdExtents* ext;  // the buffers' extents (checked in the debug build)
+  unsigned* status;
 };
 
 __device__ __forceinline__ float quad_sum(float x) {
@@ -377,7 +379,9 @@ __device__ void direct_chunk_bwd(Bwd3Smem& sm, const float* S0, int stage, int l
       const int q = idx / kN, col = idx % kN;
       const float x = red[q * kN + col] + red[(5 + q) * kN + col] + red[(10 + q) * kN + col] + red[(15 + q) * kN + col];
       float* dst = q == 0 ? o.dr : q == 1 ? o.dk : q == 2 ? o.db : q == 3 ? o.dw : o.da;
-      dst[o.base + (size_t)t * o.vstep + col] = x;
+      const Extent& xe = q == 0 ? o.ext->dr : q == 1 ? o.ext->dk : q == 2 ? o.ext->db : q == 3 ? o.ext->dw : o.ext->da;
+      float* p = dst + o.base + (size_t)t * o.vstep + col;
+      if (in_extent(o.status, xe, p)) *p = x;
     }
     named_bar(2, 128);
   }
@@ -411,7 +415,8 @@ __global__ void __launch_bounds__(kThreads, 1) wkv7_bwd3_kernel(const __grid_con
 #pragma unroll
     for (int q = 0; q < 8; ++q) {
       const int idx = tid + 128 * q;  // 16-byte piece: row idx / 16, column 4 * (idx % 16)
-      cp_async16(dst + (idx >> 4) * kLDS + 4 * (idx & 15), src + 4 * idx);
+      if (in_extent(args.status, args.ext.ckpt, reinterpret_cast<const float4*>(src + 4 * idx)))
+        cp_async16(dst + (idx >> 4) * kLDS + 4 * (idx & 15), src + 4 * idx);
     }
     cp_async_commit();
   };
@@ -431,8 +436,10 @@ __global__ void __launch_bounds__(kThreads, 1) wkv7_bwd3_kernel(const __grid_con
 #pragma unroll
     for (int nt = 0; nt < 8; ++nt) {
       const int col = 8 * nt + 2 * t4;
-      const float2 lo = *reinterpret_cast<const float2*>(src + (i0 + g) * kN + col);
-      const float2 hi = *reinterpret_cast<const float2*>(src + (i0 + g + 8) * kN + col);
+      const float2* p0 = reinterpret_cast<const float2*>(src + (i0 + g) * kN + col);
+      const float2* p1 = reinterpret_cast<const float2*>(src + (i0 + g + 8) * kN + col);
+      const float2 lo = in_extent(args.status, args.ext.dS_final, p0) ? *p0 : make_float2(0.f, 0.f);
+      const float2 hi = in_extent(args.status, args.ext.dS_final, p1) ? *p1 : make_float2(0.f, 0.f);
       G[nt][0] = lo.x;
       G[nt][1] = lo.y;
       G[nt][2] = hi.x;
@@ -462,7 +469,7 @@ __global__ void __launch_bounds__(kThreads, 1) wkv7_bwd3_kernel(const __grid_con
     const float* S0 = sm.S0s[n & 1];
     const bool unsafe = op.unsafe;
     const Outs o{args.dr, args.dw, args.dk, args.dv, args.da, args.db, ((size_t)bi * T + t0) * vstep + (size_t)hi * kN,
-                 vstep};
+                 vstep, &args.ext, args.status};
     // ================= P: carry chain of chunk n (state warps) || front half of chunk n-1 (prep warps)
     if (!is_prep) {
       // carry as a tf32 operand; S0 of this chunk is complete (waited before the last barrier)
@@ -554,8 +561,8 @@ __global__ void __launch_bounds__(kThreads, 1) wkv7_bwd3_kernel(const __grid_con
             const int t = 8 * q + 2 * t4 + e;
             if (t < len) {
               float* dst = args.dv + o.base + (size_t)t * vstep + i0 + g;
-              dst[0] = DV[q][e];
-              dst[8] = DV[q][2 + e];
+              if (in_extent(args.status, args.ext.dv, dst)) dst[0] = DV[q][e];
+              if (in_extent(args.status, args.ext.dv, dst + 8)) dst[8] = DV[q][2 + e];
             }
           }
 #pragma unroll
@@ -795,6 +802,8 @@ __global__ void __launch_bounds__(kThreads, 1) wkv7_bwd3_kernel(const __grid_con
       }
       float* out0 = grp ? args.dr : args.dk;
       float* out1 = grp ? args.da : args.db;
+      const Extent& x0 = grp ? args.ext.dr : args.ext.dk;
+      const Extent& x1 = grp ? args.ext.da : args.ext.db;
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
         const int t = g + 8 * h;
@@ -802,10 +811,13 @@ __global__ void __launch_bounds__(kThreads, 1) wkv7_bwd3_kernel(const __grid_con
           const size_t off = o.base + (size_t)t * vstep + j0 + 2 * t4;
 #pragma unroll
           for (int nt = 0; nt < 2; ++nt) {
-            *reinterpret_cast<float2*>(out0 + off + 8 * nt) = make_float2(P0[nt][2 * h], P0[nt][2 * h + 1]);
-            *reinterpret_cast<float2*>(out1 + off + 8 * nt) = make_float2(P1[nt][2 * h], P1[nt][2 * h + 1]);
+            float2* p0 = reinterpret_cast<float2*>(out0 + off + 8 * nt);
+            float2* p1 = reinterpret_cast<float2*>(out1 + off + 8 * nt);
+            if (in_extent(args.status, x0, p0)) *p0 = make_float2(P0[nt][2 * h], P0[nt][2 * h + 1]);
+            if (in_extent(args.status, x1, p1)) *p1 = make_float2(P1[nt][2 * h], P1[nt][2 * h + 1]);
           }
-          *reinterpret_cast<float2*>(args.dw + off + 8 * nw) = make_float2(dw[2 * h], dw[2 * h + 1]);
+          float2* pw = reinterpret_cast<float2*>(args.dw + off + 8 * nw);
+          if (in_extent(args.status, args.ext.dw, pw)) *pw = make_float2(dw[2 * h], dw[2 * h + 1]);
         }
       }
     }
@@ -835,8 +847,10 @@ __global__ void __launch_bounds__(kThreads, 1) wkv7_bwd3_kernel(const __grid_con
 #pragma unroll
     for (int nt = 0; nt < 8; ++nt) {
       const int col = 8 * nt + 2 * t4;
-      *reinterpret_cast<float2*>(dst + (i0 + g) * kN + col) = make_float2(G[nt][0], G[nt][1]);
-      *reinterpret_cast<float2*>(dst + (i0 + g + 8) * kN + col) = make_float2(G[nt][2], G[nt][3]);
+      float2* p0 = reinterpret_cast<float2*>(dst + (i0 + g) * kN + col);
+      float2* p1 = reinterpret_cast<float2*>(dst + (i0 + g + 8) * kN + col);
+      if (in_extent(args.status, args.ext.dS_init, p0)) *p0 = make_float2(G[nt][0], G[nt][1]);
+      if (in_extent(args.status, args.ext.dS_init, p1)) *p1 = make_float2(G[nt][2], G[nt][3]);
     }
   }
 }

@@ -199,21 +199,6 @@ __device__ __forceinline__ float col_sum(float x) {  // over the 8 row groups g 
   return x + __shfl_xor_sync(0xffffffffu, x, 16);
 }
 
-// 16 KB state (64 x 64 fp32, row-major) global -> shared rows of stride LD
-// by cp.async, spread over NT threads (this one is number `tid`), as one
-// commit group (empty unless `any`).
-template <int LD, int NT>
-__device__ __forceinline__ void fetch_state(float* dst, const float* src, int tid, bool any) {
-  if (any) {
-#pragma unroll
-    for (int q = 0; q < kN * kN / 4 / NT; ++q) {
-      const int idx = tid + NT * q;  // 16-byte piece: row idx / 16, column 4 * (idx % 16)
-      cp_async16(dst + (idx >> 4) * LD + 4 * (idx & 15), src + 4 * idx);
-    }
-  }
-  cp_async_commit();
-}
-
 // ================================================================ carry ===
 
 enum { C_R = 0, C_W = 1, C_A = 2, C_B = 3, C_DY = 4, C_NV = 5 };  // vectors staged for the carry (nv: epilogue)
@@ -514,11 +499,13 @@ __device__ void carry_direct(float (&G)[8][4], const __nv_bfloat16* rs, int len,
 
 // A staged 64 x 64 bf16 carry (rows of 72) to global memory, 128 threads, whole rows per
 // instruction.
-__device__ __forceinline__ void flush_carry(const bf16_t* src, bf16_t* dst, int ptid) {
+__device__ __forceinline__ void flush_carry(const bf16_t* src, bf16_t* dst, int ptid, const Extent& x,
+                                            unsigned* status) {
 #pragma unroll
   for (int q = 0; q < 4; ++q) {
     const int idx = ptid + 128 * q;  // row idx / 8, columns 8 (idx % 8) ..
-    *reinterpret_cast<uint4*>(dst + 8 * idx) = *reinterpret_cast<const uint4*>(src + (idx >> 3) * 72 + 8 * (idx & 7));
+    uint4* p = reinterpret_cast<uint4*>(dst + 8 * idx);
+    if (in_extent(status, x, p)) *p = *reinterpret_cast<const uint4*>(src + (idx >> 3) * 72 + 8 * (idx & 7));
   }
 }
 
@@ -556,11 +543,14 @@ __global__ void __launch_bounds__(kCarryThreads, 1) wkv7_bwd4_carry_kernel(const
   auto load_rstd = [&](int v) {
     const int t0 = chunk_of(v) * kL + 4 * ((tid - 128) >> 5);
 #pragma unroll
-    for (int e = 0; e < 4; ++e)
-      rs_next[e] = t0 + e < T ? args.epi_stats[2 * (((size_t)bi * T + t0 + e) * H + hi)] : 0.f;
+    for (int e = 0; e < 4; ++e) {
+      const float* p = args.epi_stats + 2 * (((size_t)bi * T + t0 + e) * H + hi);
+      rs_next[e] = t0 + e < T && in_extent(args.status, args.ext.stats, p) ? *p : 0.f;
+    }
   };
   if (kEpi && role == 1) {
-    epi_lw = *reinterpret_cast<const float2*>(args.epi_ln_w + (size_t)hi * kN + 2 * (lane));
+    const float2* p = reinterpret_cast<const float2*>(args.epi_ln_w + (size_t)hi * kN + 2 * (lane));
+    if (in_extent(args.status, args.ext.ln_w, p)) epi_lw = *p;
     load_rstd(0);
   }
   int waited = 0, issued = 0;
@@ -604,8 +594,10 @@ __global__ void __launch_bounds__(kCarryThreads, 1) wkv7_bwd4_carry_kernel(const
 #pragma unroll
     for (int nt = 0; nt < 8; ++nt) {
       const int col = 8 * nt + 2 * t4;
-      const float2 lo = *reinterpret_cast<const float2*>(src + (i0 + g) * kN + col);
-      const float2 hi = *reinterpret_cast<const float2*>(src + (i0 + g + 8) * kN + col);
+      const float2* p0 = reinterpret_cast<const float2*>(src + (i0 + g) * kN + col);
+      const float2* p1 = reinterpret_cast<const float2*>(src + (i0 + g + 8) * kN + col);
+      const float2 lo = in_extent(args.status, args.ext.dS_final, p0) ? *p0 : make_float2(0.f, 0.f);
+      const float2 hi = in_extent(args.status, args.ext.dS_final, p1) ? *p1 : make_float2(0.f, 0.f);
       G[nt][0] = lo.x;
       G[nt][1] = lo.y;
       G[nt][2] = hi.x;
@@ -645,7 +637,9 @@ __global__ void __launch_bounds__(kCarryThreads, 1) wkv7_bwd4_carry_kernel(const
       if (m + 2 < nchunks) form(m + 2);
     } else {
       if (m + 1 < nchunks) products(m + 1);
-      if (m > 0) flush_carry(sm.gst[(m - 1) & 1], carry_head + (size_t)chunk_of(m - 1) * kN * kN, tid - 256);
+      if (m > 0)
+        flush_carry(sm.gst[(m - 1) & 1], carry_head + (size_t)chunk_of(m - 1) * kN * kN, tid - 256, args.ext.carry,
+                    args.status);
     }
     // the stage of visit m is free (formed two visits ago, direct steps done); refill it
     if (__syncthreads_or(sm.abort_flag)) {
@@ -665,14 +659,16 @@ __global__ void __launch_bounds__(kCarryThreads, 1) wkv7_bwd4_carry_kernel(const
     __syncthreads();
     return;
   }
-  if (role == 2) flush_carry(sm.gst[(nchunks - 1) & 1], carry_head, tid - 256);  // chunk 0's
+  if (role == 2) flush_carry(sm.gst[(nchunks - 1) & 1], carry_head, tid - 256, args.ext.carry, args.status);  // chunk 0's
   if (role == 0 && args.dS_init) {
     float* dst = args.dS_init + (size_t)head * kN * kN;
 #pragma unroll
     for (int nt = 0; nt < 8; ++nt) {
       const int col = 8 * nt + 2 * t4;
-      *reinterpret_cast<float2*>(dst + (i0 + g) * kN + col) = make_float2(G[nt][0], G[nt][1]);
-      *reinterpret_cast<float2*>(dst + (i0 + g + 8) * kN + col) = make_float2(G[nt][2], G[nt][3]);
+      float2* p0 = reinterpret_cast<float2*>(dst + (i0 + g) * kN + col);
+      float2* p1 = reinterpret_cast<float2*>(dst + (i0 + g + 8) * kN + col);
+      if (in_extent(args.status, args.ext.dS_init, p0)) *p0 = make_float2(G[nt][0], G[nt][1]);
+      if (in_extent(args.status, args.ext.dS_init, p1)) *p1 = make_float2(G[nt][2], G[nt][3]);
     }
   }
 }
@@ -730,9 +726,9 @@ __device__ void epi_bonus_direct(const OutEpiSmem& ep, const bf16_t* rs, int len
     const int t = idx / kN, c = idx % kN;
     const size_t off = base + (size_t)t * vstep + c;
     const float db = ep.dbon[t];
-    args.dr[off] += db * bf(rs + V_K * RS + t * kB64 + c) * ep.rk[c];
-    args.dk[off] += db * bf(rs + V_R * RS + t * kB64 + c) * ep.rk[c];
-    args.dv[off] += bf(ep.dout + t * kB64 + c) * ep.stat[t][1];
+    if (in_extent(args.status, args.ext.dr, args.dr + off)) args.dr[off] += db * bf(rs + V_K * RS + t * kB64 + c) * ep.rk[c];
+    if (in_extent(args.status, args.ext.dk, args.dk + off)) args.dk[off] += db * bf(rs + V_R * RS + t * kB64 + c) * ep.rk[c];
+    if (in_extent(args.status, args.ext.dv, args.dv + off)) args.dv[off] += bf(ep.dout + t * kB64 + c) * ep.stat[t][1];
   }
 }
 
@@ -750,7 +746,8 @@ __device__ void epi_params_chunk(float* scratch, const float (&pp)[3][2], const 
     float x = 0.f;
 #pragma unroll
     for (int w8 = 0; w8 < 8; ++w8) x += scratch[w8 * 3 * kN + i];
-    args.epi_part[((size_t)head * nchunks + n) * 3 * kN + i] = x;
+    float* p = args.epi_part + ((size_t)head * nchunks + n) * 3 * kN + i;
+    if (in_extent(args.status, args.ext.part, p)) *p = x;
   }
 }
 
@@ -768,7 +765,8 @@ __device__ void out_direct(const bf16_t* rs, float* red, const float* S0, const 
   float G[8][2];
 #pragma unroll
   for (int nt = 0; nt < 8; ++nt) {
-    const float2 x = unpack_bf16(*reinterpret_cast<const uint32_t*>(Gcg + i * kN + 8 * nt + 2 * t4));
+    const uint32_t* p = reinterpret_cast<const uint32_t*>(Gcg + i * kN + 8 * nt + 2 * t4);
+    const float2 x = unpack_bf16(in_extent(args.status, args.ext.carry, p) ? *p : 0u);
     G[nt][0] = x.x;
     G[nt][1] = x.y;
   }
@@ -776,7 +774,8 @@ __device__ void out_direct(const bf16_t* rs, float* red, const float* S0, const 
     float sp[8][2];
 #pragma unroll
     for (int nt = 0; nt < 8; ++nt) {
-      const float2 x = *reinterpret_cast<const float2*>(S0 + i * kN + 8 * nt + 2 * t4);
+      const float2* p = reinterpret_cast<const float2*>(S0 + i * kN + 8 * nt + 2 * t4);
+      const float2 x = in_extent(args.status, args.ext.ckpt, p) ? *p : make_float2(0.f, 0.f);
       sp[nt][0] = x.x;
       sp[nt][1] = x.y;
     }
@@ -827,7 +826,8 @@ __device__ void out_direct(const bf16_t* rs, float* red, const float* S0, const 
     }
     dv = quad_sum(dv);
     ds = quad_sum(ds);
-    if (t4 == 0) args.dv[base + (size_t)t * vstep + i] = dv;
+    if (t4 == 0 && in_extent(args.status, args.ext.dv, args.dv + base + (size_t)t * vstep + i))
+      args.dv[base + (size_t)t * vstep + i] = dv;
     // da = S_prev^T dsa; carry G <- G diag(w) + dsa a^T
 #pragma unroll
     for (int nt = 0; nt < 8; ++nt) {
@@ -848,13 +848,15 @@ __device__ void out_direct(const bf16_t* rs, float* red, const float* S0, const 
 #pragma unroll
       for (int w8 = 0; w8 < 8; ++w8) x += red[(w8 * 5 + q) * kN + col];
       float* dst = q == 0 ? args.dr : q == 1 ? args.dk : q == 2 ? args.db : q == 3 ? args.dw : args.da;
+      const Extent& xe = q == 0 ? args.ext.dr : q == 1 ? args.ext.dk : q == 2 ? args.ext.db : q == 3 ? args.ext.dw
+                                                                                                  : args.ext.da;
       if constexpr (kLogit) {
         if (q == 3) {  // dL/dz from dL/dw
           const float z = bf(rs + V_W * RS + t * kB64 + col);
           x = logit_grad_from_wdw(x * decay_value<true>(z), z);
         }
       }
-      dst[base + (size_t)t * vstep + col] = x;
+      if (in_extent(args.status, xe, dst + base + (size_t)t * vstep + col)) dst[base + (size_t)t * vstep + col] = x;
     }
     __syncthreads();
   }
@@ -908,28 +910,35 @@ __global__ void __launch_bounds__(kThreads, 3) wkv7_bwd4_out_kernel(const __grid
     const bf16_t* src = static_cast<const bf16_t*>(v == 7 ? args.epi_nv : args.in[v]) + base +
                         (size_t)min(t, len - 1) * vstep + 8 * c;
     bf16_t* dst = !epi || v < V_DY ? sm.raw[v] : v == V_DY ? ep.dout : ep.nv;
-    cp_async16_zfill(dst + t * kB64 + 8 * c, src, t < len);
+    cp_async16_zfill(dst + t * kB64 + 8 * c, src,
+                     t < len && in_extent(args.status, args.ext.in[v], reinterpret_cast<const uint4*>(src)));
   }
   if (epi) {
     if (tid < kL) {
-      const float2 st = tid < len ? *reinterpret_cast<const float2*>(args.epi_stats + 2 * (((size_t)bi * T + t0 + tid) * H + hi))
-                                  : make_float2(0.f, 0.f);
+      const float2* p = reinterpret_cast<const float2*>(args.epi_stats + 2 * (((size_t)bi * T + t0 + tid) * H + hi));
+      const float2 st = tid < len && in_extent(args.status, args.ext.stats, p) ? *p : make_float2(0.f, 0.f);
       ep.stat[tid][0] = st.x;
       ep.stat[tid][1] = st.y;
     } else if (tid >= 64 && tid < 64 + kN) {
-      ep.lnw[tid - 64] = args.epi_ln_w[(size_t)hi * kN + tid - 64];
-      ep.rk[tid - 64] = args.epi_r_k[(size_t)hi * kN + tid - 64];
+      const float* pl = args.epi_ln_w + (size_t)hi * kN + tid - 64;
+      const float* pr = args.epi_r_k + (size_t)hi * kN + tid - 64;
+      ep.lnw[tid - 64] = in_extent(args.status, args.ext.ln_w, pl) ? *pl : 0.f;
+      ep.rk[tid - 64] = in_extent(args.status, args.ext.r_k, pr) ? *pr : 0.f;
     }
   }
 #pragma unroll
   for (int q = 0; q < kN * 8 / kThreads; ++q) {
     const int idx = tid + kThreads * q;  // row idx / 8, columns 8 (idx % 8) ..
-    cp_async16(sm.u.st.Gc + (idx >> 3) * kB64 + 8 * (idx & 7), Gcg + 8 * idx);
+    if (in_extent(args.status, args.ext.carry, reinterpret_cast<const uint4*>(Gcg + 8 * idx)))
+      cp_async16(sm.u.st.Gc + (idx >> 3) * kB64 + 8 * (idx & 7), Gcg + 8 * idx);
   }
   cp_async_commit();
   float4 s0v[4];
 #pragma unroll
-  for (int q = 0; q < 4; ++q) s0v[q] = *reinterpret_cast<const float4*>(S0g + 4 * (tid + kThreads * q));
+  for (int q = 0; q < 4; ++q) {
+    const float4* p = reinterpret_cast<const float4*>(S0g + 4 * (tid + kThreads * q));
+    s0v[q] = in_extent(args.status, args.ext.ckpt, p) ? *p : make_float4(0.f, 0.f, 0.f, 0.f);
+  }
 #pragma unroll
   for (int q = 0; q < 4; ++q) {
     const int idx = tid + kThreads * q;  // row idx / 16, columns 4 (idx % 16) ..
@@ -1114,8 +1123,8 @@ __global__ void __launch_bounds__(kThreads, 3) wkv7_bwd4_out_kernel(const __grid
             x0 = fmaf(bf(ep.dout + t * kB64 + r0 + g), ep.stat[t][1], x0);
             x1 = fmaf(bf(ep.dout + t * kB64 + r0 + g + 8), ep.stat[t][1], x1);
           }
-          dst[0] = x0;
-          dst[8] = x1;
+          if (in_extent(args.status, args.ext.dv, dst)) dst[0] = x0;
+          if (in_extent(args.status, args.ext.dv, dst + 8)) dst[8] = x1;
         }
       }
   } else if (warp >= 1) {
@@ -1295,6 +1304,8 @@ __global__ void __launch_bounds__(kThreads, 3) wkv7_bwd4_out_kernel(const __grid
   float* XA = sm.u.xch[2];
   float* out0 = grp ? args.dr : args.dk;
   float* out1 = grp ? args.da : args.db;
+  const Extent& x0 = grp ? args.ext.dr : args.ext.dk;
+  const Extent& x1 = grp ? args.ext.da : args.ext.db;
 #pragma unroll
   for (int h = 0; h < 2; ++h) {
     const int t = g + 8 * h;
@@ -1312,8 +1323,10 @@ __global__ void __launch_bounds__(kThreads, 3) wkv7_bwd4_out_kernel(const __grid
           o0.x = fmaf(db * x.x, ep.rk[col], o0.x);
           o0.y = fmaf(db * x.y, ep.rk[col + 1], o0.y);
         }
-        *reinterpret_cast<float2*>(out0 + off) = o0;
-        *reinterpret_cast<float2*>(out1 + off) = make_float2(P1[nt][2 * h], P1[nt][2 * h + 1]);
+        float2* p0 = reinterpret_cast<float2*>(out0 + off);
+        float2* p1 = reinterpret_cast<float2*>(out1 + off);
+        if (in_extent(args.status, x0, p0)) *p0 = o0;
+        if (in_extent(args.status, x1, p1)) *p1 = make_float2(P1[nt][2 * h], P1[nt][2 * h + 1]);
       }
     }
   }
@@ -1335,7 +1348,8 @@ __global__ void __launch_bounds__(kThreads, 3) wkv7_bwd4_out_kernel(const __grid
         v = logit_grad_from_wdw(run - XA[t * kLD64 + col], bf(rs + V_W * RS + t * kB64 + col));
       else
         v = (run - XA[t * kLD64 + col]) * rcp_approx(bf(rs + V_W * RS + t * kB64 + col));
-      if (t < len) args.dw[base + (size_t)t * vstep + col] = v;
+      float* pw = args.dw + base + (size_t)t * vstep + col;
+      if (t < len && in_extent(args.status, args.ext.dw, pw)) *pw = v;
       if (!upper) run -= x;  // start anchor minus the x of the steps before t
     }
   }
@@ -1513,10 +1527,13 @@ __device__ __forceinline__ void issue_loads_raw(unsigned char* sb, const BwdArgs
   for (int q = 0; q < 5; ++q) tma_load_4d(sb + OFF_RAW + 0x800 * q, &args.map[vec[q]], bar, 0, hi, n * kL, bi);
 }
 // The checkpoint S0 (fp32 [i][j]) rounded to bf16 into its swizzled tile, four float4 per thread.
-__device__ __forceinline__ void stage_checkpoint(unsigned char* sb, const float* S0g, int tid) {
+__device__ __forceinline__ void stage_checkpoint(unsigned char* sb, const float* S0g, int tid, const BwdArgs& args) {
   float4 x[4];
 #pragma unroll
-  for (int q = 0; q < 4; ++q) x[q] = *reinterpret_cast<const float4*>(S0g + 4 * (tid + kThreads * q));
+  for (int q = 0; q < 4; ++q) {
+    const float4* p = reinterpret_cast<const float4*>(S0g + 4 * (tid + kThreads * q));
+    x[q] = in_extent(args.status, args.ext.ckpt, p) ? *p : make_float4(0.f, 0.f, 0.f, 0.f);
+  }
 #pragma unroll
   for (int q = 0; q < 4; ++q) {
     const int idx = tid + kThreads * q, i = idx >> 4, c4 = idx & 15;
@@ -1555,7 +1572,7 @@ __device__ __forceinline__ int body(unsigned char* sb, uint32_t tb, const BwdArg
     issue_loads_vdg(sb, args, task, nchunks, bar_load);
     issue_loads_raw(sb, args, task, nchunks, bar_load);
   }
-  stage_checkpoint(sb, S0g, tid);
+  stage_checkpoint(sb, S0g, tid, args);
   // five product rounds per task: round r (from 0) waits on parity par ^ (r & 1)
   const uint32_t par = (uint32_t)mma_it & 1u;
   if (!cta_wait(args.status, bar_load, (uint32_t)ld_it & 1u)) return -1;
@@ -1819,7 +1836,8 @@ __device__ __forceinline__ int body(unsigned char* sb, uint32_t tb, const BwdArg
     tmem_wait_ld();
 #pragma unroll
     for (int t = 0; t < kL; ++t)
-      if (t < len) args.dv[base + (size_t)t * vstep + i] = v[t];
+      if (t < len && in_extent(args.status, args.ext.dv, args.dv + base + (size_t)t * vstep + i))
+        args.dv[base + (size_t)t * vstep + i] = v[t];
   }
   to_mma_sync();
 
@@ -1874,8 +1892,9 @@ __device__ __forceinline__ int body(unsigned char* sb, uint32_t tb, const BwdArg
         const float dk = fmaf(cl, p0[e], y0[e]) * ic, db = fmaf(cl, p1[e], y1[e]) * ic;
         XK[t * kN + j] = -kv * dk - bv * db;
         if (t < len) {
-          args.dk[base + (size_t)t * vstep + j] = dk;
-          args.db[base + (size_t)t * vstep + j] = db;
+          const size_t o = base + (size_t)t * vstep + j;
+          if (in_extent(args.status, args.ext.dk, args.dk + o)) args.dk[o] = dk;
+          if (in_extent(args.status, args.ext.db, args.db + o)) args.db[o] = db;
         }
       }
       anc[(2 + h) * kN + j] = cl * an;
@@ -1897,8 +1916,9 @@ __device__ __forceinline__ int body(unsigned char* sb, uint32_t tb, const BwdArg
         XR[t * kN + j] = fmaf(rv, dr, ad);
         XA[t * kN + j] = ad;
         if (t < len) {
-          args.dr[base + (size_t)t * vstep + j] = dr;
-          args.da[base + (size_t)t * vstep + j] = da;
+          const size_t o = base + (size_t)t * vstep + j;
+          if (in_extent(args.status, args.ext.dr, args.dr + o)) args.dr[o] = dr;
+          if (in_extent(args.status, args.ext.da, args.da + o)) args.da[o] = da;
         }
       }
       anc[h * kN + j] = an;
@@ -1934,7 +1954,8 @@ __device__ __forceinline__ int body(unsigned char* sb, uint32_t tb, const BwdArg
         v = logit_grad_from_wdw(run - XA[t * kN + col], wraw);
       else
         v = (run - XA[t * kN + col]) * rcp_approx(wraw);
-      if (t < len) args.dw[base + (size_t)t * vstep + col] = v;
+      if (t < len && in_extent(args.status, args.ext.dw, args.dw + base + (size_t)t * vstep + col))
+        args.dw[base + (size_t)t * vstep + col] = v;
       if (!upper) run -= x;
     }
   }

@@ -7,11 +7,30 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include "wkv7_launch.h"
+
 namespace wkv7 {
 
 // Bits of the device status word the kernels report through (a pointer in
 // their arguments). Host code reads and clears it in wkv7_status().
-enum : unsigned { STATUS_TIMEOUT = 1u };
+enum : unsigned { STATUS_TIMEOUT = 1u, STATUS_BOUNDS = 2u };
+
+// Check of a plain global load or store in the debug build (WKV7_DEBUG):
+// true when the n objects at p lie inside the buffer x; otherwise the status
+// word records STATUS_BOUNDS and the caller skips the access (a skipped load
+// reads as zero). Other builds return true without looking.
+template <typename T>
+__device__ __forceinline__ bool in_extent(unsigned* status, const Extent& x, const T* p, int n = 1) {
+#ifdef WKV7_DEBUG
+  const uintptr_t a = reinterpret_cast<uintptr_t>(p), lo = reinterpret_cast<uintptr_t>(x.lo);
+  if (a >= lo && a + (size_t)n * sizeof(T) <= lo + x.bytes) return true;
+  if (status) atomicOr(status, STATUS_BOUNDS);
+  return false;
+#else
+  (void)status, (void)x, (void)p, (void)n;
+  return true;
+#endif
+}
 
 // ---------------------------------------------------------------- types ---
 

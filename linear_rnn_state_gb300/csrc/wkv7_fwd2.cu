@@ -94,7 +94,8 @@ __global__ void __launch_bounds__(Fwd2Cfg<TIn, N, R, E, K>::THREADS)
 #pragma unroll
     for (int m = 0; m < Q; ++m) {
       float4 s4 = make_float4(0.f, 0.f, 0.f, 0.f);
-      if (args.s_init) s4 = ld_f4(args.s_init + ((size_t)head * N + row0 + i) * N + colq(m));
+      const float* src = args.s_init + ((size_t)head * N + row0 + i) * N + colq(m);
+      if (args.s_init && in_extent(args.status, args.ext.s_init, reinterpret_cast<const float4*>(src))) s4 = ld_f4(src);
       S[i][2 * m] = make_float2(s4.x, s4.y);
       S[i][2 * m + 1] = make_float2(s4.z, s4.w);
     }
@@ -263,10 +264,12 @@ __global__ void __launch_bounds__(Fwd2Cfg<TIn, N, R, E, K>::THREADS)
           for (int m = 0; m < Q; ++m) {
             const float4 c4 = l > 0 ? ld_f4(d_c + (l - 1) * N + colq(m)) : make_float4(1.f, 1.f, 1.f, 1.f);
 #pragma unroll
-            for (int i = 0; i < R; ++i)
-              *reinterpret_cast<float4*>(dst + (size_t)i * N + colq(m)) =
-                  make_float4(S[i][2 * m].x * c4.x, S[i][2 * m].y * c4.y, S[i][2 * m + 1].x * c4.z,
-                              S[i][2 * m + 1].y * c4.w);
+            for (int i = 0; i < R; ++i) {
+              float4* p = reinterpret_cast<float4*>(dst + (size_t)i * N + colq(m));
+              if (in_extent(args.status, args.ext.ckpt, p))
+                *p = make_float4(S[i][2 * m].x * c4.x, S[i][2 * m].y * c4.y, S[i][2 * m + 1].x * c4.z,
+                                 S[i][2 * m + 1].y * c4.w);
+            }
           }
         }
         const float bl = beta[l];
@@ -307,7 +310,10 @@ __global__ void __launch_bounds__(Fwd2Cfg<TIn, N, R, E, K>::THREADS)
         }
         if (l + 1 < K) load_step(l + 1);
         const float yv = rowsum_scatter<G, R>(Y, cg);
-        if (y && t < T && row_writer<G, R>(cg)) st1(y + vbase + (size_t)t * vstep + row0 + row_of_lane<G, R>(cg), yv);
+        if (y && t < T && row_writer<G, R>(cg)) {
+          TIn* p = y + vbase + (size_t)t * vstep + row0 + row_of_lane<G, R>(cg);
+          if (in_extent(args.status, args.ext.y, p)) st1(p, yv);
+        }
 #pragma unroll
         for (int i = 0; i < R; ++i) sa[i] = fmaf(sa[i], bl, X[i]);
       }
@@ -330,9 +336,11 @@ __global__ void __launch_bounds__(Fwd2Cfg<TIn, N, R, E, K>::THREADS)
 #pragma unroll
           for (int m = 0; m < Q; ++m)
 #pragma unroll
-            for (int i = 0; i < R; ++i)
-              *reinterpret_cast<float4*>(dst + (size_t)i * N + colq(m)) =
-                  make_float4(S[i][2 * m].x, S[i][2 * m].y, S[i][2 * m + 1].x, S[i][2 * m + 1].y);
+            for (int i = 0; i < R; ++i) {
+              float4* p = reinterpret_cast<float4*>(dst + (size_t)i * N + colq(m));
+              if (in_extent(args.status, args.ext.ckpt, p))
+                *p = make_float4(S[i][2 * m].x, S[i][2 * m].y, S[i][2 * m + 1].x, S[i][2 * m + 1].y);
+            }
         }
         float vr[R];
         ld_rows<R>(d_v + l * N + row0, vr);
@@ -373,7 +381,10 @@ __global__ void __launch_bounds__(Fwd2Cfg<TIn, N, R, E, K>::THREADS)
           }
         }
         const float yv = rowsum_scatter<G, R>(Y, cg);
-        if (y && t < T && row_writer<G, R>(cg)) st1(y + vbase + (size_t)t * vstep + row0 + row_of_lane<G, R>(cg), yv);
+        if (y && t < T && row_writer<G, R>(cg)) {
+          TIn* p = y + vbase + (size_t)t * vstep + row0 + row_of_lane<G, R>(cg);
+          if (in_extent(args.status, args.ext.y, p)) st1(p, yv);
+        }
       }
     }
   }
@@ -382,9 +393,11 @@ __global__ void __launch_bounds__(Fwd2Cfg<TIn, N, R, E, K>::THREADS)
 #pragma unroll
     for (int i = 0; i < R; ++i)
 #pragma unroll
-      for (int m = 0; m < Q; ++m)
-        *reinterpret_cast<float4*>(args.s_final + ((size_t)head * N + row0 + i) * N + colq(m)) =
-            make_float4(S[i][2 * m].x, S[i][2 * m].y, S[i][2 * m + 1].x, S[i][2 * m + 1].y);
+      for (int m = 0; m < Q; ++m) {
+        float4* p = reinterpret_cast<float4*>(args.s_final + ((size_t)head * N + row0 + i) * N + colq(m));
+        if (in_extent(args.status, args.ext.s_final, p))
+          *p = make_float4(S[i][2 * m].x, S[i][2 * m].y, S[i][2 * m + 1].x, S[i][2 * m + 1].y);
+      }
   }
 }
 

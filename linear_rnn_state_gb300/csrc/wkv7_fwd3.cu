@@ -247,30 +247,34 @@ __device__ __forceinline__ void stage_state(const StateCtx& c, float* dst) {
   }
 }
 
-// A staged 64 x 64 state to global memory (128 threads, whole rows per instruction).
-__device__ __forceinline__ void flush_state(const float* src, float* dst, int ptid) {
+// A staged 64 x 64 state to global memory (128 threads, whole rows per instruction);
+// dst lies in the buffer x (checked in the debug build).
+__device__ __forceinline__ void flush_state(const float* src, float* dst, int ptid, const Extent& x, unsigned* status) {
 #pragma unroll
   for (int q = 0; q < 8; ++q) {
     const int idx = ptid + 128 * q;  // row idx / 16, columns 4 (idx % 16) ..
-    *reinterpret_cast<float4*>(dst + 4 * idx) = *reinterpret_cast<const float4*>(src + (idx >> 4) * kLD64 + 4 * (idx & 15));
+    float4* p = reinterpret_cast<float4*>(dst + 4 * idx);
+    if (in_extent(status, x, p)) *p = *reinterpret_cast<const float4*>(src + (idx >> 4) * kLD64 + 4 * (idx & 15));
   }
 }
 
 // A chunk's staged y rows ([t][i] bf16) to global memory: 128 threads, 16 rows x 8 pieces of
 // 16 bytes, rows past the end of the sequence skipped.
-__device__ __forceinline__ void flush_y(const __nv_bfloat16* src, __nv_bfloat16* dst, size_t vstep, int len, int ptid) {
+__device__ __forceinline__ void flush_y(const __nv_bfloat16* src, __nv_bfloat16* dst, size_t vstep, int len, int ptid,
+                                        const Extent& x, unsigned* status) {
   const int row = ptid >> 3, piece = ptid & 7;
-  if (row < len)
-    *reinterpret_cast<uint4*>(dst + (size_t)row * vstep + 8 * piece) =
-        *reinterpret_cast<const uint4*>(src + row * kN + 8 * piece);
+  uint4* p = reinterpret_cast<uint4*>(dst + (size_t)row * vstep + 8 * piece);
+  if (row < len && in_extent(status, x, p)) *p = *reinterpret_cast<const uint4*>(src + row * kN + 8 * piece);
 }
 
-__device__ __forceinline__ void store_state(const StateCtx& c, float* dst) {
+__device__ __forceinline__ void store_state(const StateCtx& c, float* dst, const Extent& x, unsigned* status) {
 #pragma unroll
   for (int nt = 0; nt < 8; ++nt) {
     const int col = 8 * nt + 2 * c.t4;
-    *reinterpret_cast<float2*>(dst + (c.i0 + c.g) * kN + col) = make_float2(c.S[nt][0], c.S[nt][1]);
-    *reinterpret_cast<float2*>(dst + (c.i0 + c.g + 8) * kN + col) = make_float2(c.S[nt][2], c.S[nt][3]);
+    float2* p0 = reinterpret_cast<float2*>(dst + (c.i0 + c.g) * kN + col);
+    float2* p1 = reinterpret_cast<float2*>(dst + (c.i0 + c.g + 8) * kN + col);
+    if (in_extent(status, x, p0)) *p0 = make_float2(c.S[nt][0], c.S[nt][1]);
+    if (in_extent(status, x, p1)) *p1 = make_float2(c.S[nt][2], c.S[nt][3]);
   }
 }
 
@@ -464,11 +468,16 @@ __device__ void flush_epilogue(const Fwd3Smem& sm, const FwdArgs& args, int m, s
   }
   if (t < len) {
     const size_t off = vbase + ((size_t)m * kL + t) * vstep + i0;
-    *reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(args.y) + off) = make_uint4(po[0], po[1], po[2], po[3]);
-    if (args.nv)
-      *reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(args.nv) + off) = make_uint4(pn[0], pn[1], pn[2], pn[3]);
-    if (args.stats && (ptid & 7) == 0)
-      *reinterpret_cast<float2*>(args.stats + 2 * (off / kN)) = make_float2(rstd, bon);
+    uint4* py = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(args.y) + off);
+    if (in_extent(args.status, args.ext.y, py)) *py = make_uint4(po[0], po[1], po[2], po[3]);
+    if (args.nv) {
+      uint4* pv = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(args.nv) + off);
+      if (in_extent(args.status, args.ext.nv, pv)) *pv = make_uint4(pn[0], pn[1], pn[2], pn[3]);
+    }
+    if (args.stats && (ptid & 7) == 0) {
+      float2* ps = reinterpret_cast<float2*>(args.stats + 2 * (off / kN));
+      if (in_extent(args.status, args.ext.stats, ps)) *ps = make_float2(rstd, bon);
+    }
   }
 }
 
@@ -503,8 +512,9 @@ __global__ void __launch_bounds__(kThreads, 1) wkv7_fwd3_kernel(const __grid_con
   if (tid == 0) sm.abort_flag = 0;
   if constexpr (kEpi) {
     for (int i = tid; i < 3 * kN; i += kThreads) {
-      const float* src = i < kN ? args.ln_w : i < 2 * kN ? args.ln_b : args.r_k;
-      sm.epi[i / kN][i % kN] = src[(size_t)hi * kN + i % kN];
+      const float* src = (i < kN ? args.ln_w : i < 2 * kN ? args.ln_b : args.r_k) + (size_t)hi * kN + i % kN;
+      const Extent& x = i < kN ? args.ext.ln_w : i < 2 * kN ? args.ext.ln_b : args.ext.r_k;
+      sm.epi[i / kN][i % kN] = in_extent(args.status, x, src) ? *src : 0.f;
     }
   }
 
@@ -522,8 +532,10 @@ __global__ void __launch_bounds__(kThreads, 1) wkv7_fwd3_kernel(const __grid_con
 #pragma unroll
       for (int nt = 0; nt < 8; ++nt) {
         const int col = 8 * nt + 2 * c.t4;
-        const float2 lo = *reinterpret_cast<const float2*>(src + (c.i0 + c.g) * kN + col);
-        const float2 hi2 = *reinterpret_cast<const float2*>(src + (c.i0 + c.g + 8) * kN + col);
+        const float2* p0 = reinterpret_cast<const float2*>(src + (c.i0 + c.g) * kN + col);
+        const float2* p1 = reinterpret_cast<const float2*>(src + (c.i0 + c.g + 8) * kN + col);
+        const float2 lo = in_extent(args.status, args.ext.s_init, p0) ? *p0 : make_float2(0.f, 0.f);
+        const float2 hi2 = in_extent(args.status, args.ext.s_init, p1) ? *p1 : make_float2(0.f, 0.f);
         c.S[nt][0] = lo.x;
         c.S[nt][1] = lo.y;
         c.S[nt][2] = hi2.x;
@@ -575,11 +587,13 @@ __global__ void __launch_bounds__(kThreads, 1) wkv7_fwd3_kernel(const __grid_con
       // the checkpoint and the y rows the state warps staged in the previous round
       if (n > 0) {
         if (ck_head && ((n - 1) * kL) % args.C == 0)
-          flush_state(sm.ck[(n - 1) & 1], ck_head + (size_t)((n - 1) * kL / args.C) * kN * kN, gtid);
+          flush_state(sm.ck[(n - 1) & 1], ck_head + (size_t)((n - 1) * kL / args.C) * kN * kN, gtid, args.ext.ckpt,
+                      args.status);
         if constexpr (kEpi)
           flush_epilogue(sm, args, n - 1, vbase, vstep, chunk_len(n - 1), gtid);
         else if (y)
-          flush_y(sm.ys[(n - 1) & 1], y + vbase + (size_t)(n - 1) * kL * vstep, vstep, chunk_len(n - 1), gtid);
+          flush_y(sm.ys[(n - 1) & 1], y + vbase + (size_t)(n - 1) * kL * vstep, vstep, chunk_len(n - 1), gtid,
+                  args.ext.y, args.status);
       }
     } else {
       const Prep3& P = sm.prep[n % 3];
@@ -610,13 +624,14 @@ __global__ void __launch_bounds__(kThreads, 1) wkv7_fwd3_kernel(const __grid_con
   // the last staged checkpoint and y rows
   if (role == 2 && nchunks > 0) {
     const int n = nchunks - 1;
-    if (ck_head && (n * kL) % args.C == 0) flush_state(sm.ck[n & 1], ck_head + (size_t)(n * kL / args.C) * kN * kN, gtid);
+    if (ck_head && (n * kL) % args.C == 0)
+      flush_state(sm.ck[n & 1], ck_head + (size_t)(n * kL / args.C) * kN * kN, gtid, args.ext.ckpt, args.status);
     if constexpr (kEpi)
       flush_epilogue(sm, args, n, vbase, vstep, chunk_len(n), gtid);
     else if (y)
-      flush_y(sm.ys[n & 1], y + vbase + (size_t)n * kL * vstep, vstep, chunk_len(n), gtid);
+      flush_y(sm.ys[n & 1], y + vbase + (size_t)n * kL * vstep, vstep, chunk_len(n), gtid, args.ext.y, args.status);
   }
-  if (role == 0 && args.s_final) store_state(c, args.s_final + (size_t)head * kN * kN);
+  if (role == 0 && args.s_final) store_state(c, args.s_final + (size_t)head * kN * kN, args.ext.s_final, args.status);
 }
 
 }  // namespace

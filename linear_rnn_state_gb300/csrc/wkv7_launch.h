@@ -10,6 +10,22 @@ namespace wkv7 {
 // Records `msg` as the calling thread's last error and returns `code`.
 int api_fail(int code, const char* msg);
 
+// A buffer that a kernel reads or writes with plain (non-TMA) loads and
+// stores: its first byte and its size. The debug build (WKV7_DEBUG) checks
+// every such access against it (wkv7_common.cuh, in_extent); other builds
+// carry it unused. TMA copies are bounded by their tensor maps instead.
+struct Extent {
+  const void* lo = nullptr;
+  size_t bytes = 0;
+};
+struct FwdExtents {
+  Extent y, nv, stats, s_init, s_final, ckpt, ln_w, ln_b, r_k;
+};
+struct BwdExtents {
+  Extent in[8];  // r, w, k, v, a, b, dy (dout with the epilogue), nv
+  Extent ckpt, carry, dr, dw, dk, dv, da, db, dS_init, dS_final, stats, ln_w, r_k, part;
+};
+
 // Forward kernel arguments. The tensor maps describe r, w, k, v, a, b as
 // 4-D tensors (N, H, T, B) with a box of (N, 1, K, 1): K steps of one head.
 struct FwdArgs {
@@ -30,6 +46,7 @@ struct FwdArgs {
   int C;                // checkpoint interval (steps)
   int nck;              // ceil(T / C)
   int B, T, H;
+  FwdExtents ext;
   // Debug build only (WKV7_DEBUG): 1 makes the scalar forward issue no load
   // (and no expected-byte count) for its last chunk, so the wait for that
   // chunk runs out with nothing in flight. Ignored by every other build.
@@ -74,6 +91,7 @@ struct BwdArgs {
   int w_logit = 0;    // 1: the w tiles hold logits z and dw receives dL/dz (split backward only)
   int C, nck;
   int B, T, H;
+  BwdExtents ext;
 };
 
 // Steps per TMA box of the forward kernels' input rows.

@@ -14,7 +14,7 @@ import os
 PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(PKG, "libwkv7.so")
 
-OK, ERR_ALLOC, ERR_INVALID, ERR_CUDA, ERR_TIMEOUT = 0, -1, -2, -3, -4
+OK, ERR_ALLOC, ERR_INVALID, ERR_CUDA, ERR_TIMEOUT, ERR_BOUNDS = 0, -1, -2, -3, -4, -5
 
 # C functions declared in include/wkv7.h, with their argument counts.
 EXPORTS = {
@@ -328,5 +328,6 @@ def backward_epilogue(r, w, k, v, a, b, dout, nv, stats, ln_w, r_k, s_init=None,
 
 
 def status(stream=None) -> None:
-    """Wait for the stream and raise if a kernel reported a timeout."""
+    """Wait for the stream and raise if a kernel reported a timeout (or, in
+    the debug build, an access outside a buffer)."""
     _check(wkv7_status(_stream(stream)))

@@ -38,13 +38,13 @@ def test_exports_every_declared_function(lib):
 
 
 def test_debug_hook_only_in_the_debug_build(lib):
-    """include/wkv7_debug.h's entry point is exported by libwkv7_debug.so
-    alone; the product library does not carry it."""
+    """include/wkv7_debug.h's entry points are exported by libwkv7_debug.so
+    alone; the product library does not carry them."""
     from linear_rnn_state_gb300 import _build
 
     text = re.sub(r"/\*.*?\*/", "", open(os.path.join(ROOT, "include", "wkv7_debug.h")).read(), flags=re.S)
     names = sorted(set(re.findall(r"\b(wkv7_\w+)\s*\(", text)))
-    assert names == ["wkv7_debug_out_kernel", "wkv7_debug_skip_last_load"]
+    assert names == ["wkv7_debug_cut_extents", "wkv7_debug_out_kernel", "wkv7_debug_skip_last_load"]
     dbg = lib.load(_build.DEBUG_LIB)
     for n in names:
         assert hasattr(dbg, n)
