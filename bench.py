@@ -573,6 +573,10 @@ RWKV8_TRAFFIC = {
 }
 
 
+def _rwkv8_env(name):
+    return os.environ.get(name, "").startswith("1")
+
+
 def _rwkv8_work_per_token_head(L, E, C=16):
     """Algorithmic FLOP and bytes per token-head (fwd, bwd) of the RWKV-8
     recurrence, from its step-by-step definition: forward 3 L E multiply-adds
@@ -733,7 +737,11 @@ def run_rwkv8(args):
     achieved = b_flop * BTH / (bwd_ms * 1e-3)
     t_roof = max((f_flop + b_flop) * BTH / peak_flops, (f_bytes + b_bytes) * BTH / (peaks["hbm_gbs"] * 1e9))
     traffic = None
-    if RWKV8_TRAFFIC["sha256"] and sources_sha256(RWKV8_TRAFFIC["sources"]) == RWKV8_TRAFFIC["sha256"]:
+    split_bwd = _rwkv8_env("RWKV8_SPLIT_BACKWARD") and not _rwkv8_env("RWKV8_SEQUENTIAL")
+    bwd_kernel = ("rwkv8_bwd_chain_kernel + rwkv8_bwd_chunk_kernel (one rwkv8_backward call)" if split_bwd
+                  else RWKV8_TRAFFIC["kernel"])
+    if (not split_bwd and RWKV8_TRAFFIC["sha256"]
+            and sources_sha256(RWKV8_TRAFFIC["sources"]) == RWKV8_TRAFFIC["sha256"]):
         traffic = RWKV8_TRAFFIC["bytes_per_token_head"] * BTH
     line = {
         "metric": RWKV8_METRIC, "value": aggregate_tokens_per_s(world, B, T, ms), "unit": "tokens/s",
@@ -747,7 +755,7 @@ def run_rwkv8(args):
                          % ((3 * BTH * 64 * 4 + ckpt.numel() * 4 + 3 * BTH * 64 * 4) / 1e9)},
         "fwd_ms": fwd_ms, "bwd_ms": bwd_ms, "step_roofline_frac": t_roof / (ms * 1e-3),
         "roofline": {"bound": "alu", "achieved": achieved / 1e12, "peak": peak_flops / 1e12, "unit": "TFLOP/s",
-                     "frac": achieved / peak_flops, "traffic": traffic, "kernel": RWKV8_TRAFFIC["kernel"],
+                     "frac": achieved / peak_flops, "traffic": traffic, "kernel": bwd_kernel,
                      "note": "the backward call timed with CUDA events around it: algorithmic FLOP of the "
                              "recurrence (12 L E per token-head) against the FP32 CUDA-core peak",
                      "peak_source": f"{sms} SMs x {FP32_LANES_PER_SM} FP32 lanes x 2 x {peaks['sm_max_mhz']:.0f} MHz",
@@ -756,9 +764,11 @@ def run_rwkv8(args):
             "value": aggregate_tokens_per_s(world, B, T, e2e[0]), "unit": "tokens/s", "h2d_bytes_per_step": e2e[1],
             "d2h_bytes_per_step": e2e[2]},
         # forward: the chain and the per-chunk readout (one kernel with RWKV8_SEQUENTIAL=1); backward: its
-        # kernel, the ddecay sum over b and, for a shared value row, one dv sum per batch row
-        "gpu_launches": ((1 if os.environ.get("RWKV8_SEQUENTIAL") == "1" else 2) + 2 + (B if Hv == 1 and H > 1 else 0))
-                        * args.steps,
+        # kernel and the ddecay sum over b (RWKV8_SPLIT_BACKWARD=1: the chain, the per-chunk kernel and
+        # the sums over the chunks and over b); for a shared value row, one dv sum per batch row
+        "gpu_launches": ((1 if _rwkv8_env("RWKV8_SEQUENTIAL") else 2)
+                         + (4 if _rwkv8_env("RWKV8_SPLIT_BACKWARD") and not _rwkv8_env("RWKV8_SEQUENTIAL") else 2)
+                         + (B if Hv == 1 and H > 1 else 0)) * args.steps,
         "clocks": clocks.summary(),
     }
     if not args.no_cpu_baseline and T == RWKV8_SHAPE["T"]:

@@ -88,9 +88,15 @@ int rwkv8_forward(const float* q, const float* v, const float* decay, const floa
  *                            on `stream` and freed on it.
  *   dq [B][H][T][L], dv (v's shape), ddecay [H][L]     outputs (required).
  *   d_rho_init [B][H][L][E], d_rho_norm_init [B][H][L]  outputs, or NULL.
- * ddecay is summed over b in a fixed order (deterministic); with Hv = 1, dv is
- * summed over h in a fixed order. Both sums use a workspace taken with
- * cudaMallocAsync (WKV7_ERR_ALLOC if that fails).
+ * One CTA per (b, h) walks its chunks from the last to the first.
+ * RWKV8_SPLIT_BACKWARD=1 in the environment selects the split form instead:
+ * the carried gradients run alone first, one CTA per (b, h), storing their
+ * value after every chunk (and <rho0, dy> rows) in a workspace (about 1.3 KB
+ * per token-head), then every chunk's dq, dv and ddecay terms are made at
+ * once; the results agree to fp32 rounding. ddecay is summed over the chunks
+ * and over b in a fixed order (deterministic); with Hv = 1, dv is summed over
+ * h in a fixed order. The workspace is taken with cudaMallocAsync on `stream`
+ * (WKV7_ERR_ALLOC if that fails).
  * Returns WKV7_OK, WKV7_ERR_INVALID, WKV7_ERR_ALLOC or WKV7_ERR_CUDA.
  */
 int rwkv8_backward(const float* q, const float* v, const float* decay, const float* dy, const float* rho_init,

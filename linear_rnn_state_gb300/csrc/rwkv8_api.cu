@@ -64,11 +64,18 @@ int check_spans(const Span* ins, int nin, const Span* outs, int nout, int requir
 }
 
 // RWKV8_SEQUENTIAL=1 selects the kernels that walk each (b, h) through its
-// chunks in one CTA; by default the chains run alone and the per-chunk work
-// runs for every chunk at once.
+// chunks in one CTA; by default the forward's chain runs alone and its
+// per-chunk work runs for every chunk at once. The backward walks each (b, h)
+// through its chunks in one CTA unless RWKV8_SPLIT_BACKWARD=1 selects its
+// split form (the carried gradients alone, then every chunk at once), which
+// measured slower.
 bool sequential() {
   const char* s = std::getenv("RWKV8_SEQUENTIAL");
   return s && s[0] == '1';
+}
+bool split_backward() {
+  const char* s = std::getenv("RWKV8_SPLIT_BACKWARD");
+  return s && s[0] == '1' && !sequential();
 }
 
 // A stream-ordered workspace (WKV7_FAIL_ALLOC=1 makes the allocation fail, for tests).
@@ -183,10 +190,17 @@ int backward_impl(const float* q, const float* v, const float* decay, const floa
   }
 
   // Workspace: [checkpoints if none given][ddecay terms per (b, h)][dv terms per head if Hv = 1]
-  const size_t ck_ws = ckpt ? 0 : (ckpt_bytes(B, T, H) + 255) / 256 * 256;
-  const size_t dd_ws = ((size_t)B * H * kL * 4 + 255) / 256 * 256;
-  const size_t dv_ws = Hv == 1 && H > 1 ? (size_t)B * H * T * kE * 4 : 0;
-  const size_t ws_bytes = ck_ws + dd_ws + dv_ws;
+  // and, for the split form, [G15][R0][Gn15][<G15, rho0>][ddecay terms per chunk], per (b, h) and chunk.
+  auto pad = [](size_t x) { return (x + 255) / 256 * 256; };
+  const bool split = split_backward();
+  const size_t tasks = (size_t)B * H * nchunks(T);
+  const size_t ck_ws = ckpt ? 0 : pad(ckpt_bytes(B, T, H));
+  const size_t dd_ws = pad((size_t)B * H * kL * 4);
+  const size_t dv_ws = Hv == 1 && H > 1 ? pad((size_t)B * H * T * kE * 4) : 0;
+  const size_t g15_ws = split ? pad(tasks * kL * kE * 4) : 0;
+  const size_t r0_ws = split ? pad(tasks * kC * kL * 4) : 0;
+  const size_t vec_ws = split ? pad(tasks * kL * 4) : 0;  // each of Gn15, <G15, rho0>, ddecay terms
+  const size_t ws_bytes = ck_ws + dd_ws + dv_ws + g15_ws + r0_ws + 3 * vec_ws;
   const char* inject = std::getenv("WKV7_FAIL_ALLOC");
   if (inject && inject[0] == '1')
     return fail(WKV7_ERR_ALLOC, "workspace allocation failed (injected by WKV7_FAIL_ALLOC)");
@@ -213,10 +227,26 @@ int backward_impl(const float* q, const float* v, const float* decay, const floa
   a.ckpt = ckpt ? const_cast<float*>(ckpt) : reinterpret_cast<float*>(ws);
   a.d_rho_final = d_rho_final, a.d_rho_norm_final = d_rho_norm_final;
   a.dq = dq;
-  a.dv = dv_ws ? reinterpret_cast<float*>(ws + ck_ws + dd_ws) : dv;
-  a.ddecay_bh = reinterpret_cast<float*>(ws + ck_ws);
+  unsigned char* p = ws + ck_ws;
+  a.ddecay_bh = reinterpret_cast<float*>(p);
+  p += dd_ws;
+  a.dv = dv_ws ? reinterpret_cast<float*>(p) : dv;
+  p += dv_ws;
   a.d_rho_init = d_rho_init, a.d_rho_norm_init = d_rho_norm_init;
-  e = launch_backward(a, stream);
+  if (split) {
+    a.g15 = reinterpret_cast<float*>(p);
+    p += g15_ws;
+    a.r0 = reinterpret_cast<float*>(p);
+    p += r0_ws;
+    a.gn15 = reinterpret_cast<float*>(p);
+    a.gdot = reinterpret_cast<float*>(p + vec_ws);
+    a.ddecay_part = reinterpret_cast<float*>(p + 2 * vec_ws);
+    e = launch_backward_chain(a, stream);
+    if (e == cudaSuccess) e = launch_backward_chunks(a, stream);
+    if (e == cudaSuccess) e = launch_chunk_sum(a, stream);
+  } else {
+    e = launch_backward(a, stream);
+  }
   if (e == cudaSuccess) e = launch_group_sum(a.ddecay_bh, ddecay, (size_t)H * kL, (size_t)H * kL, B, stream);
   if (e == cudaSuccess && dv_ws) e = launch_head_sum(a.dv, dv, B, H, T, stream);
   cudaError_t e2 = cudaFreeAsync(ws, stream);

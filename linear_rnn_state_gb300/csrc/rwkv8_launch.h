@@ -22,6 +22,12 @@ struct Args {
   float* dv;        // [B][H][T][E]: dv itself (Hv = H) or per-head terms to sum (Hv = 1)
   float* ddecay_bh; // [B][H][L] per-(b, h) terms of ddecay
   float *d_rho_init, *d_rho_norm_init;         // NULL = skip
+  // Split backward's workspaces, per (b, h) and chunk c ([B*H][nchunks] ...):
+  float* g15;          // [L][E] gradient w.r.t. the state after the chunk's last step
+  float* gn15;         // [L] the same for the norm
+  float* r0;           // [kC][L] R0[tau][l] = <rho0[l], dy_tau>, rho0 the checkpointed state
+  float* gdot;         // [L] <G15[l], rho0[l]>
+  float* ddecay_part;  // [L] the chunk's terms of ddecay
   int B, T, H, Hv;
 };
 
@@ -35,7 +41,14 @@ cudaError_t launch_forward(const Args& a, cudaStream_t s);
 cudaError_t launch_state(const Args& a, cudaStream_t s);
 // y of every chunk at once from the checkpoints in a.ckpt.
 cudaError_t launch_forward_chunks(const Args& a, cudaStream_t s);
+// One CTA per (b, h) through all chunks (RWKV8_SEQUENTIAL=1).
 cudaError_t launch_backward(const Args& a, cudaStream_t s);
+// The split backward: the carried gradients alone (g15, gn15, r0, gdot for
+// every chunk, d_rho_init, d_rho_norm_init), then every chunk's dq, dv and
+// ddecay terms at once, then ddecay_bh = the chunk terms summed per (b, h).
+cudaError_t launch_backward_chain(const Args& a, cudaStream_t s);
+cudaError_t launch_backward_chunks(const Args& a, cudaStream_t s);
+cudaError_t launch_chunk_sum(const Args& a, cudaStream_t s);
 // out[i] = sum over g of in[g * stride + i], g = 0 .. groups-1, for i in [0, n).
 cudaError_t launch_group_sum(const float* in, float* out, size_t n, size_t stride, int groups, cudaStream_t s);
 // dv [B][1][T][E] = sum over h of part [B][H][T][E].

@@ -3,9 +3,11 @@ fp64 oracle (oracle/rwkv8_oracle.py), called through the C ABI.
 
 Inputs are the seeded synthetic ones of linear_rnn_state_gb300.inputs
 (generate_rwkv8), rounded to fp32; the oracle consumes exactly those values.
-Both launch forms are checked: by default the chains between chunks run alone
-and the per-chunk work for all chunks at once; RWKV8_SEQUENTIAL=1 walks each
-(b, h) through its chunks in one CTA.
+Every launch form is checked: by default the forward's chain between chunks
+runs alone and its per-chunk work for all chunks at once, and the backward
+walks each (b, h) through its chunks in one CTA; RWKV8_SEQUENTIAL=1 walks each
+(b, h) through its chunks in the forward too; RWKV8_SPLIT_BACKWARD=1 runs the
+backward's carried gradients alone and then every chunk at once.
 The bar is the fp32 one of this library, element by element:
 |gpu - ref| <= 1e-4 (1 + |ref|) for y, the final states, dq, dv and the
 initial-state gradients. ddecay is a sum over batch and time of terms of both
@@ -50,6 +52,35 @@ def _close(name, got, ref, scale=0.0):
     assert err.max() <= 1e-4, f"{name}: max scaled error {err.max():.3e}"
 
 
+def _dq_rounding_scale(o):
+    """Per element of dq, the fp32 rounding allowance of its first term, in
+    the units of _close's `scale`. dq_t = (g_qw - <g_qw, qw>) / (sum q_t + EPS)
+    + ..., g_qw[l] = R / (n_t[l] + EPS), R = sum_e rho_t[l][e] dy_t[e]: on a
+    query row of zeros the sum q_t is 0, so the signed 64-term sum R is divided
+    by EPS = 1e-6, and where R cancels to a small fraction of its terms no fp32
+    evaluation of it (in any order) holds 1e-4 of the result. The allowance is
+    the standard bound for a sum of 64 products, 64 * 2^-24 * sum_e |rho dy|,
+    carried through the two divisions; added, as for ddecay, to the bar's scale
+    (1e-4 (1 + |ref| + scale)). Away from such rows it is a few 1e-2 of the bar.
+    States from the recurrence rho <- d rho + q v^T, n <- d n + q (state before
+    each step)."""
+    q, v, dy, dec = o["q"], o["v"], o["dy"], o["decay"]
+    B, H, T, L = q.shape
+    Hv = v.shape[1]
+    out = np.zeros_like(q)
+    for b in range(B):
+        for h in range(H):
+            rho = np.zeros((L, v.shape[3])) if o["rho_init"] is None else o["rho_init"][b, h].copy()
+            n = np.zeros(L) if o["rho_norm_init"] is None else o["rho_norm_init"][b, h].copy()
+            vv = v[b, 0 if Hv == 1 else h]
+            for t in range(T):
+                terms = np.abs(rho * dy[b, h, t][None, :]).sum(axis=1)
+                out[b, h, t] = 64 * 2.0 ** -24 * terms / ((n + 1e-6) * (q[b, h, t].sum() + 1e-6)) / 1e-4
+                rho = dec[h][:, None] * rho + np.outer(q[b, h, t], vv[t])
+                n = dec[h] * n + q[b, h, t]
+    return out
+
+
 def _dev(x):
     return None if x is None else torch.from_numpy(np.ascontiguousarray(x)).cuda()
 
@@ -77,14 +108,16 @@ def _run(env, B, T, H, Hv, seed, state=False, boundary=False, use_ckpt=True):
     return g
 
 
-VARIANTS = ["chunked", "sequential"]
+VARIANTS = ["chunked", "sequential", "split_backward"]
 
 
 def _variant(monkeypatch, variant):
+    monkeypatch.delenv("RWKV8_SEQUENTIAL", raising=False)
+    monkeypatch.delenv("RWKV8_SPLIT_BACKWARD", raising=False)
     if variant == "sequential":
         monkeypatch.setenv("RWKV8_SEQUENTIAL", "1")
-    else:
-        monkeypatch.delenv("RWKV8_SEQUENTIAL", raising=False)
+    elif variant == "split_backward":
+        monkeypatch.setenv("RWKV8_SPLIT_BACKWARD", "1")
 
 
 @pytest.mark.parametrize("variant", VARIANTS)
@@ -185,7 +218,9 @@ def test_rwkv8_full_size_sampled(env):
 def test_rwkv8_degenerate_inputs(env, case, variant, monkeypatch):
     """Decay exactly 0 (only the previous step is seen) or 1 (plain prefix
     sums), query rows of zeros (their weights are 0 / EPS = 0), and a decay
-    that mixes 0, 1 and tiny values across latents."""
+    that mixes 0, 1 and tiny values across latents. dq carries the rounding
+    allowance of _dq_rounding_scale: on the rows of zeros it divides a signed
+    sum by EPS."""
     _variant(monkeypatch, variant)
     orc, inputs, rwkv8 = env
     B, T, H = 2, 40, 2
@@ -213,15 +248,16 @@ def test_rwkv8_degenerate_inputs(env, case, variant, monkeypatch):
     _close(f"y {case}", y.cpu().numpy(), y_ref)
     _close(f"rho_final {case}", rf.cpu().numpy(), rf_ref)
     _close(f"rho_norm_final {case}", nf.cpu().numpy(), nf_ref)
-    for k in ("dq", "dv", "d_rho_init", "d_rho_norm_init"):
+    _close(f"dq {case}", g["dq"].cpu().numpy(), g_ref["dq"], _dq_rounding_scale(o))
+    for k in ("dv", "d_rho_init", "d_rho_norm_init"):
         _close(f"{k} {case}", g[k].cpu().numpy(), g_ref[k])
     _close(f"ddecay {case}", g["ddecay"].cpu().numpy(), g_ref["ddecay"], float(np.abs(g_ref["ddecay"]).mean()))
 
 
 def test_rwkv8_launch_forms_agree(env, monkeypatch):
-    """The two launch forms on one input of several chunks and a ragged tail:
-    the forward's y, final states and checkpoints, and every gradient, agree
-    to fp32 rounding (the chain sums its terms in another order)."""
+    """The launch forms on one input of several chunks and a ragged tail: the
+    forward's y, final states and checkpoints, and every gradient, agree to
+    fp32 rounding (the chains sum their terms in another order)."""
     _, inputs, rwkv8 = env
     d = inputs.generate_rwkv8(2, 77, 3, 3, 64, 64, "f32", state_std=0.1, boundary=True, seed=12)
     t = {k: _dev(x) for k, x in d.items()}
@@ -233,8 +269,10 @@ def test_rwkv8_launch_forms_agree(env, monkeypatch):
                            d_rho_final=t["d_rho_final"], d_rho_norm_final=t["d_rho_norm_final"])
         torch.cuda.synchronize()
         out[variant] = dict(zip(("y", "rho_final", "rho_norm_final", "ckpt"), f), **g)
-    a, b = out["chunked"], out["sequential"]
-    for k in a:
-        ref = b[k].cpu().numpy().astype(np.float64)
-        scale = float(np.abs(ref).mean()) if k == "ddecay" else 0.0
-        _close(f"{k} chunked vs sequential", a[k].cpu().numpy(), ref, scale)
+    b = out["sequential"]
+    for variant in ("chunked", "split_backward"):
+        a = out[variant]
+        for k in a:
+            ref = b[k].cpu().numpy().astype(np.float64)
+            scale = float(np.abs(ref).mean()) if k == "ddecay" else 0.0
+            _close(f"{k} {variant} vs sequential", a[k].cpu().numpy(), ref, scale)
