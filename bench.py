@@ -511,7 +511,10 @@ def _report(args, wl, world, B, T, H, N, C, bf16, ms, fwd_ms, bwd_ms, e2e, ckpt,
                        "carry chain (the fp32 state and carry rounded to tf32 where they enter a product), bf16 "
                        "operands in the backward's per-chunk gradient products (the carry stored as bf16 between "
                        "the two backward kernels, the fp32 checkpoint rounded to bf16 there); fp32 accumulation, "
-                       "state and element-wise math" if chunked else "fp32 FMA throughout (scalar kernels)")
+                       "state and element-wise math" if chunked else
+                       ("forward on tensor cores in split tf32 (three tf32 products per fp32 product, fp32 "
+                        "accumulation; state and element-wise math fp32); backward fp32 FMA (scalar kernel)"
+                        if N == 64 else "fp32 FMA throughout (scalar kernels)"))
                       + "; inputs, dy and y stored in " + wl.storage,
         "config": {"workload": (wl.name + {"wkv7-logit": "-decay-logits", "wkv7-epilogue": "-with-epilogue"}.get(
                        args.workload, ""))

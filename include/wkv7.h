@@ -67,6 +67,13 @@ typedef uint16_t wkv7_bf16;
  *   ckpt              checkpoint buffer of wkv7_ckpt_bytes(B, T, H, N,
  *                     ckpt_every) bytes for wkv7_backward, or NULL.
  *   ckpt_every        checkpoint interval in steps (>= 1 when ckpt is set).
+ * Arithmetic. At N = 64 with checkpoints every multiple of 16 steps (or none)
+ * the chunked tensor-core form runs with every product taken in split tf32:
+ * each fp32 operand x is x_hi + x_lo (x_hi = x rounded to tf32, x_lo = x -
+ * x_hi rounded to tf32) and a b is a_lo b_hi + a_hi b_lo + a_hi b_hi, three
+ * tensor-core products with fp32 accumulation (relative error near 2^-21 per
+ * product); the state, its decay, the triangular solve and y stay fp32.
+ * Other N or checkpoint intervals run fp32 FMA throughout.
  * Returns WKV7_OK, WKV7_ERR_INVALID or WKV7_ERR_CUDA.
  */
 int wkv7_forward(const float* r, const float* w, const float* k, const float* v, const float* a,
@@ -100,6 +107,9 @@ int wkv7_forward_bf16(const wkv7_bf16* r, const wkv7_bf16* w, const wkv7_bf16* k
  *                  ckpt_every <= 0 lets the library pick the interval.
  *   dr, dw, dk, dv, da, db  [B][T][H][N] gradients (required).
  *   dS_init        [B][H][N][N] gradient of the initial state, or NULL.
+ * Arithmetic: fp32 FMA throughout (the reverse scan replays each window of
+ * steps from its checkpoint); when ckpt is NULL the library's checkpointing
+ * forward is wkv7_forward's, in split tf32 at N = 64.
  * Returns WKV7_OK, WKV7_ERR_INVALID, WKV7_ERR_ALLOC or WKV7_ERR_CUDA.
  */
 int wkv7_backward(const float* r, const float* w, const float* k, const float* v, const float* a,

@@ -304,7 +304,7 @@ int forward_impl(bool bf16, const void* const in[6], const float* s_init, void* 
   args.T = T;
   args.H = H;
   set_extents(args, N, bf16, ckpt ? ckpt_bytes(B, T, H, N, C) : 0);
-  cudaError_t e = use_chunked(bf16, N, ckpt ? C : kChunk) ? launch_fwd3(args, stream) : launch_fwd2(args, bf16, N, stream);
+  cudaError_t e = use_chunked_fwd(N, ckpt ? C : kChunk) ? launch_fwd3(args, bf16, stream) : launch_fwd2(args, bf16, N, stream);
   if (e != cudaSuccess) return fail_cuda(e, "forward launch");
   return WKV7_OK;
 }
@@ -412,7 +412,7 @@ int backward_impl(bool bf16, const void* const in[7], const float* s_init, const
     fa.T = T;
     fa.H = H;
     set_extents(fa, N, bf16, ckpt_bytes(B, T, H, N, C_eff));
-    cudaError_t e = use_chunked(bf16, N, C_eff) ? launch_fwd3(fa, stream) : launch_fwd2(fa, bf16, N, stream);
+    cudaError_t e = use_chunked_fwd(N, C_eff) ? launch_fwd3(fa, bf16, stream) : launch_fwd2(fa, bf16, N, stream);
     if (e != cudaSuccess) {
       cudaFreeAsync(ws, stream);
       return fail_cuda(e, "checkpointing forward launch");
@@ -589,7 +589,7 @@ int backward_noalloc_impl(const float* const in[7], const float* s_init, float* 
   for (int v = 0; v < 7; ++v) ba.in[v] = in[v];
   set_extents(fa, N, false, bytes);
   set_extents(ba, N, false, bytes);
-  cudaError_t e = launch_fwd2(fa, false, N, stream);
+  cudaError_t e = use_chunked_fwd(N, C) ? launch_fwd3(fa, false, stream) : launch_fwd2(fa, false, N, stream);
   if (e != cudaSuccess) return fail_cuda(e, "checkpointing forward launch");
   e = launch_bwd2(ba, false, N, stream);
   if (e != cudaSuccess) return fail_cuda(e, "backward launch");

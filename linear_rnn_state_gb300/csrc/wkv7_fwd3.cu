@@ -1,4 +1,4 @@
-// WKV7 forward scan on tensor cores (sm_103a): chunked form, bf16 inputs, N = 64.
+// WKV7 forward scan on tensor cores (sm_103a): chunked form, bf16 or fp32 inputs, N = 64.
 //
 // Same result as "rx_pretrain.c", rx_wkv7_forward_seq, per (b, h):
 //   sa = S a ;  S <- S diag(w) + v k^T + sa b^T ;  y = S r.
@@ -14,7 +14,10 @@
 //   S(L) = S0 diag(c(L)) + V^T Kb + SA^T Bb
 // (exact up to rounding; the reverse scan uses the same algebra). The
 // products run on tf32 tensor cores with fp32 accumulation; the state stays
-// fp32 in registers.
+// fp32 in registers. With bf16 inputs each product is one tf32 product (the
+// operands rounded to tf32 once); with fp32 inputs each is taken in split
+// tf32, three tf32 products (wkv7_mma.cuh, mma_x), so the result keeps fp32
+// accuracy.
 //
 // One CTA per (b, h), twelve warps in three groups working one chunk apart:
 //  - forming warps (4..7) turn chunk n+2's r, w, k, v, a, b (TMA tensor loads
@@ -24,7 +27,9 @@
 //  - state warps (0..3) each own 16 rows i of S as mma accumulator tiles
 //    and compute S0 [A^ R^]^T, SA, Y and S(L) for chunk n, and write y and
 //    the checkpoints.
-// Operand blocks rotate over three buffers.
+// Operand blocks rotate over three buffers. The input ring has four stages
+// for bf16 inputs and three for fp32 (twice the bytes); with fp32 inputs the
+// state warps store the checkpoints themselves instead of staging them.
 // A chunk whose decays leave [1/16, 16] (or hold a NaN) is run step by step
 // in the direct form by the state warps, in fp32.
 #include "wkv7_decay.cuh"
@@ -39,7 +44,7 @@ constexpr int kN = 64, kL = 16;
 constexpr int kLD64 = 72;  // row stride (floats) of 64-wide operands: conflict-free fragment loads
 constexpr int kLD16 = 24;  // row stride of 16-wide operands
 
-// Operand block of one chunk (tf32 values unless noted).
+// Operand block of one chunk (tf32 values for bf16 inputs, fp32 for fp32 inputs, unless noted).
 struct Prep3 {
   float X1[2 * kL * kLD64];  // rows 0..15: a^(t); rows 16..31: r^(t)   [t][j]
   float VT[kN * kLD16];      // v(s)[i]                                   [i][s]
@@ -53,37 +58,70 @@ struct Prep3 {
   int pad_[31];
 };
 
+// Input ring depth and checkpoint staging per input type.
+template <typename TIn>
+struct Fwd3Io;
+template <>
+struct Fwd3Io<__nv_bfloat16> {
+  static constexpr int kStages = 4;
+  static constexpr bool kStageCk = true;
+};
+template <>
+struct Fwd3Io<float> {
+  static constexpr int kStages = 3;
+  static constexpr bool kStageCk = false;
+};
+
+template <typename TIn>
 struct Fwd3Smem {
-  __nv_bfloat16 raw[4][6][kL * kN];  // TMA ring: r, w, k, v, a, b of one chunk per stage
+  static constexpr int kStages = Fwd3Io<TIn>::kStages;
+  static constexpr bool kStageCk = Fwd3Io<TIn>::kStageCk;
+  TIn raw[kStages][6][kL * kN];  // TMA ring: r, w, k, v, a, b of one chunk per stage
   Prep3 prep[3];
   float X2[2][2 * kL * kLD64];  // per chunk in flight: rows 0..15: k~(s); rows 16..31: b~(s)   [s][j]
-  __nv_bfloat16 ys[2][kL * kN];  // y of the chunk [t][i], on its way out (state warps write, products warps store)
+  TIn ys[2][kL * kN];  // y of the chunk [t][i], on its way out (state warps write, products warps store)
   // epilogue: the head's ln_w, ln_b, r_k; per chunk (ring of 4, written by the forming
   // group two rounds before the state warps run the chunk, read by the products group the
   // round after) the bonus partials of the two 32-column halves and the v rows
   float epi[3][kN];
   float epi_sp[4][2][kL];
   __nv_bfloat16 epi_v[4][kL * kN];
-  float ck[2][kN * kLD64];     // checkpoints on their way out (state warps write, products warps store)
-  uint64_t full[4];
+  // checkpoints on their way out (state warps write, products warps store); bf16 inputs only
+  float ck[kStageCk ? 2 : 1][kStageCk ? kN * kLD64 : 4];
+  uint64_t full[kStages];
   int abort_flag;
 };
 
-constexpr int kStages = 4;
 constexpr int kThreads = 384;  // warps 0-3: state; 4-7: forming; 8-11: products
 enum { V_R = 0, V_W = 1, V_K = 2, V_V = 3, V_A = 4, V_B = 5 };
 
 __device__ __forceinline__ float bf(const __nv_bfloat16* p) { return __bfloat162float(*p); }
+__device__ __forceinline__ float bf(const float* p) { return *p; }
 __device__ __forceinline__ float2 bf2(const __nv_bfloat16* p) {
   return __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(p));
+}
+__device__ __forceinline__ float2 bf2(const float* p) { return *reinterpret_cast<const float2*>(p); }
+
+template <typename TIn>
+constexpr bool kSplitOf = sizeof(TIn) == 4;  // fp32 inputs: products in split tf32
+
+// An operand value as stored for the products: rounded to tf32 once (one
+// product per multiply), or kept in fp32 (split products).
+template <bool kX3>
+__device__ __forceinline__ float op_val(float x) {
+  if constexpr (kX3)
+    return x;
+  else
+    return tf32r(x);
 }
 
 // ---------------------------------------------------------- forming group ---
 // 128 threads; thread (j = ptid % 64, half = ptid / 64) forms column j of
 // steps 8*half .. 8*half+7.
-template <bool kLogit, bool kEpi>
-__device__ void form_chunk(Fwd3Smem& sm, Prep3& P, float* X2, int stage, int len, int ptid, int eslot) {
-  const __nv_bfloat16* rs = sm.raw[stage][0];
+template <typename TIn, bool kLogit, bool kEpi>
+__device__ void form_chunk(Fwd3Smem<TIn>& sm, Prep3& P, float* X2, int stage, int len, int ptid, int eslot) {
+  constexpr bool kX3 = kSplitOf<TIn>;
+  const TIn* rs = sm.raw[stage][0];
   const int j = ptid & 63, half = ptid >> 6;
   // decays of this thread's 8 steps (wm) and of the other 8 (wo); padding
   // steps past the end of the sequence decay by 1
@@ -102,7 +140,7 @@ __device__ void form_chunk(Fwd3Smem& sm, Prep3& P, float* X2, int stage, int len
     rv[e] = bf(rs + V_R * kL * kN + o);
     kv[e] = bf(rs + V_K * kL * kN + o);
     bv[e] = bf(rs + V_B * kL * kN + o);
-    vt[e] = bf(rs + V_V * kL * kN + o);  // bf16 values are tf32 values
+    vt[e] = bf(rs + V_V * kL * kN + o);  // bf16 values are tf32 values; fp32 values stay fp32
   }
   if constexpr (kEpi) {
     // the epilogue's bonus sum_j r_j k_j r_k[j] of each step, over this warp's 32 columns,
@@ -155,13 +193,13 @@ __device__ void form_chunk(Fwd3Smem& sm, Prep3& P, float* X2, int stage, int len
     const float ic = rcp_approx(c);
     const int o = t * kN + j;
     const float a = av[e], r = rv[e], k = kv[e], b = bv[e];
-    X2[t * kLD64 + j] = tf32r(k * ic);
-    X2[(kL + t) * kLD64 + j] = tf32r(b * ic);
-    P.X1[t * kLD64 + j] = tf32r(a * cprev);
-    P.X1[(kL + t) * kLD64 + j] = tf32r(r * c);
+    X2[t * kLD64 + j] = op_val<kX3>(k * ic);
+    X2[(kL + t) * kLD64 + j] = op_val<kX3>(b * ic);
+    P.X1[t * kLD64 + j] = op_val<kX3>(a * cprev);
+    P.X1[(kL + t) * kLD64 + j] = op_val<kX3>(r * c);
     const float s = cL * ic;
-    kbt[e] = tf32r(k * s);
-    bbt[e] = tf32r(b * s);
+    kbt[e] = op_val<kX3>(k * s);
+    bbt[e] = op_val<kX3>(b * s);
   }
 #pragma unroll
   for (int q = 0; q < 2; ++q) {
@@ -177,6 +215,7 @@ __device__ void form_chunk(Fwd3Smem& sm, Prep3& P, float* X2, int stage, int len
 // --------------------------------------------------------- products group ---
 // The four L x L products and T of a formed chunk (128 threads; skipped by the
 // caller for a chunk in the direct form).
+template <bool kX3>
 __device__ void gram_chunk(Prep3& P, const float* X2, int gtid) {
   const int pw = gtid >> 5, lane = gtid & 31, g = lane >> 2, t4 = lane & 3;
   // Gram blocks: warp pw computes [A^ | R^](rows 16*(pw/2)) x [K~ | B~](rows 16*(pw%2))^T.
@@ -187,13 +226,13 @@ __device__ void gram_chunk(Prep3& P, const float* X2, int gtid) {
     zero4(acc[1]);
 #pragma unroll
     for (int kb = 0; kb < kN / 8; ++kb) {
-      uint32_t a[4];
-      frag_a(a, P.X1, kLD64, 16 * mt, 8 * kb, g, t4);
+      FragA<kX3> a;
+      ld_a(a, P.X1, kLD64, 16 * mt, 8 * kb, g, t4);
 #pragma unroll
       for (int nt = 0; nt < 2; ++nt) {
-        uint32_t b0, b1;
-        frag_b(b0, b1, X2, kLD64, 16 * nb + 8 * nt, 8 * kb, g, t4);
-        mma_tf32(acc[nt], a, b0, b1);
+        FragB<kX3> b;
+        ld_b(b, X2, kLD64, 16 * nb + 8 * nt, 8 * kb, g, t4);
+        mma_x(acc[nt], a, b);
       }
     }
     const bool strict = mt == 0;  // Mka, Mba: s < t; Mkr, Mbr: s <= t
@@ -205,7 +244,7 @@ __device__ void gram_chunk(Prep3& P, const float* X2, int gtid) {
         const int t = g + 8 * h, s = 8 * nt + 2 * t4;
         const float x0 = (s < t || (!strict && s == t)) ? acc[nt][2 * h] : 0.f;
         const float x1 = (s + 1 < t || (!strict && s + 1 == t)) ? acc[nt][2 * h + 1] : 0.f;
-        *reinterpret_cast<float2*>(M + t * kLD16 + s) = make_float2(tf32r(x0), tf32r(x1));
+        *reinterpret_cast<float2*>(M + t * kLD16 + s) = make_float2(op_val<kX3>(x0), op_val<kX3>(x1));
       }
   }
   // T = (I - Mba)^-1 by forward substitution; warp 1 made Mba, so a warp
@@ -224,7 +263,7 @@ __device__ void gram_chunk(Prep3& P, const float* X2, int gtid) {
     }
     if (lane < 16) {
 #pragma unroll
-      for (int t = 0; t < kL; ++t) P.Tinv[t * kLD16 + s] = tf32r(col[t]);
+      for (int t = 0; t < kL; ++t) P.Tinv[t * kLD16 + s] = op_val<kX3>(col[t]);
     }
   }
 }
@@ -267,6 +306,17 @@ __device__ __forceinline__ void flush_y(const __nv_bfloat16* src, __nv_bfloat16*
   if (row < len && in_extent(status, x, p)) *p = *reinterpret_cast<const uint4*>(src + row * kN + 8 * piece);
 }
 
+// The same for fp32 rows: 16 rows x 8 pieces of 32 bytes.
+__device__ __forceinline__ void flush_y(const float* src, float* dst, size_t vstep, int len, int ptid, const Extent& x,
+                                        unsigned* status) {
+  const int row = ptid >> 3, piece = ptid & 7;
+  uint4* p = reinterpret_cast<uint4*>(dst + (size_t)row * vstep + 8 * piece);
+  if (row < len && in_extent(status, x, p, 2)) {
+    p[0] = *reinterpret_cast<const uint4*>(src + row * kN + 8 * piece);
+    p[1] = *reinterpret_cast<const uint4*>(src + row * kN + 8 * piece + 4);
+  }
+}
+
 __device__ __forceinline__ void store_state(const StateCtx& c, float* dst, const Extent& x, unsigned* status) {
 #pragma unroll
   for (int nt = 0; nt < 8; ++nt) {
@@ -279,7 +329,9 @@ __device__ __forceinline__ void store_state(const StateCtx& c, float* dst, const
 }
 
 // Chunk on tensor cores. Writes the chunk's y into ys.
-__device__ void state_chunk(StateCtx& c, Fwd3Smem& sm, const Prep3& P) {
+template <typename TIn>
+__device__ void state_chunk(StateCtx& c, Fwd3Smem<TIn>& sm, const Prep3& P) {
+  constexpr bool kX3 = kSplitOf<TIn>;
   const int g = c.g, t4 = c.t4, i0 = c.i0;
   // PA = S0 A^^T (later + V^T Mka^T), PR = S0 R^^T (later + ...): [i][t]
   float PA[2][4], PR[2][4];
@@ -290,29 +342,29 @@ __device__ void state_chunk(StateCtx& c, Fwd3Smem& sm, const Prep3& P) {
   }
 #pragma unroll
   for (int kb = 0; kb < 8; ++kb) {
-    uint32_t a[4];
-    c2a(a, c.S[kb]);
+    FragA<kX3> a;
+    acc_to_a(a, c.S[kb]);
 #pragma unroll
     for (int q = 0; q < 2; ++q) {
-      uint32_t b0, b1;
-      frag_b(b0, b1, P.X1, kLD64, 8 * q, 8 * kb, g, t4);
-      mma_tf32(PA[q], a, b0, b1);
-      frag_b(b0, b1, P.X1, kLD64, kL + 8 * q, 8 * kb, g, t4);
-      mma_tf32(PR[q], a, b0, b1);
+      FragB<kX3> b;
+      ld_b(b, P.X1, kLD64, 8 * q, 8 * kb, g, t4);
+      mma_x(PA[q], a, b);
+      ld_b(b, P.X1, kLD64, kL + 8 * q, 8 * kb, g, t4);
+      mma_x(PR[q], a, b);
     }
   }
-  uint32_t av[2][4];  // V^T rows i0.., k = s
-  frag_a(av[0], P.VT, kLD16, i0, 0, g, t4);
-  frag_a(av[1], P.VT, kLD16, i0, 8, g, t4);
+  FragA<kX3> av[2];  // V^T rows i0.., k = s
+  ld_a(av[0], P.VT, kLD16, i0, 0, g, t4);
+  ld_a(av[1], P.VT, kLD16, i0, 8, g, t4);
 #pragma unroll
   for (int kb = 0; kb < 2; ++kb)
 #pragma unroll
     for (int q = 0; q < 2; ++q) {
-      uint32_t b0, b1;
-      frag_b(b0, b1, P.M[0], kLD16, 8 * q, 8 * kb, g, t4);  // Mka
-      mma_tf32(PA[q], av[kb], b0, b1);
-      frag_b(b0, b1, P.M[2], kLD16, 8 * q, 8 * kb, g, t4);  // Mkr
-      mma_tf32(PR[q], av[kb], b0, b1);
+      FragB<kX3> b;
+      ld_b(b, P.M[0], kLD16, 8 * q, 8 * kb, g, t4);  // Mka
+      mma_x(PA[q], av[kb], b);
+      ld_b(b, P.M[2], kLD16, 8 * q, 8 * kb, g, t4);  // Mkr
+      mma_x(PR[q], av[kb], b);
     }
   // SA^T = PA T^T  [i][t]
   float SA[2][4];
@@ -320,34 +372,34 @@ __device__ void state_chunk(StateCtx& c, Fwd3Smem& sm, const Prep3& P) {
   zero4(SA[1]);
 #pragma unroll
   for (int kb = 0; kb < 2; ++kb) {
-    uint32_t a[4];
-    c2a(a, PA[kb]);
+    FragA<kX3> a;
+    acc_to_a(a, PA[kb]);
 #pragma unroll
     for (int q = 0; q < 2; ++q) {
-      uint32_t b0, b1;
-      frag_b(b0, b1, P.Tinv, kLD16, 8 * q, 8 * kb, g, t4);
-      mma_tf32(SA[q], a, b0, b1);
+      FragB<kX3> b;
+      ld_b(b, P.Tinv, kLD16, 8 * q, 8 * kb, g, t4);
+      mma_x(SA[q], a, b);
     }
   }
-  uint32_t asa[2][4];
-  c2a(asa[0], SA[0]);
-  c2a(asa[1], SA[1]);
+  FragA<kX3> asa[2];
+  acc_to_a(asa[0], SA[0]);
+  acc_to_a(asa[1], SA[1]);
   // Y^T = PR + SA^T Mbr^T
 #pragma unroll
   for (int kb = 0; kb < 2; ++kb)
 #pragma unroll
     for (int q = 0; q < 2; ++q) {
-      uint32_t b0, b1;
-      frag_b(b0, b1, P.M[3], kLD16, 8 * q, 8 * kb, g, t4);
-      mma_tf32(PR[q], asa[kb], b0, b1);
+      FragB<kX3> b;
+      ld_b(b, P.M[3], kLD16, 8 * q, 8 * kb, g, t4);
+      mma_x(PR[q], asa[kb], b);
     }
 #pragma unroll
   for (int q = 0; q < 2; ++q)
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
       const int i = i0 + g + 8 * h, t = 8 * q + 2 * t4;
-      sm.ys[c.yb][t * kN + i] = __float2bfloat16_rn(PR[q][2 * h]);
-      sm.ys[c.yb][(t + 1) * kN + i] = __float2bfloat16_rn(PR[q][2 * h + 1]);
+      st1(&sm.ys[c.yb][t * kN + i], PR[q][2 * h]);
+      st1(&sm.ys[c.yb][(t + 1) * kN + i], PR[q][2 * h + 1]);
     }
   // S(L) = S0 diag(c(L)) + V^T Kb + SA^T Bb
 #pragma unroll
@@ -362,21 +414,21 @@ __device__ void state_chunk(StateCtx& c, Fwd3Smem& sm, const Prep3& P) {
   for (int kb = 0; kb < 2; ++kb)
 #pragma unroll
     for (int nt = 0; nt < 8; ++nt) {
-      uint32_t b0, b1;
-      frag_b(b0, b1, P.KbT, kLD16, 8 * nt, 8 * kb, g, t4);
-      mma_tf32(c.S[nt], av[kb], b0, b1);
-      frag_b(b0, b1, P.BbT, kLD16, 8 * nt, 8 * kb, g, t4);
-      mma_tf32(c.S[nt], asa[kb], b0, b1);
+      FragB<kX3> b;
+      ld_b(b, P.KbT, kLD16, 8 * nt, 8 * kb, g, t4);
+      mma_x(c.S[nt], av[kb], b);
+      ld_b(b, P.BbT, kLD16, 8 * nt, 8 * kb, g, t4);
+      mma_x(c.S[nt], asa[kb], b);
     }
 }
 
 // Chunk in the direct form (any decay), fp32 on the CUDA cores.
-template <bool kLogit>
-__device__ void state_chunk_direct(StateCtx& c, Fwd3Smem& sm, int stage, int len) {
+template <typename TIn, bool kLogit>
+__device__ void state_chunk_direct(StateCtx& c, Fwd3Smem<TIn>& sm, int stage, int len) {
   const int g = c.g, t4 = c.t4, i0 = c.i0;
-  const __nv_bfloat16* rs = sm.raw[stage][0];
+  const TIn* rs = sm.raw[stage][0];
   for (int t = 0; t < len; ++t) {
-    const __nv_bfloat16* row = rs + t * kN;
+    const TIn* row = rs + t * kN;
     float s0 = 0.f, s1 = 0.f;
 #pragma unroll
     for (int nt = 0; nt < 8; ++nt) {
@@ -407,8 +459,8 @@ __device__ void state_chunk_direct(StateCtx& c, Fwd3Smem& sm, int stage, int len
     y1 += __shfl_xor_sync(0xffffffffu, y1, 1);
     y1 += __shfl_xor_sync(0xffffffffu, y1, 2);
     if (t4 == 0) {
-      sm.ys[c.yb][t * kN + i0 + g] = __float2bfloat16_rn(y0);
-      sm.ys[c.yb][t * kN + i0 + g + 8] = __float2bfloat16_rn(y1);
+      st1(&sm.ys[c.yb][t * kN + i0 + g], y0);
+      st1(&sm.ys[c.yb][t * kN + i0 + g + 8], y1);
     }
   }
 }
@@ -420,8 +472,8 @@ __device__ void state_chunk_direct(StateCtx& c, Fwd3Smem& sm, int stage, int len
 // plus (y - mean) rstd to args.nv and (rstd, bonus) to args.stats when given.
 // The products group, eight threads per row (eight channels each); the bonus
 // partials and v rows were staged by the forming group.
-__device__ void flush_epilogue(const Fwd3Smem& sm, const FwdArgs& args, int m, size_t vbase, size_t vstep, int len,
-                               int ptid) {
+__device__ void flush_epilogue(const Fwd3Smem<__nv_bfloat16>& sm, const FwdArgs& args, int m, size_t vbase, size_t vstep,
+                               int len, int ptid) {
   const int t = ptid >> 3, i0 = 8 * (ptid & 7), es = m % 4;
   auto load8 = [](const __nv_bfloat16* p, float (&x)[8]) {
     const uint4 u = *reinterpret_cast<const uint4*>(p);
@@ -481,17 +533,20 @@ __device__ void flush_epilogue(const Fwd3Smem& sm, const FwdArgs& args, int m, s
   }
 }
 
-template <bool kLogit, bool kEpi>
+template <typename TIn, bool kLogit, bool kEpi>
 __global__ void __launch_bounds__(kThreads, 1) wkv7_fwd3_kernel(const __grid_constant__ FwdArgs args) {
   extern __shared__ __align__(128) unsigned char smem_raw[];
-  Fwd3Smem& sm = *reinterpret_cast<Fwd3Smem*>(smem_raw);
+  using Smem = Fwd3Smem<TIn>;
+  constexpr int kStages = Smem::kStages;
+  constexpr bool kStageCk = Smem::kStageCk;
+  Smem& sm = *reinterpret_cast<Smem*>(smem_raw);
   const int T = args.T, H = args.H;
   const int head = blockIdx.x, bi = head / H, hi = head % H;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int role = warp < 4 ? 0 : warp < 8 ? 1 : 2;  // state, forming, products
   const int ftid = tid - 128, gtid = tid - 256;
   const int nchunks = (T + kL - 1) / kL;
-  constexpr int kStageBytes = 6 * kL * kN * 2;
+  constexpr int kStageBytes = 6 * kL * kN * (int)sizeof(TIn);
 
   // Chunk n: the state warps run it in round n, the products group makes its
   // L x L products and T in round n-1, the forming group forms it in round
@@ -558,12 +613,12 @@ __global__ void __launch_bounds__(kThreads, 1) wkv7_fwd3_kernel(const __grid_con
       return;
     }
     waited = chunk + 1;
-    form_chunk<kLogit, kEpi>(sm, sm.prep[chunk % 3], sm.X2[chunk & 1], chunk % kStages, chunk_len(chunk), ftid,
-                             chunk % 4);
+    form_chunk<TIn, kLogit, kEpi>(sm, sm.prep[chunk % 3], sm.X2[chunk & 1], chunk % kStages, chunk_len(chunk), ftid,
+                                  chunk % 4);
   };
   auto grams = [&](int chunk) {
     Prep3& P = sm.prep[chunk % 3];
-    if (!P.unsafe) gram_chunk(P, sm.X2[chunk & 1], gtid);
+    if (!P.unsafe) gram_chunk<kSplitOf<TIn>>(P, sm.X2[chunk & 1], gtid);
   };
 
   // pipeline fill: form chunks 0 and 1, products of chunk 0
@@ -574,7 +629,7 @@ __global__ void __launch_bounds__(kThreads, 1) wkv7_fwd3_kernel(const __grid_con
     if (role == 2) grams(0);
     aborted = __syncthreads_or(sm.abort_flag) != 0;
   }
-  __nv_bfloat16* y = static_cast<__nv_bfloat16*>(args.y);
+  TIn* y = static_cast<TIn*>(args.y);
   const size_t vstep = (size_t)H * kN;
   const size_t vbase = ((size_t)bi * T * H + hi) * kN;
   float* ck_head = args.ckpt ? args.ckpt + (size_t)head * args.nck * kN * kN : nullptr;
@@ -586,7 +641,7 @@ __global__ void __launch_bounds__(kThreads, 1) wkv7_fwd3_kernel(const __grid_con
       if (n + 1 < nchunks) grams(n + 1);
       // the checkpoint and the y rows the state warps staged in the previous round
       if (n > 0) {
-        if (ck_head && ((n - 1) * kL) % args.C == 0)
+        if (kStageCk && ck_head && ((n - 1) * kL) % args.C == 0)
           flush_state(sm.ck[(n - 1) & 1], ck_head + (size_t)((n - 1) * kL / args.C) * kN * kN, gtid, args.ext.ckpt,
                       args.status);
         if constexpr (kEpi)
@@ -598,12 +653,17 @@ __global__ void __launch_bounds__(kThreads, 1) wkv7_fwd3_kernel(const __grid_con
     } else {
       const Prep3& P = sm.prep[n % 3];
       const int t0 = n * kL, len = chunk_len(n);
-      if (ck_head && t0 % args.C == 0) stage_state(c, sm.ck[n & 1]);
+      if (ck_head && t0 % args.C == 0) {
+        if constexpr (kStageCk)
+          stage_state(c, sm.ck[n & 1]);
+        else
+          store_state(c, ck_head + (size_t)(t0 / args.C) * kN * kN, args.ext.ckpt, args.status);
+      }
       c.yb = n & 1;
       if (P.unsafe)
-        state_chunk_direct<kLogit>(c, sm, n % kStages, len);
+        state_chunk_direct<TIn, kLogit>(c, sm, n % kStages, len);
       else
-        state_chunk(c, sm, P);
+        state_chunk<TIn>(c, sm, P);
     }
     // the stage of chunk n is free (formed two rounds ago, direct steps done); refill it
     aborted = __syncthreads_or(sm.abort_flag) != 0;
@@ -624,7 +684,7 @@ __global__ void __launch_bounds__(kThreads, 1) wkv7_fwd3_kernel(const __grid_con
   // the last staged checkpoint and y rows
   if (role == 2 && nchunks > 0) {
     const int n = nchunks - 1;
-    if (ck_head && (n * kL) % args.C == 0)
+    if (kStageCk && ck_head && (n * kL) % args.C == 0)
       flush_state(sm.ck[n & 1], ck_head + (size_t)(n * kL / args.C) * kN * kN, gtid, args.ext.ckpt, args.status);
     if constexpr (kEpi)
       flush_epilogue(sm, args, n, vbase, vstep, chunk_len(n), gtid);
@@ -636,20 +696,28 @@ __global__ void __launch_bounds__(kThreads, 1) wkv7_fwd3_kernel(const __grid_con
 
 }  // namespace
 
-template <bool kLogit, bool kEpi>
+template <typename TIn, bool kLogit, bool kEpi>
 cudaError_t launch_fwd3_impl(const FwdArgs& args, cudaStream_t stream) {
-  const size_t smem = sizeof(Fwd3Smem);
-  cudaError_t e =
-      cudaFuncSetAttribute(wkv7_fwd3_kernel<kLogit, kEpi>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  const size_t smem = sizeof(Fwd3Smem<TIn>);
+  static_assert(sizeof(Fwd3Smem<TIn>) <= 227 * 1024, "shared memory over budget");
+  cudaError_t e = cudaFuncSetAttribute(wkv7_fwd3_kernel<TIn, kLogit, kEpi>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       (int)smem);
   if (e != cudaSuccess) return e;
-  wkv7_fwd3_kernel<kLogit, kEpi><<<(unsigned)(args.B * args.H), kThreads, smem, stream>>>(args);
+  wkv7_fwd3_kernel<TIn, kLogit, kEpi><<<(unsigned)(args.B * args.H), kThreads, smem, stream>>>(args);
   return cudaGetLastError();
 }
 
-cudaError_t launch_fwd3(const FwdArgs& args, cudaStream_t stream) {
+cudaError_t launch_fwd3(const FwdArgs& args, bool bf16, cudaStream_t stream) {
+  using bf16_t = __nv_bfloat16;
+  if (!bf16) {  // the decay as w, no epilogue (the API allows nothing else for fp32 inputs)
+    if (args.w_logit || args.epilogue) return cudaErrorInvalidValue;
+    return launch_fwd3_impl<float, false, false>(args, stream);
+  }
   if (args.epilogue)
-    return args.w_logit ? launch_fwd3_impl<true, true>(args, stream) : launch_fwd3_impl<false, true>(args, stream);
-  return args.w_logit ? launch_fwd3_impl<true, false>(args, stream) : launch_fwd3_impl<false, false>(args, stream);
+    return args.w_logit ? launch_fwd3_impl<bf16_t, true, true>(args, stream)
+                        : launch_fwd3_impl<bf16_t, false, true>(args, stream);
+  return args.w_logit ? launch_fwd3_impl<bf16_t, true, false>(args, stream)
+                      : launch_fwd3_impl<bf16_t, false, false>(args, stream);
 }
 
 }  // namespace wkv7

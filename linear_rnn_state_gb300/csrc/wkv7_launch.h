@@ -98,9 +98,10 @@ struct BwdArgs {
 int fwd_steps_per_stage(int N, bool bf16);
 
 cudaError_t launch_fwd2(const FwdArgs& args, bool bf16, int N, cudaStream_t stream);
-// Chunked tensor-core forward: bf16 inputs, N = 64, checkpoints (if any) at a
-// multiple of its 16-step chunk.
-cudaError_t launch_fwd3(const FwdArgs& args, cudaStream_t stream);
+// Chunked tensor-core forward: N = 64, checkpoints (if any) at a multiple of
+// its 16-step chunk; bf16 inputs (one tf32 product per product) or fp32
+// inputs (split tf32, three; the decay as w and no epilogue).
+cudaError_t launch_fwd3(const FwdArgs& args, bool bf16, cudaStream_t stream);
 // Chunked tensor-core backward: bf16 inputs, N = 64, checkpoints every 16 steps.
 cudaError_t launch_bwd3(const BwdArgs& args, cudaStream_t stream);
 // The same backward as a carry-chain kernel plus a parallel per-chunk output
@@ -112,6 +113,8 @@ cudaError_t launch_epi_params(const float* part, float* dln_w, float* dln_b, flo
                               cudaStream_t stream);
 constexpr int kChunk = 16;
 inline bool use_chunked(bool bf16, int N, int C) { return bf16 && N == 64 && C % kChunk == 0; }
+// The forward takes the chunked kernel for either input type.
+inline bool use_chunked_fwd(int N, int C) { return N == 64 && C % kChunk == 0; }
 cudaError_t launch_bwd2(const BwdArgs& args, bool bf16, int N, cudaStream_t stream);
 int bwd2_steps_per_window(int N, bool bf16);
 
