@@ -25,9 +25,10 @@ BUILD_DIR = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libwkv7.so")
 DEBUG_LIB = os.path.join(PKG, "libwkv7_debug.so")
 DEBUG_SOURCES = ["wkv7_api.cu", "wkv7_fwd2.cu", "wkv7_fwd3.cu", "wkv7_bwd2.cu", "wkv7_bwd3.cu",
-                 "wkv7_bwd4.cu"]  # recompiled with -DWKV7_DEBUG for the debug build
+                 "wkv7_bwd4.cu", "wkv7_bwd4_f32.cu"]  # recompiled with -DWKV7_DEBUG for the debug build
 
-SOURCES = ["wkv7_api.cu", "wkv7_fwd2.cu", "wkv7_fwd3.cu", "wkv7_bwd2.cu", "wkv7_bwd3.cu", "wkv7_bwd4.cu", "rwkv8_api.cu",
+SOURCES = ["wkv7_api.cu", "wkv7_fwd2.cu", "wkv7_fwd3.cu", "wkv7_bwd2.cu", "wkv7_bwd3.cu", "wkv7_bwd4.cu",
+           "wkv7_bwd4_f32.cu", "rwkv8_api.cu",
            "rwkv8_fwd.cu", "rwkv8_bwd.cu", "rwkv8_bwd_split.cu", "rwkv8_state.cu", "rwkv8_chunk.cu", "wkv7_epilogue.cu"]
 HEADERS = ["wkv7_common.cuh", "wkv7_launch.h", "wkv7_mma.cuh", "wkv7_scaled.cuh", "wkv7_tmem.cuh", "wkv7_decay.cuh",
            "rwkv8_launch.h", "rwkv8_split.cuh"]

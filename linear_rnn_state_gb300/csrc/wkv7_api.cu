@@ -216,7 +216,7 @@ void set_extents(BwdArgs& a, int N, bool bf16, size_t ck_bytes) {
   for (int v = 0; v < 7; ++v) a.ext.in[v] = extent(a.in[v], vec * (bf16 ? 2 : 4));
   a.ext.in[7] = extent(a.epi_nv, vec * 2);
   a.ext.ckpt = extent(a.ckpt, ck_bytes);
-  a.ext.carry = extent(a.carry, a.carry ? bwd4_workspace_bytes(a.B, a.T, a.H) : 0);
+  a.ext.carry = extent(a.carry, a.carry ? bwd4_workspace_bytes(a.B, a.T, a.H, bf16) : 0);
   float* const g[6] = {a.dr, a.dw, a.dk, a.dv, a.da, a.db};
   Extent* const x[6] = {&a.ext.dr, &a.ext.dw, &a.ext.dk, &a.ext.dv, &a.ext.da, &a.ext.db};
   for (int q = 0; q < 6; ++q) *x[q] = extent(g[q], vec * 4);
@@ -364,11 +364,14 @@ int backward_impl(bool bf16, const void* const in[7], const float* s_init, const
   // bf16 inputs at N = 64 with 16-step checkpoints take a chunked tensor-core
   // backward: the split one (carry chain + parallel output pass), which keeps
   // the carry of every chunk in the workspace too, or, when the caller asks
-  // for it (wkv7_backward_fused_bf16), the fused one (one CTA per head).
+  // for it (wkv7_backward_fused_bf16), the fused one (one CTA per head). fp32
+  // inputs there take the split one in split tf32 (fp32 carries in the
+  // workspace).
   const bool chunked = bf16 && N == 64 && C_eff == kChunk;
   const bool split = chunked && form != BwdForm::kFused;
+  const bool split32 = !bf16 && N == 64 && C_eff == kChunk;
   const size_t ck_ws = ckpt ? 0 : (ckpt_bytes(B, T, H, N, C_eff) + 255) / 256 * 256;
-  const size_t ws_bytes = ck_ws + (split ? bwd4_workspace_bytes(B, T, H) : 0);
+  const size_t ws_bytes = ck_ws + (split || split32 ? bwd4_workspace_bytes(B, T, H, bf16) : 0);
   if (ws_bytes) {
     // Fault injection for tests: make the workspace allocation fail.
     const char* inject = std::getenv("WKV7_FAIL_ALLOC");
@@ -436,7 +439,7 @@ int backward_impl(bool bf16, const void* const in[7], const float* s_init, const
   args.dS_init = dS_init;
   args.dS_final = dS_final;
   args.w_logit = logit ? 1 : 0;
-  args.carry = split ? ws + ck_ws / sizeof(float) : nullptr;
+  args.carry = split || split32 ? ws + ck_ws / sizeof(float) : nullptr;
 #ifdef WKV7_DEBUG
   args.out_kernel = g_debug_out_kernel.load();
 #endif
@@ -468,7 +471,13 @@ int backward_impl(bool bf16, const void* const in[7], const float* s_init, const
   args.T = T;
   args.H = H;
   set_extents(args, N, bf16, ckpt_bytes(B, T, H, N, C_eff));
-  cudaError_t e = split ? launch_bwd4(args, stream) : chunked ? launch_bwd3(args, stream) : launch_bwd2(args, bf16, N, stream);
+  cudaError_t e;
+  if (split32) {
+    e = launch_bwd4_carry_f32(args, stream);
+    if (e == cudaSuccess) e = launch_bwd4_out_f32(args, stream);
+  } else {
+    e = split ? launch_bwd4(args, stream) : chunked ? launch_bwd3(args, stream) : launch_bwd2(args, bf16, N, stream);
+  }
   if (ws) {
     cudaError_t e2 = cudaFreeAsync(ws, stream);
     if (e == cudaSuccess && e2 != cudaSuccess) return fail_cuda(e2, "cudaFreeAsync(workspace)");

@@ -352,8 +352,9 @@ __device__ void direct_chunk_bwd(Bwd3Smem& sm, const float* S0, int stage, int l
     ds0 = quad_sum(ds0);
     ds1 = quad_sum(ds1);
     if (t4 == 0) {
-      o.dv[o.base + (size_t)t * o.vstep + i0 + g] = dv0;
-      o.dv[o.base + (size_t)t * o.vstep + i0 + g + 8] = dv1;
+      float* p = o.dv + o.base + (size_t)t * o.vstep + i0 + g;
+      if (in_extent(o.status, o.ext->dv, p)) p[0] = dv0;
+      if (in_extent(o.status, o.ext->dv, p + 8)) p[8] = dv1;
     }
     // da = S_prev^T dsa; carry G <- G diag(w) + dsa a^T; column sums to shared memory
 #pragma unroll

@@ -63,10 +63,26 @@ constexpr int kThreads = 256;
 enum { V_R = 0, V_W = 1, V_K = 2, V_V = 3, V_A = 4, V_B = 5, V_DY = 6 };
 
 __device__ __forceinline__ float bf(const __nv_bfloat16* p) { return __bfloat162float(*p); }
+__device__ __forceinline__ float bf(const float* p) { return *p; }
 __device__ __forceinline__ float2 bf2(const __nv_bfloat16* p) {
   return __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(p));
 }
+__device__ __forceinline__ float2 bf2(const float* p) { return *reinterpret_cast<const float2*>(p); }
 __device__ __forceinline__ float2 tf32r2(float2 x) { return make_float2(tf32r(x.x), tf32r(x.y)); }
+
+// Operand values as the carry chain's products take them: tf32 (one product
+// each, bf16 inputs) or fp32 (split tf32, fp32 inputs).
+template <bool kX3>
+__device__ __forceinline__ float op_val(float x) {
+  if constexpr (kX3)
+    return x;
+  else
+    return tf32r(x);
+}
+template <bool kX3>
+__device__ __forceinline__ float2 op_val2(float2 x) {
+  return make_float2(op_val<kX3>(x.x), op_val<kX3>(x.y));
+}
 
 // ----------------------------------------------------------- bf16 operands ---
 
@@ -169,6 +185,7 @@ __device__ __forceinline__ void store_masked16(const float (&acc)[2][4], bf16_t*
 // T = (I - M)^-1 for a strictly lower 16 x 16 M (stride kLD16) by forward
 // substitution, one warp; lane s < 16 owns column s. Writes T (row-major)
 // and/or its transpose as tf32 values.
+template <bool kX3 = false>
 __device__ __forceinline__ void unit_lower_inverse(const float* M, float* Tout, float* TTout, int lane) {
   const int s = lane & 15;
   float col[kL];
@@ -182,7 +199,7 @@ __device__ __forceinline__ void unit_lower_inverse(const float* M, float* Tout, 
   if (lane < 16) {
 #pragma unroll
     for (int t = 0; t < kL; ++t) {
-      const float x = tf32r(col[t]);
+      const float x = op_val<kX3>(col[t]);
       if (Tout) Tout[t * kLD16 + s] = x;
       if (TTout) TTout[s * kLD16 + t] = x;
     }
@@ -224,16 +241,23 @@ struct ScratchC {
   float Mbr[kL * kLD16], Mba[kL * kLD16];  // R^ B~^T (with diagonal), A^ B~^T (strictly lower) [t][s]
 };
 
-struct CarrySmem {
-  __nv_bfloat16 raw[kCarryStages][6][kTile];  // r, w, a, b, dy (or dout), nv (epilogue) of one chunk per stage
+// Shared memory of the carry kernel for bf16 (TIn = bf16_t: six vectors per stage, the
+// epilogue's nv the sixth; carries stored as bf16) or fp32 inputs (five vectors; carries
+// stored as fp32).
+template <typename TIn>
+struct CarrySmemT {
+  static constexpr int kVecs = sizeof(TIn) == 2 ? 6 : 5;
+  typedef TIn CarryT;
+  TIn raw[kCarryStages][kVecs][kTile];  // r, w, a, b, dy (or dout), nv (epilogue) of one chunk per stage
   OpC op[3];
   ScratchC sc[2];
   float TT[kL * kLD16];  // T^T, T = (I - Mba)^-1
-  float Pc[4][kN];
-  bf16_t gst[2][kN * 72];  // carries on their way out (state warps write, products warps store)                                         // products of the decays of four-step blocks
+  float Pc[4][kN];       // products of the decays of four-step blocks
+  TIn gst[2][kN * 72];   // carries on their way out (state warps write, products warps store)
   uint64_t full[kCarryStages];
   int abort_flag;
 };
+typedef CarrySmemT<bf16_t> CarrySmem;
 
 // Sum over the 32 lanes (xor 16, 8, 4, 2, 1).
 __device__ __forceinline__ float warp_sum(float x) {
@@ -260,9 +284,10 @@ __device__ __forceinline__ __nv_bfloat162 gn_backward_row(float2 d, float2 nv, f
 // running products c(t) are taken per block of four steps and the blocks'
 // products chained in step order. Returns (uniformly over the group) whether
 // some decay leaves the range of the scaled form.
-template <bool kLogit, bool kEpi>
-__device__ bool form_carry(ScratchC& sc, float (&Pc)[4][kN], __nv_bfloat16* rs, OpC& op, int len, int ftid,
+template <typename TIn, bool kLogit, bool kEpi>
+__device__ bool form_carry(ScratchC& sc, float (&Pc)[4][kN], TIn* rs, OpC& op, int len, int ftid,
                            const float* epi_rstd, float2 epi_lw) {
+  constexpr bool kX3 = sizeof(TIn) == 4;
   const int lane = ftid & 31, pf = ftid >> 5, j = 2 * lane, t0 = 4 * pf;
   float2 wv[4], av[4], rv[4], bv[4], dyv[4];
   if constexpr (kEpi) {  // epilogue: the stage holds dout and nv; dy replaces dout (the step-by-step path reads it)
@@ -306,12 +331,12 @@ __device__ bool form_carry(ScratchC& sc, float (&Pc)[4][kN], __nv_bfloat16* rs, 
     const float2 cprev = c;
     c = fmul2(c, wv[e]);
     const float2 ic = make_float2(rcp_approx(c.x), rcp_approx(c.y));
-    const float2 ah = tf32r2(fmul2(av[e], cprev));
+    const float2 ah = op_val2<kX3>(fmul2(av[e], cprev));
     *reinterpret_cast<float2*>(sc.Ah + q) = ah;
     *reinterpret_cast<float2*>(op.Ah68 + q68) = ah;
-    *reinterpret_cast<float2*>(op.Rh + q) = tf32r2(fmul2(rv[e], c));
-    *reinterpret_cast<float2*>(sc.Bt + q) = tf32r2(fmul2(bv[e], ic));
-    *reinterpret_cast<float2*>(sc.Bb68 + q68) = tf32r2(fmul2(bv[e], fmul2(cL, ic)));
+    *reinterpret_cast<float2*>(op.Rh + q) = op_val2<kX3>(fmul2(rv[e], c));
+    *reinterpret_cast<float2*>(sc.Bt + q) = op_val2<kX3>(fmul2(bv[e], ic));
+    *reinterpret_cast<float2*>(sc.Bb68 + q68) = op_val2<kX3>(fmul2(bv[e], fmul2(cL, ic)));
     *reinterpret_cast<float2*>(op.DYs + q) = dyv[e];
   }
   return false;
@@ -319,53 +344,57 @@ __device__ bool form_carry(ScratchC& sc, float (&Pc)[4][kN], __nv_bfloat16* rs, 
 
 // n-tile nt of P Q^T (16 x 16, K = 64, tf32 values, stride kLD64) stored to M
 // (stride kLD16) as tf32, masked to s < t (strict) or s <= t.
+template <bool kX3>
 __device__ __forceinline__ void gram_tile(float* M, const float* P, const float* Q, int nt, bool strict, int lane) {
   const int g = lane >> 2, t4 = lane & 3;
   float acc[4];
   zero4(acc);
 #pragma unroll
   for (int kb = 0; kb < kN / 8; ++kb) {
-    uint32_t a[4], b0, b1;
-    frag_a(a, P, kLD64, 0, 8 * kb, g, t4);
-    frag_b(b0, b1, Q, kLD64, 8 * nt, 8 * kb, g, t4);
-    mma_tf32(acc, a, b0, b1);
+    FragA<kX3> a;
+    FragB<kX3> b;
+    ld_a(a, P, kLD64, 0, 8 * kb, g, t4);
+    ld_b(b, Q, kLD64, 8 * nt, 8 * kb, g, t4);
+    mma_x(acc, a, b);
   }
 #pragma unroll
   for (int h = 0; h < 2; ++h) {
     const int t = g + 8 * h, s = 8 * nt + 2 * t4;
     const bool k0 = strict ? s < t : s <= t, k1 = strict ? s + 1 < t : s + 1 <= t;
     *reinterpret_cast<float2*>(M + t * kLD16 + s) =
-        make_float2(k0 ? tf32r(acc[2 * h]) : 0.f, k1 ? tf32r(acc[2 * h + 1]) : 0.f);
+        make_float2(k0 ? op_val<kX3>(acc[2 * h]) : 0.f, k1 ? op_val<kX3>(acc[2 * h + 1]) : 0.f);
   }
 }
 
 // Forming group: wait for a chunk's inputs and form its operands. Returns
 // false on a timeout.
-template <bool kLogit, bool kEpi>
-__device__ bool front_form(CarrySmem& sm, ScratchC& sc, OpC& op, __nv_bfloat16* rs, uint64_t* bar,
-                           uint32_t parity, int len, unsigned* status, const float* epi_rstd, float2 epi_lw) {
+template <typename TIn, bool kLogit, bool kEpi>
+__device__ bool front_form(CarrySmemT<TIn>& sm, ScratchC& sc, OpC& op, TIn* rs, uint64_t* bar, uint32_t parity,
+                           int len, unsigned* status, const float* epi_rstd, float2 epi_lw) {
   const int ftid = threadIdx.x - 128;
   const bool ok = mbar_wait_bounded(status, bar, parity);
   if (named_bar_or(1, 128, !ok)) {
     if (ftid == 0) sm.abort_flag = 1;
     return false;
   }
-  const bool unsafe = form_carry<kLogit, kEpi>(sc, sm.Pc, rs, op, len, ftid, epi_rstd, epi_lw);
+  const bool unsafe = form_carry<TIn, kLogit, kEpi>(sc, sm.Pc, rs, op, len, ftid, epi_rstd, epi_lw);
   if (ftid == 0) op.unsafe = unsafe;
   if (unsafe) return true;
   named_bar(1, 128);
   // n-tile pf - 2 of Mba = A^ B~^T (warps 2, 3); the products group makes Mbr
   const int pf = ftid >> 5;
-  if (pf >= 2) gram_tile(sc.Mba, sc.Ah, sc.Bt, pf - 2, true, ftid & 31);
+  if (pf >= 2) gram_tile<sizeof(TIn) == 4>(sc.Mba, sc.Ah, sc.Bt, pf - 2, true, ftid & 31);
   return true;
 }
 
 // Products group (128 threads): T, Mbr = R^ B~^T (with diagonal), T^T Bb and Mbr T of a
 // formed chunk.
-__device__ void front_products(CarrySmem& sm, ScratchC& sc, OpC& op) {
+template <typename TIn>
+__device__ void front_products(CarrySmemT<TIn>& sm, ScratchC& sc, OpC& op) {
+  constexpr bool kX3 = sizeof(TIn) == 4;
   const int pp = (threadIdx.x >> 5) - 8, lane = threadIdx.x & 31, g = lane >> 2, t4 = lane & 3;
-  if (pp == 0) unit_lower_inverse(sc.Mba, nullptr, sm.TT, lane);
-  else if (pp <= 2) gram_tile(sc.Mbr, op.Rh, sc.Bt, pp - 1, false, lane);
+  if (pp == 0) unit_lower_inverse<kX3>(sc.Mba, nullptr, sm.TT, lane);
+  else if (pp <= 2) gram_tile<kX3>(sc.Mbr, op.Rh, sc.Bt, pp - 1, false, lane);
   named_bar(2, 128);
   {  // T^T Bb, n-tiles 2 pp and 2 pp + 1
     float acc[2][4];
@@ -373,13 +402,13 @@ __device__ void front_products(CarrySmem& sm, ScratchC& sc, OpC& op) {
     zero4(acc[1]);
 #pragma unroll
     for (int kb = 0; kb < 2; ++kb) {
-      uint32_t a[4];
-      frag_a(a, sm.TT, kLD16, 0, 8 * kb, g, t4);
+      FragA<kX3> a;
+      ld_a(a, sm.TT, kLD16, 0, 8 * kb, g, t4);
 #pragma unroll
       for (int nt = 0; nt < 2; ++nt) {
-        uint32_t b0, b1;
-        frag_b_t(b0, b1, sc.Bb68, kLDT, 8 * (2 * pp + nt), 8 * kb, g, t4);
-        mma_tf32(acc[nt], a, b0, b1);
+        FragB<kX3> b;
+        ld_b_t(b, sc.Bb68, kLDT, 8 * (2 * pp + nt), 8 * kb, g, t4);
+        mma_x(acc[nt], a, b);
       }
     }
 #pragma unroll
@@ -387,7 +416,7 @@ __device__ void front_products(CarrySmem& sm, ScratchC& sc, OpC& op) {
 #pragma unroll
       for (int h = 0; h < 2; ++h)
         *reinterpret_cast<float2*>(op.Btp + (g + 8 * h) * kLD64 + 8 * (2 * pp + nt) + 2 * t4) =
-            make_float2(tf32r(acc[nt][2 * h]), tf32r(acc[nt][2 * h + 1]));
+            make_float2(op_val<kX3>(acc[nt][2 * h]), op_val<kX3>(acc[nt][2 * h + 1]));
   }
   if (pp >= 2) {  // W = Mbr T, n-tile pp - 2
     const int q = pp - 2;
@@ -395,27 +424,26 @@ __device__ void front_products(CarrySmem& sm, ScratchC& sc, OpC& op) {
     zero4(acc);
 #pragma unroll
     for (int kb = 0; kb < 2; ++kb) {
-      uint32_t a[4], b0, b1;
-      frag_a(a, sc.Mbr, kLD16, 0, 8 * kb, g, t4);
-      frag_b(b0, b1, sm.TT, kLD16, 8 * q, 8 * kb, g, t4);
-      mma_tf32(acc, a, b0, b1);
+      FragA<kX3> a;
+      FragB<kX3> b;
+      ld_a(a, sc.Mbr, kLD16, 0, 8 * kb, g, t4);
+      ld_b(b, sm.TT, kLD16, 8 * q, 8 * kb, g, t4);
+      mma_x(acc, a, b);
     }
 #pragma unroll
     for (int h = 0; h < 2; ++h)
       *reinterpret_cast<float2*>(op.W + (g + 8 * h) * kLD16 + 8 * q + 2 * t4) =
-          make_float2(tf32r(acc[2 * h]), tf32r(acc[2 * h + 1]));
+          make_float2(op_val<kX3>(acc[2 * h]), op_val<kX3>(acc[2 * h + 1]));
   }
 }
 
 // One chunk of the carry (state warp, rows i0 .. i0+15 of G):
 //   DSA^T = G (T^T Bb)^T + DY^T (Mbr T);  G <- G diag(c(L)) + DY^T R^ + DSA^T A^
+template <bool kX3>
 __device__ __forceinline__ void carry_chunk(float (&G)[8][4], const OpC& op, int i0, int g, int t4) {
-  uint32_t aG[8][4];
+  FragA<kX3> aD[2];
 #pragma unroll
-  for (int kb = 0; kb < 8; ++kb) c2a(aG[kb], G[kb]);
-  uint32_t aD[2][4];
-#pragma unroll
-  for (int kb = 0; kb < 2; ++kb) frag_a_ts(aD[kb], op.DYs, kLD64, i0, 8 * kb, g, t4);  // DY^T (hardware k order)
+  for (int kb = 0; kb < 2; ++kb) ld_a_ts(aD[kb], op.DYs, kLD64, i0, 8 * kb, g, t4);  // DY^T (hardware k order)
   float DS[2][4];
   zero4(DS[0]);
   zero4(DS[1]);
@@ -423,18 +451,21 @@ __device__ __forceinline__ void carry_chunk(float (&G)[8][4], const OpC& op, int
   for (int kb = 0; kb < 2; ++kb)
 #pragma unroll
     for (int q = 0; q < 2; ++q) {
-      uint32_t b0, b1;
-      frag_b_ts(b0, b1, op.W, kLD16, 8 * q, 8 * kb, g, t4);
-      mma_tf32(DS[q], aD[kb], b0, b1);
+      FragB<kX3> b;
+      ld_b_ts(b, op.W, kLD16, 8 * q, 8 * kb, g, t4);
+      mma_x(DS[q], aD[kb], b);
     }
 #pragma unroll
-  for (int kb = 0; kb < 8; ++kb)
+  for (int kb = 0; kb < 8; ++kb) {
+    FragA<kX3> aG;
+    acc_to_a(aG, G[kb]);
 #pragma unroll
     for (int q = 0; q < 2; ++q) {
-      uint32_t b0, b1;
-      frag_b(b0, b1, op.Btp, kLD64, 8 * q, 8 * kb, g, t4);
-      mma_tf32(DS[q], aG[kb], b0, b1);
+      FragB<kX3> b;
+      ld_b(b, op.Btp, kLD64, 8 * q, 8 * kb, g, t4);
+      mma_x(DS[q], aG, b);
     }
+  }
 #pragma unroll
   for (int nt = 0; nt < 8; ++nt) {
     const float2 cl = *reinterpret_cast<const float2*>(op.cL + 8 * nt + 2 * t4);
@@ -447,29 +478,29 @@ __device__ __forceinline__ void carry_chunk(float (&G)[8][4], const OpC& op, int
   for (int kb = 0; kb < 2; ++kb)
 #pragma unroll
     for (int nt = 0; nt < 8; ++nt) {
-      uint32_t b0, b1;
-      frag_b_ts(b0, b1, op.Rh, kLD64, 8 * nt, 8 * kb, g, t4);
-      mma_tf32(G[nt], aD[kb], b0, b1);
+      FragB<kX3> b;
+      ld_b_ts(b, op.Rh, kLD64, 8 * nt, 8 * kb, g, t4);
+      mma_x(G[nt], aD[kb], b);
     }
-  uint32_t aS[2][4];
-  c2a(aS[0], DS[0]);
-  c2a(aS[1], DS[1]);
+  FragA<kX3> aS[2];
+  acc_to_a(aS[0], DS[0]);
+  acc_to_a(aS[1], DS[1]);
 #pragma unroll
   for (int kb = 0; kb < 2; ++kb)
 #pragma unroll
     for (int nt = 0; nt < 8; ++nt) {
-      uint32_t b0, b1;
-      frag_b_t(b0, b1, op.Ah68, kLDT, 8 * nt, 8 * kb, g, t4);
-      mma_tf32(G[nt], aS[kb], b0, b1);
+      FragB<kX3> b;
+      ld_b_t(b, op.Ah68, kLDT, 8 * nt, 8 * kb, g, t4);
+      mma_x(G[nt], aS[kb], b);
     }
 }
 
 // The same chunk step by step in fp32 (a chunk outside the scaled form's
 // range): G += dy r^T ; dsa = G b ; G <- G diag(w) + dsa a^T.
-template <bool kLogit>
-__device__ void carry_direct(float (&G)[8][4], const __nv_bfloat16* rs, int len, int i0, int g, int t4) {
+template <typename TIn, bool kLogit>
+__device__ void carry_direct(float (&G)[8][4], const TIn* rs, int len, int i0, int g, int t4) {
   for (int t = len - 1; t >= 0; --t) {
-    const __nv_bfloat16* row = rs + t * kN;
+    const TIn* row = rs + t * kN;
     const float dy0 = bf(row + C_DY * kTile + i0 + g), dy1 = bf(row + C_DY * kTile + i0 + g + 8);
     float ds0 = 0.f, ds1 = 0.f;
 #pragma unroll
@@ -499,6 +530,16 @@ __device__ void carry_direct(float (&G)[8][4], const __nv_bfloat16* rs, int len,
 
 // A staged 64 x 64 bf16 carry (rows of 72) to global memory, 128 threads, whole rows per
 // instruction.
+// The same for an fp32 carry: 64 rows of 16 pieces of 16 bytes.
+__device__ __forceinline__ void flush_carry(const float* src, float* dst, int ptid, const Extent& x, unsigned* status) {
+#pragma unroll
+  for (int q = 0; q < 8; ++q) {
+    const int idx = ptid + 128 * q;  // row idx / 16, columns 4 (idx % 16) ..
+    uint4* p = reinterpret_cast<uint4*>(dst + 4 * idx);
+    if (in_extent(status, x, p)) *p = *reinterpret_cast<const uint4*>(src + (idx >> 4) * 72 + 4 * (idx & 15));
+  }
+}
+
 __device__ __forceinline__ void flush_carry(const bf16_t* src, bf16_t* dst, int ptid, const Extent& x,
                                             unsigned* status) {
 #pragma unroll
@@ -509,10 +550,12 @@ __device__ __forceinline__ void flush_carry(const bf16_t* src, bf16_t* dst, int 
   }
 }
 
-template <bool kLogit, bool kEpi>
+template <typename TIn, bool kLogit, bool kEpi>
 __global__ void __launch_bounds__(kCarryThreads, 1) wkv7_bwd4_carry_kernel(const __grid_constant__ BwdArgs args) {
   extern __shared__ __align__(128) unsigned char smem_raw[];
-  CarrySmem& sm = *reinterpret_cast<CarrySmem*>(smem_raw);
+  using Smem = CarrySmemT<TIn>;
+  constexpr bool kX3 = sizeof(TIn) == 4;
+  Smem& sm = *reinterpret_cast<Smem*>(smem_raw);
   const int T = args.T, H = args.H;
   const int head = blockIdx.x, bi = head / H, hi = head % H;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, g = lane >> 2, t4 = lane & 3;
@@ -520,8 +563,8 @@ __global__ void __launch_bounds__(kCarryThreads, 1) wkv7_bwd4_carry_kernel(const
   const int i0 = 16 * warp;                          // state warps: rows of the carry
   const int nchunks = (T + kL - 1) / kL;
   const int nvec = kEpi ? 6 : 5;
-  const uint32_t stage_bytes = (uint32_t)(nvec * kTile * 2);
-  bf16_t* carry_head = reinterpret_cast<bf16_t*>(args.carry) + (size_t)head * nchunks * kN * kN;
+  const uint32_t stage_bytes = (uint32_t)(nvec * kTile * sizeof(TIn));
+  TIn* carry_head = reinterpret_cast<TIn*>(args.carry) + (size_t)head * nchunks * kN * kN;
 
   // Chunks are visited in reverse: visit v is chunk nchunks-1-v. In visit m the state warps
   // advance the carry through chunk m, the products group finishes chunk m+1 and the
@@ -563,15 +606,16 @@ __global__ void __launch_bounds__(kCarryThreads, 1) wkv7_bwd4_carry_kernel(const
       if (v + 1 < nchunks) load_rstd(v + 1);
       rst = rs_cur;
     }
-    if (!front_form<kLogit, kEpi>(sm, sm.sc[c & 1], sm.op[c % 3], sm.raw[v % kCarryStages][0], &sm.full[v % kCarryStages],
-                            (v / kCarryStages) & 1, len_of(v), args.status, rst, epi_lw))
+    if (!front_form<TIn, kLogit, kEpi>(sm, sm.sc[c & 1], sm.op[c % 3], sm.raw[v % kCarryStages][0],
+                                       &sm.full[v % kCarryStages], (v / kCarryStages) & 1, len_of(v), args.status, rst,
+                                       epi_lw))
       return false;
     waited = v + 1;
     return true;
   };
   auto products = [&](int v) {  // products group
     const int c = chunk_of(v);
-    if (!sm.op[c % 3].unsafe) front_products(sm, sm.sc[c & 1], sm.op[c % 3]);
+    if (!sm.op[c % 3].unsafe) front_products<TIn>(sm, sm.sc[c & 1], sm.op[c % 3]);
   };
   // TMA copies are issued by a products-group thread (that group has the most slack); the
   // forming group waits for them
@@ -620,19 +664,25 @@ __global__ void __launch_bounds__(kCarryThreads, 1) wkv7_bwd4_carry_kernel(const
     const int n = chunk_of(m), st = m % kCarryStages;
     if (role == 0) {
       const OpC& op = sm.op[n % 3];
-      // the carry entering this chunk (gradient w.r.t. the state after it), as the bf16
-      // operand the output kernel multiplies with; the products group stores it next round
-      bf16_t* dst = sm.gst[m & 1];
+      // the carry entering this chunk (gradient w.r.t. the state after it), as the output
+      // pass multiplies with it (bf16, or fp32 for fp32 inputs); the products group stores it
+      // next round
+      TIn* dst = sm.gst[m & 1];
 #pragma unroll
       for (int nt = 0; nt < 8; ++nt) {
         const int col = 8 * nt + 2 * t4;
-        *reinterpret_cast<uint32_t*>(dst + (i0 + g) * 72 + col) = pack_bf16(G[nt][0], G[nt][1]);
-        *reinterpret_cast<uint32_t*>(dst + (i0 + g + 8) * 72 + col) = pack_bf16(G[nt][2], G[nt][3]);
+        if constexpr (kX3) {
+          *reinterpret_cast<float2*>(dst + (i0 + g) * 72 + col) = make_float2(G[nt][0], G[nt][1]);
+          *reinterpret_cast<float2*>(dst + (i0 + g + 8) * 72 + col) = make_float2(G[nt][2], G[nt][3]);
+        } else {
+          *reinterpret_cast<uint32_t*>(dst + (i0 + g) * 72 + col) = pack_bf16(G[nt][0], G[nt][1]);
+          *reinterpret_cast<uint32_t*>(dst + (i0 + g + 8) * 72 + col) = pack_bf16(G[nt][2], G[nt][3]);
+        }
       }
       if (op.unsafe)
-        carry_direct<kLogit>(G, sm.raw[st][0], len_of(m), i0, g, t4);
+        carry_direct<TIn, kLogit>(G, sm.raw[st][0], len_of(m), i0, g, t4);
       else
-        carry_chunk(G, op, i0, g, t4);
+        carry_chunk<kX3>(G, op, i0, g, t4);
     } else if (role == 1) {
       if (m + 2 < nchunks) form(m + 2);
     } else {
@@ -2003,19 +2053,19 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) wkv7_bwd4_tc_kernel(cons
 
 }  // namespace
 
-size_t bwd4_workspace_bytes(int B, int T, int H) {
+size_t bwd4_workspace_bytes(int B, int T, int H, bool bf16) {
   const size_t nchunks = ((size_t)T + kL - 1) / kL, heads = (size_t)B * H;
-  return heads * nchunks * kN * kN * sizeof(__nv_bfloat16);
+  return heads * nchunks * kN * kN * (bf16 ? sizeof(__nv_bfloat16) : sizeof(float));
 }
 
 template <bool kLogit, bool kEpi>
 cudaError_t launch_bwd4_impl(const BwdArgs& args, cudaStream_t stream) {
   const size_t smem_c = sizeof(CarrySmem), smem_o = sizeof(OutSmem) + (kEpi ? sizeof(OutEpiSmem) : 0);
-  cudaError_t e = cudaFuncSetAttribute(wkv7_bwd4_carry_kernel<kLogit, kEpi>,
+  cudaError_t e = cudaFuncSetAttribute(wkv7_bwd4_carry_kernel<bf16_t, kLogit, kEpi>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_c);
   if (e != cudaSuccess) return e;
   const unsigned heads = (unsigned)(args.B * args.H), nchunks = (unsigned)((args.T + kL - 1) / kL);
-  wkv7_bwd4_carry_kernel<kLogit, kEpi><<<heads, kCarryThreads, smem_c, stream>>>(args);
+  wkv7_bwd4_carry_kernel<bf16_t, kLogit, kEpi><<<heads, kCarryThreads, smem_c, stream>>>(args);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   if (args.out_kernel != 1 || kEpi) {
@@ -2033,6 +2083,17 @@ cudaError_t launch_bwd4_impl(const BwdArgs& args, cudaStream_t stream) {
   if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
   const unsigned ntasks = heads * nchunks, grid = std::min<unsigned>(ntasks, (unsigned)tcout::kCtasPerSm * (unsigned)sms);
   tcout::wkv7_bwd4_tc_kernel<kLogit><<<grid, tcout::kThreads, tcout::kSmemBytes, stream>>>(args, (int)ntasks);
+  return cudaGetLastError();
+}
+
+// fp32 inputs: the carry chain alone, in split tf32, storing fp32 carries.
+cudaError_t launch_bwd4_carry_f32(const BwdArgs& args, cudaStream_t stream) {
+  const size_t smem = sizeof(CarrySmemT<float>);
+  static_assert(sizeof(CarrySmemT<float>) <= 227 * 1024, "shared memory over budget");
+  cudaError_t e = cudaFuncSetAttribute(wkv7_bwd4_carry_kernel<float, false, false>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  wkv7_bwd4_carry_kernel<float, false, false><<<(unsigned)(args.B * args.H), kCarryThreads, smem, stream>>>(args);
   return cudaGetLastError();
 }
 

@@ -107,7 +107,11 @@ cudaError_t launch_bwd3(const BwdArgs& args, cudaStream_t stream);
 // The same backward as a carry-chain kernel plus a parallel per-chunk output
 // kernel; needs args.carry, a workspace of bwd4_workspace_bytes.
 cudaError_t launch_bwd4(const BwdArgs& args, cudaStream_t stream);
-size_t bwd4_workspace_bytes(int B, int T, int H);
+// The same split for fp32 inputs (products in split tf32): the carry chain, storing fp32
+// carries in the workspace, then the per-chunk output pass.
+cudaError_t launch_bwd4_carry_f32(const BwdArgs& args, cudaStream_t stream);
+cudaError_t launch_bwd4_out_f32(const BwdArgs& args, cudaStream_t stream);
+size_t bwd4_workspace_bytes(int B, int T, int H, bool bf16);
 // dln_w, dln_b, dr_k [H][N] from the output pass's per-chunk terms, summed in a fixed order.
 cudaError_t launch_epi_params(const float* part, float* dln_w, float* dln_b, float* dr_k, int B, int H, int nchunks,
                               cudaStream_t stream);

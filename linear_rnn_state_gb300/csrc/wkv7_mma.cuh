@@ -193,6 +193,48 @@ __device__ __forceinline__ void ld_b(FragB<kX3>& b, const float* bt, int ld, int
   make_b(b, v.x, v.y);
 }
 
+// The transposed and hardware-order forms of frag_a_t, frag_a_ts, frag_b_t,
+// frag_b_ts (same element order).
+template <bool kX3>
+__device__ __forceinline__ void ld_a_t(FragA<kX3>& a, const float* m, int ld, int m0, int k0, int g, int t) {
+  const float* p = m + (k0 + 2 * t) * ld + m0 + g;
+  make_a(a, p[0], p[8], p[ld], p[ld + 8]);
+}
+template <bool kX3>
+__device__ __forceinline__ void ld_a_ts(FragA<kX3>& a, const float* m, int ld, int m0, int k0, int g, int t) {
+  const float* p = m + (k0 + t) * ld + m0 + g;
+  make_a(a, p[0], p[8], p[4 * ld], p[4 * ld + 8]);
+}
+template <bool kX3>
+__device__ __forceinline__ void ld_b_t(FragB<kX3>& b, const float* m, int ld, int n0, int k0, int g, int t) {
+  const float* p = m + (k0 + 2 * t) * ld + n0 + g;
+  make_b(b, p[0], p[ld]);
+}
+template <bool kX3>
+__device__ __forceinline__ void ld_b_ts(FragB<kX3>& b, const float* m, int ld, int n0, int k0, int g, int t) {
+  const float* p = m + (k0 + t) * ld + n0 + g;
+  make_b(b, p[0], p[4 * ld]);
+}
+// frag_a_r / frag_b_t_r: fp32 storage rounded to tf32 (kX3 = false), or split.
+template <bool kX3>
+__device__ __forceinline__ void ld_a_r(FragA<kX3>& a, const float* m, int ld, int r0, int k0, int g, int t) {
+  if constexpr (kX3) {
+    ld_a(a, m, ld, r0, k0, g, t);
+  } else {
+    uint32_t x[4];
+    frag_a_r(x, m, ld, r0, k0, g, t);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) a.h[i] = x[i];
+  }
+}
+template <bool kX3>
+__device__ __forceinline__ void ld_b_t_r(FragB<kX3>& b, const float* m, int ld, int n0, int k0, int g, int t) {
+  if constexpr (kX3)
+    ld_b_t(b, m, ld, n0, k0, g, t);
+  else
+    frag_b_t_r(b.h0, b.h1, m, ld, n0, k0, g, t);
+}
+
 // Accumulator tile -> A fragment over the same columns: rounded to tf32
 // (kX3 = false), or split.
 template <bool kX3>
