@@ -36,20 +36,22 @@ TRAFFIC = {
     "kernel": "wkv7_bwd4_carry_kernel + wkv7_bwd4_out_kernel (one wkv7_backward_bf16 call)",
     "sources": ("wkv7_bwd4.cu", "wkv7_common.cuh", "wkv7_scaled.cuh", "wkv7_mma.cuh", "wkv7_launch.h",
                 "wkv7_decay.cuh", "wkv7_tmem.cuh"),
-    "sha256": "19536b6bd69788d0742498ac2300cefb7d7f19e6c539777052b5d1524ab3689d",
-    "bytes_per_token_head": (83.953920e6 + 28.895744e6 + 318.861056e6 + 161.701376e6) / 131072,
+    "sha256": "ecc1a31653def886294f515a1acd7687e70297aa777a487aac4d618352f81fa4",
+    "bytes_per_token_head": (83.953920e6 + 28.128512e6 + 318.836992e6 + 161.838592e6) / 131072,
 }
 
 
-# The fp32 backward (wkv7_backward at N = 64) runs one kernel; its DRAM bytes per token-head from
-# one ncu capture at the 8 x 4096 x 12 workload (dram__bytes_read.sum + dram__bytes_write.sum of
-# one launch / (B*T*H)), null once its sources change.
+# The fp32 backward (wkv7_backward at N = 64, 16-step checkpoints) runs the carry chain and the
+# per-chunk output pass in split tf32; their DRAM bytes per token-head from one ncu capture of the
+# 8 x 1024 x 12 case (dram__bytes_read.sum + dram__bytes_write.sum / (B*T*H)), null once their
+# sources change.
 TRAFFIC_FP32 = {
-    "kernel": "wkv7_bwd2_kernel (one wkv7_backward call, fp32 inputs)",
-    "sources": ("wkv7_bwd2.cu", "wkv7_common.cuh", "wkv7_scaled.cuh", "wkv7_tmem.cuh", "wkv7_launch.h"),
-    "sha256": "eed32800391914dce60eb7b191285669bca86d5bcf4aa6e18465af8b80d628a2",
+    "kernel": "wkv7_bwd4_carry_kernel<float> + wkv7_bwd4_out_f32_kernel (one wkv7_backward call, fp32 inputs)",
+    "sources": ("wkv7_bwd4.cu", "wkv7_bwd4_f32.cu", "wkv7_common.cuh", "wkv7_scaled.cuh", "wkv7_mma.cuh",
+                "wkv7_launch.h", "wkv7_decay.cuh", "wkv7_tmem.cuh"),
+    "sha256": "a33903b1cb9635d26b778256e544d20cc939d892409bb716b9cea94d185e3b1b",
     "N": 64,
-    "bytes_per_token_head": (1107.634432e6 + 571.360768e6) / 393216,
+    "bytes_per_token_head": (125.942784e6 + 59.765504e6 + 377.598720e6 + 124.783872e6) / 98304,
 }
 
 
@@ -512,9 +514,10 @@ def _report(args, wl, world, B, T, H, N, C, bf16, ms, fwd_ms, bwd_ms, e2e, ckpt,
                        "operands in the backward's per-chunk gradient products (the carry stored as bf16 between "
                        "the two backward kernels, the fp32 checkpoint rounded to bf16 there); fp32 accumulation, "
                        "state and element-wise math" if chunked else
-                       ("forward on tensor cores in split tf32 (three tf32 products per fp32 product, fp32 "
-                        "accumulation; state and element-wise math fp32); backward fp32 FMA (scalar kernel)"
-                        if N == 64 else "fp32 FMA throughout (scalar kernels)"))
+                       ("tensor-core products in split tf32 in the forward, the backward's carry chain and its "
+                        "per-chunk output pass (three tf32 products per fp32 product, fp32 accumulation); the "
+                        "state, the carried gradient (stored as fp32 between the two backward kernels) and "
+                        "every element-wise step fp32" if N == 64 and C == 16 else "fp32 FMA throughout (scalar kernels)"))
                       + "; inputs, dy and y stored in " + wl.storage,
         "config": {"workload": (wl.name + {"wkv7-logit": "-decay-logits", "wkv7-epilogue": "-with-epilogue"}.get(
                        args.workload, ""))
@@ -524,12 +527,17 @@ def _report(args, wl, world, B, T, H, N, C, bf16, ms, fwd_ms, bwd_ms, e2e, ckpt,
         "fwd_ms": fwd_ms, "bwd_ms": bwd_ms, "step_roofline_frac": t_roof / (ms * 1e-3),
         "roofline": {"bound": "alu", "achieved": achieved / 1e12, "peak": peak_flops / 1e12, "unit": "TFLOP/s",
                      "frac": achieved / peak_flops,
-                     "traffic": measured_traffic(BTH) if chunked else measured_traffic_fp32(BTH, N),
-                     "kernel": TRAFFIC["kernel"] if chunked else TRAFFIC_FP32["kernel"],
+                     "traffic": measured_traffic(BTH) if chunked else measured_traffic_fp32(BTH, N) if C == 16 else None,
+                     "kernel": TRAFFIC["kernel"] if chunked else TRAFFIC_FP32["kernel"] if N == 64 and C == 16
+                     else "wkv7_bwd2_kernel (one wkv7_backward call)",
                      "note": ("the backward call (its two kernels, timed together with CUDA events around the "
                               "call): algorithmic FLOP of the recurrence (24 N^2 per token-head) against the FP32 "
                               "CUDA-core peak, the roofline the metric names; the kernels form them as tensor-core "
                               "products (tf32 in the carry chain, bf16 in the output pass)") if chunked else
+                             ("the backward call (its two kernels, timed together with CUDA events around the call): "
+                              "algorithmic FLOP of the recurrence (24 N^2 per token-head) against the FP32 CUDA-core "
+                              "peak; the kernels form them as split-tf32 tensor-core products")
+                             if N == 64 and C == 16 else
                              ("the backward call (one kernel, timed with CUDA events around the call): algorithmic "
                               "FLOP of the recurrence (24 N^2 per token-head) against the FP32 CUDA-core peak"),
                      "peak_source": f"{sms} SMs x {FP32_LANES_PER_SM} FP32 lanes x 2 x {peaks['sm_max_mhz']:.0f} MHz",
@@ -537,7 +545,9 @@ def _report(args, wl, world, B, T, H, N, C, bf16, ms, fwd_ms, bwd_ms, e2e, ckpt,
         "e2e": None if e2e is None else {
             "value": aggregate_tokens_per_s(world, B, T, e2e[0]), "unit": "tokens/s", "h2d_bytes_per_step": e2e[1],
             "d2h_bytes_per_step": e2e[2]},
-        "gpu_launches": (4 if args.workload == "wkv7-epilogue" else 3 if (bf16 and N == 64) else 2) * args.steps,
+        # bf16 at N = 64: forward, carry chain, output pass (+ the epilogue's parameter sum); fp32 at
+        # N = 64 with 16-step checkpoints the same three; otherwise the scalar forward and backward
+        "gpu_launches": (4 if args.workload == "wkv7-epilogue" else 3 if N == 64 and C == 16 else 2) * args.steps,
         "clocks": clocks.summary(),
     }
     if args.workload == "wkv7-epilogue":

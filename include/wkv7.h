@@ -107,9 +107,13 @@ int wkv7_forward_bf16(const wkv7_bf16* r, const wkv7_bf16* w, const wkv7_bf16* k
  *                  ckpt_every <= 0 lets the library pick the interval.
  *   dr, dw, dk, dv, da, db  [B][T][H][N] gradients (required).
  *   dS_init        [B][H][N][N] gradient of the initial state, or NULL.
- * Arithmetic: fp32 FMA throughout (the reverse scan replays each window of
- * steps from its checkpoint); when ckpt is NULL the library's checkpointing
- * forward is wkv7_forward's, in split tf32 at N = 64.
+ * Arithmetic. At N = 64 with 16-step checkpoints the chunked form runs in
+ * two passes, every product in split tf32 (as wkv7_forward): the carried
+ * gradient at every chunk boundary first (one sequential pass per (b, h), the
+ * carry held and stored in fp32, in a workspace of B*H*ceil(T/16)*N*N floats
+ * taken with cudaMallocAsync on `stream`, so WKV7_ERR_ALLOC can also be
+ * returned when ckpt is given), then every chunk's gradients at once. Other N
+ * or checkpoint intervals run fp32 FMA throughout.
  * Returns WKV7_OK, WKV7_ERR_INVALID, WKV7_ERR_ALLOC or WKV7_ERR_CUDA.
  */
 int wkv7_backward(const float* r, const float* w, const float* k, const float* v, const float* a,

@@ -7,9 +7,10 @@ outside it is skipped and sets the status word (WKV7_ERR_BOUNDS from
 wkv7_status). Two things are tested:
 
 * every kernel the library selects (scalar fp32 forward and backward, the
-  chunked bf16 forward, the split backward with either output pass, the fused
-  backward, the fused epilogue in both directions, the no-allocation
-  backward) runs its parity case through the checks with the status word
+  chunked forward and split backward for fp32 inputs, the chunked bf16
+  forward, the split backward with either output pass, the fused backward,
+  the fused epilogue in both directions, the no-allocation backward) runs its
+  parity case through the checks with the status word
   clean and the results still equal to the oracle's: no index of theirs
   leaves its buffer;
 * the checks fire: with every buffer's extent cut by 4 bytes
@@ -101,12 +102,12 @@ def _scan_case(env, path):
     """Forward and backward of one path through the debug build; returns the
     outputs (torch tensors) and the oracle's."""
     oracle, _, inputs, wkv7, dbg = env
-    bf16 = path != "fp32"
-    B, T, H, N = (2, 130, 3, 64) if bf16 else (2, 80, 3, 32)
+    bf16 = not path.startswith("fp32")
+    B, T, H, N = (2, 80, 3, 32) if path == "fp32" else (2, 130, 3, 64)
     t, o = _data(inputs, B, T, H, N, "bf16" if bf16 else "f32", seed=300 + len(path))
     dbg.wkv7_debug_out_kernel(1 if path == "tc" else 0)
     try:
-        y, sf, ck, C = wkv7.forward(*(t[n] for n in NAMES), t["s_init"], ckpt_every=16 if bf16 else None)
+        y, sf, ck, C = wkv7.forward(*(t[n] for n in NAMES), t["s_init"], ckpt_every=None if path == "fp32" else 16)
         g = wkv7.backward(*(t[n] for n in NAMES), t["dy"], t["s_init"], ck, C, dS_final=t["dS_final"],
                           fused=path == "fused")
     finally:
@@ -117,7 +118,7 @@ def _scan_case(env, path):
     return got, {"y": y_ref, "s_final": sf_ref, **gr}, bf16
 
 
-@pytest.mark.parametrize("path", ["fp32", "split", "tc", "fused"])
+@pytest.mark.parametrize("path", ["fp32", "fp32-chunked", "split", "tc", "fused"])
 def test_scan_kernels_stay_inside_their_buffers(env, path):
     wkv7 = env[3]
     got, ref, bf16 = _scan_case(env, path)
@@ -170,9 +171,9 @@ def _sentinel_run(env, path):
     """One forward and one backward of `path` into NaN-filled outputs; returns
     them and the status after each call."""
     _, _, inputs, wkv7, dbg = env
-    bf16 = path != "fp32"
-    B, T, H, N = (2, 130, 3, 64) if bf16 else (2, 80, 3, 32)
-    C = 16 if bf16 else wkv7.wkv7_default_ckpt_every(N, False)
+    bf16 = not path.startswith("fp32")
+    B, T, H, N = (2, 80, 3, 32) if path == "fp32" else (2, 130, 3, 64)
+    C = wkv7.wkv7_default_ckpt_every(N, False) if path == "fp32" else 16
     t, _ = _data(inputs, B, T, H, N, "bf16" if bf16 else "f32", seed=340)
     dev = t["r"].device
     nan = float("nan")
@@ -202,7 +203,7 @@ def _sentinel_run(env, path):
     return {"y": y, "s_final": sf, "ckpt": ck_out, **g, "dS_init": dS}, st_fwd, st_bwd
 
 
-@pytest.mark.parametrize("path", ["fp32", "split", "tc", "fused"])
+@pytest.mark.parametrize("path", ["fp32", "fp32-chunked", "split", "tc", "fused"])
 def test_a_cut_extent_is_reported_and_its_access_skipped(env, path):
     dbg = env[4]
     assert dbg.wkv7_status(_stream()) == 0

@@ -70,10 +70,12 @@ def _run_gpu(wkv7, t, s0, C, use_ckpt=True):
     return y, s_final, g
 
 
-def _full_parity(env, B, T, H, N, storage, s_init_std, C, seed=0, use_ckpt=True, zero_buffer=False):
+def _full_parity(env, B, T, H, N, storage, s_init_std, C, seed=0, use_ckpt=True, zero_buffer=False, edit=None):
     oracle, inputs, wkv7 = env
     dev = torch.device("cuda:0")
-    d = inputs.generate(B, T, H, N, storage, s_init_std, seed=seed)
+    d = dict(inputs.generate(B, T, H, N, storage, s_init_std, seed=seed))
+    if edit is not None:
+        edit(d)
     t = _upload(d, storage, dev)
     s0_np = _s_init_f32(d)
     if s0_np is None and zero_buffer:
@@ -129,8 +131,11 @@ def test_bf16_inputs(env, N):
     _full_parity(env, 2, 130, 3, N, "bf16", None, 8)
 
 
-def test_decay_zero_and_one(env):
-    """w = 0 (every step forgets) and w = 1 with a = b = 0 (pure accumulation)."""
+@pytest.mark.parametrize("C", [8, 16])
+def test_decay_zero_and_one(env, C):
+    """w = 0 (every step forgets) and w = 1 with a = b = 0 (pure accumulation);
+    C = 16 runs the chunked kernels (w = 0 leaves the scaled form's range:
+    every chunk step by step), C = 8 the scalar ones."""
     oracle, inputs, wkv7 = env
     dev = torch.device("cuda:0")
     B, T, H, N = 1, 33, 2, 64
@@ -146,7 +151,7 @@ def test_decay_zero_and_one(env):
         t = _upload(e, "f32", dev)
         s0_np = _s_init_f32(e)
         s0 = torch.from_numpy(s0_np).to(dev)
-        y, s_final, g = _run_gpu(wkv7, t, s0, 8)
+        y, s_final, g = _run_gpu(wkv7, t, s0, C)
         o = _oracle_inputs(inputs, e, "f32")
         y_ref, sf_ref = oracle.forward(*(o[n] for n in NAMES), s0_np.astype(np.float64))
         g_ref = oracle.backward(*(o[n] for n in NAMES), o["dy"], s0_np.astype(np.float64))
@@ -154,6 +159,30 @@ def test_decay_zero_and_one(env):
         _assert_close("s_final", s_final.cpu().numpy(), sf_ref, "f32", f" ({case})")
         for n in GRADS + ("dS_init",):
             _assert_close(n, g[n].cpu().numpy(), g_ref[n], "f32", f" ({case})")
+
+
+@pytest.mark.parametrize("B,T,H,C", [(1, 3, 2, 16), (1, 16, 1, 16), (2, 130, 3, 16), (1, 200, 2, 32)])
+def test_fp32_chunked_shapes(env, B, T, H, C):
+    """fp32 inputs at N = 64 with checkpoints on multiples of 16 steps: the
+    chunked forward in split tf32; the chunked backward (carry chain + per-chunk
+    output pass, split tf32) where the checkpoints come every 16 steps, the
+    scalar backward at C = 32. Shorter than a chunk, exactly one chunk, ragged
+    tails, carried state."""
+    _full_parity(env, B, T, H, 64, "f32", 0.3, C, seed=7 * T + B)
+
+
+def test_fp32_chunked_direct_form_chunks(env):
+    """Chunks whose decays leave the scaled form's range run step by step in
+    the chunked fp32 kernels: a whole chunk with w = 0 (head 0), one growing
+    column (w = 20, head 1), a zero decay in the last, partial chunk."""
+    def edit(d):
+        w = d["w"].copy()
+        w[0, 32:48, 0, :] = 0.0
+        w[0, 70, 1, 5] = 20.0
+        w[0, 99, 0, 63] = 0.0
+        d["w"] = w
+
+    _full_parity(env, 1, 100, 2, 64, "f32", 0.1, 16, seed=31, edit=edit)
 
 
 def test_empty_sequence(env):
