@@ -64,16 +64,27 @@ struct OpF {
   int pad_[3];
 };
 
+// A chunk's inputs: its rows, checkpoint and carry (two sets: the next task's arrive while
+// the current one is processed).
+struct InF32 {
+  float raw[7][kTile];   // r, w, k, v, a, b, dy of the chunk [t][j], zero past the sequence
+  float GcS[kN * kLDT];  // the carry after the chunk [i][j]; in the output phase, the dw exchange
+  float S0s[kN * kLDS];  // the checkpoint [i][j]
+};
+
 struct OutF32Smem {
-  float raw[7][kTile];  // r, w, k, v, a, b, dy of the chunk [t][j], zero past the sequence
+  InF32 in[2];
   OpF op;
   float U[3][kL * kLD16];                    // triu(V DSA^T, 1), triu(SA DY^T), triu(SA DSA^T, 1)
   float SAs[kL * kLD64], DSAs[kL * kLD64];  // sa(t), dsa(t) [t][i]
-  float GcS[kN * kLDT];                     // the carry after the chunk [i][j]
-  float S0s[kN * kLDS];                     // the checkpoint [i][j]
   float Epart[4][kN];                       // colsum(Gc o S0) over each state warp's rows
   float anc[2][kN];                         // colsum(R^ o DY S0 + A^ o DSA S0), colsum(Kb o V Gc + Bb o SA Gc)
 };
+
+template <int N>
+__device__ __forceinline__ void cp_async_wait_group() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
 
 __device__ __forceinline__ float quad_sum(float x) {
   x += __shfl_xor_sync(0xffffffffu, x, 1);
@@ -174,10 +185,10 @@ __device__ __forceinline__ void store_masked(const float (&acc)[2][4], float* ds
 }
 
 // Warps 4..7: the operands, the masked L x L products, T and triu(V DY^T).
-__device__ void front_f32(OutF32Smem& sm, int len) {
+__device__ void front_f32(OutF32Smem& sm, const InF32& in, int len) {
   const int ptid = threadIdx.x - 128, pw = ptid >> 5, lane = threadIdx.x & 31, g = lane >> 2, t4 = lane & 3;
   OpF& op = sm.op;
-  const bool unsafe = prep_f32(&sm.raw[0][0], op, len, ptid);
+  const bool unsafe = prep_f32(&in.raw[0][0], op, len, ptid);
   if (ptid == 0) op.unsafe = unsafe;
   if (unsafe) return;
   named_bar(1, 128);
@@ -236,11 +247,12 @@ __device__ __forceinline__ void put(const BwdArgs& a, float* dst, const Extent& 
 
 // Step-by-step reverse scan of the chunk (warps 0..3, fp32): the carry G
 // starts at Gc, S_prev of step t is recomputed from the checkpoint.
-__device__ void direct_f32(OutF32Smem& sm, int len, const OutPtrs& o, float (&G)[8][4], int warp, int lane) {
+__device__ void direct_f32(OutF32Smem& sm, const InF32& in, int len, const OutPtrs& o, float (&G)[8][4], int warp,
+                           int lane) {
   const BwdArgs& a = *o.a;
   const int g = lane >> 2, t4 = lane & 3, i0 = 16 * warp, tid = threadIdx.x;
-  const float* rs = &sm.raw[0][0];
-  const float* S0 = sm.S0s;
+  const float* rs = &in.raw[0][0];
+  const float* S0 = in.S0s;
   float* red = sm.SAs;  // [4 warps][5][64], in SAs and DSAs (unused by a direct chunk)
   for (int t = len - 1; t >= 0; --t) {
     float sp[8][4];
@@ -346,7 +358,8 @@ __device__ void direct_f32(OutF32Smem& sm, int len, const OutPtrs& o, float (&G)
 }
 
 // Warps 0..3: SA, DSA (to shared memory) and dv of the chunk (rows i0 .. i0+15).
-__device__ void state_f32(OutF32Smem& sm, const float (&G)[8][4], int len, const OutPtrs& o, int warp, int lane) {
+__device__ void state_f32(OutF32Smem& sm, const InF32& in, const float (&G)[8][4], int len, const OutPtrs& o, int warp,
+                          int lane) {
   const BwdArgs& a = *o.a;
   const int g = lane >> 2, t4 = lane & 3, i0 = 16 * warp;
   const OpF& op = sm.op;
@@ -360,7 +373,7 @@ __device__ void state_f32(OutF32Smem& sm, const float (&G)[8][4], int len, const
 #pragma unroll
   for (int kb = 0; kb < 8; ++kb) {
     FragA<true> aS, aG;
-    ld_a(aS, sm.S0s, kLDS, i0, 8 * kb, g, t4);
+    ld_a(aS, in.S0s, kLDS, i0, 8 * kb, g, t4);
     acc_to_a(aG, G[kb]);
 #pragma unroll
     for (int q = 0; q < 2; ++q) {
@@ -445,7 +458,7 @@ __device__ void state_f32(OutF32Smem& sm, const float (&G)[8][4], int len, const
 
 // All eight warps: dk, db (warps 0..3), dr, da (warps 4..7) and dw. Warp
 // (grp, jb) covers columns j0 .. j0+15, j0 = 16 jb.
-__device__ void outputs_f32(OutF32Smem& sm, int len, const OutPtrs& o) {
+__device__ void outputs_f32(OutF32Smem& sm, InF32& in, int len, const OutPtrs& o) {
   const BwdArgs& a = *o.a;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, g = lane >> 2, t4 = lane & 3;
   const int grp = warp >> 2, jb = warp & 3, j0 = 16 * jb;
@@ -462,7 +475,7 @@ __device__ void outputs_f32(OutF32Smem& sm, int len, const OutPtrs& o) {
     zero4(P0[nt]);
     zero4(P1[nt]);
   }
-  const float* Bm = grp ? sm.S0s : sm.GcS;
+  const float* Bm = grp ? in.S0s : in.GcS;
   const int ldb = grp ? kLDS : kLDT;
 #pragma unroll
   for (int kb = 0; kb < 8; ++kb) {
@@ -553,7 +566,7 @@ __device__ void outputs_f32(OutF32Smem& sm, int len, const OutPtrs& o) {
   }
   // unscale: dk = dk~ / c, db = db~ / c (grp 0); dr = dr^ c, da = da^ c(t-1) (grp 1); and this
   // group's part of x = r dr - k dk - b db + a da
-  const float* rs = &sm.raw[0][0];
+  const float* rs = &in.raw[0][0];
   float X[2][4], AD[2][4];
 #pragma unroll
   for (int nt = 0; nt < 2; ++nt)
@@ -586,9 +599,9 @@ __device__ void outputs_f32(OutF32Smem& sm, int len, const OutPtrs& o) {
     }
   // exchange with the partner warp of the other group (same columns): grp 0 keeps dw of
   // n-tile 0, grp 1 of n-tile 1. The carry tile is free in this phase.
-  float* XK = sm.GcS;                   // grp 0's x part, [t][j] stride 72
-  float* XR = sm.GcS + kL * kLD64;      // grp 1's x part
-  float* XA = sm.GcS + 2 * kL * kLD64;  // grp 1's a da
+  float* XK = in.GcS;                   // grp 0's x part, [t][j] stride 72
+  float* XR = in.GcS + kL * kLD64;      // grp 1's x part
+  float* XA = in.GcS + 2 * kL * kLD64;  // grp 1's a da
 #pragma unroll
   for (int h = 0; h < 2; ++h) {
     const int t = g + 8 * h;
@@ -668,47 +681,59 @@ __global__ void __launch_bounds__(kThreads, 1) wkv7_bwd4_out_f32_kernel(const __
   const int T = args.T, H = args.H, nchunks = (T + kL - 1) / kL;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, g = lane >> 2, t4 = lane & 3;
   const size_t vstep = (size_t)H * kN;
-  for (long long task = blockIdx.x; task < ntasks; task += gridDim.x) {
+  // The rows (zeros past T), checkpoint and carry of `task` into input set `in`, as one
+  // cp.async group (empty past the last task).
+  auto load = [&](InF32& in, long long task) {
+    if (task < ntasks) {
+      const int head = (int)(task / nchunks), n = (int)(task % nchunks), bi = head / H, hi = head % H;
+      const int t0 = n * kL, len = min(kL, T - t0);
+      const size_t base = ((size_t)bi * T + t0) * vstep + (size_t)hi * kN;
+      const float* S0g = args.ckpt + ((size_t)head * args.nck + n) * kN * kN;
+      const float* Gcg = reinterpret_cast<const float*>(args.carry) + ((size_t)head * nchunks + n) * kN * kN;
+      for (int idx = tid; idx < 7 * kL * (kN / 4); idx += kThreads) {
+        const int v = idx / (kL * kN / 4), t = (idx / (kN / 4)) % kL, c4 = idx % (kN / 4);
+        float* dst = &in.raw[v][t * kN + 4 * c4];
+        const float* src = static_cast<const float*>(args.in[v]) + base + (size_t)t * vstep + 4 * c4;
+        if (t < len && in_extent(args.status, args.ext.in[v], reinterpret_cast<const float4*>(src)))
+          cp_async16(dst, src);
+        else
+          *reinterpret_cast<float4*>(dst) = make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+#pragma unroll
+      for (int q = 0; q < kN * kN / 4 / kThreads; ++q) {
+        const int idx = tid + kThreads * q, r = idx >> 4, c4 = idx & 15;  // row r, columns 4 c4 ..
+        if (in_extent(args.status, args.ext.ckpt, reinterpret_cast<const float4*>(S0g + 4 * idx)))
+          cp_async16(in.S0s + r * kLDS + 4 * c4, S0g + 4 * idx);
+        if (in_extent(args.status, args.ext.carry, reinterpret_cast<const float4*>(Gcg + 4 * idx)))
+          cp_async16(in.GcS + r * kLDT + 4 * c4, Gcg + 4 * idx);
+      }
+    }
+    cp_async_commit();
+  };
+  load(sm.in[0], blockIdx.x);
+  int cur = 0;
+  for (long long task = blockIdx.x; task < ntasks; task += gridDim.x, cur ^= 1) {
     const int head = (int)(task / nchunks), n = (int)(task % nchunks), bi = head / H, hi = head % H;
     const int t0 = n * kL, len = min(kL, T - t0);
     const OutPtrs o{&args, ((size_t)bi * T + t0) * vstep + (size_t)hi * kN, vstep};
-    const float* S0g = args.ckpt + ((size_t)head * args.nck + n) * kN * kN;
-    const float* Gcg = reinterpret_cast<const float*>(args.carry) + ((size_t)head * nchunks + n) * kN * kN;
-    __syncthreads();  // the previous task is done with shared memory
-    // ---- loads: the chunk's rows (zeros past T), the checkpoint and the carry
-    for (int idx = tid; idx < 7 * kL * (kN / 4); idx += kThreads) {
-      const int v = idx / (kL * kN / 4), t = (idx / (kN / 4)) % kL, c4 = idx % (kN / 4);
-      float* dst = &sm.raw[v][t * kN + 4 * c4];
-      const float* src = static_cast<const float*>(args.in[v]) + o.base + (size_t)t * vstep + 4 * c4;
-      if (t < len && in_extent(args.status, args.ext.in[v], reinterpret_cast<const float4*>(src)))
-        cp_async16(dst, src);
-      else
-        *reinterpret_cast<float4*>(dst) = make_float4(0.f, 0.f, 0.f, 0.f);
-    }
-#pragma unroll
-    for (int q = 0; q < kN * kN / 4 / kThreads; ++q) {
-      const int idx = tid + kThreads * q, r = idx >> 4, c4 = idx & 15;  // row r, columns 4 c4 ..
-      if (in_extent(args.status, args.ext.ckpt, reinterpret_cast<const float4*>(S0g + 4 * idx)))
-        cp_async16(sm.S0s + r * kLDS + 4 * c4, S0g + 4 * idx);
-      if (in_extent(args.status, args.ext.carry, reinterpret_cast<const float4*>(Gcg + 4 * idx)))
-        cp_async16(sm.GcS + r * kLDT + 4 * c4, Gcg + 4 * idx);
-    }
-    cp_async_commit();
-    cp_async_wait_all();
+    InF32& in = sm.in[cur];
+    __syncthreads();  // the previous task is done with shared memory (and its input set)
+    load(sm.in[cur ^ 1], task + gridDim.x);  // the next task's inputs, while this one runs
+    cp_async_wait_group<1>();                // this task's group complete
     __syncthreads();
 
     // ---- warps 4..7: operands and products; warps 0..3: the carry into registers and
     //      colsum(Gc o S0) over their rows
     float G[8][4];
     if (warp >= 4) {
-      front_f32(sm, len);
+      front_f32(sm, in, len);
     } else {
       const int i0 = 16 * warp;
 #pragma unroll
       for (int nt = 0; nt < 8; ++nt) {
         const int col = 8 * nt + 2 * t4;
-        const float2 lo = f2at(sm.GcS + (i0 + g) * kLDT + col), hi = f2at(sm.GcS + (i0 + g + 8) * kLDT + col);
-        const float2 s_lo = f2at(sm.S0s + (i0 + g) * kLDS + col), s_hi = f2at(sm.S0s + (i0 + g + 8) * kLDS + col);
+        const float2 lo = f2at(in.GcS + (i0 + g) * kLDT + col), hi = f2at(in.GcS + (i0 + g + 8) * kLDT + col);
+        const float2 s_lo = f2at(in.S0s + (i0 + g) * kLDS + col), s_hi = f2at(in.S0s + (i0 + g + 8) * kLDS + col);
         G[nt][0] = lo.x;
         G[nt][1] = lo.y;
         G[nt][2] = hi.x;
@@ -723,14 +748,15 @@ __global__ void __launch_bounds__(kThreads, 1) wkv7_bwd4_out_f32_kernel(const __
     // ---- warps 0..3: SA, DSA and dv (or the whole chunk step by step)
     if (warp < 4) {
       if (unsafe)
-        direct_f32(sm, len, o, G, warp, lane);
+        direct_f32(sm, in, len, o, G, warp, lane);
       else
-        state_f32(sm, G, len, o, warp, lane);
+        state_f32(sm, in, G, len, o, warp, lane);
     }
     __syncthreads();
     // ---- all warps: dk, db, dr, da, dw
-    if (!unsafe) outputs_f32(sm, len, o);
+    if (!unsafe) outputs_f32(sm, in, len, o);
   }
+  cp_async_wait_all();  // the trailing (empty) group
 }
 
 }  // namespace
