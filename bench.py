@@ -509,11 +509,12 @@ def _report(args, wl, world, B, T, H, N, C, bf16, ms, fwd_ms, bwd_ms, e2e, ckpt,
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16" if (bf16 and N == 64) else "f32", "data": "synthetic",
-        "arithmetic": ("tensor-core products with fp32 accumulation: tf32 operands in the forward and the backward's "
-                       "carry chain (the fp32 state and carry rounded to tf32 where they enter a product), bf16 "
-                       "operands in the backward's per-chunk gradient products (the carry stored as bf16 between "
-                       "the two backward kernels, the fp32 checkpoint rounded to bf16 there); fp32 accumulation, "
-                       "state and element-wise math" if chunked else
+        "arithmetic": ("tensor-core products with fp32 accumulation: bf16 operands in the forward (the fp32 state "
+                       "rounded to bf16 where it enters a product; the state update's scaled k and b as bf16 hi + lo "
+                       "pairs), tf32 operands in the backward's carry chain (the fp32 carry rounded to tf32 where it "
+                       "enters a product), bf16 operands in the backward's per-chunk gradient products (the carry "
+                       "stored as bf16 between the two backward kernels, the fp32 checkpoint rounded to bf16 "
+                       "there); fp32 accumulation, state and element-wise math" if chunked else
                        ("tensor-core products in split tf32 in the forward, the backward's carry chain and its "
                         "per-chunk output pass (three tf32 products per fp32 product, fp32 accumulation); the "
                         "state, the carried gradient (stored as fp32 between the two backward kernels) and "

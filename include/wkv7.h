@@ -84,11 +84,14 @@ int wkv7_forward(const float* r, const float* w, const float* k, const float* v,
  * s_final and the checkpoints are fp32 in memory.
  * Arithmetic. At N = 64 with checkpoints every multiple of 16 steps (or none)
  * the chunked tensor-core form runs: every product is a tensor-core product
- * with tf32 operands (10-bit mantissa) and fp32 accumulation, and the carried
- * state, held and decayed in fp32, is rounded to tf32 where it enters one;
- * the element-wise work (decay products, the triangular solve) is fp32. The
- * bfloat16 y is rounded once from the fp32 result. Other N or checkpoint
- * intervals run fp32 FMA throughout. */
+ * with bfloat16 operands (the inputs' own precision) and fp32 accumulation.
+ * The scaled operands and the carried state (held and decayed in fp32) are
+ * rounded to bfloat16 where they enter a product, except that the state
+ * update takes its two scaled operands (k and b times the decay products) as
+ * bfloat16 pairs hi + lo, about 16 bits, so that the carried state keeps
+ * them at that precision. The element-wise work (decay products, the
+ * triangular solve) is fp32. The bfloat16 y is rounded once from the fp32
+ * result. Other N or checkpoint intervals run fp32 FMA throughout. */
 int wkv7_forward_bf16(const wkv7_bf16* r, const wkv7_bf16* w, const wkv7_bf16* k, const wkv7_bf16* v,
                       const wkv7_bf16* a, const wkv7_bf16* b, const float* s_init, wkv7_bf16* y,
                       float* s_final, float* ckpt, int ckpt_every, int B, int T, int H, int N,

@@ -48,6 +48,7 @@
 #include "wkv7_decay.cuh"
 #include "wkv7_launch.h"
 #include "wkv7_mma.cuh"
+#include "wkv7_mma16.cuh"
 #include "wkv7_scaled.cuh"
 #include "wkv7_tmem.cuh"
 
@@ -83,104 +84,6 @@ template <bool kX3>
 __device__ __forceinline__ float2 op_val2(float2 x) {
   return make_float2(op_val<kX3>(x.x), op_val<kX3>(x.y));
 }
-
-// ----------------------------------------------------------- bf16 operands ---
-
-constexpr int kB64 = 72;  // row stride (bf16 elements) of 64-wide tiles
-constexpr int kB16 = 24;  // row stride of 16-wide tiles
-typedef __nv_bfloat16 bf16_t;
-
-__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
-  uint32_t r;
-  asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
-  return r;
-}
-__device__ __forceinline__ float2 unpack_bf16(uint32_t u) {
-  return make_float2(__uint_as_float(u << 16), __uint_as_float(u & 0xFFFF0000u));
-}
-__device__ __forceinline__ void st_pair(bf16_t* p, float2 x) { *reinterpret_cast<uint32_t*>(p) = pack_bf16(x.x, x.y); }
-
-// d += a * b for one 16 x 8 x 16 tile (bf16 inputs, fp32 accumulation).
-__device__ __forceinline__ void mma16(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
-  asm("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
-      "{%0,%1,%2,%3};\n"
-      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
-}
-__device__ __forceinline__ void ldsm4(uint32_t (&r)[4], const bf16_t* p) {
-  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
-               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
-               : "r"(smem_addr(p)));
-}
-__device__ __forceinline__ void ldsm4t(uint32_t (&r)[4], const bf16_t* p) {
-  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
-               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
-               : "r"(smem_addr(p)));
-}
-__device__ __forceinline__ void stsm4t(bf16_t* p, const uint32_t (&r)[4]) {
-  asm volatile("stmatrix.sync.aligned.m8n8.x4.trans.shared.b16 [%0], {%1,%2,%3,%4};" ::"r"(smem_addr(p)), "r"(r[0]),
-               "r"(r[1]), "r"(r[2]), "r"(r[3])
-               : "memory");
-}
-
-// Fragment loads for one k16 block. "A" is 16 rows (m) x 16 k, "B" two n8
-// tiles x 16 k (r[0], r[1] for columns n0 .. n0+7, r[2], r[3] for n0+8 ..).
-// Storage is row-major with stride ld; the suffix says how it is laid out:
-//   a_mk: A[m][k] stored [m][k];  a_km: stored [k][m] (transposed load)
-//   b_nk: B^T[n][k] stored [n][k]; b_kn: B[k][n] stored [k][n] (transposed load)
-__device__ __forceinline__ void a_mk(uint32_t (&r)[4], const bf16_t* s, int ld, int m0, int k0, int lane) {
-  ldsm4(r, s + (m0 + (lane & 7) + ((lane >> 3) & 1) * 8) * ld + k0 + (lane >> 4) * 8);
-}
-__device__ __forceinline__ void a_km(uint32_t (&r)[4], const bf16_t* s, int ld, int m0, int k0, int lane) {
-  ldsm4t(r, s + (k0 + (lane & 7) + (lane >> 4) * 8) * ld + m0 + ((lane >> 3) & 1) * 8);
-}
-__device__ __forceinline__ void b_nk(uint32_t (&r)[4], const bf16_t* s, int ld, int n0, int k0, int lane) {
-  ldsm4(r, s + (n0 + (lane & 7) + (lane >> 4) * 8) * ld + k0 + ((lane >> 3) & 1) * 8);
-}
-__device__ __forceinline__ void b_kn(uint32_t (&r)[4], const bf16_t* s, int ld, int n0, int k0, int lane) {
-  ldsm4t(r, s + (k0 + (lane & 7) + ((lane >> 3) & 1) * 8) * ld + n0 + (lane >> 4) * 8);
-}
-// Two accumulator tiles (columns k0 .. k0+7 and k0+8 .. k0+15 of 16 rows) as
-// the A fragment of a product over those 16 columns.
-__device__ __forceinline__ void c2a16(uint32_t (&a)[4], const float (&lo)[4], const float (&hi)[4]) {
-  a[0] = pack_bf16(lo[0], lo[1]);
-  a[1] = pack_bf16(lo[2], lo[3]);
-  a[2] = pack_bf16(hi[0], hi[1]);
-  a[3] = pack_bf16(hi[2], hi[3]);
-}
-// acc[nt] += A B over K = 16 * KB for two n8 tiles, A from [m][k], B from [n][k].
-template <int KB>
-__device__ __forceinline__ void mm_mk_nk(float (&acc)[2][4], const bf16_t* A, int lda, int m0, const bf16_t* Bt, int ldb,
-                                         int n0, int lane) {
-#pragma unroll
-  for (int kb = 0; kb < KB; ++kb) {
-    uint32_t a[4], b[4];
-    a_mk(a, A, lda, m0, 16 * kb, lane);
-    b_nk(b, Bt, ldb, n0, 16 * kb, lane);
-    mma16(acc[0], a, b[0], b[1]);
-    mma16(acc[1], a, b[2], b[3]);
-  }
-}
-// Store a 16 x 16 fp32 accumulator (tiles acc[0], acc[1]) as bf16 [t][s],
-// keeping lower: s < t (+ diagonal if incl), upper: s > t (+ diagonal if incl).
-__device__ __forceinline__ void store_masked16(const float (&acc)[2][4], bf16_t* dst, bool lower, bool incl, int g,
-                                               int t4) {
-#pragma unroll
-  for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-    for (int h = 0; h < 2; ++h) {
-      const int t = g + 8 * h, s = 8 * nt + 2 * t4;
-      float x[2];
-#pragma unroll
-      for (int e = 0; e < 2; ++e) {
-        const int se = s + e;
-        const bool keep = lower ? (se < t || (incl && se == t)) : (se > t || (incl && se == t));
-        x[e] = keep ? acc[nt][2 * h + e] : 0.f;
-      }
-      st_pair(dst + t * kB16 + s, make_float2(x[0], x[1]));
-    }
-}
-
 
 // T = (I - M)^-1 for a strictly lower 16 x 16 M (stride kLD16) by forward
 // substitution, one warp; lane s < 16 owns column s. Writes T (row-major)

@@ -13,11 +13,12 @@
 //   Y   = R^ S0^T + Mkr V + Mbr SA                   rows: y(t)
 //   S(L) = S0 diag(c(L)) + V^T Kb + SA^T Bb
 // (exact up to rounding; the reverse scan uses the same algebra). The
-// products run on tf32 tensor cores with fp32 accumulation; the state stays
-// fp32 in registers. With bf16 inputs each product is one tf32 product (the
-// operands rounded to tf32 once); with fp32 inputs each is taken in split
-// tf32, three tf32 products (wkv7_mma.cuh, mma_x), so the result keeps fp32
-// accuracy.
+// products run on tensor cores with fp32 accumulation; the state stays fp32
+// in registers. With bf16 inputs the products take bf16 operands (mma.sync
+// m16n8k16, wkv7_mma16.cuh): the inputs' own precision, the scaled operands
+// and the state rounded to bf16 as they enter a product. With fp32 inputs
+// each product is taken in split tf32, three tf32 products (wkv7_mma.cuh,
+// mma_x), so the result keeps fp32 accuracy.
 //
 // One CTA per (b, h), twelve warps in three groups working one chunk apart:
 //  - forming warps (4..7) turn chunk n+2's r, w, k, v, a, b (TMA tensor loads
@@ -35,6 +36,7 @@
 #include "wkv7_decay.cuh"
 #include "wkv7_launch.h"
 #include "wkv7_mma.cuh"
+#include "wkv7_mma16.cuh"
 #include "wkv7_scaled.cuh"
 
 namespace wkv7 {
@@ -44,7 +46,7 @@ constexpr int kN = 64, kL = 16;
 constexpr int kLD64 = 72;  // row stride (floats) of 64-wide operands: conflict-free fragment loads
 constexpr int kLD16 = 24;  // row stride of 16-wide operands
 
-// Operand block of one chunk (tf32 values for bf16 inputs, fp32 for fp32 inputs, unless noted).
+// Operand block of one chunk for fp32 inputs (fp32 values, split as they enter a product).
 struct Prep3 {
   float X1[2 * kL * kLD64];  // rows 0..15: a^(t); rows 16..31: r^(t)   [t][j]
   float VT[kN * kLD16];      // v(s)[i]                                   [i][s]
@@ -58,28 +60,57 @@ struct Prep3 {
   int pad_[31];
 };
 
-// Input ring depth and checkpoint staging per input type.
+// Operand block of one chunk for bf16 inputs (bf16 operands; row strides of 72 and 24
+// elements put the eight 16-byte rows of every ldmatrix on distinct banks).
+struct alignas(16) Prep16 {
+  bf16_t X1[2 * kL * kB64];  // rows 0..15: a^(t); rows 16..31: r^(t)   [t][j]
+  bf16_t VT[kN * kB16];      // v(s)[i]                                   [i][s]
+  // k(s)[j] c(L)[j] / c(s)[j] and b(s)[j] c(L)[j] / c(s)[j], each as a bf16 pair hi + lo
+  // ([0] = hi, the value rounded to bf16; [1] = lo, the remainder rounded to bf16): the
+  // state update takes them at about 16 bits, the rest of the chunk at the inputs' 8
+  bf16_t KbT[2][kN * kB16];  // [j][s]
+  bf16_t BbT[2][kN * kB16];  // [j][s]
+  bf16_t M[3][kL * kB16];    // Mka (strictly lower), Mkr, Mbr (lower)    [t][s]
+  bf16_t Tinv[kL * kB16];    // (I - Mba)^-1                              [t][s]
+  float Mba[kL * kLD16];     // Mba (strictly lower, fp32: T is formed from it)
+  float cL[kN];              // c(L) (fp32)
+  float ph[2][kN];           // decay logits: product of each half's 8 decays
+  int unsafe;
+  int pad_[31];
+};
+
+// Per input type: input ring depth, checkpoint staging, operand block and operand type,
+// and the row strides of the k~/b~ block and of the staged y rows.
 template <typename TIn>
 struct Fwd3Io;
 template <>
 struct Fwd3Io<__nv_bfloat16> {
   static constexpr int kStages = 4;
   static constexpr bool kStageCk = true;
+  using Prep = Prep16;
+  using Op = bf16_t;
+  static constexpr int kLDX = kB64;
+  static constexpr int kYS = kB64;  // padded: the transposed matrix stores of y hit distinct banks
 };
 template <>
 struct Fwd3Io<float> {
   static constexpr int kStages = 3;
   static constexpr bool kStageCk = false;
+  using Prep = Prep3;
+  using Op = float;
+  static constexpr int kLDX = kLD64;
+  static constexpr int kYS = kN;
 };
 
 template <typename TIn>
 struct Fwd3Smem {
-  static constexpr int kStages = Fwd3Io<TIn>::kStages;
-  static constexpr bool kStageCk = Fwd3Io<TIn>::kStageCk;
+  using Io = Fwd3Io<TIn>;
+  static constexpr int kStages = Io::kStages;
+  static constexpr bool kStageCk = Io::kStageCk;
   TIn raw[kStages][6][kL * kN];  // TMA ring: r, w, k, v, a, b of one chunk per stage
-  Prep3 prep[3];
-  float X2[2][2 * kL * kLD64];  // per chunk in flight: rows 0..15: k~(s); rows 16..31: b~(s)   [s][j]
-  TIn ys[2][kL * kN];  // y of the chunk [t][i], on its way out (state warps write, products warps store)
+  typename Io::Prep prep[3];
+  typename Io::Op X2[2][2 * kL * Io::kLDX];  // per chunk in flight: rows 0..15: k~(s); rows 16..31: b~(s)   [s][j]
+  TIn ys[2][kL * Io::kYS];  // y of the chunk [t][i], on its way out (state warps write, products warps store)
   // epilogue: the head's ln_w, ln_b, r_k; per chunk (ring of 4, written by the forming
   // group two rounds before the state warps run the chunk, read by the products group the
   // round after) the bonus partials of the two 32-column halves and the v rows
@@ -119,8 +150,9 @@ __device__ __forceinline__ float op_val(float x) {
 // 128 threads; thread (j = ptid % 64, half = ptid / 64) forms column j of
 // steps 8*half .. 8*half+7.
 template <typename TIn, bool kLogit, bool kEpi>
-__device__ void form_chunk(Fwd3Smem<TIn>& sm, Prep3& P, float* X2, int stage, int len, int ptid, int eslot) {
-  constexpr bool kX3 = kSplitOf<TIn>;
+__device__ void form_chunk(Fwd3Smem<TIn>& sm, typename Fwd3Io<TIn>::Prep& P, typename Fwd3Io<TIn>::Op* X2, int stage,
+                           int len, int ptid, int eslot) {
+  constexpr bool kX3 = kSplitOf<TIn>;  // fp32 inputs: fp32 operands; bf16 inputs: bf16 operands
   const TIn* rs = sm.raw[stage][0];
   const int j = ptid & 63, half = ptid >> 6;
   // decays of this thread's 8 steps (wm) and of the other 8 (wo); padding
@@ -140,7 +172,7 @@ __device__ void form_chunk(Fwd3Smem<TIn>& sm, Prep3& P, float* X2, int stage, in
     rv[e] = bf(rs + V_R * kL * kN + o);
     kv[e] = bf(rs + V_K * kL * kN + o);
     bv[e] = bf(rs + V_B * kL * kN + o);
-    vt[e] = bf(rs + V_V * kL * kN + o);  // bf16 values are tf32 values; fp32 values stay fp32
+    vt[e] = bf(rs + V_V * kL * kN + o);
   }
   if constexpr (kEpi) {
     // the epilogue's bonus sum_j r_j k_j r_k[j] of each step, over this warp's 32 columns,
@@ -191,22 +223,48 @@ __device__ void form_chunk(Fwd3Smem<TIn>& sm, Prep3& P, float* X2, int stage, in
     const float cprev = c;
     c *= wm[e];
     const float ic = rcp_approx(c);
-    const int o = t * kN + j;
     const float a = av[e], r = rv[e], k = kv[e], b = bv[e];
-    X2[t * kLD64 + j] = op_val<kX3>(k * ic);
-    X2[(kL + t) * kLD64 + j] = op_val<kX3>(b * ic);
-    P.X1[t * kLD64 + j] = op_val<kX3>(a * cprev);
-    P.X1[(kL + t) * kLD64 + j] = op_val<kX3>(r * c);
+    if constexpr (kX3) {
+      X2[t * kLD64 + j] = k * ic;
+      X2[(kL + t) * kLD64 + j] = b * ic;
+      P.X1[t * kLD64 + j] = a * cprev;
+      P.X1[(kL + t) * kLD64 + j] = r * c;
+    } else {
+      X2[t * kB64 + j] = __float2bfloat16_rn(k * ic);
+      X2[(kL + t) * kB64 + j] = __float2bfloat16_rn(b * ic);
+      P.X1[t * kB64 + j] = __float2bfloat16_rn(a * cprev);
+      P.X1[(kL + t) * kB64 + j] = __float2bfloat16_rn(r * c);
+    }
     const float s = cL * ic;
-    kbt[e] = op_val<kX3>(k * s);
-    bbt[e] = op_val<kX3>(b * s);
+    kbt[e] = k * s;
+    bbt[e] = b * s;
   }
+  if constexpr (kX3) {
 #pragma unroll
-  for (int q = 0; q < 2; ++q) {
-    const int o = j * kLD16 + 8 * half + 4 * q;
-    *reinterpret_cast<float4*>(P.VT + o) = make_float4(vt[4 * q], vt[4 * q + 1], vt[4 * q + 2], vt[4 * q + 3]);
-    *reinterpret_cast<float4*>(P.KbT + o) = make_float4(kbt[4 * q], kbt[4 * q + 1], kbt[4 * q + 2], kbt[4 * q + 3]);
-    *reinterpret_cast<float4*>(P.BbT + o) = make_float4(bbt[4 * q], bbt[4 * q + 1], bbt[4 * q + 2], bbt[4 * q + 3]);
+    for (int q = 0; q < 2; ++q) {
+      const int o = j * kLD16 + 8 * half + 4 * q;
+      *reinterpret_cast<float4*>(P.VT + o) = make_float4(vt[4 * q], vt[4 * q + 1], vt[4 * q + 2], vt[4 * q + 3]);
+      *reinterpret_cast<float4*>(P.KbT + o) = make_float4(kbt[4 * q], kbt[4 * q + 1], kbt[4 * q + 2], kbt[4 * q + 3]);
+      *reinterpret_cast<float4*>(P.BbT + o) = make_float4(bbt[4 * q], bbt[4 * q + 1], bbt[4 * q + 2], bbt[4 * q + 3]);
+    }
+  } else {
+    // eight steps of column j: one 16-byte row piece of each transposed block (v is bf16
+    // already; kb and bb as hi and lo parts)
+    auto pack8 = [](const float (&x)[8]) {
+      return make_uint4(pack_bf16(x[0], x[1]), pack_bf16(x[2], x[3]), pack_bf16(x[4], x[5]), pack_bf16(x[6], x[7]));
+    };
+    auto lo8 = [](float (&x)[8]) {  // x <- x - bf16(x), exact in fp32
+#pragma unroll
+      for (int e = 0; e < 8; ++e) x[e] -= __bfloat162float(__float2bfloat16_rn(x[e]));
+    };
+    const int o = j * kB16 + 8 * half;
+    *reinterpret_cast<uint4*>(P.VT + o) = pack8(vt);
+    *reinterpret_cast<uint4*>(P.KbT[0] + o) = pack8(kbt);
+    *reinterpret_cast<uint4*>(P.BbT[0] + o) = pack8(bbt);
+    lo8(kbt);
+    lo8(bbt);
+    *reinterpret_cast<uint4*>(P.KbT[1] + o) = pack8(kbt);
+    *reinterpret_cast<uint4*>(P.BbT[1] + o) = pack8(bbt);
   }
   unsafe = named_bar_or(1, 128, unsafe);
   if (ptid == 0) P.unsafe = unsafe;
@@ -268,6 +326,45 @@ __device__ void gram_chunk(Prep3& P, const float* X2, int gtid) {
   }
 }
 
+// The same for bf16 operands: the Gram blocks from bf16 operands (K = 64 in four k16
+// steps), Mka, Mkr, Mbr stored as bf16, Mba kept in fp32 for T, T stored as bf16.
+__device__ void gram_chunk16(Prep16& P, const bf16_t* X2, int gtid) {
+  const int pw = gtid >> 5, lane = gtid & 31, g = lane >> 2, t4 = lane & 3;
+  const int mt = pw >> 1, nb = pw & 1;
+  float acc[2][4];
+  zero4(acc[0]);
+  zero4(acc[1]);
+  mm_mk_nk<4>(acc, P.X1, kB64, 16 * mt, X2, kB64, 16 * nb, lane);
+  if (pw != 1) {
+    // pw 0: Mka (s < t); 2: Mkr, 3: Mbr (s <= t)
+    store_masked16(acc, P.M[pw == 0 ? 0 : pw - 1], true, pw >= 2, g, t4);
+    return;
+  }
+#pragma unroll
+  for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const int tt = g + 8 * h, s = 8 * nt + 2 * t4;
+      *reinterpret_cast<float2*>(P.Mba + tt * kLD16 + s) =
+          make_float2(s < tt ? acc[nt][2 * h] : 0.f, s + 1 < tt ? acc[nt][2 * h + 1] : 0.f);
+    }
+  __syncwarp();
+  // T = (I - Mba)^-1 by forward substitution in fp32; lane s (< 16) owns column s
+  const int s = lane & 15;
+  float col[kL];
+#pragma unroll
+  for (int tt = 0; tt < kL; ++tt) {
+    float x = tt == s ? 1.f : 0.f;
+#pragma unroll
+    for (int u = 0; u < tt; ++u) x = fmaf(P.Mba[tt * kLD16 + u], col[u], x);
+    col[tt] = x;
+  }
+  if (lane < 16) {
+#pragma unroll
+    for (int tt = 0; tt < kL; ++tt) P.Tinv[tt * kB16 + s] = __float2bfloat16_rn(col[tt]);
+  }
+}
+
 // ----------------------------------------------------------- state warps ---
 
 struct StateCtx {
@@ -297,13 +394,13 @@ __device__ __forceinline__ void flush_state(const float* src, float* dst, int pt
   }
 }
 
-// A chunk's staged y rows ([t][i] bf16) to global memory: 128 threads, 16 rows x 8 pieces of
-// 16 bytes, rows past the end of the sequence skipped.
+// A chunk's staged y rows ([t][i] bf16, row stride kB64) to global memory: 128 threads, 16
+// rows x 8 pieces of 16 bytes, rows past the end of the sequence skipped.
 __device__ __forceinline__ void flush_y(const __nv_bfloat16* src, __nv_bfloat16* dst, size_t vstep, int len, int ptid,
                                         const Extent& x, unsigned* status) {
   const int row = ptid >> 3, piece = ptid & 7;
   uint4* p = reinterpret_cast<uint4*>(dst + (size_t)row * vstep + 8 * piece);
-  if (row < len && in_extent(status, x, p)) *p = *reinterpret_cast<const uint4*>(src + row * kN + 8 * piece);
+  if (row < len && in_extent(status, x, p)) *p = *reinterpret_cast<const uint4*>(src + row * kB64 + 8 * piece);
 }
 
 // The same for fp32 rows: 16 rows x 8 pieces of 32 bytes.
@@ -329,6 +426,7 @@ __device__ __forceinline__ void store_state(const StateCtx& c, float* dst, const
 }
 
 // Chunk on tensor cores. Writes the chunk's y into ys.
+// (fp32 inputs: every product in split tf32)
 template <typename TIn>
 __device__ void state_chunk(StateCtx& c, Fwd3Smem<TIn>& sm, const Prep3& P) {
   constexpr bool kX3 = kSplitOf<TIn>;
@@ -422,6 +520,91 @@ __device__ void state_chunk(StateCtx& c, Fwd3Smem<TIn>& sm, const Prep3& P) {
     }
 }
 
+// Chunk on tensor cores with bf16 operands (bf16 inputs). Four k16 steps over j for
+// S0 [A^ R^]^T, one k16 step over s for every product with V, T, Mbr; Kb and Bb enter
+// the state update as hi + lo pairs (two products each), so the carried state keeps
+// about 16 bits of them. Writes the chunk's y into ys (row stride kB64) by transposed
+// matrix stores.
+__device__ void state_chunk16(StateCtx& c, Fwd3Smem<bf16_t>& sm, const Prep16& P, int lane) {
+  const int i0 = c.i0;
+  // PA = S0 A^^T (later + V^T Mka^T), PR = S0 R^^T (later + ...): [i][t]
+  float PA[2][4], PR[2][4];
+#pragma unroll
+  for (int q = 0; q < 2; ++q) {
+    zero4(PA[q]);
+    zero4(PR[q]);
+  }
+  uint32_t b[4];
+#pragma unroll
+  for (int kb = 0; kb < 4; ++kb) {
+    uint32_t a[4];
+    c2a16(a, c.S[2 * kb], c.S[2 * kb + 1]);
+    b_nk(b, P.X1, kB64, 0, 16 * kb, lane);  // A^, steps 0..15 as two n8 tiles
+    mma16(PA[0], a, b[0], b[1]);
+    mma16(PA[1], a, b[2], b[3]);
+    b_nk(b, P.X1, kB64, kL, 16 * kb, lane);  // R^
+    mma16(PR[0], a, b[0], b[1]);
+    mma16(PR[1], a, b[2], b[3]);
+  }
+  uint32_t av[4];  // V^T rows i0.., k = s
+  a_mk(av, P.VT, kB16, i0, 0, lane);
+  b_nk(b, P.M[0], kB16, 0, 0, lane);  // Mka
+  mma16(PA[0], av, b[0], b[1]);
+  mma16(PA[1], av, b[2], b[3]);
+  b_nk(b, P.M[1], kB16, 0, 0, lane);  // Mkr
+  mma16(PR[0], av, b[0], b[1]);
+  mma16(PR[1], av, b[2], b[3]);
+  // S(L) = S0 diag(c(L)) + V^T Kb + SA^T Bb; the first two terms need no SA, so they are
+  // issued here, while SA is under way
+#pragma unroll
+  for (int nt = 0; nt < 8; ++nt) {
+    const float2 cl = *reinterpret_cast<const float2*>(P.cL + 8 * nt + 2 * c.t4);
+    c.S[nt][0] *= cl.x;
+    c.S[nt][1] *= cl.y;
+    c.S[nt][2] *= cl.x;
+    c.S[nt][3] *= cl.y;
+  }
+#pragma unroll
+  for (int np = 0; np < 4; ++np)
+#pragma unroll
+    for (int p = 1; p >= 0; --p) {  // the lo part first
+      b_nk(b, P.KbT[p], kB16, 16 * np, 0, lane);
+      mma16(c.S[2 * np], av, b[0], b[1]);
+      mma16(c.S[2 * np + 1], av, b[2], b[3]);
+    }
+  // SA^T = PA T^T  [i][t]
+  float SA[2][4];
+  zero4(SA[0]);
+  zero4(SA[1]);
+  {
+    uint32_t a[4];
+    c2a16(a, PA[0], PA[1]);
+    b_nk(b, P.Tinv, kB16, 0, 0, lane);
+    mma16(SA[0], a, b[0], b[1]);
+    mma16(SA[1], a, b[2], b[3]);
+  }
+  uint32_t asa[4];
+  c2a16(asa, SA[0], SA[1]);
+  // Y^T = PR + SA^T Mbr^T, stored transposed as the chunk's y rows [t][i]
+  b_nk(b, P.M[2], kB16, 0, 0, lane);
+  mma16(PR[0], asa, b[0], b[1]);
+  mma16(PR[1], asa, b[2], b[3]);
+  {
+    uint32_t yv[4];
+    c2a16(yv, PR[0], PR[1]);
+    stsm4t(&sm.ys[c.yb][((lane & 7) + (lane >> 4) * 8) * kB64 + i0 + ((lane >> 3) & 1) * 8], yv);
+  }
+  // + SA^T Bb
+#pragma unroll
+  for (int np = 0; np < 4; ++np)
+#pragma unroll
+    for (int p = 1; p >= 0; --p) {
+      b_nk(b, P.BbT[p], kB16, 16 * np, 0, lane);
+      mma16(c.S[2 * np], asa, b[0], b[1]);
+      mma16(c.S[2 * np + 1], asa, b[2], b[3]);
+    }
+}
+
 // Chunk in the direct form (any decay), fp32 on the CUDA cores.
 template <typename TIn, bool kLogit>
 __device__ void state_chunk_direct(StateCtx& c, Fwd3Smem<TIn>& sm, int stage, int len) {
@@ -459,8 +642,9 @@ __device__ void state_chunk_direct(StateCtx& c, Fwd3Smem<TIn>& sm, int stage, in
     y1 += __shfl_xor_sync(0xffffffffu, y1, 1);
     y1 += __shfl_xor_sync(0xffffffffu, y1, 2);
     if (t4 == 0) {
-      st1(&sm.ys[c.yb][t * kN + i0 + g], y0);
-      st1(&sm.ys[c.yb][t * kN + i0 + g + 8], y1);
+      constexpr int kYS = Fwd3Io<TIn>::kYS;
+      st1(&sm.ys[c.yb][t * kYS + i0 + g], y0);
+      st1(&sm.ys[c.yb][t * kYS + i0 + g + 8], y1);
     }
   }
 }
@@ -486,7 +670,7 @@ __device__ void flush_epilogue(const Fwd3Smem<__nv_bfloat16>& sm, const FwdArgs&
     }
   };
   float y[8], v[8];
-  load8(&sm.ys[m & 1][t * kN + i0], y);
+  load8(&sm.ys[m & 1][t * kB64 + i0], y);
   load8(&sm.epi_v[es][t * kN + i0], v);
   float sum = 0.f;
 #pragma unroll
@@ -556,8 +740,9 @@ __global__ void __launch_bounds__(kThreads, 1) wkv7_fwd3_kernel(const __grid_con
     mbar_arrive_expect_tx(&sm.full[st], kStageBytes);
     for (int v = 0; v < 6; ++v) tma_load_4d(sm.raw[st][v], &args.map[v], &sm.full[st], 0, hi, chunk * kL, bi);
   };
-  // TMA copies are issued by the forming group's first thread
-  constexpr int kIssuer = 128;
+  // TMA copies are issued by the first thread of the forming group (fp32 inputs) or of the
+  // products group (bf16 inputs, where that group has the shorter round)
+  constexpr int kIssuer = kSplitOf<TIn> ? 128 : 256;
   if (tid == kIssuer) {
     for (int s = 0; s < kStages; ++s) mbar_init(&sm.full[s], 1);
     fence_mbar_init();
@@ -617,8 +802,12 @@ __global__ void __launch_bounds__(kThreads, 1) wkv7_fwd3_kernel(const __grid_con
                                   chunk % 4);
   };
   auto grams = [&](int chunk) {
-    Prep3& P = sm.prep[chunk % 3];
-    if (!P.unsafe) gram_chunk<kSplitOf<TIn>>(P, sm.X2[chunk & 1], gtid);
+    auto& P = sm.prep[chunk % 3];
+    if (P.unsafe) return;
+    if constexpr (kSplitOf<TIn>)
+      gram_chunk<true>(P, sm.X2[chunk & 1], gtid);
+    else
+      gram_chunk16(P, sm.X2[chunk & 1], gtid);
   };
 
   // pipeline fill: form chunks 0 and 1, products of chunk 0
@@ -651,7 +840,7 @@ __global__ void __launch_bounds__(kThreads, 1) wkv7_fwd3_kernel(const __grid_con
                   args.ext.y, args.status);
       }
     } else {
-      const Prep3& P = sm.prep[n % 3];
+      const auto& P = sm.prep[n % 3];
       const int t0 = n * kL, len = chunk_len(n);
       if (ck_head && t0 % args.C == 0) {
         if constexpr (kStageCk)
@@ -662,8 +851,10 @@ __global__ void __launch_bounds__(kThreads, 1) wkv7_fwd3_kernel(const __grid_con
       c.yb = n & 1;
       if (P.unsafe)
         state_chunk_direct<TIn, kLogit>(c, sm, n % kStages, len);
-      else
+      else if constexpr (kSplitOf<TIn>)
         state_chunk<TIn>(c, sm, P);
+      else
+        state_chunk16(c, sm, P, lane);
     }
     // the stage of chunk n is free (formed two rounds ago, direct steps done); refill it
     aborted = __syncthreads_or(sm.abort_flag) != 0;
