@@ -511,8 +511,8 @@ def _report(args, wl, world, B, T, H, N, C, bf16, ms, fwd_ms, bwd_ms, e2e, ckpt,
         "vs_baseline": None, "dtype": "bf16" if (bf16 and N == 64) else "f32", "data": "synthetic",
         "arithmetic": ("tensor-core products with fp32 accumulation: bf16 operands in the forward (the fp32 state "
                        "rounded to bf16 where it enters a product; the state update's scaled k and b as bf16 hi + lo "
-                       "pairs), tf32 operands in the backward's carry chain (the fp32 carry rounded to tf32 where it "
-                       "enters a product), bf16 operands in the backward's per-chunk gradient products (the carry "
+                       "pairs), bf16 operands in the backward's carry chain (the fp32 carry rounded to bf16 where it "
+                       "enters a product) and in its per-chunk gradient products (the carry "
                        "stored as bf16 between the two backward kernels, the fp32 checkpoint rounded to bf16 "
                        "there); fp32 accumulation, state and element-wise math" if chunked else
                        ("tensor-core products in split tf32 in the forward, the backward's carry chain and its "
@@ -534,7 +534,7 @@ def _report(args, wl, world, B, T, H, N, C, bf16, ms, fwd_ms, bwd_ms, e2e, ckpt,
                      "note": ("the backward call (its two kernels, timed together with CUDA events around the "
                               "call): algorithmic FLOP of the recurrence (24 N^2 per token-head) against the FP32 "
                               "CUDA-core peak, the roofline the metric names; the kernels form them as tensor-core "
-                              "products (tf32 in the carry chain, bf16 in the output pass)") if chunked else
+                              "products with bf16 operands") if chunked else
                              ("the backward call (its two kernels, timed together with CUDA events around the call): "
                               "algorithmic FLOP of the recurrence (24 N^2 per token-head) against the FP32 CUDA-core "
                               "peak; the kernels form them as split-tf32 tensor-core products")

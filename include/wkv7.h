@@ -128,14 +128,15 @@ int wkv7_backward(const float* r, const float* w, const float* k, const float* v
  * gradient are fp32 in memory.
  * At N = 64 with 16-step checkpoints the chunked tensor-core form runs, split
  * in two passes. The carried gradient G at every chunk boundary is computed
- * first (one sequential pass per (b, h): tf32 operands, fp32 accumulation, G
- * carried in fp32) and stored as bfloat16 in a workspace of
+ * first (one sequential pass per (b, h): bfloat16 operands, fp32
+ * accumulation, G carried in fp32 and rounded to bfloat16 where it enters a
+ * product) and stored as bfloat16 in a workspace of
  * B*H*ceil(T/16)*N*N values. Then every chunk's gradients are formed
  * independently with bfloat16 operands and fp32 accumulation: the chunk's
  * inputs, its stored bfloat16 carry and its fp32 checkpoint rounded once to
  * bfloat16; the decay scaling, the triangular solve and the dw sums are fp32.
- * (Measured relative L2 error of the gradients against an fp64 reference at
- * 4 x 4096 x 32 heads: 2e-3 to 5e-3.) The workspace is taken with
+ * (Measured relative L2 error against an fp64 reference at 4 x 4096 x 32
+ * heads: the gradients 2e-3 to 5e-3, dS_init 1.7e-3.) The workspace is taken with
  * cudaMallocAsync on `stream` and freed on it after the call (together with
  * the checkpoint workspace when ckpt is NULL), so WKV7_ERR_ALLOC can also be
  * returned when ckpt is given. wkv7_backward_fused_bf16 runs the other form.

@@ -38,9 +38,10 @@
 //    chunk's own column products: with S(L) = S0 diag(c(L)) + V^T Kb + SA^T Bb,
 //      colsum(Gc o S(L)) = c(L) colsum(Gc o S0) + sum_t (Kb o V Gc + Bb o SA Gc)
 //      colsum(Gc' o S0)  = c(L) colsum(Gc o S0) + sum_t (R^ o DY S0 + A^ o DSA S0).
-// Arithmetic: every product accumulates in fp32. The carry kernel's products
-// take tf32 operands (mma.sync m16n8k8) and carry Gc in fp32, storing it as
-// bf16 for the output kernel. The output kernel's products take bf16 operands
+// Arithmetic: every product accumulates in fp32. For bf16 inputs the carry
+// kernel's products take bf16 operands (mma.sync m16n8k16; for fp32 inputs
+// split tf32, three m16n8k8) and carry Gc in fp32, storing it as bf16 for the
+// output kernel. The output kernel's products take bf16 operands
 // (mma.sync m16n8k16): the chunk's inputs, the stored bf16 carry, and the fp32
 // checkpoint rounded once to bf16; its scaling, triangular solve and dw sums
 // are fp32. A chunk whose decays leave [1/16, 16] (or hold a NaN) is run step
@@ -125,7 +126,8 @@ enum { C_R = 0, C_W = 1, C_A = 2, C_B = 3, C_DY = 4, C_NV = 5 };  // vectors sta
 constexpr int kCarryStages = 4;
 constexpr int kCarryThreads = 384;  // warps 0-3: state; 4-7: forming (F); 8-11: products (P)
 
-// Operands of one chunk for the carry update (tf32 values unless noted).
+// Operands of one chunk for the carry update, fp32 inputs (fp32 values, split as they
+// enter a product).
 struct OpC {
   float Rh[kL * kLD64];   // R^ [t][j]
   float DYs[kL * kLD64];  // DY [t][i] (bf16 values)
@@ -144,6 +146,34 @@ struct ScratchC {
   float Mbr[kL * kLD16], Mba[kL * kLD16];  // R^ B~^T (with diagonal), A^ B~^T (strictly lower) [t][s]
 };
 
+// The same for bf16 inputs: bf16 tiles (rows of kB64 / kB16 elements, read by ldmatrix).
+struct alignas(16) OpC16 {
+  bf16_t Rh[kL * kB64];   // R^ [t][j]
+  bf16_t DYs[kL * kB64];  // DY [t][i]
+  bf16_t Btp[kL * kB64];  // T^T Bb [t][j]
+  bf16_t Ah[kL * kB64];   // A^ [t][j]
+  bf16_t W[kL * kB16];    // Mbr T [s][t]
+  float cL[kN];           // c(L), fp32
+  int unsafe;
+  int pad_[3];
+};
+struct alignas(16) ScratchC16 {
+  bf16_t Bt[kL * kB64];   // B~ [t][j]
+  bf16_t Bb[kL * kB64];   // Bb [s][j]
+  bf16_t Mbr[kL * kB16];  // R^ B~^T (with diagonal) [t][s]
+  float Mba[kL * kLD16];  // A^ B~^T (strictly lower) [t][s], fp32: T is formed from it
+};
+template <typename TIn>
+struct CarryIo {  // bf16 inputs: bf16 operands
+  using Op = OpC16;
+  using Scratch = ScratchC16;
+};
+template <>
+struct CarryIo<float> {  // fp32 inputs: split tf32
+  using Op = OpC;
+  using Scratch = ScratchC;
+};
+
 // Shared memory of the carry kernel for bf16 (TIn = bf16_t: six vectors per stage, the
 // epilogue's nv the sixth; carries stored as bf16) or fp32 inputs (five vectors; carries
 // stored as fp32).
@@ -152,9 +182,10 @@ struct CarrySmemT {
   static constexpr int kVecs = sizeof(TIn) == 2 ? 6 : 5;
   typedef TIn CarryT;
   TIn raw[kCarryStages][kVecs][kTile];  // r, w, a, b, dy (or dout), nv (epilogue) of one chunk per stage
-  OpC op[3];
-  ScratchC sc[2];
-  float TT[kL * kLD16];  // T^T, T = (I - Mba)^-1
+  typename CarryIo<TIn>::Op op[3];
+  typename CarryIo<TIn>::Scratch sc[2];
+  float TT[kL * kLD16];   // T^T, T = (I - Mba)^-1 (fp32 inputs)
+  bf16_t Tm[kL * kB16];   // T [t][s] (bf16 inputs)
   float Pc[4][kN];       // products of the decays of four-step blocks
   TIn gst[2][kN * 72];   // carries on their way out (state warps write, products warps store)
   uint64_t full[kCarryStages];
@@ -188,8 +219,8 @@ __device__ __forceinline__ __nv_bfloat162 gn_backward_row(float2 d, float2 nv, f
 // products chained in step order. Returns (uniformly over the group) whether
 // some decay leaves the range of the scaled form.
 template <typename TIn, bool kLogit, bool kEpi>
-__device__ bool form_carry(ScratchC& sc, float (&Pc)[4][kN], TIn* rs, OpC& op, int len, int ftid,
-                           const float* epi_rstd, float2 epi_lw) {
+__device__ bool form_carry(typename CarryIo<TIn>::Scratch& sc, float (&Pc)[4][kN], TIn* rs,
+                           typename CarryIo<TIn>::Op& op, int len, int ftid, const float* epi_rstd, float2 epi_lw) {
   constexpr bool kX3 = sizeof(TIn) == 4;
   const int lane = ftid & 31, pf = ftid >> 5, j = 2 * lane, t0 = 4 * pf;
   float2 wv[4], av[4], rv[4], bv[4], dyv[4];
@@ -230,17 +261,27 @@ __device__ bool form_carry(ScratchC& sc, float (&Pc)[4][kN], TIn* rs, OpC& op, i
   float2 c = cpre;
 #pragma unroll
   for (int e = 0; e < 4; ++e) {
-    const int t = t0 + e, q = t * kLD64 + j, q68 = t * kLDT + j;
+    const int t = t0 + e;
     const float2 cprev = c;
     c = fmul2(c, wv[e]);
     const float2 ic = make_float2(rcp_approx(c.x), rcp_approx(c.y));
-    const float2 ah = op_val2<kX3>(fmul2(av[e], cprev));
-    *reinterpret_cast<float2*>(sc.Ah + q) = ah;
-    *reinterpret_cast<float2*>(op.Ah68 + q68) = ah;
-    *reinterpret_cast<float2*>(op.Rh + q) = op_val2<kX3>(fmul2(rv[e], c));
-    *reinterpret_cast<float2*>(sc.Bt + q) = op_val2<kX3>(fmul2(bv[e], ic));
-    *reinterpret_cast<float2*>(sc.Bb68 + q68) = op_val2<kX3>(fmul2(bv[e], fmul2(cL, ic)));
-    *reinterpret_cast<float2*>(op.DYs + q) = dyv[e];
+    if constexpr (kX3) {
+      const int q = t * kLD64 + j, q68 = t * kLDT + j;
+      const float2 ah = fmul2(av[e], cprev);
+      *reinterpret_cast<float2*>(sc.Ah + q) = ah;
+      *reinterpret_cast<float2*>(op.Ah68 + q68) = ah;
+      *reinterpret_cast<float2*>(op.Rh + q) = fmul2(rv[e], c);
+      *reinterpret_cast<float2*>(sc.Bt + q) = fmul2(bv[e], ic);
+      *reinterpret_cast<float2*>(sc.Bb68 + q68) = fmul2(bv[e], fmul2(cL, ic));
+      *reinterpret_cast<float2*>(op.DYs + q) = dyv[e];
+    } else {
+      const int q = t * kB64 + j;
+      st_pair(op.Ah + q, fmul2(av[e], cprev));
+      st_pair(op.Rh + q, fmul2(rv[e], c));
+      st_pair(sc.Bt + q, fmul2(bv[e], ic));
+      st_pair(sc.Bb + q, fmul2(bv[e], fmul2(cL, ic)));
+      st_pair(op.DYs + q, dyv[e]);  // bf16 values already: exact
+    }
   }
   return false;
 }
@@ -269,11 +310,41 @@ __device__ __forceinline__ void gram_tile(float* M, const float* P, const float*
   }
 }
 
+// n-tile nt of P Q^T (16 x 8, K = 64, bf16 tiles of stride kB64), masked to s < t (strict)
+// or s <= t, stored as fp32 (stride kLD16) or bf16 (stride kB16).
+__device__ __forceinline__ void ldsm2(uint32_t (&r)[2], const bf16_t* p) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x2.shared.b16 {%0,%1}, [%2];" : "=r"(r[0]), "=r"(r[1]) : "r"(smem_addr(p)));
+}
+template <typename TOut>
+__device__ __forceinline__ void gram_tile16(TOut* M, const bf16_t* P, const bf16_t* Q, int nt, bool strict, int lane) {
+  const int g = lane >> 2, t4 = lane & 3;
+  float acc[4];
+  zero4(acc);
+#pragma unroll
+  for (int kb = 0; kb < kN / 16; ++kb) {
+    uint32_t a[4], b[2];
+    a_mk(a, P, kB64, 0, 16 * kb, lane);
+    ldsm2(b, Q + (8 * nt + (lane & 7)) * kB64 + 16 * kb + ((lane >> 3) & 1) * 8);
+    mma16(acc, a, b[0], b[1]);
+  }
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    const int t = g + 8 * h, s = 8 * nt + 2 * t4;
+    const bool k0 = strict ? s < t : s <= t, k1 = strict ? s + 1 < t : s + 1 <= t;
+    const float2 x = make_float2(k0 ? acc[2 * h] : 0.f, k1 ? acc[2 * h + 1] : 0.f);
+    if constexpr (sizeof(TOut) == 4)
+      *reinterpret_cast<float2*>(M + t * kLD16 + s) = x;
+    else
+      st_pair(M + t * kB16 + s, x);
+  }
+}
+
 // Forming group: wait for a chunk's inputs and form its operands. Returns
 // false on a timeout.
 template <typename TIn, bool kLogit, bool kEpi>
-__device__ bool front_form(CarrySmemT<TIn>& sm, ScratchC& sc, OpC& op, TIn* rs, uint64_t* bar, uint32_t parity,
-                           int len, unsigned* status, const float* epi_rstd, float2 epi_lw) {
+__device__ bool front_form(CarrySmemT<TIn>& sm, typename CarryIo<TIn>::Scratch& sc, typename CarryIo<TIn>::Op& op,
+                           TIn* rs, uint64_t* bar, uint32_t parity, int len, unsigned* status, const float* epi_rstd,
+                           float2 epi_lw) {
   const int ftid = threadIdx.x - 128;
   const bool ok = mbar_wait_bounded(status, bar, parity);
   if (named_bar_or(1, 128, !ok)) {
@@ -286,12 +357,70 @@ __device__ bool front_form(CarrySmemT<TIn>& sm, ScratchC& sc, OpC& op, TIn* rs, 
   named_bar(1, 128);
   // n-tile pf - 2 of Mba = A^ B~^T (warps 2, 3); the products group makes Mbr
   const int pf = ftid >> 5;
-  if (pf >= 2) gram_tile<sizeof(TIn) == 4>(sc.Mba, sc.Ah, sc.Bt, pf - 2, true, ftid & 31);
+  if (pf >= 2) {
+    if constexpr (sizeof(TIn) == 4)
+      gram_tile<true>(sc.Mba, sc.Ah, sc.Bt, pf - 2, true, ftid & 31);
+    else
+      gram_tile16(sc.Mba, op.Ah, sc.Bt, pf - 2, true, ftid & 31);
+  }
   return true;
 }
 
-// Products group (128 threads): T, Mbr = R^ B~^T (with diagonal), T^T Bb and Mbr T of a
-// formed chunk.
+// Products group (128 threads), bf16 operands: T (fp32 forward substitution, stored as
+// bf16), Mbr = R^ B~^T (with diagonal), then T^T Bb and W = Mbr T.
+__device__ void front_products16(CarrySmemT<bf16_t>& sm, ScratchC16& sc, OpC16& op) {
+  const int pp = (threadIdx.x >> 5) - 8, lane = threadIdx.x & 31, g = lane >> 2, t4 = lane & 3;
+  if (pp == 0) {
+    const int s = lane & 15;
+    float col[kL];
+#pragma unroll
+    for (int t = 0; t < kL; ++t) {
+      float x = t == s ? 1.f : 0.f;
+#pragma unroll
+      for (int u = 0; u < t; ++u) x = fmaf(sc.Mba[t * kLD16 + u], col[u], x);
+      col[t] = x;
+    }
+    if (lane < 16) {
+#pragma unroll
+      for (int t = 0; t < kL; ++t) sm.Tm[t * kB16 + s] = __float2bfloat16_rn(col[t]);
+    }
+  } else if (pp <= 2) {
+    gram_tile16(sc.Mbr, op.Rh, sc.Bt, pp - 1, false, lane);
+  }
+  named_bar(2, 128);
+  uint32_t a[4], b[4];
+  {  // T^T Bb [t][j], columns 16 pp .. 16 pp + 15: A = T^T (T stored [s][t] is A stored [k][m])
+    float acc[2][4];
+    zero4(acc[0]);
+    zero4(acc[1]);
+    a_km(a, sm.Tm, kB16, 0, 0, lane);
+    b_kn(b, sc.Bb, kB64, 16 * pp, 0, lane);
+    mma16(acc[0], a, b[0], b[1]);
+    mma16(acc[1], a, b[2], b[3]);
+#pragma unroll
+    for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+      for (int h = 0; h < 2; ++h)
+        st_pair(op.Btp + (g + 8 * h) * kB64 + 16 * pp + 8 * nt + 2 * t4, make_float2(acc[nt][2 * h], acc[nt][2 * h + 1]));
+  }
+  if (pp == 3) {  // W = Mbr T [s][t]
+    float acc[2][4];
+    zero4(acc[0]);
+    zero4(acc[1]);
+    a_mk(a, sc.Mbr, kB16, 0, 0, lane);
+    b_kn(b, sm.Tm, kB16, 0, 0, lane);
+    mma16(acc[0], a, b[0], b[1]);
+    mma16(acc[1], a, b[2], b[3]);
+#pragma unroll
+    for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+      for (int h = 0; h < 2; ++h)
+        st_pair(op.W + (g + 8 * h) * kB16 + 8 * nt + 2 * t4, make_float2(acc[nt][2 * h], acc[nt][2 * h + 1]));
+  }
+}
+
+// Products group (128 threads), fp32 inputs: T, Mbr = R^ B~^T (with diagonal), T^T Bb and
+// Mbr T of a formed chunk, in split tf32.
 template <typename TIn>
 __device__ void front_products(CarrySmemT<TIn>& sm, ScratchC& sc, OpC& op) {
   constexpr bool kX3 = sizeof(TIn) == 4;
@@ -396,6 +525,49 @@ __device__ __forceinline__ void carry_chunk(float (&G)[8][4], const OpC& op, int
       ld_b_t(b, op.Ah68, kLDT, 8 * nt, 8 * kb, g, t4);
       mma_x(G[nt], aS[kb], b);
     }
+}
+
+// The same with bf16 operands (bf16 inputs): G, DY, T^T Bb, W, R^, A^ and DSA^T enter
+// the products as bf16; G stays fp32 in its accumulator tiles.
+__device__ __forceinline__ void carry_chunk16(float (&G)[8][4], const OpC16& op, int i0, int t4, int lane) {
+  uint32_t aD[4], b[4];
+  a_km(aD, op.DYs, kB64, i0, 0, lane);  // DY^T rows i0.., k = s (DY stored [s][i])
+  float DS[2][4];
+  zero4(DS[0]);
+  zero4(DS[1]);
+  b_kn(b, op.W, kB16, 0, 0, lane);  // W [s][t]
+  mma16(DS[0], aD, b[0], b[1]);
+  mma16(DS[1], aD, b[2], b[3]);
+#pragma unroll
+  for (int kb = 0; kb < 4; ++kb) {
+    uint32_t aG[4];
+    c2a16(aG, G[2 * kb], G[2 * kb + 1]);
+    b_nk(b, op.Btp, kB64, 0, 16 * kb, lane);  // (T^T Bb)^T: B^T = T^T Bb stored [t][j]
+    mma16(DS[0], aG, b[0], b[1]);
+    mma16(DS[1], aG, b[2], b[3]);
+  }
+#pragma unroll
+  for (int nt = 0; nt < 8; ++nt) {
+    const float2 cl = *reinterpret_cast<const float2*>(op.cL + 8 * nt + 2 * t4);
+    G[nt][0] *= cl.x;
+    G[nt][1] *= cl.y;
+    G[nt][2] *= cl.x;
+    G[nt][3] *= cl.y;
+  }
+#pragma unroll
+  for (int np = 0; np < 4; ++np) {  // + DY^T R^ (R^ stored [t][j])
+    b_kn(b, op.Rh, kB64, 16 * np, 0, lane);
+    mma16(G[2 * np], aD, b[0], b[1]);
+    mma16(G[2 * np + 1], aD, b[2], b[3]);
+  }
+  uint32_t aS[4];
+  c2a16(aS, DS[0], DS[1]);
+#pragma unroll
+  for (int np = 0; np < 4; ++np) {  // + DSA^T A^
+    b_kn(b, op.Ah, kB64, 16 * np, 0, lane);
+    mma16(G[2 * np], aS, b[0], b[1]);
+    mma16(G[2 * np + 1], aS, b[2], b[3]);
+  }
 }
 
 // The same chunk step by step in fp32 (a chunk outside the scaled form's
@@ -518,7 +690,11 @@ __global__ void __launch_bounds__(kCarryThreads, 1) wkv7_bwd4_carry_kernel(const
   };
   auto products = [&](int v) {  // products group
     const int c = chunk_of(v);
-    if (!sm.op[c % 3].unsafe) front_products<TIn>(sm, sm.sc[c & 1], sm.op[c % 3]);
+    if (sm.op[c % 3].unsafe) return;
+    if constexpr (kX3)
+      front_products<TIn>(sm, sm.sc[c & 1], sm.op[c % 3]);
+    else
+      front_products16(sm, sm.sc[c & 1], sm.op[c % 3]);
   };
   // TMA copies are issued by a products-group thread (that group has the most slack); the
   // forming group waits for them
@@ -566,7 +742,7 @@ __global__ void __launch_bounds__(kCarryThreads, 1) wkv7_bwd4_carry_kernel(const
   for (int m = 0; m < nchunks && !aborted; ++m) {
     const int n = chunk_of(m), st = m % kCarryStages;
     if (role == 0) {
-      const OpC& op = sm.op[n % 3];
+      const auto& op = sm.op[n % 3];
       // the carry entering this chunk (gradient w.r.t. the state after it), as the output
       // pass multiplies with it (bf16, or fp32 for fp32 inputs); the products group stores it
       // next round
@@ -584,8 +760,10 @@ __global__ void __launch_bounds__(kCarryThreads, 1) wkv7_bwd4_carry_kernel(const
       }
       if (op.unsafe)
         carry_direct<TIn, kLogit>(G, sm.raw[st][0], len_of(m), i0, g, t4);
+      else if constexpr (kX3)
+        carry_chunk<true>(G, op, i0, g, t4);
       else
-        carry_chunk<kX3>(G, op, i0, g, t4);
+        carry_chunk16(G, op, i0, t4, lane);
     } else if (role == 1) {
       if (m + 2 < nchunks) form(m + 2);
     } else {
