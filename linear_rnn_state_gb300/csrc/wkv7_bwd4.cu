@@ -147,20 +147,21 @@ struct ScratchC {
 };
 
 // The same for bf16 inputs: bf16 tiles (rows of kB64 / kB16 elements, read by ldmatrix).
+// The forming group writes the vectors, the products group adds Mbr and T a round later,
+// the state warps read them all a round after that.
 struct alignas(16) OpC16 {
   bf16_t Rh[kL * kB64];   // R^ [t][j]
   bf16_t DYs[kL * kB64];  // DY [t][i]
-  bf16_t Btp[kL * kB64];  // T^T Bb [t][j]
   bf16_t Ah[kL * kB64];   // A^ [t][j]
-  bf16_t W[kL * kB16];    // Mbr T [s][t]
+  bf16_t Bb[kL * kB64];   // Bb [s][j]
+  bf16_t Mbr[kL * kB16];  // R^ B~^T (with diagonal) [t][s]
+  bf16_t Tm[kL * kB16];   // T = (I - Mba)^-1 [t][s]
   float cL[kN];           // c(L), fp32
   int unsafe;
   int pad_[3];
 };
 struct alignas(16) ScratchC16 {
   bf16_t Bt[kL * kB64];   // B~ [t][j]
-  bf16_t Bb[kL * kB64];   // Bb [s][j]
-  bf16_t Mbr[kL * kB16];  // R^ B~^T (with diagonal) [t][s]
   float Mba[kL * kLD16];  // A^ B~^T (strictly lower) [t][s], fp32: T is formed from it
 };
 template <typename TIn>
@@ -185,7 +186,6 @@ struct CarrySmemT {
   typename CarryIo<TIn>::Op op[3];
   typename CarryIo<TIn>::Scratch sc[2];
   float TT[kL * kLD16];   // T^T, T = (I - Mba)^-1 (fp32 inputs)
-  bf16_t Tm[kL * kB16];   // T [t][s] (bf16 inputs)
   float Pc[4][kN];       // products of the decays of four-step blocks
   TIn gst[2][kN * 72];   // carries on their way out (state warps write, products warps store)
   uint64_t full[kCarryStages];
@@ -242,14 +242,7 @@ __device__ bool form_carry(typename CarryIo<TIn>::Scratch& sc, float (&Pc)[4][kN
     pb = fmul2(pb, wv[e]);
   }
   *reinterpret_cast<float2*>(&Pc[pf][j]) = pb;
-  if (named_bar_or(1, 128, !safe)) return true;
-  float2 cL = make_float2(1.f, 1.f), cpre = cL;  // cpre = c(t0 - 1)
-#pragma unroll
-  for (int q = 0; q < 4; ++q) {
-    cL = fmul2(cL, *reinterpret_cast<const float2*>(&Pc[q][j]));
-    if (q < pf) cpre = cL;
-  }
-  if (pf == 0) *reinterpret_cast<float2*>(op.cL + j) = cL;
+  // the other vectors are read before the group barrier, so their loads overlap it
 #pragma unroll
   for (int e = 0; e < 4; ++e) {
     const int o = (t0 + e) * kN + j;
@@ -258,6 +251,14 @@ __device__ bool form_carry(typename CarryIo<TIn>::Scratch& sc, float (&Pc)[4][kN
     bv[e] = bf2(rs + C_B * kTile + o);
     dyv[e] = bf2(rs + C_DY * kTile + o);
   }
+  if (named_bar_or(1, 128, !safe)) return true;
+  float2 cL = make_float2(1.f, 1.f), cpre = cL;  // cpre = c(t0 - 1)
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    cL = fmul2(cL, *reinterpret_cast<const float2*>(&Pc[q][j]));
+    if (q < pf) cpre = cL;
+  }
+  if (pf == 0) *reinterpret_cast<float2*>(op.cL + j) = cL;
   float2 c = cpre;
 #pragma unroll
   for (int e = 0; e < 4; ++e) {
@@ -279,7 +280,7 @@ __device__ bool form_carry(typename CarryIo<TIn>::Scratch& sc, float (&Pc)[4][kN
       st_pair(op.Ah + q, fmul2(av[e], cprev));
       st_pair(op.Rh + q, fmul2(rv[e], c));
       st_pair(sc.Bt + q, fmul2(bv[e], ic));
-      st_pair(sc.Bb + q, fmul2(bv[e], fmul2(cL, ic)));
+      st_pair(op.Bb + q, fmul2(bv[e], fmul2(cL, ic)));
       st_pair(op.DYs + q, dyv[e]);  // bf16 values already: exact
     }
   }
@@ -357,65 +358,34 @@ __device__ bool front_form(CarrySmemT<TIn>& sm, typename CarryIo<TIn>::Scratch& 
   named_bar(1, 128);
   // n-tile pf - 2 of Mba = A^ B~^T (warps 2, 3); the products group makes Mbr
   const int pf = ftid >> 5;
-  if (pf >= 2) {
-    if constexpr (sizeof(TIn) == 4)
-      gram_tile<true>(sc.Mba, sc.Ah, sc.Bt, pf - 2, true, ftid & 31);
+  if constexpr (sizeof(TIn) == 4) {
+    if (pf >= 2) gram_tile<true>(sc.Mba, sc.Ah, sc.Bt, pf - 2, true, ftid & 31);
+  } else {  // n-tile pf % 2 of Mba (warps 0, 1; fp32) or of Mbr (warps 2, 3; bf16)
+    if (pf < 2)
+      gram_tile16(sc.Mba, op.Ah, sc.Bt, pf, true, ftid & 31);
     else
-      gram_tile16(sc.Mba, op.Ah, sc.Bt, pf - 2, true, ftid & 31);
+      gram_tile16(op.Mbr, op.Rh, sc.Bt, pf - 2, false, ftid & 31);
   }
   return true;
 }
 
-// Products group (128 threads), bf16 operands: T (fp32 forward substitution, stored as
-// bf16), Mbr = R^ B~^T (with diagonal), then T^T Bb and W = Mbr T.
-__device__ void front_products16(CarrySmemT<bf16_t>& sm, ScratchC16& sc, OpC16& op) {
-  const int pp = (threadIdx.x >> 5) - 8, lane = threadIdx.x & 31, g = lane >> 2, t4 = lane & 3;
-  if (pp == 0) {
-    const int s = lane & 15;
-    float col[kL];
+// Products group (128 threads), bf16 operands: T = (I - Mba)^-1 by fp32 forward
+// substitution (warp 0; the forming group made Mba and Mbr), stored as bf16.
+__device__ void front_products16(ScratchC16& sc, OpC16& op) {
+  const int pp = (threadIdx.x >> 5) - 8, lane = threadIdx.x & 31;
+  if (pp != 0) return;
+  const int s = lane & 15;
+  float col[kL];
 #pragma unroll
-    for (int t = 0; t < kL; ++t) {
-      float x = t == s ? 1.f : 0.f;
+  for (int tt = 0; tt < kL; ++tt) {
+    float x = tt == s ? 1.f : 0.f;
 #pragma unroll
-      for (int u = 0; u < t; ++u) x = fmaf(sc.Mba[t * kLD16 + u], col[u], x);
-      col[t] = x;
-    }
-    if (lane < 16) {
-#pragma unroll
-      for (int t = 0; t < kL; ++t) sm.Tm[t * kB16 + s] = __float2bfloat16_rn(col[t]);
-    }
-  } else if (pp <= 2) {
-    gram_tile16(sc.Mbr, op.Rh, sc.Bt, pp - 1, false, lane);
+    for (int u = 0; u < tt; ++u) x = fmaf(sc.Mba[tt * kLD16 + u], col[u], x);
+    col[tt] = x;
   }
-  named_bar(2, 128);
-  uint32_t a[4], b[4];
-  {  // T^T Bb [t][j], columns 16 pp .. 16 pp + 15: A = T^T (T stored [s][t] is A stored [k][m])
-    float acc[2][4];
-    zero4(acc[0]);
-    zero4(acc[1]);
-    a_km(a, sm.Tm, kB16, 0, 0, lane);
-    b_kn(b, sc.Bb, kB64, 16 * pp, 0, lane);
-    mma16(acc[0], a, b[0], b[1]);
-    mma16(acc[1], a, b[2], b[3]);
+  if (lane < 16) {
 #pragma unroll
-    for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-      for (int h = 0; h < 2; ++h)
-        st_pair(op.Btp + (g + 8 * h) * kB64 + 16 * pp + 8 * nt + 2 * t4, make_float2(acc[nt][2 * h], acc[nt][2 * h + 1]));
-  }
-  if (pp == 3) {  // W = Mbr T [s][t]
-    float acc[2][4];
-    zero4(acc[0]);
-    zero4(acc[1]);
-    a_mk(a, sc.Mbr, kB16, 0, 0, lane);
-    b_kn(b, sm.Tm, kB16, 0, 0, lane);
-    mma16(acc[0], a, b[0], b[1]);
-    mma16(acc[1], a, b[2], b[3]);
-#pragma unroll
-    for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-      for (int h = 0; h < 2; ++h)
-        st_pair(op.W + (g + 8 * h) * kB16 + 8 * nt + 2 * t4, make_float2(acc[nt][2 * h], acc[nt][2 * h + 1]));
+    for (int tt = 0; tt < kL; ++tt) op.Tm[tt * kB16 + s] = __float2bfloat16_rn(col[tt]);
   }
 }
 
@@ -527,24 +497,36 @@ __device__ __forceinline__ void carry_chunk(float (&G)[8][4], const OpC& op, int
     }
 }
 
-// The same with bf16 operands (bf16 inputs): G, DY, T^T Bb, W, R^, A^ and DSA^T enter
-// the products as bf16; G stays fp32 in its accumulator tiles.
+// The same with bf16 operands (bf16 inputs), T applied last:
+//   DSA^T = (G Bb^T + DY^T Mbr) T;  G <- G diag(c(L)) + DY^T R^ + DSA^T A^
+// G, DY, Bb, Mbr, T, R^, A^ and the intermediate products enter as bf16; G stays fp32 in
+// its accumulator tiles.
 __device__ __forceinline__ void carry_chunk16(float (&G)[8][4], const OpC16& op, int i0, int t4, int lane) {
   uint32_t aD[4], b[4];
   a_km(aD, op.DYs, kB64, i0, 0, lane);  // DY^T rows i0.., k = s (DY stored [s][i])
-  float DS[2][4];
-  zero4(DS[0]);
-  zero4(DS[1]);
-  b_kn(b, op.W, kB16, 0, 0, lane);  // W [s][t]
-  mma16(DS[0], aD, b[0], b[1]);
-  mma16(DS[1], aD, b[2], b[3]);
+  float X[2][4];
+  zero4(X[0]);
+  zero4(X[1]);
+  b_kn(b, op.Mbr, kB16, 0, 0, lane);  // Mbr [u][s]
+  mma16(X[0], aD, b[0], b[1]);
+  mma16(X[1], aD, b[2], b[3]);
 #pragma unroll
   for (int kb = 0; kb < 4; ++kb) {
     uint32_t aG[4];
     c2a16(aG, G[2 * kb], G[2 * kb + 1]);
-    b_nk(b, op.Btp, kB64, 0, 16 * kb, lane);  // (T^T Bb)^T: B^T = T^T Bb stored [t][j]
-    mma16(DS[0], aG, b[0], b[1]);
-    mma16(DS[1], aG, b[2], b[3]);
+    b_nk(b, op.Bb, kB64, 0, 16 * kb, lane);  // Bb^T: Bb stored [s][j]
+    mma16(X[0], aG, b[0], b[1]);
+    mma16(X[1], aG, b[2], b[3]);
+  }
+  float DS[2][4];
+  zero4(DS[0]);
+  zero4(DS[1]);
+  {
+    uint32_t aX[4];
+    c2a16(aX, X[0], X[1]);
+    b_kn(b, op.Tm, kB16, 0, 0, lane);  // T [s][t]
+    mma16(DS[0], aX, b[0], b[1]);
+    mma16(DS[1], aX, b[2], b[3]);
   }
 #pragma unroll
   for (int nt = 0; nt < 8; ++nt) {
@@ -694,7 +676,7 @@ __global__ void __launch_bounds__(kCarryThreads, 1) wkv7_bwd4_carry_kernel(const
     if constexpr (kX3)
       front_products<TIn>(sm, sm.sc[c & 1], sm.op[c % 3]);
     else
-      front_products16(sm, sm.sc[c & 1], sm.op[c % 3]);
+      front_products16(sm.sc[c & 1], sm.op[c % 3]);
   };
   // TMA copies are issued by a products-group thread (that group has the most slack); the
   // forming group waits for them
