@@ -1134,7 +1134,7 @@ __global__ void __launch_bounds__(kThreads, 3) wkv7_bwd4_out_kernel(const __grid
 
   // ---- B: L x L products and T (warps 0-3), the K = 64 parts of sa, dsa, dv (rows i of block rb)
   const int rb = warp & 3, r0 = 16 * rb;
-  float X1[2][4], X2[2][4];  // warps 0-3: RDSA^T; warps 4-7: RSA^T, DV^T (rows i, columns t)
+  float X1[2][4], X2[2][4];  // warps 0-3: RDSA^T, DV^T; warps 4-7: RSA^T (rows i, columns t)
 #pragma unroll
   for (int q = 0; q < 2; ++q) {
     zero4(X1[q]);
@@ -1160,10 +1160,19 @@ __global__ void __launch_bounds__(kThreads, 3) wkv7_bwd4_out_kernel(const __grid
     } else {
       store_masked16(acc, sm.M[warp == 0 ? 0 : warp - 1], true, warp >= 2, g, t4);
     }
-    mm_mk_nk<4>(X1, sm.u.st.Gc, kB64, r0, sm.Bb, kB64, 0, lane);  // Gc Bb^T
+#pragma unroll
+    for (int kb = 0; kb < 4; ++kb) {  // Gc Bb^T and Gc Kb^T, one A fragment for both
+      uint32_t a[4], b[4];
+      a_mk(a, sm.u.st.Gc, kB64, r0, 16 * kb, lane);
+      b_nk(b, sm.Bb, kB64, 0, 16 * kb, lane);
+      mma16(X1[0], a, b[0], b[1]);
+      mma16(X1[1], a, b[2], b[3]);
+      b_nk(b, sm.Kb, kB64, 0, 16 * kb, lane);
+      mma16(X2[0], a, b[0], b[1]);
+      mma16(X2[1], a, b[2], b[3]);
+    }
   } else {
     mm_mk_nk<4>(X1, sm.u.st.S0, kB64, r0, sm.Ah, kB64, 0, lane);  // S0 A^T
-    mm_mk_nk<4>(X2, sm.u.st.Gc, kB64, r0, sm.Kb, kB64, 0, lane);  // Gc Kb^T
     // this row block's part of colsum(Gc o S0), columns 2 lane, 2 lane + 1
     float2 ep = make_float2(0.f, 0.f);
 #pragma unroll
@@ -1182,18 +1191,22 @@ __global__ void __launch_bounds__(kThreads, 3) wkv7_bwd4_out_kernel(const __grid
   }
   __syncthreads();
 
-  // ---- C: DSA^T = (Gc Bb^T + DY^T Mbr) T (warps 0-3); SA^T = (S0 A^T + V^T Mka^T) T^T and
-  //      DV^T += DY^T Mkr (warps 4-7); sa and dsa stored as bf16 [t][i]
+  // ---- C: DSA^T = (Gc Bb^T + DY^T Mbr) T, DV^T += DY^T Mkr + DSA^T Mka and dv (warps 0-3);
+  //      SA^T = (S0 A^T + V^T Mka^T) T^T (warps 4-7); sa and dsa stored as bf16 [t][i]
   {
-    uint32_t aD[4], b[4], p[4];
-    a_km(aD, sm.raw[V_DY], kB64, r0, 0, lane);  // DY^T
+    uint32_t b[4], p[4];
     float Y[2][4];
     zero4(Y[0]);
     zero4(Y[1]);
     if (warp < 4) {
-      b_kn(b, sm.M[2], kB16, 0, 0, lane);  // Mbr
+      uint32_t aD[4];
+      a_km(aD, sm.raw[V_DY], kB64, r0, 0, lane);  // DY^T
+      b_kn(b, sm.M[2], kB16, 0, 0, lane);         // Mbr
       mma16(X1[0], aD, b[0], b[1]);
       mma16(X1[1], aD, b[2], b[3]);
+      b_kn(b, sm.M[1], kB16, 0, 0, lane);  // Mkr
+      mma16(X2[0], aD, b[0], b[1]);
+      mma16(X2[1], aD, b[2], b[3]);
       c2a16(p, X1[0], X1[1]);
       b_kn(b, sm.Tm, kB16, 0, 0, lane);  // T
       mma16(Y[0], p, b[0], b[1]);
@@ -1204,9 +1217,6 @@ __global__ void __launch_bounds__(kThreads, 3) wkv7_bwd4_out_kernel(const __grid
       b_nk(b, sm.M[0], kB16, 0, 0, lane);        // Mka^T
       mma16(X1[0], aV, b[0], b[1]);
       mma16(X1[1], aV, b[2], b[3]);
-      b_kn(b, sm.M[1], kB16, 0, 0, lane);  // Mkr
-      mma16(X2[0], aD, b[0], b[1]);
-      mma16(X2[1], aD, b[2], b[3]);
       c2a16(p, X1[0], X1[1]);
       b_nk(b, sm.Tm, kB16, 0, 0, lane);  // T^T
       mma16(Y[0], p, b[0], b[1]);
@@ -1214,38 +1224,38 @@ __global__ void __launch_bounds__(kThreads, 3) wkv7_bwd4_out_kernel(const __grid
     }
     c2a16(p, Y[0], Y[1]);
     stsm4t((warp < 4 ? sm.DSA : sm.SA) + ((lane & 7) + (lane >> 4) * 8) * kB64 + r0 + ((lane >> 3) & 1) * 8, p);
+    if (warp < 4) {  // DV^T += DSA^T Mka (DSA^T from the registers just stored), then dv
+      b_kn(b, sm.M[0], kB16, 0, 0, lane);  // Mka
+      mma16(X2[0], p, b[0], b[1]);
+      mma16(X2[1], p, b[2], b[3]);
+#pragma unroll
+      for (int q = 0; q < 2; ++q)
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          const int t = 8 * q + 2 * t4 + e;
+          if (t < len) {
+            float* dst = args.dv + base + (size_t)t * vstep + r0 + g;
+            float x0 = X2[q][e], x1 = X2[q][2 + e];
+            if (epi) {  // + dout bonus
+              x0 = fmaf(bf(ep.dout + t * kB64 + r0 + g), ep.stat[t][1], x0);
+              x1 = fmaf(bf(ep.dout + t * kB64 + r0 + g + 8), ep.stat[t][1], x1);
+            }
+            if (in_extent(args.status, args.ext.dv, dst)) dst[0] = x0;
+            if (in_extent(args.status, args.ext.dv, dst + 8)) dst[8] = x1;
+          }
+        }
+    }
   }
   __syncthreads();
 
-  // ---- D: DV^T += DSA^T Mka and dv (warps 4-7); triu(V DSA^T, 1), triu(SA DY^T), triu(SA DSA^T, 1) (warps 1-3)
-  if (warp >= 4) {
-    uint32_t aS[4], b[4];
-    a_km(aS, sm.DSA, kB64, r0, 0, lane);  // DSA^T
-    b_kn(b, sm.M[0], kB16, 0, 0, lane);   // Mka
-    mma16(X2[0], aS, b[0], b[1]);
-    mma16(X2[1], aS, b[2], b[3]);
-#pragma unroll
-    for (int q = 0; q < 2; ++q)
-#pragma unroll
-      for (int e = 0; e < 2; ++e) {
-        const int t = 8 * q + 2 * t4 + e;
-        if (t < len) {
-          float* dst = args.dv + base + (size_t)t * vstep + r0 + g;
-          float x0 = X2[q][e], x1 = X2[q][2 + e];
-          if (epi) {  // + dout bonus
-            x0 = fmaf(bf(ep.dout + t * kB64 + r0 + g), ep.stat[t][1], x0);
-            x1 = fmaf(bf(ep.dout + t * kB64 + r0 + g + 8), ep.stat[t][1], x1);
-          }
-          if (in_extent(args.status, args.ext.dv, dst)) dst[0] = x0;
-          if (in_extent(args.status, args.ext.dv, dst + 8)) dst[8] = x1;
-        }
-      }
-  } else if (warp >= 1) {
+  // ---- D: U1 = triu(V DSA^T, 1), U2 = triu(SA DY^T), U3 = triu(SA DSA^T, 1) (warps 5-7)
+  if (warp >= 5) {
+    const int u = warp - 4;
     float acc[2][4];
     zero4(acc[0]);
     zero4(acc[1]);
-    mm_mk_nk<4>(acc, warp == 1 ? sm.raw[V_V] : sm.SA, kB64, 0, warp == 2 ? sm.raw[V_DY] : sm.DSA, kB64, 0, lane);
-    store_masked16(acc, sm.U[warp], false, warp == 2, g, t4);
+    mm_mk_nk<4>(acc, u == 1 ? sm.raw[V_V] : sm.SA, kB64, 0, u == 2 ? sm.raw[V_DY] : sm.DSA, kB64, 0, lane);
+    store_masked16(acc, sm.U[u], false, u == 2, g, t4);
   }
   __syncthreads();
 
