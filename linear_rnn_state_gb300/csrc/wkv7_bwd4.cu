@@ -38,9 +38,10 @@
 //    chunk's own column products: with S(L) = S0 diag(c(L)) + V^T Kb + SA^T Bb,
 //      colsum(Gc o S(L)) = c(L) colsum(Gc o S0) + sum_t (Kb o V Gc + Bb o SA Gc)
 //      colsum(Gc' o S0)  = c(L) colsum(Gc o S0) + sum_t (R^ o DY S0 + A^ o DSA S0).
-// Arithmetic: every product accumulates in fp32. For bf16 inputs the carry
-// kernel's products take bf16 operands (mma.sync m16n8k16; for fp32 inputs
-// split tf32, three m16n8k8) and carry Gc in fp32, storing it as bf16 for the
+// Arithmetic: every product accumulates in fp32. The carry kernel's products
+// take bf16 operands (mma.sync m16n8k16): one bf16 value per operand for bf16
+// inputs, a pair hi + lo (three products per product) for fp32 inputs; it
+// carries Gc in fp32 and stores it as bf16 (fp32 for fp32 inputs) for the
 // output kernel. The output kernel's products take bf16 operands
 // (mma.sync m16n8k16): the chunk's inputs, the stored bf16 carry, and the fp32
 // checkpoint rounded once to bf16; its scaling, triangular solve and dw sums
@@ -70,45 +71,6 @@ __device__ __forceinline__ float2 bf2(const __nv_bfloat16* p) {
   return __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(p));
 }
 __device__ __forceinline__ float2 bf2(const float* p) { return *reinterpret_cast<const float2*>(p); }
-__device__ __forceinline__ float2 tf32r2(float2 x) { return make_float2(tf32r(x.x), tf32r(x.y)); }
-
-// Operand values as the carry chain's products take them: tf32 (one product
-// each, bf16 inputs) or fp32 (split tf32, fp32 inputs).
-template <bool kX3>
-__device__ __forceinline__ float op_val(float x) {
-  if constexpr (kX3)
-    return x;
-  else
-    return tf32r(x);
-}
-template <bool kX3>
-__device__ __forceinline__ float2 op_val2(float2 x) {
-  return make_float2(op_val<kX3>(x.x), op_val<kX3>(x.y));
-}
-
-// T = (I - M)^-1 for a strictly lower 16 x 16 M (stride kLD16) by forward
-// substitution, one warp; lane s < 16 owns column s. Writes T (row-major)
-// and/or its transpose as tf32 values.
-template <bool kX3 = false>
-__device__ __forceinline__ void unit_lower_inverse(const float* M, float* Tout, float* TTout, int lane) {
-  const int s = lane & 15;
-  float col[kL];
-#pragma unroll
-  for (int t = 0; t < kL; ++t) {
-    float x = t == s ? 1.f : 0.f;
-#pragma unroll
-    for (int u = 0; u < t; ++u) x = fmaf(M[t * kLD16 + u], col[u], x);
-    col[t] = x;
-  }
-  if (lane < 16) {
-#pragma unroll
-    for (int t = 0; t < kL; ++t) {
-      const float x = op_val<kX3>(col[t]);
-      if (Tout) Tout[t * kLD16 + s] = x;
-      if (TTout) TTout[s * kLD16 + t] = x;
-    }
-  }
-}
 
 __device__ __forceinline__ float quad_sum(float x) {
   x += __shfl_xor_sync(0xffffffffu, x, 1);
@@ -126,54 +88,29 @@ enum { C_R = 0, C_W = 1, C_A = 2, C_B = 3, C_DY = 4, C_NV = 5 };  // vectors sta
 constexpr int kCarryStages = 4;
 constexpr int kCarryThreads = 384;  // warps 0-3: state; 4-7: forming (F); 8-11: products (P)
 
-// Operands of one chunk for the carry update, fp32 inputs (fp32 values, split as they
-// enter a product).
-struct OpC {
-  float Rh[kL * kLD64];   // R^ [t][j]
-  float DYs[kL * kLD64];  // DY [t][i] (bf16 values)
-  float Btp[kL * kLD64];  // T^T Bb [t][j]
-  float Ah68[kL * kLDT];  // A^ [t][j]
-  float W[kL * kLD16];    // Mbr T [s][t]
-  float cL[kN];           // c(L), fp32
-  int unsafe;
-  int pad_[3];
-};
-
-// Per chunk in flight between the forming and the products group.
-struct ScratchC {
-  float Ah[kL * kLD64], Bt[kL * kLD64];  // A^, B~ [t][j]
-  float Bb68[kL * kLDT];                 // Bb [t][j]
-  float Mbr[kL * kLD16], Mba[kL * kLD16];  // R^ B~^T (with diagonal), A^ B~^T (strictly lower) [t][s]
-};
-
-// The same for bf16 inputs: bf16 tiles (rows of kB64 / kB16 elements, read by ldmatrix).
-// The forming group writes the vectors, the products group adds Mbr and T a round later,
-// the state warps read them all a round after that.
+// Operands of one chunk for the carry update: bf16 tiles (rows of kB64 / kB16 elements,
+// read by ldmatrix) in kP parts, one for bf16 inputs and hi + lo for fp32 inputs. The
+// forming group writes the vectors and the two Gram blocks, the products group adds T a
+// round later, the state warps read them all a round after that.
+template <int kP>
 struct alignas(16) OpC16 {
-  bf16_t Rh[kL * kB64];   // R^ [t][j]
-  bf16_t DYs[kL * kB64];  // DY [t][i]
-  bf16_t Ah[kL * kB64];   // A^ [t][j]
-  bf16_t Bb[kL * kB64];   // Bb [s][j]
-  bf16_t Mbr[kL * kB16];  // R^ B~^T (with diagonal) [t][s]
-  bf16_t Tm[kL * kB16];   // T = (I - Mba)^-1 [t][s]
-  float cL[kN];           // c(L), fp32
+  bf16_t Rh[kP][kL * kB64];   // R^ [t][j]
+  bf16_t DYs[kP][kL * kB64];  // DY [t][i]
+  bf16_t Ah[kP][kL * kB64];   // A^ [t][j]
+  bf16_t Bb[kP][kL * kB64];   // Bb [s][j]
+  bf16_t Mbr[kP][kL * kB16];  // R^ B~^T (with diagonal) [t][s]
+  bf16_t Tm[kP][kL * kB16];   // T = (I - Mba)^-1 [t][s]
+  float cL[kN];               // c(L), fp32
   int unsafe;
   int pad_[3];
 };
+template <int kP>
 struct alignas(16) ScratchC16 {
-  bf16_t Bt[kL * kB64];   // B~ [t][j]
-  float Mba[kL * kLD16];  // A^ B~^T (strictly lower) [t][s], fp32: T is formed from it
+  bf16_t Bt[kP][kL * kB64];  // B~ [t][j]
+  float Mba[kL * kLD16];     // A^ B~^T (strictly lower) [t][s], fp32: T is formed from it
 };
 template <typename TIn>
-struct CarryIo {  // bf16 inputs: bf16 operands
-  using Op = OpC16;
-  using Scratch = ScratchC16;
-};
-template <>
-struct CarryIo<float> {  // fp32 inputs: split tf32
-  using Op = OpC;
-  using Scratch = ScratchC;
-};
+constexpr int kCarryParts = sizeof(TIn) == 2 ? 1 : 2;
 
 // Shared memory of the carry kernel for bf16 (TIn = bf16_t: six vectors per stage, the
 // epilogue's nv the sixth; carries stored as bf16) or fp32 inputs (five vectors; carries
@@ -181,11 +118,11 @@ struct CarryIo<float> {  // fp32 inputs: split tf32
 template <typename TIn>
 struct CarrySmemT {
   static constexpr int kVecs = sizeof(TIn) == 2 ? 6 : 5;
+  static constexpr int kP = kCarryParts<TIn>;
   typedef TIn CarryT;
   TIn raw[kCarryStages][kVecs][kTile];  // r, w, a, b, dy (or dout), nv (epilogue) of one chunk per stage
-  typename CarryIo<TIn>::Op op[3];
-  typename CarryIo<TIn>::Scratch sc[2];
-  float TT[kL * kLD16];   // T^T, T = (I - Mba)^-1 (fp32 inputs)
+  OpC16<kP> op[3];
+  ScratchC16<kP> sc[2];
   float Pc[4][kN];       // products of the decays of four-step blocks
   TIn gst[2][kN * 72];   // carries on their way out (state warps write, products warps store)
   uint64_t full[kCarryStages];
@@ -219,9 +156,9 @@ __device__ __forceinline__ __nv_bfloat162 gn_backward_row(float2 d, float2 nv, f
 // products chained in step order. Returns (uniformly over the group) whether
 // some decay leaves the range of the scaled form.
 template <typename TIn, bool kLogit, bool kEpi>
-__device__ bool form_carry(typename CarryIo<TIn>::Scratch& sc, float (&Pc)[4][kN], TIn* rs,
-                           typename CarryIo<TIn>::Op& op, int len, int ftid, const float* epi_rstd, float2 epi_lw) {
-  constexpr bool kX3 = sizeof(TIn) == 4;
+__device__ bool form_carry(ScratchC16<kCarryParts<TIn>>& sc, float (&Pc)[4][kN], TIn* rs,
+                           OpC16<kCarryParts<TIn>>& op, int len, int ftid, const float* epi_rstd, float2 epi_lw) {
+  constexpr int kP = kCarryParts<TIn>, kLo = kP - 1;  // index of the lo part (the hi part for kP = 1)
   const int lane = ftid & 31, pf = ftid >> 5, j = 2 * lane, t0 = 4 * pf;
   float2 wv[4], av[4], rv[4], bv[4], dyv[4];
   if constexpr (kEpi) {  // epilogue: the stage holds dout and nv; dy replaces dout (the step-by-step path reads it)
@@ -266,66 +203,41 @@ __device__ bool form_carry(typename CarryIo<TIn>::Scratch& sc, float (&Pc)[4][kN
     const float2 cprev = c;
     c = fmul2(c, wv[e]);
     const float2 ic = make_float2(rcp_approx(c.x), rcp_approx(c.y));
-    if constexpr (kX3) {
-      const int q = t * kLD64 + j, q68 = t * kLDT + j;
-      const float2 ah = fmul2(av[e], cprev);
-      *reinterpret_cast<float2*>(sc.Ah + q) = ah;
-      *reinterpret_cast<float2*>(op.Ah68 + q68) = ah;
-      *reinterpret_cast<float2*>(op.Rh + q) = fmul2(rv[e], c);
-      *reinterpret_cast<float2*>(sc.Bt + q) = fmul2(bv[e], ic);
-      *reinterpret_cast<float2*>(sc.Bb68 + q68) = fmul2(bv[e], fmul2(cL, ic));
-      *reinterpret_cast<float2*>(op.DYs + q) = dyv[e];
-    } else {
-      const int q = t * kB64 + j;
-      st_pair(op.Ah + q, fmul2(av[e], cprev));
-      st_pair(op.Rh + q, fmul2(rv[e], c));
-      st_pair(sc.Bt + q, fmul2(bv[e], ic));
-      st_pair(op.Bb + q, fmul2(bv[e], fmul2(cL, ic)));
-      st_pair(op.DYs + q, dyv[e]);  // bf16 values already: exact
-    }
+    const int q = t * kB64 + j;
+    st_pair_p<kP>(op.Ah[0] + q, op.Ah[kLo] + q, fmul2(av[e], cprev));
+    st_pair_p<kP>(op.Rh[0] + q, op.Rh[kLo] + q, fmul2(rv[e], c));
+    st_pair_p<kP>(sc.Bt[0] + q, sc.Bt[kLo] + q, fmul2(bv[e], ic));
+    st_pair_p<kP>(op.Bb[0] + q, op.Bb[kLo] + q, fmul2(bv[e], fmul2(cL, ic)));
+    st_pair_p<kP>(op.DYs[0] + q, op.DYs[kLo] + q, dyv[e]);  // bf16 inputs: exact
   }
   return false;
 }
 
-// n-tile nt of P Q^T (16 x 16, K = 64, tf32 values, stride kLD64) stored to M
-// (stride kLD16) as tf32, masked to s < t (strict) or s <= t.
-template <bool kX3>
-__device__ __forceinline__ void gram_tile(float* M, const float* P, const float* Q, int nt, bool strict, int lane) {
-  const int g = lane >> 2, t4 = lane & 3;
-  float acc[4];
-  zero4(acc);
-#pragma unroll
-  for (int kb = 0; kb < kN / 8; ++kb) {
-    FragA<kX3> a;
-    FragB<kX3> b;
-    ld_a(a, P, kLD64, 0, 8 * kb, g, t4);
-    ld_b(b, Q, kLD64, 8 * nt, 8 * kb, g, t4);
-    mma_x(acc, a, b);
-  }
-#pragma unroll
-  for (int h = 0; h < 2; ++h) {
-    const int t = g + 8 * h, s = 8 * nt + 2 * t4;
-    const bool k0 = strict ? s < t : s <= t, k1 = strict ? s + 1 < t : s + 1 <= t;
-    *reinterpret_cast<float2*>(M + t * kLD16 + s) =
-        make_float2(k0 ? op_val<kX3>(acc[2 * h]) : 0.f, k1 ? op_val<kX3>(acc[2 * h + 1]) : 0.f);
-  }
-}
-
-// n-tile nt of P Q^T (16 x 8, K = 64, bf16 tiles of stride kB64), masked to s < t (strict)
-// or s <= t, stored as fp32 (stride kLD16) or bf16 (stride kB16).
+// n-tile nt of P Q^T (16 x 8, K = 64, bf16 tiles of stride kB64 in kP parts: P and Q the
+// hi parts, Pl and Ql the lo parts), masked to s < t (strict) or s <= t, stored as fp32
+// (stride kLD16, to M) or in kP bf16 parts (stride kB16, to M and Ml).
 __device__ __forceinline__ void ldsm2(uint32_t (&r)[2], const bf16_t* p) {
   asm volatile("ldmatrix.sync.aligned.m8n8.x2.shared.b16 {%0,%1}, [%2];" : "=r"(r[0]), "=r"(r[1]) : "r"(smem_addr(p)));
 }
-template <typename TOut>
-__device__ __forceinline__ void gram_tile16(TOut* M, const bf16_t* P, const bf16_t* Q, int nt, bool strict, int lane) {
+template <int kP, typename TOut>
+__device__ __forceinline__ void gram_tile16(TOut* M, TOut* Ml, const bf16_t* P, const bf16_t* Pl, const bf16_t* Q,
+                                            const bf16_t* Ql, int nt, bool strict, int lane) {
   const int g = lane >> 2, t4 = lane & 3;
   float acc[4];
   zero4(acc);
+  const int qo = (8 * nt + (lane & 7)) * kB64 + ((lane >> 3) & 1) * 8;
 #pragma unroll
   for (int kb = 0; kb < kN / 16; ++kb) {
     uint32_t a[4], b[2];
     a_mk(a, P, kB64, 0, 16 * kb, lane);
-    ldsm2(b, Q + (8 * nt + (lane & 7)) * kB64 + 16 * kb + ((lane >> 3) & 1) * 8);
+    ldsm2(b, Q + qo + 16 * kb);
+    if constexpr (kP == 2) {  // lo parts: a_lo b_hi + a_hi b_lo
+      uint32_t al[4], bl[2];
+      a_mk(al, Pl, kB64, 0, 16 * kb, lane);
+      ldsm2(bl, Ql + qo + 16 * kb);
+      mma16(acc, al, b[0], b[1]);
+      mma16(acc, a, bl[0], bl[1]);
+    }
     mma16(acc, a, b[0], b[1]);
   }
 #pragma unroll
@@ -336,16 +248,17 @@ __device__ __forceinline__ void gram_tile16(TOut* M, const bf16_t* P, const bf16
     if constexpr (sizeof(TOut) == 4)
       *reinterpret_cast<float2*>(M + t * kLD16 + s) = x;
     else
-      st_pair(M + t * kB16 + s, x);
+      st_pair_p<kP>(M + t * kB16 + s, Ml + t * kB16 + s, x);
   }
 }
 
 // Forming group: wait for a chunk's inputs and form its operands. Returns
 // false on a timeout.
 template <typename TIn, bool kLogit, bool kEpi>
-__device__ bool front_form(CarrySmemT<TIn>& sm, typename CarryIo<TIn>::Scratch& sc, typename CarryIo<TIn>::Op& op,
+__device__ bool front_form(CarrySmemT<TIn>& sm, ScratchC16<kCarryParts<TIn>>& sc, OpC16<kCarryParts<TIn>>& op,
                            TIn* rs, uint64_t* bar, uint32_t parity, int len, unsigned* status, const float* epi_rstd,
                            float2 epi_lw) {
+  constexpr int kP = kCarryParts<TIn>, kLo = kP - 1;
   const int ftid = threadIdx.x - 128;
   const bool ok = mbar_wait_bounded(status, bar, parity);
   if (named_bar_or(1, 128, !ok)) {
@@ -358,20 +271,18 @@ __device__ bool front_form(CarrySmemT<TIn>& sm, typename CarryIo<TIn>::Scratch& 
   named_bar(1, 128);
   // n-tile pf - 2 of Mba = A^ B~^T (warps 2, 3); the products group makes Mbr
   const int pf = ftid >> 5;
-  if constexpr (sizeof(TIn) == 4) {
-    if (pf >= 2) gram_tile<true>(sc.Mba, sc.Ah, sc.Bt, pf - 2, true, ftid & 31);
-  } else {  // n-tile pf % 2 of Mba (warps 0, 1; fp32) or of Mbr (warps 2, 3; bf16)
-    if (pf < 2)
-      gram_tile16(sc.Mba, op.Ah, sc.Bt, pf, true, ftid & 31);
-    else
-      gram_tile16(op.Mbr, op.Rh, sc.Bt, pf - 2, false, ftid & 31);
-  }
+  // n-tile pf % 2 of Mba (warps 0, 1; fp32) or of Mbr (warps 2, 3; kP bf16 parts)
+  if (pf < 2)
+    gram_tile16<kP>(sc.Mba, sc.Mba, op.Ah[0], op.Ah[kLo], sc.Bt[0], sc.Bt[kLo], pf, true, ftid & 31);
+  else
+    gram_tile16<kP>(op.Mbr[0], op.Mbr[kLo], op.Rh[0], op.Rh[kLo], sc.Bt[0], sc.Bt[kLo], pf - 2, false, ftid & 31);
   return true;
 }
 
-// Products group (128 threads), bf16 operands: T = (I - Mba)^-1 by fp32 forward
-// substitution (warp 0; the forming group made Mba and Mbr), stored as bf16.
-__device__ void front_products16(ScratchC16& sc, OpC16& op) {
+// Products group (128 threads): T = (I - Mba)^-1 by fp32 forward substitution (warp 0; the
+// forming group made Mba and Mbr), stored in kP bf16 parts.
+template <int kP>
+__device__ void front_products16(ScratchC16<kP>& sc, OpC16<kP>& op) {
   const int pp = (threadIdx.x >> 5) - 8, lane = threadIdx.x & 31;
   if (pp != 0) return;
   const int s = lane & 15;
@@ -385,148 +296,40 @@ __device__ void front_products16(ScratchC16& sc, OpC16& op) {
   }
   if (lane < 16) {
 #pragma unroll
-    for (int tt = 0; tt < kL; ++tt) op.Tm[tt * kB16 + s] = __float2bfloat16_rn(col[tt]);
+    for (int tt = 0; tt < kL; ++tt) put_p<kP>(op.Tm[0] + tt * kB16 + s, op.Tm[kP - 1] + tt * kB16 + s, col[tt]);
   }
 }
 
-// Products group (128 threads), fp32 inputs: T, Mbr = R^ B~^T (with diagonal), T^T Bb and
-// Mbr T of a formed chunk, in split tf32.
-template <typename TIn>
-__device__ void front_products(CarrySmemT<TIn>& sm, ScratchC& sc, OpC& op) {
-  constexpr bool kX3 = sizeof(TIn) == 4;
-  const int pp = (threadIdx.x >> 5) - 8, lane = threadIdx.x & 31, g = lane >> 2, t4 = lane & 3;
-  if (pp == 0) unit_lower_inverse<kX3>(sc.Mba, nullptr, sm.TT, lane);
-  else if (pp <= 2) gram_tile<kX3>(sc.Mbr, op.Rh, sc.Bt, pp - 1, false, lane);
-  named_bar(2, 128);
-  {  // T^T Bb, n-tiles 2 pp and 2 pp + 1
-    float acc[2][4];
-    zero4(acc[0]);
-    zero4(acc[1]);
-#pragma unroll
-    for (int kb = 0; kb < 2; ++kb) {
-      FragA<kX3> a;
-      ld_a(a, sm.TT, kLD16, 0, 8 * kb, g, t4);
-#pragma unroll
-      for (int nt = 0; nt < 2; ++nt) {
-        FragB<kX3> b;
-        ld_b_t(b, sc.Bb68, kLDT, 8 * (2 * pp + nt), 8 * kb, g, t4);
-        mma_x(acc[nt], a, b);
-      }
-    }
-#pragma unroll
-    for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-      for (int h = 0; h < 2; ++h)
-        *reinterpret_cast<float2*>(op.Btp + (g + 8 * h) * kLD64 + 8 * (2 * pp + nt) + 2 * t4) =
-            make_float2(op_val<kX3>(acc[nt][2 * h]), op_val<kX3>(acc[nt][2 * h + 1]));
-  }
-  if (pp >= 2) {  // W = Mbr T, n-tile pp - 2
-    const int q = pp - 2;
-    float acc[4];
-    zero4(acc);
-#pragma unroll
-    for (int kb = 0; kb < 2; ++kb) {
-      FragA<kX3> a;
-      FragB<kX3> b;
-      ld_a(a, sc.Mbr, kLD16, 0, 8 * kb, g, t4);
-      ld_b(b, sm.TT, kLD16, 8 * q, 8 * kb, g, t4);
-      mma_x(acc, a, b);
-    }
-#pragma unroll
-    for (int h = 0; h < 2; ++h)
-      *reinterpret_cast<float2*>(op.W + (g + 8 * h) * kLD16 + 8 * q + 2 * t4) =
-          make_float2(op_val<kX3>(acc[2 * h]), op_val<kX3>(acc[2 * h + 1]));
-  }
-}
-
-// One chunk of the carry (state warp, rows i0 .. i0+15 of G):
-//   DSA^T = G (T^T Bb)^T + DY^T (Mbr T);  G <- G diag(c(L)) + DY^T R^ + DSA^T A^
-template <bool kX3>
-__device__ __forceinline__ void carry_chunk(float (&G)[8][4], const OpC& op, int i0, int g, int t4) {
-  FragA<kX3> aD[2];
-#pragma unroll
-  for (int kb = 0; kb < 2; ++kb) ld_a_ts(aD[kb], op.DYs, kLD64, i0, 8 * kb, g, t4);  // DY^T (hardware k order)
-  float DS[2][4];
-  zero4(DS[0]);
-  zero4(DS[1]);
-#pragma unroll
-  for (int kb = 0; kb < 2; ++kb)
-#pragma unroll
-    for (int q = 0; q < 2; ++q) {
-      FragB<kX3> b;
-      ld_b_ts(b, op.W, kLD16, 8 * q, 8 * kb, g, t4);
-      mma_x(DS[q], aD[kb], b);
-    }
-#pragma unroll
-  for (int kb = 0; kb < 8; ++kb) {
-    FragA<kX3> aG;
-    acc_to_a(aG, G[kb]);
-#pragma unroll
-    for (int q = 0; q < 2; ++q) {
-      FragB<kX3> b;
-      ld_b(b, op.Btp, kLD64, 8 * q, 8 * kb, g, t4);
-      mma_x(DS[q], aG, b);
-    }
-  }
-#pragma unroll
-  for (int nt = 0; nt < 8; ++nt) {
-    const float2 cl = *reinterpret_cast<const float2*>(op.cL + 8 * nt + 2 * t4);
-    G[nt][0] *= cl.x;
-    G[nt][1] *= cl.y;
-    G[nt][2] *= cl.x;
-    G[nt][3] *= cl.y;
-  }
-#pragma unroll
-  for (int kb = 0; kb < 2; ++kb)
-#pragma unroll
-    for (int nt = 0; nt < 8; ++nt) {
-      FragB<kX3> b;
-      ld_b_ts(b, op.Rh, kLD64, 8 * nt, 8 * kb, g, t4);
-      mma_x(G[nt], aD[kb], b);
-    }
-  FragA<kX3> aS[2];
-  acc_to_a(aS[0], DS[0]);
-  acc_to_a(aS[1], DS[1]);
-#pragma unroll
-  for (int kb = 0; kb < 2; ++kb)
-#pragma unroll
-    for (int nt = 0; nt < 8; ++nt) {
-      FragB<kX3> b;
-      ld_b_t(b, op.Ah68, kLDT, 8 * nt, 8 * kb, g, t4);
-      mma_x(G[nt], aS[kb], b);
-    }
-}
-
-// The same with bf16 operands (bf16 inputs), T applied last:
+// One chunk of the carry (state warp, rows i0 .. i0+15 of G), T applied last:
 //   DSA^T = (G Bb^T + DY^T Mbr) T;  G <- G diag(c(L)) + DY^T R^ + DSA^T A^
-// G, DY, Bb, Mbr, T, R^, A^ and the intermediate products enter as bf16; G stays fp32 in
-// its accumulator tiles.
-__device__ __forceinline__ void carry_chunk16(float (&G)[8][4], const OpC16& op, int i0, int t4, int lane) {
-  uint32_t aD[4], b[4];
-  a_km(aD, op.DYs, kB64, i0, 0, lane);  // DY^T rows i0.., k = s (DY stored [s][i])
+// Every operand enters in kP bf16 parts (G, X and DSA^T split from their fp32 accumulator
+// tiles); G stays fp32 in its accumulator tiles.
+template <int kP>
+__device__ __forceinline__ void carry_chunk16(float (&G)[8][4], const OpC16<kP>& op, int i0, int t4, int lane) {
+  constexpr int kLo = kP - 1;
+  using Acc2 = float[2][4];
+  FragP<kP> aD, b;
+  a_km_p<kP>(aD, op.DYs[0], op.DYs[kLo], kB64, i0, 0, lane);  // DY^T rows i0.., k = s (DY stored [s][i])
   float X[2][4];
   zero4(X[0]);
   zero4(X[1]);
-  b_kn(b, op.Mbr, kB16, 0, 0, lane);  // Mbr [u][s]
-  mma16(X[0], aD, b[0], b[1]);
-  mma16(X[1], aD, b[2], b[3]);
+  b_kn_p<kP>(b, op.Mbr[0], op.Mbr[kLo], kB16, 0, 0, lane);  // Mbr [u][s]
+  mma_pp<kP, kP>(X, aD, b);
 #pragma unroll
   for (int kb = 0; kb < 4; ++kb) {
-    uint32_t aG[4];
-    c2a16(aG, G[2 * kb], G[2 * kb + 1]);
-    b_nk(b, op.Bb, kB64, 0, 16 * kb, lane);  // Bb^T: Bb stored [s][j]
-    mma16(X[0], aG, b[0], b[1]);
-    mma16(X[1], aG, b[2], b[3]);
+    FragP<kP> aG;
+    c2a_p<kP>(aG, G[2 * kb], G[2 * kb + 1]);
+    b_nk_p<kP>(b, op.Bb[0], op.Bb[kLo], kB64, 0, 16 * kb, lane);  // Bb^T: Bb stored [s][j]
+    mma_pp<kP, kP>(X, aG, b);
   }
   float DS[2][4];
   zero4(DS[0]);
   zero4(DS[1]);
   {
-    uint32_t aX[4];
-    c2a16(aX, X[0], X[1]);
-    b_kn(b, op.Tm, kB16, 0, 0, lane);  // T [s][t]
-    mma16(DS[0], aX, b[0], b[1]);
-    mma16(DS[1], aX, b[2], b[3]);
+    FragP<kP> aX;
+    c2a_p<kP>(aX, X[0], X[1]);
+    b_kn_p<kP>(b, op.Tm[0], op.Tm[kLo], kB16, 0, 0, lane);  // T [s][t]
+    mma_pp<kP, kP>(DS, aX, b);
   }
 #pragma unroll
   for (int nt = 0; nt < 8; ++nt) {
@@ -538,17 +341,15 @@ __device__ __forceinline__ void carry_chunk16(float (&G)[8][4], const OpC16& op,
   }
 #pragma unroll
   for (int np = 0; np < 4; ++np) {  // + DY^T R^ (R^ stored [t][j])
-    b_kn(b, op.Rh, kB64, 16 * np, 0, lane);
-    mma16(G[2 * np], aD, b[0], b[1]);
-    mma16(G[2 * np + 1], aD, b[2], b[3]);
+    b_kn_p<kP>(b, op.Rh[0], op.Rh[kLo], kB64, 16 * np, 0, lane);
+    mma_pp<kP, kP>(reinterpret_cast<Acc2&>(G[2 * np]), aD, b);
   }
-  uint32_t aS[4];
-  c2a16(aS, DS[0], DS[1]);
+  FragP<kP> aS;
+  c2a_p<kP>(aS, DS[0], DS[1]);
 #pragma unroll
   for (int np = 0; np < 4; ++np) {  // + DSA^T A^
-    b_kn(b, op.Ah, kB64, 16 * np, 0, lane);
-    mma16(G[2 * np], aS, b[0], b[1]);
-    mma16(G[2 * np + 1], aS, b[2], b[3]);
+    b_kn_p<kP>(b, op.Ah[0], op.Ah[kLo], kB64, 16 * np, 0, lane);
+    mma_pp<kP, kP>(reinterpret_cast<Acc2&>(G[2 * np]), aS, b);
   }
 }
 
@@ -672,11 +473,7 @@ __global__ void __launch_bounds__(kCarryThreads, 1) wkv7_bwd4_carry_kernel(const
   };
   auto products = [&](int v) {  // products group
     const int c = chunk_of(v);
-    if (sm.op[c % 3].unsafe) return;
-    if constexpr (kX3)
-      front_products<TIn>(sm, sm.sc[c & 1], sm.op[c % 3]);
-    else
-      front_products16(sm.sc[c & 1], sm.op[c % 3]);
+    if (!sm.op[c % 3].unsafe) front_products16<Smem::kP>(sm.sc[c & 1], sm.op[c % 3]);
   };
   // TMA copies are issued by a products-group thread (that group has the most slack); the
   // forming group waits for them
@@ -742,10 +539,8 @@ __global__ void __launch_bounds__(kCarryThreads, 1) wkv7_bwd4_carry_kernel(const
       }
       if (op.unsafe)
         carry_direct<TIn, kLogit>(G, sm.raw[st][0], len_of(m), i0, g, t4);
-      else if constexpr (kX3)
-        carry_chunk<true>(G, op, i0, g, t4);
       else
-        carry_chunk16(G, op, i0, t4, lane);
+        carry_chunk16<Smem::kP>(G, op, i0, t4, lane);
     } else if (role == 1) {
       if (m + 2 < nchunks) form(m + 2);
     } else {
@@ -2159,7 +1954,7 @@ cudaError_t launch_bwd4_impl(const BwdArgs& args, cudaStream_t stream) {
   return cudaGetLastError();
 }
 
-// fp32 inputs: the carry chain alone, in split tf32, storing fp32 carries.
+// fp32 inputs: the carry chain alone, in split bf16, storing fp32 carries.
 cudaError_t launch_bwd4_carry_f32(const BwdArgs& args, cudaStream_t stream) {
   const size_t smem = sizeof(CarrySmemT<float>);
   static_assert(sizeof(CarrySmemT<float>) <= 227 * 1024, "shared memory over budget");

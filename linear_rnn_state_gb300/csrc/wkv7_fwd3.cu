@@ -13,12 +13,14 @@
 //   Y   = R^ S0^T + Mkr V + Mbr SA                   rows: y(t)
 //   S(L) = S0 diag(c(L)) + V^T Kb + SA^T Bb
 // (exact up to rounding; the reverse scan uses the same algebra). The
-// products run on tensor cores with fp32 accumulation; the state stays fp32
-// in registers. With bf16 inputs the products take bf16 operands (mma.sync
-// m16n8k16, wkv7_mma16.cuh): the inputs' own precision, the scaled operands
-// and the state rounded to bf16 as they enter a product. With fp32 inputs
-// each product is taken in split tf32, three tf32 products (wkv7_mma.cuh,
-// mma_x), so the result keeps fp32 accuracy.
+// products run on tensor cores with bf16 operands (mma.sync m16n8k16,
+// wkv7_mma16.cuh) and fp32 accumulation; the state stays fp32 in registers.
+// With bf16 inputs each operand is one bf16 value (the inputs' own precision;
+// the scaled operands and the state rounded to bf16 as they enter a product).
+// With fp32 inputs each operand is a pair hi + lo of bf16 values (hi = x
+// rounded to bf16, lo = the remainder rounded to bf16) and a product a b is
+// taken as a_lo b_hi + a_hi b_lo + a_hi b_hi, about 16 bits of each operand.
+// The state update takes Kb and Bb as such pairs for either input type.
 //
 // One CTA per (b, h), twelve warps in three groups working one chunk apart:
 //  - forming warps (4..7) turn chunk n+2's r, w, k, v, a, b (TMA tensor loads
@@ -46,59 +48,43 @@ constexpr int kN = 64, kL = 16;
 constexpr int kLD64 = 72;  // row stride (floats) of 64-wide operands: conflict-free fragment loads
 constexpr int kLD16 = 24;  // row stride of 16-wide operands
 
-// Operand block of one chunk for fp32 inputs (fp32 values, split as they enter a product).
-struct Prep3 {
-  float X1[2 * kL * kLD64];  // rows 0..15: a^(t); rows 16..31: r^(t)   [t][j]
-  float VT[kN * kLD16];      // v(s)[i]                                   [i][s]
-  float KbT[kN * kLD16];     // k(s)[j] c(L)[j] / c(s)[j]                 [j][s]
-  float BbT[kN * kLD16];     // b(s)[j] c(L)[j] / c(s)[j]                 [j][s]
-  float M[4][kL * kLD16];    // Mka, Mba (strictly lower), Mkr, Mbr (lower) [t][s]
-  float Tinv[kL * kLD16];    // (I - Mba)^-1                              [t][s]
-  float cL[kN];              // c(L) (fp32)
-  float ph[2][kN];           // decay logits: product of each half's 8 decays
-  int unsafe;
-  int pad_[31];
-};
-
-// Operand block of one chunk for bf16 inputs (bf16 operands; row strides of 72 and 24
-// elements put the eight 16-byte rows of every ldmatrix on distinct banks).
+// Operand block of one chunk: bf16 tiles (row strides of 72 and 24 elements put the eight
+// 16-byte rows of every ldmatrix on distinct banks). kP = 1 (bf16 inputs): each operand is
+// one bf16 value, the inputs' own precision. kP = 2 (fp32 inputs): each operand is a pair
+// hi + lo ([0] = the value rounded to bf16, [1] = the remainder rounded to bf16), about 16
+// bits, and a product a b is taken as a_lo b_hi + a_hi b_lo + a_hi b_hi. Kb and Bb are
+// pairs either way: the state update keeps them to about 16 bits.
+template <int kP>
 struct alignas(16) Prep16 {
-  bf16_t X1[2 * kL * kB64];  // rows 0..15: a^(t); rows 16..31: r^(t)   [t][j]
-  bf16_t VT[kN * kB16];      // v(s)[i]                                   [i][s]
-  // k(s)[j] c(L)[j] / c(s)[j] and b(s)[j] c(L)[j] / c(s)[j], each as a bf16 pair hi + lo
-  // ([0] = hi, the value rounded to bf16; [1] = lo, the remainder rounded to bf16): the
-  // state update takes them at about 16 bits, the rest of the chunk at the inputs' 8
-  bf16_t KbT[2][kN * kB16];  // [j][s]
-  bf16_t BbT[2][kN * kB16];  // [j][s]
-  bf16_t M[3][kL * kB16];    // Mka (strictly lower), Mkr, Mbr (lower)    [t][s]
-  bf16_t Tinv[kL * kB16];    // (I - Mba)^-1                              [t][s]
-  float Mba[kL * kLD16];     // Mba (strictly lower, fp32: T is formed from it)
-  float cL[kN];              // c(L) (fp32)
-  float ph[2][kN];           // decay logits: product of each half's 8 decays
+  bf16_t X1[kP][2 * kL * kB64];  // rows 0..15: a^(t); rows 16..31: r^(t)   [t][j]
+  bf16_t VT[kP][kN * kB16];      // v(s)[i]                                   [i][s]
+  bf16_t KbT[2][kN * kB16];      // k(s)[j] c(L)[j] / c(s)[j]                 [j][s]
+  bf16_t BbT[2][kN * kB16];      // b(s)[j] c(L)[j] / c(s)[j]                 [j][s]
+  bf16_t M[kP][3][kL * kB16];    // Mka (strictly lower), Mkr, Mbr (lower)    [t][s]
+  bf16_t Tinv[kP][kL * kB16];    // (I - Mba)^-1                              [t][s]
+  float Mba[kL * kLD16];         // Mba (strictly lower, fp32: T is formed from it)
+  float cL[kN];                  // c(L) (fp32)
+  float ph[2][kN];               // decay logits: product of each half's 8 decays
   int unsafe;
   int pad_[31];
 };
 
-// Per input type: input ring depth, checkpoint staging, operand block and operand type,
-// and the row strides of the k~/b~ block and of the staged y rows.
+// Per input type: input ring depth, checkpoint staging, operand parts and the row stride
+// of the staged y rows.
 template <typename TIn>
 struct Fwd3Io;
 template <>
 struct Fwd3Io<__nv_bfloat16> {
   static constexpr int kStages = 4;
   static constexpr bool kStageCk = true;
-  using Prep = Prep16;
-  using Op = bf16_t;
-  static constexpr int kLDX = kB64;
+  static constexpr int kP = 1;
   static constexpr int kYS = kB64;  // padded: the transposed matrix stores of y hit distinct banks
 };
 template <>
 struct Fwd3Io<float> {
   static constexpr int kStages = 3;
   static constexpr bool kStageCk = false;
-  using Prep = Prep3;
-  using Op = float;
-  static constexpr int kLDX = kLD64;
+  static constexpr int kP = 2;
   static constexpr int kYS = kN;
 };
 
@@ -108,8 +94,8 @@ struct Fwd3Smem {
   static constexpr int kStages = Io::kStages;
   static constexpr bool kStageCk = Io::kStageCk;
   TIn raw[kStages][6][kL * kN];  // TMA ring: r, w, k, v, a, b of one chunk per stage
-  typename Io::Prep prep[3];
-  typename Io::Op X2[2][2 * kL * Io::kLDX];  // per chunk in flight: rows 0..15: k~(s); rows 16..31: b~(s)   [s][j]
+  Prep16<Io::kP> prep[3];
+  bf16_t X2[2][Io::kP][2 * kL * kB64];  // per chunk in flight: rows 0..15: k~(s); rows 16..31: b~(s)   [s][j]
   TIn ys[2][kL * Io::kYS];  // y of the chunk [t][i], on its way out (state warps write, products warps store)
   // epilogue: the head's ln_w, ln_b, r_k; per chunk (ring of 4, written by the forming
   // group two rounds before the state warps run the chunk, read by the products group the
@@ -133,26 +119,13 @@ __device__ __forceinline__ float2 bf2(const __nv_bfloat16* p) {
 }
 __device__ __forceinline__ float2 bf2(const float* p) { return *reinterpret_cast<const float2*>(p); }
 
-template <typename TIn>
-constexpr bool kSplitOf = sizeof(TIn) == 4;  // fp32 inputs: products in split tf32
-
-// An operand value as stored for the products: rounded to tf32 once (one
-// product per multiply), or kept in fp32 (split products).
-template <bool kX3>
-__device__ __forceinline__ float op_val(float x) {
-  if constexpr (kX3)
-    return x;
-  else
-    return tf32r(x);
-}
-
 // ---------------------------------------------------------- forming group ---
 // 128 threads; thread (j = ptid % 64, half = ptid / 64) forms column j of
 // steps 8*half .. 8*half+7.
 template <typename TIn, bool kLogit, bool kEpi>
-__device__ void form_chunk(Fwd3Smem<TIn>& sm, typename Fwd3Io<TIn>::Prep& P, typename Fwd3Io<TIn>::Op* X2, int stage,
+__device__ void form_chunk(Fwd3Smem<TIn>& sm, Prep16<Fwd3Io<TIn>::kP>& P, bf16_t (*X2)[2 * kL * kB64], int stage,
                            int len, int ptid, int eslot) {
-  constexpr bool kX3 = kSplitOf<TIn>;  // fp32 inputs: fp32 operands; bf16 inputs: bf16 operands
+  constexpr int kP = Fwd3Io<TIn>::kP, kLo = kP - 1;  // index of the lo part (the hi part for kP = 1)
   const TIn* rs = sm.raw[stage][0];
   const int j = ptid & 63, half = ptid >> 6;
   // decays of this thread's 8 steps (wm) and of the other 8 (wo); padding
@@ -224,120 +197,57 @@ __device__ void form_chunk(Fwd3Smem<TIn>& sm, typename Fwd3Io<TIn>::Prep& P, typ
     c *= wm[e];
     const float ic = rcp_approx(c);
     const float a = av[e], r = rv[e], k = kv[e], b = bv[e];
-    if constexpr (kX3) {
-      X2[t * kLD64 + j] = k * ic;
-      X2[(kL + t) * kLD64 + j] = b * ic;
-      P.X1[t * kLD64 + j] = a * cprev;
-      P.X1[(kL + t) * kLD64 + j] = r * c;
-    } else {
-      X2[t * kB64 + j] = __float2bfloat16_rn(k * ic);
-      X2[(kL + t) * kB64 + j] = __float2bfloat16_rn(b * ic);
-      P.X1[t * kB64 + j] = __float2bfloat16_rn(a * cprev);
-      P.X1[(kL + t) * kB64 + j] = __float2bfloat16_rn(r * c);
-    }
+    const int o0 = t * kB64 + j, o1 = (kL + t) * kB64 + j;
+    put_p<kP>(X2[0] + o0, X2[kLo] + o0, k * ic);
+    put_p<kP>(X2[0] + o1, X2[kLo] + o1, b * ic);
+    put_p<kP>(P.X1[0] + o0, P.X1[kLo] + o0, a * cprev);
+    put_p<kP>(P.X1[0] + o1, P.X1[kLo] + o1, r * c);
     const float s = cL * ic;
     kbt[e] = k * s;
     bbt[e] = b * s;
   }
-  if constexpr (kX3) {
-#pragma unroll
-    for (int q = 0; q < 2; ++q) {
-      const int o = j * kLD16 + 8 * half + 4 * q;
-      *reinterpret_cast<float4*>(P.VT + o) = make_float4(vt[4 * q], vt[4 * q + 1], vt[4 * q + 2], vt[4 * q + 3]);
-      *reinterpret_cast<float4*>(P.KbT + o) = make_float4(kbt[4 * q], kbt[4 * q + 1], kbt[4 * q + 2], kbt[4 * q + 3]);
-      *reinterpret_cast<float4*>(P.BbT + o) = make_float4(bbt[4 * q], bbt[4 * q + 1], bbt[4 * q + 2], bbt[4 * q + 3]);
-    }
-  } else {
-    // eight steps of column j: one 16-byte row piece of each transposed block (v is bf16
-    // already; kb and bb as hi and lo parts)
-    auto pack8 = [](const float (&x)[8]) {
-      return make_uint4(pack_bf16(x[0], x[1]), pack_bf16(x[2], x[3]), pack_bf16(x[4], x[5]), pack_bf16(x[6], x[7]));
-    };
-    auto lo8 = [](float (&x)[8]) {  // x <- x - bf16(x), exact in fp32
-#pragma unroll
-      for (int e = 0; e < 8; ++e) x[e] -= __bfloat162float(__float2bfloat16_rn(x[e]));
-    };
-    const int o = j * kB16 + 8 * half;
-    *reinterpret_cast<uint4*>(P.VT + o) = pack8(vt);
-    *reinterpret_cast<uint4*>(P.KbT[0] + o) = pack8(kbt);
-    *reinterpret_cast<uint4*>(P.BbT[0] + o) = pack8(bbt);
-    lo8(kbt);
-    lo8(bbt);
-    *reinterpret_cast<uint4*>(P.KbT[1] + o) = pack8(kbt);
-    *reinterpret_cast<uint4*>(P.BbT[1] + o) = pack8(bbt);
-  }
+  // eight steps of column j: one 16-byte row piece of each transposed block, per part (v in
+  // kP parts: exact for bf16 inputs; kb and bb as hi and lo parts)
+  const int o = j * kB16 + 8 * half;
+  put8_p<kP>(P.VT[0] + o, P.VT[kLo] + o, vt);
+  put8_p<2>(P.KbT[0] + o, P.KbT[1] + o, kbt);
+  put8_p<2>(P.BbT[0] + o, P.BbT[1] + o, bbt);
   unsafe = named_bar_or(1, 128, unsafe);
   if (ptid == 0) P.unsafe = unsafe;
 }
 
 // --------------------------------------------------------- products group ---
-// The four L x L products and T of a formed chunk (128 threads; skipped by the
-// caller for a chunk in the direct form).
-template <bool kX3>
-__device__ void gram_chunk(Prep3& P, const float* X2, int gtid) {
-  const int pw = gtid >> 5, lane = gtid & 31, g = lane >> 2, t4 = lane & 3;
-  // Gram blocks: warp pw computes [A^ | R^](rows 16*(pw/2)) x [K~ | B~](rows 16*(pw%2))^T.
-  {
-    const int mt = pw >> 1, nb = pw & 1;
-    float acc[2][4];
-    zero4(acc[0]);
-    zero4(acc[1]);
-#pragma unroll
-    for (int kb = 0; kb < kN / 8; ++kb) {
-      FragA<kX3> a;
-      ld_a(a, P.X1, kLD64, 16 * mt, 8 * kb, g, t4);
-#pragma unroll
-      for (int nt = 0; nt < 2; ++nt) {
-        FragB<kX3> b;
-        ld_b(b, X2, kLD64, 16 * nb + 8 * nt, 8 * kb, g, t4);
-        mma_x(acc[nt], a, b);
-      }
-    }
-    const bool strict = mt == 0;  // Mka, Mba: s < t; Mkr, Mbr: s <= t
-    float* M = P.M[pw];
-#pragma unroll
-    for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        const int t = g + 8 * h, s = 8 * nt + 2 * t4;
-        const float x0 = (s < t || (!strict && s == t)) ? acc[nt][2 * h] : 0.f;
-        const float x1 = (s + 1 < t || (!strict && s + 1 == t)) ? acc[nt][2 * h + 1] : 0.f;
-        *reinterpret_cast<float2*>(M + t * kLD16 + s) = make_float2(op_val<kX3>(x0), op_val<kX3>(x1));
-      }
-  }
-  // T = (I - Mba)^-1 by forward substitution; warp 1 made Mba, so a warp
-  // barrier suffices. Lane s (< 16) owns column s.
-  if (pw == 1) {
-    __syncwarp();
-    const float* Mba = P.M[1];
-    const int s = lane & 15;
-    float col[kL];
-#pragma unroll
-    for (int t = 0; t < kL; ++t) {
-      float acc = t == s ? 1.f : 0.f;
-#pragma unroll
-      for (int u = 0; u < t; ++u) acc = fmaf(Mba[t * kLD16 + u], col[u], acc);
-      col[t] = acc;
-    }
-    if (lane < 16) {
-#pragma unroll
-      for (int t = 0; t < kL; ++t) P.Tinv[t * kLD16 + s] = op_val<kX3>(col[t]);
-    }
-  }
-}
-
-// The same for bf16 operands: the Gram blocks from bf16 operands (K = 64 in four k16
-// steps), Mka, Mkr, Mbr stored as bf16, Mba kept in fp32 for T, T stored as bf16.
-__device__ void gram_chunk16(Prep16& P, const bf16_t* X2, int gtid) {
+// The four L x L products and T of a formed chunk (128 threads; skipped by the caller for
+// a chunk in the direct form). Warp pw computes the Gram block [A^ | R^](rows 16 (pw / 2))
+// x [K~ | B~](rows 16 (pw % 2))^T (K = 64 in four k16 steps); Mka, Mkr, Mbr are stored in
+// kP bf16 parts, Mba in fp32, from which one warp forms T by fp32 forward substitution
+// and stores it in kP parts.
+template <int kP>
+__device__ void gram_chunk16(Prep16<kP>& P, const bf16_t (*X2)[2 * kL * kB64], int gtid) {
+  constexpr int kLo = kP - 1;
   const int pw = gtid >> 5, lane = gtid & 31, g = lane >> 2, t4 = lane & 3;
   const int mt = pw >> 1, nb = pw & 1;
   float acc[2][4];
   zero4(acc[0]);
   zero4(acc[1]);
-  mm_mk_nk<4>(acc, P.X1, kB64, 16 * mt, X2, kB64, 16 * nb, lane);
+#pragma unroll
+  for (int kb = 0; kb < 4; ++kb) {
+    FragP<kP> a, b;
+    a_mk_p<kP>(a, P.X1[0], P.X1[kLo], kB64, 16 * mt, 16 * kb, lane);
+    b_nk_p<kP>(b, X2[0], X2[kLo], kB64, 16 * nb, 16 * kb, lane);
+    mma_pp<kP, kP>(acc, a, b);
+  }
   if (pw != 1) {
     // pw 0: Mka (s < t); 2: Mkr, 3: Mbr (s <= t)
-    store_masked16(acc, P.M[pw == 0 ? 0 : pw - 1], true, pw >= 2, g, t4);
+    const int m = pw == 0 ? 0 : pw - 1;
+    store_masked16(acc, P.M[0][m], true, pw >= 2, g, t4);
+    if constexpr (kP == 2) {  // the remainders after rounding to bf16
+#pragma unroll
+      for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) acc[nt][e] -= __bfloat162float(__float2bfloat16_rn(acc[nt][e]));
+      store_masked16(acc, P.M[kLo][m], true, pw >= 2, g, t4);
+    }
     return;
   }
 #pragma unroll
@@ -361,7 +271,7 @@ __device__ void gram_chunk16(Prep16& P, const bf16_t* X2, int gtid) {
   }
   if (lane < 16) {
 #pragma unroll
-    for (int tt = 0; tt < kL; ++tt) P.Tinv[tt * kB16 + s] = __float2bfloat16_rn(col[tt]);
+    for (int tt = 0; tt < kL; ++tt) put_p<kP>(P.Tinv[0] + tt * kB16 + s, P.Tinv[kLo] + tt * kB16 + s, col[tt]);
   }
 }
 
@@ -425,108 +335,17 @@ __device__ __forceinline__ void store_state(const StateCtx& c, float* dst, const
   }
 }
 
-// Chunk on tensor cores. Writes the chunk's y into ys.
-// (fp32 inputs: every product in split tf32)
+// Chunk on tensor cores with bf16 operands in kP parts (bf16 inputs: one; fp32 inputs: hi
+// + lo). Four k16 steps over j for S0 [A^ R^]^T, one k16 step over s for every product
+// with V, T, Mbr; Kb and Bb enter the state update as hi + lo pairs, so the carried state
+// keeps them to about 16 bits. The state, P and SA enter the next product in kP parts.
+// Writes the chunk's y into ys: bf16 rows of stride kB64 by transposed matrix stores, or
+// fp32 rows of stride kN.
 template <typename TIn>
-__device__ void state_chunk(StateCtx& c, Fwd3Smem<TIn>& sm, const Prep3& P) {
-  constexpr bool kX3 = kSplitOf<TIn>;
-  const int g = c.g, t4 = c.t4, i0 = c.i0;
-  // PA = S0 A^^T (later + V^T Mka^T), PR = S0 R^^T (later + ...): [i][t]
-  float PA[2][4], PR[2][4];
-#pragma unroll
-  for (int q = 0; q < 2; ++q) {
-    zero4(PA[q]);
-    zero4(PR[q]);
-  }
-#pragma unroll
-  for (int kb = 0; kb < 8; ++kb) {
-    FragA<kX3> a;
-    acc_to_a(a, c.S[kb]);
-#pragma unroll
-    for (int q = 0; q < 2; ++q) {
-      FragB<kX3> b;
-      ld_b(b, P.X1, kLD64, 8 * q, 8 * kb, g, t4);
-      mma_x(PA[q], a, b);
-      ld_b(b, P.X1, kLD64, kL + 8 * q, 8 * kb, g, t4);
-      mma_x(PR[q], a, b);
-    }
-  }
-  FragA<kX3> av[2];  // V^T rows i0.., k = s
-  ld_a(av[0], P.VT, kLD16, i0, 0, g, t4);
-  ld_a(av[1], P.VT, kLD16, i0, 8, g, t4);
-#pragma unroll
-  for (int kb = 0; kb < 2; ++kb)
-#pragma unroll
-    for (int q = 0; q < 2; ++q) {
-      FragB<kX3> b;
-      ld_b(b, P.M[0], kLD16, 8 * q, 8 * kb, g, t4);  // Mka
-      mma_x(PA[q], av[kb], b);
-      ld_b(b, P.M[2], kLD16, 8 * q, 8 * kb, g, t4);  // Mkr
-      mma_x(PR[q], av[kb], b);
-    }
-  // SA^T = PA T^T  [i][t]
-  float SA[2][4];
-  zero4(SA[0]);
-  zero4(SA[1]);
-#pragma unroll
-  for (int kb = 0; kb < 2; ++kb) {
-    FragA<kX3> a;
-    acc_to_a(a, PA[kb]);
-#pragma unroll
-    for (int q = 0; q < 2; ++q) {
-      FragB<kX3> b;
-      ld_b(b, P.Tinv, kLD16, 8 * q, 8 * kb, g, t4);
-      mma_x(SA[q], a, b);
-    }
-  }
-  FragA<kX3> asa[2];
-  acc_to_a(asa[0], SA[0]);
-  acc_to_a(asa[1], SA[1]);
-  // Y^T = PR + SA^T Mbr^T
-#pragma unroll
-  for (int kb = 0; kb < 2; ++kb)
-#pragma unroll
-    for (int q = 0; q < 2; ++q) {
-      FragB<kX3> b;
-      ld_b(b, P.M[3], kLD16, 8 * q, 8 * kb, g, t4);
-      mma_x(PR[q], asa[kb], b);
-    }
-#pragma unroll
-  for (int q = 0; q < 2; ++q)
-#pragma unroll
-    for (int h = 0; h < 2; ++h) {
-      const int i = i0 + g + 8 * h, t = 8 * q + 2 * t4;
-      st1(&sm.ys[c.yb][t * kN + i], PR[q][2 * h]);
-      st1(&sm.ys[c.yb][(t + 1) * kN + i], PR[q][2 * h + 1]);
-    }
-  // S(L) = S0 diag(c(L)) + V^T Kb + SA^T Bb
-#pragma unroll
-  for (int nt = 0; nt < 8; ++nt) {
-    const float2 cl = *reinterpret_cast<const float2*>(P.cL + 8 * nt + 2 * t4);
-    c.S[nt][0] *= cl.x;
-    c.S[nt][1] *= cl.y;
-    c.S[nt][2] *= cl.x;
-    c.S[nt][3] *= cl.y;
-  }
-#pragma unroll
-  for (int kb = 0; kb < 2; ++kb)
-#pragma unroll
-    for (int nt = 0; nt < 8; ++nt) {
-      FragB<kX3> b;
-      ld_b(b, P.KbT, kLD16, 8 * nt, 8 * kb, g, t4);
-      mma_x(c.S[nt], av[kb], b);
-      ld_b(b, P.BbT, kLD16, 8 * nt, 8 * kb, g, t4);
-      mma_x(c.S[nt], asa[kb], b);
-    }
-}
-
-// Chunk on tensor cores with bf16 operands (bf16 inputs). Four k16 steps over j for
-// S0 [A^ R^]^T, one k16 step over s for every product with V, T, Mbr; Kb and Bb enter
-// the state update as hi + lo pairs (two products each), so the carried state keeps
-// about 16 bits of them. Writes the chunk's y into ys (row stride kB64) by transposed
-// matrix stores.
-__device__ void state_chunk16(StateCtx& c, Fwd3Smem<bf16_t>& sm, const Prep16& P, int lane) {
+__device__ void state_chunk16(StateCtx& c, Fwd3Smem<TIn>& sm, const Prep16<Fwd3Io<TIn>::kP>& P, int lane) {
+  constexpr int kP = Fwd3Io<TIn>::kP, kLo = kP - 1;
   const int i0 = c.i0;
+  using Acc2 = float[2][4];
   // PA = S0 A^^T (later + V^T Mka^T), PR = S0 R^^T (later + ...): [i][t]
   float PA[2][4], PR[2][4];
 #pragma unroll
@@ -534,26 +353,22 @@ __device__ void state_chunk16(StateCtx& c, Fwd3Smem<bf16_t>& sm, const Prep16& P
     zero4(PA[q]);
     zero4(PR[q]);
   }
-  uint32_t b[4];
+  FragP<kP> b;
 #pragma unroll
   for (int kb = 0; kb < 4; ++kb) {
-    uint32_t a[4];
-    c2a16(a, c.S[2 * kb], c.S[2 * kb + 1]);
-    b_nk(b, P.X1, kB64, 0, 16 * kb, lane);  // A^, steps 0..15 as two n8 tiles
-    mma16(PA[0], a, b[0], b[1]);
-    mma16(PA[1], a, b[2], b[3]);
-    b_nk(b, P.X1, kB64, kL, 16 * kb, lane);  // R^
-    mma16(PR[0], a, b[0], b[1]);
-    mma16(PR[1], a, b[2], b[3]);
+    FragP<kP> a;
+    c2a_p<kP>(a, c.S[2 * kb], c.S[2 * kb + 1]);
+    b_nk_p<kP>(b, P.X1[0], P.X1[kLo], kB64, 0, 16 * kb, lane);  // A^, steps 0..15 as two n8 tiles
+    mma_pp<kP, kP>(PA, a, b);
+    b_nk_p<kP>(b, P.X1[0], P.X1[kLo], kB64, kL, 16 * kb, lane);  // R^
+    mma_pp<kP, kP>(PR, a, b);
   }
-  uint32_t av[4];  // V^T rows i0.., k = s
-  a_mk(av, P.VT, kB16, i0, 0, lane);
-  b_nk(b, P.M[0], kB16, 0, 0, lane);  // Mka
-  mma16(PA[0], av, b[0], b[1]);
-  mma16(PA[1], av, b[2], b[3]);
-  b_nk(b, P.M[1], kB16, 0, 0, lane);  // Mkr
-  mma16(PR[0], av, b[0], b[1]);
-  mma16(PR[1], av, b[2], b[3]);
+  FragP<kP> av;  // V^T rows i0.., k = s
+  a_mk_p<kP>(av, P.VT[0], P.VT[kLo], kB16, i0, 0, lane);
+  b_nk_p<kP>(b, P.M[0][0], P.M[kLo][0], kB16, 0, 0, lane);  // Mka
+  mma_pp<kP, kP>(PA, av, b);
+  b_nk_p<kP>(b, P.M[0][1], P.M[kLo][1], kB16, 0, 0, lane);  // Mkr
+  mma_pp<kP, kP>(PR, av, b);
   // S(L) = S0 diag(c(L)) + V^T Kb + SA^T Bb; the first two terms need no SA, so they are
   // issued here, while SA is under way
 #pragma unroll
@@ -564,45 +379,47 @@ __device__ void state_chunk16(StateCtx& c, Fwd3Smem<bf16_t>& sm, const Prep16& P
     c.S[nt][2] *= cl.x;
     c.S[nt][3] *= cl.y;
   }
+  FragP<2> bk;
 #pragma unroll
-  for (int np = 0; np < 4; ++np)
-#pragma unroll
-    for (int p = 1; p >= 0; --p) {  // the lo part first
-      b_nk(b, P.KbT[p], kB16, 16 * np, 0, lane);
-      mma16(c.S[2 * np], av, b[0], b[1]);
-      mma16(c.S[2 * np + 1], av, b[2], b[3]);
-    }
+  for (int np = 0; np < 4; ++np) {
+    b_nk_p<2>(bk, P.KbT[0], P.KbT[1], kB16, 16 * np, 0, lane);
+    mma_pp<kP, 2>(reinterpret_cast<Acc2&>(c.S[2 * np]), av, bk);
+  }
   // SA^T = PA T^T  [i][t]
   float SA[2][4];
   zero4(SA[0]);
   zero4(SA[1]);
   {
-    uint32_t a[4];
-    c2a16(a, PA[0], PA[1]);
-    b_nk(b, P.Tinv, kB16, 0, 0, lane);
-    mma16(SA[0], a, b[0], b[1]);
-    mma16(SA[1], a, b[2], b[3]);
+    FragP<kP> a;
+    c2a_p<kP>(a, PA[0], PA[1]);
+    b_nk_p<kP>(b, P.Tinv[0], P.Tinv[kLo], kB16, 0, 0, lane);
+    mma_pp<kP, kP>(SA, a, b);
   }
-  uint32_t asa[4];
-  c2a16(asa, SA[0], SA[1]);
-  // Y^T = PR + SA^T Mbr^T, stored transposed as the chunk's y rows [t][i]
-  b_nk(b, P.M[2], kB16, 0, 0, lane);
-  mma16(PR[0], asa, b[0], b[1]);
-  mma16(PR[1], asa, b[2], b[3]);
-  {
+  FragP<kP> asa;
+  c2a_p<kP>(asa, SA[0], SA[1]);
+  // Y^T = PR + SA^T Mbr^T, stored as the chunk's y rows [t][i]
+  b_nk_p<kP>(b, P.M[0][2], P.M[kLo][2], kB16, 0, 0, lane);
+  mma_pp<kP, kP>(PR, asa, b);
+  if constexpr (kP == 1) {
     uint32_t yv[4];
     c2a16(yv, PR[0], PR[1]);
     stsm4t(&sm.ys[c.yb][((lane & 7) + (lane >> 4) * 8) * kB64 + i0 + ((lane >> 3) & 1) * 8], yv);
+  } else {
+#pragma unroll
+    for (int q = 0; q < 2; ++q)
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const int i = i0 + c.g + 8 * h, tt = 8 * q + 2 * c.t4;
+        st1(&sm.ys[c.yb][tt * kN + i], PR[q][2 * h]);
+        st1(&sm.ys[c.yb][(tt + 1) * kN + i], PR[q][2 * h + 1]);
+      }
   }
   // + SA^T Bb
 #pragma unroll
-  for (int np = 0; np < 4; ++np)
-#pragma unroll
-    for (int p = 1; p >= 0; --p) {
-      b_nk(b, P.BbT[p], kB16, 16 * np, 0, lane);
-      mma16(c.S[2 * np], asa, b[0], b[1]);
-      mma16(c.S[2 * np + 1], asa, b[2], b[3]);
-    }
+  for (int np = 0; np < 4; ++np) {
+    b_nk_p<2>(bk, P.BbT[0], P.BbT[1], kB16, 16 * np, 0, lane);
+    mma_pp<kP, 2>(reinterpret_cast<Acc2&>(c.S[2 * np]), asa, bk);
+  }
 }
 
 // Chunk in the direct form (any decay), fp32 on the CUDA cores.
@@ -742,7 +559,7 @@ __global__ void __launch_bounds__(kThreads, 1) wkv7_fwd3_kernel(const __grid_con
   };
   // TMA copies are issued by the first thread of the forming group (fp32 inputs) or of the
   // products group (bf16 inputs, where that group has the shorter round)
-  constexpr int kIssuer = kSplitOf<TIn> ? 128 : 256;
+  constexpr int kIssuer = sizeof(TIn) == 4 ? 128 : 256;
   if (tid == kIssuer) {
     for (int s = 0; s < kStages; ++s) mbar_init(&sm.full[s], 1);
     fence_mbar_init();
@@ -803,11 +620,7 @@ __global__ void __launch_bounds__(kThreads, 1) wkv7_fwd3_kernel(const __grid_con
   };
   auto grams = [&](int chunk) {
     auto& P = sm.prep[chunk % 3];
-    if (P.unsafe) return;
-    if constexpr (kSplitOf<TIn>)
-      gram_chunk<true>(P, sm.X2[chunk & 1], gtid);
-    else
-      gram_chunk16(P, sm.X2[chunk & 1], gtid);
+    if (!P.unsafe) gram_chunk16<Fwd3Io<TIn>::kP>(P, sm.X2[chunk & 1], gtid);
   };
 
   // pipeline fill: form chunks 0 and 1, products of chunk 0
@@ -851,10 +664,8 @@ __global__ void __launch_bounds__(kThreads, 1) wkv7_fwd3_kernel(const __grid_con
       c.yb = n & 1;
       if (P.unsafe)
         state_chunk_direct<TIn, kLogit>(c, sm, n % kStages, len);
-      else if constexpr (kSplitOf<TIn>)
-        state_chunk<TIn>(c, sm, P);
       else
-        state_chunk16(c, sm, P, lane);
+        state_chunk16<TIn>(c, sm, P, lane);
     }
     // the stage of chunk n is free (formed two rounds ago, direct steps done); refill it
     aborted = __syncthreads_or(sm.abort_flag) != 0;

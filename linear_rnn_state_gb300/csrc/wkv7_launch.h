@@ -99,15 +99,15 @@ int fwd_steps_per_stage(int N, bool bf16);
 
 cudaError_t launch_fwd2(const FwdArgs& args, bool bf16, int N, cudaStream_t stream);
 // Chunked tensor-core forward: N = 64, checkpoints (if any) at a multiple of
-// its 16-step chunk; bf16 inputs (one tf32 product per product) or fp32
-// inputs (split tf32, three; the decay as w and no epilogue).
+// its 16-step chunk; bf16 inputs (bf16 operands, one product per product) or
+// fp32 inputs (split bf16, three; the decay as w and no epilogue).
 cudaError_t launch_fwd3(const FwdArgs& args, bool bf16, cudaStream_t stream);
 // Chunked tensor-core backward: bf16 inputs, N = 64, checkpoints every 16 steps.
 cudaError_t launch_bwd3(const BwdArgs& args, cudaStream_t stream);
 // The same backward as a carry-chain kernel plus a parallel per-chunk output
 // kernel; needs args.carry, a workspace of bwd4_workspace_bytes.
 cudaError_t launch_bwd4(const BwdArgs& args, cudaStream_t stream);
-// The same split for fp32 inputs (products in split tf32): the carry chain, storing fp32
+// The same split for fp32 inputs: the carry chain (products in split bf16), storing fp32
 // carries in the workspace, then the per-chunk output pass.
 cudaError_t launch_bwd4_carry_f32(const BwdArgs& args, cudaStream_t stream);
 cudaError_t launch_bwd4_out_f32(const BwdArgs& args, cudaStream_t stream);

@@ -112,4 +112,101 @@ __device__ __forceinline__ void store_masked16(const float (&acc)[2][4], bf16_t*
     }
 }
 
+// ------------------------------------------------- operands in one or two parts ---
+//
+// An operand in kP bf16 parts: kP = 1, one bf16 value; kP = 2, a pair hi + lo (hi = the
+// value rounded to bf16, lo = the remainder rounded to bf16, about 16 bits in all), and a
+// product a b is then taken as a_lo b_hi + a_hi b_lo + a_hi b_hi.
+
+// A fragment (A or two n8 tiles of B) of an operand in kP bf16 parts: h, and for kP = 2 l.
+template <int kP>
+struct FragP {
+  uint32_t h[4];
+  uint32_t l[kP == 2 ? 4 : 1];
+};
+
+// Two accumulator tiles as the A fragment of a product over their 16 columns, and for kP
+// = 2 the remainder after rounding to bf16 as the lo part.
+template <int kP>
+__device__ __forceinline__ void c2a_p(FragP<kP>& a, const float (&lo)[4], const float (&hi)[4]) {
+  c2a16(a.h, lo, hi);
+  if constexpr (kP == 2) {
+    const float2 u0 = unpack_bf16(a.h[0]), u1 = unpack_bf16(a.h[1]), u2 = unpack_bf16(a.h[2]),
+                 u3 = unpack_bf16(a.h[3]);
+    const float rl[4] = {lo[0] - u0.x, lo[1] - u0.y, lo[2] - u1.x, lo[3] - u1.y};
+    const float rh[4] = {hi[0] - u2.x, hi[1] - u2.y, hi[2] - u3.x, hi[3] - u3.y};
+    c2a16(a.l, rl, rh);
+  }
+}
+// Fragments of a row-major tile stored in kP parts: hi, and lo (read only for kP = 2).
+template <int kP>
+__device__ __forceinline__ void a_mk_p(FragP<kP>& a, const bf16_t* hi, const bf16_t* lo, int ld, int m0, int k0,
+                                       int lane) {
+  a_mk(a.h, hi, ld, m0, k0, lane);
+  if constexpr (kP == 2) a_mk(a.l, lo, ld, m0, k0, lane);
+}
+template <int kP>
+__device__ __forceinline__ void b_nk_p(FragP<kP>& b, const bf16_t* hi, const bf16_t* lo, int ld, int n0, int k0,
+                                       int lane) {
+  b_nk(b.h, hi, ld, n0, k0, lane);
+  if constexpr (kP == 2) b_nk(b.l, lo, ld, n0, k0, lane);
+}
+// acc (two n8 tiles) += a b with the parts each side has: the small terms first.
+__device__ __forceinline__ void mma2(float (&acc)[2][4], const uint32_t (&a)[4], const uint32_t (&b)[4]) {
+  mma16(acc[0], a, b[0], b[1]);
+  mma16(acc[1], a, b[2], b[3]);
+}
+template <int kPa, int kPb>
+__device__ __forceinline__ void mma_pp(float (&acc)[2][4], const FragP<kPa>& a, const FragP<kPb>& b) {
+  if constexpr (kPa == 2) mma2(acc, a.l, b.h);
+  if constexpr (kPb == 2) mma2(acc, a.h, b.l);
+  mma2(acc, a.h, b.h);
+}
+// An fp32 value stored as kP bf16 parts: hi, and lo (written only for kP = 2).
+template <int kP>
+__device__ __forceinline__ void put_p(bf16_t* hi, bf16_t* lo, float x) {
+  const bf16_t h = __float2bfloat16_rn(x);
+  *hi = h;
+  if constexpr (kP == 2) *lo = __float2bfloat16_rn(x - __bfloat162float(h));
+}
+// Eight fp32 values as one 16-byte piece per part.
+__device__ __forceinline__ uint4 pack8(const float (&x)[8]) {
+  return make_uint4(pack_bf16(x[0], x[1]), pack_bf16(x[2], x[3]), pack_bf16(x[4], x[5]), pack_bf16(x[6], x[7]));
+}
+__device__ __forceinline__ void lo8(float (&x)[8]) {  // x <- x - bf16(x), exact in fp32
+#pragma unroll
+  for (int e = 0; e < 8; ++e) x[e] -= __bfloat162float(__float2bfloat16_rn(x[e]));
+}
+template <int kP>
+__device__ __forceinline__ void put8_p(bf16_t* hi, bf16_t* lo, float (&x)[8]) {
+  *reinterpret_cast<uint4*>(hi) = pack8(x);
+  if constexpr (kP == 2) {
+    lo8(x);
+    *reinterpret_cast<uint4*>(lo) = pack8(x);
+  }
+}
+
+template <int kP>
+__device__ __forceinline__ void a_km_p(FragP<kP>& a, const bf16_t* hi, const bf16_t* lo, int ld, int m0, int k0,
+                                       int lane) {
+  a_km(a.h, hi, ld, m0, k0, lane);
+  if constexpr (kP == 2) a_km(a.l, lo, ld, m0, k0, lane);
+}
+template <int kP>
+__device__ __forceinline__ void b_kn_p(FragP<kP>& b, const bf16_t* hi, const bf16_t* lo, int ld, int n0, int k0,
+                                       int lane) {
+  b_kn(b.h, hi, ld, n0, k0, lane);
+  if constexpr (kP == 2) b_kn(b.l, lo, ld, n0, k0, lane);
+}
+// A pair of fp32 values stored as kP bf16 pairs: hi, and lo (written only for kP = 2).
+template <int kP>
+__device__ __forceinline__ void st_pair_p(bf16_t* hi, bf16_t* lo, float2 x) {
+  const uint32_t h = pack_bf16(x.x, x.y);
+  *reinterpret_cast<uint32_t*>(hi) = h;
+  if constexpr (kP == 2) {
+    const float2 u = unpack_bf16(h);
+    *reinterpret_cast<uint32_t*>(lo) = pack_bf16(x.x - u.x, x.y - u.y);
+  }
+}
+
 }  // namespace wkv7

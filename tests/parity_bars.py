@@ -121,6 +121,11 @@ def _record(name, kind, s):
         f.write(json.dumps({"test": test, "name": name, "kind": kind, "whole": s[0], "chunk": s[1], "elem": s[2]}) + "\n")
 
 
+def record_f32(name, scaled_max):
+    """Record, under PARITY_STATS, an fp32 check's largest |gpu - ref| / (1 + |ref|)."""
+    _record(name, "fp32", (float(scaled_max), float(scaled_max), float(scaled_max)))
+
+
 def check_bf16(name, got, ref, kind="seq", tau=None):
     """Assert the bf16 bar on got against ref: whole tensor, every chunk, and
     every element (see the module docstring). The element guard takes

@@ -10,7 +10,7 @@ guard. The oracle sees exactly the values stored in the GPU's input buffers
 import numpy as np
 import pytest
 
-from parity_bars import check_bf16
+from parity_bars import check_bf16, record_f32
 
 pytestmark = pytest.mark.gpu
 
@@ -60,6 +60,7 @@ def _assert_close(name, got, ref, storage, what=""):
     else:
         err = np.abs(got - ref) / (1.0 + np.abs(ref))
         i = np.unravel_index(np.argmax(err), err.shape)
+        record_f32(f"{name}{what}", err.max())
         assert err.max() <= FP32_TOL, f"{name}{what}: max scaled error {err.max():.3e} at {i}: {got[i]} vs {ref[i]}"
 
 
