@@ -36,8 +36,8 @@ TRAFFIC = {
     "kernel": "wkv7_bwd4_carry_kernel + wkv7_bwd4_out_kernel (one wkv7_backward_bf16 call)",
     "sources": ("wkv7_bwd4.cu", "wkv7_common.cuh", "wkv7_scaled.cuh", "wkv7_mma.cuh", "wkv7_mma16.cuh",
                 "wkv7_launch.h", "wkv7_decay.cuh", "wkv7_tmem.cuh"),
-    "sha256": "ecc1a31653def886294f515a1acd7687e70297aa777a487aac4d618352f81fa4",
-    "bytes_per_token_head": (83.953920e6 + 28.128512e6 + 318.836992e6 + 161.838592e6) / 131072,
+    "sha256": "4796a1f491261989b24be41333279f686d8f5766d51b7c38d2b595e92dbd829a",
+    "bytes_per_token_head": (83.937536e6 + 28.234240e6 + 318.859776e6 + 161.499904e6) / 131072,
 }
 
 
@@ -49,9 +49,9 @@ TRAFFIC_FP32 = {
     "kernel": "wkv7_bwd4_carry_kernel<float> + wkv7_bwd4_out_f32_kernel (one wkv7_backward call, fp32 inputs)",
     "sources": ("wkv7_bwd4.cu", "wkv7_bwd4_f32.cu", "wkv7_common.cuh", "wkv7_scaled.cuh", "wkv7_mma.cuh",
                 "wkv7_mma16.cuh", "wkv7_launch.h", "wkv7_decay.cuh", "wkv7_tmem.cuh"),
-    "sha256": "a33903b1cb9635d26b778256e544d20cc939d892409bb716b9cea94d185e3b1b",
+    "sha256": "1290a157d6420d5ae93c4add64037f05a3a3c29346c167c8ce05cb7e243ca9f1",
     "N": 64,
-    "bytes_per_token_head": (125.942784e6 + 59.765504e6 + 377.598720e6 + 124.783872e6) / 98304,
+    "bytes_per_token_head": (125.890816e6 + 60.149504e6 + 377.603584e6 + 124.715520e6) / 98304,
 }
 
 
