@@ -41,8 +41,8 @@ TRAFFIC = {
 }
 
 
-# The fp32 backward (wkv7_backward at N = 64, 16-step checkpoints) runs the carry chain (split
-# bf16) and the per-chunk output pass (split tf32); their DRAM bytes per token-head from one ncu capture of the
+# The fp32 backward (wkv7_backward at N = 64, 16-step checkpoints) runs the carry chain and the
+# per-chunk output pass in split bf16; their DRAM bytes per token-head from one ncu capture of the
 # 8 x 1024 x 12 case (dram__bytes_read.sum + dram__bytes_write.sum / (B*T*H)), null once their
 # sources change.
 TRAFFIC_FP32 = {
@@ -515,10 +515,10 @@ def _report(args, wl, world, B, T, H, N, C, bf16, ms, fwd_ms, bwd_ms, e2e, ckpt,
                        "enters a product) and in its per-chunk gradient products (the carry "
                        "stored as bf16 between the two backward kernels, the fp32 checkpoint rounded to bf16 "
                        "there); fp32 accumulation, state and element-wise math" if chunked else
-                       ("tensor-core products with fp32 accumulation, three per fp32 product: split bf16 "
-                        "(each operand a bf16 hi + lo pair) in the forward and the backward's carry chain, split "
-                        "tf32 in the backward's per-chunk output pass; the state, the carried gradient (stored "
-                        "as fp32 between the two backward kernels) and every element-wise step fp32"
+                       ("tensor-core products in split bf16 (each operand a bf16 hi + lo pair, three products per "
+                        "fp32 product, fp32 accumulation) in the forward, the backward's carry chain and its "
+                        "per-chunk output pass; the state, the carried gradient (stored as fp32 between the two "
+                        "backward kernels) and every element-wise step fp32"
                         if N == 64 and C == 16 else "fp32 FMA throughout (scalar kernels)"))
                       + "; inputs, dy and y stored in " + wl.storage,
         "config": {"workload": (wl.name + {"wkv7-logit": "-decay-logits", "wkv7-epilogue": "-with-epilogue"}.get(

@@ -365,8 +365,8 @@ int backward_impl(bool bf16, const void* const in[7], const float* s_init, const
   // backward: the split one (carry chain + parallel output pass), which keeps
   // the carry of every chunk in the workspace too, or, when the caller asks
   // for it (wkv7_backward_fused_bf16), the fused one (one CTA per head). fp32
-  // inputs there take the split one (the carry chain in split bf16, fp32
-  // carries in the workspace, the output pass in split tf32).
+  // inputs there take the split one in split bf16 (fp32 carries in the
+  // workspace).
   const bool chunked = bf16 && N == 64 && C_eff == kChunk;
   const bool split = chunked && form != BwdForm::kFused;
   const bool split32 = !bf16 && N == 64 && C_eff == kChunk;

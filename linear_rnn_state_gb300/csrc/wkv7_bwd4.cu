@@ -789,13 +789,6 @@ __device__ __forceinline__ void unit_lower_inverse16(const float* M, bf16_t* Tou
   }
 }
 
-// 16-byte asynchronous copy that writes zeros instead when `valid` is false.
-__device__ __forceinline__ void cp_async16_zfill(void* dst, const void* src, bool valid) {
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(smem_addr(dst)), "l"(src),
-               "r"(valid ? 16 : 0)
-               : "memory");
-}
-
 template <bool kLogit, bool kEpi>
 __global__ void __launch_bounds__(kThreads, 3) wkv7_bwd4_out_kernel(const __grid_constant__ BwdArgs args) {
   extern __shared__ __align__(128) unsigned char smem_raw[];

@@ -126,144 +126,16 @@ __device__ __forceinline__ void c2a(uint32_t (&a)[4], const float (&c)[4]) {
 
 __device__ __forceinline__ void zero4(float (&c)[4]) { c[0] = c[1] = c[2] = c[3] = 0.f; }
 
-// ------------------------------------------------ one or three tf32 products ---
-//
-// Operand fragments for products taken either as one tf32 product (kX3 =
-// false: the shared-memory operands already hold tf32 values, accumulators
-// are rounded to tf32 on the way in) or in split tf32 (kX3 = true, for fp32
-// inputs: each fp32 operand x is hi + lo, hi = x rounded to tf32 and lo = x -
-// hi, exact in fp32, itself rounded to tf32; a b is taken as a_lo b_hi +
-// a_hi b_lo + a_hi b_hi, three mma.sync with fp32 accumulation, a relative
-// error near 2^-21 against 2^-11 for one product). The split rounds with
-// integer arithmetic: add half a tf32 unit (bit 12) to the pattern and clear
-// the 13 low bits (nearest, ties away from zero; finite values).
-
-__device__ __forceinline__ uint32_t tf32_round_int(uint32_t bits) { return (bits + 0x1000u) & 0xffffe000u; }
-
-__device__ __forceinline__ void split_x3(float x, uint32_t& hi, uint32_t& lo) {
-  hi = tf32_round_int(__float_as_uint(x));
-  lo = tf32_round_int(__float_as_uint(x - __uint_as_float(hi)));
-}
-
-template <bool kX3>
-struct FragA {
-  uint32_t h[4];
-  uint32_t l[kX3 ? 4 : 1];
-};
-template <bool kX3>
-struct FragB {
-  uint32_t h0, h1;
-  uint32_t l0, l1;  // unused unless kX3
-};
-
-// From four fp32 values in A-fragment order: tf32 values as they are (kX3 =
-// false), or split.
-template <bool kX3>
-__device__ __forceinline__ void make_a(FragA<kX3>& a, float x0, float x1, float x2, float x3) {
-  const float x[4] = {x0, x1, x2, x3};
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    if constexpr (kX3)
-      split_x3(x[i], a.h[i], a.l[i]);
-    else
-      a.h[i] = __float_as_uint(x[i]);
-  }
-}
-template <bool kX3>
-__device__ __forceinline__ void make_b(FragB<kX3>& b, float x0, float x1) {
-  if constexpr (kX3) {
-    split_x3(x0, b.h0, b.l0);
-    split_x3(x1, b.h1, b.l1);
-  } else {
-    b.h0 = __float_as_uint(x0);
-    b.h1 = __float_as_uint(x1);
-  }
-}
-
-// frag_a / frag_b of a row-major operand (see the fragment convention above).
-template <bool kX3>
-__device__ __forceinline__ void ld_a(FragA<kX3>& a, const float* m, int ld, int r0, int k0, int g, int t) {
-  const float2 lo = *reinterpret_cast<const float2*>(m + (r0 + g) * ld + k0 + 2 * t);
-  const float2 hi = *reinterpret_cast<const float2*>(m + (r0 + g + 8) * ld + k0 + 2 * t);
-  make_a(a, lo.x, hi.x, lo.y, hi.y);
-}
-template <bool kX3>
-__device__ __forceinline__ void ld_b(FragB<kX3>& b, const float* bt, int ld, int n0, int k0, int g, int t) {
-  const float2 v = *reinterpret_cast<const float2*>(bt + (n0 + g) * ld + k0 + 2 * t);
-  make_b(b, v.x, v.y);
-}
-
-// The transposed and hardware-order forms of frag_a_t, frag_a_ts, frag_b_t,
-// frag_b_ts (same element order).
-template <bool kX3>
-__device__ __forceinline__ void ld_a_t(FragA<kX3>& a, const float* m, int ld, int m0, int k0, int g, int t) {
-  const float* p = m + (k0 + 2 * t) * ld + m0 + g;
-  make_a(a, p[0], p[8], p[ld], p[ld + 8]);
-}
-template <bool kX3>
-__device__ __forceinline__ void ld_a_ts(FragA<kX3>& a, const float* m, int ld, int m0, int k0, int g, int t) {
-  const float* p = m + (k0 + t) * ld + m0 + g;
-  make_a(a, p[0], p[8], p[4 * ld], p[4 * ld + 8]);
-}
-template <bool kX3>
-__device__ __forceinline__ void ld_b_t(FragB<kX3>& b, const float* m, int ld, int n0, int k0, int g, int t) {
-  const float* p = m + (k0 + 2 * t) * ld + n0 + g;
-  make_b(b, p[0], p[ld]);
-}
-template <bool kX3>
-__device__ __forceinline__ void ld_b_ts(FragB<kX3>& b, const float* m, int ld, int n0, int k0, int g, int t) {
-  const float* p = m + (k0 + t) * ld + n0 + g;
-  make_b(b, p[0], p[4 * ld]);
-}
-// frag_a_r / frag_b_t_r: fp32 storage rounded to tf32 (kX3 = false), or split.
-template <bool kX3>
-__device__ __forceinline__ void ld_a_r(FragA<kX3>& a, const float* m, int ld, int r0, int k0, int g, int t) {
-  if constexpr (kX3) {
-    ld_a(a, m, ld, r0, k0, g, t);
-  } else {
-    uint32_t x[4];
-    frag_a_r(x, m, ld, r0, k0, g, t);
-#pragma unroll
-    for (int i = 0; i < 4; ++i) a.h[i] = x[i];
-  }
-}
-template <bool kX3>
-__device__ __forceinline__ void ld_b_t_r(FragB<kX3>& b, const float* m, int ld, int n0, int k0, int g, int t) {
-  if constexpr (kX3)
-    ld_b_t(b, m, ld, n0, k0, g, t);
-  else
-    frag_b_t_r(b.h0, b.h1, m, ld, n0, k0, g, t);
-}
-
-// Accumulator tile -> A fragment over the same columns: rounded to tf32
-// (kX3 = false), or split.
-template <bool kX3>
-__device__ __forceinline__ void acc_to_a(FragA<kX3>& a, const float (&c)[4]) {
-  if constexpr (kX3) {
-    make_a(a, c[0], c[2], c[1], c[3]);
-  } else {
-    a.h[0] = tf32_bits(c[0]);
-    a.h[1] = tf32_bits(c[2]);
-    a.h[2] = tf32_bits(c[1]);
-    a.h[3] = tf32_bits(c[3]);
-  }
-}
-
-// d += a b: one product, or the three of the split (small terms first).
-template <bool kX3>
-__device__ __forceinline__ void mma_x(float (&d)[4], const FragA<kX3>& a, const FragB<kX3>& b) {
-  if constexpr (kX3) {
-    const uint32_t al[4] = {a.l[0], a.l[1], a.l[2], a.l[3]};
-    mma_tf32(d, al, b.h0, b.h1);
-    mma_tf32(d, a.h, b.l0, b.l1);
-  }
-  mma_tf32(d, a.h, b.h0, b.h1);
-}
-
 // 16-byte asynchronous copy global -> shared (both addresses 16-byte aligned).
 __device__ __forceinline__ void cp_async16(void* dst, const void* src) {
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(static_cast<uint32_t>(__cvta_generic_to_shared(dst))),
                "l"(src)
+               : "memory");
+}
+// 16-byte asynchronous copy that writes zeros instead when `valid` is false.
+__device__ __forceinline__ void cp_async16_zfill(void* dst, const void* src, bool valid) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(static_cast<uint32_t>(__cvta_generic_to_shared(dst))),
+               "l"(src), "r"(valid ? 16 : 0)
                : "memory");
 }
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }

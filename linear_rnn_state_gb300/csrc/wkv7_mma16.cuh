@@ -209,4 +209,37 @@ __device__ __forceinline__ void st_pair_p(bf16_t* hi, bf16_t* lo, float2 x) {
   }
 }
 
+// A 16 x 16 fp32 accumulator (tiles acc[0], acc[1]) as kP bf16 parts [t][s] (row stride
+// kB16), keeping lower: s < t (+ diagonal if incl), upper: s > t (+ diagonal if incl).
+template <int kP>
+__device__ __forceinline__ void store_masked16_p(const float (&acc)[2][4], bf16_t* hi, bf16_t* lo, bool lower,
+                                                 bool incl, int g, int t4) {
+#pragma unroll
+  for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const int t = g + 8 * h, s = 8 * nt + 2 * t4;
+      float x[2];
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        const int se = s + e;
+        const bool keep = lower ? (se < t || (incl && se == t)) : (se > t || (incl && se == t));
+        x[e] = keep ? acc[nt][2 * h + e] : 0.f;
+      }
+      st_pair_p<kP>(hi + t * kB16 + s, lo + t * kB16 + s, make_float2(x[0], x[1]));
+    }
+}
+// acc[nt] += A B over K = 16 * KB for two n8 tiles, A from [m][k], B from [n][k], both in kP parts.
+template <int KB, int kP>
+__device__ __forceinline__ void mm_mk_nk_p(float (&acc)[2][4], const bf16_t* A, const bf16_t* Al, int lda, int m0,
+                                           const bf16_t* Bt, const bf16_t* Btl, int ldb, int n0, int lane) {
+#pragma unroll
+  for (int kb = 0; kb < KB; ++kb) {
+    FragP<kP> a, b;
+    a_mk_p<kP>(a, A, Al, lda, m0, 16 * kb, lane);
+    b_nk_p<kP>(b, Bt, Btl, ldb, n0, 16 * kb, lane);
+    mma_pp<kP, kP>(acc, a, b);
+  }
+}
+
 }  // namespace wkv7
