@@ -49,9 +49,9 @@ TRAFFIC_FP32 = {
     "kernel": "wkv7_bwd4_carry_kernel<float> + wkv7_bwd4_out_f32_kernel (one wkv7_backward call, fp32 inputs)",
     "sources": ("wkv7_bwd4.cu", "wkv7_bwd4_f32.cu", "wkv7_common.cuh", "wkv7_scaled.cuh", "wkv7_mma.cuh",
                 "wkv7_mma16.cuh", "wkv7_launch.h", "wkv7_decay.cuh", "wkv7_tmem.cuh"),
-    "sha256": "1290a157d6420d5ae93c4add64037f05a3a3c29346c167c8ce05cb7e243ca9f1",
+    "sha256": "3814de236be2f48554d0f3cc6476c3e4dbaff5eeb79805e88841b62198e87f50",
     "N": 64,
-    "bytes_per_token_head": (125.890816e6 + 60.149504e6 + 377.603584e6 + 124.715520e6) / 98304,
+    "bytes_per_token_head": (125.891328e6 + 59.876352e6 + 377.680128e6 + 123.846144e6) / 98304,
 }
 
 
