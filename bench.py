@@ -538,7 +538,7 @@ def _report(args, wl, world, B, T, H, N, C, bf16, ms, fwd_ms, bwd_ms, e2e, ckpt,
                               "products with bf16 operands") if chunked else
                              ("the backward call (its two kernels, timed together with CUDA events around the call): "
                               "algorithmic FLOP of the recurrence (24 N^2 per token-head) against the FP32 CUDA-core "
-                              "peak; the kernels form them as split-tf32 tensor-core products")
+                              "peak; the kernels form them as split-bf16 tensor-core products")
                              if N == 64 and C == 16 else
                              ("the backward call (one kernel, timed with CUDA events around the call): algorithmic "
                               "FLOP of the recurrence (24 N^2 per token-head) against the FP32 CUDA-core peak"),
@@ -753,7 +753,8 @@ def run_rwkv8(args):
     t_roof = max((f_flop + b_flop) * BTH / peak_flops, (f_bytes + b_bytes) * BTH / (peaks["hbm_gbs"] * 1e9))
     traffic = None
     split_bwd = _rwkv8_env("RWKV8_SPLIT_BACKWARD") and not _rwkv8_env("RWKV8_SEQUENTIAL")
-    bwd_kernel = ("rwkv8_bwd_chain_kernel + rwkv8_bwd_chunk_kernel (one rwkv8_backward call)" if split_bwd
+    bwd_kernel = ("rwkv8_bwd_r0_kernel + rwkv8_bwd_chain_kernel + rwkv8_bwd_chunk_kernel (one rwkv8_backward call)"
+                  if split_bwd
                   else RWKV8_TRAFFIC["kernel"])
     if (not split_bwd and RWKV8_TRAFFIC["sha256"]
             and sources_sha256(RWKV8_TRAFFIC["sources"]) == RWKV8_TRAFFIC["sha256"]):
@@ -779,10 +780,11 @@ def run_rwkv8(args):
             "value": aggregate_tokens_per_s(world, B, T, e2e[0]), "unit": "tokens/s", "h2d_bytes_per_step": e2e[1],
             "d2h_bytes_per_step": e2e[2]},
         # forward: the chain and the per-chunk readout (one kernel with RWKV8_SEQUENTIAL=1); backward: its
-        # kernel and the ddecay sum over b (RWKV8_SPLIT_BACKWARD=1: the chain, the per-chunk kernel and
-        # the sums over the chunks and over b); for a shared value row, one dv sum per batch row
+        # kernel and the ddecay sum over b (RWKV8_SPLIT_BACKWARD=1: the R0 pass, the chain, the
+        # per-chunk kernel and the sums over the chunks and over b); for a shared value row, one dv sum
+        # per batch row
         "gpu_launches": ((1 if _rwkv8_env("RWKV8_SEQUENTIAL") else 2)
-                         + (4 if _rwkv8_env("RWKV8_SPLIT_BACKWARD") and not _rwkv8_env("RWKV8_SEQUENTIAL") else 2)
+                         + (5 if _rwkv8_env("RWKV8_SPLIT_BACKWARD") and not _rwkv8_env("RWKV8_SEQUENTIAL") else 2)
                          + (B if Hv == 1 and H > 1 else 0)) * args.steps,
         "clocks": clocks.summary(),
     }

@@ -90,10 +90,10 @@ int rwkv8_forward(const float* q, const float* v, const float* decay, const floa
  *   d_rho_init [B][H][L][E], d_rho_norm_init [B][H][L]  outputs, or NULL.
  * One CTA per (b, h) walks its chunks from the last to the first.
  * RWKV8_SPLIT_BACKWARD=1 in the environment selects the split form instead:
- * the carried gradients run alone first, one CTA per (b, h), storing their
- * value after every chunk (and <rho0, dy> rows) in a workspace (about 1.3 KB
- * per token-head), then every chunk's dq, dv and ddecay terms are made at
- * once; the results agree to fp32 rounding. ddecay is summed over the chunks
+ * the <rho0, dy> rows of every chunk first, then the carried gradients alone,
+ * one CTA per (b, h), storing their value after every chunk in a workspace
+ * (about 1.3 KB per token-head with those rows), then every chunk's dq, dv and
+ * ddecay terms at once; the results agree to fp32 rounding. ddecay is summed over the chunks
  * and over b in a fixed order (deterministic); with Hv = 1, dv is summed over
  * h in a fixed order. The workspace is taken with cudaMallocAsync on `stream`
  * (WKV7_ERR_ALLOC if that fails).

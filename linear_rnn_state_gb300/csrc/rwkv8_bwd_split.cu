@@ -14,10 +14,11 @@
 // every chunk are known, its dq, dv and decay terms need nothing from any
 // other chunk.
 //
+// rwkv8_bwd_r0_kernel: R0 of every chunk at once (one CTA per chunk), fp32 FFMA.
 // rwkv8_bwd_chain_kernel: one CTA of 256 threads per (b, h), chunks from the
-// last to the first, inputs and checkpoints through a four-chunk cp.async
-// ring. Per chunk it stores G15, Gn15, R0 and <G15[l], rho0[l]> to the
-// workspace, then advances G (accumulator tiles) and Gn.
+// last to the first, inputs, checkpoints and R0 through a four-chunk cp.async
+// ring. Per chunk it stores G15, Gn15 and <G15[l], rho0[l]> to the workspace,
+// then advances G (accumulator tiles) and Gn.
 // rwkv8_bwd_chunk_kernel: one CTA of 256 threads per (b, h, chunk): the rest
 // of the chunk's formulas (rwkv8_bwd.cu lists them) from its own q, v, dy and
 // n0 and those four stored values; the checkpointed rho0 is not read again.
@@ -155,6 +156,37 @@ __device__ __forceinline__ float m_entry(const float* dys, const float* vs, int 
   return m;
 }
 
+// ================================================================== R0 ===
+
+// R0[tau][l] = <rho0[l], dy_tau> of one chunk per CTA (256 threads: latent l = tid % 64,
+// steps 4 (tid / 64) ..), the same FFMA sequence as everywhere it is formed.
+__global__ void __launch_bounds__(kThreads) rwkv8_bwd_r0_kernel(const Args a) {
+  __shared__ __align__(16) float rho[kL][kP4];
+  __shared__ __align__(16) float dys[kC][kP8];
+  const int tid = threadIdx.x, T = a.T, nck = (T + kC - 1) / kC;
+  const long long task = blockIdx.x;
+  const int bh = (int)(task / nck), c = (int)(task % nck);
+  {
+    const int row = tid >> 4, col = 4 * (tid & 15), tt = c * kC + row;
+    const float* ck = a.ckpt + (size_t)task * kL * kE;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) cp_async16(&rho[row + 16 * i][col], ck + (size_t)(row + 16 * i) * kE + col);
+    if (tt < T)
+      cp_async16(&dys[row][col], a.dy + ((size_t)bh * T + tt) * kE + col);
+    else
+      zero16(&dys[row][col]);
+    cp_async_commit();
+    cp_async_wait_all();
+  }
+  __syncthreads();
+  const int l = tid & 63, q4 = tid >> 6;
+  float r[4];
+  r0_rows(&rho[0][0], &dys[0][0], l, q4, r);
+  float* dst = a.r0 + (size_t)task * kC * kL;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) dst[(4 * q4 + i) * kL + l] = r[i];
+}
+
 // ================================================================ chain ===
 
 struct ChainSmem {
@@ -167,7 +199,7 @@ struct ChainSmem {
   float Ut[kC][kP8];          // U[s][l] d_l^s: the G update's A operand, stored [k = s][m = l]
   float U[kC][kL];
   float NB[kC][kL];           // n before every step
-  float R0[kC][kL];
+  float R0[kRing][kC][kL];     // R0 of the chunk (the pre-pass's)
   float M[kC][kPM];
   float mend[4][kL];
   float sqp[2][kC];
@@ -176,7 +208,7 @@ struct ChainSmem {
 };
 
 struct HeadPtrs {
-  const float *q, *v, *dy, *ck_rho, *ck_n;
+  const float *q, *v, *dy, *ck_rho, *ck_n, *r0;
   int T;
 };
 
@@ -199,6 +231,7 @@ __device__ __forceinline__ void chain_load(ChainSmem& sm, int slot, const HeadPt
 #pragma unroll
     for (int i = 0; i < 4; ++i) cp_async16(&sm.rho[slot][row + 16 * i][col], ck + (size_t)(row + 16 * i) * kE + col);
     if (tid < kL / 4) cp_async16(&sm.n0[slot][4 * tid], hp.ck_n + (size_t)c * kL + 4 * tid);
+    cp_async16(&sm.R0[slot][row][col], hp.r0 + ((size_t)c * kC + row) * kL + col);
   }
   cp_async_commit();
 }
@@ -213,7 +246,7 @@ __device__ __forceinline__ float chain_elements(const ChainSmem& sm, int slot, i
 #pragma unroll
   for (int j = 0; j < 4; ++j) {
     const int tau = SEG + 4 * j;
-    float R = pcol[tau] * sm.R0[tau][l];
+    float R = pcol[tau] * sm.R0[slot][tau][l];
 #pragma unroll
     for (int s = 0; s < tau; ++s) R = fmaf(pcol[tau - 1 - s], qcol[s] * sm.M[tau][s], R);
     const float gn = -sm.U[tau][l] * __fdividef(R, sm.NB[tau][l] + kEps);  // denominator >= 1e-6
@@ -240,6 +273,7 @@ __global__ void __launch_bounds__(kThreads, 1) rwkv8_bwd_chain_kernel(const Args
   hp.dy = a.dy + (size_t)bh * T * kE;
   hp.ck_rho = a.ckpt + (size_t)bh * nck * kL * kE;
   hp.ck_n = a.ckpt + ckpt_norm_offset(a.B, T, a.H) + (size_t)bh * nck * kL;
+  hp.r0 = a.r0 + (size_t)bh * nck * kC * kL;
 
   // visit v handles chunk nck - 1 - v
 #pragma unroll
@@ -307,16 +341,10 @@ __global__ void __launch_bounds__(kThreads, 1) rwkv8_bwd_chain_kernel(const Args
 
     float x[4], loc[4];
     local_scan(&sm.qs[slot][0][0], pcol[1], l_s, seg, lane, w, x, loc, &sm.mend[0][0], &sm.sqp[0][0]);
-    {  // R0 = DY rho0^T and M = DY V^T (fp32 FFMA)
-      float r[4];
-      r0_rows(&sm.rho[slot][0][0], &sm.dys[slot][0][0], l_s, seg, r);
-#pragma unroll
-      for (int i = 0; i < 4; ++i) sm.R0[4 * seg + i][l_s] = r[i];
-      sm.M[tid >> 4][tid & 15] = m_entry(&sm.dys[slot][0][0], &sm.vs[slot][0][0], tid);
-    }
+    sm.M[tid >> 4][tid & 15] = m_entry(&sm.dys[slot][0][0], &sm.vs[slot][0][0], tid);  // M = DY V^T (fp32 FFMA)
     __syncthreads();
 
-    // ---- n before every step, U, U d^tau; <G15, rho0> and R0 to the workspace
+    // ---- n before every step, U, U d^tau; <G15, rho0> to the workspace
     {
       float start = sm.n0[slot][l_s];
       for (int s2 = 0; s2 < seg; ++s2) start = fmaf(pcol[4], start, sm.mend[s2][l_s]);
@@ -332,10 +360,6 @@ __global__ void __launch_bounds__(kThreads, 1) rwkv8_bwd_chain_kernel(const Args
       }
     }
     if (tid < kL) a.gdot[task * kL + tid] = sm.gdp[0][tid] + sm.gdp[1][tid];
-    {
-      const int row = tid >> 4, col = 4 * (tid & 15);
-      *reinterpret_cast<float4*>(a.r0 + (task * kC + row) * kL + col) = *reinterpret_cast<const float4*>(&sm.R0[row][col]);
-    }
     __syncthreads();
 
     // ---- G <- d^len (.) G + (U d^s)^T DY; this thread's share of sum_tau d^tau g_n[tau]
@@ -667,6 +691,10 @@ __global__ void chunk_sum_kernel(const float* __restrict__ part, float* __restri
 }  // namespace
 
 cudaError_t launch_backward_chain(const Args& a, cudaStream_t s) {
+  const long long ntasks = (long long)a.B * a.H * (long long)nchunks(a.T);
+  if (ntasks <= 0) return cudaSuccess;
+  if (ntasks >= (1ll << 31)) return cudaErrorInvalidValue;
+  rwkv8_bwd_r0_kernel<<<(unsigned)ntasks, kThreads, 0, s>>>(a);  // R0 of every chunk, before the chain reads it
   const size_t smem = sizeof(ChainSmem);
   cudaError_t e = cudaFuncSetAttribute(rwkv8_bwd_chain_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
