@@ -60,7 +60,6 @@ namespace {
 constexpr int kN = 64, kL = 16;
 constexpr int kLD64 = 72;  // row stride (floats) of 64-wide operands read along k
 constexpr int kLD16 = 24;  // row stride of 16-wide operands
-constexpr int kLDT = 68;   // row stride of operands read only as [k][n] B operands
 constexpr int kTile = kL * kN;
 constexpr int kThreads = 256;
 enum { V_R = 0, V_W = 1, V_K = 2, V_V = 3, V_A = 4, V_B = 5, V_DY = 6 };
