@@ -36,8 +36,8 @@ TRAFFIC = {
     "kernel": "wkv7_bwd4_carry_kernel + wkv7_bwd4_out_kernel (one wkv7_backward_bf16 call)",
     "sources": ("wkv7_bwd4.cu", "wkv7_common.cuh", "wkv7_scaled.cuh", "wkv7_mma.cuh", "wkv7_mma16.cuh",
                 "wkv7_launch.h", "wkv7_decay.cuh", "wkv7_tmem.cuh"),
-    "sha256": "4796a1f491261989b24be41333279f686d8f5766d51b7c38d2b595e92dbd829a",
-    "bytes_per_token_head": (83.937536e6 + 28.234240e6 + 318.859776e6 + 161.499904e6) / 131072,
+    "sha256": "c60415d811c22ba5d5ea5006594005c3d57081aae44a87499ffbd84e1b3ddeee",
+    "bytes_per_token_head": (83.938048e6 + 27.935744e6 + 318.857984e6 + 161.485056e6) / 131072,
 }
 
 
@@ -49,9 +49,9 @@ TRAFFIC_FP32 = {
     "kernel": "wkv7_bwd4_carry_kernel<float> + wkv7_bwd4_out_f32_kernel (one wkv7_backward call, fp32 inputs)",
     "sources": ("wkv7_bwd4.cu", "wkv7_bwd4_f32.cu", "wkv7_common.cuh", "wkv7_scaled.cuh", "wkv7_mma.cuh",
                 "wkv7_mma16.cuh", "wkv7_launch.h", "wkv7_decay.cuh", "wkv7_tmem.cuh"),
-    "sha256": "3814de236be2f48554d0f3cc6476c3e4dbaff5eeb79805e88841b62198e87f50",
+    "sha256": "fd3d98fb5142d4609ad7ab0cf35f5bb468b673b37942d4a0582b0bec254a9610",
     "N": 64,
-    "bytes_per_token_head": (125.891328e6 + 59.876352e6 + 377.680128e6 + 123.846144e6) / 98304,
+    "bytes_per_token_head": (125.889792e6 + 59.840768e6 + 377.635328e6 + 123.891456e6) / 98304,
 }
 
 
