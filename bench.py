@@ -435,7 +435,7 @@ def _pipelined_e2e(args, host_in, sets, step_on, stream, dist, dev):
     h2d = sum(x.numel() * x.element_size() for x in host_in.values())
     d2h = sum(x.numel() * x.element_size() for x in host_out.values())
     s_in, s_out = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
-    n_steps = max(2, min(args.steps, 6))
+    n_steps = max(2, min(args.steps, 20))
 
     def run(k, ev_in, ev_done, ev_out):
         dev_in, dev_out = sets[k % 2]

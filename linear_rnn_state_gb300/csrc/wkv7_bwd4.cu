@@ -251,8 +251,10 @@ __device__ __forceinline__ void gram_tile16(TOut* M, TOut* Ml, const bf16_t* P, 
   }
 }
 
-// Forming group: wait for a chunk's inputs and form its operands. Returns
-// false on a timeout.
+// Forming group: wait for a chunk's inputs and form its operands. A timeout
+// raises the CTA's abort flag and returns false, after forming the operands
+// all the same (from whatever the stage holds) so that the group's named
+// barriers stay matched; every thread reads the flag after the round's barrier.
 template <typename TIn, bool kLogit, bool kEpi>
 __device__ bool front_form(CarrySmemT<TIn>& sm, ScratchC16<kCarryParts<TIn>>& sc, OpC16<kCarryParts<TIn>>& op,
                            TIn* rs, uint64_t* bar, uint32_t parity, int len, unsigned* status, const float* epi_rstd,
@@ -260,13 +262,10 @@ __device__ bool front_form(CarrySmemT<TIn>& sm, ScratchC16<kCarryParts<TIn>>& sc
   constexpr int kP = kCarryParts<TIn>, kLo = kP - 1;
   const int ftid = threadIdx.x - 128;
   const bool ok = mbar_wait_bounded(status, bar, parity);
-  if (named_bar_or(1, 128, !ok)) {
-    if (ftid == 0) sm.abort_flag = 1;
-    return false;
-  }
+  if (!ok) *reinterpret_cast<volatile int*>(&sm.abort_flag) = 1;
   const bool unsafe = form_carry<TIn, kLogit, kEpi>(sc, sm.Pc, rs, op, len, ftid, epi_rstd, epi_lw);
   if (ftid == 0) op.unsafe = unsafe;
-  if (unsafe) return true;
+  if (unsafe) return ok;
   named_bar(1, 128);
   // n-tile pf - 2 of Mba = A^ B~^T (warps 2, 3); the products group makes Mbr
   const int pf = ftid >> 5;
@@ -275,7 +274,7 @@ __device__ bool front_form(CarrySmemT<TIn>& sm, ScratchC16<kCarryParts<TIn>>& sc
     gram_tile16<kP>(sc.Mba, sc.Mba, op.Ah[0], op.Ah[kLo], sc.Bt[0], sc.Bt[kLo], pf, true, ftid & 31);
   else
     gram_tile16<kP>(op.Mbr[0], op.Mbr[kLo], op.Rh[0], op.Rh[kLo], sc.Bt[0], sc.Bt[kLo], pf - 2, false, ftid & 31);
-  return true;
+  return ok;
 }
 
 // Products group (128 threads): T = (I - Mba)^-1 by fp32 forward substitution (warp 0; the
@@ -549,7 +548,8 @@ __global__ void __launch_bounds__(kCarryThreads, 1) wkv7_bwd4_carry_kernel(const
                     args.status);
     }
     // the stage of visit m is free (formed two visits ago, direct steps done); refill it
-    if (__syncthreads_or(sm.abort_flag)) {
+    __syncthreads();
+    if (*reinterpret_cast<volatile int*>(&sm.abort_flag)) {
       aborted = true;
       break;
     }

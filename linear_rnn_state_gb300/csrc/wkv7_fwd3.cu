@@ -602,19 +602,19 @@ __global__ void __launch_bounds__(kThreads, 1) wkv7_fwd3_kernel(const __grid_con
   }
   __syncthreads();
 
-  // The forming group waits for a stage together: the group agrees on the
-  // outcome, so its named barriers stay matched; a timeout raises the CTA's
-  // abort flag.
+  // Each forming thread waits for the stage itself. A timeout raises the CTA's
+  // abort flag and the thread forms the chunk all the same (from whatever the
+  // stage holds), so the group's named barriers stay matched; every thread
+  // reads the flag after the round's barrier and leaves the loop.
   int waited = 0;  // chunks whose stage has landed (forming group)
   int issued = min(kStages, nchunks);  // chunks whose copy was started (every thread keeps count)
   auto chunk_len = [&](int chunk) { return min(kL, T - chunk * kL); };
   auto form = [&](int chunk) {
     const bool ok = mbar_wait_bounded(args.status, &sm.full[chunk % kStages], (chunk / kStages) & 1);
-    if (named_bar_or(1, 128, !ok)) {
-      if (ftid == 0) sm.abort_flag = 1;
-      return;
-    }
-    waited = chunk + 1;
+    if (ok)
+      waited = chunk + 1;
+    else
+      *reinterpret_cast<volatile int*>(&sm.abort_flag) = 1;
     form_chunk<TIn, kLogit, kEpi>(sm, sm.prep[chunk % 3], sm.X2[chunk & 1], chunk % kStages, chunk_len(chunk), ftid,
                                   chunk % 4);
   };
@@ -668,7 +668,8 @@ __global__ void __launch_bounds__(kThreads, 1) wkv7_fwd3_kernel(const __grid_con
         state_chunk16<TIn>(c, sm, P, lane);
     }
     // the stage of chunk n is free (formed two rounds ago, direct steps done); refill it
-    aborted = __syncthreads_or(sm.abort_flag) != 0;
+    __syncthreads();
+    aborted = *reinterpret_cast<volatile int*>(&sm.abort_flag) != 0;
     if (!aborted && tid == kIssuer && n + kStages < nchunks) {
       fence_proxy_async_smem();
       issue(n + kStages);
