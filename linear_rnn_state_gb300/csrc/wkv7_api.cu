@@ -198,6 +198,7 @@ Extent extent(const void* p, size_t bytes) {
 // buffer holds ck_bytes.
 void set_extents(FwdArgs& a, int N, bool bf16, size_t ck_bytes) {
   const size_t vec = (size_t)a.B * a.T * a.H * N, st = (size_t)a.B * a.H * N * N * 4, par = (size_t)a.H * N * 4;
+  for (int v = 0; v < 6; ++v) a.ext.in[v] = extent(a.in[v], vec * (bf16 ? 2 : 4));
   a.ext.y = extent(a.y, vec * (bf16 ? 2 : 4));
   a.ext.nv = extent(a.nv, vec * 2);
   a.ext.stats = extent(a.stats, (size_t)a.B * a.T * a.H * 2 * 4);
@@ -279,8 +280,10 @@ int forward_impl(bool bf16, const void* const in[6], const float* s_init, void* 
 
   FwdArgs args;
   const int K = fwd_steps_per_stage(N, bf16);
-  for (int v = 0; v < 6; ++v)
+  for (int v = 0; v < 6; ++v) {
     if ((rc = make_map(&args.map[v], in[v], bf16, B, T, H, N, K))) return rc;
+    args.in[v] = in[v];
+  }
   if ((rc = status_word(&args.status))) return rc;
   args.s_init = s_init;
   args.y = y;
@@ -395,11 +398,13 @@ int backward_impl(bool bf16, const void* const in[7], const float* s_init, const
   if (!ckpt) {
     FwdArgs fa;
     const int K = fwd_steps_per_stage(N, bf16);
-    for (int v = 0; v < 6; ++v)
+    for (int v = 0; v < 6; ++v) {
       if ((rc = make_map(&fa.map[v], in[v], bf16, B, T, H, N, K))) {
         cudaFreeAsync(ws, stream);
         return rc;
       }
+      fa.in[v] = in[v];
+    }
     if ((rc = status_word(&fa.status))) {
       cudaFreeAsync(ws, stream);
       return rc;
@@ -564,8 +569,10 @@ int backward_noalloc_impl(const float* const in[7], const float* s_init, float* 
   float* scratch = nullptr;
   if ((rc = noalloc_scratch(&scratch))) return rc;
   FwdArgs fa;
-  for (int v = 0; v < 6; ++v)
+  for (int v = 0; v < 6; ++v) {
     if ((rc = make_map(&fa.map[v], in[v], false, B, T, H, N, fwd_steps_per_stage(N, false)))) return rc;
+    fa.in[v] = in[v];
+  }
   if ((rc = status_word(&fa.status))) return rc;
   fa.s_init = s_init;
   fa.y = nullptr;

@@ -108,6 +108,8 @@ struct alignas(16) ScratchC16 {
   bf16_t Bt[kP][kL * kB64];  // B~ [t][j]
   float Mba[kL * kLD16];     // A^ B~^T (strictly lower) [t][s], fp32: T is formed from it
 };
+static_assert(offsetof(ScratchC16<1>, Mba) % 16 == 0 && offsetof(ScratchC16<2>, Mba) % 16 == 0,
+              "Mba rows are read 16 bytes at a time");
 template <typename TIn>
 constexpr int kCarryParts = sizeof(TIn) == 2 ? 1 : 2;
 
@@ -285,13 +287,7 @@ __device__ void front_products16(ScratchC16<kP>& sc, OpC16<kP>& op) {
   if (pp != 0) return;
   const int s = lane & 15;
   float col[kL];
-#pragma unroll
-  for (int tt = 0; tt < kL; ++tt) {
-    float x = tt == s ? 1.f : 0.f;
-#pragma unroll
-    for (int u = 0; u < tt; ++u) x = fmaf(sc.Mba[tt * kLD16 + u], col[u], x);
-    col[tt] = x;
-  }
+  unit_lower_inverse_col16<kLD16>(sc.Mba, s, col);
   if (lane < 16) {
 #pragma unroll
     for (int tt = 0; tt < kL; ++tt) put_p<kP>(op.Tm[0] + tt * kB16 + s, op.Tm[kP - 1] + tt * kB16 + s, col[tt]);
@@ -614,6 +610,7 @@ struct OutSmem {
   float cLs[kN];          // c(L) = product of the chunk's decays
   float anc[2][kN];  // the chunk's parts of colsum(carry o state) at its start and end, without c(L) colsum(Gc o S0)
 };
+static_assert(offsetof(OutSmem, Mba) % 16 == 0, "Mba rows are read 16 bytes at a time");
 
 // Extra shared memory of the output pass with the epilogue's backward fused (after OutSmem).
 struct OutEpiSmem {
@@ -775,13 +772,7 @@ __device__ void out_direct(const bf16_t* rs, float* red, const float* S0, const 
 __device__ __forceinline__ void unit_lower_inverse16(const float* M, bf16_t* Tout, int lane) {
   const int s = lane & 15;
   float col[kL];
-#pragma unroll
-  for (int t = 0; t < kL; ++t) {
-    float x = t == s ? 1.f : 0.f;
-#pragma unroll
-    for (int u = 0; u < t; ++u) x = fmaf(M[t * kLD16 + u], col[u], x);
-    col[t] = x;
-  }
+  unit_lower_inverse_col16<kLD16>(M, s, col);
   if (lane < 16) {
 #pragma unroll
     for (int t = 0; t < kL; ++t) Tout[t * kB16 + s] = __float2bfloat16_rn(col[t]);
@@ -968,13 +959,6 @@ __global__ void __launch_bounds__(kThreads, 3) wkv7_bwd4_out_kernel(const __grid
       ep = ffma2(gc, s0, ep);
     }
     *reinterpret_cast<float2*>(&sm.Epart[rb][2 * lane]) = ep;
-    if (warp == 4) {  // U0 = triu(V DY^T)
-      float acc[2][4];
-      zero4(acc[0]);
-      zero4(acc[1]);
-      mm_mk_nk<4>(acc, sm.raw[V_V], kB64, 0, sm.raw[V_DY], kB64, 0, lane);
-      store_masked16(acc, sm.U[0], false, true, g, t4);
-    }
   }
   __syncthreads();
 
@@ -1035,16 +1019,17 @@ __global__ void __launch_bounds__(kThreads, 3) wkv7_bwd4_out_kernel(const __grid
   }
   __syncthreads();
 
-  // ---- D: U1 = triu(V DSA^T, 1), U2 = triu(SA DY^T), U3 = triu(SA DSA^T, 1) (warps 5-7)
-  if (warp >= 5) {
+  // ---- D: U0 = triu(V DY^T), U1 = triu(V DSA^T, 1), U2 = triu(SA DY^T), U3 = triu(SA DSA^T, 1)
+  //      (warps 4-7), while warps 0-3 go on to the column products; the barrier after the
+  //      column products orders them before the triangular terms read them
+  if (warp >= 4) {
     const int u = warp - 4;
     float acc[2][4];
     zero4(acc[0]);
     zero4(acc[1]);
-    mm_mk_nk<4>(acc, u == 1 ? sm.raw[V_V] : sm.SA, kB64, 0, u == 2 ? sm.raw[V_DY] : sm.DSA, kB64, 0, lane);
-    store_masked16(acc, sm.U[u], false, u == 2, g, t4);
+    mm_mk_nk<4>(acc, u < 2 ? sm.raw[V_V] : sm.SA, kB64, 0, u % 2 == 0 ? sm.raw[V_DY] : sm.DSA, kB64, 0, lane);
+    store_masked16(acc, sm.U[u], false, u % 2 == 0, g, t4);
   }
-  __syncthreads();
 
   // ---- E: column products, 8 warps: warp (grp, jb) covers columns j0 .. j0+15 of
   //      dk~, db~ (grp 0) or dr^, da^ (grp 1)

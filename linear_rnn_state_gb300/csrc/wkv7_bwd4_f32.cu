@@ -84,6 +84,7 @@ struct F2Smem {
   float cLs[kN];          // c(L)
   float anc[2][kN];       // the chunk's parts of colsum(carry o state) at its start and end, without c(L) E
 };
+static_assert(offsetof(F2Smem, Mba) % 16 == 0, "Mba rows are read 16 bytes at a time");
 
 __device__ __forceinline__ float quad_sum(float x) {
   x += __shfl_xor_sync(0xffffffffu, x, 1);
@@ -339,13 +340,7 @@ __global__ void __launch_bounds__(kThreads, 2) wkv7_bwd4_out_f32_kernel(const __
       // T = (I - Mba)^-1 by forward substitution in fp32; lane s (< 16) owns column s
       const int s = lane & 15;
       float col[kL];
-#pragma unroll
-      for (int t = 0; t < kL; ++t) {
-        float x = t == s ? 1.f : 0.f;
-#pragma unroll
-        for (int u = 0; u < t; ++u) x = fmaf(sm.Mba[t * kLD16 + u], col[u], x);
-        col[t] = x;
-      }
+      unit_lower_inverse_col16<kLD16>(sm.Mba, s, col);
       if (lane < 16) {
 #pragma unroll
         for (int t = 0; t < kL; ++t) put_p<2>(sm.a.t.Tm[0] + t * kB16 + s, sm.a.t.Tm[1] + t * kB16 + s, col[t]);

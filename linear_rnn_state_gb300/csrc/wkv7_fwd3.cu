@@ -24,7 +24,7 @@
 //
 // One CTA per (b, h), twelve warps in three groups working one chunk apart:
 //  - forming warps (4..7) turn chunk n+2's r, w, k, v, a, b (TMA tensor loads
-//    into a four-stage ring) into the scaled operands;
+//    into a ring of stages) into the scaled operands;
 //  - products warps (8..11) make chunk n+1's four L x L products and
 //    T = (I - Mba)^-1 (forward substitution, one warp);
 //  - state warps (0..3) each own 16 rows i of S as mma accumulator tiles
@@ -68,14 +68,22 @@ struct alignas(16) Prep16 {
   int unsafe;
   int pad_[31];
 };
+static_assert(offsetof(Prep16<1>, Mba) % 16 == 0 && offsetof(Prep16<2>, Mba) % 16 == 0,
+              "Mba rows are read 16 bytes at a time");
 
-// Per input type: input ring depth, checkpoint staging, operand parts and the row stride
-// of the staged y rows.
+// Per input type: input ring depth and refill point, checkpoint staging, operand parts and
+// the row stride of the staged y rows. With fp32 inputs (three stages of twice the bytes) the
+// stage of chunk n is refilled once the chunk is formed (round n - 2), two rounds before the
+// next chunk in it is formed, and a chunk in the direct form reads its rows from global
+// memory; refilled after round n the forming group waited for its copy every round. With
+// bf16 inputs (four stages) the stage is refilled after round n, a round to spare, and the
+// direct form reads the stage.
 template <typename TIn>
 struct Fwd3Io;
 template <>
 struct Fwd3Io<__nv_bfloat16> {
   static constexpr int kStages = 4;
+  static constexpr int kRefillAhead = 0;  // the stage of chunk n + kRefillAhead is refilled after round n
   static constexpr bool kStageCk = true;
   static constexpr int kP = 1;
   static constexpr int kYS = kB64;  // padded: the transposed matrix stores of y hit distinct banks
@@ -83,6 +91,7 @@ struct Fwd3Io<__nv_bfloat16> {
 template <>
 struct Fwd3Io<float> {
   static constexpr int kStages = 3;
+  static constexpr int kRefillAhead = 2;
   static constexpr bool kStageCk = false;
   static constexpr int kP = 2;
   static constexpr int kYS = kN;
@@ -262,13 +271,7 @@ __device__ void gram_chunk16(Prep16<kP>& P, const bf16_t (*X2)[2 * kL * kB64], i
   // T = (I - Mba)^-1 by forward substitution in fp32; lane s (< 16) owns column s
   const int s = lane & 15;
   float col[kL];
-#pragma unroll
-  for (int tt = 0; tt < kL; ++tt) {
-    float x = tt == s ? 1.f : 0.f;
-#pragma unroll
-    for (int u = 0; u < tt; ++u) x = fmaf(P.Mba[tt * kLD16 + u], col[u], x);
-    col[tt] = x;
-  }
+  unit_lower_inverse_col16<kLD16>(P.Mba, s, col);
   if (lane < 16) {
 #pragma unroll
     for (int tt = 0; tt < kL; ++tt) put_p<kP>(P.Tinv[0] + tt * kB16 + s, P.Tinv[kLo] + tt * kB16 + s, col[tt]);
@@ -422,7 +425,7 @@ __device__ void state_chunk16(StateCtx& c, Fwd3Smem<TIn>& sm, const Prep16<Fwd3I
   }
 }
 
-// Chunk in the direct form (any decay), fp32 on the CUDA cores.
+// Chunk in the direct form (any decay), fp32 on the CUDA cores, from its input stage.
 template <typename TIn, bool kLogit>
 __device__ void state_chunk_direct(StateCtx& c, Fwd3Smem<TIn>& sm, int stage, int len) {
   const int g = c.g, t4 = c.t4, i0 = c.i0;
@@ -447,6 +450,58 @@ __device__ void state_chunk_direct(StateCtx& c, Fwd3Smem<TIn>& sm, int stage, in
       const int col = 8 * nt + 2 * t4;
       const float2 w = decay_value2<kLogit>(bf2(row + V_W * kL * kN + col)), k = bf2(row + V_K * kL * kN + col);
       const float2 b = bf2(row + V_B * kL * kN + col), r = bf2(row + V_R * kL * kN + col);
+      c.S[nt][0] = fmaf(s0, b.x, fmaf(c.S[nt][0], w.x, v0 * k.x));
+      c.S[nt][1] = fmaf(s0, b.y, fmaf(c.S[nt][1], w.y, v0 * k.y));
+      c.S[nt][2] = fmaf(s1, b.x, fmaf(c.S[nt][2], w.x, v1 * k.x));
+      c.S[nt][3] = fmaf(s1, b.y, fmaf(c.S[nt][3], w.y, v1 * k.y));
+      y0 = fmaf(c.S[nt][0], r.x, fmaf(c.S[nt][1], r.y, y0));
+      y1 = fmaf(c.S[nt][2], r.x, fmaf(c.S[nt][3], r.y, y1));
+    }
+    y0 += __shfl_xor_sync(0xffffffffu, y0, 1);
+    y0 += __shfl_xor_sync(0xffffffffu, y0, 2);
+    y1 += __shfl_xor_sync(0xffffffffu, y1, 1);
+    y1 += __shfl_xor_sync(0xffffffffu, y1, 2);
+    if (t4 == 0) {
+      constexpr int kYS = Fwd3Io<TIn>::kYS;
+      st1(&sm.ys[c.yb][t * kYS + i0 + g], y0);
+      st1(&sm.ys[c.yb][t * kYS + i0 + g + 8], y1);
+    }
+  }
+}
+
+// The same from the chunk's rows in global memory (row0 = the offset of its first row, vstep
+// between steps), for an input stage refilled as soon as its chunk was formed.
+template <typename TIn, bool kLogit>
+__device__ void state_chunk_direct_global(StateCtx& c, Fwd3Smem<TIn>& sm, const FwdArgs& args, size_t row0,
+                                          size_t vstep, int len) {
+  const int g = c.g, t4 = c.t4, i0 = c.i0;
+  auto ld2 = [&](int v, int t, int col) {
+    const TIn* p = static_cast<const TIn*>(args.in[v]) + row0 + (size_t)t * vstep + col;
+    return in_extent(args.status, args.ext.in[v], p, 2) ? bf2(p) : make_float2(0.f, 0.f);
+  };
+  auto ld1 = [&](int v, int t, int col) {
+    const TIn* p = static_cast<const TIn*>(args.in[v]) + row0 + (size_t)t * vstep + col;
+    return in_extent(args.status, args.ext.in[v], p) ? bf(p) : 0.f;
+  };
+  for (int t = 0; t < len; ++t) {
+    float s0 = 0.f, s1 = 0.f;
+#pragma unroll
+    for (int nt = 0; nt < 8; ++nt) {
+      const float2 a = ld2(V_A, t, 8 * nt + 2 * t4);
+      s0 = fmaf(c.S[nt][0], a.x, fmaf(c.S[nt][1], a.y, s0));
+      s1 = fmaf(c.S[nt][2], a.x, fmaf(c.S[nt][3], a.y, s1));
+    }
+    s0 += __shfl_xor_sync(0xffffffffu, s0, 1);
+    s0 += __shfl_xor_sync(0xffffffffu, s0, 2);
+    s1 += __shfl_xor_sync(0xffffffffu, s1, 1);
+    s1 += __shfl_xor_sync(0xffffffffu, s1, 2);
+    const float v0 = ld1(V_V, t, i0 + g), v1 = ld1(V_V, t, i0 + g + 8);
+    float y0 = 0.f, y1 = 0.f;
+#pragma unroll
+    for (int nt = 0; nt < 8; ++nt) {
+      const int col = 8 * nt + 2 * t4;
+      const float2 w = decay_value2<kLogit>(ld2(V_W, t, col)), k = ld2(V_K, t, col);
+      const float2 b = ld2(V_B, t, col), r = ld2(V_R, t, col);
       c.S[nt][0] = fmaf(s0, b.x, fmaf(c.S[nt][0], w.x, v0 * k.x));
       c.S[nt][1] = fmaf(s0, b.y, fmaf(c.S[nt][1], w.y, v0 * k.y));
       c.S[nt][2] = fmaf(s1, b.x, fmaf(c.S[nt][2], w.x, v1 * k.x));
@@ -551,15 +606,17 @@ __global__ void __launch_bounds__(kThreads, 1) wkv7_fwd3_kernel(const __grid_con
 
   // Chunk n: the state warps run it in round n, the products group makes its
   // L x L products and T in round n-1, the forming group forms it in round
-  // n-2; its inputs arrive by TMA four rounds ahead (a four-stage ring).
+  // n-2. Its inputs arrive by TMA in a ring of kStages stages; after round n
+  // the stage of chunk n + kRefillAhead is refilled.
+  constexpr int kRefillAhead = Smem::Io::kRefillAhead;
   auto issue = [&](int chunk) {
     const int st = chunk % kStages;
     mbar_arrive_expect_tx(&sm.full[st], kStageBytes);
     for (int v = 0; v < 6; ++v) tma_load_4d(sm.raw[st][v], &args.map[v], &sm.full[st], 0, hi, chunk * kL, bi);
   };
-  // TMA copies are issued by the first thread of the forming group (fp32 inputs) or of the
-  // products group (bf16 inputs, where that group has the shorter round)
-  constexpr int kIssuer = sizeof(TIn) == 4 ? 128 : 256;
+  // TMA copies are issued by the first thread of the products group, the group with the
+  // shortest round
+  constexpr int kIssuer = 256;
   if (tid == kIssuer) {
     for (int s = 0; s < kStages; ++s) mbar_init(&sm.full[s], 1);
     fence_mbar_init();
@@ -623,13 +680,25 @@ __global__ void __launch_bounds__(kThreads, 1) wkv7_fwd3_kernel(const __grid_con
     if (!P.unsafe) gram_chunk16<Fwd3Io<TIn>::kP>(P, sm.X2[chunk & 1], gtid);
   };
 
+  // refill the stage of a chunk just formed (every thread calls it after a barrier)
+  auto refill = [&](int formed) {
+    if (tid == kIssuer && formed + kStages < nchunks) {
+      fence_proxy_async_smem();
+      issue(formed + kStages);
+    }
+    issued = min(formed + 1 + kStages, nchunks);
+  };
   // pipeline fill: form chunks 0 and 1, products of chunk 0
   if (role == 1) form(0);
   bool aborted = __syncthreads_or(sm.abort_flag) != 0;
   if (!aborted) {
+    if constexpr (kRefillAhead == 2) refill(0);
     if (role == 1 && nchunks > 1) form(1);
     if (role == 2) grams(0);
     aborted = __syncthreads_or(sm.abort_flag) != 0;
+    if constexpr (kRefillAhead == 2) {
+      if (!aborted) refill(1);
+    }
   }
   TIn* y = static_cast<TIn*>(args.y);
   const size_t vstep = (size_t)H * kN;
@@ -662,19 +731,27 @@ __global__ void __launch_bounds__(kThreads, 1) wkv7_fwd3_kernel(const __grid_con
           store_state(c, ck_head + (size_t)(t0 / args.C) * kN * kN, args.ext.ckpt, args.status);
       }
       c.yb = n & 1;
-      if (P.unsafe)
-        state_chunk_direct<TIn, kLogit>(c, sm, n % kStages, len);
+      if (P.unsafe) {
+        if constexpr (kRefillAhead > 0)
+          state_chunk_direct_global<TIn, kLogit>(c, sm, args, vbase + (size_t)t0 * vstep, vstep, len);
+        else
+          state_chunk_direct<TIn, kLogit>(c, sm, n % kStages, len);
+      }
       else
         state_chunk16<TIn>(c, sm, P, lane);
     }
-    // the stage of chunk n is free (formed two rounds ago, direct steps done); refill it
     __syncthreads();
     aborted = *reinterpret_cast<volatile int*>(&sm.abort_flag) != 0;
-    if (!aborted && tid == kIssuer && n + kStages < nchunks) {
-      fence_proxy_async_smem();
-      issue(n + kStages);
+    if constexpr (kRefillAhead == 0) {
+      // the stage of chunk n is free (formed two rounds ago, direct steps done); refill it
+      if (!aborted && tid == kIssuer && n + kStages < nchunks) {
+        fence_proxy_async_smem();
+        issue(n + kStages);
+      }
+      if (!aborted) issued = min(n + 1 + kStages, nchunks);
+    } else {
+      if (!aborted) refill(n + kRefillAhead);  // the stage of chunk n + 2, formed in this round
     }
-    if (!aborted) issued = min(n + 1 + kStages, nchunks);
   }
   if (aborted) {
     // let the copies still in flight land before the CTA's shared memory is released

@@ -19,6 +19,7 @@ struct Extent {
   size_t bytes = 0;
 };
 struct FwdExtents {
+  Extent in[6];  // r, w, k, v, a, b
   Extent y, nv, stats, s_init, s_final, ckpt, ln_w, ln_b, r_k;
 };
 struct BwdExtents {
@@ -30,6 +31,8 @@ struct BwdExtents {
 // 4-D tensors (N, H, T, B) with a box of (N, 1, K, 1): K steps of one head.
 struct FwdArgs {
   CUtensorMap map[6];
+  const void* in[6];    // r, w, k, v, a, b ([B][T][H][N], the input type), the tensor maps'
+                        // buffers: the chunked kernel's direct form reads fp32 rows here
   const float* s_init;  // [B][H][N][N] or null (zeros)
   void* y;              // [B][T][H][N] of the input type, or null
   float* s_final;       // [B][H][N][N] or null

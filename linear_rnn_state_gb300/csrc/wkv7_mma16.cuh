@@ -242,4 +242,24 @@ __device__ __forceinline__ void mm_mk_nk_p(float (&acc)[2][4], const bf16_t* A, 
   }
 }
 
+// Column s of T = (I - M)^-1 for a strictly lower 16 x 16 fp32 M (row stride kLD floats,
+// rows 16-byte aligned): forward substitution, col[t] = [t == s] + sum_{u < t} M[t][u] col[u]
+// summed in ascending u, each row of M read four entries per load.
+template <int kLD>
+__device__ __forceinline__ void unit_lower_inverse_col16(const float* M, int s, float (&col)[16]) {
+#pragma unroll
+  for (int t = 0; t < 16; ++t) {
+    float x = t == s ? 1.f : 0.f;
+#pragma unroll
+    for (int u4 = 0; u4 < t; u4 += 4) {
+      const float4 m = *reinterpret_cast<const float4*>(M + t * kLD + u4);
+      x = fmaf(m.x, col[u4], x);
+      if (u4 + 1 < t) x = fmaf(m.y, col[u4 + 1], x);
+      if (u4 + 2 < t) x = fmaf(m.z, col[u4 + 2], x);
+      if (u4 + 3 < t) x = fmaf(m.w, col[u4 + 3], x);
+    }
+    col[t] = x;
+  }
+}
+
 }  // namespace wkv7
