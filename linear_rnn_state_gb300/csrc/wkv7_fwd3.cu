@@ -57,14 +57,13 @@ constexpr int kLD16 = 24;  // row stride of 16-wide operands
 template <int kP>
 struct alignas(16) Prep16 {
   bf16_t X1[kP][2 * kL * kB64];  // rows 0..15: a^(t); rows 16..31: r^(t)   [t][j]
-  bf16_t VT[kP][kN * kB16];      // v(s)[i]                                   [i][s]
-  bf16_t KbT[2][kN * kB16];      // k(s)[j] c(L)[j] / c(s)[j]                 [j][s]
-  bf16_t BbT[2][kN * kB16];      // b(s)[j] c(L)[j] / c(s)[j]                 [j][s]
+  bf16_t V[kP][kL * kB64];       // v(s)[i]                                   [s][i]
+  bf16_t Kb[2][kL * kB64];       // k(s)[j] c(L)[j] / c(s)[j]                 [s][j]
+  bf16_t Bb[2][kL * kB64];       // b(s)[j] c(L)[j] / c(s)[j]                 [s][j]
   bf16_t M[kP][3][kL * kB16];    // Mka (strictly lower), Mkr, Mbr (lower)    [t][s]
   bf16_t Tinv[kP][kL * kB16];    // (I - Mba)^-1                              [t][s]
   float Mba[kL * kLD16];         // Mba (strictly lower, fp32: T is formed from it)
   float cL[kN];                  // c(L) (fp32)
-  float ph[2][kN];               // decay logits: product of each half's 8 decays
   int unsafe;
   int pad_[31];
 };
@@ -110,10 +109,11 @@ struct Fwd3Smem {
   // group two rounds before the state warps run the chunk, read by the products group the
   // round after) the bonus partials of the two 32-column halves and the v rows
   float epi[3][kN];
-  float epi_sp[4][2][kL];
+  float epi_sp[4][kL];
   __nv_bfloat16 epi_v[4][kL * kN];
   // checkpoints on their way out (state warps write, products warps store); bf16 inputs only
   float ck[kStageCk ? 2 : 1][kStageCk ? kN * kLD64 : 4];
+  float pq[4][kN];  // forming group: the product of each quarter's four decays, per column
   uint64_t full[kStages];
   int abort_flag;
 };
@@ -129,100 +129,86 @@ __device__ __forceinline__ float2 bf2(const __nv_bfloat16* p) {
 __device__ __forceinline__ float2 bf2(const float* p) { return *reinterpret_cast<const float2*>(p); }
 
 // ---------------------------------------------------------- forming group ---
-// 128 threads; thread (j = ptid % 64, half = ptid / 64) forms column j of
-// steps 8*half .. 8*half+7.
+// 128 threads; thread (lane, q = ptid / 32) forms columns 2 lane, 2 lane + 1 of steps
+// 4 q .. 4 q + 3: pairs of row elements, so every load and store moves two columns. The
+// running products c(t) are taken per quarter of four steps and the quarters' products
+// chained in step order through shared memory; the same group barrier votes on whether the
+// chunk leaves the scaled form's range.
 template <typename TIn, bool kLogit, bool kEpi>
 __device__ void form_chunk(Fwd3Smem<TIn>& sm, Prep16<Fwd3Io<TIn>::kP>& P, bf16_t (*X2)[2 * kL * kB64], int stage,
                            int len, int ptid, int eslot) {
   constexpr int kP = Fwd3Io<TIn>::kP, kLo = kP - 1;  // index of the lo part (the hi part for kP = 1)
   const TIn* rs = sm.raw[stage][0];
-  const int j = ptid & 63, half = ptid >> 6;
-  // decays of this thread's 8 steps (wm) and of the other 8 (wo); padding
-  // steps past the end of the sequence decay by 1
-  float wm[8], wo[8];
-  const int tm = 8 * half, to = 8 - tm;
-#pragma unroll
-  for (int e = 0; e < 8; ++e) {
-    wm[e] = tm + e < len ? decay_value<kLogit>(bf(rs + V_W * kL * kN + (tm + e) * kN + j)) : 1.f;
-    if constexpr (!kLogit) wo[e] = to + e < len ? bf(rs + V_W * kL * kN + (to + e) * kN + j) : 1.f;
-  }
-  float av[8], rv[8], kv[8], bv[8], vt[8];
-#pragma unroll
-  for (int e = 0; e < 8; ++e) {
-    const int o = (tm + e) * kN + j;
-    av[e] = bf(rs + V_A * kL * kN + o);
-    rv[e] = bf(rs + V_R * kL * kN + o);
-    kv[e] = bf(rs + V_K * kL * kN + o);
-    bv[e] = bf(rs + V_B * kL * kN + o);
-    vt[e] = bf(rs + V_V * kL * kN + o);
-  }
-  if constexpr (kEpi) {
-    // the epilogue's bonus sum_j r_j k_j r_k[j] of each step, over this warp's 32 columns,
-    // reduce-scattered over the lanes (lane bits 4, 3, 2 pick the step), and the v rows
-    const int lane = ptid & 31;
-    const float rk = sm.epi[2][j];
-    float p[8], q4[4], q2[2];
-#pragma unroll
-    for (int e = 0; e < 8; ++e) p[e] = rv[e] * kv[e] * rk;
-    const bool b4 = lane & 16, b3 = lane & 8, b2 = lane & 4;
-#pragma unroll
-    for (int u = 0; u < 4; ++u)
-      q4[u] = (b4 ? p[4 + u] : p[u]) + __shfl_xor_sync(0xffffffffu, b4 ? p[u] : p[4 + u], 16);
-#pragma unroll
-    for (int u = 0; u < 2; ++u)
-      q2[u] = (b3 ? q4[2 + u] : q4[u]) + __shfl_xor_sync(0xffffffffu, b3 ? q4[u] : q4[2 + u], 8);
-    float sum = (b2 ? q2[1] : q2[0]) + __shfl_xor_sync(0xffffffffu, b2 ? q2[0] : q2[1], 4);
-    sum += __shfl_xor_sync(0xffffffffu, sum, 2);
-    sum += __shfl_xor_sync(0xffffffffu, sum, 1);
-    if ((lane & 3) == 0) sm.epi_sp[eslot][j >> 5][tm + 4 * (b4 ? 1 : 0) + 2 * (b3 ? 1 : 0) + (b2 ? 1 : 0)] = sum;
-#pragma unroll
-    for (int e = 0; e < 8; ++e) sm.epi_v[eslot][(tm + e) * kN + j] = rs[V_V * kL * kN + (tm + e) * kN + j];
-  }
+  const int lane = ptid & 31, q = ptid >> 5, j = 2 * lane, t0 = 4 * q;
+  // decays of this thread's four steps; padding steps past the end of the sequence decay by 1
+  float2 wv[4], av[4], rv[4], kv[4], bv[4], vv[4];
   bool unsafe = false;
+  float2 pq = make_float2(1.f, 1.f);
 #pragma unroll
-  for (int e = 0; e < 8; ++e) unsafe |= !decay_is_safe(wm[e]);
-  float pm = 1.f, po = 1.f;
+  for (int e = 0; e < 4; ++e) {
+    const int o = (t0 + e) * kN + j;
+    wv[e] = t0 + e < len ? decay_value2<kLogit>(bf2(rs + V_W * kL * kN + o)) : make_float2(1.f, 1.f);
+    unsafe |= !decay_is_safe(wv[e].x) || !decay_is_safe(wv[e].y);
+    pq = fmul2(pq, wv[e]);
+  }
+  *reinterpret_cast<float2*>(&sm.pq[q][j]) = pq;
+  // the other rows are read before the group barrier, so their loads overlap it
 #pragma unroll
-  for (int e = 0; e < 8; ++e) {
-    pm *= wm[e];
-    if constexpr (!kLogit) po *= wo[e];
+  for (int e = 0; e < 4; ++e) {
+    const int o = (t0 + e) * kN + j;
+    av[e] = bf2(rs + V_A * kL * kN + o);
+    rv[e] = bf2(rs + V_R * kL * kN + o);
+    kv[e] = bf2(rs + V_K * kL * kN + o);
+    bv[e] = bf2(rs + V_B * kL * kN + o);
+    vv[e] = bf2(rs + V_V * kL * kN + o);
   }
-  if constexpr (kLogit) {
-    // each half forms its own decays once (three MUFU operations per logit)
-    // and takes the other half's product from shared memory
-    P.ph[half][j] = pm;
-    named_bar(1, 128);
-    po = P.ph[half ^ 1][j];
-  }
-  const float p_first = half ? po : pm;  // w(1)...w(8), multiplied in step order
-  const float cL = half ? po * pm : pm * po;
-  float c = half ? p_first : 1.f;
-  if (half == 0) P.cL[j] = cL;
-  float kbt[8], bbt[8];
-#pragma unroll
-  for (int e = 0; e < 8; ++e) {
-    const int t = tm + e;
-    const float cprev = c;
-    c *= wm[e];
-    const float ic = rcp_approx(c);
-    const float a = av[e], r = rv[e], k = kv[e], b = bv[e];
-    const int o0 = t * kB64 + j, o1 = (kL + t) * kB64 + j;
-    put_p<kP>(X2[0] + o0, X2[kLo] + o0, k * ic);
-    put_p<kP>(X2[0] + o1, X2[kLo] + o1, b * ic);
-    put_p<kP>(P.X1[0] + o0, P.X1[kLo] + o0, a * cprev);
-    put_p<kP>(P.X1[0] + o1, P.X1[kLo] + o1, r * c);
-    const float s = cL * ic;
-    kbt[e] = k * s;
-    bbt[e] = b * s;
-  }
-  // eight steps of column j: one 16-byte row piece of each transposed block, per part (v in
-  // kP parts: exact for bf16 inputs; kb and bb as hi and lo parts)
-  const int o = j * kB16 + 8 * half;
-  put8_p<kP>(P.VT[0] + o, P.VT[kLo] + o, vt);
-  put8_p<2>(P.KbT[0] + o, P.KbT[1] + o, kbt);
-  put8_p<2>(P.BbT[0] + o, P.BbT[1] + o, bbt);
   unsafe = named_bar_or(1, 128, unsafe);
   if (ptid == 0) P.unsafe = unsafe;
+  if constexpr (kEpi) {
+    // the epilogue's bonus sum_j r_j k_j r_k[j] of each step over the 64 columns,
+    // reduce-scattered over the lanes (lane bits 4, 3 pick the step), and the v rows
+    const float2 rk = *reinterpret_cast<const float2*>(&sm.epi[2][j]);
+    float p[4], q2[2];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) p[e] = fmaf(rv[e].x * kv[e].x, rk.x, rv[e].y * kv[e].y * rk.y);
+    const bool b4 = lane & 16, b3 = lane & 8;
+#pragma unroll
+    for (int u = 0; u < 2; ++u)
+      q2[u] = (b4 ? p[2 + u] : p[u]) + __shfl_xor_sync(0xffffffffu, b4 ? p[u] : p[2 + u], 16);
+    float sum = (b3 ? q2[1] : q2[0]) + __shfl_xor_sync(0xffffffffu, b3 ? q2[0] : q2[1], 8);
+    sum += __shfl_xor_sync(0xffffffffu, sum, 4);
+    sum += __shfl_xor_sync(0xffffffffu, sum, 2);
+    sum += __shfl_xor_sync(0xffffffffu, sum, 1);
+    if ((lane & 7) == 0) sm.epi_sp[eslot][t0 + 2 * (b4 ? 1 : 0) + (b3 ? 1 : 0)] = sum;
+#pragma unroll
+    for (int e = 0; e < 4; ++e)
+      *reinterpret_cast<uint32_t*>(&sm.epi_v[eslot][(t0 + e) * kN + j]) =
+          *reinterpret_cast<const uint32_t*>(rs + V_V * kL * kN + (t0 + e) * kN + j);
+  }
+  if (unsafe) return;  // the state warps run the chunk step by step
+  float2 cL = make_float2(1.f, 1.f), c = cL;  // c = c(t0 - 1) after the loop
+#pragma unroll
+  for (int u = 0; u < 4; ++u) {
+    cL = fmul2(cL, *reinterpret_cast<const float2*>(&sm.pq[u][j]));
+    if (u < q) c = cL;
+  }
+  if (q == 0) *reinterpret_cast<float2*>(&P.cL[j]) = cL;
+#pragma unroll
+  for (int e = 0; e < 4; ++e) {
+    const int t = t0 + e;
+    const float2 cprev = c;
+    c = fmul2(c, wv[e]);
+    const float2 ic = make_float2(rcp_approx(c.x), rcp_approx(c.y)), s = fmul2(cL, ic);
+    const int o0 = t * kB64 + j, o1 = (kL + t) * kB64 + j;
+    st_pair_p<kP>(X2[0] + o0, X2[kLo] + o0, fmul2(kv[e], ic));
+    st_pair_p<kP>(X2[0] + o1, X2[kLo] + o1, fmul2(bv[e], ic));
+    st_pair_p<kP>(P.X1[0] + o0, P.X1[kLo] + o0, fmul2(av[e], cprev));
+    st_pair_p<kP>(P.X1[0] + o1, P.X1[kLo] + o1, fmul2(rv[e], c));
+    // v in kP parts (exact for bf16 inputs); kb and bb as hi and lo parts
+    st_pair_p<kP>(P.V[0] + o0, P.V[kLo] + o0, vv[e]);
+    st_pair_p<2>(P.Kb[0] + o0, P.Kb[1] + o0, fmul2(kv[e], s));
+    st_pair_p<2>(P.Bb[0] + o0, P.Bb[1] + o0, fmul2(bv[e], s));
+  }
 }
 
 // --------------------------------------------------------- products group ---
@@ -367,7 +353,7 @@ __device__ void state_chunk16(StateCtx& c, Fwd3Smem<TIn>& sm, const Prep16<Fwd3I
     mma_pp<kP, kP>(PR, a, b);
   }
   FragP<kP> av;  // V^T rows i0.., k = s
-  a_mk_p<kP>(av, P.VT[0], P.VT[kLo], kB16, i0, 0, lane);
+  a_km_p<kP>(av, P.V[0], P.V[kLo], kB64, i0, 0, lane);
   b_nk_p<kP>(b, P.M[0][0], P.M[kLo][0], kB16, 0, 0, lane);  // Mka
   mma_pp<kP, kP>(PA, av, b);
   b_nk_p<kP>(b, P.M[0][1], P.M[kLo][1], kB16, 0, 0, lane);  // Mkr
@@ -385,7 +371,7 @@ __device__ void state_chunk16(StateCtx& c, Fwd3Smem<TIn>& sm, const Prep16<Fwd3I
   FragP<2> bk;
 #pragma unroll
   for (int np = 0; np < 4; ++np) {
-    b_nk_p<2>(bk, P.KbT[0], P.KbT[1], kB16, 16 * np, 0, lane);
+    b_kn_p<2>(bk, P.Kb[0], P.Kb[1], kB64, 16 * np, 0, lane);
     mma_pp<kP, 2>(reinterpret_cast<Acc2&>(c.S[2 * np]), av, bk);
   }
   // SA^T = PA T^T  [i][t]
@@ -420,7 +406,7 @@ __device__ void state_chunk16(StateCtx& c, Fwd3Smem<TIn>& sm, const Prep16<Fwd3I
   // + SA^T Bb
 #pragma unroll
   for (int np = 0; np < 4; ++np) {
-    b_nk_p<2>(bk, P.BbT[0], P.BbT[1], kB16, 16 * np, 0, lane);
+    b_kn_p<2>(bk, P.Bb[0], P.Bb[1], kB64, 16 * np, 0, lane);
     mma_pp<kP, 2>(reinterpret_cast<Acc2&>(c.S[2 * np]), asa, bk);
   }
 }
@@ -559,7 +545,7 @@ __device__ void flush_epilogue(const Fwd3Smem<__nv_bfloat16>& sm, const FwdArgs&
 #pragma unroll
   for (int o = 1; o < 8; o <<= 1) sq += __shfl_xor_sync(0xffffffffu, sq, o);
   const float rstd = rsqrtf(sq * (1.f / kN) + 64e-5f);
-  const float bon = sm.epi_sp[es][0][t] + sm.epi_sp[es][1][t];
+  const float bon = sm.epi_sp[es][t];
   uint32_t po[4], pn[4];
 #pragma unroll
   for (int q = 0; q < 4; ++q) {
