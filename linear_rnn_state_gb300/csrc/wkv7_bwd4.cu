@@ -380,23 +380,26 @@ __device__ void carry_direct(float (&G)[8][4], const TIn* rs, int len, int i0, i
   }
 }
 
-// A staged 64 x 64 bf16 carry (rows of 72) to global memory, 128 threads, whole rows per
-// instruction.
-// The same for an fp32 carry: 64 rows of 16 pieces of 16 bytes.
+// A staged 64 x 64 carry (rows of 72) to global memory, kT threads, whole rows per
+// instruction: fp32 (64 rows of 16 pieces of 16 bytes) or bf16 (64 rows of 8 pieces).
+template <int kT>
 __device__ __forceinline__ void flush_carry(const float* src, float* dst, int ptid, const Extent& x, unsigned* status) {
 #pragma unroll
-  for (int q = 0; q < 8; ++q) {
-    const int idx = ptid + 128 * q;  // row idx / 16, columns 4 (idx % 16) ..
+  for (int q = 0; q < (kN * 16 + kT - 1) / kT; ++q) {
+    const int idx = ptid + kT * q;  // row idx / 16, columns 4 (idx % 16) ..
+    if (kT * (q + 1) > kN * 16 && idx >= kN * 16) break;
     uint4* p = reinterpret_cast<uint4*>(dst + 4 * idx);
     if (in_extent(status, x, p)) *p = *reinterpret_cast<const uint4*>(src + (idx >> 4) * 72 + 4 * (idx & 15));
   }
 }
 
+template <int kT>
 __device__ __forceinline__ void flush_carry(const bf16_t* src, bf16_t* dst, int ptid, const Extent& x,
                                             unsigned* status) {
 #pragma unroll
-  for (int q = 0; q < 4; ++q) {
-    const int idx = ptid + 128 * q;  // row idx / 8, columns 8 (idx % 8) ..
+  for (int q = 0; q < (kN * 8 + kT - 1) / kT; ++q) {
+    const int idx = ptid + kT * q;  // row idx / 8, columns 8 (idx % 8) ..
+    if (kT * (q + 1) > kN * 8 && idx >= kN * 8) break;
     uint4* p = reinterpret_cast<uint4*>(dst + 8 * idx);
     if (in_extent(status, x, p)) *p = *reinterpret_cast<const uint4*>(src + (idx >> 3) * 72 + 8 * (idx & 7));
   }
@@ -539,9 +542,11 @@ __global__ void __launch_bounds__(kCarryThreads, 1) wkv7_bwd4_carry_kernel(const
       if (m + 2 < nchunks) form(m + 2);
     } else {
       if (m + 1 < nchunks) products(m + 1);
-      if (m > 0)
-        flush_carry(sm.gst[(m - 1) & 1], carry_head + (size_t)chunk_of(m - 1) * kN * kN, tid - 256, args.ext.carry,
-                    args.status);
+      // the carry the state warps staged last round, stored by the products warps other than
+      // the one forming T
+      if (m > 0 && tid >= 288)
+        flush_carry<96>(sm.gst[(m - 1) & 1], carry_head + (size_t)chunk_of(m - 1) * kN * kN, tid - 288,
+                        args.ext.carry, args.status);
     }
     // the stage of visit m is free (formed two visits ago, direct steps done); refill it
     __syncthreads();
@@ -562,7 +567,7 @@ __global__ void __launch_bounds__(kCarryThreads, 1) wkv7_bwd4_carry_kernel(const
     __syncthreads();
     return;
   }
-  if (role == 2) flush_carry(sm.gst[(nchunks - 1) & 1], carry_head, tid - 256, args.ext.carry, args.status);  // chunk 0's
+  if (role == 2) flush_carry<128>(sm.gst[(nchunks - 1) & 1], carry_head, tid - 256, args.ext.carry, args.status);  // chunk 0's
   if (role == 0 && args.dS_init) {
     float* dst = args.dS_init + (size_t)head * kN * kN;
 #pragma unroll

@@ -282,34 +282,48 @@ __device__ __forceinline__ void stage_state(const StateCtx& c, float* dst) {
   }
 }
 
-// A staged 64 x 64 state to global memory (128 threads, whole rows per instruction);
+// A staged 64 x 64 state to global memory (kT threads, whole rows per instruction);
 // dst lies in the buffer x (checked in the debug build).
+template <int kT>
 __device__ __forceinline__ void flush_state(const float* src, float* dst, int ptid, const Extent& x, unsigned* status) {
 #pragma unroll
-  for (int q = 0; q < 8; ++q) {
-    const int idx = ptid + 128 * q;  // row idx / 16, columns 4 (idx % 16) ..
+  for (int q = 0; q < (kN * kN / 4 + kT - 1) / kT; ++q) {
+    const int idx = ptid + kT * q;  // row idx / 16, columns 4 (idx % 16) ..
+    if (kT * (q + 1) > kN * kN / 4 && idx >= kN * kN / 4) break;
     float4* p = reinterpret_cast<float4*>(dst + 4 * idx);
     if (in_extent(status, x, p)) *p = *reinterpret_cast<const float4*>(src + (idx >> 4) * kLD64 + 4 * (idx & 15));
   }
 }
 
-// A chunk's staged y rows ([t][i] bf16, row stride kB64) to global memory: 128 threads, 16
+// A chunk's staged y rows ([t][i] bf16, row stride kB64) to global memory: kT threads, 16
 // rows x 8 pieces of 16 bytes, rows past the end of the sequence skipped.
+template <int kT>
 __device__ __forceinline__ void flush_y(const __nv_bfloat16* src, __nv_bfloat16* dst, size_t vstep, int len, int ptid,
                                         const Extent& x, unsigned* status) {
-  const int row = ptid >> 3, piece = ptid & 7;
-  uint4* p = reinterpret_cast<uint4*>(dst + (size_t)row * vstep + 8 * piece);
-  if (row < len && in_extent(status, x, p)) *p = *reinterpret_cast<const uint4*>(src + row * kB64 + 8 * piece);
+#pragma unroll
+  for (int q = 0; q < (kL * 8 + kT - 1) / kT; ++q) {
+    const int idx = ptid + kT * q;
+    if (kT * (q + 1) > kL * 8 && idx >= kL * 8) break;
+    const int row = idx >> 3, piece = idx & 7;
+    uint4* p = reinterpret_cast<uint4*>(dst + (size_t)row * vstep + 8 * piece);
+    if (row < len && in_extent(status, x, p)) *p = *reinterpret_cast<const uint4*>(src + row * kB64 + 8 * piece);
+  }
 }
 
 // The same for fp32 rows: 16 rows x 8 pieces of 32 bytes.
+template <int kT>
 __device__ __forceinline__ void flush_y(const float* src, float* dst, size_t vstep, int len, int ptid, const Extent& x,
                                         unsigned* status) {
-  const int row = ptid >> 3, piece = ptid & 7;
-  uint4* p = reinterpret_cast<uint4*>(dst + (size_t)row * vstep + 8 * piece);
-  if (row < len && in_extent(status, x, p, 2)) {
-    p[0] = *reinterpret_cast<const uint4*>(src + row * kN + 8 * piece);
-    p[1] = *reinterpret_cast<const uint4*>(src + row * kN + 8 * piece + 4);
+#pragma unroll
+  for (int q = 0; q < (kL * 8 + kT - 1) / kT; ++q) {
+    const int idx = ptid + kT * q;
+    if (kT * (q + 1) > kL * 8 && idx >= kL * 8) break;
+    const int row = idx >> 3, piece = idx & 7;
+    uint4* p = reinterpret_cast<uint4*>(dst + (size_t)row * vstep + 8 * piece);
+    if (row < len && in_extent(status, x, p, 2)) {
+      p[0] = *reinterpret_cast<const uint4*>(src + row * kN + 8 * piece);
+      p[1] = *reinterpret_cast<const uint4*>(src + row * kN + 8 * piece + 4);
+    }
   }
 }
 
@@ -600,9 +614,9 @@ __global__ void __launch_bounds__(kThreads, 1) wkv7_fwd3_kernel(const __grid_con
     mbar_arrive_expect_tx(&sm.full[st], kStageBytes);
     for (int v = 0; v < 6; ++v) tma_load_4d(sm.raw[st][v], &args.map[v], &sm.full[st], 0, hi, chunk * kL, bi);
   };
-  // TMA copies are issued by the first thread of the products group, the group with the
-  // shortest round
-  constexpr int kIssuer = 256;
+  // TMA copies are issued by the first thread of products warp 10: the products group has
+  // the shortest round, and its warp 9 (T) the longest work in it
+  constexpr int kIssuer = 320;
   if (tid == kIssuer) {
     for (int s = 0; s < kStages; ++s) mbar_init(&sm.full[s], 1);
     fence_mbar_init();
@@ -696,16 +710,21 @@ __global__ void __launch_bounds__(kThreads, 1) wkv7_fwd3_kernel(const __grid_con
       if (n + 2 < nchunks) form(n + 2);
     } else if (role == 2) {
       if (n + 1 < nchunks) grams(n + 1);
-      // the checkpoint and the y rows the state warps staged in the previous round
-      if (n > 0) {
+      // the checkpoint and the y rows the state warps staged in the previous round, stored by
+      // the products warps other than the one forming T (the longest products work)
+      if (n > 0 && gtid >> 5 != 1) {
+        const int fl = gtid < 32 ? gtid : gtid - 32;
         if (kStageCk && ck_head && ((n - 1) * kL) % args.C == 0)
-          flush_state(sm.ck[(n - 1) & 1], ck_head + (size_t)((n - 1) * kL / args.C) * kN * kN, gtid, args.ext.ckpt,
-                      args.status);
-        if constexpr (kEpi)
-          flush_epilogue(sm, args, n - 1, vbase, vstep, chunk_len(n - 1), gtid);
-        else if (y)
-          flush_y(sm.ys[(n - 1) & 1], y + vbase + (size_t)(n - 1) * kL * vstep, vstep, chunk_len(n - 1), gtid,
-                  args.ext.y, args.status);
+          flush_state<96>(sm.ck[(n - 1) & 1], ck_head + (size_t)((n - 1) * kL / args.C) * kN * kN, fl, args.ext.ckpt,
+                          args.status);
+        if constexpr (!kEpi) {
+          if (y)
+            flush_y<96>(sm.ys[(n - 1) & 1], y + vbase + (size_t)(n - 1) * kL * vstep, vstep, chunk_len(n - 1), fl,
+                        args.ext.y, args.status);
+        }
+      }
+      if constexpr (kEpi) {
+        if (n > 0) flush_epilogue(sm, args, n - 1, vbase, vstep, chunk_len(n - 1), gtid);
       }
     } else {
       const auto& P = sm.prep[n % 3];
@@ -751,11 +770,12 @@ __global__ void __launch_bounds__(kThreads, 1) wkv7_fwd3_kernel(const __grid_con
   if (role == 2 && nchunks > 0) {
     const int n = nchunks - 1;
     if (kStageCk && ck_head && (n * kL) % args.C == 0)
-      flush_state(sm.ck[n & 1], ck_head + (size_t)(n * kL / args.C) * kN * kN, gtid, args.ext.ckpt, args.status);
+      flush_state<128>(sm.ck[n & 1], ck_head + (size_t)(n * kL / args.C) * kN * kN, gtid, args.ext.ckpt, args.status);
     if constexpr (kEpi)
       flush_epilogue(sm, args, n, vbase, vstep, chunk_len(n), gtid);
     else if (y)
-      flush_y(sm.ys[n & 1], y + vbase + (size_t)n * kL * vstep, vstep, chunk_len(n), gtid, args.ext.y, args.status);
+      flush_y<128>(sm.ys[n & 1], y + vbase + (size_t)n * kL * vstep, vstep, chunk_len(n), gtid, args.ext.y,
+                   args.status);
   }
   if (role == 0 && args.s_final) store_state(c, args.s_final + (size_t)head * kN * kN, args.ext.s_final, args.status);
 }
