@@ -253,6 +253,13 @@ __device__ __forceinline__ void gram_tile16(TOut* M, TOut* Ml, const bf16_t* P, 
   }
 }
 
+// Where the carry's Gram blocks Mba and Mbr are made: in the products group with bf16 operands
+// (the forming group has the longest round: about 1,390 cycles against 520-970 for the
+// products warps), in the forming group with split-bf16 operands (three products each, which
+// would make the products warp that forms T the longest).
+template <int kP>
+constexpr bool kGramsInProducts = kP == 1;
+
 // Forming group: wait for a chunk's inputs and form its operands. A timeout
 // raises the CTA's abort flag and returns false, after forming the operands
 // all the same (from whatever the stage holds) so that the group's named
@@ -267,11 +274,11 @@ __device__ bool front_form(CarrySmemT<TIn>& sm, ScratchC16<kCarryParts<TIn>>& sc
   if (!ok) *reinterpret_cast<volatile int*>(&sm.abort_flag) = 1;
   const bool unsafe = form_carry<TIn, kLogit, kEpi>(sc, sm.Pc, rs, op, len, ftid, epi_rstd, epi_lw);
   if (ftid == 0) op.unsafe = unsafe;
-  if (unsafe) return ok;
+  if (unsafe || kGramsInProducts<kP>) return ok;
   named_bar(1, 128);
-  // n-tile pf - 2 of Mba = A^ B~^T (warps 2, 3); the products group makes Mbr
   const int pf = ftid >> 5;
-  // n-tile pf % 2 of Mba (warps 0, 1; fp32) or of Mbr (warps 2, 3; kP bf16 parts)
+  // n-tile pf of Mba = A^ B~^T (warps 0, 1; fp32, strictly lower) or pf - 2 of Mbr = R^ B~^T
+  // (warps 2, 3; kP bf16 parts, with the diagonal)
   if (pf < 2)
     gram_tile16<kP>(sc.Mba, sc.Mba, op.Ah[0], op.Ah[kLo], sc.Bt[0], sc.Bt[kLo], pf, true, ftid & 31);
   else
@@ -279,12 +286,24 @@ __device__ bool front_form(CarrySmemT<TIn>& sm, ScratchC16<kCarryParts<TIn>>& sc
   return ok;
 }
 
-// Products group (128 threads): T = (I - Mba)^-1 by fp32 forward substitution (warp 0; the
-// forming group made Mba and Mbr), stored in kP bf16 parts.
+// Products group (128 threads), a round after the forming group: with bf16 operands the Gram
+// blocks Mba = A^ B~^T (n-tile pp of warps 0, 1; fp32, strictly lower) and Mbr = R^ B~^T
+// (n-tile pp - 2 of warps 2, 3, with the diagonal) first; then T = (I - Mba)^-1 by fp32 forward
+// substitution on warp 0 (once warp 1's n-tile is in: named barrier 2), stored in kP bf16 parts.
 template <int kP>
 __device__ void front_products16(ScratchC16<kP>& sc, OpC16<kP>& op) {
   const int pp = (threadIdx.x >> 5) - 8, lane = threadIdx.x & 31;
-  if (pp != 0) return;
+  if constexpr (kGramsInProducts<kP>) {
+    if (pp < 2)
+      gram_tile16<kP>(sc.Mba, sc.Mba, op.Ah[0], op.Ah[0], sc.Bt[0], sc.Bt[0], pp, true, lane);
+    else
+      gram_tile16<kP>(op.Mbr[0], op.Mbr[0], op.Rh[0], op.Rh[0], sc.Bt[0], sc.Bt[0], pp - 2, false, lane);
+    if (pp == 1) named_arrive(2, 64);
+    if (pp != 0) return;
+    named_bar(2, 64);
+  } else {
+    if (pp != 0) return;
+  }
   const int s = lane & 15;
   float col[kL];
   unit_lower_inverse_col16<kLD16>(sc.Mba, s, col);

@@ -146,6 +146,12 @@ __device__ __forceinline__ void named_bar(int id, int count) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
 }
 
+// Arrival at a named barrier without waiting (the producer side of bar.sync on the same
+// barrier and count).
+__device__ __forceinline__ void named_arrive(int id, int count) {
+  asm volatile("bar.arrive %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
+
 // Named barrier that also returns whether any participating thread passed a
 // true predicate.
 __device__ __forceinline__ bool named_bar_or(int id, int count, bool pred) {
