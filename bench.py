@@ -36,8 +36,8 @@ TRAFFIC = {
     "kernel": "wkv7_bwd4_carry_kernel + wkv7_bwd4_out_kernel (one wkv7_backward_bf16 call)",
     "sources": ("wkv7_bwd4.cu", "wkv7_common.cuh", "wkv7_scaled.cuh", "wkv7_mma.cuh", "wkv7_mma16.cuh",
                 "wkv7_launch.h", "wkv7_decay.cuh", "wkv7_tmem.cuh"),
-    "sha256": "c60415d811c22ba5d5ea5006594005c3d57081aae44a87499ffbd84e1b3ddeee",
-    "bytes_per_token_head": (83.938048e6 + 27.935744e6 + 318.857984e6 + 161.485056e6) / 131072,
+    "sha256": "899673a9c877216d7d4638a15cfe0470ba169a470784601a014ef8795cd281da",
+    "bytes_per_token_head": (83.937280e6 + 28.293376e6 + 318.861312e6 + 161.522944e6) / 131072,
 }
 
 
@@ -49,9 +49,9 @@ TRAFFIC_FP32 = {
     "kernel": "wkv7_bwd4_carry_kernel<float> + wkv7_bwd4_out_f32_kernel (one wkv7_backward call, fp32 inputs)",
     "sources": ("wkv7_bwd4.cu", "wkv7_bwd4_f32.cu", "wkv7_common.cuh", "wkv7_scaled.cuh", "wkv7_mma.cuh",
                 "wkv7_mma16.cuh", "wkv7_launch.h", "wkv7_decay.cuh", "wkv7_tmem.cuh"),
-    "sha256": "fd3d98fb5142d4609ad7ab0cf35f5bb468b673b37942d4a0582b0bec254a9610",
+    "sha256": "bdbcc5c26ae502ad4d5d4b1223b836964b52e925b2f3a7a2221892e6647700dd",
     "N": 64,
-    "bytes_per_token_head": (125.889792e6 + 59.840768e6 + 377.635328e6 + 123.891456e6) / 98304,
+    "bytes_per_token_head": (125.889792e6 + 60.157952e6 + 377.625344e6 + 123.926272e6) / 98304,
 }
 
 
