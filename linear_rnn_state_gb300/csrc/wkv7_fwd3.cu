@@ -26,10 +26,11 @@
 //  - forming warps (4..7) turn chunk n+2's r, w, k, v, a, b (TMA tensor loads
 //    into a ring of stages) into the scaled operands;
 //  - products warps (8..11) make chunk n+1's four L x L products and
-//    T = (I - Mba)^-1 (forward substitution, one warp);
+//    T = (I - Mba)^-1 (forward substitution, one warp), and store the y rows
+//    and checkpoint the state warps staged a round before;
 //  - state warps (0..3) each own 16 rows i of S as mma accumulator tiles
-//    and compute S0 [A^ R^]^T, SA, Y and S(L) for chunk n, and write y and
-//    the checkpoints.
+//    and compute S0 [A^ R^]^T, SA, Y and S(L) for chunk n, staging y and the
+//    checkpoints (fp32 inputs: the state warps store the checkpoints).
 // Operand blocks rotate over three buffers. The input ring has four stages
 // for bf16 inputs and three for fp32 (twice the bytes); with fp32 inputs the
 // state warps store the checkpoints themselves instead of staging them.
